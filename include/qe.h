@@ -1,0 +1,220 @@
+/*
+ * qe.h -- C ABI of the tiered (BF16 / INT2 / evicted) KV-cache decode path.
+ *
+ * The cache keeps, per (batch element, layer, KV head) "unit", a sink prefix
+ * and the recent tokens in bf16, the top-Kf windows of w tokens in bf16, the
+ * next Kq windows as 2-bit codes with float32 min/scale parameters, and
+ * drops the rest.  Each decode step attends over that mixed set and adds
+ * every window's attention mass (summed over the unit's GQA query heads) to
+ * the window's cumulative score; every Omega steps the windows are
+ * re-ranked and promoted, demoted or evicted.
+ *
+ * Sources (page title, section / equation):
+ *  - QEvict reading notes (zhongzhuzhou.org, 2026-08-08): §2 Figure 1 (pipeline,
+ *    windows start in full precision), §4.1 eq. "attention" and eq. "budget",
+ *    §4.2 eq. (1) cumulative window score, §4.3 eq. (3) capacities, §4.4
+ *    eqs. (4)-(6) and Algorithm 1 (routing, quantize-once ledger, promotion).
+ *  - H2O: keeping heavy hitters by cumulative attention (PaperTrace 3.1.2):
+ *    §2.1 step order, §5.1 GQA group sum and state arrays, §5.1 ties broken on
+ *    the original position, §3.1 / §5.1 float32 score storage.
+ *  - HqeKV reading notes (zhongzhuzhou.org, 2026-08-26): §2.3 eq. (2) uniform
+ *    min/scale quantizer.
+ *  - KV Cache technology evolution (zane-jiang.github.io): §5 KIVI axes (keys
+ *    per channel across tokens, values per token).
+ *
+ * Conventions for every call:
+ *  - All work is enqueued on the CUDA stream given to qe_init (the handle's
+ *    stream) and returns without waiting, except where stated.  Device buffers
+ *    passed in must stay valid until the stream has reached the call.
+ *  - Status codes are returned, never exceptions or traps.  A device-side
+ *    consistency flag (free-list underflow, table corruption, bounded wait
+ *    expiry) is sticky; qe_synchronize() reports it as QE_ERR_DEVICE.
+ *  - qe_last_error() returns a message for the last failing call on the
+ *    handle (or on qe_init when the handle is NULL); the string is owned by the
+ *    library and valid until the next call on that handle.
+ *  - Unit index u = b * n_kv_heads + kvh; query head h of unit u is
+ *    kvh * G + i, i < G = n_q_heads / n_kv_heads.
+ *  - Window j of a sequence covers positions [j w, (j+1) w); the sink
+ *    positions [0, n_sink) are carved out of window 0.
+ */
+#ifndef QE_H
+#define QE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef struct qe_handle_s* qe_handle;
+
+typedef enum {
+  QE_OK = 0,
+  QE_ERR_INVALID_ARG = 1,  /* bad pointer, index, size or unsupported shape */
+  QE_ERR_OOM = 2,          /* device or pinned host allocation failed */
+  QE_ERR_CAPACITY = 3,     /* appending beyond max_context, or a pool would overflow */
+  QE_ERR_CUDA = 4,         /* a CUDA runtime call failed (message has the CUDA error string) */
+  QE_ERR_TIMEOUT = 5,      /* a bounded device wait expired */
+  QE_ERR_STATE = 6,        /* call not valid in the handle's current state */
+  QE_ERR_HOST_STORE = 7,   /* pinned host backing store could not be mapped */
+  QE_ERR_DEVICE = 8        /* sticky device-side consistency flag was raised */
+} qe_status;
+
+/* Tier of a window (qe_get_tiers). */
+enum {
+  QE_TIER_NONE = 0,      /* window not reached yet */
+  QE_TIER_PINNED = 1,    /* bf16, not yet ranked (recent or awaiting its first routing event) */
+  QE_TIER_FULL = 2,      /* bf16, among the top Kf */
+  QE_TIER_QUANT = 3,     /* 2-bit codes + float32 min/scale, among the next Kq */
+  QE_TIER_EVICTED = 4    /* dropped for good */
+};
+
+/* Capacity rule (QEvict notes §4.3 eq. (3); the mapping from the workloads'
+ * token shares to window counts is this library's reading):
+ *   0: Kf = kf, Kq = kq windows;
+ *   1: Kf = max(0, floor((frac_bf16 L - n_sink - n_recent) / w)),
+ *      Kq = floor(frac_int2 L / w);
+ *   2: Kf as in 1, Kq = floor((budget_frac - frac_bf16) L * 4 d / M_q(w)),
+ *      M_q(w) = w d / 2 + 8 d + 8 w bytes (codes + float32 min/scale).
+ * L is the sequence length at the routing event; all in double precision. */
+typedef struct {
+  int batch;
+  int n_layers;
+  int n_q_heads;
+  int n_kv_heads;      /* n_q_heads / n_kv_heads in {1, 2, 4} */
+  int head_dim;        /* 64 or 128 */
+  int window;          /* w: 16, 32 or 64 tokens */
+  int route_period;    /* Omega (the caller calls qe_route every Omega steps) */
+  int n_sink;          /* 0 <= n_sink < min(window, 16) */
+  int n_recent;        /* recent region length, tokens, >= 1 */
+  int max_context;     /* most tokens per sequence the cache will hold */
+  int cap_mode;        /* 0, 1 or 2, see above */
+  int kf, kq;          /* cap_mode 0 */
+  double frac_bf16;    /* cap_mode 1, 2 */
+  double frac_int2;    /* cap_mode 1 */
+  double budget_frac;  /* cap_mode 2 */
+  int out_fp32;        /* 1: qe_decode_step writes float32, 0: bf16 */
+} qe_config;
+
+/* Pointer-location flags for qe_append / qe_decode_step. */
+enum {
+  QE_DEVICE_PTRS = 0,  /* all buffers are device memory */
+  QE_HOST_PTRS = 1     /* all buffers are host memory (pinned for async copies; pageable works
+                          but the copies then block the calling thread) */
+};
+
+/* Create a cache for cfg on the current CUDA device.  Allocates the device
+ * window pools (bf16 slots for every window up to max_context, 2-bit slots for
+ * the largest Kq), the window table and scores, and a pinned, device-mapped
+ * host backing store that keeps the exact bf16 copy and the 2-bit ledger
+ * entry of every window that has ever been demoted and not evicted.
+ * cuda_stream: a cudaStream_t (NULL = legacy default stream).  The handle
+ * owns everything it allocates.  No kernel runs. */
+qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out);
+
+/* Free everything the handle owns (waits for its stream first). */
+qe_status qe_destroy(qe_handle h);
+
+const char* qe_last_error(qe_handle h);
+
+/* Append n_tokens positions to every sequence of one layer.
+ * k, v: [batch][n_kv_heads][n_tokens][head_dim] bf16 (row-major).
+ * Windows reached for the first time start Pinned with score 0 (QEvict notes
+ * §2 Figure 1: every window starts in full precision).  Prefill is one call
+ * with n_tokens = prompt length; a decode step appends 1 token.
+ * Errors: QE_ERR_CAPACITY if the length would pass max_context. */
+qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_tokens, int flags);
+
+/* One decode step of one layer (QEvict notes §4.1 eq. "attention"; H2O page
+ * §2.1 order: the token appended last is attended too).
+ * q:   [batch][n_q_heads][head_dim] bf16.
+ * out: [batch][n_q_heads][head_dim] float32 (out_fp32) or bf16.
+ * Computes softmax(q K_acc^T / sqrt(d)) V_acc over the sink, the Pinned and
+ * Full bf16 windows and the dequantized INT2 windows (x = code * s + z), and
+ * adds each window's mass, summed over the unit's query heads, to its
+ * float32 score (eq. (1) with the GQA group sum).  Sink tokens are never
+ * scored. */
+qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int flags);
+
+/* Routing event of one layer (layer = -1: all layers), QEvict notes §4.4
+ * Algorithm 1: candidates = Full u Quantized u Pinned windows that are
+ * complete and wholly older than the last n_recent positions (eq. (4));
+ * sorted by score descending, ties to the lower window index (original
+ * position); top Kf -> Full, next Kq -> Quantized, rest -> Evicted (eq. (5)).
+ * A window quantized for the first time is packed from its bf16 values (keys
+ * per channel over the window's tokens, values per token over head_dim,
+ * eq. (2) with b = 2, round half to even, float32 min and scale) and its bf16
+ * values and codes are written to the host backing store; a later demotion
+ * reuses the stored codes; a promotion copies the stored bf16 values back.
+ * All moves complete on the handle's stream before it runs anything else. */
+qe_status qe_route(qe_handle h, int layer);
+
+/* Wait for the handle's stream and report the sticky device flag. */
+qe_status qe_synchronize(qe_handle h);
+
+/* ---------------------------------------------------------------- introspection */
+
+typedef struct {
+  int length;             /* tokens per sequence */
+  int n_windows;          /* windows reached, ceil(length / w) */
+  int routed_upto;        /* windows [0, routed_upto) have entered the candidate pool */
+  int n_full, n_quant;    /* per unit */
+  int n_pinned;           /* per unit, bf16 windows not yet ranked */
+  int kf, kq;             /* capacities at the last routing event */
+  int max_windows;        /* row length of qe_get_tiers / qe_get_scores */
+  int units;              /* batch * n_kv_heads */
+  double attn_bytes;      /* algorithmic bytes one qe_decode_step of this layer reads:
+                             bf16 tokens * 4 d + INT2 windows * M_q(w) */
+} qe_layer_info;
+
+qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info);
+
+/* Tiers [units][max_windows] uint8 (QE_TIER_*); synchronous. */
+qe_status qe_get_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes);
+
+/* Scores [units][max_windows] float32; synchronous. */
+qe_status qe_get_scores(qe_handle h, int layer, float* host, size_t bytes);
+
+/* Overwrite scores [units][max_windows] float32 (tests drive the router with
+ * chosen scores); synchronous with respect to the host buffer. */
+qe_status qe_set_scores(qe_handle h, int layer, const float* host, size_t bytes);
+
+/* Contents of one Quantized window in canonical order; synchronous.
+ * k_codes, v_codes: [w][head_dim] uint8 in 0..3 (rows below n_sink of window 0
+ * are 0); k_min, k_scale: [head_dim] float32; v_min, v_scale: [w] float32.
+ * Errors: QE_ERR_STATE if the window is not Quantized. */
+qe_status qe_get_quant_window(qe_handle h, int layer, int unit, int window,
+                              uint8_t* k_codes, uint8_t* v_codes,
+                              float* k_min, float* k_scale, float* v_min, float* v_scale);
+
+/* bf16 contents [w][head_dim] of a Pinned or Full window (or of the sink when
+ * window = -1); synchronous. */
+qe_status qe_get_bf16_window(qe_handle h, int layer, int unit, int window, uint16_t* k, uint16_t* v);
+
+typedef struct {
+  long long routes;        /* routing events run on this layer */
+  long long first_packs;   /* windows quantized for the first time */
+  long long ledger_reuses; /* demotions that reused stored codes */
+  long long promotions;    /* Quantized -> Full */
+  long long evictions;
+} qe_route_stats;
+
+/* Cumulative routing counters of one layer (layer = -1: summed); synchronous. */
+qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out);
+
+/* Time every qe_decode_step attention launch with CUDA events on the handle's
+ * stream (enable = 1) or stop (0).  qe_get_timing returns the summed device
+ * time in ms, the number of launches and the summed algorithmic bytes of
+ * the timed launches since the last enable, and resets nothing. */
+qe_status qe_set_timing(qe_handle h, int enable);
+qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, double* attn_bytes);
+
+/* Number of kernel launches the handle has enqueued since qe_init. */
+long long qe_kernel_launches(qe_handle h);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QE_H */

@@ -1,0 +1,189 @@
+// qe_common.cuh -- device state layout, fragment-native tile layouts and PTX wrappers.
+//
+// Window slots are stored in the exact register order the m16n8k16 tensor-core
+// fragments want, so the attention kernel moves a whole tile into shared
+// memory with one bulk copy and each lane then reads its operands with
+// conflict-free 16-byte loads (no ldmatrix, no swizzle, no shuffles).
+//
+// bf16 window slot (4 w d bytes): w/16 sub-tiles of 16 tokens; each sub-tile
+// holds the key fragments (d/16 of 512 B, A operand of Q K^T with tokens as
+// rows) followed by the value fragments (d/16 of 512 B, A operand of V^T P^T
+// with channels as rows).
+//
+// 2-bit window slot: key codes (w d / 4 B), value codes (w d / 4 B), key
+// min[d], key scale[d], value min[w], value scale[w] (float32).  Codes are
+// grouped per lane in 32-bit words; a word carries two fragments of 8 codes;
+// fragment f, register r, element e sits at bit 2 (4 f + r) + 16 e, so
+// (word >> 2j) & 0x00030003 yields a bf16x2 pair after adding the exponent.
+#pragma once
+#include <cstdint>
+#include <cuda_runtime.h>
+
+#ifndef QE_HD
+#define QE_HD __host__ __device__ __forceinline__
+#endif
+
+namespace qe {
+
+enum : int { TIER_NONE = 0, TIER_PINNED = 1, TIER_FULL = 2, TIER_QUANT = 3, TIER_EVICTED = 4 };
+
+enum : unsigned { ERR_FREELIST = 1u, ERR_TABLE = 2u, ERR_TIMEOUT = 4u, ERR_COUNT = 8u, ERR_MOVES = 16u };
+
+// ---------------------------------------------------------------------------- geometry
+struct Geo {
+  int D, W;
+  QE_HD int sub_tiles() const { return W / 16; }
+  QE_HD int sub_bytes() const { return 64 * D; }                 // 16 tokens, K + V, bf16
+  QE_HD int bslot_bytes() const { return 4 * W * D; }
+  QE_HD int kcode_bytes() const { return W * D / 4; }
+  QE_HD int qslot_bytes() const { return 2 * (W * D / 4) + 8 * D + 8 * W; }
+  QE_HD int wpl() const { return (W / 16) * (D / 16) / 2; }       // code words per lane (K or V)
+  QE_HD int cw() const { return wpl() < 4 ? wpl() : 4; }          // words per lane per chunk
+  QE_HD int off_kmin() const { return 2 * kcode_bytes(); }
+  QE_HD int off_kscale() const { return 2 * kcode_bytes() + 4 * D; }
+  QE_HD int off_vmin() const { return 2 * kcode_bytes() + 8 * D; }
+  QE_HD int off_vscale() const { return 2 * kcode_bytes() + 8 * D + 4 * W; }
+};
+
+// byte offset of K[r][c] inside a bf16 slot (r < W)
+QE_HD int bf16_k_off(const Geo& g, int r, int c) {
+  int sub = r >> 4, rr = r & 15, ks = c >> 4, ci = c & 15;
+  int lane = (rr & 7) * 4 + ((ci & 7) >> 1);
+  int reg = (rr >> 3) + 2 * (ci >> 3);
+  return sub * g.sub_bytes() + ks * 512 + lane * 16 + reg * 4 + (ci & 1) * 2;
+}
+// byte offset of V[r][c] inside a bf16 slot
+QE_HD int bf16_v_off(const Geo& g, int r, int c) {
+  int sub = r >> 4, rt = r & 15, mc = c >> 4, rc = c & 15;
+  int lane = (rc & 7) * 4 + ((rt & 7) >> 1);
+  int reg = (rc >> 3) + 2 * (rt >> 3);
+  return sub * g.sub_bytes() + 32 * g.D + mc * 512 + lane * 16 + reg * 4 + (rt & 1) * 2;
+}
+
+// (byte offset of the 32-bit word, bit position) of a code inside the K or V code block
+struct CodePos { int byte; int bit; };
+QE_HD CodePos code_word(const Geo& g, int F, int lane, int reg, int e) {
+  int wi = F >> 1, f = F & 1;
+  int cw = g.cw();
+  CodePos p;
+  p.byte = ((wi / cw) * 32 + lane) * (cw * 4) + (wi % cw) * 4;
+  p.bit = 2 * (4 * f + reg) + 16 * e;
+  return p;
+}
+// key code of token r, channel c (fragments ordered token-tile major, channel-step minor)
+QE_HD CodePos kcode_pos(const Geo& g, int r, int c) {
+  int mt = r >> 4, rr = r & 15, ks = c >> 4, ci = c & 15;
+  int lane = (rr & 7) * 4 + ((ci & 7) >> 1);
+  int reg = (rr >> 3) + 2 * (ci >> 3);
+  return code_word(g, mt * (g.D / 16) + ks, lane, reg, ci & 1);
+}
+// value code of token r, channel c (A = V^T: fragments ordered channel-tile major, token-step minor)
+QE_HD CodePos vcode_pos(const Geo& g, int r, int c) {
+  int mc = c >> 4, rc = c & 15, kt = r >> 4, rt = r & 15;
+  int lane = (rc & 7) * 4 + ((rt & 7) >> 1);
+  int reg = (rc >> 3) + 2 * (rt >> 3);
+  CodePos p = code_word(g, mc * (g.W / 16) + kt, lane, reg, rt & 1);
+  p.byte += g.kcode_bytes();
+  return p;
+}
+
+// ---------------------------------------------------------------------------- cache state
+// Arrays are indexed by the global unit gu = layer * units + (b * n_kv_heads + kvh).
+struct State {
+  int units;          // per layer
+  int n_layers;
+  int maxw;           // windows per sequence
+  int capb, capq, caps;
+  int n_sink, n_recent, G, Hq, Hkv;
+  Geo geo;
+  uint8_t* tier;      // [GU][maxw]
+  int* bslot;         // [GU][maxw]
+  int* qslot;         // [GU][maxw]
+  int* sent;          // [GU][maxw] host store / ledger entry
+  float* score;       // [GU][maxw]
+  int2* blist;        // [GU][capb] {window, slot}; entry 0 is the sink {-1, 0}
+  int2* qlist;        // [GU][capq]
+  int* bfree; int* bfree_top;   // [GU][capb], [GU]
+  int* qfree; int* qfree_top;   // [GU][capq], [GU]
+  int* sfree; int* sfree_top;   // [GU][caps], [GU]
+  uint8_t* bslab;     // [GU][capb][bslot_bytes]
+  uint8_t* qslab;     // [GU][capq][qslot_bytes]
+  uint8_t* hstore;    // device pointer to pinned host [GU][caps][bslot_bytes]
+  uint8_t* hledger;   // device pointer to pinned host [GU][caps][qslot_bytes]
+  unsigned* err;      // sticky flag
+  unsigned long long* stats;  // [layers][5]
+};
+
+// ---------------------------------------------------------------------------- PTX helpers
+#if defined(__CUDACC__)
+__device__ __forceinline__ unsigned smem_u32(const void* p) {
+  return static_cast<unsigned>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void mbar_fence_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(unsigned bar, unsigned bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(unsigned bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done) : "r"(bar), "r"(parity) : "memory");
+  return done != 0;
+}
+__device__ __forceinline__ void bulk_g2s(unsigned dst, const void* src, unsigned bytes, unsigned bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+      ::"r"(dst), "l"(src), "r"(bytes), "r"(bar) : "memory");
+}
+__device__ __forceinline__ unsigned long long globaltimer_ns() {
+  unsigned long long t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+__device__ __forceinline__ void mma_bf16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                         unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ unsigned movmatrix_t(unsigned a) {
+  unsigned d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+// two small codes in the halves of x (bits 0-1 and 16-17) -> exact bf16x2 values
+__device__ __forceinline__ unsigned codes_to_bf16x2(unsigned x) {
+  unsigned v = (x & 0x00030003u) | 0x43004300u;      // 128 + code in each half
+  unsigned d;
+  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(0x43004300u));
+  return d;
+}
+// bf16x2 from two floats: lo -> low half, hi -> high half (round to nearest even)
+__device__ __forceinline__ unsigned pack_bf16x2(float lo, float hi) {
+  unsigned d;
+  asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float lg2(float x) {
+  float y;
+  asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+__device__ __forceinline__ float bf16lo_to_f32(unsigned x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf16hi_to_f32(unsigned x) { return __uint_as_float(x & 0xFFFF0000u); }
+#endif
+
+}  // namespace qe

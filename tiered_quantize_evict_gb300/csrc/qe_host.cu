@@ -1,0 +1,699 @@
+// qe_host.cu -- C ABI (include/qe.h): handle, device pools, host mirror, launches.
+//
+// The host keeps a mirror of the per-layer counts that every unit shares (all sequences of a
+// layer have the same length, so after each routing event every unit has the same number of
+// Full, Quantized and Pinned windows); launch shapes are computed from it without reading the
+// device.  Window identities, slots, scores and codes live only on the device.
+#include <cmath>
+#include <cstdarg>
+#include <cstdio>
+#include <cstdlib>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qe.h"
+#include "qe_kernels.cuh"
+
+namespace {
+
+struct LayerMirror {
+  int L = 0;
+  int routed_upto = 0;
+  int n_full = 0;
+  int n_quant = 0;
+  int kf = 0, kq = 0;
+};
+
+thread_local std::string g_init_error;
+
+}  // namespace
+
+struct qe_handle_s {
+  qe_config cfg{};
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  int n_sm = 0;
+  qe::State st{};
+  std::vector<LayerMirror> lay;
+  int units = 0;
+  long long gu_total = 0;
+  // scratch for the attention split-K
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  float* lse = nullptr;
+  long long part_slots = 0;   // warps * maxseg capacity
+  int maxseg_cap = 0;
+  int ntiles_cap = 0;
+  // moves
+  qe::Move* moves = nullptr;
+  int* n_moves = nullptr;
+  int max_moves = 0;
+  // staging for host pointers
+  void* stage[4] = {nullptr, nullptr, nullptr, nullptr};
+  size_t stage_bytes[4] = {0, 0, 0, 0};
+  // pinned host store
+  void* hstore_host = nullptr;
+  void* hledger_host = nullptr;
+  // tile costs of the split-K partition
+  int cost_b = 8, cost_q = 6;
+  // timing
+  bool timing = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  double timed_bytes = 0;
+  long long timed_launches = 0;
+  long long launches = 0;
+  std::string err;
+};
+
+namespace {
+
+qe_status fail(qe_handle h, qe_status s, const char* fmt, ...) {
+  char buf[512];
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(buf, sizeof buf, fmt, ap);
+  va_end(ap);
+  if (h) h->err = buf; else g_init_error = buf;
+  return s;
+}
+
+#define QE_CK(h, call)                                                                            \
+  do {                                                                                            \
+    cudaError_t e_ = (call);                                                                      \
+    if (e_ != cudaSuccess)                                                                        \
+      return fail((h), e_ == cudaErrorMemoryAllocation ? QE_ERR_OOM : QE_ERR_CUDA, "%s: %s (%s:%d)", #call, \
+                  cudaGetErrorString(e_), __FILE__, __LINE__);                                    \
+  } while (0)
+
+int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
+
+int qslot_bytes(int w, int d) { return 2 * (w * d / 4) + 8 * d + 8 * w; }
+
+// Capacity rule, see qe.h (evaluated in double in the order written there)
+void capacities(const qe_config& c, int L, int& kf, int& kq) {
+  if (c.cap_mode == 0) {
+    kf = c.kf;
+    kq = c.kq;
+    return;
+  }
+  double f = std::floor((c.frac_bf16 * L - c.n_sink - c.n_recent) / c.window);
+  kf = f < 0 ? 0 : (int)f;
+  double q;
+  if (c.cap_mode == 1) q = std::floor(c.frac_int2 * L / c.window);
+  else q = std::floor((c.budget_frac - c.frac_bf16) * L * (4.0 * c.head_dim) / qslot_bytes(c.window, c.head_dim));
+  kq = q < 0 ? 0 : (int)q;
+}
+
+template <class T>
+qe_status dalloc(qe_handle h, T** p, size_t count, const char* what) {
+  cudaError_t e = cudaMalloc((void**)p, count * sizeof(T) > 0 ? count * sizeof(T) : 16);
+  if (e != cudaSuccess)
+    return fail(h, QE_ERR_OOM, "cudaMalloc of %s (%zu bytes) failed: %s", what, count * sizeof(T), cudaGetErrorString(e));
+  return QE_OK;
+}
+
+qe_status check_layer(qe_handle h, int layer) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  if (layer < 0 || layer >= h->cfg.n_layers) return fail(h, QE_ERR_INVALID_ARG, "layer %d out of range", layer);
+  return QE_OK;
+}
+
+qe_status ensure_stage(qe_handle h, int i, size_t bytes) {
+  if (h->stage_bytes[i] >= bytes) return QE_OK;
+  if (h->stage[i]) cudaFree(h->stage[i]);
+  h->stage[i] = nullptr;
+  h->stage_bytes[i] = 0;
+  QE_CK(h, cudaMalloc(&h->stage[i], bytes));
+  h->stage_bytes[i] = bytes;
+  return QE_OK;
+}
+
+int nbw_of(const qe_handle h, const LayerMirror& m) {
+  const int nwin = ceil_div(m.L, h->cfg.window);
+  return 1 + m.n_full + (nwin - m.routed_upto);
+}
+
+void free_all(qe_handle h) {
+  qe::State& s = h->st;
+  void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_top, s.qfree,
+                  s.qfree_top, s.sfree, s.sfree_top, s.bslab, s.qslab, s.err, s.stats, h->part_o, h->part_ml,
+                  h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3]};
+  for (void* p : ptrs)
+    if (p) cudaFree(p);
+  if (h->hstore_host) cudaFreeHost(h->hstore_host);
+  if (h->hledger_host) cudaFreeHost(h->hledger_host);
+  for (cudaEvent_t e : h->ev_pool) cudaEventDestroy(e);
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* qe_last_error(qe_handle h) { return h ? h->err.c_str() : g_init_error.c_str(); }
+
+long long qe_kernel_launches(qe_handle h) { return h ? h->launches : 0; }
+
+qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
+  if (!cfg || !out) return fail(nullptr, QE_ERR_INVALID_ARG, "null argument");
+  const qe_config& c = *cfg;
+  if (c.batch < 1 || c.n_layers < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1 || c.n_q_heads % c.n_kv_heads)
+    return fail(nullptr, QE_ERR_INVALID_ARG, "bad head/batch/layer counts");
+  const int G = c.n_q_heads / c.n_kv_heads;
+  if (G != 1 && G != 2 && G != 4) return fail(nullptr, QE_ERR_INVALID_ARG, "query heads per KV head must be 1, 2 or 4");
+  if (c.head_dim != 64 && c.head_dim != 128) return fail(nullptr, QE_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  if (c.window != 16 && c.window != 32 && c.window != 64) return fail(nullptr, QE_ERR_INVALID_ARG, "window must be 16, 32 or 64");
+  if (c.n_sink < 0 || c.n_sink >= c.window || c.n_sink >= 16) return fail(nullptr, QE_ERR_INVALID_ARG, "need 0 <= n_sink < min(window, 16)");
+  if (c.n_recent < 1) return fail(nullptr, QE_ERR_INVALID_ARG, "n_recent must be >= 1");
+  if (c.max_context < 1 || c.cap_mode < 0 || c.cap_mode > 2) return fail(nullptr, QE_ERR_INVALID_ARG, "bad max_context or cap_mode");
+  if (c.cap_mode == 0 && (c.kf < 0 || c.kq < 0)) return fail(nullptr, QE_ERR_INVALID_ARG, "kf, kq must be >= 0");
+
+  qe_handle h = new qe_handle_s();
+  h->cfg = c;
+  h->stream = static_cast<cudaStream_t>(cuda_stream);
+  cudaError_t e = cudaGetDevice(&h->device);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&h->n_sm, cudaDevAttrMultiProcessorCount, h->device);
+  if (e != cudaSuccess) {
+    delete h;
+    return fail(nullptr, QE_ERR_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
+  }
+  if (const char* s = getenv("QE_TILE_COSTS")) sscanf(s, "%d,%d", &h->cost_b, &h->cost_q);
+  h->cost_q = h->cost_q * c.window / 32 > 0 ? h->cost_q * c.window / 32 : 1;
+
+  const int maxw = ceil_div(c.max_context, c.window);
+  if (maxw > 4096) {
+    delete h;
+    return fail(nullptr, QE_ERR_INVALID_ARG, "max_context / window must be <= 4096 windows");
+  }
+  int kf_max = 0, kq_max = 0;
+  capacities(c, c.max_context, kf_max, kq_max);
+  h->units = c.batch * c.n_kv_heads;
+  h->gu_total = (long long)h->units * c.n_layers;
+  qe::State& st = h->st;
+  st.units = h->units;
+  st.n_layers = c.n_layers;
+  st.maxw = maxw;
+  st.capb = 1 + maxw;
+  st.capq = kq_max > 0 ? kq_max : 1;
+  st.caps = (kf_max + kq_max) > 0 ? kf_max + kq_max : 1;
+  if (st.caps > maxw) st.caps = maxw;
+  if (st.capq > maxw) st.capq = maxw;
+  st.n_sink = c.n_sink;
+  st.n_recent = c.n_recent;
+  st.G = G;
+  st.Hq = c.n_q_heads;
+  st.Hkv = c.n_kv_heads;
+  st.geo.D = c.head_dim;
+  st.geo.W = c.window;
+  h->lay.assign(c.n_layers, LayerMirror{});
+
+  const long long GU = h->gu_total;
+  const size_t bslot_b = (size_t)st.geo.bslot_bytes(), qslot_b = (size_t)st.geo.qslot_bytes();
+  qe_status s;
+#define QE_ALLOC(ptr, n, what)                              \
+  if ((s = dalloc(h, &(ptr), (size_t)(n), what)) != QE_OK) { \
+    std::string m = h->err;                                 \
+    free_all(h);                                            \
+    delete h;                                               \
+    g_init_error = m;                                       \
+    return s;                                               \
+  }
+  QE_ALLOC(st.tier, GU * maxw, "tier");
+  QE_ALLOC(st.bslot, GU * maxw, "bslot");
+  QE_ALLOC(st.qslot, GU * maxw, "qslot");
+  QE_ALLOC(st.sent, GU * maxw, "sent");
+  QE_ALLOC(st.score, GU * maxw, "score");
+  QE_ALLOC(st.blist, GU * st.capb, "blist");
+  QE_ALLOC(st.qlist, GU * st.capq, "qlist");
+  QE_ALLOC(st.bfree, GU * st.capb, "bfree");
+  QE_ALLOC(st.bfree_top, GU, "bfree_top");
+  QE_ALLOC(st.qfree, GU * st.capq, "qfree");
+  QE_ALLOC(st.qfree_top, GU, "qfree_top");
+  QE_ALLOC(st.sfree, GU * st.caps, "sfree");
+  QE_ALLOC(st.sfree_top, GU, "sfree_top");
+  QE_ALLOC(st.bslab, GU * st.capb * bslot_b, "bf16 window pool");
+  QE_ALLOC(st.qslab, GU * st.capq * qslot_b, "2-bit window pool");
+  QE_ALLOC(st.err, 1, "error flag");
+  QE_ALLOC(st.stats, (size_t)c.n_layers * 5, "stats");
+
+  // split-K scratch: one CTA per SM, attn_warps_per_cta() warps each
+  const int NW = h->n_sm * qe::attn_warps_per_cta();
+  h->maxseg_cap = ceil_div(h->units, NW) + 3;
+  h->part_slots = (long long)NW * h->maxseg_cap;
+  h->ntiles_cap = st.capb * (c.window / 16) + st.capq;
+  QE_ALLOC(h->part_o, h->part_slots * G * c.head_dim, "partials");
+  QE_ALLOC(h->part_ml, h->part_slots * G, "partial stats");
+  QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
+  h->max_moves = h->units * st.caps + 16;
+  {
+    void* mp = nullptr;
+    if (cudaMalloc(&mp, (size_t)h->max_moves * sizeof(qe::Move)) != cudaSuccess) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, QE_ERR_OOM, "cudaMalloc of the move list failed");
+    }
+    h->moves = static_cast<qe::Move*>(mp);
+  }
+  QE_ALLOC(h->n_moves, 1, "move count");
+#undef QE_ALLOC
+
+  // pinned host backing store, mapped into the device address space
+  e = cudaHostAlloc(&h->hstore_host, (size_t)GU * st.caps * bslot_b, cudaHostAllocMapped);
+  if (e == cudaSuccess) e = cudaHostAlloc(&h->hledger_host, (size_t)GU * st.caps * qslot_b, cudaHostAllocMapped);
+  void* dstore = nullptr;
+  void* dledger = nullptr;
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dstore, h->hstore_host, 0);
+  if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dledger, h->hledger_host, 0);
+  if (e != cudaSuccess) {
+    std::string m = std::string("pinned host store: ") + cudaGetErrorString(e);
+    free_all(h);
+    delete h;
+    g_init_error = m;
+    return QE_ERR_HOST_STORE;
+  }
+  st.hstore = static_cast<uint8_t*>(dstore);
+  st.hledger = static_cast<uint8_t*>(dledger);
+
+  // initial table: nothing reached; free stacks hold every slot (bf16 slot 0 is the sink's)
+  cudaError_t ie = cudaSuccess;
+  auto set = [&](cudaError_t x) { if (ie == cudaSuccess) ie = x; };
+  set(cudaMemsetAsync(st.tier, 0, GU * maxw, h->stream));
+  set(cudaMemsetAsync(st.bslot, 0xFF, GU * maxw * 4, h->stream));
+  set(cudaMemsetAsync(st.qslot, 0xFF, GU * maxw * 4, h->stream));
+  set(cudaMemsetAsync(st.sent, 0xFF, GU * maxw * 4, h->stream));
+  set(cudaMemsetAsync(st.score, 0, GU * maxw * 4, h->stream));
+  set(cudaMemsetAsync(st.bslab, 0, GU * st.capb * bslot_b, h->stream));
+  set(cudaMemsetAsync(st.qslab, 0, GU * st.capq * qslot_b, h->stream));
+  set(cudaMemsetAsync(st.err, 0, 4, h->stream));
+  set(cudaMemsetAsync(st.stats, 0, (size_t)c.n_layers * 5 * 8, h->stream));
+  {
+    std::vector<int> tmp;
+    tmp.resize((size_t)GU * st.capb);
+    for (long long gu = 0; gu < GU; ++gu)
+      for (int i = 0; i < st.capb - 1; ++i) tmp[gu * st.capb + i] = st.capb - 1 - i;
+    set(cudaMemcpy(st.bfree, tmp.data(), tmp.size() * 4, cudaMemcpyHostToDevice));
+    std::vector<int> top(GU, st.capb - 1);
+    set(cudaMemcpy(st.bfree_top, top.data(), GU * 4, cudaMemcpyHostToDevice));
+    tmp.assign((size_t)GU * st.capq, 0);
+    for (long long gu = 0; gu < GU; ++gu)
+      for (int i = 0; i < st.capq; ++i) tmp[gu * st.capq + i] = st.capq - 1 - i;
+    set(cudaMemcpy(st.qfree, tmp.data(), tmp.size() * 4, cudaMemcpyHostToDevice));
+    top.assign(GU, st.capq);
+    set(cudaMemcpy(st.qfree_top, top.data(), GU * 4, cudaMemcpyHostToDevice));
+    tmp.assign((size_t)GU * st.caps, 0);
+    for (long long gu = 0; gu < GU; ++gu)
+      for (int i = 0; i < st.caps; ++i) tmp[gu * st.caps + i] = st.caps - 1 - i;
+    set(cudaMemcpy(st.sfree, tmp.data(), tmp.size() * 4, cudaMemcpyHostToDevice));
+    top.assign(GU, st.caps);
+    set(cudaMemcpy(st.sfree_top, top.data(), GU * 4, cudaMemcpyHostToDevice));
+    std::vector<int2> bl((size_t)GU * st.capb, make_int2(-1, -1));
+    for (long long gu = 0; gu < GU; ++gu) bl[gu * st.capb] = make_int2(-1, 0);
+    set(cudaMemcpy(st.blist, bl.data(), bl.size() * sizeof(int2), cudaMemcpyHostToDevice));
+  }
+  set(cudaStreamSynchronize(h->stream));
+  if (ie != cudaSuccess) {
+    std::string m = std::string("initialising the cache: ") + cudaGetErrorString(ie);
+    free_all(h);
+    delete h;
+    g_init_error = m;
+    return QE_ERR_CUDA;
+  }
+  *out = h;
+  return QE_OK;
+}
+
+qe_status qe_destroy(qe_handle h) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  cudaStreamSynchronize(h->stream);
+  free_all(h);
+  delete h;
+  return QE_OK;
+}
+
+qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_tokens, int flags) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if (!k || !v || n_tokens < 1) return fail(h, QE_ERR_INVALID_ARG, "append needs K, V and n_tokens >= 1");
+  LayerMirror& m = h->lay[layer];
+  if (m.L + n_tokens > h->cfg.max_context)
+    return fail(h, QE_ERR_CAPACITY, "append of %d tokens passes max_context %d (length %d)", n_tokens,
+                h->cfg.max_context, m.L);
+  const size_t bytes = (size_t)h->units * n_tokens * h->cfg.head_dim * 2;
+  const uint16_t* kd = static_cast<const uint16_t*>(k);
+  const uint16_t* vd = static_cast<const uint16_t*>(v);
+  if (flags & QE_HOST_PTRS) {
+    if ((s = ensure_stage(h, 0, bytes)) != QE_OK || (s = ensure_stage(h, 1, bytes)) != QE_OK) return s;
+    QE_CK(h, cudaMemcpyAsync(h->stage[0], k, bytes, cudaMemcpyHostToDevice, h->stream));
+    QE_CK(h, cudaMemcpyAsync(h->stage[1], v, bytes, cudaMemcpyHostToDevice, h->stream));
+    kd = static_cast<const uint16_t*>(h->stage[0]);
+    vd = static_cast<const uint16_t*>(h->stage[1]);
+  }
+  const int w_old = ceil_div(m.L, h->cfg.window), w_new = ceil_div(m.L + n_tokens, h->cfg.window);
+  if (w_new > w_old) {
+    const int nbw_old = nbw_of(h, m);
+    QE_CK(h, qe::launch_open_windows(h->st, layer, w_old, w_new, nbw_old, h->stream));
+    ++h->launches;
+  }
+  QE_CK(h, qe::launch_append(h->st, layer, m.L, n_tokens, kd, vd, h->n_sm, h->stream));
+  ++h->launches;
+  m.L += n_tokens;
+  return QE_OK;
+}
+
+qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int flags) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if (!q || !out) return fail(h, QE_ERR_INVALID_ARG, "decode needs q and out");
+  LayerMirror& m = h->lay[layer];
+  if (m.L < 1) return fail(h, QE_ERR_STATE, "decode on an empty layer");
+  const qe_config& c = h->cfg;
+  const int D = c.head_dim;
+  const size_t qbytes = (size_t)c.batch * c.n_q_heads * D * 2;
+  const size_t obytes = (size_t)c.batch * c.n_q_heads * D * (c.out_fp32 ? 4 : 2);
+  const uint16_t* qd = static_cast<const uint16_t*>(q);
+  void* od = out;
+  if (flags & QE_HOST_PTRS) {
+    if ((s = ensure_stage(h, 2, qbytes)) != QE_OK || (s = ensure_stage(h, 3, obytes)) != QE_OK) return s;
+    QE_CK(h, cudaMemcpyAsync(h->stage[2], q, qbytes, cudaMemcpyHostToDevice, h->stream));
+    qd = static_cast<const uint16_t*>(h->stage[2]);
+    od = h->stage[3];
+  }
+  qe::AttnParams p{};
+  p.st = h->st;
+  p.layer = layer;
+  p.L = m.L;
+  p.nbw = nbw_of(h, m);
+  p.nq = m.n_quant;
+  p.cb = h->cost_b;
+  p.cq = h->cost_q;
+  const int sub = c.window / 16;
+  p.ntiles = p.nbw * sub + p.nq;
+  if (p.ntiles > h->ntiles_cap) return fail(h, QE_ERR_CAPACITY, "tile count %d exceeds %d", p.ntiles, h->ntiles_cap);
+  p.Cu = (long long)p.nbw * sub * p.cb + (long long)p.nq * p.cq;
+  p.C = p.Cu * h->units;
+  // warps: at most one per SM slot, at most one per unit of cost granularity, and few
+  // enough that a unit never meets more than 256 partials
+  const int wpc = qe::attn_warps_per_cta();
+  long long nw = (long long)h->n_sm * wpc;
+  const long long tiles_total = (long long)p.ntiles * h->units;
+  if (nw > tiles_total) nw = tiles_total;
+  if (nw > 250LL * h->units) nw = 250LL * h->units;
+  int grid = ceil_div(nw, wpc);
+  if (grid < 1) grid = 1;
+  p.NW = grid * wpc;
+  // partial slots per warp: units met by one warp range
+  p.maxseg = (int)((p.C / p.NW) / p.Cu) + 2;
+  if (p.maxseg > h->maxseg_cap) return fail(h, QE_ERR_CAPACITY, "split-K needs %d partial slots per warp", p.maxseg);
+  if ((long long)p.NW * p.maxseg > h->part_slots)
+    return fail(h, QE_ERR_CAPACITY, "split-K scratch too small (%d x %d)", p.NW, p.maxseg);
+  p.q = qd;
+  p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  p.part_o = h->part_o;
+  p.part_ml = h->part_ml;
+  p.lse = h->lse;
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  if (h->timing) {
+    while (h->ev_pool.size() < h->ev_used + 2) {
+      cudaEvent_t ev;
+      QE_CK(h, cudaEventCreate(&ev));
+      h->ev_pool.push_back(ev);
+    }
+    e0 = h->ev_pool[h->ev_used];
+    e1 = h->ev_pool[h->ev_used + 1];
+    h->ev_used += 2;
+    QE_CK(h, cudaEventRecord(e0, h->stream));
+  }
+  QE_CK(h, qe::launch_decode_attn(p, grid, h->stream));
+  ++h->launches;
+  if (h->timing) {
+    QE_CK(h, cudaEventRecord(e1, h->stream));
+    h->timed_launches += 1;
+    qe_layer_info info;
+    qe_get_layer_info(h, layer, &info);
+    h->timed_bytes += info.attn_bytes;
+  }
+  qe::CombineParams cp{};
+  cp.st = h->st;
+  cp.layer = layer;
+  cp.L = m.L;
+  cp.nbw = p.nbw;
+  cp.nq = p.nq;
+  cp.ntiles = p.ntiles;
+  cp.cb = p.cb;
+  cp.cq = p.cq;
+  cp.Cu = p.Cu;
+  cp.C = p.C;
+  cp.NW = p.NW;
+  cp.maxseg = p.maxseg;
+  cp.part_o = h->part_o;
+  cp.part_ml = h->part_ml;
+  cp.lse = h->lse;
+  cp.out = od;
+  cp.out_fp32 = c.out_fp32;
+  QE_CK(h, qe::launch_attn_combine(cp, h->stream));
+  ++h->launches;
+  if (flags & QE_HOST_PTRS) QE_CK(h, cudaMemcpyAsync(out, od, obytes, cudaMemcpyDeviceToHost, h->stream));
+  return QE_OK;
+}
+
+static qe_status route_layer(qe_handle h, int layer) {
+  LayerMirror& m = h->lay[layer];
+  const qe_config& c = h->cfg;
+  const int nwin = ceil_div(m.L, c.window);
+  int aged = (m.L - c.n_recent) >= 0 ? (m.L - c.n_recent) / c.window : 0;
+  if (aged < m.routed_upto) aged = m.routed_upto;
+  int kf, kq;
+  capacities(c, m.L, kf, kq);
+  if (kq > h->st.capq) return fail(h, QE_ERR_CAPACITY, "Kq %d exceeds the 2-bit pool (%d)", kq, h->st.capq);
+  const int ncand = m.n_full + m.n_quant + (aged - m.routed_upto);
+  const int nf = kf < ncand ? kf : ncand;
+  const int nq = kq < ncand - nf ? kq : ncand - nf;
+  if (nf + nq > h->st.caps) return fail(h, QE_ERR_CAPACITY, "kept windows %d exceed the host store (%d)", nf + nq, h->st.caps);
+  qe::RouteParams p{};
+  p.st = h->st;
+  p.layer = layer;
+  p.L = m.L;
+  p.n_windows = nwin;
+  p.routed_old = m.routed_upto;
+  p.aged_upto = aged;
+  p.kf = kf;
+  p.kq = kq;
+  p.exp_nfull = nf;
+  p.exp_nquant = nq;
+  p.moves = h->moves;
+  p.n_moves = h->n_moves;
+  p.max_moves = h->max_moves;
+  QE_CK(h, cudaMemsetAsync(h->n_moves, 0, 4, h->stream));
+  QE_CK(h, qe::launch_route(p, h->stream));
+  QE_CK(h, qe::launch_moves(h->st, h->moves, h->n_moves, h->n_sm, h->stream));
+  h->launches += 2;
+  m.routed_upto = aged;
+  m.n_full = nf;
+  m.n_quant = nq;
+  m.kf = kf;
+  m.kq = kq;
+  return QE_OK;
+}
+
+qe_status qe_route(qe_handle h, int layer) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  if (layer == -1) {
+    for (int l = 0; l < h->cfg.n_layers; ++l) {
+      qe_status s = route_layer(h, l);
+      if (s != QE_OK) return s;
+    }
+    return QE_OK;
+  }
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  return route_layer(h, layer);
+}
+
+qe_status qe_synchronize(qe_handle h) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  unsigned flag = 0;
+  QE_CK(h, cudaMemcpy(&flag, h->st.err, 4, cudaMemcpyDeviceToHost));
+  if (flag)
+    return fail(h, flag & qe::ERR_TIMEOUT ? QE_ERR_TIMEOUT : QE_ERR_DEVICE,
+                "device consistency flag 0x%x (1 free list, 2 table, 4 wait timeout, 8 count mismatch, 16 move list)",
+                flag);
+  return QE_OK;
+}
+
+qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if (!info) return fail(h, QE_ERR_INVALID_ARG, "null info");
+  const LayerMirror& m = h->lay[layer];
+  const qe_config& c = h->cfg;
+  info->length = m.L;
+  info->n_windows = ceil_div(m.L, c.window);
+  info->routed_upto = m.routed_upto;
+  info->n_full = m.n_full;
+  info->n_quant = m.n_quant;
+  info->n_pinned = info->n_windows - m.routed_upto;
+  info->kf = m.kf;
+  info->kq = m.kq;
+  info->max_windows = h->st.maxw;
+  info->units = h->units;
+  // bf16 tokens actually present: sink + Full windows (complete) + Pinned windows (window 0
+  // and the current window partial)
+  double tok = std::min(c.n_sink, m.L);
+  tok += (double)m.n_full * c.window;
+  for (int j = m.routed_upto; j < info->n_windows; ++j) {
+    int lo = j == 0 ? c.n_sink : 0;
+    int hi = std::min(c.window, m.L - j * c.window);
+    if (hi > lo) tok += hi - lo;
+  }
+  // a Full window 0 holds w - n_sink tokens; the correction is below one window per unit
+  info->attn_bytes = (tok * 4.0 * c.head_dim + (double)m.n_quant * qslot_bytes(c.window, c.head_dim)) * h->units;
+  return QE_OK;
+}
+
+qe_status qe_get_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  const size_t need = (size_t)h->units * h->st.maxw;
+  if (!host || bytes < need) return fail(h, QE_ERR_INVALID_ARG, "tier buffer needs %zu bytes", need);
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  QE_CK(h, cudaMemcpy(host, h->st.tier + (size_t)layer * need, need, cudaMemcpyDeviceToHost));
+  return QE_OK;
+}
+
+qe_status qe_get_scores(qe_handle h, int layer, float* host, size_t bytes) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  const size_t n = (size_t)h->units * h->st.maxw;
+  if (!host || bytes < n * 4) return fail(h, QE_ERR_INVALID_ARG, "score buffer needs %zu bytes", n * 4);
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  QE_CK(h, cudaMemcpy(host, h->st.score + (size_t)layer * n, n * 4, cudaMemcpyDeviceToHost));
+  return QE_OK;
+}
+
+qe_status qe_set_scores(qe_handle h, int layer, const float* host, size_t bytes) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  const size_t n = (size_t)h->units * h->st.maxw;
+  if (!host || bytes < n * 4) return fail(h, QE_ERR_INVALID_ARG, "score buffer needs %zu bytes", n * 4);
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  QE_CK(h, cudaMemcpy(h->st.score + (size_t)layer * n, host, n * 4, cudaMemcpyHostToDevice));
+  return QE_OK;
+}
+
+static qe_status read_int(qe_handle h, const int* dptr, int* out) {
+  QE_CK(h, cudaMemcpy(out, dptr, 4, cudaMemcpyDeviceToHost));
+  return QE_OK;
+}
+
+qe_status qe_get_quant_window(qe_handle h, int layer, int unit, int window, uint8_t* k_codes, uint8_t* v_codes,
+                              float* k_min, float* k_scale, float* v_min, float* v_scale) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if (unit < 0 || unit >= h->units || window < 0 || window >= h->st.maxw)
+    return fail(h, QE_ERR_INVALID_ARG, "unit or window out of range");
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  const long long gu = (long long)layer * h->units + unit;
+  uint8_t tier = 0;
+  QE_CK(h, cudaMemcpy(&tier, h->st.tier + gu * h->st.maxw + window, 1, cudaMemcpyDeviceToHost));
+  if (tier != QE_TIER_QUANT) return fail(h, QE_ERR_STATE, "window %d is not Quantized (tier %d)", window, tier);
+  int slot = -1;
+  if ((s = read_int(h, h->st.qslot + gu * h->st.maxw + window, &slot)) != QE_OK) return s;
+  if (slot < 0 || slot >= h->st.capq) return fail(h, QE_ERR_DEVICE, "bad 2-bit slot %d", slot);
+  const qe::Geo g = h->st.geo;
+  std::vector<uint8_t> buf(g.qslot_bytes());
+  QE_CK(h, cudaMemcpy(buf.data(), h->st.qslab + (gu * h->st.capq + slot) * (long long)g.qslot_bytes(), buf.size(),
+                      cudaMemcpyDeviceToHost));
+  for (int r = 0; r < g.W; ++r)
+    for (int c = 0; c < g.D; ++c) {
+      qe::CodePos pk = qe::kcode_pos(g, r, c), pv = qe::vcode_pos(g, r, c);
+      unsigned wk, wv;
+      memcpy(&wk, buf.data() + pk.byte, 4);
+      memcpy(&wv, buf.data() + pv.byte, 4);
+      if (k_codes) k_codes[r * g.D + c] = (wk >> pk.bit) & 3u;
+      if (v_codes) v_codes[r * g.D + c] = (wv >> pv.bit) & 3u;
+    }
+  if (k_min) memcpy(k_min, buf.data() + g.off_kmin(), 4 * g.D);
+  if (k_scale) memcpy(k_scale, buf.data() + g.off_kscale(), 4 * g.D);
+  if (v_min) memcpy(v_min, buf.data() + g.off_vmin(), 4 * g.W);
+  if (v_scale) memcpy(v_scale, buf.data() + g.off_vscale(), 4 * g.W);
+  return QE_OK;
+}
+
+qe_status qe_get_bf16_window(qe_handle h, int layer, int unit, int window, uint16_t* k, uint16_t* v) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if (unit < 0 || unit >= h->units || window < -1 || window >= h->st.maxw)
+    return fail(h, QE_ERR_INVALID_ARG, "unit or window out of range");
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  const long long gu = (long long)layer * h->units + unit;
+  int slot = 0;
+  if (window >= 0) {
+    uint8_t tier = 0;
+    QE_CK(h, cudaMemcpy(&tier, h->st.tier + gu * h->st.maxw + window, 1, cudaMemcpyDeviceToHost));
+    if (tier != QE_TIER_PINNED && tier != QE_TIER_FULL)
+      return fail(h, QE_ERR_STATE, "window %d is not in bf16 (tier %d)", window, tier);
+    if ((s = read_int(h, h->st.bslot + gu * h->st.maxw + window, &slot)) != QE_OK) return s;
+  }
+  if (slot < 0 || slot >= h->st.capb) return fail(h, QE_ERR_DEVICE, "bad bf16 slot %d", slot);
+  const qe::Geo g = h->st.geo;
+  std::vector<uint8_t> buf(g.bslot_bytes());
+  QE_CK(h, cudaMemcpy(buf.data(), h->st.bslab + (gu * h->st.capb + slot) * (long long)g.bslot_bytes(), buf.size(),
+                      cudaMemcpyDeviceToHost));
+  for (int r = 0; r < g.W; ++r)
+    for (int c = 0; c < g.D; ++c) {
+      if (k) memcpy(k + r * g.D + c, buf.data() + qe::bf16_k_off(g, r, c), 2);
+      if (v) memcpy(v + r * g.D + c, buf.data() + qe::bf16_v_off(g, r, c), 2);
+    }
+  return QE_OK;
+}
+
+qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out) {
+  if (!h || !out) return QE_ERR_INVALID_ARG;
+  if (layer < -1 || layer >= h->cfg.n_layers) return fail(h, QE_ERR_INVALID_ARG, "layer out of range");
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  std::vector<unsigned long long> v((size_t)h->cfg.n_layers * 5);
+  QE_CK(h, cudaMemcpy(v.data(), h->st.stats, v.size() * 8, cudaMemcpyDeviceToHost));
+  long long a[5] = {0, 0, 0, 0, 0};
+  for (int l = 0; l < h->cfg.n_layers; ++l)
+    if (layer == -1 || l == layer)
+      for (int i = 0; i < 5; ++i) a[i] += (long long)v[(size_t)l * 5 + i];
+  out->routes = a[0];
+  out->first_packs = a[1];
+  out->ledger_reuses = a[2];
+  out->promotions = a[3];
+  out->evictions = a[4];
+  return QE_OK;
+}
+
+qe_status qe_set_timing(qe_handle h, int enable) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  h->timing = enable != 0;
+  if (h->timing) {
+    h->ev_used = 0;
+    h->timed_bytes = 0;
+    h->timed_launches = 0;
+  }
+  return QE_OK;
+}
+
+qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, double* attn_bytes) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  double ms = 0;
+  for (size_t i = 0; i + 1 < h->ev_used; i += 2) {
+    float t = 0;
+    QE_CK(h, cudaEventElapsedTime(&t, h->ev_pool[i], h->ev_pool[i + 1]));
+    ms += t;
+  }
+  if (attn_ms) *attn_ms = ms;
+  if (launches) *launches = h->timed_launches;
+  if (attn_bytes) *attn_bytes = h->timed_bytes;
+  return QE_OK;
+}
+
+}  // extern "C"
