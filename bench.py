@@ -1,0 +1,390 @@
+"""Decode throughput of the tiered KV cache on the headline workload.
+
+One step = one decode token for the whole stack: for every layer, append the new K/V,
+run the attention with fused window scoring (qe_decode_attn + qe_attn_combine), and every
+Omega steps route all layers (segmented top-K, packing, moves).  Inputs are seeded synthetic
+tensors with the workload's shapes (qe_inputs), generated on the device before the timed
+region; the cache per layer (~280 MB) and per step (~8.9 GB) is far larger than L2.
+
+  python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference] [--workload NAME]
+
+Prints one JSON line (rank 0).  --impl reference times the CPU oracle (the only other
+implementation of this path) on the host cores, on a bounded sample of the same workload.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s and attn HBM GB/s vs peak; GQA 32q/8kv d128, 32K ctx"
+
+
+def _peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def _dist():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    return rank, world
+
+
+# ---------------------------------------------------------------------------- clocks
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "samples": len(sm), "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------------------- ncu traffic record
+def _traffic(workload: str):
+    """DRAM bytes per launch of qe_decode_attn from the committed ncu summary, if the kernel
+    source is unchanged since it was captured (else None)."""
+    path = os.path.join(ROOT, "profiles", f"qe_decode_attn_{workload}.json")
+    try:
+        with open(path) as f:
+            rec = json.load(f)
+        src = open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", "qe_attn.cu"), "rb").read()
+        if rec.get("qe_attn_sha256") != hashlib.sha256(src).hexdigest():
+            return None
+        return rec.get("dram_bytes_per_launch_full")
+    except Exception:
+        return None
+
+
+# ---------------------------------------------------------------------------- our implementation
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    import qe_inputs as gen
+    import qe_inputs.cuda as gcuda
+    import tiered_quantize_evict_gb300 as qe
+
+    rank, world = _dist()
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl")
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    wl = gen.WORKLOADS[args.workload]
+    if args.layers or args.batch:          # profiling cases only: smaller stack, same per-layer shapes
+        import dataclasses
+        wl = dataclasses.replace(wl, n_layers=args.layers or wl.n_layers, batch=args.batch or wl.batch)
+    B, Lyr, Hq, Hkv, D = wl.batch, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
+    omega = wl.route_period
+    K, W = args.steps, args.warmup
+    # decode steps: Omega pre-roll (all-bf16 cache, first routing event), W warm-up, K timed, K e2e
+    total_steps = omega + W + 2 * K
+    max_ctx = wl.prefill + max(wl.decode_steps, total_steps + omega)
+    stream = torch.cuda.current_stream(dev)
+    cache = qe.QECache(qe.config_from_workload(wl, max_context=max_ctx), stream.cuda_stream)
+    g = gcuda.DeviceGenerator(wl, device=dev)
+
+    # prefill, one layer at a time (2 x B x Hkv x L0 x d bf16 = 2 GB per layer)
+    kbuf = torch.empty(B, Hkv, wl.prefill, D, device=dev, dtype=torch.int16)
+    vbuf = torch.empty_like(kbuf)
+    for layer in range(Lyr):
+        g.keys_values(layer, 0, wl.prefill, kbuf, vbuf, stream.cuda_stream)
+        cache.qe_append(layer, kbuf, vbuf, wl.prefill)
+    cache.qe_synchronize()
+    del kbuf, vbuf
+    torch.cuda.empty_cache()
+
+    # per-step inputs, device resident
+    def make_inputs(t):
+        k = torch.empty(Lyr, B, Hkv, 1, D, device=dev, dtype=torch.int16)
+        v = torch.empty_like(k)
+        q = torch.empty(Lyr, B, Hq, D, device=dev, dtype=torch.int16)
+        for layer in range(Lyr):
+            g.keys_values(layer, wl.prefill + t - 1, 1, k[layer], v[layer], stream.cuda_stream)
+            g.queries(layer, t, q[layer], stream.cuda_stream)
+        return k, v, q
+
+    out = torch.empty(B, Hq, D, device=dev, dtype=torch.float32)
+
+    def step(t, k, v, q, o=out):
+        for layer in range(Lyr):
+            cache.qe_append(layer, k[layer], v[layer], 1)
+            cache.qe_decode_step(layer, q[layer], o)
+        if t % omega == 0:
+            cache.qe_route(-1)
+
+    t = 0
+    for _ in range(omega + W):          # pre-roll through the first routing event, then warm-up
+        t += 1
+        k, v, q = make_inputs(t)
+        step(t, k, v, q)
+    cache.qe_synchronize()
+    timed = [make_inputs(t + 1 + i) for i in range(K)]
+    torch.cuda.synchronize(dev)
+    launches0 = cache.kernel_launches()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize(dev)
+    cache.set_timing(True)
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for i in range(K):
+        t += 1
+        step(t, *timed[i])
+    e1.record(stream)
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    cache.set_timing(False)
+    clk = clocks.stop()
+    ms_total = e0.elapsed_time(e1)
+    attn_ms, attn_launches, attn_bytes = cache.timing()
+    launches = cache.kernel_launches() - launches0
+    cache.qe_synchronize()
+    del timed
+
+    # end to end through the C ABI with host buffers: pinned inputs copied in and the
+    # outputs read back every step, inside the timed region
+    host_in = []
+    for i in range(K):
+        k, v, q = make_inputs(t + 1 + i)
+        host_in.append((k.cpu().pin_memory(), v.cpu().pin_memory(), q.cpu().pin_memory()))
+    host_out = torch.empty(B, Hq, D, dtype=torch.float32).pin_memory()
+    h2d = sum(x.numel() * x.element_size() for x in host_in[0])
+    d2h = host_out.numel() * host_out.element_size() * Lyr
+    torch.cuda.synchronize(dev)
+    if world > 1:
+        dist.barrier()
+    t_e2e0 = time.perf_counter()
+    e2 = torch.cuda.Event(enable_timing=True)
+    e3 = torch.cuda.Event(enable_timing=True)
+    e2.record(stream)
+    for i in range(K):
+        t += 1
+        kh, vh, qh = host_in[i]
+        for layer in range(Lyr):
+            cache.qe_append(layer, kh[layer], vh[layer], 1)
+            cache.qe_decode_step(layer, qh[layer], host_out)
+        if t % omega == 0:
+            cache.qe_route(-1)
+    e3.record(stream)
+    torch.cuda.synchronize(dev)
+    e2e_ms = max(e2.elapsed_time(e3), (time.perf_counter() - t_e2e0) * 1e3)
+    cache.qe_synchronize()
+
+    # max over ranks
+    def allmax(x):
+        if world == 1:
+            return x
+        tt = torch.tensor([x], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        return float(tt.item())
+
+    ms_total = allmax(ms_total)
+    e2e_ms = allmax(e2e_ms)
+    value = world * B * K / (ms_total / 1e3)
+    e2e_val = world * B * K / (e2e_ms / 1e3)
+    peak, peak_kind = _peaks()
+    achieved = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
+    info = cache.layer_info(0)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
+        "warmup": W, "ms_per_step": round(ms_total / K, 4), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded qe_inputs generator, device-side)",
+        "config": {
+            "workload": wl.name, "batch": B, "context": wl.prefill, "layers": Lyr, "q_heads": Hq, "kv_heads": Hkv,
+            "head_dim": D, "window": wl.window, "route_period": omega, "bf16_token_share": wl.frac_bf16,
+            "int2_token_share": wl.frac_int2, "n_sink": wl.n_sink, "n_recent": wl.n_recent,
+            "timed_decode_steps": [omega + W + 1, omega + W + K], "parallelism": f"replicas{world}",
+            "kv_per_layer_unit": {"full": info.n_full, "quant": info.n_quant, "pinned": info.n_pinned},
+            "l2": "inputs larger than L2: %.0f MB read per layer launch, %.1f GB per step" % (
+                info.attn_bytes / 1e6, info.attn_bytes * Lyr / 1e9),
+            "kv_dtypes": "bf16 tiles + 2-bit codes (fp32 min/scale); fp32 accumulate",
+        },
+        "roofline": {
+            "bound": "hbm", "kernel": "qe_decode_attn", "achieved": round(achieved, 1) if achieved else None,
+            "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
+            "frac": round(achieved / peak, 4) if achieved else None,
+            "traffic": _traffic(wl.name),
+            "algorithmic_bytes_per_launch": round(attn_bytes / max(attn_launches, 1)),
+            "avg_launch_us": round(attn_ms * 1e3 / max(attn_launches, 1), 2),
+            "attn_share_of_step": round(attn_ms / ms_total, 4) if ms_total > 0 else None,
+        },
+        "e2e": {"value": round(e2e_val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h},
+        "gpu_launches": launches,
+        "clocks": clk,
+    }
+    cache.close()
+    if world > 1:
+        dist.destroy_process_group()
+    return line
+
+
+# ---------------------------------------------------------------------------- the oracle on host cores
+def _oracle_worker(a):
+    """Set one unit up to its steady state (untimed), then time `steps` decode steps."""
+    name, b, layer, kvh, n_steps, first_step = a
+    import numpy as np
+    import qe_inputs as gen
+    from oracle.run import make_unit, prefill, step_inputs
+    wl = gen.WORKLOADS[name]
+    unit = make_unit(wl, max_context=wl.prefill + first_step + n_steps + 1)
+    prefill(wl, unit, b, layer, kvh)
+    for t in range(1, first_step):
+        q, k, v = step_inputs(wl, b, layer, kvh, t)
+        unit.decode_step(q, k, v)
+        if t % wl.route_period == 0:
+            unit.route()
+    times = []
+    for t in range(first_step, first_step + n_steps):
+        q, k, v = step_inputs(wl, b, layer, kvh, t)
+        t0 = time.perf_counter()
+        unit.decode_step(q, k, v)
+        if t % wl.route_period == 0:
+            unit.route()
+        times.append(time.perf_counter() - t0)
+    return times
+
+
+def oracle_baseline(workload: str, n_units: int, n_steps: int):
+    """Tokens/s of the CPU oracle extrapolated from a bounded sample of units."""
+    import multiprocessing as mp
+
+    import qe_inputs as gen
+    wl = gen.WORKLOADS[workload]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+    os.environ.setdefault("OMP_NUM_THREADS", "1")
+    units_total = wl.batch * wl.n_layers * wl.n_kv_heads
+    first = wl.route_period + 1
+    jobs = []
+    for i in range(n_units):
+        u = (i * 2654435761) % units_total
+        b, rest = divmod(u, wl.n_layers * wl.n_kv_heads)
+        layer, kvh = divmod(rest, wl.n_kv_heads)
+        jobs.append((workload, b, layer, kvh, n_steps, first))
+    workers = min(cores, n_units)
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(workers) as pool:
+        res = pool.map(_oracle_worker, jobs)
+    per_unit_step = sum(sum(r) for r in res) / (n_units * n_steps)      # seconds, one core
+    step_s = per_unit_step * units_total / workers                       # all units, `workers` cores
+    return {"value": round(wl.batch / step_s, 4), "unit": "tokens/s", "cores": workers, "kind": "oracle",
+            "sample": f"{n_units} units x {n_steps} steady-state decode steps (after the first routing event) "
+                      f"of {workload}, extrapolated to all {units_total} units on {workers} cores; "
+                      f"setup (prefill, pre-roll, first route) untimed"}, step_s
+
+
+def run_reference(args):
+    rank, world = _dist()
+    if rank != 0:
+        return None
+    import qe_inputs as gen
+    wl = gen.WORKLOADS[args.workload]
+    cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
+    # each step: one decode step of `cores` sampled units (bounded sample of the workload)
+    n_units = max(1, min(cores, 16))
+    steps = args.warmup + args.steps
+    t0 = time.perf_counter()
+    base, step_s = oracle_baseline(args.workload, n_units, steps)
+    wall = time.perf_counter() - t0
+    v = base["value"]
+    base["sample"] = base["sample"].replace("steady-state", f"steady-state ({args.warmup} warm-up + {args.steps} timed)")
+    return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic (seeded qe_inputs generator)",
+            "config": {"workload": wl.name, "batch": wl.batch, "context": wl.prefill, "layers": wl.n_layers},
+            "cpu_baseline": base,
+            "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=4)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--workload", default="throughput_32k")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer layers than the workload")
+    ap.add_argument("--batch", type=int, default=0, help="profiling only: other batch than the workload")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world = _dist()
+    if args.impl == "reference":
+        line = run_reference(args)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+    line = run_ours(args)
+    if rank == 0:
+        if world == 1 and not args.no_cpu_baseline:
+            base, _ = oracle_baseline(args.workload, n_units=min(16, len(os.sched_getaffinity(0))), n_steps=2)
+            line["cpu_baseline"] = base
+        print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

@@ -16,11 +16,16 @@
 //    is busy until the last tile regardless of how units and tiles divide.
 //  * The G query heads of a KV head share every K/V element: the Q K^T and P V products are
 //    small dense contractions ([16 tokens x d] x [d x 8]) run on the tensor cores with
-//    mma.m16n8k16 (bf16 in, fp32 accumulate).  The 8 columns hold the G heads twice, as a
-//    bf16 "hi" part and a bf16 "lo" remainder of the fp32 operand (q * s_K for 2-bit keys,
-//    p or p * s_V for the values), so the products keep ~16 bits of operand precision.
+//    mma.m16n8k16 (fp32 accumulate).  Column 2h carries head h's operand truncated to the
+//    input precision ("hi"), column 2h+1 the exact remainder ("lo"), so the products keep
+//    ~16 (bf16 tiles) or ~22 (2-bit tiles, f16) bits of operand precision; each lane then owns
+//    one head (its accumulator pair is that head's hi and lo), so the softmax needs no
+//    cross-lane merging and no lane duplicates another's work.
 //  * 2-bit codes are unpacked in registers straight into mma fragments (the slots are stored
-//    in fragment order), never materialised as bf16 in memory.
+//    in fragment order): a code is the low half of an FP4 (e2m1) nibble, value code / 2, and
+//    one cvt.f16x2.e2m1x2 turns two codes into an f16 pair; the factor 2 is folded into the
+//    B operand (2 q s_K for keys, 2 p s_V for values).  Dequantized values never exist in
+//    memory.
 //  * Per-window mass leaves the kernel as a log-sum-exp per (tile, head); the combine kernel
 //    turns it into a probability mass once the unit's global softmax normaliser is known.
 #include <cstdint>
@@ -40,7 +45,7 @@ struct TileDesc {
   int slot, win;   // slot in its pool, window id (-1 for the sink)
   int lo, hi;      // valid rows inside the tile
   int kind;        // 0 bf16 sub-tile, 1 2-bit window
-  int pad;
+  int sub;         // bf16 sub-tile index inside its window slot
 };
 
 __device__ __forceinline__ long long tile_start(const AttnParams& p, int u, int i, int nbt) {
@@ -65,20 +70,34 @@ __device__ __forceinline__ void first_tile(const AttnParams& p, long long x, int
   }
 }
 
-// fill the descriptor of (u, i); returns false if the tile has no valid row
-__device__ __forceinline__ bool describe(const AttnParams& p, int u, int i, int nbt, TileDesc& d) {
+__device__ __forceinline__ void next_tile(const AttnParams& p, int& u, int& i) {
+  i += 1;
+  if (i >= p.ntiles) {
+    i = 0;
+    u += 1;
+  }
+}
+
+// list entry {window, slot} of tile (u, i)
+__device__ __forceinline__ int2 list_entry(const AttnParams& p, int u, int i, int nbt, int sub_tiles) {
+  const State& st = p.st;
+  const long long gu = (long long)p.layer * st.units + u;
+  if (i < nbt) return st.blist[gu * st.capb + i / sub_tiles];
+  return st.qlist[gu * st.capq + (i - nbt)];
+}
+
+// descriptor of tile (u, i) from its list entry; false if it has no valid row (or is corrupt)
+__device__ __forceinline__ bool describe(const AttnParams& p, int u, int i, int nbt, int2 ent, TileDesc& d) {
   const State& st = p.st;
   const int W = st.geo.W;
   const int sub_tiles = W / 16;
-  const long long gu = (long long)p.layer * st.units + u;
   d.u = u;
   d.i = i;
+  d.win = ent.x;
+  d.slot = ent.y;
   if (i < nbt) {
-    int e = i / sub_tiles, sub = i - e * sub_tiles;
-    int2 ent = st.blist[gu * st.capb + e];
-    d.win = ent.x;
-    d.slot = ent.y;
     d.kind = 0;
+    d.sub = i % sub_tiles;
     if (ent.y < 0 || ent.y >= st.capb || ent.x < -1 || ent.x >= st.maxw) {   // corrupt entry: skip, flag
       atomicOr(st.err, ERR_TABLE);
       return false;
@@ -89,27 +108,23 @@ __device__ __forceinline__ bool describe(const AttnParams& p, int u, int i, int 
       hi = st.n_sink;
     } else {
       lo = (ent.x == 0) ? st.n_sink : 0;
-      int h = p.L - ent.x * W;
+      const int h = p.L - ent.x * W;
       hi = h < W ? h : W;
     }
-    int base = sub * 16;
-    int tl = lo - base, th = hi - base;
+    const int base = d.sub * 16;
+    const int tl = lo - base, th = hi - base;
     d.lo = tl < 0 ? 0 : tl;
     d.hi = th > 16 ? 16 : th;
-    d.pad = sub;
     return d.hi > d.lo;
   }
-  int2 ent = st.qlist[gu * st.capq + (i - nbt)];
-  d.win = ent.x;
-  d.slot = ent.y;
   d.kind = 1;
+  d.sub = 0;
   if (ent.y < 0 || ent.y >= st.capq || ent.x < 0 || ent.x >= st.maxw) {
     atomicOr(st.err, ERR_TABLE);
     return false;
   }
   d.lo = (ent.x == 0) ? st.n_sink : 0;
   d.hi = W;
-  d.pad = 0;
   return true;
 }
 
@@ -118,19 +133,10 @@ __device__ __forceinline__ const uint8_t* tile_src(const AttnParams& p, const Ti
   const long long gu = (long long)p.layer * st.units + d.u;
   if (d.kind == 0) {
     bytes = st.geo.sub_bytes();
-    return st.bslab + ((gu * st.capb + d.slot) * (long long)st.geo.bslot_bytes()) + (long long)d.pad * st.geo.sub_bytes();
+    return st.bslab + ((gu * st.capb + d.slot) * (long long)st.geo.bslot_bytes()) + (long long)d.sub * st.geo.sub_bytes();
   }
   bytes = st.geo.qslot_bytes();
   return st.qslab + (gu * st.capq + d.slot) * (long long)st.geo.qslot_bytes();
-}
-
-// Advance (u, i) to the next tile in sequence order.
-__device__ __forceinline__ void next_tile(const AttnParams& p, int& u, int& i) {
-  i += 1;
-  if (i >= p.ntiles) {
-    i = 0;
-    u += 1;
-  }
 }
 
 template <int D, int W>
@@ -172,104 +178,110 @@ __device__ __forceinline__ void load_words(const uint8_t* blk, int lane, unsigne
   }
 }
 
-// Online-softmax step over one tile of MT m-tiles whose Q K^T accumulators are in acc.
-// Produces the P^T B-fragments (hi/lo split) for the P V product, updates (m, l, zsum, O).
-template <int MT, int MC, bool INT2>
-__device__ __forceinline__ void softmax_tile(float (&acc)[MT][4], int lo, int hi, const float (&bias)[2],
-                                             const float* vmin, const float* vscale, float scale_log2,
-                                             float (&m)[2], float (&l)[2], float (&zs)[2], float (&O)[MC][4],
-                                             unsigned (&Bp)[MT][2], float* lse_out, int G, int lane) {
+// N floats starting at p (16-byte vectors where possible)
+template <int N>
+__device__ __forceinline__ void load_floats(const float* p, float (&v)[N]) {
+  if constexpr (N % 4 == 0) {
+#pragma unroll
+    for (int i = 0; i < N / 4; ++i) {
+      const float4 f = reinterpret_cast<const float4*>(p)[i];
+      v[4 * i] = f.x; v[4 * i + 1] = f.y; v[4 * i + 2] = f.z; v[4 * i + 3] = f.w;
+    }
+  } else {
+    const float2 f = *reinterpret_cast<const float2*>(p);
+    v[0] = f.x; v[1] = f.y;
+  }
+}
+
+// Running softmax state of one warp for the unit it is working on.  Column n of every
+// mma fragment is head n/2, "hi" part (n even) or "lo" remainder (n odd), so lane (g, t) owns
+// head t: its accumulator pair (2t, 2t+1) holds that head's hi and lo parts for rows g, g+8.
+// Scores are kept in the log2 domain against a reference maximum mref that is only raised when
+// a tile's maximum exceeds it by more than 8 (so p <= 2^8): most tiles skip the rescale.
+template <int MC>
+struct RunState {
+  float mref;      // head t
+  float l;
+  float zs;        // sum of p * z_V over 2-bit tokens (value offsets), partial over this lane's rows
+  float O[MC][4];  // O^T fragments: rows = channels, columns 2t (hi) and 2t+1 (lo) of head t
+};
+
+// acc[mt][f][.] are split accumulators of the Q K^T products of token tile mt (summed here).
+template <int MT, int NF, int MC, bool INT2>
+__device__ __forceinline__ void softmax_tile(float (&acc)[MT][NF][4], bool full, int lo, int hi, float bias,
+                                             const float (&vz)[2 * MT], const float (&vs)[2 * MT], float scale_log2,
+                                             RunState<MC>& st, unsigned (&Bp)[MT][2], float* lse_out, int G, int lane) {
   const int g = lane >> 2, t = lane & 3;
-  float x[MT][4];
+  float x[MT][2];   // rows g and g + 8 of each token tile
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      float v = acc[mt][r] + __shfl_xor_sync(0xffffffffu, acc[mt][r], 2);
-      int row = mt * 16 + g + ((r & 2) ? 8 : 0);
-      v = (v + bias[r & 1]) * scale_log2;
-      x[mt][r] = (row >= lo && row < hi) ? v : -INFINITY;
+    for (int j = 0; j < 2; ++j) {
+      float v = 0.f;
+#pragma unroll
+      for (int f = 0; f < NF; ++f) v += acc[mt][f][2 * j] + acc[mt][f][2 * j + 1];
+      x[mt][j] = (v + bias) * scale_log2;
     }
-  float mx[2] = {-INFINITY, -INFINITY};
+  if (!full) {
 #pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
+    for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) mx[r & 1] = fmaxf(mx[r & 1], x[mt][r]);
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 4));
-    mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 8));
-    mx[e] = fmaxf(mx[e], __shfl_xor_sync(0xffffffffu, mx[e], 16));
-  }
-  float mnew[2], muse[2], alpha[2];
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    mnew[e] = fmaxf(m[e], mx[e]);
-    muse[e] = (mnew[e] == -INFINITY) ? 0.f : mnew[e];
-    alpha[e] = ex2(m[e] - muse[e]);
-  }
-  float pr[MT][4];
-  float mass[2] = {0.f, 0.f};
-  float zadd[2] = {0.f, 0.f};
-#pragma unroll
-  for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      float pv = ex2(x[mt][r] - muse[r & 1]);
-      pr[mt][r] = pv;
-      mass[r & 1] += pv;
-      if constexpr (INT2) {
-        int row = mt * 16 + g + ((r & 2) ? 8 : 0);
-        zadd[r & 1] = fmaf(pv, vmin[row], zadd[r & 1]);
+      for (int j = 0; j < 2; ++j) {
+        const int row = mt * 16 + g + 8 * j;
+        if (row < lo || row >= hi) x[mt][j] = -INFINITY;
       }
-    }
-#pragma unroll
-  for (int e = 0; e < 2; ++e) {
-    mass[e] += __shfl_xor_sync(0xffffffffu, mass[e], 4);
-    mass[e] += __shfl_xor_sync(0xffffffffu, mass[e], 8);
-    mass[e] += __shfl_xor_sync(0xffffffffu, mass[e], 16);
-    l[e] = fmaf(l[e], alpha[e], mass[e]);
-    zs[e] = fmaf(zs[e], alpha[e], zadd[e]);
-    m[e] = mnew[e];
   }
-  // per-tile log2-sum-exp of each head (heads 2t, 2t+1 written by lanes 0 and 1)
-  if (lse_out != nullptr && g == 0 && t < 2) {
+  float mx = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      int h = 2 * t + e;
-      if (h < G) lse_out[h] = mass[e] > 0.f ? muse[e] + lg2(mass[e]) : -INFINITY;
-    }
+  for (int mt = 0; mt < MT; ++mt) mx = fmaxf(mx, fmaxf(x[mt][0], x[mt][1]));
+  // only a lane that may exceed 2^8 needs the exact maximum of its head
+  if (__any_sync(0xffffffffu, mx > st.mref + 8.f)) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(st.mref, mx);
+    const float alpha = (st.mref == -INFINITY) ? 0.f : ex2(st.mref - mn);
+    st.mref = mn;
+    st.l *= alpha;
+    st.zs *= alpha;
+#pragma unroll
+    for (int mc = 0; mc < MC; ++mc)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) st.O[mc][r] *= alpha;
   }
+  const float muse = st.mref == -INFINITY ? 0.f : st.mref;
+  float pr[MT][2];
+  float mass = 0.f, zadd = 0.f;
 #pragma unroll
-  for (int mc = 0; mc < MC; ++mc)
+  for (int mt = 0; mt < MT; ++mt)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) O[mc][r] *= alpha[r & 1];
-  // P^T fragments: columns 0..3 carry the bf16 "hi" part of each head, 4..7 the remainder
-  const bool lo_lane = t >= 2;
+    for (int j = 0; j < 2; ++j) {
+      const float pv = ex2(x[mt][j] - muse);
+      pr[mt][j] = pv;
+      mass += pv;
+      if constexpr (INT2) zadd = fmaf(pv, vz[mt * 2 + j], zadd);
+    }
+  if constexpr (INT2) st.zs += zadd;
+  mass += __shfl_xor_sync(0xffffffffu, mass, 4);
+  mass += __shfl_xor_sync(0xffffffffu, mass, 8);
+  mass += __shfl_xor_sync(0xffffffffu, mass, 16);
+  st.l += mass;
+  if (g == 0 && t < G) lse_out[t] = mass > 0.f ? muse + lg2(mass) : -INFINITY;
+  // P^T fragments in D layout: (row g: hi, lo of head t), (row g+8: ...), then transposed
+  constexpr unsigned KEEP = INT2 ? 0xFFFFE000u : 0xFFFF0000u;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
-    float y[4];
+    unsigned rr[2];
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      float v = pr[mt][r];
-      if constexpr (INT2) {
-        int row = mt * 16 + g + ((r & 2) ? 8 : 0);
-        v *= vscale[row];
-      }
-      y[r] = v;
+    for (int j = 0; j < 2; ++j) {
+      float y = pr[mt][j];
+      if constexpr (INT2) y *= vs[mt * 2 + j];
+      const float yh = __uint_as_float(__float_as_uint(y) & KEEP);
+      if constexpr (INT2) rr[j] = pack_f16x2_rz(yh, y - yh);
+      else rr[j] = pack_bf16x2_rz(yh, y - yh);
     }
-    unsigned top, bot;
-    {
-      unsigned y0 = __float_as_uint(y[0]), y1 = __float_as_uint(y[1]);
-      unsigned y2 = __float_as_uint(y[2]), y3 = __float_as_uint(y[3]);
-      unsigned h01 = __byte_perm(y0, y1, 0x7632), h23 = __byte_perm(y2, y3, 0x7632);
-      unsigned l01 = pack_bf16x2(y[0] - __uint_as_float(y0 & 0xFFFF0000u), y[1] - __uint_as_float(y1 & 0xFFFF0000u));
-      unsigned l23 = pack_bf16x2(y[2] - __uint_as_float(y2 & 0xFFFF0000u), y[3] - __uint_as_float(y3 & 0xFFFF0000u));
-      top = lo_lane ? l01 : h01;
-      bot = lo_lane ? l23 : h23;
-    }
-    Bp[mt][0] = movmatrix_t(top);
-    Bp[mt][1] = movmatrix_t(bot);
+    Bp[mt][0] = movmatrix_t(rr[0]);
+    Bp[mt][1] = movmatrix_t(rr[1]);
   }
 }
 
@@ -277,6 +289,7 @@ template <int D, int W>
 __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(const AttnParams p) {
   using S = Shape<D, W>;
   constexpr int KS = S::KS, MC = S::MC, MT = S::MT, KT = S::KT, WPL = S::WPL, CW = S::CW, NST = S::NST;
+  constexpr int SUBT = W / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) unsigned long long bars[ATTN_WARPS][NST];
   __shared__ TileDesc descs[ATTN_WARPS][NST];
@@ -288,7 +301,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   const long long x_lo = (wg * p.C + p.NW - 1) / p.NW;
   const long long x_hi = ((wg + 1) * p.C + p.NW - 1) / p.NW;
   if (x_lo >= x_hi) return;
-  const int nbt = p.nbw * (W / 16);
+  const int nbt = p.nbw * SUBT;
   const int u_first = (int)(x_lo / p.Cu);
   const int u_last = (int)((x_hi - 1) / p.Cu);
 
@@ -299,87 +312,72 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   }
   __syncwarp();
 
-  // producer cursor
+  // ---- producer: cursor (pu, pi) with its list entry prefetched one tile ahead
   int pu, pi;
   first_tile(p, x_lo, nbt, pu, pi);
-  int issued = 0;
-  auto issue_next = [&](int slot_stage) -> bool {
-    // advance the producer cursor to the next non-empty tile inside the range
+  const bool pvalid0 = pu < p.st.units && tile_start(p, pu, pi, nbt) < x_hi;
+  int2 pent = pvalid0 ? list_entry(p, pu, pi, nbt, SUBT) : make_int2(0, 0);
+  auto issue_next = [&](int stage) -> bool {
     while (pu < p.st.units && tile_start(p, pu, pi, nbt) < x_hi) {
       TileDesc d;
-      bool ok = describe(p, pu, pi, nbt, d);
+      const bool ok = describe(p, pu, pi, nbt, pent, d);
       next_tile(p, pu, pi);
+      if (pu < p.st.units && tile_start(p, pu, pi, nbt) < x_hi) pent = list_entry(p, pu, pi, nbt, SUBT);
       if (!ok) continue;
       if (lane == 0) {
-        descs[warp][slot_stage] = d;
+        descs[warp][stage] = d;
         unsigned bytes;
         const uint8_t* src = tile_src(p, d, bytes);
-        unsigned bar = smem_u32(&bars[warp][slot_stage]);
+        const unsigned bar = smem_u32(&bars[warp][stage]);
         mbar_expect_tx(bar, bytes);
-        bulk_g2s(smem_u32(stage_base + (size_t)slot_stage * S::STAGE), src, bytes, bar);
+        bulk_g2s(smem_u32(stage_base + (size_t)stage * S::STAGE), src, bytes, bar);
       }
       return true;
     }
     return false;
   };
-  int n_inflight = 0;
+  int issued = 0;
   for (int s = 0; s < NST; ++s) {
     if (!issue_next(s)) break;
-    ++n_inflight;
     ++issued;
   }
   __syncwarp();
 
-  // consumer state of the current unit
-  float m[2], l[2], zs[2];
-  float O[MC][4];
-  unsigned qv[KS][2];      // this lane's head (g & 3) query values, bf16 pairs
-  unsigned qb[KS][2];      // B fragments for bf16 tiles (zero in lo columns)
+  // ---- consumer
+  RunState<MC> rs;
+  float qf[KS][4];         // 2 q of head g/2 at channels 16ks + 2t, +1, +8, +9 (2-bit tiles)
+  unsigned qb[KS][2];      // bf16 B fragments: q of head g/2 in even columns, 0 in odd ones
   int cur_u = u_first;
   int q_unit = -1;
   auto reset = [&]() {
-    m[0] = m[1] = -INFINITY;
-    l[0] = l[1] = 0.f;
-    zs[0] = zs[1] = 0.f;
+    rs.mref = -INFINITY;
+    rs.l = 0.f;
+    rs.zs = 0.f;
 #pragma unroll
     for (int mc = 0; mc < MC; ++mc)
 #pragma unroll
-      for (int r = 0; r < 4; ++r) O[mc][r] = 0.f;
+      for (int r = 0; r < 4; ++r) rs.O[mc][r] = 0.f;
   };
   auto flush = [&](int u) {
     const long long pidx = (long long)wg * p.maxseg + (u - u_first);
-    // O^T[c][n]: add the lo column (n + 4) to the hi column n; add the value-bias term
-    float zt[2];
+    float z = rs.zs;
+    z += __shfl_xor_sync(0xffffffffu, z, 4);
+    z += __shfl_xor_sync(0xffffffffu, z, 8);
+    z += __shfl_xor_sync(0xffffffffu, z, 16);
+    if (t < G) {
+      float* po = p.part_o + (pidx * G + t) * D;
 #pragma unroll
-    for (int e = 0; e < 2; ++e) {
-      float z = zs[e];
-      z += __shfl_xor_sync(0xffffffffu, z, 4);
-      z += __shfl_xor_sync(0xffffffffu, z, 8);
-      z += __shfl_xor_sync(0xffffffffu, z, 16);
-      zt[e] = z;   // lanes t < 2 hold the sum over all rows for heads 2t, 2t+1
-    }
-#pragma unroll
-    for (int mc = 0; mc < MC; ++mc)
-#pragma unroll
-      for (int r = 0; r < 4; ++r) {
-        float v = O[mc][r] + __shfl_xor_sync(0xffffffffu, O[mc][r], 2);
-        int h = 2 * t + (r & 1);
-        int c = mc * 16 + g + ((r & 2) ? 8 : 0);
-        if (t < 2 && h < G) p.part_o[(pidx * G + h) * D + c] = v + zt[r & 1];
+      for (int mc = 0; mc < MC; ++mc) {
+        po[mc * 16 + g] = rs.O[mc][0] + rs.O[mc][1] + z;
+        po[mc * 16 + g + 8] = rs.O[mc][2] + rs.O[mc][3] + z;
       }
-    if (g == 0 && t < 2) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        int h = 2 * t + e;
-        if (h < G) p.part_ml[pidx * G + h] = make_float2(m[e], l[e]);
-      }
+      if (g == 0) p.part_ml[pidx * G + t] = make_float2(rs.mref, rs.l);
     }
   };
   reset();
 
-  const int hh = g & 3;
-  const bool lo_lane_b = g >= 4;
-  // bounded wait for the bulk copy of the k-th tile (false: gave up after WAIT_LIMIT_NS)
+  const int hh = g >> 1;               // head of the B columns this lane supplies
+  const bool lo_col = (g & 1) != 0;    // ... and whether it is the remainder column
   auto wait_tile = [&](int k) -> bool {
     const unsigned bar = smem_u32(&bars[warp][k % NST]);
     const unsigned parity = (k / NST) & 1;
@@ -415,88 +413,84 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       const bool act = hh < G;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
-        unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
-        qv[ks][0] = a0;
-        qv[ks][1] = a1;
-        qb[ks][0] = lo_lane_b ? 0u : a0;
-        qb[ks][1] = lo_lane_b ? 0u : a1;
+        const unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
+        const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
+        qf[ks][0] = 2.f * bf16lo_to_f32(a0);
+        qf[ks][1] = 2.f * bf16hi_to_f32(a0);
+        qf[ks][2] = 2.f * bf16lo_to_f32(a1);
+        qf[ks][3] = 2.f * bf16hi_to_f32(a1);
+        qb[ks][0] = lo_col ? 0u : a0;
+        qb[ks][1] = lo_col ? 0u : a1;
       }
     }
     float* lse_out = p.lse + ((size_t)d.u * p.ntiles + d.i) * G;
     if (d.kind == 0) {
-      // ---- bf16 sub-tile: 16 tokens
-      float acc[1][4] = {{0.f, 0.f, 0.f, 0.f}};
+      // ---- bf16 sub-tile: 16 tokens; two accumulators halve the mma dependency chain
+      float acc[1][2][4] = {};
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        uint4 a = lds128(sp + ks * 512 + lane * 16);
-        mma_bf16(acc[0], a.x, a.y, a.z, a.w, qb[ks][0], qb[ks][1]);
+        const uint4 a = lds128(sp + ks * 512 + lane * 16);
+        mma_bf16(acc[0][ks & 1], a.x, a.y, a.z, a.w, qb[ks][0], qb[ks][1]);
       }
-      const float bias[2] = {0.f, 0.f};
+      const float vnone[2] = {0.f, 0.f};
       unsigned Bp[1][2];
-      softmax_tile<1, MC, false>(acc, d.lo, d.hi, bias, nullptr, nullptr, p.scale_log2, m, l, zs, O, Bp, lse_out, G,
-                                 lane);
+      softmax_tile<1, 2, MC, false>(acc, d.lo == 0 && d.hi == 16, d.lo, d.hi, 0.f, vnone, vnone, p.scale_log2, rs,
+                                    Bp, lse_out, G, lane);
 #pragma unroll
       for (int mc = 0; mc < MC; ++mc) {
-        uint4 a = lds128(sp + 32 * D + mc * 512 + lane * 16);
-        mma_bf16(O[mc], a.x, a.y, a.z, a.w, Bp[0][0], Bp[0][1]);
+        const uint4 a = lds128(sp + 32 * D + mc * 512 + lane * 16);
+        mma_bf16(rs.O[mc], a.x, a.y, a.z, a.w, Bp[0][0], Bp[0][1]);
       }
     } else {
       // ---- 2-bit window: W tokens
       const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
       const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
-      const float* vmin = reinterpret_cast<const float*>(sp + S::OFF_VMIN);
-      const float* vscale = reinterpret_cast<const float*>(sp + S::OFF_VSCALE);
-      // B fragments q' = q * s_K (hi part in lanes g < 4, remainder in lanes g >= 4), bias q . z_K
+      // B fragments 2 q s_K in f16: trunc part in even columns, remainder in odd ones; bias q . z_K
       unsigned qp[KS][2];
       float bpart = 0.f;
+      const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
+        const float4 sc = *reinterpret_cast<const float4*>(kscale + ks * 16 + t * 4);
+        const float4 zc = *reinterpret_cast<const float4*>(kmin + ks * 16 + t * 4);
+        bpart = fmaf(qf[ks][0], zc.x, bpart);
+        bpart = fmaf(qf[ks][1], zc.y, bpart);
+        bpart = fmaf(qf[ks][2], zc.z, bpart);
+        bpart = fmaf(qf[ks][3], zc.w, bpart);
+        float y[4] = {qf[ks][0] * sc.x, qf[ks][1] * sc.y, qf[ks][2] * sc.z, qf[ks][3] * sc.w};
 #pragma unroll
-        for (int hf = 0; hf < 2; ++hf) {
-          const int c = ks * 16 + hf * 8 + 2 * t;
-          const float2 sc = *reinterpret_cast<const float2*>(kscale + c);
-          const float2 zc = *reinterpret_cast<const float2*>(kmin + c);
-          const float q0 = bf16lo_to_f32(qv[ks][hf]), q1 = bf16hi_to_f32(qv[ks][hf]);
-          bpart = fmaf(q0, zc.x, bpart);
-          bpart = fmaf(q1, zc.y, bpart);
-          const float y0 = q0 * sc.x, y1 = q1 * sc.y;
-          const unsigned u0 = __float_as_uint(y0), u1 = __float_as_uint(y1);
-          const unsigned hi2 = __byte_perm(u0, u1, 0x7632);
-          const unsigned lo2 = pack_bf16x2(y0 - __uint_as_float(u0 & 0xFFFF0000u), y1 - __uint_as_float(u1 & 0xFFFF0000u));
-          qp[ks][hf] = lo_lane_b ? lo2 : hi2;
-        }
+        for (int i = 0; i < 4; ++i) y[i] -= __uint_as_float(__float_as_uint(y[i]) & keep);
+        qp[ks][0] = pack_f16x2_rz(y[0], y[1]);
+        qp[ks][1] = pack_f16x2_rz(y[2], y[3]);
       }
       bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
       bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-      float bias[2];
-      bias[0] = __shfl_sync(0xffffffffu, bpart, (2 * (t & 1)) * 4);
-      bias[1] = __shfl_sync(0xffffffffu, bpart, (2 * (t & 1) + 1) * 4);
-      // Q K^T over the unpacked key codes
-      float acc[MT][4];
+      const float bias = 0.5f * __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . z_K of head t
+      float vz[2 * MT], vs[2 * MT];
+      load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
+      load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
 #pragma unroll
-      for (int mt = 0; mt < MT; ++mt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) acc[mt][r] = 0.f;
+      for (int i = 0; i < 2 * MT; ++i) vs[i] *= 2.f;   // codes arrive as code / 2
+      // Q K^T over the unpacked key codes; fragment parity splits the accumulators
+      float acc[MT][2][4] = {};
       {
         unsigned wk[WPL];
         load_words<WPL, CW>(sp, lane, wk);
 #pragma unroll
         for (int wi = 0; wi < WPL; ++wi) {
           unsigned a[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) a[j] = codes_to_bf16x2(wk[wi] >> (2 * j));
+          unpack_word(wk[wi], a);
 #pragma unroll
           for (int f = 0; f < 2; ++f) {
             const int F = 2 * wi + f;
             const int mt = F / KS, ks = F % KS;
-            mma_bf16(acc[mt], a[4 * f + 0], a[4 * f + 1], a[4 * f + 2], a[4 * f + 3], qp[ks][0], qp[ks][1]);
+            mma_f16(acc[mt][f], a[4 * f + 0], a[4 * f + 1], a[4 * f + 2], a[4 * f + 3], qp[ks][0], qp[ks][1]);
           }
         }
       }
       unsigned Bp[MT][2];
-      softmax_tile<MT, MC, true>(acc, d.lo, d.hi, bias, vmin, vscale, p.scale_log2, m, l, zs, O, Bp, lse_out, G,
-                                 lane);
+      softmax_tile<MT, 2, MC, true>(acc, d.lo == 0, d.lo, d.hi, bias, vz, vs, p.scale_log2, rs, Bp, lse_out, G,
+                                    lane);
       // P V over the unpacked value codes (A = V^T: channel tiles x token steps)
       {
         unsigned wv[WPL];
@@ -504,20 +498,18 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
 #pragma unroll
         for (int wi = 0; wi < WPL; ++wi) {
           unsigned a[8];
-#pragma unroll
-          for (int j = 0; j < 8; ++j) a[j] = codes_to_bf16x2(wv[wi] >> (2 * j));
+          unpack_word(wv[wi], a);
 #pragma unroll
           for (int f = 0; f < 2; ++f) {
             const int F = 2 * wi + f;
             const int mc = F / KT, kt = F % KT;
-            mma_bf16(O[mc], a[4 * f + 0], a[4 * f + 1], a[4 * f + 2], a[4 * f + 3], Bp[kt][0], Bp[kt][1]);
+            mma_f16(rs.O[mc], a[4 * f + 0], a[4 * f + 1], a[4 * f + 2], a[4 * f + 3], Bp[kt][0], Bp[kt][1]);
           }
         }
       }
     }
     __syncwarp();
-    // refill this stage
-    if (issue_next(s)) ++issued;
+    if (issue_next(s)) ++issued;   // refill this stage
     __syncwarp();
   }
   if (timed_out) {
@@ -537,77 +529,102 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
 // One CTA per unit: merge the partials of every warp whose range meets the unit, write
 // o = sum / l, then turn each tile's log2-sum-exp into mass, sum it over the G heads and
 // add it to the window's float32 score (eq. (1) with the GQA group sum).
+constexpr int COMBINE_THREADS = 256;
+constexpr int MAXP = 256;
+
 template <int D>
-__global__ void __launch_bounds__(128) qe_attn_combine_kernel(const CombineParams p) {
+__global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const CombineParams p) {
   const int u = blockIdx.x;
   const int G = p.st.G;
   const long long gu = (long long)p.layer * p.st.units + u;
-  constexpr int MAXP = 256;
-  __shared__ float s_M[4], s_scale[4 * MAXP], s_lse[4];
-  __shared__ int s_np;
   __shared__ long long s_pidx[MAXP];
-  // partial producers: warps whose position range meets [u Cu, (u+1) Cu)
-  if (threadIdx.x == 0) {
-    long long a = (long long)u * p.Cu, b = a + p.Cu - 1;
-    long long w0 = a * p.NW / p.C, w1 = b * p.NW / p.C;
-    int np = 0;
-    for (long long w = w0; w <= w1 && np < MAXP; ++w) {
-      long long xl = (w * p.C + p.NW - 1) / p.NW, xh = ((w + 1) * p.C + p.NW - 1) / p.NW;
-      if (xl >= xh) continue;
-      s_pidx[np++] = w * p.maxseg + (u - (int)(xl / p.Cu));
-    }
-    if (w1 - w0 + 1 > MAXP) atomicOr(p.st.err, ERR_COUNT);
-    s_np = np;
+  __shared__ float2 s_ml[MAXP * 4];
+  __shared__ float s_sc[4 * MAXP];
+  __shared__ float s_inv[4], s_lse[4];
+  __shared__ int s_wcount[COMBINE_THREADS / 32];
+  __shared__ int s_np;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  // 1. partial producers: warps whose position range meets [u Cu, (u+1) Cu), in order
+  const long long a = (long long)u * p.Cu, b = a + p.Cu - 1;
+  const long long w0 = a * p.NW / p.C, w1 = b * p.NW / p.C;
+  if (tid == 0 && w1 - w0 + 1 > MAXP) atomicOr(p.st.err, ERR_COUNT);
+  const long long w = w0 + tid;
+  bool valid = false;
+  long long pidx = 0;
+  if (tid < MAXP && w <= w1) {
+    const long long xl = (w * p.C + p.NW - 1) / p.NW, xh = ((w + 1) * p.C + p.NW - 1) / p.NW;
+    valid = xl < xh;
+    pidx = w * p.maxseg + (u - (int)(xl / p.Cu));
+  }
+  const unsigned bal = __ballot_sync(0xffffffffu, valid);
+  if (lane == 0) s_wcount[warp] = __popc(bal);
+  __syncthreads();
+  int base = 0;
+  for (int i = 0; i < warp; ++i) base += s_wcount[i];
+  if (valid) s_pidx[base + __popc(bal & ((1u << lane) - 1))] = pidx;
+  if (tid == 0) {
+    int n = 0;
+    for (int i = 0; i < COMBINE_THREADS / 32; ++i) n += s_wcount[i];
+    s_np = n;
   }
   __syncthreads();
   const int np = s_np;
-  if (threadIdx.x < G) {
-    const int h = threadIdx.x;
+  // 2. (max, sum) of every partial and head
+  for (int i = tid; i < np * G; i += COMBINE_THREADS) s_ml[i] = p.part_ml[s_pidx[i / G] * G + (i % G)];
+  __syncthreads();
+  // 3. per head: global max, scale of each partial, normaliser (one warp per head)
+  if (warp < G) {
+    const int h = warp;
     float M = -INFINITY;
-    for (int k = 0; k < np; ++k) M = fmaxf(M, p.part_ml[s_pidx[k] * G + h].x);
-    float Mu = (M == -INFINITY) ? 0.f : M;
+    for (int k2 = lane; k2 < np; k2 += 32) M = fmaxf(M, s_ml[k2 * G + h].x);
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float Mu = (M == -INFINITY) ? 0.f : M;
     float Ls = 0.f;
-    for (int k = 0; k < np; ++k) {
-      float2 ml = p.part_ml[s_pidx[k] * G + h];
-      float sc = ex2(ml.x - Mu);
-      s_scale[h * MAXP + k] = sc;
-      Ls += ml.y * sc;
+    for (int k2 = lane; k2 < np; k2 += 32) {
+      const float2 ml = s_ml[k2 * G + h];
+      const float sc = ex2(ml.x - Mu);
+      s_sc[h * MAXP + k2] = sc;
+      Ls = fmaf(ml.y, sc, Ls);
     }
-    s_M[h] = Ls;
-    s_lse[h] = Mu + lg2(Ls);
+    for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    if (lane == 0) {
+      s_inv[h] = 1.f / Ls;
+      s_lse[h] = Mu + lg2(Ls);
+    }
   }
   __syncthreads();
-  const int b = u / p.st.Hkv, kvh = u - b * p.st.Hkv;
-  for (int e = threadIdx.x; e < G * D; e += blockDim.x) {
+  // 4. output
+  const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
+  for (int e = tid; e < G * D; e += COMBINE_THREADS) {
     const int h = e / D, c = e - h * D;
     float acc = 0.f;
-    for (int k = 0; k < np; ++k) acc = fmaf(p.part_o[(s_pidx[k] * G + h) * D + c], s_scale[h * MAXP + k], acc);
-    const float o = acc / s_M[h];
-    const size_t oi = ((size_t)b * p.st.Hq + kvh * G + h) * D + c;
+    for (int k2 = 0; k2 < np; ++k2) acc = fmaf(p.part_o[(s_pidx[k2] * G + h) * D + c], s_sc[h * MAXP + k2], acc);
+    const float o = acc * s_inv[h];
+    const size_t oi = ((size_t)bb * p.st.Hq + kvh * G + h) * D + c;
     if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
     else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
   }
-  // scores: bf16 window entries (skip the sink) and 2-bit windows
+  // 5. scores: bf16 window entries (the sink is never scored) and 2-bit windows
   const int W = p.st.geo.W, sub_tiles = W / 16;
   const int nent = p.nbw + p.nq;
-  for (int e = threadIdx.x; e < nent; e += blockDim.x) {
+  for (int e = tid; e < nent; e += COMBINE_THREADS) {
     int win;
     float dS = 0.f;
     if (e < p.nbw) {
-      int2 ent = p.st.blist[gu * p.st.capb + e];
+      const int2 ent = p.st.blist[gu * p.st.capb + e];
       win = ent.x;
       if (win < 0) continue;
-      int lo = (win == 0) ? p.st.n_sink : 0;
+      const int lo = (win == 0) ? p.st.n_sink : 0;
       int hi = p.L - win * W;
       hi = hi < W ? hi : W;
       for (int s = 0; s < sub_tiles; ++s) {
-        int tl = lo - 16 * s, th = hi - 16 * s;
+        const int tl = lo - 16 * s, th = hi - 16 * s;
         if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
         const float* ls = p.lse + ((size_t)u * p.ntiles + e * sub_tiles + s) * G;
         for (int h = 0; h < G; ++h) dS += ex2(ls[h] - s_lse[h]);
       }
     } else {
-      int2 ent = p.st.qlist[gu * p.st.capq + (e - p.nbw)];
+      const int2 ent = p.st.qlist[gu * p.st.capq + (e - p.nbw)];
       win = ent.x;
       const float* ls = p.lse + ((size_t)u * p.ntiles + p.nbw * sub_tiles + (e - p.nbw)) * G;
       for (int h = 0; h < G; ++h) dS += ex2(ls[h] - s_lse[h]);
@@ -649,8 +666,8 @@ cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t strea
 }
 
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream) {
-  if (p.st.geo.D == 128) qe_attn_combine_kernel<128><<<p.st.units, 128, 0, stream>>>(p);
-  else qe_attn_combine_kernel<64><<<p.st.units, 128, 0, stream>>>(p);
+  if (p.st.geo.D == 128) qe_attn_combine_kernel<128><<<p.st.units, COMBINE_THREADS, 0, stream>>>(p);
+  else qe_attn_combine_kernel<64><<<p.st.units, COMBINE_THREADS, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

@@ -11,10 +11,13 @@
 // with channels as rows).
 //
 // 2-bit window slot: key codes (w d / 4 B), value codes (w d / 4 B), key
-// min[d], key scale[d], value min[w], value scale[w] (float32).  Codes are
-// grouped per lane in 32-bit words; a word carries two fragments of 8 codes;
-// fragment f, register r, element e sits at bit 2 (4 f + r) + 16 e, so
-// (word >> 2j) & 0x00030003 yields a bf16x2 pair after adding the exponent.
+// min[d], key scale[d], value min[w], value scale[w] (float32; the parameter
+// arrays are permuted so each lane reads its own as 16-byte vectors).  Codes
+// are grouped per lane in 32-bit words; a word carries two fragments of 8
+// codes; fragment f, register r, element e sits at bit 8 r + 2 f + 4 e.  Then
+// (word >> 2f) & 0x33333333 holds, in byte r, the register's two codes as two
+// FP4 (e2m1) nibbles whose values are code / 2, and one cvt.f16x2.e2m1x2 per
+// register turns them into the f16 pair the tensor core consumes.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -67,7 +70,7 @@ QE_HD CodePos code_word(const Geo& g, int F, int lane, int reg, int e) {
   int cw = g.cw();
   CodePos p;
   p.byte = ((wi / cw) * 32 + lane) * (cw * 4) + (wi % cw) * 4;
-  p.bit = 2 * (4 * f + reg) + 16 * e;
+  p.bit = 8 * reg + 2 * f + 4 * e;
   return p;
 }
 // key code of token r, channel c (fragments ordered token-tile major, channel-step minor)
@@ -85,6 +88,16 @@ QE_HD CodePos vcode_pos(const Geo& g, int r, int c) {
   CodePos p = code_word(g, mc * (g.W / 16) + kt, lane, reg, rt & 1);
   p.byte += g.kcode_bytes();
   return p;
+}
+
+// Position of key channel c inside the key min / key scale arrays of a 2-bit slot: lane t of
+// channel step ks reads channels (16 ks + 2t, +1, +8, +9) -- its B-fragment channels -- as one
+// 16-byte vector.
+QE_HD int kparam_pos(int c) { return (c & ~15) + (((c & 7) >> 1) << 2) + (c & 1) + (((c >> 3) & 1) << 1); }
+// Position of token r inside the value min / value scale arrays: lane group gg = r % 8 reads its
+// rows (16 mt + gg and 16 mt + gg + 8 for every token tile mt) as one vector.
+QE_HD int vparam_pos(const Geo& g, int r) {
+  return (r & 7) * (2 * (g.W / 16)) + (r >> 4) * 2 + ((r >> 3) & 1);
 }
 
 // ---------------------------------------------------------------------------- cache state
@@ -159,11 +172,41 @@ __device__ __forceinline__ unsigned movmatrix_t(unsigned a) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
-// two small codes in the halves of x (bits 0-1 and 16-17) -> exact bf16x2 values
-__device__ __forceinline__ unsigned codes_to_bf16x2(unsigned x) {
-  unsigned v = (x & 0x00030003u) | 0x43004300u;      // 128 + code in each half
+// byte `b` of x holds two FP4 (e2m1) nibbles -> f16x2 (low nibble -> low half).  2-bit codes
+// sit in the low two bits of each nibble, so the values are code / 2, exactly.
+template <int B>
+__device__ __forceinline__ unsigned e2m1x2_to_f16x2(unsigned x) {
   unsigned d;
-  asm("sub.rn.bf16x2 %0, %1, %2;" : "=r"(d) : "r"(v), "r"(0x43004300u));
+  asm("{\n\t.reg .b16 s;\n\t.reg .b8 t;\n\tcvt.u16.u32 s, %1;\n\tcvt.u8.u16 t, s;\n\t"
+      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
+      : "=r"(d) : "r"(x >> (8 * B)));
+  return d;
+}
+// the 8 f16x2 A-fragment registers (two fragments) carried by one code word
+__device__ __forceinline__ void unpack_word(unsigned w, unsigned (&a)[8]) {
+  const unsigned t0 = w & 0x33333333u, t1 = (w >> 2) & 0x33333333u;
+  a[0] = e2m1x2_to_f16x2<0>(t0); a[1] = e2m1x2_to_f16x2<1>(t0);
+  a[2] = e2m1x2_to_f16x2<2>(t0); a[3] = e2m1x2_to_f16x2<3>(t0);
+  a[4] = e2m1x2_to_f16x2<0>(t1); a[5] = e2m1x2_to_f16x2<1>(t1);
+  a[6] = e2m1x2_to_f16x2<2>(t1); a[7] = e2m1x2_to_f16x2<3>(t1);
+}
+__device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                        unsigned b0, unsigned b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// bf16x2 with round-toward-zero: lo -> low half
+__device__ __forceinline__ unsigned pack_bf16x2_rz(float lo, float hi) {
+  unsigned d;
+  asm("cvt.rz.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// f16x2 with round-toward-zero: lo -> low half
+__device__ __forceinline__ unsigned pack_f16x2_rz(float lo, float hi) {
+  unsigned d;
+  asm("cvt.rz.f16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
   return d;
 }
 // bf16x2 from two floats: lo -> low half, hi -> high half (round to nearest even)

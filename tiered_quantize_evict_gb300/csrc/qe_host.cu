@@ -617,10 +617,14 @@ qe_status qe_get_quant_window(qe_handle h, int layer, int unit, int window, uint
       if (k_codes) k_codes[r * g.D + c] = (wk >> pk.bit) & 3u;
       if (v_codes) v_codes[r * g.D + c] = (wv >> pv.bit) & 3u;
     }
-  if (k_min) memcpy(k_min, buf.data() + g.off_kmin(), 4 * g.D);
-  if (k_scale) memcpy(k_scale, buf.data() + g.off_kscale(), 4 * g.D);
-  if (v_min) memcpy(v_min, buf.data() + g.off_vmin(), 4 * g.W);
-  if (v_scale) memcpy(v_scale, buf.data() + g.off_vscale(), 4 * g.W);
+  for (int c = 0; c < g.D; ++c) {
+    if (k_min) memcpy(k_min + c, buf.data() + g.off_kmin() + 4 * qe::kparam_pos(c), 4);
+    if (k_scale) memcpy(k_scale + c, buf.data() + g.off_kscale() + 4 * qe::kparam_pos(c), 4);
+  }
+  for (int r = 0; r < g.W; ++r) {
+    if (v_min) memcpy(v_min + r, buf.data() + g.off_vmin() + 4 * qe::vparam_pos(g, r), 4);
+    if (v_scale) memcpy(v_scale + r, buf.data() + g.off_vscale() + 4 * qe::vparam_pos(g, r), 4);
+  }
   return QE_OK;
 }
 

@@ -420,12 +420,12 @@ __global__ void __launch_bounds__(MOVE_THREADS) qe_move_kernel(State st, const M
     __syncthreads();
     for (int i = tid; i < nwords; i += MOVE_THREADS) reinterpret_cast<unsigned*>(qs)[i] = words[i];
     for (int c = tid; c < D; c += MOVE_THREADS) {
-      reinterpret_cast<float*>(qs + g.off_kmin())[c] = kz[c];
-      reinterpret_cast<float*>(qs + g.off_kscale())[c] = ks[c];
+      reinterpret_cast<float*>(qs + g.off_kmin())[kparam_pos(c)] = kz[c];
+      reinterpret_cast<float*>(qs + g.off_kscale())[kparam_pos(c)] = ks[c];
     }
     for (int r = tid; r < W; r += MOVE_THREADS) {
-      reinterpret_cast<float*>(qs + g.off_vmin())[r] = vz[r];
-      reinterpret_cast<float*>(qs + g.off_vscale())[r] = vs[r];
+      reinterpret_cast<float*>(qs + g.off_vmin())[vparam_pos(g, r)] = vz[r];
+      reinterpret_cast<float*>(qs + g.off_vscale())[vparam_pos(g, r)] = vs[r];
     }
     __syncthreads();
     // the ledger copy of the codes and the exact bf16 copy go to the mapped host store
