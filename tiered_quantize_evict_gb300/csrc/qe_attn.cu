@@ -36,7 +36,7 @@
 
 namespace qe {
 
-constexpr int ATTN_WARPS = 8;
+constexpr int ATTN_WARPS = 12;
 constexpr int ATTN_SMEM_STAGES_BYTES = 196608;   // 192 KB of stages per CTA
 constexpr unsigned long long WAIT_LIMIT_NS = 200000000ull;  // 0.2 s
 
