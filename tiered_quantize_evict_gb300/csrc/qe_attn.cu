@@ -48,6 +48,23 @@ struct TileDesc {
   int sub;         // bf16 sub-tile index inside its window slot
 };
 
+// What the consumer needs of a tile (written per stage by the producer lane).
+struct StageDesc {
+  int u;           // unit
+  int lse_off;     // (u * ntiles + i) * G
+  int meta;        // lo | hi << 8 | kind << 16
+  int pad;
+};
+
+// A tile ready to issue: its source and its consumer descriptor.
+struct BatchDesc {
+  const uint8_t* src;
+  unsigned bytes;
+  StageDesc sd;
+  int pad;
+};
+constexpr int BATCH = 32;
+
 __device__ __forceinline__ long long tile_start(const AttnParams& p, int u, int i, int nbt) {
   long long r = (i < nbt) ? (long long)i * p.cb : (long long)nbt * p.cb + (long long)(i - nbt) * p.cq;
   return (long long)u * p.Cu + r;
@@ -292,7 +309,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   constexpr int SUBT = W / 16;
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ __align__(8) unsigned long long bars[ATTN_WARPS][NST];
-  __shared__ TileDesc descs[ATTN_WARPS][NST];
+  __shared__ StageDesc descs[ATTN_WARPS][NST];
+  __shared__ BatchDesc batches[ATTN_WARPS][BATCH];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = lane >> 2, t = lane & 3;
@@ -312,29 +330,56 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   }
   __syncwarp();
 
-  // ---- producer: cursor (pu, pi) with its list entry prefetched one tile ahead
-  int pu, pi;
-  first_tile(p, x_lo, nbt, pu, pi);
-  const bool pvalid0 = pu < p.st.units && tile_start(p, pu, pi, nbt) < x_hi;
-  int2 pent = pvalid0 ? list_entry(p, pu, pi, nbt, SUBT) : make_int2(0, 0);
-  auto issue_next = [&](int stage) -> bool {
-    while (pu < p.st.units && tile_start(p, pu, pi, nbt) < x_hi) {
+  // ---- producer: the warp describes BATCH tiles at a time (one per lane, empty tiles
+  //      compacted out), then issues them one by one from shared memory
+  BatchDesc* batch = batches[warp];
+  int cu, ci;                        // cursor: first tile not yet described
+  first_tile(p, x_lo, nbt, cu, ci);
+  bool range_done = !(cu < p.st.units && tile_start(p, cu, ci, nbt) < x_hi);
+  int bcount = 0, bnext = 0;
+  auto describe_batch = [&]() {
+    while (!range_done) {
+      int u = cu, i = ci + lane;
+      while (i >= p.ntiles) { i -= p.ntiles; ++u; }
+      const bool inr = u < p.st.units && tile_start(p, u, i, nbt) < x_hi;
       TileDesc d;
-      const bool ok = describe(p, pu, pi, nbt, pent, d);
-      next_tile(p, pu, pi);
-      if (pu < p.st.units && tile_start(p, pu, pi, nbt) < x_hi) pent = list_entry(p, pu, pi, nbt, SUBT);
-      if (!ok) continue;
-      if (lane == 0) {
-        descs[warp][stage] = d;
-        unsigned bytes;
-        const uint8_t* src = tile_src(p, d, bytes);
-        const unsigned bar = smem_u32(&bars[warp][stage]);
-        mbar_expect_tx(bar, bytes);
-        bulk_g2s(smem_u32(stage_base + (size_t)stage * S::STAGE), src, bytes, bar);
+      bool ok = false;
+      if (inr) ok = describe(p, u, i, nbt, list_entry(p, u, i, nbt, SUBT), d);
+      const unsigned vb = __ballot_sync(0xffffffffu, ok);
+      if (ok) {
+        BatchDesc bd;
+        bd.src = tile_src(p, d, bd.bytes);
+        bd.sd.u = u;
+        bd.sd.lse_off = (u * p.ntiles + i) * G;
+        bd.sd.meta = d.lo | (d.hi << 8) | (d.kind << 16);
+        bd.sd.pad = 0;
+        bd.pad = 0;
+        batch[__popc(vb & ((1u << lane) - 1))] = bd;
       }
-      return true;
+      range_done = __any_sync(0xffffffffu, !inr);
+      ci += BATCH;
+      while (ci >= p.ntiles) { ci -= p.ntiles; ++cu; }
+      bcount = __popc(vb);
+      bnext = 0;
+      __syncwarp();
+      if (bcount > 0) return;
     }
-    return false;
+  };
+  auto issue_next = [&](int stage) -> bool {
+    if (bnext == bcount) {
+      if (range_done) return false;
+      describe_batch();
+      if (bcount == 0) return false;
+    }
+    if (lane == 0) {
+      const BatchDesc bd = batch[bnext];
+      descs[warp][stage] = bd.sd;
+      const unsigned bar = smem_u32(&bars[warp][stage]);
+      mbar_expect_tx(bar, bd.bytes);
+      bulk_g2s(smem_u32(stage_base + (size_t)stage * S::STAGE), bd.src, bd.bytes, bar);
+    }
+    ++bnext;
+    return true;
   };
   int issued = 0;
   for (int s = 0; s < NST; ++s) {
@@ -399,9 +444,10 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   for (; k < issued; ++k) {
     const int s = k % NST;
     if (!wait_tile(k)) { timed_out = true; break; }
-    const TileDesc d = descs[warp][s];
+    const StageDesc sd = descs[warp][s];
+    const int d_lo = sd.meta & 0xFF, d_hi = (sd.meta >> 8) & 0xFF, d_kind = sd.meta >> 16;
     const uint8_t* sp = stage_base + (size_t)s * S::STAGE;
-    while (d.u > cur_u) {
+    while (sd.u > cur_u) {
       flush(cur_u);
       reset();
       ++cur_u;
@@ -423,8 +469,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         qb[ks][1] = lo_col ? 0u : a1;
       }
     }
-    float* lse_out = p.lse + ((size_t)d.u * p.ntiles + d.i) * G;
-    if (d.kind == 0) {
+    float* lse_out = p.lse + sd.lse_off;
+    if (d_kind == 0) {
       // ---- bf16 sub-tile: 16 tokens; two accumulators halve the mma dependency chain
       float acc[1][2][4] = {};
 #pragma unroll
@@ -434,7 +480,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       }
       const float vnone[2] = {0.f, 0.f};
       unsigned Bp[1][2];
-      softmax_tile<1, 2, MC, false>(acc, d.lo == 0 && d.hi == 16, d.lo, d.hi, 0.f, vnone, vnone, p.scale_log2, rs,
+      softmax_tile<1, 2, MC, false>(acc, d_lo == 0 && d_hi == 16, d_lo, d_hi, 0.f, vnone, vnone, p.scale_log2, rs,
                                     Bp, lse_out, G, lane);
 #pragma unroll
       for (int mc = 0; mc < MC; ++mc) {
@@ -489,7 +535,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         }
       }
       unsigned Bp[MT][2];
-      softmax_tile<MT, 2, MC, true>(acc, d.lo == 0, d.lo, d.hi, bias, vz, vs, p.scale_log2, rs, Bp, lse_out, G,
+      softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, p.scale_log2, rs, Bp, lse_out, G,
                                     lane);
       // P V over the unpacked value codes (A = V^T: channel tiles x token steps)
       {
