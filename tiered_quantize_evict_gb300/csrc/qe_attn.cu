@@ -318,7 +318,13 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   const int wg = blockIdx.x * ATTN_WARPS + warp;
   const long long x_lo = (wg * p.C + p.NW - 1) / p.NW;
   const long long x_hi = ((wg + 1) * p.C + p.NW - 1) / p.NW;
-  if (x_lo >= x_hi) return;
+  // the warps whose ranges meet unit u are u NW / units .. ; partial slot = warp - first warp
+  auto slot_of = [&](int u) -> long long { return (long long)u * p.pslots + (wg - (int)((long long)u * p.NW / p.st.units)); };
+  if (x_lo >= x_hi) {   // empty range: leave an empty partial in the unit it falls into
+    const int u = (int)(x_lo / p.Cu);
+    if (u < p.st.units && lane < G) p.part_ml[slot_of(u) * G + lane] = make_float2(-INFINITY, 0.f);
+    return;
+  }
   const int nbt = p.nbw * SUBT;
   const int u_first = (int)(x_lo / p.Cu);
   const int u_last = (int)((x_hi - 1) / p.Cu);
@@ -337,14 +343,25 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   first_tile(p, x_lo, nbt, cu, ci);
   bool range_done = !(cu < p.st.units && tile_start(p, cu, ci, nbt) < x_hi);
   int bcount = 0, bnext = 0;
+  // each lane keeps the list entry of its tile of the next batch in flight (prefetch)
+  int lu, li;
+  bool linr;
+  int2 lent = make_int2(0, 0);
+  auto prefetch = [&]() {
+    lu = cu;
+    li = ci + lane;
+    while (li >= p.ntiles) { li -= p.ntiles; ++lu; }
+    linr = lu < p.st.units && tile_start(p, lu, li, nbt) < x_hi;
+    if (linr) lent = list_entry(p, lu, li, nbt, SUBT);
+  };
+  if (!range_done) prefetch();
   auto describe_batch = [&]() {
     while (!range_done) {
-      int u = cu, i = ci + lane;
-      while (i >= p.ntiles) { i -= p.ntiles; ++u; }
-      const bool inr = u < p.st.units && tile_start(p, u, i, nbt) < x_hi;
+      const int u = lu, i = li;
+      const bool inr = linr;
       TileDesc d;
       bool ok = false;
-      if (inr) ok = describe(p, u, i, nbt, list_entry(p, u, i, nbt, SUBT), d);
+      if (inr) ok = describe(p, u, i, nbt, lent, d);
       const unsigned vb = __ballot_sync(0xffffffffu, ok);
       if (ok) {
         BatchDesc bd;
@@ -359,6 +376,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       range_done = __any_sync(0xffffffffu, !inr);
       ci += BATCH;
       while (ci >= p.ntiles) { ci -= p.ntiles; ++cu; }
+      if (!range_done) prefetch();
       bcount = __popc(vb);
       bnext = 0;
       __syncwarp();
@@ -404,7 +422,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       for (int r = 0; r < 4; ++r) rs.O[mc][r] = 0.f;
   };
   auto flush = [&](int u) {
-    const long long pidx = (long long)wg * p.maxseg + (u - u_first);
+    const long long pidx = slot_of(u);
     float z = rs.zs;
     z += __shfl_xor_sync(0xffffffffu, z, 4);
     z += __shfl_xor_sync(0xffffffffu, z, 8);
@@ -572,115 +590,144 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
 }
 
 // ------------------------------------------------------------------------------ combine
-// One CTA per unit: merge the partials of every warp whose range meets the unit, write
-// o = sum / l, then turn each tile's log2-sum-exp into mass, sum it over the G heads and
-// add it to the window's float32 score (eq. (1) with the GQA group sum).
-constexpr int COMBINE_THREADS = 256;
-constexpr int MAXP = 256;
+// Grid (units, G + 1).  CTA (u, h < G) merges the partials of unit u for query head h and
+// writes o_h = sum / l; CTA (u, G) recomputes every head's log-sum-exp, turns each tile's
+// log2-sum-exp into mass, sums it over the G heads and adds it to the window's float32 score
+// (eq. (1) with the GQA group sum).  The partial list comes from the attention launch.
+constexpr int COMBINE_THREADS = 128;
+constexpr int MAXP = COMBINE_MAXP;
+
+// partial slots of unit u: one per warp whose position range meets [u Cu, (u+1) Cu)
+__device__ __forceinline__ int unit_partials(const CombineParams& p, int u) {
+  const long long w0 = (long long)u * p.NW / p.st.units;
+  const long long w1 = (((long long)u + 1) * p.Cu - 1) * p.NW / p.C;
+  int np = (int)(w1 - w0 + 1);
+  if (np > p.pslots) np = p.pslots;
+  return np;
+}
+
+// head h's global max over the partials, the scale of each partial and log2 of the normaliser;
+// executed by one warp
+__device__ __forceinline__ void head_stats(const CombineParams& p, int u, int np, int h, float* s_sc, float& inv,
+                                           float& lse) {
+  const int lane = threadIdx.x & 31;
+  const int G = p.st.G;
+  const float2* ml0 = p.part_ml + (size_t)u * p.pslots * G + h;
+  float2 ml[MAXP / 32];
+#pragma unroll
+  for (int j = 0; j < MAXP / 32; ++j) {
+    const int k = lane + 32 * j;
+    ml[j] = k < np ? ml0[(size_t)k * G] : make_float2(-INFINITY, 0.f);
+  }
+  float M = -INFINITY;
+#pragma unroll
+  for (int j = 0; j < MAXP / 32; ++j) M = fmaxf(M, ml[j].x);
+  for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+  const float Mu = (M == -INFINITY) ? 0.f : M;
+  float Ls = 0.f;
+#pragma unroll
+  for (int j = 0; j < MAXP / 32; ++j) {
+    const int k = lane + 32 * j;
+    const float sc = ml[j].y > 0.f ? ex2(ml[j].x - Mu) : 0.f;
+    if (s_sc && k < np) s_sc[k] = sc;
+    Ls = fmaf(ml[j].y, sc, Ls);
+  }
+  for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+  inv = 1.f / Ls;
+  lse = Mu + lg2(Ls);
+}
 
 template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const CombineParams p) {
-  const int u = blockIdx.x;
+  const int u = blockIdx.x, part = blockIdx.y;
   const int G = p.st.G;
   const long long gu = (long long)p.layer * p.st.units + u;
-  __shared__ long long s_pidx[MAXP];
-  __shared__ float2 s_ml[MAXP * 4];
-  __shared__ float s_sc[4 * MAXP];
+  __shared__ float s_sc[MAXP];
   __shared__ float s_inv[4], s_lse[4];
-  __shared__ int s_wcount[COMBINE_THREADS / 32];
-  __shared__ int s_np;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  // 1. partial producers: warps whose position range meets [u Cu, (u+1) Cu), in order
-  const long long a = (long long)u * p.Cu, b = a + p.Cu - 1;
-  const long long w0 = a * p.NW / p.C, w1 = b * p.NW / p.C;
-  if (tid == 0 && w1 - w0 + 1 > MAXP) atomicOr(p.st.err, ERR_COUNT);
-  const long long w = w0 + tid;
-  bool valid = false;
-  long long pidx = 0;
-  if (tid < MAXP && w <= w1) {
-    const long long xl = (w * p.C + p.NW - 1) / p.NW, xh = ((w + 1) * p.C + p.NW - 1) / p.NW;
-    valid = xl < xh;
-    pidx = w * p.maxseg + (u - (int)(xl / p.Cu));
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int np = unit_partials(p, u);
+  if (part < G) {
+    // ---- output of head h = part
+    const int h = part;
+    if (warp == 0) {
+      float inv, lse;
+      head_stats(p, u, np, h, s_sc, inv, lse);
+      if (tid == 0) s_inv[0] = inv;
+    }
+    __syncthreads();
+    const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
+    const float* po = p.part_o + ((size_t)u * p.pslots * G + h) * D;
+    for (int c = tid; c < D; c += COMBINE_THREADS) {
+      float acc = 0.f;
+      for (int k0 = 0; k0 < np; k0 += 8) {
+        float v[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          v[j] = (k0 + j < np && s_sc[k0 + j] != 0.f) ? po[(size_t)(k0 + j) * G * D + c] : 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j)
+          if (k0 + j < np) acc = fmaf(v[j], s_sc[k0 + j], acc);
+      }
+      const float o = acc * s_inv[0];
+      const size_t oi = ((size_t)bb * p.st.Hq + kvh * G + h) * D + c;
+      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+    }
+    return;
   }
-  const unsigned bal = __ballot_sync(0xffffffffu, valid);
-  if (lane == 0) s_wcount[warp] = __popc(bal);
-  __syncthreads();
-  int base = 0;
-  for (int i = 0; i < warp; ++i) base += s_wcount[i];
-  if (valid) s_pidx[base + __popc(bal & ((1u << lane) - 1))] = pidx;
-  if (tid == 0) {
-    int n = 0;
-    for (int i = 0; i < COMBINE_THREADS / 32; ++i) n += s_wcount[i];
-    s_np = n;
-  }
-  __syncthreads();
-  const int np = s_np;
-  // 2. (max, sum) of every partial and head
-  for (int i = tid; i < np * G; i += COMBINE_THREADS) s_ml[i] = p.part_ml[s_pidx[i / G] * G + (i % G)];
-  __syncthreads();
-  // 3. per head: global max, scale of each partial, normaliser (one warp per head)
+  // ---- scores
   if (warp < G) {
-    const int h = warp;
-    float M = -INFINITY;
-    for (int k2 = lane; k2 < np; k2 += 32) M = fmaxf(M, s_ml[k2 * G + h].x);
-    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float Mu = (M == -INFINITY) ? 0.f : M;
-    float Ls = 0.f;
-    for (int k2 = lane; k2 < np; k2 += 32) {
-      const float2 ml = s_ml[k2 * G + h];
-      const float sc = ex2(ml.x - Mu);
-      s_sc[h * MAXP + k2] = sc;
-      Ls = fmaf(ml.y, sc, Ls);
-    }
-    for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
-    if (lane == 0) {
-      s_inv[h] = 1.f / Ls;
-      s_lse[h] = Mu + lg2(Ls);
-    }
+    float inv, lse;
+    head_stats(p, u, np, warp, nullptr, inv, lse);
+    if ((tid & 31) == 0) s_lse[warp] = lse;
   }
   __syncthreads();
-  // 4. output
-  const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
-  for (int e = tid; e < G * D; e += COMBINE_THREADS) {
-    const int h = e / D, c = e - h * D;
-    float acc = 0.f;
-    for (int k2 = 0; k2 < np; ++k2) acc = fmaf(p.part_o[(s_pidx[k2] * G + h) * D + c], s_sc[h * MAXP + k2], acc);
-    const float o = acc * s_inv[h];
-    const size_t oi = ((size_t)bb * p.st.Hq + kvh * G + h) * D + c;
-    if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
-    else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-  }
-  // 5. scores: bf16 window entries (the sink is never scored) and 2-bit windows
   const int W = p.st.geo.W, sub_tiles = W / 16;
   const int nent = p.nbw + p.nq;
-  for (int e = tid; e < nent; e += COMBINE_THREADS) {
-    int win;
-    float dS = 0.f;
-    if (e < p.nbw) {
-      const int2 ent = p.st.blist[gu * p.st.capb + e];
-      win = ent.x;
-      if (win < 0) continue;
-      const int lo = (win == 0) ? p.st.n_sink : 0;
-      int hi = p.L - win * W;
-      hi = hi < W ? hi : W;
-      for (int s = 0; s < sub_tiles; ++s) {
-        const int tl = lo - 16 * s, th = hi - 16 * s;
-        if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
-        const float* ls = p.lse + ((size_t)u * p.ntiles + e * sub_tiles + s) * G;
-        for (int h = 0; h < G; ++h) dS += ex2(ls[h] - s_lse[h]);
+  constexpr int EPT = 4;   // entries per thread per round: their loads are issued together
+  for (int e0 = tid; e0 < nent; e0 += COMBINE_THREADS * EPT) {
+    int2 ent[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int e = e0 + j * COMBINE_THREADS;
+      ent[j] = make_int2(-1, -1);
+      if (e < p.nbw) ent[j] = p.st.blist[gu * p.st.capb + e];
+      else if (e < nent) ent[j] = p.st.qlist[gu * p.st.capq + (e - p.nbw)];
+    }
+    float dS[EPT];
+    int win[EPT];
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int e = e0 + j * COMBINE_THREADS;
+      win[j] = ent[j].x;
+      dS[j] = 0.f;
+      if (e >= nent || win[j] < 0) continue;
+      if (e < p.nbw) {
+        const int lo = (win[j] == 0) ? p.st.n_sink : 0;
+        int hi = p.L - win[j] * W;
+        hi = hi < W ? hi : W;
+        for (int s = 0; s < sub_tiles; ++s) {
+          const int tl = lo - 16 * s, th = hi - 16 * s;
+          if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
+          const float* ls = p.lse + ((size_t)u * p.ntiles + e * sub_tiles + s) * G;
+          for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
+        }
+      } else {
+        const float* ls = p.lse + ((size_t)u * p.ntiles + p.nbw * sub_tiles + (e - p.nbw)) * G;
+        for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
       }
-    } else {
-      const int2 ent = p.st.qlist[gu * p.st.capq + (e - p.nbw)];
-      win = ent.x;
-      const float* ls = p.lse + ((size_t)u * p.ntiles + p.nbw * sub_tiles + (e - p.nbw)) * G;
-      for (int h = 0; h < G; ++h) dS += ex2(ls[h] - s_lse[h]);
     }
-    if (win < 0 || win >= p.st.maxw) {
-      atomicOr(p.st.err, ERR_TABLE);
-      continue;
+#pragma unroll
+    for (int j = 0; j < EPT; ++j) {
+      const int e = e0 + j * COMBINE_THREADS;
+      if (e >= nent || win[j] < 0) continue;
+      if (win[j] >= p.st.maxw) {
+        atomicOr(p.st.err, ERR_TABLE);
+        continue;
+      }
+      float* sp = p.st.score + gu * p.st.maxw + win[j];
+      *sp = *sp + dS[j];
     }
-    float* sp = p.st.score + gu * p.st.maxw + win;
-    *sp = *sp + dS;
   }
 }
 
@@ -712,8 +759,9 @@ cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t strea
 }
 
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream) {
-  if (p.st.geo.D == 128) qe_attn_combine_kernel<128><<<p.st.units, COMBINE_THREADS, 0, stream>>>(p);
-  else qe_attn_combine_kernel<64><<<p.st.units, COMBINE_THREADS, 0, stream>>>(p);
+  const dim3 grid(p.st.units, p.st.G + 1);
+  if (p.st.geo.D == 128) qe_attn_combine_kernel<128><<<grid, COMBINE_THREADS, 0, stream>>>(p);
+  else qe_attn_combine_kernel<64><<<grid, COMBINE_THREADS, 0, stream>>>(p);
   return cudaGetLastError();
 }
 

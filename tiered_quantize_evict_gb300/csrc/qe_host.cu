@@ -45,8 +45,7 @@ struct qe_handle_s {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   float* lse = nullptr;
-  long long part_slots = 0;   // warps * maxseg capacity
-  int maxseg_cap = 0;
+  int pslots_cap = 0;         // partial slots per unit
   int ntiles_cap = 0;
   // moves
   qe::Move* moves = nullptr;
@@ -240,13 +239,14 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(st.err, 1, "error flag");
   QE_ALLOC(st.stats, (size_t)c.n_layers * 5, "stats");
 
-  // split-K scratch: one CTA per SM, attn_warps_per_cta() warps each
+  // split-K scratch: one CTA per SM, attn_warps_per_cta() warps each; a unit meets at most
+  // NW / units + 2 warp ranges
   const int NW = h->n_sm * qe::attn_warps_per_cta();
-  h->maxseg_cap = ceil_div(h->units, NW) + 3;
-  h->part_slots = (long long)NW * h->maxseg_cap;
+  h->pslots_cap = NW / h->units + 3;
+  if (h->pslots_cap > qe::COMBINE_MAXP) h->pslots_cap = qe::COMBINE_MAXP;
   h->ntiles_cap = st.capb * (c.window / 16) + st.capq;
-  QE_ALLOC(h->part_o, h->part_slots * G * c.head_dim, "partials");
-  QE_ALLOC(h->part_ml, h->part_slots * G, "partial stats");
+  QE_ALLOC(h->part_o, (size_t)h->units * h->pslots_cap * G * c.head_dim, "partials");
+  QE_ALLOC(h->part_ml, (size_t)h->units * h->pslots_cap * G, "partial stats");
   QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
   h->max_moves = h->units * st.caps + 16;
   {
@@ -395,21 +395,22 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   if (p.ntiles > h->ntiles_cap) return fail(h, QE_ERR_CAPACITY, "tile count %d exceeds %d", p.ntiles, h->ntiles_cap);
   p.Cu = (long long)p.nbw * sub * p.cb + (long long)p.nq * p.cq;
   p.C = p.Cu * h->units;
-  // warps: at most one per SM slot, at most one per unit of cost granularity, and few
-  // enough that a unit never meets more than 256 partials
+  // warps: at most one per SM slot, at most one per tile, and few enough that a unit never
+  // meets more warp ranges than it has partial slots
   const int wpc = qe::attn_warps_per_cta();
   long long nw = (long long)h->n_sm * wpc;
   const long long tiles_total = (long long)p.ntiles * h->units;
   if (nw > tiles_total) nw = tiles_total;
-  if (nw > 250LL * h->units) nw = 250LL * h->units;
+  if (nw > (long long)(h->pslots_cap - 2) * h->units) nw = (long long)(h->pslots_cap - 2) * h->units;
   int grid = ceil_div(nw, wpc);
   if (grid < 1) grid = 1;
   p.NW = grid * wpc;
-  // partial slots per warp: units met by one warp range
-  p.maxseg = (int)((p.C / p.NW) / p.Cu) + 2;
-  if (p.maxseg > h->maxseg_cap) return fail(h, QE_ERR_CAPACITY, "split-K needs %d partial slots per warp", p.maxseg);
-  if ((long long)p.NW * p.maxseg > h->part_slots)
-    return fail(h, QE_ERR_CAPACITY, "split-K scratch too small (%d x %d)", p.NW, p.maxseg);
+  if ((long long)p.NW > (long long)(h->pslots_cap - 2) * h->units) {
+    grid = (int)(((long long)(h->pslots_cap - 2) * h->units) / wpc);
+    if (grid < 1) return fail(h, QE_ERR_CAPACITY, "too few partial slots for one CTA");
+    p.NW = grid * wpc;
+  }
+  p.pslots = h->pslots_cap;
   p.q = qd;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.part_o = h->part_o;
@@ -448,7 +449,7 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   cp.Cu = p.Cu;
   cp.C = p.C;
   cp.NW = p.NW;
-  cp.maxseg = p.maxseg;
+  cp.pslots = p.pslots;
   cp.part_o = h->part_o;
   cp.part_ml = h->part_ml;
   cp.lse = h->lse;

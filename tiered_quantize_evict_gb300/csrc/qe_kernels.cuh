@@ -19,12 +19,12 @@ struct AttnParams {
   long long Cu;          // cost of one unit
   long long C;           // cost of the layer
   int NW;                // warps in the grid
-  int maxseg;            // partial slots per warp
+  int pslots;            // partial slots per unit (>= warps whose range meets one unit)
   int ntiles;            // tiles per unit = nbw * w/16 + nq
   const uint16_t* q;     // [B][Hq][D] bf16
   float scale_log2;      // log2(e) / sqrt(d)
-  float* part_o;         // [NW * maxseg][G][D] unnormalised output
-  float2* part_ml;       // [NW * maxseg][G] (running max, sum) in the log2 domain
+  float* part_o;         // [units][pslots][G][D] unnormalised output
+  float2* part_ml;       // [units][pslots][G] (reference max, sum) in the log2 domain
   float* lse;            // [units][ntiles][G] per-tile log2-sum-exp
 };
 
@@ -36,13 +36,15 @@ struct CombineParams {
   int nbw, nq, ntiles;
   int cb, cq;
   long long Cu, C;
-  int NW, maxseg;
+  int NW, pslots;
   const float* part_o;
   const float2* part_ml;
   const float* lse;
   void* out;             // [B][Hq][D] float32 or bf16
   int out_fp32;
 };
+
+constexpr int COMBINE_MAXP = 256;   // partials one unit may receive
 
 // one window move decided by a routing event
 struct Move {
