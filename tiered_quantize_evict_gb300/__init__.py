@@ -167,6 +167,11 @@ class QECache:
         self._check(self._lib.qe_get_layer_info(self.h, layer, ctypes.byref(info)))
         return info
 
+    def qe_layer_info_sync(self):
+        """Resynchronise the host's view of every layer with the device (after graph replays)."""
+        for layer in range(self.cfg.n_layers):
+            self.layer_info(layer)
+
     def tiers(self, layer: int) -> np.ndarray:
         info = self.layer_info(layer)
         out = np.zeros((info.units, info.max_windows), np.uint8)

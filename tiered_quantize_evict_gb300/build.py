@@ -19,7 +19,8 @@ LIBDIR = os.path.join(HERE, "_lib")
 BUILD = os.path.join(HERE, "_build")
 SOURCES = ["qe_attn.cu", "qe_route.cu", "qe_host.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr"]
+FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
+         "--expt-relaxed-constexpr"]
 
 
 def nvcc() -> str:

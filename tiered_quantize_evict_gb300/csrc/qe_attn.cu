@@ -65,21 +65,44 @@ struct BatchDesc {
 };
 constexpr int BATCH = 32;
 
-__device__ __forceinline__ long long tile_start(const AttnParams& p, int u, int i, int nbt) {
+// Step-dependent counts of the layer being processed, read from the device-resident header.
+struct Lay {
+  int L, nbw, nq, nbt, ntiles, NW;
+  long long Cu, C;   // cost of one unit, of the layer
+};
+__device__ __forceinline__ Lay make_lay(const State& st, int layer, int pend, int cb, int cq, int NW) {
+  LayerDev h = st.ldev[layer];
+  h.L += pend;
+  const LayerView v = layer_view(st.geo, h);
+  Lay y;
+  y.L = v.L;
+  y.nbw = v.nbw;
+  y.nq = v.nq;
+  y.nbt = v.nbw * (st.geo.W / 16);
+  y.ntiles = y.nbt + y.nq;
+  y.Cu = (long long)y.nbt * cb + (long long)y.nq * cq;
+  y.C = y.Cu * st.units;
+  y.NW = NW;
+  return y;
+}
+
+__device__ __forceinline__ long long tile_start(const AttnParams& p, const Lay& y, int u, int i) {
+  const int nbt = y.nbt;
   long long r = (i < nbt) ? (long long)i * p.cb : (long long)nbt * p.cb + (long long)(i - nbt) * p.cq;
-  return (long long)u * p.Cu + r;
+  return (long long)u * y.Cu + r;
 }
 
 // first tile whose start position is >= x
-__device__ __forceinline__ void first_tile(const AttnParams& p, long long x, int nbt, int& u, int& i) {
-  u = (int)(x / p.Cu);
-  long long r = x - (long long)u * p.Cu;
+__device__ __forceinline__ void first_tile(const AttnParams& p, const Lay& y, long long x, int& u, int& i) {
+  const int nbt = y.nbt;
+  u = (int)(x / y.Cu);
+  long long r = x - (long long)u * y.Cu;
   long long bend = (long long)nbt * p.cb;
   if (r <= (long long)(nbt - 1) * p.cb) {
     i = (int)((r + p.cb - 1) / p.cb);
-  } else if (p.nq > 0 && r <= bend) {
+  } else if (y.nq > 0 && r <= bend) {
     i = nbt;                                   // between the last bf16 tile and the first 2-bit one
-  } else if (p.nq > 0 && r <= bend + (long long)(p.nq - 1) * p.cq) {
+  } else if (y.nq > 0 && r <= bend + (long long)(y.nq - 1) * p.cq) {
     i = nbt + (int)((r - bend + p.cq - 1) / p.cq);
   } else {
     u += 1;
@@ -87,24 +110,25 @@ __device__ __forceinline__ void first_tile(const AttnParams& p, long long x, int
   }
 }
 
-__device__ __forceinline__ void next_tile(const AttnParams& p, int& u, int& i) {
+__device__ __forceinline__ void next_tile(const Lay& y, int& u, int& i) {
   i += 1;
-  if (i >= p.ntiles) {
+  if (i >= y.ntiles) {
     i = 0;
     u += 1;
   }
 }
 
 // list entry {window, slot} of tile (u, i)
-__device__ __forceinline__ int2 list_entry(const AttnParams& p, int u, int i, int nbt, int sub_tiles) {
+__device__ __forceinline__ int2 list_entry(const AttnParams& p, const Lay& y, int u, int i, int sub_tiles) {
   const State& st = p.st;
   const long long gu = (long long)p.layer * st.units + u;
-  if (i < nbt) return st.blist[gu * st.capb + i / sub_tiles];
-  return st.qlist[gu * st.capq + (i - nbt)];
+  if (i < y.nbt) return st.blist[gu * st.capb + i / sub_tiles];
+  return st.qlist[gu * st.capq + (i - y.nbt)];
 }
 
 // descriptor of tile (u, i) from its list entry; false if it has no valid row (or is corrupt)
-__device__ __forceinline__ bool describe(const AttnParams& p, int u, int i, int nbt, int2 ent, TileDesc& d) {
+__device__ __forceinline__ bool describe(const AttnParams& p, const Lay& y, int u, int i, int2 ent, TileDesc& d) {
+  const int nbt = y.nbt;
   const State& st = p.st;
   const int W = st.geo.W;
   const int sub_tiles = W / 16;
@@ -125,7 +149,7 @@ __device__ __forceinline__ bool describe(const AttnParams& p, int u, int i, int 
       hi = st.n_sink;
     } else {
       lo = (ent.x == 0) ? st.n_sink : 0;
-      const int h = p.L - ent.x * W;
+      const int h = y.L - ent.x * W;
       hi = h < W ? h : W;
     }
     const int base = d.sub * 16;
@@ -316,18 +340,30 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   const int g = lane >> 2, t = lane & 3;
   const int G = p.st.G;
   const int wg = blockIdx.x * ATTN_WARPS + warp;
-  const long long x_lo = (wg * p.C + p.NW - 1) / p.NW;
-  const long long x_hi = ((wg + 1) * p.C + p.NW - 1) / p.NW;
+  // the layer's step-dependent counts live in shared memory (read when a batch of tiles is
+  // described), not in registers the tile loop needs
+  __shared__ Lay s_lay;
+  if (threadIdx.x == 0) {
+    s_lay = make_lay(p.st, p.layer, p.pend, p.cb, p.cq, gridDim.x * ATTN_WARPS);
+    if (blockIdx.x == 0) {   // the combine launch reads these instead of the header
+      p.lay_out[0] = s_lay.L;
+      p.lay_out[1] = s_lay.nbw;
+      p.lay_out[2] = s_lay.nq;
+    }
+  }
+  __syncthreads();
+  const Lay& y = s_lay;
+  const long long x_lo = (wg * y.C + y.NW - 1) / y.NW;
+  const long long x_hi = ((wg + 1) * y.C + y.NW - 1) / y.NW;
   // the warps whose ranges meet unit u are u NW / units .. ; partial slot = warp - first warp
-  auto slot_of = [&](int u) -> long long { return (long long)u * p.pslots + (wg - (int)((long long)u * p.NW / p.st.units)); };
+  auto slot_of = [&](int u) -> long long { return (long long)u * p.pslots + (wg - (int)((long long)u * y.NW / p.st.units)); };
   if (x_lo >= x_hi) {   // empty range: leave an empty partial in the unit it falls into
-    const int u = (int)(x_lo / p.Cu);
+    const int u = (int)(x_lo / y.Cu);
     if (u < p.st.units && lane < G) p.part_ml[slot_of(u) * G + lane] = make_float2(-INFINITY, 0.f);
     return;
   }
-  const int nbt = p.nbw * SUBT;
-  const int u_first = (int)(x_lo / p.Cu);
-  const int u_last = (int)((x_hi - 1) / p.Cu);
+  const int u_first = (int)(x_lo / y.Cu);
+  const int u_last = (int)((x_hi - 1) / y.Cu);
 
   uint8_t* stage_base = smem + (size_t)warp * NST * S::STAGE;
   if (lane == 0) {
@@ -340,34 +376,23 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   //      compacted out), then issues them one by one from shared memory
   BatchDesc* batch = batches[warp];
   int cu, ci;                        // cursor: first tile not yet described
-  first_tile(p, x_lo, nbt, cu, ci);
-  bool range_done = !(cu < p.st.units && tile_start(p, cu, ci, nbt) < x_hi);
+  first_tile(p, y, x_lo, cu, ci);
+  bool range_done = !(cu < p.st.units && tile_start(p, y, cu, ci) < x_hi);
   int bcount = 0, bnext = 0;
-  // each lane keeps the list entry of its tile of the next batch in flight (prefetch)
-  int lu, li;
-  bool linr;
-  int2 lent = make_int2(0, 0);
-  auto prefetch = [&]() {
-    lu = cu;
-    li = ci + lane;
-    while (li >= p.ntiles) { li -= p.ntiles; ++lu; }
-    linr = lu < p.st.units && tile_start(p, lu, li, nbt) < x_hi;
-    if (linr) lent = list_entry(p, lu, li, nbt, SUBT);
-  };
-  if (!range_done) prefetch();
   auto describe_batch = [&]() {
     while (!range_done) {
-      const int u = lu, i = li;
-      const bool inr = linr;
+      int u = cu, i = ci + lane;
+      while (i >= y.ntiles) { i -= y.ntiles; ++u; }
+      const bool inr = u < p.st.units && tile_start(p, y, u, i) < x_hi;
       TileDesc d;
       bool ok = false;
-      if (inr) ok = describe(p, u, i, nbt, lent, d);
+      if (inr) ok = describe(p, y, u, i, list_entry(p, y, u, i, SUBT), d);
       const unsigned vb = __ballot_sync(0xffffffffu, ok);
       if (ok) {
         BatchDesc bd;
         bd.src = tile_src(p, d, bd.bytes);
         bd.sd.u = u;
-        bd.sd.lse_off = (u * p.ntiles + i) * G;
+        bd.sd.lse_off = (u * y.ntiles + i) * G;
         bd.sd.meta = d.lo | (d.hi << 8) | (d.kind << 16);
         bd.sd.pad = 0;
         bd.pad = 0;
@@ -375,8 +400,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       }
       range_done = __any_sync(0xffffffffu, !inr);
       ci += BATCH;
-      while (ci >= p.ntiles) { ci -= p.ntiles; ++cu; }
-      if (!range_done) prefetch();
+      while (ci >= y.ntiles) { ci -= y.ntiles; ++cu; }
       bcount = __popc(vb);
       bnext = 0;
       __syncwarp();
@@ -408,7 +432,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
 
   // ---- consumer
   RunState<MC> rs;
-  float qf[KS][4];         // 2 q of head g/2 at channels 16ks + 2t, +1, +8, +9 (2-bit tiles)
+  unsigned long long qf[KS][2];   // q of head g/2 at channels (16ks + 2t, +1), (+8, +9), as fp32 pairs
   unsigned qb[KS][2];      // bf16 B fragments: q of head g/2 in even columns, 0 in odd ones
   int cur_u = u_first;
   int q_unit = -1;
@@ -479,10 +503,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       for (int ks = 0; ks < KS; ++ks) {
         const unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
         const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
-        qf[ks][0] = 2.f * bf16lo_to_f32(a0);
-        qf[ks][1] = 2.f * bf16hi_to_f32(a0);
-        qf[ks][2] = 2.f * bf16lo_to_f32(a1);
-        qf[ks][3] = 2.f * bf16hi_to_f32(a1);
+        qf[ks][0] = f2_pack(bf16lo_to_f32(a0), bf16hi_to_f32(a0));
+        qf[ks][1] = f2_pack(bf16lo_to_f32(a1), bf16hi_to_f32(a1));
         qb[ks][0] = lo_col ? 0u : a0;
         qb[ks][1] = lo_col ? 0u : a1;
       }
@@ -510,26 +532,26 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
       const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
       // B fragments 2 q s_K in f16: trunc part in even columns, remainder in odd ones; bias q . z_K
+      // (the codes arrive as code / 2: the logit scale below carries the factor 2)
       unsigned qp[KS][2];
-      float bpart = 0.f;
+      unsigned long long bp2 = 0ull;
       const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
-        const float4 sc = *reinterpret_cast<const float4*>(kscale + ks * 16 + t * 4);
-        const float4 zc = *reinterpret_cast<const float4*>(kmin + ks * 16 + t * 4);
-        bpart = fmaf(qf[ks][0], zc.x, bpart);
-        bpart = fmaf(qf[ks][1], zc.y, bpart);
-        bpart = fmaf(qf[ks][2], zc.z, bpart);
-        bpart = fmaf(qf[ks][3], zc.w, bpart);
-        float y[4] = {qf[ks][0] * sc.x, qf[ks][1] * sc.y, qf[ks][2] * sc.z, qf[ks][3] * sc.w};
-#pragma unroll
-        for (int i = 0; i < 4; ++i) y[i] -= __uint_as_float(__float_as_uint(y[i]) & keep);
-        qp[ks][0] = pack_f16x2_rz(y[0], y[1]);
-        qp[ks][1] = pack_f16x2_rz(y[2], y[3]);
+        const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
+        const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
+        bp2 = f2_fma(qf[ks][0], zc.x, bp2);
+        bp2 = f2_fma(qf[ks][1], zc.y, bp2);
+        const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
+        const unsigned long long k2 = ((unsigned long long)keep << 32) | keep;
+        const unsigned long long r01 = f2_sub(y01, y01 & k2), r23 = f2_sub(y23, y23 & k2);
+        qp[ks][0] = pack_f16x2_rz(f2_lo(r01), f2_hi(r01));
+        qp[ks][1] = pack_f16x2_rz(f2_lo(r23), f2_hi(r23));
       }
+      float bpart = f2_lo(bp2) + f2_hi(bp2);
       bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
       bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-      const float bias = 0.5f * __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . z_K of head t
+      const float bias = 0.5f * __shfl_sync(0xffffffffu, bpart, 8 * t);   // half of q . z_K of head t
       float vz[2 * MT], vs[2 * MT];
       load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
       load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
@@ -553,8 +575,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         }
       }
       unsigned Bp[MT][2];
-      softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, p.scale_log2, rs, Bp, lse_out, G,
-                                    lane);
+      softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 2.f * p.scale_log2, rs, Bp, lse_out,
+                                    G, lane);
       // P V over the unpacked value codes (A = V^T: channel tiles x token steps)
       {
         unsigned wv[WPL];
@@ -598,9 +620,9 @@ constexpr int COMBINE_THREADS = 128;
 constexpr int MAXP = COMBINE_MAXP;
 
 // partial slots of unit u: one per warp whose position range meets [u Cu, (u+1) Cu)
-__device__ __forceinline__ int unit_partials(const CombineParams& p, int u) {
+__device__ __forceinline__ int unit_partials(const CombineParams& p, const Lay& y, int u) {
   const long long w0 = (long long)u * p.NW / p.st.units;
-  const long long w1 = (((long long)u + 1) * p.Cu - 1) * p.NW / p.C;
+  const long long w1 = (((long long)u + 1) * y.Cu - 1) * p.NW / y.C;
   int np = (int)(w1 - w0 + 1);
   if (np > p.pslots) np = p.pslots;
   return np;
@@ -645,7 +667,17 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
   __shared__ float s_sc[MAXP];
   __shared__ float s_inv[4], s_lse[4];
   const int tid = threadIdx.x, warp = tid >> 5;
-  const int np = unit_partials(p, u);
+  Lay y;   // the counts the attention launch used (its length includes the pending token)
+  y.L = p.lay_in[0];
+  y.nbw = p.lay_in[1];
+  y.nq = p.lay_in[2];
+  y.nbt = y.nbw * (p.st.geo.W / 16);
+  y.ntiles = y.nbt + y.nq;
+  y.Cu = (long long)y.nbt * p.cb + (long long)y.nq * p.cq;
+  y.C = y.Cu * p.st.units;
+  y.NW = p.NW;
+  const int np = unit_partials(p, y, u);
+  if (u == 0 && part == 0 && threadIdx.x == 0) p.st.ldev[p.layer].L = y.L;   // commit the length
   if (part < G) {
     // ---- output of head h = part
     const int h = part;
@@ -683,7 +715,7 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
   }
   __syncthreads();
   const int W = p.st.geo.W, sub_tiles = W / 16;
-  const int nent = p.nbw + p.nq;
+  const int nent = y.nbw + y.nq;
   constexpr int EPT = 4;   // entries per thread per round: their loads are issued together
   for (int e0 = tid; e0 < nent; e0 += COMBINE_THREADS * EPT) {
     int2 ent[EPT];
@@ -691,8 +723,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
     for (int j = 0; j < EPT; ++j) {
       const int e = e0 + j * COMBINE_THREADS;
       ent[j] = make_int2(-1, -1);
-      if (e < p.nbw) ent[j] = p.st.blist[gu * p.st.capb + e];
-      else if (e < nent) ent[j] = p.st.qlist[gu * p.st.capq + (e - p.nbw)];
+      if (e < y.nbw) ent[j] = p.st.blist[gu * p.st.capb + e];
+      else if (e < nent) ent[j] = p.st.qlist[gu * p.st.capq + (e - y.nbw)];
     }
     float dS[EPT];
     int win[EPT];
@@ -702,18 +734,18 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
       win[j] = ent[j].x;
       dS[j] = 0.f;
       if (e >= nent || win[j] < 0) continue;
-      if (e < p.nbw) {
+      if (e < y.nbw) {
         const int lo = (win[j] == 0) ? p.st.n_sink : 0;
-        int hi = p.L - win[j] * W;
+        int hi = y.L - win[j] * W;
         hi = hi < W ? hi : W;
         for (int s = 0; s < sub_tiles; ++s) {
           const int tl = lo - 16 * s, th = hi - 16 * s;
           if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
-          const float* ls = p.lse + ((size_t)u * p.ntiles + e * sub_tiles + s) * G;
+          const float* ls = p.lse + ((size_t)u * y.ntiles + e * sub_tiles + s) * G;
           for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
         }
       } else {
-        const float* ls = p.lse + ((size_t)u * p.ntiles + p.nbw * sub_tiles + (e - p.nbw)) * G;
+        const float* ls = p.lse + ((size_t)u * y.ntiles + y.nbw * sub_tiles + (e - y.nbw)) * G;
         for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
       }
     }
@@ -733,18 +765,32 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
 
 // ------------------------------------------------------------------------------ launchers
 template <int D, int W>
-static cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t stream) {
+static size_t attn_smem_bytes() {
   using S = Shape<D, W>;
-  const size_t smem = (size_t)ATTN_WARPS * S::NST * S::STAGE;
-  static bool attr_set = false;
-  if (!attr_set) {
-    cudaError_t e = cudaFuncSetAttribute(qe_decode_attn_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (int)smem);
-    if (e != cudaSuccess) return e;
-    attr_set = true;
-  }
-  qe_decode_attn_kernel<D, W><<<grid, ATTN_WARPS * 32, smem, stream>>>(p);
+  return (size_t)ATTN_WARPS * S::NST * S::STAGE;
+}
+
+template <int D, int W>
+static cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t stream) {
+  qe_decode_attn_kernel<D, W><<<grid, ATTN_WARPS * 32, attn_smem_bytes<D, W>(), stream>>>(p);
   return cudaGetLastError();
+}
+
+template <int D, int W>
+static cudaError_t prepare_attn_t() {
+  return cudaFuncSetAttribute(qe_decode_attn_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)attn_smem_bytes<D, W>());
+}
+
+// kernel attributes, set once (outside any stream capture)
+cudaError_t prepare_attn_kernels(int D, int W) {
+  if (D == 128 && W == 32) return prepare_attn_t<128, 32>();
+  if (D == 128 && W == 16) return prepare_attn_t<128, 16>();
+  if (D == 128 && W == 64) return prepare_attn_t<128, 64>();
+  if (D == 64 && W == 16) return prepare_attn_t<64, 16>();
+  if (D == 64 && W == 32) return prepare_attn_t<64, 32>();
+  if (D == 64 && W == 64) return prepare_attn_t<64, 64>();
+  return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t stream) {
@@ -766,5 +812,13 @@ cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream) {
 }
 
 int attn_warps_per_cta() { return ATTN_WARPS; }
+
+// Persistent grid: one CTA per SM, but few enough warps that a unit meets at most pslots - 2
+// warp ranges.
+int attn_grid(int n_sm, int units, int pslots) {
+  long long g = ((long long)(pslots - 2) * units) / ATTN_WARPS;
+  if (g > n_sm) g = n_sm;
+  return g < 1 ? 1 : (int)g;
+}
 
 }  // namespace qe

@@ -30,7 +30,8 @@ namespace qe {
 
 enum : int { TIER_NONE = 0, TIER_PINNED = 1, TIER_FULL = 2, TIER_QUANT = 3, TIER_EVICTED = 4 };
 
-enum : unsigned { ERR_FREELIST = 1u, ERR_TABLE = 2u, ERR_TIMEOUT = 4u, ERR_COUNT = 8u, ERR_MOVES = 16u };
+enum : unsigned { ERR_FREELIST = 1u, ERR_TABLE = 2u, ERR_TIMEOUT = 4u, ERR_COUNT = 8u, ERR_MOVES = 16u,
+                  ERR_CAPACITY = 32u };
 
 // ---------------------------------------------------------------------------- geometry
 struct Geo {
@@ -101,6 +102,25 @@ QE_HD int vparam_pos(const Geo& g, int r) {
 }
 
 // ---------------------------------------------------------------------------- cache state
+// Per-layer dynamic state, resident on the device and updated by the kernels themselves, so
+// that every launch has step-invariant arguments (a decode step can be captured once in a CUDA
+// graph and replayed).  All sequences of a layer share these counts.
+struct LayerDev {
+  int L;             // tokens per sequence
+  int routed_upto;   // windows [0, routed_upto) have entered the candidate pool
+  int n_full;        // Full windows per unit
+  int n_quant;       // Quantized windows per unit
+  int kf, kq;        // capacities at the last routing event
+  unsigned done;     // blocks finished in the kernel that updates this header (last one commits)
+  int pad;
+};
+
+// Capacity rule (see qe.h)
+struct CapCfg {
+  int mode, kf, kq;
+  double frac_bf16, frac_int2, budget_frac;
+};
+
 // Arrays are indexed by the global unit gu = layer * units + (b * n_kv_heads + kvh).
 struct State {
   int units;          // per layer
@@ -125,7 +145,52 @@ struct State {
   uint8_t* hledger;   // device pointer to pinned host [GU][caps][qslot_bytes]
   unsigned* err;      // sticky flag
   unsigned long long* stats;  // [layers][5]
+  LayerDev* ldev;     // [layers]
+  CapCfg cap;
+  int max_context;
 };
+
+// Capacity rule in double precision, operations in the order qe.h states, each rounded once
+// (no fused multiply-add), so host, device and the reference give identical window counts.
+QE_HD int qslot_bytes_of(int W, int D) { return 2 * (W * D / 4) + 8 * D + 8 * W; }
+#if defined(__CUDA_ARCH__)
+#define QE_DMUL(a, b) __dmul_rn((a), (b))
+#define QE_DSUB(a, b) __dsub_rn((a), (b))
+#define QE_DDIV(a, b) __ddiv_rn((a), (b))
+#else
+#define QE_DMUL(a, b) ((a) * (b))
+#define QE_DSUB(a, b) ((a) - (b))
+#define QE_DDIV(a, b) ((a) / (b))
+#endif
+QE_HD void capacities_at(const CapCfg& c, int n_sink, int n_recent, int W, int D, int L, int& kf, int& kq) {
+  if (c.mode == 0) {
+    kf = c.kf;
+    kq = c.kq;
+    return;
+  }
+  const double f = floor(QE_DDIV(QE_DSUB(QE_DSUB(QE_DMUL(c.frac_bf16, (double)L), (double)n_sink), (double)n_recent),
+                                 (double)W));
+  kf = f < 0 ? 0 : (int)f;
+  double q;
+  if (c.mode == 1) q = floor(QE_DDIV(QE_DMUL(c.frac_int2, (double)L), (double)W));
+  else
+    q = floor(QE_DDIV(QE_DMUL(QE_DMUL(QE_DSUB(c.budget_frac, c.frac_bf16), (double)L), 4.0 * D),
+                      (double)qslot_bytes_of(W, D)));
+  kq = q < 0 ? 0 : (int)q;
+}
+
+// Derived counts of one layer (identical on every thread that reads the same header).
+struct LayerView {
+  int L, nwin, nbw, nq;
+};
+QE_HD LayerView layer_view(const Geo& g, const LayerDev& h) {
+  LayerView v;
+  v.L = h.L;
+  v.nwin = (h.L + g.W - 1) / g.W;
+  v.nbw = 1 + h.n_full + (v.nwin - h.routed_upto);   // sink + Full + Pinned windows
+  v.nq = h.n_quant;
+  return v;
+}
 
 // ---------------------------------------------------------------------------- PTX helpers
 #if defined(__CUDACC__)
@@ -201,6 +266,27 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1,
 __device__ __forceinline__ unsigned pack_bf16x2_rz(float lo, float hi) {
   unsigned d;
   asm("cvt.rz.bf16x2.f32 %0, %1, %2;" : "=r"(d) : "f"(hi), "f"(lo));
+  return d;
+}
+// packed fp32 pair arithmetic (one instruction for two lanes' worth of values)
+__device__ __forceinline__ unsigned long long f2_pack(float a, float b) {
+  return (unsigned long long)__float_as_uint(a) | ((unsigned long long)__float_as_uint(b) << 32);
+}
+__device__ __forceinline__ float f2_lo(unsigned long long x) { return __uint_as_float((unsigned)x); }
+__device__ __forceinline__ float f2_hi(unsigned long long x) { return __uint_as_float((unsigned)(x >> 32)); }
+__device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("mul.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
+  unsigned long long d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 // f16x2 with round-toward-zero: lo -> low half

@@ -22,6 +22,7 @@ namespace {
 
 struct LayerMirror {
   int L = 0;
+  int pending = 0;    // single-token appends whose length the device has not committed yet
   int routed_upto = 0;
   int n_full = 0;
   int n_quant = 0;
@@ -45,7 +46,9 @@ struct qe_handle_s {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   float* lse = nullptr;
+  int* lay_buf = nullptr;     // [n_layers][4] counts handed from attention to combine
   int pslots_cap = 0;         // partial slots per unit
+  int attn_grid = 0;          // CTAs of every attention launch (fixed)
   int ntiles_cap = 0;
   // moves
   qe::Move* moves = nullptr;
@@ -93,19 +96,10 @@ int ceil_div(long long a, long long b) { return (int)((a + b - 1) / b); }
 
 int qslot_bytes(int w, int d) { return 2 * (w * d / 4) + 8 * d + 8 * w; }
 
-// Capacity rule, see qe.h (evaluated in double in the order written there)
+// Capacity rule, see qe.h (qe::capacities_at: double precision, no fused operations)
 void capacities(const qe_config& c, int L, int& kf, int& kq) {
-  if (c.cap_mode == 0) {
-    kf = c.kf;
-    kq = c.kq;
-    return;
-  }
-  double f = std::floor((c.frac_bf16 * L - c.n_sink - c.n_recent) / c.window);
-  kf = f < 0 ? 0 : (int)f;
-  double q;
-  if (c.cap_mode == 1) q = std::floor(c.frac_int2 * L / c.window);
-  else q = std::floor((c.budget_frac - c.frac_bf16) * L * (4.0 * c.head_dim) / qslot_bytes(c.window, c.head_dim));
-  kq = q < 0 ? 0 : (int)q;
+  qe::CapCfg cc{c.cap_mode, c.kf, c.kq, c.frac_bf16, c.frac_int2, c.budget_frac};
+  qe::capacities_at(cc, c.n_sink, c.n_recent, c.window, c.head_dim, L, kf, kq);
 }
 
 template <class T>
@@ -132,6 +126,18 @@ qe_status ensure_stage(qe_handle h, int i, size_t bytes) {
   return QE_OK;
 }
 
+void fill_info(qe_handle h, const LayerMirror& m, qe_layer_info* info);
+
+// a single-token append that no decode step consumed: advance the device length now
+qe_status commit_pending(qe_handle h, int layer) {
+  LayerMirror& m = h->lay[layer];
+  if (!m.pending) return QE_OK;
+  QE_CK(h, qe::launch_commit_length(h->st, layer, m.pending, h->stream));
+  ++h->launches;
+  m.pending = 0;
+  return QE_OK;
+}
+
 int nbw_of(const qe_handle h, const LayerMirror& m) {
   const int nwin = ceil_div(m.L, h->cfg.window);
   return 1 + m.n_full + (nwin - m.routed_upto);
@@ -140,8 +146,9 @@ int nbw_of(const qe_handle h, const LayerMirror& m) {
 void free_all(qe_handle h) {
   qe::State& s = h->st;
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_top, s.qfree,
-                  s.qfree_top, s.sfree, s.sfree_top, s.bslab, s.qslab, s.err, s.stats, h->part_o, h->part_ml,
-                  h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3]};
+                  s.qfree_top, s.sfree, s.sfree_top, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
+                  h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
+                  h->lay_buf};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -208,6 +215,8 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   st.Hkv = c.n_kv_heads;
   st.geo.D = c.head_dim;
   st.geo.W = c.window;
+  st.cap = qe::CapCfg{c.cap_mode, c.kf, c.kq, c.frac_bf16, c.frac_int2, c.budget_frac};
+  st.max_context = c.max_context;
   h->lay.assign(c.n_layers, LayerMirror{});
 
   const long long GU = h->gu_total;
@@ -238,16 +247,19 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(st.qslab, GU * st.capq * qslot_b, "2-bit window pool");
   QE_ALLOC(st.err, 1, "error flag");
   QE_ALLOC(st.stats, (size_t)c.n_layers * 5, "stats");
+  QE_ALLOC(st.ldev, (size_t)c.n_layers, "layer headers");
 
   // split-K scratch: one CTA per SM, attn_warps_per_cta() warps each; a unit meets at most
   // NW / units + 2 warp ranges
   const int NW = h->n_sm * qe::attn_warps_per_cta();
   h->pslots_cap = NW / h->units + 3;
   if (h->pslots_cap > qe::COMBINE_MAXP) h->pslots_cap = qe::COMBINE_MAXP;
+  h->attn_grid = qe::attn_grid(h->n_sm, h->units, h->pslots_cap);
   h->ntiles_cap = st.capb * (c.window / 16) + st.capq;
   QE_ALLOC(h->part_o, (size_t)h->units * h->pslots_cap * G * c.head_dim, "partials");
   QE_ALLOC(h->part_ml, (size_t)h->units * h->pslots_cap * G, "partial stats");
   QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
+  QE_ALLOC(h->lay_buf, (size_t)c.n_layers * 4, "layer counts");
   h->max_moves = h->units * st.caps + 16;
   {
     void* mp = nullptr;
@@ -290,6 +302,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   set(cudaMemsetAsync(st.qslab, 0, GU * st.capq * qslot_b, h->stream));
   set(cudaMemsetAsync(st.err, 0, 4, h->stream));
   set(cudaMemsetAsync(st.stats, 0, (size_t)c.n_layers * 5 * 8, h->stream));
+  set(cudaMemsetAsync(st.ldev, 0, (size_t)c.n_layers * sizeof(qe::LayerDev), h->stream));
   {
     std::vector<int> tmp;
     tmp.resize((size_t)GU * st.capb);
@@ -314,6 +327,8 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
     for (long long gu = 0; gu < GU; ++gu) bl[gu * st.capb] = make_int2(-1, 0);
     set(cudaMemcpy(st.blist, bl.data(), bl.size() * sizeof(int2), cudaMemcpyHostToDevice));
   }
+  set(qe::prepare_attn_kernels(c.head_dim, c.window));
+  set(qe::prepare_route_kernels(st));
   set(cudaStreamSynchronize(h->stream));
   if (ie != cudaSuccess) {
     std::string m = std::string("initialising the cache: ") + cudaGetErrorString(ie);
@@ -352,14 +367,10 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
     kd = static_cast<const uint16_t*>(h->stage[0]);
     vd = static_cast<const uint16_t*>(h->stage[1]);
   }
-  const int w_old = ceil_div(m.L, h->cfg.window), w_new = ceil_div(m.L + n_tokens, h->cfg.window);
-  if (w_new > w_old) {
-    const int nbw_old = nbw_of(h, m);
-    QE_CK(h, qe::launch_open_windows(h->st, layer, w_old, w_new, nbw_old, h->stream));
-    ++h->launches;
-  }
-  QE_CK(h, qe::launch_append(h->st, layer, m.L, n_tokens, kd, vd, h->n_sm, h->stream));
-  ++h->launches;
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
+  QE_CK(h, qe::launch_append(h->st, layer, n_tokens, kd, vd, h->n_sm, h->stream));
+  h->launches += n_tokens == 1 ? 1 : 2;
+  if (n_tokens == 1) m.pending = 1;   // counted by the next decode step, committed by its combine
   m.L += n_tokens;
   return QE_OK;
 }
@@ -385,37 +396,23 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   qe::AttnParams p{};
   p.st = h->st;
   p.layer = layer;
-  p.L = m.L;
-  p.nbw = nbw_of(h, m);
-  p.nq = m.n_quant;
+  p.pend = m.pending;
+  p.lay_out = h->lay_buf + 4 * layer;
+  m.pending = 0;
   p.cb = h->cost_b;
   p.cq = h->cost_q;
-  const int sub = c.window / 16;
-  p.ntiles = p.nbw * sub + p.nq;
-  if (p.ntiles > h->ntiles_cap) return fail(h, QE_ERR_CAPACITY, "tile count %d exceeds %d", p.ntiles, h->ntiles_cap);
-  p.Cu = (long long)p.nbw * sub * p.cb + (long long)p.nq * p.cq;
-  p.C = p.Cu * h->units;
-  // warps: at most one per SM slot, at most one per tile, and few enough that a unit never
-  // meets more warp ranges than it has partial slots
-  const int wpc = qe::attn_warps_per_cta();
-  long long nw = (long long)h->n_sm * wpc;
-  const long long tiles_total = (long long)p.ntiles * h->units;
-  if (nw > tiles_total) nw = tiles_total;
-  if (nw > (long long)(h->pslots_cap - 2) * h->units) nw = (long long)(h->pslots_cap - 2) * h->units;
-  int grid = ceil_div(nw, wpc);
-  if (grid < 1) grid = 1;
-  p.NW = grid * wpc;
-  if ((long long)p.NW > (long long)(h->pslots_cap - 2) * h->units) {
-    grid = (int)(((long long)(h->pslots_cap - 2) * h->units) / wpc);
-    if (grid < 1) return fail(h, QE_ERR_CAPACITY, "too few partial slots for one CTA");
-    p.NW = grid * wpc;
-  }
   p.pslots = h->pslots_cap;
   p.q = qd;
   p.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
   p.part_o = h->part_o;
   p.part_ml = h->part_ml;
   p.lse = h->lse;
+  {
+    const int sub = c.window / 16;
+    const int ntiles = nbw_of(h, m) * sub + m.n_quant;
+    if (ntiles > h->ntiles_cap) return fail(h, QE_ERR_CAPACITY, "tile count %d exceeds %d", ntiles, h->ntiles_cap);
+  }
+  const int grid = h->attn_grid;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
   if (h->timing) {
     while (h->ev_pool.size() < h->ev_used + 2) {
@@ -434,21 +431,16 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
     QE_CK(h, cudaEventRecord(e1, h->stream));
     h->timed_launches += 1;
     qe_layer_info info;
-    qe_get_layer_info(h, layer, &info);
+    fill_info(h, m, &info);   // host shadow: no synchronisation inside the timed path
     h->timed_bytes += info.attn_bytes;
   }
   qe::CombineParams cp{};
   cp.st = h->st;
   cp.layer = layer;
-  cp.L = m.L;
-  cp.nbw = p.nbw;
-  cp.nq = p.nq;
-  cp.ntiles = p.ntiles;
+  cp.lay_in = h->lay_buf + 4 * layer;
   cp.cb = p.cb;
   cp.cq = p.cq;
-  cp.Cu = p.Cu;
-  cp.C = p.C;
-  cp.NW = p.NW;
+  cp.NW = grid * qe::attn_warps_per_cta();
   cp.pslots = p.pslots;
   cp.part_o = h->part_o;
   cp.part_ml = h->part_ml;
@@ -462,9 +454,10 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
 }
 
 static qe_status route_layer(qe_handle h, int layer) {
+  qe_status s0 = commit_pending(h, layer);
+  if (s0 != QE_OK) return s0;
   LayerMirror& m = h->lay[layer];
   const qe_config& c = h->cfg;
-  const int nwin = ceil_div(m.L, c.window);
   int aged = (m.L - c.n_recent) >= 0 ? (m.L - c.n_recent) / c.window : 0;
   if (aged < m.routed_upto) aged = m.routed_upto;
   int kf, kq;
@@ -477,14 +470,6 @@ static qe_status route_layer(qe_handle h, int layer) {
   qe::RouteParams p{};
   p.st = h->st;
   p.layer = layer;
-  p.L = m.L;
-  p.n_windows = nwin;
-  p.routed_old = m.routed_upto;
-  p.aged_upto = aged;
-  p.kf = kf;
-  p.kq = kq;
-  p.exp_nfull = nf;
-  p.exp_nquant = nq;
   p.moves = h->moves;
   p.n_moves = h->n_moves;
   p.max_moves = h->max_moves;
@@ -526,11 +511,10 @@ qe_status qe_synchronize(qe_handle h) {
   return QE_OK;
 }
 
-qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
-  qe_status s = check_layer(h, layer);
-  if (s != QE_OK) return s;
-  if (!info) return fail(h, QE_ERR_INVALID_ARG, "null info");
-  const LayerMirror& m = h->lay[layer];
+}  // extern "C"
+
+namespace {
+void fill_info(qe_handle h, const LayerMirror& m, qe_layer_info* info) {
   const qe_config& c = h->cfg;
   info->length = m.L;
   info->n_windows = ceil_div(m.L, c.window);
@@ -542,23 +526,47 @@ qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
   info->kq = m.kq;
   info->max_windows = h->st.maxw;
   info->units = h->units;
-  // bf16 tokens actually present: sink + Full windows (complete) + Pinned windows (window 0
-  // and the current window partial)
+  // bf16 tokens present: sink + Full windows (complete) + Pinned windows (window 0 and the
+  // current window partial).  A Full window 0 holds w - n_sink tokens; counting it as w
+  // overstates the bytes by at most n_sink tokens per unit.
   double tok = std::min(c.n_sink, m.L);
   tok += (double)m.n_full * c.window;
   for (int j = m.routed_upto; j < info->n_windows; ++j) {
-    int lo = j == 0 ? c.n_sink : 0;
-    int hi = std::min(c.window, m.L - j * c.window);
+    const int lo = j == 0 ? c.n_sink : 0;
+    const int hi = std::min(c.window, m.L - j * c.window);
     if (hi > lo) tok += hi - lo;
   }
-  // a Full window 0 holds w - n_sink tokens; the correction is below one window per unit
   info->attn_bytes = (tok * 4.0 * c.head_dim + (double)m.n_quant * qslot_bytes(c.window, c.head_dim)) * h->units;
+}
+}  // namespace
+
+extern "C" {
+
+qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
+  if (!info) return fail(h, QE_ERR_INVALID_ARG, "null info");
+  // the device header is authoritative (it also advances under CUDA-graph replays)
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  qe::LayerDev d{};
+  QE_CK(h, cudaMemcpy(&d, h->st.ldev + layer, sizeof d, cudaMemcpyDeviceToHost));
+  LayerMirror m;
+  m.L = d.L;
+  m.routed_upto = d.routed_upto;
+  m.n_full = d.n_full;
+  m.n_quant = d.n_quant;
+  m.kf = d.kf;
+  m.kq = d.kq;
+  h->lay[layer] = m;   // resynchronise the host shadow
+  fill_info(h, m, info);
   return QE_OK;
 }
 
 qe_status qe_get_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes) {
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
   const size_t need = (size_t)h->units * h->st.maxw;
   if (!host || bytes < need) return fail(h, QE_ERR_INVALID_ARG, "tier buffer needs %zu bytes", need);
   QE_CK(h, cudaStreamSynchronize(h->stream));
@@ -569,6 +577,7 @@ qe_status qe_get_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes) {
 qe_status qe_get_scores(qe_handle h, int layer, float* host, size_t bytes) {
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
   const size_t n = (size_t)h->units * h->st.maxw;
   if (!host || bytes < n * 4) return fail(h, QE_ERR_INVALID_ARG, "score buffer needs %zu bytes", n * 4);
   QE_CK(h, cudaStreamSynchronize(h->stream));
@@ -579,6 +588,7 @@ qe_status qe_get_scores(qe_handle h, int layer, float* host, size_t bytes) {
 qe_status qe_set_scores(qe_handle h, int layer, const float* host, size_t bytes) {
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
   const size_t n = (size_t)h->units * h->st.maxw;
   if (!host || bytes < n * 4) return fail(h, QE_ERR_INVALID_ARG, "score buffer needs %zu bytes", n * 4);
   QE_CK(h, cudaStreamSynchronize(h->stream));

@@ -8,19 +8,16 @@
 
 namespace qe {
 
-// qe_decode_attn: one layer, all units; see qe_attn.cu
+// qe_decode_attn: one layer, all units; see qe_attn.cu.  Step-dependent counts come from the
+// device-resident layer header; every field here is fixed for the handle's lifetime except
+// the buffers, which the caller may keep fixed too.
 struct AttnParams {
   State st;
   int layer;
-  int L;                 // tokens per sequence (after this step's append)
-  int nbw;               // bf16 window entries per unit (sink included)
-  int nq;                // 2-bit windows per unit
+  int pend;              // single-token appends not yet counted in the header's length (0 or 1)
+  int* lay_out;          // [4]: length, bf16 entries, 2-bit entries, tiles per unit, for the combine
   int cb, cq;            // cost of one 16-token bf16 tile and of one 2-bit window
-  long long Cu;          // cost of one unit
-  long long C;           // cost of the layer
-  int NW;                // warps in the grid
   int pslots;            // partial slots per unit (>= warps whose range meets one unit)
-  int ntiles;            // tiles per unit = nbw * w/16 + nq
   const uint16_t* q;     // [B][Hq][D] bf16
   float scale_log2;      // log2(e) / sqrt(d)
   float* part_o;         // [units][pslots][G][D] unnormalised output
@@ -32,11 +29,9 @@ struct AttnParams {
 struct CombineParams {
   State st;
   int layer;
-  int L;
-  int nbw, nq, ntiles;
+  const int* lay_in;     // written by the attention launch; the combine commits the length
   int cb, cq;
-  long long Cu, C;
-  int NW, pslots;
+  int NW, pslots;        // warps of the attention launch, partial slots per unit
   const float* part_o;
   const float2* part_ml;
   const float* lse;
@@ -59,24 +54,21 @@ struct Move {
 struct RouteParams {
   State st;
   int layer;
-  int L;
-  int n_windows;     // windows reached
-  int routed_old;    // windows [0, routed_old) entered the pool at earlier events
-  int aged_upto;     // windows [0, aged_upto) are complete and older than the recent region
-  int kf, kq;
-  int exp_nfull, exp_nquant;   // host mirror of the per-unit counts after this event
   Move* moves;
   int* n_moves;
   int max_moves;
 };
 
 cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t stream);
+int attn_grid(int n_sm, int units, int pslots);
+cudaError_t prepare_attn_kernels(int D, int W);
+cudaError_t prepare_route_kernels(const State& st);
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream);
 int attn_warps_per_cta();
-cudaError_t launch_open_windows(const State& st, int layer, int w_old, int w_new, int nbw_old, cudaStream_t s);
-cudaError_t launch_append(const State& st, int layer, int pos0, int n, const uint16_t* k, const uint16_t* v,
-                          int n_sm, cudaStream_t s);
+cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
+                          cudaStream_t s);
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t s);
 cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves, int n_sm, cudaStream_t s);
 
 }  // namespace qe

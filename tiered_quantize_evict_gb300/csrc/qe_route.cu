@@ -15,32 +15,112 @@
 namespace qe {
 
 // ------------------------------------------------------------------------------ append
-// Open windows [w_old, w_new) of every unit of one layer: pop a bf16 slot, Pinned, score 0,
-// append the entry to the bf16 tile list.  One thread per unit.
-__global__ void qe_open_windows_kernel(State st, int layer, int w_old, int w_new, int nbw_old) {
-  const int u = blockIdx.x * blockDim.x + threadIdx.x;
-  if (u >= st.units) return;
-  const long long gu = (long long)layer * st.units + u;
-  int top = st.bfree_top[gu];
-  int nb = nbw_old;
-  for (int j = w_old; j < w_new; ++j) {
-    if (top <= 0 || nb >= st.capb) { atomicOr(st.err, ERR_FREELIST); break; }
-    const int s = st.bfree[gu * st.capb + (--top)];
-    st.bslot[gu * st.maxw + j] = s;
-    st.tier[gu * st.maxw + j] = TIER_PINNED;
-    st.score[gu * st.maxw + j] = 0.f;
-    st.blist[gu * st.capb + nb] = make_int2(j, s);
-    ++nb;
+// Every append kernel reads the layer's length from the device header and the last CTA to
+// finish commits the new length, so the launch arguments never change from step to step.
+__device__ __forceinline__ void commit_length(const State& st, int layer, int L_new) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    LayerDev* h = st.ldev + layer;
+    if (atomicAdd(&h->done, 1u) == gridDim.x - 1) {
+      h->L = L_new;
+      h->done = 0;
+      __threadfence();
+    }
   }
-  st.bfree_top[gu] = top;
 }
 
-// Copy n new tokens (positions [pos0, pos0+n)) of K and V into their window slots in
-// fragment order.  Thread per (unit, token, channel pair).  Sink positions go to the sink
-// slot (slot 0); window 0 keeps them masked.
-__global__ void qe_append_kernel(State st, int layer, int pos0, int n, const uint16_t* __restrict__ k,
+// open window j of unit gu: pop a bf16 slot, Pinned, score 0, entry `nb` of the bf16 list
+__device__ __forceinline__ int open_window(const State& st, long long gu, int j, int nb) {
+  int top = st.bfree_top[gu];
+  if (top <= 0 || nb >= st.capb) {
+    atomicOr(st.err, ERR_FREELIST);
+    return -1;
+  }
+  const int s = st.bfree[gu * st.capb + (--top)];
+  st.bfree_top[gu] = top;
+  st.bslot[gu * st.maxw + j] = s;
+  st.tier[gu * st.maxw + j] = TIER_PINNED;
+  st.score[gu * st.maxw + j] = 0.f;
+  st.blist[gu * st.capb + nb] = make_int2(j, s);
+  return s;
+}
+
+__device__ __forceinline__ void write_token(const State& st, long long gu, int slot, int row, int c, unsigned kk,
+                                            uint16_t v0, uint16_t v1) {
+  uint8_t* base = st.bslab + (gu * st.capb + slot) * (long long)st.geo.bslot_bytes();
+  *reinterpret_cast<unsigned*>(base + bf16_k_off(st.geo, row, c)) = kk;
+  *reinterpret_cast<uint16_t*>(base + bf16_v_off(st.geo, row, c)) = v0;
+  *reinterpret_cast<uint16_t*>(base + bf16_v_off(st.geo, row, c + 1)) = v1;
+}
+
+// One decode token: APPEND1_UNITS units per CTA, one thread per channel pair.  The token that
+// starts a window opens it (QEvict notes §2 Figure 1: every window starts in full precision).
+// The length is not advanced here: the next decode step counts this token as pending and its
+// combine launch commits the new length (see qe_decode_step), so the launch stays step-invariant.
+constexpr int APPEND1_UNITS = 2;
+__global__ void qe_append1_kernel(State st, int layer, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v) {
+  __shared__ int s_slot[APPEND1_UNITS];
+  const LayerDev hd = st.ldev[layer];
+  const int L = hd.L, W = st.geo.W, D = st.geo.D;
+  if (L + 1 > st.max_context) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) atomicOr(st.err, ERR_CAPACITY);
+    return;
+  }
+  const int j = L / W;
+  const int u0 = blockIdx.x * APPEND1_UNITS;
+  if (threadIdx.x < APPEND1_UNITS && u0 + (int)threadIdx.x < st.units) {
+    const long long gu = (long long)layer * st.units + u0 + threadIdx.x;
+    int slot;
+    if (L % W == 0) slot = open_window(st, gu, j, 1 + hd.n_full + (j - hd.routed_upto));
+    else slot = st.bslot[gu * st.maxw + j];
+    if (L < st.n_sink) slot = 0;
+    s_slot[threadIdx.x] = slot;
+  }
+  __syncthreads();
+  const int row = L < st.n_sink ? L : L - j * W;
+  const int ul = threadIdx.x / (D / 2), c = 2 * (threadIdx.x % (D / 2));
+  const int u = u0 + ul;
+  if (ul >= APPEND1_UNITS || u >= st.units) return;
+  const int slot = s_slot[ul];
+  if (slot < 0 || slot >= st.capb || (slot == 0 && L >= st.n_sink)) {
+    atomicOr(st.err, ERR_TABLE);
+    return;
+  }
+  const long long gu = (long long)layer * st.units + u;
+  const size_t src = (size_t)u * D + c;
+  write_token(st, gu, slot, row, c, *reinterpret_cast<const unsigned*>(k + src), v[src], v[src + 1]);
+}
+
+// Advance the committed length of a layer by n (a single-token append that no decode step
+// consumed).
+__global__ void qe_commit_length_kernel(State st, int layer, int n) { st.ldev[layer].L += n; }
+
+// Prefill part 1: open the windows [ceil(L/w), ceil((L+n)/w)) of every unit.  One thread per unit.
+__global__ void qe_open_windows_kernel(State st, int layer, int n) {
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= st.units) return;
+  const LayerDev hd = st.ldev[layer];
+  if (hd.L + n > st.max_context) return;
+  const int W = st.geo.W;
+  const int w_old = (hd.L + W - 1) / W, w_new = (hd.L + n + W - 1) / W;
+  const long long gu = (long long)layer * st.units + u;
+  int nb = 1 + hd.n_full + (w_old - hd.routed_upto);
+  for (int j = w_old; j < w_new; ++j, ++nb)
+    if (open_window(st, gu, j, nb) < 0) break;
+}
+
+// Prefill part 2: copy n tokens (positions [L, L+n)) of K and V into their window slots in
+// fragment order.  Thread per (unit, token, channel pair); sink positions go to the sink slot.
+__global__ void qe_append_kernel(State st, int layer, int n, const uint16_t* __restrict__ k,
                                  const uint16_t* __restrict__ v) {
   const int D = st.geo.D, W = st.geo.W;
+  const int pos0 = st.ldev[layer].L;
+  if (pos0 + n > st.max_context) {
+    if (blockIdx.x == 0 && threadIdx.x == 0) atomicOr(st.err, ERR_CAPACITY);
+    commit_length(st, layer, pos0);
+    return;
+  }
   const long long total = (long long)st.units * n * (D / 2);
   for (long long idx = blockIdx.x * (long long)blockDim.x + threadIdx.x; idx < total;
        idx += (long long)gridDim.x * blockDim.x) {
@@ -52,8 +132,6 @@ __global__ void qe_append_kernel(State st, int layer, int pos0, int n, const uin
     const int c = 2 * cp;
     const long long gu = (long long)layer * st.units + u;
     const size_t src = ((size_t)u * n + tk) * D + c;
-    const unsigned kk = *reinterpret_cast<const unsigned*>(k + src);
-    const uint16_t v0 = v[src], v1 = v[src + 1];
     int slot, row;
     if (pos < st.n_sink) {
       slot = 0;
@@ -64,11 +142,9 @@ __global__ void qe_append_kernel(State st, int layer, int pos0, int n, const uin
       row = pos - j * W;
       if (slot <= 0 || slot >= st.capb) { atomicOr(st.err, ERR_TABLE); continue; }
     }
-    uint8_t* base = st.bslab + (gu * st.capb + slot) * (long long)st.geo.bslot_bytes();
-    *reinterpret_cast<unsigned*>(base + bf16_k_off(st.geo, row, c)) = kk;
-    *reinterpret_cast<uint16_t*>(base + bf16_v_off(st.geo, row, c)) = v0;
-    *reinterpret_cast<uint16_t*>(base + bf16_v_off(st.geo, row, c + 1)) = v1;
+    write_token(st, gu, slot, row, c, *reinterpret_cast<const unsigned*>(k + src), v[src], v[src + 1]);
   }
+  commit_length(st, layer, pos0 + n);
 }
 
 // ------------------------------------------------------------------------------ route
@@ -92,14 +168,31 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   __shared__ int s_nmoves;
 
   const int tid = threadIdx.x;
+  // this event's geometry and capacities, from the device-resident header (identical in every CTA)
+  const LayerDev hd = st.ldev[p.layer];
+  const int W = st.geo.W;
+  const int L = hd.L;
+  const int n_windows = (L + W - 1) / W;
+  int aged_upto = (L - st.n_recent) >= 0 ? (L - st.n_recent) / W : 0;
+  if (aged_upto < hd.routed_upto) aged_upto = hd.routed_upto;
+  int kf, kq;
+  capacities_at(st.cap, st.n_sink, st.n_recent, W, st.geo.D, L, kf, kq);
+  const int ncand = hd.n_full + hd.n_quant + (aged_upto - hd.routed_upto);
+  const int exp_nfull = kf < ncand ? kf : ncand;
+  const int exp_nquant = kq < ncand - exp_nfull ? kq : ncand - exp_nfull;
+  const bool fits = exp_nquant <= st.capq && exp_nfull + exp_nquant <= st.caps && ncand <= ROUTE_MAX_CAND;
   if (tid == 0) { s_n = 0; s_nch = 0; s_nmoves = 0; }
   __syncthreads();
+  if (!fits) {   // the pools cannot hold this event's result: flag and leave the layer unchanged
+    if (tid == 0 && u == 0) atomicOr(st.err, ERR_CAPACITY);
+    return;
+  }
   // 1. candidate pool, eq. (4): Full u Quantized u newly aged Pinned windows
   const uint8_t* tier = st.tier + gu * st.maxw;
   const float* score = st.score + gu * st.maxw;
-  for (int j = tid; j < p.aged_upto; j += ROUTE_THREADS) {
+  for (int j = tid; j < aged_upto; j += ROUTE_THREADS) {
     const int z = tier[j];
-    const bool cand = (z == TIER_FULL) || (z == TIER_QUANT) || (z == TIER_PINNED && j >= p.routed_old);
+    const bool cand = (z == TIER_FULL) || (z == TIER_QUANT) || (z == TIER_PINNED && j >= hd.routed_upto);
     if (cand) {
       const int pos = atomicAdd(&s_n, 1);
       if (pos < ROUTE_MAX_CAND) {
@@ -110,11 +203,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     }
   }
   __syncthreads();
-  const int n = s_n;
-  if (n > ROUTE_MAX_CAND) {
-    if (tid == 0) atomicOr(st.err, ERR_COUNT);
-    return;
-  }
+  if (tid == 0 && s_n > ROUTE_MAX_CAND) atomicOr(st.err, ERR_COUNT);
+  const int n = s_n < ROUTE_MAX_CAND ? s_n : ROUTE_MAX_CAND;
   int npow = 1;
   while (npow < n) npow <<= 1;
   for (int i = n + tid; i < npow; i += ROUTE_THREADS) keys[i] = ~0ull;
@@ -136,7 +226,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   // 3. eq. (5): rank -> tier; collect the windows whose tier changes
   for (int r = tid; r < n; r += ROUTE_THREADS) {
     const int j = (int)(keys[r] & 0xFFFFFFFFu);
-    const int nt = r < p.kf ? TIER_FULL : (r < p.kf + p.kq ? TIER_QUANT : TIER_EVICTED);
+    const int nt = r < kf ? TIER_FULL : (r < kf + kq ? TIER_QUANT : TIER_EVICTED);
     const int ot = tier[j];
     const int ot2 = ot == TIER_PINNED ? TIER_FULL : ot;   // Pinned -> Full moves no data
     if (nt != ot) {
@@ -269,8 +359,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   // 5. rebuild the tile lists: bf16 = sink + Pinned/Full windows, 2-bit = Quantized windows,
   //    both in ascending window order (block-wide stream compaction)
   __shared__ int s_cnt[ROUTE_THREADS][2];
-  const int per = (p.n_windows + ROUTE_THREADS - 1) / ROUTE_THREADS;
-  const int j0 = tid * per, j1 = min(j0 + per, p.n_windows);
+  const int per = (n_windows + ROUTE_THREADS - 1) / ROUTE_THREADS;
+  const int j0 = tid * per, j1 = min(j0 + per, n_windows);
   int cb = 0, cq = 0;
   for (int j = j0; j < j1; ++j) {
     const int z = st.tier[gu * st.maxw + j];
@@ -289,8 +379,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       ab += b;
       aq += q;
     }
-    const int exp_b = 1 + p.exp_nfull + (p.n_windows - p.aged_upto);
-    if (ab != exp_b || aq != p.exp_nquant) atomicOr(st.err, ERR_COUNT);
+    const int exp_b = 1 + exp_nfull + (n_windows - aged_upto);
+    if (ab != exp_b || aq != exp_nquant) atomicOr(st.err, ERR_COUNT);
     st.blist[gu * st.capb] = make_int2(-1, 0);
   }
   __syncthreads();
@@ -303,6 +393,21 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     } else if (z == TIER_QUANT) {
       if (oq < st.capq) st.qlist[gu * st.capq + oq] = make_int2(j, st.qslot[gu * st.maxw + j]);
       ++oq;
+    }
+  }
+  // 6. the last CTA commits the new counts to the layer header
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    LayerDev* h = st.ldev + p.layer;
+    if (atomicAdd(&h->done, 1u) == gridDim.x - 1) {
+      h->routed_upto = aged_upto;
+      h->n_full = exp_nfull;
+      h->n_quant = exp_nquant;
+      h->kf = kf;
+      h->kq = kq;
+      h->done = 0;
+      __threadfence();
     }
   }
 }
@@ -438,19 +543,25 @@ __global__ void __launch_bounds__(MOVE_THREADS) qe_move_kernel(State st, const M
 }
 
 // ------------------------------------------------------------------------------ launchers
-cudaError_t launch_open_windows(const State& st, int layer, int w_old, int w_new, int nbw_old, cudaStream_t s) {
-  qe_open_windows_kernel<<<(st.units + 127) / 128, 128, 0, s>>>(st, layer, w_old, w_new, nbw_old);
-  return cudaGetLastError();
-}
-
-cudaError_t launch_append(const State& st, int layer, int pos0, int n, const uint16_t* k, const uint16_t* v,
-                          int n_sm, cudaStream_t s) {
+cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
+                          cudaStream_t s) {
+  if (n == 1) {
+    qe_append1_kernel<<<(st.units + APPEND1_UNITS - 1) / APPEND1_UNITS, APPEND1_UNITS * (st.geo.D / 2), 0, s>>>(
+        st, layer, k, v);
+    return cudaGetLastError();
+  }
+  qe_open_windows_kernel<<<(st.units + 127) / 128, 128, 0, s>>>(st, layer, n);
   const long long total = (long long)st.units * n * (st.geo.D / 2);
   long long blocks = (total + 255) / 256;
   const long long cap = (long long)n_sm * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  qe_append_kernel<<<(int)blocks, 256, 0, s>>>(st, layer, pos0, n, k, v);
+  qe_append_kernel<<<(int)blocks, 256, 0, s>>>(st, layer, n, k, v);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t s) {
+  qe_commit_length_kernel<<<1, 1, 0, s>>>(st, layer, n);
   return cudaGetLastError();
 }
 
@@ -459,14 +570,7 @@ size_t route_smem_bytes(const State& st) {
 }
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
-  const size_t smem = route_smem_bytes(p.st);
-  static size_t attr = 0;
-  if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(qe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = smem;
-  }
-  qe_route_kernel<<<p.st.units, ROUTE_THREADS, smem, s>>>(p);
+  qe_route_kernel<<<p.st.units, ROUTE_THREADS, route_smem_bytes(p.st), s>>>(p);
   return cudaGetLastError();
 }
 
@@ -476,16 +580,16 @@ size_t move_smem_bytes(const State& st) {
 }
 
 cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves, int n_sm, cudaStream_t s) {
-  const size_t smem = move_smem_bytes(st);
-  static size_t attr = 0;
-  if (smem > attr) {
-    cudaError_t e = cudaFuncSetAttribute(qe_move_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    attr = smem;
-  }
-  qe_move_kernel<<<n_sm * 2, MOVE_THREADS, smem, s>>>(st, moves, n_moves);
+  qe_move_kernel<<<n_sm * 2, MOVE_THREADS, move_smem_bytes(st), s>>>(st, moves, n_moves);
   return cudaGetLastError();
 }
 
+// kernel attributes, set once (outside any stream capture)
+cudaError_t prepare_route_kernels(const State& st) {
+  cudaError_t e = cudaFuncSetAttribute(qe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)route_smem_bytes(st));
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(qe_move_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)move_smem_bytes(st));
+}
 
 }  // namespace qe
