@@ -86,59 +86,73 @@ __device__ __forceinline__ Lay make_lay(const State& st, int layer, int pend, in
   return y;
 }
 
+// Tile order inside a unit: the nbt bf16 sub-tiles and the nq 2-bit windows are interleaved
+// evenly (tile i is a 2-bit window iff floor((i+1) nq / ntiles) > floor(i nq / ntiles)), so every
+// warp's range mixes memory-bound bf16 tiles with compute-bound 2-bit tiles and the SM's warps
+// overlap the two instead of splitting into bf16 warps and 2-bit warps.
+__device__ __forceinline__ int q_before(const Lay& y, int i) {   // 2-bit tiles among [0, i)
+  return (int)(((long long)i * y.nq) / y.ntiles);
+}
+__device__ __forceinline__ long long tile_start_in(const AttnParams& p, const Lay& y, int i) {
+  const int qb = q_before(y, i);
+  return (long long)(i - qb) * p.cb + (long long)qb * p.cq;
+}
 __device__ __forceinline__ long long tile_start(const AttnParams& p, const Lay& y, int u, int i) {
-  const int nbt = y.nbt;
-  long long r = (i < nbt) ? (long long)i * p.cb : (long long)nbt * p.cb + (long long)(i - nbt) * p.cq;
-  return (long long)u * y.Cu + r;
+  return (long long)u * y.Cu + tile_start_in(p, y, i);
 }
 
 // first tile whose start position is >= x
 __device__ __forceinline__ void first_tile(const AttnParams& p, const Lay& y, long long x, int& u, int& i) {
-  const int nbt = y.nbt;
   u = (int)(x / y.Cu);
-  long long r = x - (long long)u * y.Cu;
-  long long bend = (long long)nbt * p.cb;
-  if (r <= (long long)(nbt - 1) * p.cb) {
-    i = (int)((r + p.cb - 1) / p.cb);
-  } else if (y.nq > 0 && r <= bend) {
-    i = nbt;                                   // between the last bf16 tile and the first 2-bit one
-  } else if (y.nq > 0 && r <= bend + (long long)(y.nq - 1) * p.cq) {
-    i = nbt + (int)((r - bend + p.cq - 1) / p.cq);
-  } else {
+  const long long r = x - (long long)u * y.Cu;
+  int lo = 0, hi = y.ntiles;   // smallest i in [0, ntiles] with start(i) >= r (start is increasing)
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (tile_start_in(p, y, mid) >= r) hi = mid;
+    else lo = mid + 1;
+  }
+  i = lo;
+  if (i >= y.ntiles) {
     u += 1;
     i = 0;
   }
 }
 
-__device__ __forceinline__ void next_tile(const Lay& y, int& u, int& i) {
-  i += 1;
-  if (i >= y.ntiles) {
-    i = 0;
-    u += 1;
+// kind and kind-local index of tile i: bf16 sub-tile b (returns false) or 2-bit window k (true)
+__device__ __forceinline__ bool tile_kind(const Lay& y, int i, int& local) {
+  const int qb = q_before(y, i);
+  if (q_before(y, i + 1) > qb) {
+    local = qb;
+    return true;
   }
+  local = i - qb;
+  return false;
 }
 
 // list entry {window, slot} of tile (u, i)
 __device__ __forceinline__ int2 list_entry(const AttnParams& p, const Lay& y, int u, int i, int sub_tiles) {
   const State& st = p.st;
   const long long gu = (long long)p.layer * st.units + u;
-  if (i < y.nbt) return st.blist[gu * st.capb + i / sub_tiles];
-  return st.qlist[gu * st.capq + (i - y.nbt)];
+  int loc;
+  if (!tile_kind(y, i, loc)) return st.blist[gu * st.capb + loc / sub_tiles];
+  return st.qlist[gu * st.capq + loc];
 }
 
-// descriptor of tile (u, i) from its list entry; false if it has no valid row (or is corrupt)
+// descriptor of tile (u, i) from its list entry; false if it has no valid row (or is corrupt).
+// d.i is the tile's index in the per-unit log-sum-exp array: bf16 sub-tiles first, then 2-bit.
 __device__ __forceinline__ bool describe(const AttnParams& p, const Lay& y, int u, int i, int2 ent, TileDesc& d) {
-  const int nbt = y.nbt;
   const State& st = p.st;
   const int W = st.geo.W;
   const int sub_tiles = W / 16;
+  int loc;
+  const bool is_q = tile_kind(y, i, loc);
   d.u = u;
-  d.i = i;
+  d.i = is_q ? y.nbt + loc : loc;
   d.win = ent.x;
   d.slot = ent.y;
-  if (i < nbt) {
+  if (!is_q) {
     d.kind = 0;
-    d.sub = i % sub_tiles;
+    d.sub = loc % sub_tiles;
     if (ent.y < 0 || ent.y >= st.capb || ent.x < -1 || ent.x >= st.maxw) {   // corrupt entry: skip, flag
       atomicOr(st.err, ERR_TABLE);
       return false;
@@ -392,7 +406,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         BatchDesc bd;
         bd.src = tile_src(p, d, bd.bytes);
         bd.sd.u = u;
-        bd.sd.lse_off = (u * y.ntiles + i) * G;
+        bd.sd.lse_off = (u * y.ntiles + d.i) * G;
         bd.sd.meta = d.lo | (d.hi << 8) | (d.kind << 16);
         bd.sd.pad = 0;
         bd.pad = 0;
