@@ -213,6 +213,33 @@ qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, doubl
 /* Number of kernel launches the handle has enqueued since qe_init. */
 long long qe_kernel_launches(qe_handle h);
 
+/* ---------------------------------------------------------------- no-allocation decode step
+ *
+ * Not part of the method on the pages (the paper has no counterpart): a library service.
+ *
+ * The same decode step as qe_decode_step (same kernels, same results up to the summation order
+ * of the split-K merge), for callers that may not allocate device memory on the decode path:
+ * callers whose device memory is owned by an arena or budget manager that forbids new
+ * allocations once serving has started, callers for which a cudaMalloc could block on the
+ * allocator or synchronise the device at the wrong moment, or threads that are not allowed to
+ * make allocating CUDA calls.  It calls no cudaMalloc, cudaFree or other allocating routine:
+ *  - q and out must be device memory ([batch][n_q_heads][head_dim] bf16 in, float32 or bf16
+ *    out as configured); host pointers are not accepted (qe_decode_step would stage them
+ *    through buffers it allocates on first use);
+ *  - the split-K scratch comes from a fixed static device array inside the library (about
+ *    4.1 MiB, held on every GPU that loads the library until the process exits), not from
+ *    the handle.
+ * Limits (QE_ERR_CAPACITY beyond them): batch * n_kv_heads <= 16 units; at most 8192 tiles per
+ * unit (a tile is 16 bf16 tokens or one 2-bit window); G <= 4; head_dim <= 128.
+ * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.  All calls share
+ * the one array: calls whose work may overlap on the GPU (other streams, other handles on the
+ * same device) race on it and must be serialised by the caller.  Nothing in the array needs to
+ * start at zero: each call writes every scratch value it reads.  Like qe_decode_step, it counts
+ * a pending single-token append, updates the window scores and is enqueued on the handle's
+ * stream without waiting. */
+qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* q, void* out);
+
 #ifdef __cplusplus
 }
 #endif

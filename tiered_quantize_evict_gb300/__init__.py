@@ -27,7 +27,7 @@ EXPORTED = [
     "qe_init", "qe_destroy", "qe_last_error", "qe_append", "qe_decode_step", "qe_route",
     "qe_synchronize", "qe_get_layer_info", "qe_get_tiers", "qe_get_scores", "qe_set_scores",
     "qe_get_quant_window", "qe_get_bf16_window", "qe_get_route_stats", "qe_set_timing",
-    "qe_get_timing", "qe_kernel_launches",
+    "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc",
 ]
 
 
@@ -93,6 +93,7 @@ def load_library() -> ctypes.CDLL:
         "qe_set_timing": ([P, I], I),
         "qe_get_timing": ([P, ctypes.POINTER(D), ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(D)], I),
         "qe_kernel_launches": ([P], ctypes.c_longlong),
+        "qe_decode_step_noalloc": ([P, I, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -154,6 +155,12 @@ class QECache:
     def qe_decode_step(self, layer: int, q, out):
         flags = QE_HOST_PTRS if _is_host(q) else QE_DEVICE_PTRS
         self._check(self._lib.qe_decode_step(self.h, layer, _ptr(q), _ptr(out), flags))
+
+    def qe_decode_step_noalloc(self, layer: int, q, out):
+        """qe_decode_step without any device allocation (device q/out only; scratch is a static array)."""
+        if _is_host(q) or _is_host(out):
+            raise ValueError("qe_decode_step_noalloc takes device tensors only")
+        self._check(self._lib.qe_decode_step_noalloc(self.h, layer, _ptr(q), _ptr(out)))
 
     def qe_route(self, layer: int = -1):
         self._check(self._lib.qe_route(self.h, layer))

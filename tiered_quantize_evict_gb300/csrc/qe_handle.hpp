@@ -1,0 +1,63 @@
+// qe_handle.hpp -- the handle behind the C ABI (internal; shared by the library's host files).
+#pragma once
+#include <string>
+#include <vector>
+
+#include <cuda_runtime.h>
+
+#include "qe.h"
+#include "qe_kernels.cuh"
+
+namespace qe {
+
+// Host shadow of a layer's device header (launch shapes never depend on it; checks and
+// introspection do).
+struct LayerMirror {
+  int L = 0;
+  int pending = 0;    // single-token appends whose length the device has not committed yet
+  int routed_upto = 0;
+  int n_full = 0;
+  int n_quant = 0;
+  int kf = 0, kq = 0;
+};
+
+}  // namespace qe
+
+struct qe_handle_s {
+  qe_config cfg{};
+  cudaStream_t stream = nullptr;
+  int device = 0;
+  int n_sm = 0;
+  qe::State st{};
+  std::vector<qe::LayerMirror> lay;
+  int units = 0;
+  long long gu_total = 0;
+  // scratch for the attention split-K
+  float* part_o = nullptr;
+  float2* part_ml = nullptr;
+  float* lse = nullptr;
+  int* lay_buf = nullptr;     // [n_layers][4] counts handed from attention to combine
+  int pslots_cap = 0;         // partial slots per unit
+  int attn_grid = 0;          // CTAs of every attention launch (fixed)
+  int ntiles_cap = 0;
+  // moves
+  qe::Move* moves = nullptr;
+  int* n_moves = nullptr;
+  int max_moves = 0;
+  // staging for host pointers
+  void* stage[4] = {nullptr, nullptr, nullptr, nullptr};
+  size_t stage_bytes[4] = {0, 0, 0, 0};
+  // pinned host store
+  void* hstore_host = nullptr;
+  void* hledger_host = nullptr;
+  // tile costs of the split-K partition
+  int cost_b = 8, cost_q = 6;
+  // timing
+  bool timing = false;
+  std::vector<cudaEvent_t> ev_pool;
+  size_t ev_used = 0;
+  double timed_bytes = 0;
+  long long timed_launches = 0;
+  long long launches = 0;
+  std::string err;
+};
