@@ -21,6 +21,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 ROOT = os.path.dirname(os.path.abspath(__file__))
@@ -45,6 +46,32 @@ def _dist():
     return rank, world
 
 
+def max_over_ranks(x: float, world: int, device) -> float:
+    """The largest of every rank's x (the job ends when its slowest rank does)."""
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], device=device, dtype=torch.float64)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(tokens_per_rank: float, world: int, ms: float) -> float:
+    """Tokens/s of the whole job: every rank's tokens over the slowest rank's time."""
+    return world * tokens_per_rank / (ms / 1e3)
+
+
+def workload_config(wl, world: int) -> dict:
+    """The `config` object of the JSON line (shared by both arms)."""
+    return {
+        "workload": wl.name, "batch": wl.batch, "context": wl.prefill, "layers": wl.n_layers,
+        "q_heads": wl.n_q_heads, "kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "window": wl.window,
+        "route_period": wl.route_period, "bf16_token_share": wl.frac_bf16, "int2_token_share": wl.frac_int2,
+        "n_sink": wl.n_sink, "n_recent": wl.n_recent, "parallelism": f"replicas{world}",
+    }
+
+
 # ---------------------------------------------------------------------------- clocks
 class ClockSampler:
     FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
@@ -54,7 +81,9 @@ class ClockSampler:
     def __init__(self, index: int):
         self.index = index
         self.proc = None
-        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{index}.csv")
+        # the raw samples go to $QE_CLOCKS_DIR (default: the temp directory); the JSON line
+        # carries their summary
+        self.path = os.path.join(os.environ.get("QE_CLOCKS_DIR", tempfile.gettempdir()), f"clocks_rank{index}.csv")
 
     def start(self):
         try:
@@ -268,18 +297,10 @@ def run_ours(args):
     e2e_ms = max(e2.elapsed_time(e3), (time.perf_counter() - t_e2e0) * 1e3)
     cache.qe_synchronize()
 
-    # max over ranks
-    def allmax(x):
-        if world == 1:
-            return x
-        tt = torch.tensor([x], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        return float(tt.item())
-
-    ms_total = allmax(ms_total)
-    e2e_ms = allmax(e2e_ms)
-    value = world * B * K / (ms_total / 1e3)
-    e2e_val = world * B * K / (e2e_ms / 1e3)
+    ms_total = max_over_ranks(ms_total, world, dev)
+    e2e_ms = max_over_ranks(e2e_ms, world, dev)
+    value = whole_job_rate(B * K, world, ms_total)
+    e2e_val = whole_job_rate(B * K, world, e2e_ms)
     peak, peak_kind = _peaks()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
     info = cache.layer_info(0)
@@ -288,11 +309,10 @@ def run_ours(args):
         "warmup": W, "ms_per_step": round(ms_total / K, 4), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded qe_inputs generator, device-side)",
         "config": {
-            "workload": wl.name, "batch": B, "context": wl.prefill, "layers": Lyr, "q_heads": Hq, "kv_heads": Hkv,
-            "head_dim": D, "window": wl.window, "route_period": omega, "bf16_token_share": wl.frac_bf16,
-            "int2_token_share": wl.frac_int2, "n_sink": wl.n_sink, "n_recent": wl.n_recent,
-            "timed_decode_steps": [omega + W + 1, omega + W + K], "parallelism": f"replicas{world}",
-            "launch": "one CUDA graph per decode step (32 layers x append, attention, combine; routing every Omega)",
+            **workload_config(wl, world),
+            "timed_decode_steps": [omega + W + 1, omega + W + K],
+            "launch": "one CUDA graph per decode step (%d layers x append, attention, combine; routing every "
+                      "Omega)" % Lyr,
             "kv_per_layer_unit": {"full": info.n_full, "quant": info.n_quant, "pinned": info.n_pinned},
             "l2": "inputs larger than L2: %.0f MB read per layer launch, %.1f GB per step" % (
                 info.attn_bytes / 1e6, info.attn_bytes * Lyr / 1e9),
@@ -345,8 +365,11 @@ def _oracle_worker(a):
     return times
 
 
-def oracle_baseline(workload: str, n_units: int, n_steps: int):
-    """Tokens/s of the CPU oracle extrapolated from a bounded sample of units."""
+def oracle_baseline(workload: str, n_units: int, n_steps: int, n_warm: int = 0):
+    """Tokens/s of the CPU oracle extrapolated from a bounded sample of units.
+
+    Each sampled unit runs `n_warm` untimed and then `n_steps` timed decode steps.
+    """
     import multiprocessing as mp
 
     import qe_inputs as gen
@@ -355,23 +378,24 @@ def oracle_baseline(workload: str, n_units: int, n_steps: int):
     os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
     os.environ.setdefault("OMP_NUM_THREADS", "1")
     units_total = wl.batch * wl.n_layers * wl.n_kv_heads
+    n_units = max(1, min(n_units, units_total))      # distinct units (the stride is prime)
     first = wl.route_period + 1
     jobs = []
     for i in range(n_units):
         u = (i * 2654435761) % units_total
         b, rest = divmod(u, wl.n_layers * wl.n_kv_heads)
         layer, kvh = divmod(rest, wl.n_kv_heads)
-        jobs.append((workload, b, layer, kvh, n_steps, first))
+        jobs.append((workload, b, layer, kvh, n_warm + n_steps, first))
     workers = min(cores, n_units)
     ctx = mp.get_context("spawn")
     with ctx.Pool(workers) as pool:
         res = pool.map(_oracle_worker, jobs)
-    per_unit_step = sum(sum(r) for r in res) / (n_units * n_steps)      # seconds, one core
+    per_unit_step = sum(sum(r[n_warm:]) for r in res) / (n_units * n_steps)   # seconds, one core
     step_s = per_unit_step * units_total / workers                       # all units, `workers` cores
     return {"value": round(wl.batch / step_s, 4), "unit": "tokens/s", "cores": workers, "kind": "oracle",
-            "sample": f"{n_units} units x {n_steps} steady-state decode steps (after the first routing event) "
-                      f"of {workload}, extrapolated to all {units_total} units on {workers} cores; "
-                      f"setup (prefill, pre-roll, first route) untimed"}, step_s
+            "sample": f"{n_units} units x {n_steps} timed steady-state decode steps (after the first routing "
+                      f"event and {n_warm} untimed warm-up steps) of {workload}, extrapolated to all "
+                      f"{units_total} units on {workers} cores; setup (prefill, pre-roll, first route) untimed"}, step_s
 
 
 def run_reference(args):
@@ -383,17 +407,15 @@ def run_reference(args):
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else os.cpu_count()
     # each step: one decode step of `cores` sampled units (bounded sample of the workload)
     n_units = max(1, min(cores, 16))
-    steps = args.warmup + args.steps
     t0 = time.perf_counter()
-    base, step_s = oracle_baseline(args.workload, n_units, steps)
+    base, step_s = oracle_baseline(args.workload, n_units, args.steps, n_warm=args.warmup)
     wall = time.perf_counter() - t0
     v = base["value"]
-    base["sample"] = base["sample"].replace("steady-state", f"steady-state ({args.warmup} warm-up + {args.steps} timed)")
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded qe_inputs generator)",
-            "config": {"workload": wl.name, "batch": wl.batch, "context": wl.prefill, "layers": wl.n_layers},
+            "config": workload_config(wl, world),
             "cpu_baseline": base,
             "e2e": {"value": v, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "wall_s": round(wall, 1)}

@@ -15,7 +15,7 @@ Sources
 * H2O page, §1 (capacity M_KV = 2 L H_kv D N b).
 
 Capacity rule per workload (the pages leave the mapping of "x % of tokens"
-to window counts open; reading stated in the design doc): at a routing event with
+to window counts open; the reading adopted here): at a routing event with
 current length L,
 * fixed:        K_f, K_q given;
 * token shares: K_f = max(0, floor((f_bf16 L - n_sink - n_recent) / w)),

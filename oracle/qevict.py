@@ -17,7 +17,7 @@ Sources
 * H2O page, §2.1: per-step order append -> attention over the current
   candidates (including the new token) -> score update -> eviction.
 
-Readings (the design doc lists them all):
+Readings where the pages leave a step open:
 * window j covers positions [j w, (j+1) w); the sink tokens are carved out of
   window 0, whose routable part is [n_sink, w);
 * a window is "Pinned" (full precision, not ranked) until it is complete and

@@ -15,7 +15,7 @@ Sources
 * KV Cache technology evolution (zane-jiang.github.io), §5: KIVI groups
   keys along channels across tokens and values along each token.
 
-Readings where the pages are silent (listed in the design doc):
+Readings where the pages are silent:
 * rounding is to nearest with ties to even (``np.rint``), codes clipped to
   ``[0, 2^b - 1]``;
 * the scale and the normalised value are computed in float32 with IEEE

@@ -18,7 +18,7 @@ Row keys chain SplitMix64 over (seed, tensor id, batch, layer, head,
 position-or-step), see :func:`row_key`.
 
 Workloads (shapes, windows, capacities, value recipes) are defined in
-:data:`WORKLOADS`; see the design doc for the recipe and its readings.
+:data:`WORKLOADS`, each with the value recipe of the workload it stands for.
 """
 from __future__ import annotations
 

@@ -174,10 +174,13 @@ class ParityRun:
                 assert err <= SCORE_RTOL * s_ref + SCORE_ATOL, (
                     f"step {self.t} unit {(tr.b, tr.layer, tr.kvh)} window {j}: score {gs[j]} vs {s_ref}")
 
-    def route_and_check(self):
+    def route_and_check(self, gpu_routed: bool = False):
+        """Route the oracle units (and the cache, unless a replayed graph already did) and
+        compare tiers and codes; scores are compared first (routing leaves them unchanged)."""
         wl = self.wl
         self.check_scores()
-        self.cache.qe_route(-1)
+        if not gpu_routed:
+            self.cache.qe_route(-1)
         self.route_events += 1
         tiers = {}
         for tr in self.tracked:

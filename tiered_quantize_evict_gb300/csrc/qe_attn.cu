@@ -9,7 +9,7 @@
 // window receives summed over the G heads, added to the window's float32 score.
 //
 // GB300 design:
-//  * One persistent CTA per SM, 8 independent consumer warps.  The unit x tile sequence of
+//  * One persistent CTA per SM, 12 independent consumer warps.  The unit x tile sequence of
 //    the layer is cut into one contiguous, cost-weighted range per warp (stream-K), so every
 //    warp streams its own range through a private ring of shared-memory stages filled by
 //    cp.async.bulk (one 1-D bulk copy per tile, completion on an mbarrier), and the whole GPU
