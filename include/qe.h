@@ -107,8 +107,9 @@ enum {
 /* Create a cache for cfg on the current CUDA device.  Allocates the device
  * window pools (bf16 slots for every window up to max_context, 2-bit slots for
  * the largest Kq), the window table and scores, and a pinned, device-mapped
- * host backing store that keeps the exact bf16 copy and the 2-bit ledger
- * entry of every window that has ever been demoted and not evicted.
+ * host backing store that keeps the exact bf16 copy of every kept (Full or
+ * Quantized) window, written when the window is first kept, and the 2-bit
+ * ledger entry of every window that has been demoted and not evicted.
  * cuda_stream: a cudaStream_t (NULL = legacy default stream).  The handle
  * owns everything it allocates.  No kernel runs. */
 qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out);

@@ -91,6 +91,30 @@ QE_HD CodePos vcode_pos(const Geo& g, int r, int c) {
   return p;
 }
 
+// Inverse of kcode_pos / vcode_pos: the (token r, channel c) whose code sits at bit
+// 8 reg + 2 f + 4 e of word widx of the key code block (value = false) or of the value code
+// block (value = true; widx counted from the start of that block).
+struct RC { int r, c; };
+QE_HD RC code_rc(const Geo& g, bool value, int widx, int reg, int f, int e) {
+  const int cw = g.cw();
+  const int chunk = widx / (32 * cw), rem = widx - chunk * 32 * cw;
+  const int lane = rem / cw, wi = chunk * cw + (rem - lane * cw);
+  const int F = 2 * wi + f;
+  const int a = (lane >> 2) + 8 * (reg & 1);              // row inside the 16 x 16 fragment
+  const int b = ((lane & 3) << 1) + e + 8 * (reg >> 1);   // column inside the fragment
+  RC o;
+  if (!value) {
+    const int mt = F / (g.D / 16), ks = F - mt * (g.D / 16);
+    o.r = 16 * mt + a;
+    o.c = 16 * ks + b;
+  } else {
+    const int mc = F / (g.W / 16), kt = F - mc * (g.W / 16);
+    o.c = 16 * mc + a;
+    o.r = 16 * kt + b;
+  }
+  return o;
+}
+
 // Position of key channel c inside the key min / key scale arrays of a 2-bit slot: lane t of
 // channel step ks reads channels (16 ks + 2t, +1, +8, +9) -- its B-fragment channels -- as one
 // 16-byte vector.

@@ -41,15 +41,27 @@ struct CombineParams {
 
 constexpr int COMBINE_MAXP = 256;   // partials one unit may receive
 
-// one window move decided by a routing event
+// One window move decided by a routing event.  A window's exact bf16 copy goes to its host
+// store entry the first time the window is kept (Full or Quantized) after leaving the Pinned
+// state: a complete window never changes, so a Full window's copy, written when it became Full,
+// already serves its first demotion, which then only has to write the ledger.
+enum : int {
+  MOVE_PACK_COPY = 0,   // Pinned -> Quantized: pack, ledger and exact copy to the host
+  MOVE_REUSE = 1,       // -> Quantized again: ledger -> 2-bit slot
+  MOVE_PROMOTE = 2,     // Quantized -> Full: exact copy -> bf16 slot
+  MOVE_PACK = 3,        // Full -> Quantized, first time: pack and ledger (the exact copy exists)
+  MOVE_COPY = 4         // Pinned -> Full: exact copy to the host
+};
 struct Move {
-  int kind;    // 0 pack (first demotion), 1 ledger reuse, 2 promotion
+  int kind;
   int gu;
   int win;
-  int src;     // pack: bf16 slot; reuse/promotion: store entry
-  int dst;     // pack/reuse: 2-bit slot; promotion: bf16 slot
-  int sent;    // pack: store entry to fill
+  int src;     // pack / copy: bf16 slot; reuse / promotion: store entry
+  int dst;     // pack / reuse: 2-bit slot; promotion: bf16 slot; copy: store entry
+  int sent;    // pack: store entry (ledger, and the exact copy for MOVE_PACK_COPY)
 };
+// bit of a window's store entry number that says its ledger (2-bit codes) exists
+constexpr int SENT_LEDGER = 1 << 30;
 
 struct RouteParams {
   State st;

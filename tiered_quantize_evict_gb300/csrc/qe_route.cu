@@ -157,15 +157,19 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   const State& st = p.st;
   const int u = blockIdx.x;
   const long long gu = (long long)p.layer * st.units + u;
+  // Changed windows carry a shared-memory copy of their table entries (old tier, bf16 slot,
+  // 2-bit slot, store entry), so the serial bookkeeping below touches no global memory.
   unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm);              // ROUTE_MAX_CAND
   int* ch_win = reinterpret_cast<int*>(keys + ROUTE_MAX_CAND);                       // ROUTE_MAX_CAND
-  uint8_t* ch_new = reinterpret_cast<uint8_t*>(ch_win + ROUTE_MAX_CAND);             // ROUTE_MAX_CAND
-  int* bstack = reinterpret_cast<int*>(ch_new + ROUTE_MAX_CAND);                     // capb
+  int* ch_b = ch_win + ROUTE_MAX_CAND;                                               // ROUTE_MAX_CAND
+  int* ch_q = ch_b + ROUTE_MAX_CAND;                                                 // ROUTE_MAX_CAND
+  int* ch_s = ch_q + ROUTE_MAX_CAND;                                                 // ROUTE_MAX_CAND
+  uint8_t* ch_new = reinterpret_cast<uint8_t*>(ch_s + ROUTE_MAX_CAND);               // ROUTE_MAX_CAND
+  uint8_t* ch_old = ch_new + ROUTE_MAX_CAND;                                         // ROUTE_MAX_CAND
+  int* bstack = reinterpret_cast<int*>(ch_old + ROUTE_MAX_CAND);                     // capb
   int* qstack = bstack + st.capb;                                                    // capq
   int* sstack = qstack + st.capq;                                                    // caps
-  __shared__ int s_n, s_nch, s_pos[2];
-  __shared__ int s_moves_base;
-  __shared__ int s_nmoves;
+  __shared__ int s_n, s_nch, s_pos[3];
 
   const int tid = threadIdx.x;
   // this event's geometry and capacities, from the device-resident header (identical in every CTA)
@@ -181,7 +185,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   const int exp_nfull = kf < ncand ? kf : ncand;
   const int exp_nquant = kq < ncand - exp_nfull ? kq : ncand - exp_nfull;
   const bool fits = exp_nquant <= st.capq && exp_nfull + exp_nquant <= st.caps && ncand <= ROUTE_MAX_CAND;
-  if (tid == 0) { s_n = 0; s_nch = 0; s_nmoves = 0; }
+  if (tid == 0) { s_n = 0; s_nch = 0; }
   __syncthreads();
   if (!fits) {   // the pools cannot hold this event's result: flag and leave the layer unchanged
     if (tid == 0 && u == 0) atomicOr(st.err, ERR_CAPACITY);
@@ -224,18 +228,22 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     }
   }
   // 3. eq. (5): rank -> tier; collect the windows whose tier changes
+  int* bsl = st.bslot + gu * st.maxw;
+  int* qsl = st.qslot + gu * st.maxw;
+  int* sen = st.sent + gu * st.maxw;
   for (int r = tid; r < n; r += ROUTE_THREADS) {
     const int j = (int)(keys[r] & 0xFFFFFFFFu);
     const int nt = r < kf ? TIER_FULL : (r < kf + kq ? TIER_QUANT : TIER_EVICTED);
     const int ot = tier[j];
-    const int ot2 = ot == TIER_PINNED ? TIER_FULL : ot;   // Pinned -> Full moves no data
     if (nt != ot) {
-      if (nt == ot2) {
-        st.tier[gu * st.maxw + j] = (uint8_t)nt;
-      } else {
+      {
         const int c = atomicAdd(&s_nch, 1);
         ch_win[c] = j;
         ch_new[c] = (uint8_t)nt;
+        ch_old[c] = (uint8_t)ot;
+        ch_b[c] = bsl[j];
+        ch_q[c] = qsl[j];
+        ch_s[c] = sen[j];
       }
     }
   }
@@ -245,94 +253,87 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   for (int i = tid; i < qtop; i += ROUTE_THREADS) qstack[i] = st.qfree[gu * st.capq + i];
   for (int i = tid; i < stop; i += ROUTE_THREADS) sstack[i] = st.sfree[gu * st.caps + i];
   __syncthreads();
-  // 4. bookkeeping, one thread, in an order that never hands out a slot whose data a move
-  //    still has to read: 2-bit and store frees first (their contents are not needed),
-  //    bf16 slots for promotions next, then demotions, then the bf16 frees.
+  const int nch = s_nch;
+  // 4. bookkeeping, one thread, on the shared copies, in an order that never hands out a slot
+  //    whose data a move still has to read: 2-bit and store frees first (their contents are not
+  //    needed), bf16 slots for promotions next, then demotions, then the bf16 frees.
   if (tid == 0) {
-    const int nch = s_nch;
     int bt = btop, qt = qtop, stt = stop;
     unsigned err = 0;
     int nm = 0;
-    int* bsl = st.bslot + gu * st.maxw;
-    int* qsl = st.qslot + gu * st.maxw;
-    int* sen = st.sent + gu * st.maxw;
     // (a) leaving the 2-bit pool: promotions and evictions of Quantized windows
     for (int c = 0; c < nch; ++c) {
-      const int j = ch_win[c];
-      if (tier[j] == TIER_QUANT) {
-        const int s = qsl[j];
+      if (ch_old[c] == TIER_QUANT) {
+        const int s = ch_q[c];
         if (s < 0 || qt >= st.capq) err |= ERR_FREELIST; else qstack[qt++] = s;
-        qsl[j] = -1;
+        ch_q[c] = -1;
       }
     }
     // (b) evictions release their store / ledger entry
     for (int c = 0; c < nch; ++c) {
-      const int j = ch_win[c];
-      if (ch_new[c] == TIER_EVICTED && sen[j] >= 0) {
-        if (stt >= st.caps) err |= ERR_FREELIST; else sstack[stt++] = sen[j];
-        sen[j] = -1;
+      if (ch_new[c] == TIER_EVICTED && ch_s[c] >= 0) {
+        if (stt >= st.caps) err |= ERR_FREELIST; else sstack[stt++] = ch_s[c] & ~SENT_LEDGER;
+        ch_s[c] = -1;
       }
     }
-    // (c) promotions: a bf16 slot, filled from the exact host copy
+    // (c) promotions: a bf16 slot, filled from the exact host copy; Pinned windows kept Full
+    //     get a store entry and their exact copy is written now
     for (int c = 0; c < nch; ++c) {
-      const int j = ch_win[c];
-      if (ch_new[c] == TIER_FULL && tier[j] == TIER_QUANT) {
-        if (bt <= 0 || sen[j] < 0) { err |= ERR_FREELIST; continue; }
-        const int s = bstack[--bt];
-        bsl[j] = s;
-        keys[nm++] = ((unsigned long long)2 << 56) | ((unsigned long long)(unsigned)c << 24);
+      if (ch_new[c] != TIER_FULL) continue;
+      if (ch_old[c] == TIER_QUANT) {
+        if (bt <= 0 || ch_s[c] < 0) { err |= ERR_FREELIST; continue; }
+        ch_b[c] = bstack[--bt];
+        keys[nm++] = ((unsigned long long)MOVE_PROMOTE << 56) | ((unsigned long long)(unsigned)c << 24);
+      } else if (ch_s[c] < 0) {
+        if (stt <= 0) { err |= ERR_FREELIST; continue; }
+        ch_s[c] = sstack[--stt];
+        keys[nm++] = ((unsigned long long)MOVE_COPY << 56) | ((unsigned long long)(unsigned)c << 24);
       }
     }
-    // (d) demotions: a 2-bit slot; first demotion packs and takes a store entry, later ones reuse
+    // (d) demotions: a 2-bit slot; the first demotion packs (and, from Pinned, takes a store
+    //     entry for the exact copy), later ones reuse the ledger
     for (int c = 0; c < nch; ++c) {
-      const int j = ch_win[c];
       if (ch_new[c] == TIER_QUANT) {
         if (qt <= 0) { err |= ERR_FREELIST; continue; }
-        qsl[j] = qstack[--qt];
-        if (sen[j] < 0) {
+        ch_q[c] = qstack[--qt];
+        int kind;
+        if (ch_s[c] < 0) {
           if (stt <= 0) { err |= ERR_FREELIST; continue; }
-          sen[j] = sstack[--stt];
-          keys[nm++] = ((unsigned long long)0 << 56) | ((unsigned long long)(unsigned)c << 24);
+          ch_s[c] = sstack[--stt];
+          kind = MOVE_PACK_COPY;
         } else {
-          keys[nm++] = ((unsigned long long)1 << 56) | ((unsigned long long)(unsigned)c << 24);
+          kind = (ch_s[c] & SENT_LEDGER) ? MOVE_REUSE : MOVE_PACK;
         }
+        ch_s[c] |= SENT_LEDGER;
+        keys[nm++] = ((unsigned long long)kind << 56) | ((unsigned long long)(unsigned)c << 24);
       }
     }
-    // (e) bf16 frees (after the moves above were decided; the move kernel reads them first)
-    s_nmoves = nm;
-    // write the move records (slot numbers captured before the frees below clear bslot)
+    // move records (slot numbers captured before the bf16 frees below clear them)
     int base = 0;
     if (nm > 0) base = atomicAdd(p.n_moves, nm);
-    s_moves_base = base;
-    for (int k = 0; k < nm; ++k) {
-      const int kind = (int)(keys[k] >> 56);
-      const int c = (int)((keys[k] >> 24) & 0xFFFFFFFF);
-      const int j = ch_win[c];
-      Move mv;
-      mv.kind = kind;
-      mv.gu = (int)gu;
-      mv.win = j;
-      if (kind == 0) { mv.src = bsl[j]; mv.dst = qsl[j]; mv.sent = sen[j]; }
-      else if (kind == 1) { mv.src = sen[j]; mv.dst = qsl[j]; mv.sent = sen[j]; }
-      else { mv.src = sen[j]; mv.dst = bsl[j]; mv.sent = sen[j]; }
-      if (base + k < p.max_moves) p.moves[base + k] = mv; else err |= ERR_MOVES;
-    }
-    for (int c = 0; c < nch; ++c) {
-      const int j = ch_win[c];
-      const int ot = tier[j];
-      if ((ot == TIER_PINNED || ot == TIER_FULL) && ch_new[c] != TIER_FULL) {
-        if (bsl[j] < 0 || bt >= st.capb) err |= ERR_FREELIST; else bstack[bt++] = bsl[j];
-        bsl[j] = -1;
-      }
-    }
-    // tier updates and statistics
     unsigned long long nfirst = 0, nreuse = 0, nprom = 0, nev = 0;
     for (int k = 0; k < nm; ++k) {
       const int kind = (int)(keys[k] >> 56);
-      if (kind == 0) ++nfirst; else if (kind == 1) ++nreuse; else ++nprom;
+      const int c = (int)((keys[k] >> 24) & 0xFFFFFFFF);
+      const int ent = ch_s[c] & ~SENT_LEDGER;
+      Move mv;
+      mv.kind = kind;
+      mv.gu = (int)gu;
+      mv.win = ch_win[c];
+      mv.sent = ent;
+      if (kind == MOVE_PACK_COPY || kind == MOVE_PACK) { mv.src = ch_b[c]; mv.dst = ch_q[c]; ++nfirst; }
+      else if (kind == MOVE_REUSE) { mv.src = ent; mv.dst = ch_q[c]; ++nreuse; }
+      else if (kind == MOVE_PROMOTE) { mv.src = ent; mv.dst = ch_b[c]; ++nprom; }
+      else { mv.src = ch_b[c]; mv.dst = ent; }
+      if (base + k < p.max_moves) p.moves[base + k] = mv; else err |= ERR_MOVES;
     }
+    // (e) bf16 frees (after the moves above were decided; the move kernel reads them first)
     for (int c = 0; c < nch; ++c) {
-      st.tier[gu * st.maxw + ch_win[c]] = ch_new[c];
+      const int ot = ch_old[c];
+      if ((ot == TIER_PINNED || ot == TIER_FULL) && ch_new[c] != TIER_FULL) {
+        if (ch_b[c] < 0 || bt >= st.capb) err |= ERR_FREELIST; else bstack[bt++] = ch_b[c];
+        ch_b[c] = -1;
+      }
       if (ch_new[c] == TIER_EVICTED) ++nev;
     }
     unsigned long long* sp = st.stats + (size_t)p.layer * 5;
@@ -346,11 +347,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     st.sfree_top[gu] = stt;
     s_pos[0] = bt;
     s_pos[1] = qt;
+    s_pos[2] = stt;
     if (err) atomicOr(st.err, err);
   }
   __syncthreads();
   {
-    const int bt = s_pos[0], qt = s_pos[1], stt = st.sfree_top[gu];
+    // table entries and tiers of the changed windows, and the free stacks, back to global memory
+    for (int c = tid; c < nch; c += ROUTE_THREADS) {
+      const int j = ch_win[c];
+      bsl[j] = ch_b[c];
+      qsl[j] = ch_q[c];
+      sen[j] = ch_s[c];
+      st.tier[gu * st.maxw + j] = ch_new[c];
+    }
+    const int bt = s_pos[0], qt = s_pos[1], stt = s_pos[2];
     for (int i = tid; i < bt; i += ROUTE_THREADS) st.bfree[gu * st.capb + i] = bstack[i];
     for (int i = tid; i < qt; i += ROUTE_THREADS) st.qfree[gu * st.capq + i] = qstack[i];
     for (int i = tid; i < stt; i += ROUTE_THREADS) st.sfree[gu * st.caps + i] = sstack[i];
@@ -413,132 +423,231 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
 }
 
 // ------------------------------------------------------------------------------ moves
-// Grid-stride over the move list; one CTA per move.
+// Grid-stride over the move list; one CTA per move.  The host ledger and store are mapped
+// pinned memory, read and written directly over the host link.
 //  pack:      bf16 slot -> 2-bit slot (eq. (2), b = 2: keys per channel over the window's
-//             valid tokens, values per token over head_dim), then the 2-bit slot and the
-//             bf16 slot are copied to the host ledger / store entry (mapped pinned memory)
+//             valid tokens, values per token over head_dim), and the codes to the host ledger;
+//             from Pinned also the exact bf16 copy to the store entry
+//  copy:      bf16 slot -> host store entry (a Pinned window kept Full)
 //  reuse:     host ledger entry -> 2-bit slot
 //  promotion: host store entry -> bf16 slot
 constexpr int MOVE_THREADS = 256;
+constexpr int MOVE_CTAS_PER_SM = 3;
 
-__device__ __forceinline__ void copy16(uint8_t* dst, const uint8_t* src, int bytes, int tid, int nthr) {
-  for (int o = tid * 16; o < bytes; o += nthr * 16)
-    *reinterpret_cast<uint4*>(dst + o) = *reinterpret_cast<const uint4*>(src + o);
+// Copy `bytes` (a multiple of 16) with every thread's 16-byte loads issued before its stores,
+// so a CTA keeps up to 4 x 4 KB in flight (the host side of a move is latency-bound).
+__device__ __forceinline__ void copy16(uint8_t* dst, const uint8_t* src, int bytes, int tid) {
+  constexpr int STEP = MOVE_THREADS * 16;
+  for (int o0 = 0; o0 < bytes; o0 += 4 * STEP) {
+    uint4 x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int o = o0 + i * STEP + tid * 16;
+      if (o < bytes) x[i] = *reinterpret_cast<const uint4*>(src + o);
+    }
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int o = o0 + i * STEP + tid * 16;
+      if (o < bytes) *reinterpret_cast<uint4*>(dst + o) = x[i];
+    }
+  }
 }
 
-// eq. (2): code = clamp(rint((x - z) / s), 0, 3) with z = min, s = (max - min) / 3 in float32
+// eq. (2): code = clamp(rint((x - z) / s), 0, 3) with z = min, s = (max - min) / 3 in float32.
+// The quotient is decided as the IEEE float32 division would decide it: a fast estimate (a few
+// ulp from the true quotient) settles every value that is not within 1e-5 of a half-integer;
+// those few, and scales outside [1e-30, 1e30], take the correctly rounded division.
 __device__ __forceinline__ unsigned quant_code(float x, float z, float s) {
   if (s == 0.f) return 0u;
-  float qv = rintf(__fdiv_rn(__fsub_rn(x, z), s));
+  const float d = __fsub_rn(x, z);
+  float qv = __fdividef(d, s);
+  const float fr = qv - floorf(qv);
+  if (fabsf(fr - 0.5f) < 1e-5f || !(s >= 1e-30f && s <= 1e30f)) qv = __fdiv_rn(d, s);
+  qv = rintf(qv);
   qv = fminf(fmaxf(qv, 0.f), 3.f);
   return (unsigned)qv;
 }
 
-__global__ void __launch_bounds__(MOVE_THREADS) qe_move_kernel(State st, const Move* __restrict__ moves,
-                                                               const int* __restrict__ n_moves) {
+__device__ __forceinline__ float bf16_at(const uint8_t* raw, int off) {
+  return __uint_as_float((unsigned)*reinterpret_cast<const uint16_t*>(raw + off) << 16);
+}
+
+__global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel(State st, const Move* __restrict__ moves,
+                                                                                const int* __restrict__ n_moves) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int n = *n_moves;
   const Geo g = st.geo;
   const int D = g.D, W = g.W;
-  float* kf = reinterpret_cast<float*>(sm);          // [W][D]
-  float* vf = kf + W * D;                            // [W][D]
-  float* kz = vf + W * D;                            // [D]
-  float* ks = kz + D;                                // [D]
-  float* vz = ks + D;                                // [W]
-  float* vs = vz + W;                                // [W]
-  unsigned* words = reinterpret_cast<unsigned*>(vs + W);   // [2 * W * D / 16]
+  uint8_t* raw = sm;                                                   // the bf16 slot [4 W D]
+  float* kz = reinterpret_cast<float*>(sm + g.bslot_bytes());          // [D]
+  float* ks = kz + D;                                                  // [D]
+  float* vz = ks + D;                                                  // [W]
+  float* vs = vz + W;                                                  // [W]
   const int tid = threadIdx.x;
   for (int mi = blockIdx.x; mi < n; mi += gridDim.x) {
     const Move mv = moves[mi];
     const long long gu = mv.gu;
     {
       const bool ok_gu = gu >= 0 && gu < (long long)st.units * st.n_layers;
-      const bool ok = ok_gu && mv.win >= 0 && mv.win < st.maxw &&
-                      (mv.kind == 2 ? (mv.src >= 0 && mv.src < st.caps && mv.dst > 0 && mv.dst < st.capb)
-                                    : (mv.dst >= 0 && mv.dst < st.capq &&
-                                       (mv.kind == 1 ? (mv.src >= 0 && mv.src < st.caps)
-                                                     : (mv.src > 0 && mv.src < st.capb && mv.sent >= 0 &&
-                                                        mv.sent < st.caps))));
+      const bool src_store = mv.src >= 0 && mv.src < st.caps, src_bf16 = mv.src > 0 && mv.src < st.capb;
+      const bool dst_q = mv.dst >= 0 && mv.dst < st.capq, sent_ok = mv.sent >= 0 && mv.sent < st.caps;
+      bool ok = ok_gu && mv.win >= 0 && mv.win < st.maxw;
+      switch (mv.kind) {
+        case MOVE_PROMOTE: ok = ok && src_store && mv.dst > 0 && mv.dst < st.capb; break;
+        case MOVE_REUSE: ok = ok && src_store && dst_q; break;
+        case MOVE_PACK_COPY:
+        case MOVE_PACK: ok = ok && src_bf16 && dst_q && sent_ok; break;
+        case MOVE_COPY: ok = ok && src_bf16 && mv.dst >= 0 && mv.dst < st.caps; break;
+        default: ok = false;
+      }
       if (!ok) {
         if (tid == 0) atomicOr(st.err, ERR_MOVES);
         continue;
       }
     }
-    if (mv.kind == 2) {
+    if (mv.kind == MOVE_PROMOTE) {
       const uint8_t* src = st.hstore + (gu * st.caps + mv.src) * (long long)g.bslot_bytes();
       uint8_t* dst = st.bslab + (gu * st.capb + mv.dst) * (long long)g.bslot_bytes();
-      copy16(dst, src, g.bslot_bytes(), tid, MOVE_THREADS);
+      copy16(dst, src, g.bslot_bytes(), tid);
       continue;
     }
-    if (mv.kind == 1) {
+    if (mv.kind == MOVE_COPY) {
+      const uint8_t* src = st.bslab + (gu * st.capb + mv.src) * (long long)g.bslot_bytes();
+      uint8_t* dst = st.hstore + (gu * st.caps + mv.dst) * (long long)g.bslot_bytes();
+      copy16(dst, src, g.bslot_bytes(), tid);
+      continue;
+    }
+    if (mv.kind == MOVE_REUSE) {
       const uint8_t* src = st.hledger + (gu * st.caps + mv.src) * (long long)g.qslot_bytes();
       uint8_t* dst = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
-      copy16(dst, src, g.qslot_bytes(), tid, MOVE_THREADS);
+      copy16(dst, src, g.qslot_bytes(), tid);
       continue;
     }
-    // ---- pack
+    // ---- pack: the bf16 slot into shared memory, and its exact copy into the host store
     const uint8_t* bs = st.bslab + (gu * st.capb + mv.src) * (long long)g.bslot_bytes();
     uint8_t* qs = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
-    const int lo = (mv.win == 0) ? st.n_sink : 0;
-    for (int e = tid; e < W * D; e += MOVE_THREADS) {
-      const int r = e / D, c = e - r * D;
-      const uint16_t kb = *reinterpret_cast<const uint16_t*>(bs + bf16_k_off(g, r, c));
-      const uint16_t vb = *reinterpret_cast<const uint16_t*>(bs + bf16_v_off(g, r, c));
-      kf[e] = __uint_as_float((unsigned)kb << 16);
-      vf[e] = __uint_as_float((unsigned)vb << 16);
+    uint8_t* hs = st.hstore + (gu * st.caps + mv.sent) * (long long)g.bslot_bytes();
+    uint8_t* hl = st.hledger + (gu * st.caps + mv.sent) * (long long)g.qslot_bytes();
+    const bool copy_exact = mv.kind == MOVE_PACK_COPY;
+    {
+      constexpr int STEP = MOVE_THREADS * 16;
+      for (int o0 = 0; o0 < g.bslot_bytes(); o0 += 4 * STEP) {
+        uint4 x[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int o = o0 + i * STEP + tid * 16;
+          if (o < g.bslot_bytes()) x[i] = *reinterpret_cast<const uint4*>(bs + o);
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+          const int o = o0 + i * STEP + tid * 16;
+          if (o < g.bslot_bytes()) {
+            *reinterpret_cast<uint4*>(raw + o) = x[i];
+            if (copy_exact) *reinterpret_cast<uint4*>(hs + o) = x[i];
+          }
+        }
+      }
     }
     __syncthreads();
-    // key groups: one per channel over rows [lo, W); value groups: one per token over D
+    const int lo = (mv.win == 0) ? st.n_sink : 0;
+    // key groups: one per channel over rows [lo, W)
     for (int c = tid; c < D; c += MOVE_THREADS) {
-      float mn = kf[lo * D + c], mx = mn;
+      float mn = bf16_at(raw, bf16_k_off(g, lo, c)), mx = mn;
       for (int r = lo + 1; r < W; ++r) {
-        const float x = kf[r * D + c];
+        const float x = bf16_at(raw, bf16_k_off(g, r, c));
         mn = fminf(mn, x);
         mx = fmaxf(mx, x);
       }
       kz[c] = mn;
       ks[c] = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
     }
-    for (int r = tid; r < W; r += MOVE_THREADS) {
-      float mn = vf[r * D], mx = mn;
-      for (int c = 1; c < D; ++c) {
-        const float x = vf[r * D + c];
-        mn = fminf(mn, x);
-        mx = fmaxf(mx, x);
+    // value groups: one per token over D channels; 8 threads per token, shuffle-reduced
+    for (int t0 = 0; t0 < W; t0 += MOVE_THREADS / 8) {
+      const int r = t0 + tid / 8, part = tid % 8;
+      float mn = INFINITY, mx = -INFINITY;
+      if (r < W) {
+        for (int c = part; c < D; c += 8) {
+          const float x = bf16_at(raw, bf16_v_off(g, r, c));
+          mn = fminf(mn, x);
+          mx = fmaxf(mx, x);
+        }
       }
-      vz[r] = (r < lo) ? 0.f : mn;
-      vs[r] = (r < lo) ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
-    }
-    const int nwords = 2 * W * D / 16;
-    for (int i = tid; i < nwords; i += MOVE_THREADS) words[i] = 0u;
-    __syncthreads();
-    // codes into their fragment words (word index = byte offset / 4)
-    for (int e = tid; e < W * D; e += MOVE_THREADS) {
-      const int r = e / D, c = e - r * D;
-      const unsigned ck = (r < lo) ? 0u : quant_code(kf[e], kz[c], ks[c]);
-      const unsigned cv = (r < lo) ? 0u : quant_code(vf[e], vz[r], vs[r]);
-      const CodePos pk = kcode_pos(g, r, c);
-      const CodePos pv = vcode_pos(g, r, c);
-      atomicOr(&words[pk.byte >> 2], ck << pk.bit);
-      atomicOr(&words[pv.byte >> 2], cv << pv.bit);
+#pragma unroll
+      for (int o = 4; o; o >>= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      if (r < W && part == 0) {
+        vz[r] = (r < lo) ? 0.f : mn;
+        vs[r] = (r < lo) ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      }
     }
     __syncthreads();
-    for (int i = tid; i < nwords; i += MOVE_THREADS) reinterpret_cast<unsigned*>(qs)[i] = words[i];
+    // codes: each thread assembles whole 32-bit words.  Word (lane, wi) of a code block holds
+    // fragments 2 wi and 2 wi + 1 of that lane; the bf16 slot stores the same fragment of the
+    // same lane as one 16-byte vector (element (reg, e) at bits 32 reg + 16 e), so a word needs
+    // two vector loads and its code (reg, f, e) goes to bit 8 reg + 2 f + 4 e.
+    const int wpl = g.wpl(), cw = g.cw(), KS = D / 16, KT = W / 16;
+    for (int t = tid; t < 64 * wpl; t += MOVE_THREADS) {
+      const bool value = t >= 32 * wpl;
+      const int tt = value ? t - 32 * wpl : t;
+      const int lane = tt & 31, wi = tt >> 5;
+      const int widx = ((wi / cw) * 32 + lane) * cw + (wi - (wi / cw) * cw);
+      const int a = lane >> 2, b = 2 * (lane & 3);
+      unsigned word = 0u;
+#pragma unroll
+      for (int f = 0; f < 2; ++f) {
+        const int F = 2 * wi + f;
+        uint4 x;
+        int r0, c0;   // row / column of element (reg 0, e 0) of this lane's fragment
+        if (!value) {
+          const int mt = F / KS, kst = F - mt * KS;
+          x = *reinterpret_cast<const uint4*>(raw + mt * g.sub_bytes() + kst * 512 + lane * 16);
+          r0 = 16 * mt + a;
+          c0 = 16 * kst + b;
+        } else {
+          const int mc = F / KT, kt = F - mc * KT;
+          x = *reinterpret_cast<const uint4*>(raw + kt * g.sub_bytes() + 32 * D + mc * 512 + lane * 16);
+          r0 = 16 * kt + b;   // token
+          c0 = 16 * mc + a;   // channel
+        }
+        const unsigned xr[4] = {x.x, x.y, x.z, x.w};
+#pragma unroll
+        for (int reg = 0; reg < 4; ++reg) {
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const float xv = __uint_as_float(e ? (xr[reg] & 0xFFFF0000u) : (xr[reg] << 16));
+            unsigned code;
+            if (!value) {
+              const int r = r0 + 8 * (reg & 1), c = c0 + e + 8 * (reg >> 1);
+              code = r >= lo ? quant_code(xv, kz[c], ks[c]) : 0u;
+            } else {
+              const int r = r0 + e + 8 * (reg >> 1);
+              code = r >= lo ? quant_code(xv, vz[r], vs[r]) : 0u;
+            }
+            word |= code << (8 * reg + 2 * f + 4 * e);
+          }
+        }
+      }
+      const int wo = (value ? g.kcode_bytes() / 4 : 0) + widx;
+      reinterpret_cast<unsigned*>(qs)[wo] = word;
+      reinterpret_cast<unsigned*>(hl)[wo] = word;
+    }
     for (int c = tid; c < D; c += MOVE_THREADS) {
-      reinterpret_cast<float*>(qs + g.off_kmin())[kparam_pos(c)] = kz[c];
-      reinterpret_cast<float*>(qs + g.off_kscale())[kparam_pos(c)] = ks[c];
+      const int pc = kparam_pos(c);
+      reinterpret_cast<float*>(qs + g.off_kmin())[pc] = kz[c];
+      reinterpret_cast<float*>(qs + g.off_kscale())[pc] = ks[c];
+      reinterpret_cast<float*>(hl + g.off_kmin())[pc] = kz[c];
+      reinterpret_cast<float*>(hl + g.off_kscale())[pc] = ks[c];
     }
     for (int r = tid; r < W; r += MOVE_THREADS) {
-      reinterpret_cast<float*>(qs + g.off_vmin())[vparam_pos(g, r)] = vz[r];
-      reinterpret_cast<float*>(qs + g.off_vscale())[vparam_pos(g, r)] = vs[r];
+      const int pr = vparam_pos(g, r);
+      reinterpret_cast<float*>(qs + g.off_vmin())[pr] = vz[r];
+      reinterpret_cast<float*>(qs + g.off_vscale())[pr] = vs[r];
+      reinterpret_cast<float*>(hl + g.off_vmin())[pr] = vz[r];
+      reinterpret_cast<float*>(hl + g.off_vscale())[pr] = vs[r];
     }
-    __syncthreads();
-    // the ledger copy of the codes and the exact bf16 copy go to the mapped host store
-    copy16(st.hledger + (gu * st.caps + mv.sent) * (long long)g.qslot_bytes(), qs, g.qslot_bytes(), tid,
-           MOVE_THREADS);
-    copy16(st.hstore + (gu * st.caps + mv.sent) * (long long)g.bslot_bytes(), bs, g.bslot_bytes(), tid,
-           MOVE_THREADS);
-    __syncthreads();
+    __syncthreads();   // shared memory is reused by this CTA's next move
   }
 }
 
@@ -566,7 +675,7 @@ cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t
 }
 
 size_t route_smem_bytes(const State& st) {
-  return (size_t)ROUTE_MAX_CAND * (8 + 4 + 1) + (size_t)(st.capb + st.capq + st.caps) * 4 + 16;
+  return (size_t)ROUTE_MAX_CAND * (8 + 4 * 4 + 2) + (size_t)(st.capb + st.capq + st.caps) * 4 + 16;
 }
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
@@ -576,11 +685,11 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
 
 size_t move_smem_bytes(const State& st) {
   const int W = st.geo.W, D = st.geo.D;
-  return (size_t)(2 * W * D + 2 * D + 2 * W) * 4 + (size_t)(2 * W * D / 16) * 4;
+  return (size_t)st.geo.bslot_bytes() + (size_t)(2 * D + 2 * W) * 4;
 }
 
 cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves, int n_sm, cudaStream_t s) {
-  qe_move_kernel<<<n_sm * 2, MOVE_THREADS, move_smem_bytes(st), s>>>(st, moves, n_moves);
+  qe_move_kernel<<<n_sm * MOVE_CTAS_PER_SM, MOVE_THREADS, move_smem_bytes(st), s>>>(st, moves, n_moves);
   return cudaGetLastError();
 }
 
