@@ -224,7 +224,7 @@ def run_ours(args):
     cache.qe_layer_info_sync()
     timed = [make_inputs(t + 1 + i) for i in range(K)]
     torch.cuda.synchronize(dev)
-    launches_per_step = 2 * Lyr * 1 + Lyr          # append, attention, combine per layer
+    launches_per_step = 2 * Lyr                    # attention (with the append) and combine per layer
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -311,8 +311,8 @@ def run_ours(args):
         "config": {
             **workload_config(wl, world),
             "timed_decode_steps": [omega + W + 1, omega + W + K],
-            "launch": "one CUDA graph per decode step (%d layers x append, attention, combine; routing every "
-                      "Omega)" % Lyr,
+            "launch": "one CUDA graph per decode step (%d layers x attention with the token append, combine; "
+                      "routing every Omega)" % Lyr,
             "kv_per_layer_unit": {"full": info.n_full, "quant": info.n_quant, "pinned": info.n_pinned},
             "l2": "inputs larger than L2: %.0f MB read per layer launch, %.1f GB per step" % (
                 info.attn_bytes / 1e6, info.attn_bytes * Lyr / 1e9),

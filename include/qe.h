@@ -124,6 +124,11 @@ const char* qe_last_error(qe_handle h);
  * Windows reached for the first time start Pinned with score 0 (QEvict notes
  * §2 Figure 1: every window starts in full precision).  Prefill is one call
  * with n_tokens = prompt length; a decode step appends 1 token.
+ * A single-token append launches nothing: the next qe_decode_step of the layer
+ * writes the token inside its attention launch (any other call on the layer
+ * writes it first).  Device k and v must therefore stay valid until the
+ * stream reaches that call; host k and v are copied to the layer's own
+ * staging buffers at once.
  * Errors: QE_ERR_CAPACITY if the length would pass max_context. */
 qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_tokens, int flags);
 

@@ -140,12 +140,16 @@ __device__ __forceinline__ int2 list_entry(const AttnParams& p, const Lay& y, in
 
 // descriptor of tile (u, i) from its list entry; false if it has no valid row (or is corrupt).
 // d.i is the tile's index in the per-unit log-sum-exp array: bf16 sub-tiles first, then 2-bit.
-__device__ __forceinline__ bool describe(const AttnParams& p, const Lay& y, int u, int i, int2 ent, TileDesc& d) {
+// inew / opens: the tile of this step's appended token, and whether that token opens its window
+// (then the other sub-tiles of the window, entry nbw - 1, are empty and their entry unread).
+__device__ __forceinline__ bool describe(const AttnParams& p, const Lay& y, int u, int i, int2 ent, TileDesc& d,
+                                         int inew, bool opens) {
   const State& st = p.st;
   const int W = st.geo.W;
   const int sub_tiles = W / 16;
   int loc;
   const bool is_q = tile_kind(y, i, loc);
+  if (opens && !is_q && i != inew && loc / sub_tiles == y.nbw - 1) return false;
   d.u = u;
   d.i = is_q ? y.nbt + loc : loc;
   d.win = ent.x;
@@ -192,6 +196,83 @@ __device__ __forceinline__ const uint8_t* tile_src(const AttnParams& p, const Ti
   }
   bytes = st.geo.qslot_bytes();
   return st.qslab + (gu * st.capq + d.slot) * (long long)st.geo.qslot_bytes();
+}
+
+// Index (in the interleaved tile order) of the bf16 sub-tile that holds the newest token,
+// position L - 1: the sink tile, or the sub-tile of the last bf16 list entry (the current
+// window has the highest index of the bf16 windows).  Identical for every unit of the layer.
+__device__ __forceinline__ int newest_token_tile(const State& st, const Lay& y) {
+  const int P = y.L - 1, W = st.geo.W;
+  int loc = 0;   // bf16 tile number (bf16 list order)
+  if (P >= st.n_sink) loc = (y.nbw - 1) * (W / 16) + (P - (P / W) * W) / 16;
+  // tile i is bf16 tile number i - q_before(i); find the smallest i with (i + 1) - q_before(i + 1) > loc
+  int lo = 0, hi = y.ntiles - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi) >> 1;
+    if (mid + 1 - q_before(y, mid + 1) > loc) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
+// The decode step's own append, done at the start of the launch by the one warp that owns the
+// tile holding the new token: open the token's window if the token starts it, then write K and
+// V into the slot in fragment order.  The token's values are loaded together with the slot
+// lookup (one round trip).  The stores are made visible at device scope and ordered, by the
+// async-proxy fence, before the bulk copy that later reads the tile.  Returns the slot, -1 on
+// error.
+__device__ __forceinline__ int append_newest(const AttnParams& p, const Lay& y, int u, int lane) {
+  const State& st = p.st;
+  const Geo& g = st.geo;
+  const int W = g.W, D = g.D;
+  const long long gu = (long long)p.layer * st.units + u;
+  const int P = y.L - 1, j = P / W;
+  constexpr int MAXPAIRS = 2;   // channel pairs per lane (D <= 128)
+  unsigned kk[MAXPAIRS];
+  uint16_t v0[MAXPAIRS], v1[MAXPAIRS];
+  const uint16_t* k = p.knew + (size_t)u * D;
+  const uint16_t* v = p.vnew + (size_t)u * D;
+#pragma unroll
+  for (int i = 0; i < MAXPAIRS; ++i) {
+    const int c = 2 * lane + 64 * i;
+    if (c < D) {
+      kk[i] = *reinterpret_cast<const unsigned*>(k + c);
+      v0[i] = v[c];
+      v1[i] = v[c + 1];
+    }
+  }
+  int slot = -1;
+  if (lane == 0) {
+    if (P >= st.max_context || j >= st.maxw) {
+      atomicOr(st.err, ERR_CAPACITY);
+    } else {
+      if (P % W == 0) slot = open_window(st, gu, j, y.nbw - 1);
+      else slot = st.bslot[gu * st.maxw + j];
+      if (P < st.n_sink && slot >= 0) slot = 0;
+      if (slot < 0 || slot >= st.capb || (slot == 0 && P >= st.n_sink)) {
+        atomicOr(st.err, ERR_TABLE);
+        slot = -1;
+      }
+    }
+  }
+  slot = __shfl_sync(0xffffffffu, slot, 0);
+  if (slot >= 0) {
+    const int row = P < st.n_sink ? P : P - j * W;
+    uint8_t* base = st.bslab + (gu * st.capb + slot) * (long long)g.bslot_bytes();
+#pragma unroll
+    for (int i = 0; i < MAXPAIRS; ++i) {
+      const int c = 2 * lane + 64 * i;
+      if (c < D) {
+        *reinterpret_cast<unsigned*>(base + bf16_k_off(g, row, c)) = kk[i];
+        *reinterpret_cast<uint16_t*>(base + bf16_v_off(g, row, c)) = v0[i];
+        *reinterpret_cast<uint16_t*>(base + bf16_v_off(g, row, c + 1)) = v1[i];
+      }
+    }
+    __threadfence();
+    asm volatile("fence.proxy.async;" ::: "memory");
+  }
+  __syncwarp();
+  return slot;
 }
 
 template <int D, int W>
@@ -378,6 +459,18 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   }
   const int u_first = (int)(x_lo / y.Cu);
   const int u_last = (int)((x_hi - 1) / y.Cu);
+  // This decode step's appended token sits in tile inew of every unit; the warp that owns that
+  // tile writes it first.  When the token opens its window, only that warp may use the window's
+  // list entry (it writes it): the window's other sub-tiles are empty (rows past the token) and
+  // describe() drops them without a look at the entry.
+  const int inew = p.pend > 0 ? newest_token_tile(p.st, y) : -1;
+  const bool opens = p.pend > 0 && (y.L - 1) % p.st.geo.W == 0;
+  if (inew >= 0) {
+    for (int u = u_first; u <= u_last; ++u) {
+      const long long x = tile_start(p, y, u, inew);
+      if (x >= x_lo && x < x_hi) append_newest(p, y, u, lane);
+    }
+  }
 
   uint8_t* stage_base = smem + (size_t)warp * NST * S::STAGE;
   if (lane == 0) {
@@ -400,7 +493,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       const bool inr = u < p.st.units && tile_start(p, y, u, i) < x_hi;
       TileDesc d;
       bool ok = false;
-      if (inr) ok = describe(p, y, u, i, list_entry(p, y, u, i, SUBT), d);
+      if (inr) ok = describe(p, y, u, i, list_entry(p, y, u, i, SUBT), d, inew, opens);
       const unsigned vb = __ballot_sync(0xffffffffu, ok);
       if (ok) {
         BatchDesc bd;

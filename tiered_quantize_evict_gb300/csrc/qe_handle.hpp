@@ -15,6 +15,8 @@ namespace qe {
 struct LayerMirror {
   int L = 0;
   int pending = 0;    // single-token appends whose length the device has not committed yet
+  const uint16_t* pk = nullptr;   // pending token's K and V (device): written by the next decode step
+  const uint16_t* pv = nullptr;
   int routed_upto = 0;
   int n_full = 0;
   int n_quant = 0;
@@ -45,6 +47,7 @@ struct qe_handle_s {
   int* n_moves = nullptr;
   int max_moves = 0;
   // staging for host pointers
+  uint16_t* tok_stage = nullptr;   // [n_layers][2][units][D]: single-token appends from host memory
   void* stage[4] = {nullptr, nullptr, nullptr, nullptr};
   size_t stage_bytes[4] = {0, 0, 0, 0};
   // pinned host store

@@ -83,13 +83,16 @@ qe_status ensure_stage(qe_handle h, int i, size_t bytes) {
 
 void fill_info(qe_handle h, const LayerMirror& m, qe_layer_info* info);
 
-// a single-token append that no decode step consumed: advance the device length now
+// a single-token append that no decode step consumed: write the token and advance the device
+// length now
 qe_status commit_pending(qe_handle h, int layer) {
   LayerMirror& m = h->lay[layer];
   if (!m.pending) return QE_OK;
+  QE_CK(h, qe::launch_append(h->st, layer, 1, m.pk, m.pv, h->n_sm, h->stream));
   QE_CK(h, qe::launch_commit_length(h->st, layer, m.pending, h->stream));
-  ++h->launches;
+  h->launches += 2;
   m.pending = 0;
+  m.pk = m.pv = nullptr;
   return QE_OK;
 }
 
@@ -103,7 +106,7 @@ void free_all(qe_handle h) {
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_top, s.qfree,
                   s.qfree_top, s.sfree, s.sfree_top, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
-                  h->lay_buf};
+                  h->lay_buf, h->tok_stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -215,6 +218,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(h->part_ml, (size_t)h->units * h->pslots_cap * G, "partial stats");
   QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
   QE_ALLOC(h->lay_buf, (size_t)c.n_layers * 4, "layer counts");
+  QE_ALLOC(h->tok_stage, (size_t)c.n_layers * 2 * h->units * c.head_dim, "token staging");
   h->max_moves = h->units * st.caps + 16;
   {
     void* mp = nullptr;
@@ -312,9 +316,27 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
   if (m.L + n_tokens > h->cfg.max_context)
     return fail(h, QE_ERR_CAPACITY, "append of %d tokens passes max_context %d (length %d)", n_tokens,
                 h->cfg.max_context, m.L);
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
   const size_t bytes = (size_t)h->units * n_tokens * h->cfg.head_dim * 2;
   const uint16_t* kd = static_cast<const uint16_t*>(k);
   const uint16_t* vd = static_cast<const uint16_t*>(v);
+  if (n_tokens == 1) {
+    // The next decode step of this layer writes the token (inside its attention launch) and its
+    // combine commits the length; host tokens wait in the layer's own staging slots.
+    if (flags & QE_HOST_PTRS) {
+      uint16_t* ks = h->tok_stage + (size_t)layer * 2 * h->units * h->cfg.head_dim;
+      uint16_t* vs = ks + (size_t)h->units * h->cfg.head_dim;
+      QE_CK(h, cudaMemcpyAsync(ks, k, bytes, cudaMemcpyHostToDevice, h->stream));
+      QE_CK(h, cudaMemcpyAsync(vs, v, bytes, cudaMemcpyHostToDevice, h->stream));
+      kd = ks;
+      vd = vs;
+    }
+    m.pending = 1;
+    m.pk = kd;
+    m.pv = vd;
+    m.L += 1;
+    return QE_OK;
+  }
   if (flags & QE_HOST_PTRS) {
     if ((s = ensure_stage(h, 0, bytes)) != QE_OK || (s = ensure_stage(h, 1, bytes)) != QE_OK) return s;
     QE_CK(h, cudaMemcpyAsync(h->stage[0], k, bytes, cudaMemcpyHostToDevice, h->stream));
@@ -322,10 +344,8 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
     kd = static_cast<const uint16_t*>(h->stage[0]);
     vd = static_cast<const uint16_t*>(h->stage[1]);
   }
-  if ((s = commit_pending(h, layer)) != QE_OK) return s;
   QE_CK(h, qe::launch_append(h->st, layer, n_tokens, kd, vd, h->n_sm, h->stream));
-  h->launches += n_tokens == 1 ? 1 : 2;
-  if (n_tokens == 1) m.pending = 1;   // counted by the next decode step, committed by its combine
+  h->launches += 2;
   m.L += n_tokens;
   return QE_OK;
 }
@@ -352,8 +372,11 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   p.st = h->st;
   p.layer = layer;
   p.pend = m.pending;
+  p.knew = m.pk;
+  p.vnew = m.pv;
   p.lay_out = h->lay_buf + 4 * layer;
   m.pending = 0;
+  m.pk = m.pv = nullptr;
   p.cb = h->cost_b;
   p.cq = h->cost_q;
   p.pslots = h->pslots_cap;

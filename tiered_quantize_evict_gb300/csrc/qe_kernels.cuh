@@ -15,6 +15,8 @@ struct AttnParams {
   State st;
   int layer;
   int pend;              // single-token appends not yet counted in the header's length (0 or 1)
+  const uint16_t* knew;  // pend = 1: the token's K and V [B][Hkv][D] bf16, written by this launch
+  const uint16_t* vnew;
   int* lay_out;          // [4]: length, bf16 entries, 2-bit entries, tiles per unit, for the combine
   int cb, cq;            // cost of one 16-token bf16 tile and of one 2-bit window
   int pslots;            // partial slots per unit (>= warps whose range meets one unit)
@@ -62,6 +64,25 @@ struct Move {
 };
 // bit of a window's store entry number that says its ledger (2-bit codes) exists
 constexpr int SENT_LEDGER = 1 << 30;
+
+#if defined(__CUDACC__)
+// Open window j of unit gu when its first token arrives: pop a bf16 slot, Pinned, score 0,
+// entry nb of the bf16 list.  Returns the slot (-1 and the error flag if the pool is empty).
+__device__ __forceinline__ int open_window(const State& st, long long gu, int j, int nb) {
+  int top = st.bfree_top[gu];
+  if (top <= 0 || nb >= st.capb) {
+    atomicOr(st.err, ERR_FREELIST);
+    return -1;
+  }
+  const int s = st.bfree[gu * st.capb + (--top)];
+  st.bfree_top[gu] = top;
+  st.bslot[gu * st.maxw + j] = s;
+  st.tier[gu * st.maxw + j] = TIER_PINNED;
+  st.score[gu * st.maxw + j] = 0.f;
+  st.blist[gu * st.capb + nb] = make_int2(j, s);
+  return s;
+}
+#endif
 
 struct RouteParams {
   State st;

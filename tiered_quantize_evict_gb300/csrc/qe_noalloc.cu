@@ -104,6 +104,8 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   p.st = h->st;
   p.layer = layer;
   p.pend = m.pending;
+  p.knew = m.pk;
+  p.vnew = m.pv;
   p.lay_out = lay;
   p.cb = h->cost_b;
   p.cq = h->cost_q;
@@ -117,6 +119,7 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   e = qe::launch_decode_attn(p, grid, h->stream);
   if (e != cudaSuccess) return na_fail(h, QE_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));
   m.pending = 0;
+  m.pk = m.pv = nullptr;
   qe::CombineParams cp{};
   cp.st = h->st;
   cp.layer = layer;

@@ -30,22 +30,6 @@ __device__ __forceinline__ void commit_length(const State& st, int layer, int L_
   }
 }
 
-// open window j of unit gu: pop a bf16 slot, Pinned, score 0, entry `nb` of the bf16 list
-__device__ __forceinline__ int open_window(const State& st, long long gu, int j, int nb) {
-  int top = st.bfree_top[gu];
-  if (top <= 0 || nb >= st.capb) {
-    atomicOr(st.err, ERR_FREELIST);
-    return -1;
-  }
-  const int s = st.bfree[gu * st.capb + (--top)];
-  st.bfree_top[gu] = top;
-  st.bslot[gu * st.maxw + j] = s;
-  st.tier[gu * st.maxw + j] = TIER_PINNED;
-  st.score[gu * st.maxw + j] = 0.f;
-  st.blist[gu * st.capb + nb] = make_int2(j, s);
-  return s;
-}
-
 __device__ __forceinline__ void write_token(const State& st, long long gu, int slot, int row, int c, unsigned kk,
                                             uint16_t v0, uint16_t v1) {
   uint8_t* base = st.bslab + (gu * st.capb + slot) * (long long)st.geo.bslot_bytes();
@@ -54,10 +38,10 @@ __device__ __forceinline__ void write_token(const State& st, long long gu, int s
   *reinterpret_cast<uint16_t*>(base + bf16_v_off(st.geo, row, c + 1)) = v1;
 }
 
-// One decode token: APPEND1_UNITS units per CTA, one thread per channel pair.  The token that
-// starts a window opens it (QEvict notes §2 Figure 1: every window starts in full precision).
-// The length is not advanced here: the next decode step counts this token as pending and its
-// combine launch commits the new length (see qe_decode_step), so the launch stays step-invariant.
+// One single-token append that no decode step consumed (a decode step writes its pending
+// token itself, inside the attention launch): APPEND1_UNITS units per CTA, one thread per
+// channel pair.  The token that starts a window opens it (QEvict notes §2 Figure 1: every
+// window starts in full precision).  The length is advanced by a separate commit launch.
 constexpr int APPEND1_UNITS = 2;
 __global__ void qe_append1_kernel(State st, int layer, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v) {
   __shared__ int s_slot[APPEND1_UNITS];
