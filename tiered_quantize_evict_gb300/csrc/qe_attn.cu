@@ -438,14 +438,9 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   // the layer's step-dependent counts live in shared memory (read when a batch of tiles is
   // described), not in registers the tile loop needs
   __shared__ Lay s_lay;
-  if (threadIdx.x == 0) {
-    s_lay = make_lay(p.st, p.layer, p.pend, p.cb, p.cq, gridDim.x * ATTN_WARPS);
-    if (blockIdx.x == 0) {   // the combine launch reads these instead of the header
-      p.lay_out[0] = s_lay.L;
-      p.lay_out[1] = s_lay.nbw;
-      p.lay_out[2] = s_lay.nq;
-    }
-  }
+  if (threadIdx.x == 0) s_lay = make_lay(p.st, p.layer, p.pend, p.cb, p.cq, gridDim.x * ATTN_WARPS);
+  // the combine launch may start as CTAs of this one leave (it waits for this grid's completion)
+  griddep_launch_dependents();
   __syncthreads();
   const Lay& y = s_lay;
   const long long x_lo = (wg * y.C + y.NW - 1) / y.NW;
@@ -664,41 +659,42 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
 #pragma unroll
       for (int i = 0; i < 2 * MT; ++i) vs[i] *= 2.f;   // codes arrive as code / 2
-      // Q K^T over the unpacked key codes; fragment parity splits the accumulators
+      // Q K^T over the unpacked key codes (fragment F = mt KS + ks is half F % 2 of word F / 2);
+      // channel-step parity splits the accumulators, and consecutive mma go to different
+      // accumulators (2 MT independent chains)
       float acc[MT][2][4] = {};
       {
         unsigned wk[WPL];
         load_words<WPL, CW>(sp, lane, wk);
 #pragma unroll
-        for (int wi = 0; wi < WPL; ++wi) {
-          unsigned a[8];
-          unpack_word(wk[wi], a);
+        for (int ks = 0; ks < KS; ++ks)
 #pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            const int F = 2 * wi + f;
-            const int mt = F / KS, ks = F % KS;
-            mma_f16(acc[mt][f], a[4 * f + 0], a[4 * f + 1], a[4 * f + 2], a[4 * f + 3], qp[ks][0], qp[ks][1]);
+          for (int mt = 0; mt < MT; ++mt) {
+            const int F = mt * KS + ks;
+            unsigned a[4];
+            if (F & 1) unpack_half<1>(wk[F >> 1], a);
+            else unpack_half<0>(wk[F >> 1], a);
+            mma_f16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qp[ks][0], qp[ks][1]);
           }
-        }
       }
       unsigned Bp[MT][2];
       softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 2.f * p.scale_log2, rs, Bp, lse_out,
                                     G, lane);
-      // P V over the unpacked value codes (A = V^T: channel tiles x token steps)
+      // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
+      // the outer loop, so consecutive mma go to the MC independent accumulators
       {
         unsigned wv[WPL];
         load_words<WPL, CW>(sp + S::KCODE, lane, wv);
 #pragma unroll
-        for (int wi = 0; wi < WPL; ++wi) {
-          unsigned a[8];
-          unpack_word(wv[wi], a);
+        for (int kt = 0; kt < KT; ++kt)
 #pragma unroll
-          for (int f = 0; f < 2; ++f) {
-            const int F = 2 * wi + f;
-            const int mc = F / KT, kt = F % KT;
-            mma_f16(rs.O[mc], a[4 * f + 0], a[4 * f + 1], a[4 * f + 2], a[4 * f + 3], Bp[kt][0], Bp[kt][1]);
+          for (int mc = 0; mc < MC; ++mc) {
+            const int F = mc * KT + kt;
+            unsigned a[4];
+            if (F & 1) unpack_half<1>(wv[F >> 1], a);
+            else unpack_half<0>(wv[F >> 1], a);
+            mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
           }
-        }
       }
     }
     __syncwarp();
@@ -766,6 +762,11 @@ __device__ __forceinline__ void head_stats(const CombineParams& p, int u, int np
   lse = Mu + lg2(Ls);
 }
 
+// The combine is launched as a programmatic dependent of the attention launch: its CTAs start
+// as attention CTAs leave, compute the layer's counts from the header (the attention read the
+// same header and does not change it), load what the attention does not write (list entries
+// and scores of windows that existed before this step), then wait for the attention grid
+// (griddepcontrol.wait: completion and memory flush) before reading the partials.
 template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const CombineParams p) {
   const int u = blockIdx.x, part = blockIdx.y;
@@ -774,39 +775,34 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
   __shared__ float s_sc[MAXP];
   __shared__ float s_inv[4], s_lse[4];
   const int tid = threadIdx.x, warp = tid >> 5;
-  Lay y;   // the counts the attention launch used (its length includes the pending token)
-  y.L = p.lay_in[0];
-  y.nbw = p.lay_in[1];
-  y.nq = p.lay_in[2];
-  y.nbt = y.nbw * (p.st.geo.W / 16);
-  y.ntiles = y.nbt + y.nq;
-  y.Cu = (long long)y.nbt * p.cb + (long long)y.nq * p.cq;
-  y.C = y.Cu * p.st.units;
-  y.NW = p.NW;
+  const Lay y = make_lay(p.st, p.layer, p.pend, p.cb, p.cq, p.NW);   // counts incl. the pending token
   const int np = unit_partials(p, y, u);
-  if (u == 0 && part == 0 && threadIdx.x == 0) p.st.ldev[p.layer].L = y.L;   // commit the length
   if (part < G) {
-    // ---- output of head h = part
+    // ---- output of head h = part: every partial of this thread's channels is loaded at once
     const int h = part;
+    const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
+    const float* po = p.part_o + ((size_t)u * p.pslots * G + h) * D;
+    griddep_wait();
+    constexpr int PR = 32;   // partials held in registers per round
+    float v[PR];
+    const int c = tid;       // COMBINE_THREADS >= D
+    if (c < D) {
+#pragma unroll
+      for (int k = 0; k < PR; ++k) v[k] = k < np ? po[(size_t)k * G * D + c] : 0.f;
+    }
     if (warp == 0) {
       float inv, lse;
       head_stats(p, u, np, h, s_sc, inv, lse);
       if (tid == 0) s_inv[0] = inv;
     }
     __syncthreads();
-    const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
-    const float* po = p.part_o + ((size_t)u * p.pslots * G + h) * D;
-    for (int c = tid; c < D; c += COMBINE_THREADS) {
+    if (c < D) {
       float acc = 0.f;
-      for (int k0 = 0; k0 < np; k0 += 8) {
-        float v[8];
 #pragma unroll
-        for (int j = 0; j < 8; ++j)
-          v[j] = (k0 + j < np && s_sc[k0 + j] != 0.f) ? po[(size_t)(k0 + j) * G * D + c] : 0.f;
-#pragma unroll
-        for (int j = 0; j < 8; ++j)
-          if (k0 + j < np) acc = fmaf(v[j], s_sc[k0 + j], acc);
-      }
+      for (int k = 0; k < PR; ++k)
+        if (k < np && s_sc[k] != 0.f) acc = fmaf(v[k], s_sc[k], acc);
+      for (int k = PR; k < np; ++k)
+        if (s_sc[k] != 0.f) acc = fmaf(po[(size_t)k * G * D + c], s_sc[k], acc);
       const float o = acc * s_inv[0];
       const size_t oi = ((size_t)bb * p.st.Hq + kvh * G + h) * D + c;
       if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
@@ -814,58 +810,83 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
     }
     return;
   }
-  // ---- scores
+  // ---- scores: this thread's list entries and their scores before the wait (a window this
+  //      step opened, the last bf16 entry, is read after it: the attention launch wrote it)
+  const int W = p.st.geo.W, sub_tiles = W / 16;
+  const int nent = y.nbw + y.nq;
+  const bool opens = p.pend > 0 && (y.L - 1) % W == 0;
+  constexpr int EPT = 4;   // entries per thread per round
+  int2 ent[EPT];
+  float sc[EPT];
+  const int e0 = tid;
+  auto load_ent = [&](int e) -> int2 {
+    if (e < y.nbw) return p.st.blist[gu * p.st.capb + e];
+    if (e < nent) return p.st.qlist[gu * p.st.capq + (e - y.nbw)];
+    return make_int2(-1, -1);
+  };
+  const bool fits = nent <= COMBINE_THREADS * EPT;
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) {
+    const int e = e0 + j * COMBINE_THREADS;
+    const bool late = opens && e == y.nbw - 1;
+    ent[j] = (fits && !late) ? load_ent(e) : make_int2(-1, -1);
+    sc[j] = 0.f;
+    if (fits && !late && ent[j].x >= 0 && ent[j].x < p.st.maxw) sc[j] = p.st.score[gu * p.st.maxw + ent[j].x];
+  }
+  griddep_wait();
+  if (u == 0 && tid == 0) p.st.ldev[p.layer].L = y.L;   // commit the length (the attention has finished)
   if (warp < G) {
     float inv, lse;
     head_stats(p, u, np, warp, nullptr, inv, lse);
     if ((tid & 31) == 0) s_lse[warp] = lse;
   }
   __syncthreads();
-  const int W = p.st.geo.W, sub_tiles = W / 16;
-  const int nent = y.nbw + y.nq;
-  constexpr int EPT = 4;   // entries per thread per round: their loads are issued together
-  for (int e0 = tid; e0 < nent; e0 += COMBINE_THREADS * EPT) {
-    int2 ent[EPT];
+  for (int r0 = 0; r0 < nent; r0 += COMBINE_THREADS * EPT) {
+    if (!fits || r0 > 0) {   // entries beyond the preloaded round (or all of them): load now
 #pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = e0 + j * COMBINE_THREADS;
-      ent[j] = make_int2(-1, -1);
-      if (e < y.nbw) ent[j] = p.st.blist[gu * p.st.capb + e];
-      else if (e < nent) ent[j] = p.st.qlist[gu * p.st.capq + (e - y.nbw)];
+      for (int j = 0; j < EPT; ++j) {
+        const int e = r0 + e0 + j * COMBINE_THREADS;
+        ent[j] = load_ent(e);
+        sc[j] = (ent[j].x >= 0 && ent[j].x < p.st.maxw) ? p.st.score[gu * p.st.maxw + ent[j].x] : 0.f;
+      }
+    } else if (opens) {
+#pragma unroll
+      for (int j = 0; j < EPT; ++j)
+        if (e0 + j * COMBINE_THREADS == y.nbw - 1) {
+          ent[j] = load_ent(y.nbw - 1);
+          sc[j] = 0.f;   // opened by this step's attention launch with score 0
+        }
     }
     float dS[EPT];
-    int win[EPT];
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
-      const int e = e0 + j * COMBINE_THREADS;
-      win[j] = ent[j].x;
+      const int e = r0 + e0 + j * COMBINE_THREADS;
       dS[j] = 0.f;
-      if (e >= nent || win[j] < 0) continue;
+      if (e >= nent || ent[j].x < 0) continue;
       if (e < y.nbw) {
-        const int lo = (win[j] == 0) ? p.st.n_sink : 0;
-        int hi = y.L - win[j] * W;
+        const int lo = (ent[j].x == 0) ? p.st.n_sink : 0;
+        int hi = y.L - ent[j].x * W;
         hi = hi < W ? hi : W;
-        for (int s = 0; s < sub_tiles; ++s) {
-          const int tl = lo - 16 * s, th = hi - 16 * s;
+        for (int s2 = 0; s2 < sub_tiles; ++s2) {
+          const int tl = lo - 16 * s2, th = hi - 16 * s2;
           if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
-          const float* ls = p.lse + ((size_t)u * y.ntiles + e * sub_tiles + s) * G;
+          const float* ls = p.lse + ((size_t)u * y.ntiles + e * sub_tiles + s2) * G;
           for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
         }
       } else {
-        const float* ls = p.lse + ((size_t)u * y.ntiles + y.nbw * sub_tiles + (e - y.nbw)) * G;
+        const float* ls = p.lse + ((size_t)u * y.ntiles + y.nbt + (e - y.nbw)) * G;
         for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
       }
     }
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
-      const int e = e0 + j * COMBINE_THREADS;
-      if (e >= nent || win[j] < 0) continue;
-      if (win[j] >= p.st.maxw) {
+      const int e = r0 + e0 + j * COMBINE_THREADS;
+      if (e >= nent || ent[j].x < 0) continue;
+      if (ent[j].x >= p.st.maxw) {
         atomicOr(p.st.err, ERR_TABLE);
         continue;
       }
-      float* sp = p.st.score + gu * p.st.maxw + win[j];
-      *sp = *sp + dS[j];
+      p.st.score[gu * p.st.maxw + ent[j].x] = sc[j] + dS[j];
     }
   }
 }
@@ -911,11 +932,20 @@ cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t strea
   return cudaErrorInvalidValue;
 }
 
+// programmatic dependent of the attention launch before it on the stream (see the kernel)
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream) {
-  const dim3 grid(p.st.units, p.st.G + 1);
-  if (p.st.geo.D == 128) qe_attn_combine_kernel<128><<<grid, COMBINE_THREADS, 0, stream>>>(p);
-  else qe_attn_combine_kernel<64><<<grid, COMBINE_THREADS, 0, stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(p.st.units, p.st.G + 1);
+  cfg.blockDim = dim3(COMBINE_THREADS);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.st.geo.D == 128) return cudaLaunchKernelEx(&cfg, qe_attn_combine_kernel<128>, p);
+  return cudaLaunchKernelEx(&cfg, qe_attn_combine_kernel<64>, p);
 }
 
 int attn_warps_per_cta() { return ATTN_WARPS; }

@@ -221,6 +221,10 @@ QE_HD LayerView layer_view(const Geo& g, const LayerDev& h) {
 __device__ __forceinline__ unsigned smem_u32(const void* p) {
   return static_cast<unsigned>(__cvta_generic_to_shared(p));
 }
+// programmatic dependent launch: let the next launch on the stream begin / wait for the
+// previous launch's completion and memory flush
+__device__ __forceinline__ void griddep_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void mbar_init(unsigned bar, unsigned count) {
   asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
 }
@@ -251,7 +255,7 @@ __device__ __forceinline__ unsigned long long globaltimer_ns() {
 }
 __device__ __forceinline__ void mma_bf16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
                                          unsigned b0, unsigned b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
@@ -271,6 +275,13 @@ __device__ __forceinline__ unsigned e2m1x2_to_f16x2(unsigned x) {
       : "=r"(d) : "r"(x >> (8 * B)));
   return d;
 }
+// the 4 f16x2 A-fragment registers of fragment f (0 or 1) of a code word
+template <int F>
+__device__ __forceinline__ void unpack_half(unsigned w, unsigned (&a)[4]) {
+  const unsigned t = (F ? (w >> 2) : w) & 0x33333333u;
+  a[0] = e2m1x2_to_f16x2<0>(t); a[1] = e2m1x2_to_f16x2<1>(t);
+  a[2] = e2m1x2_to_f16x2<2>(t); a[3] = e2m1x2_to_f16x2<3>(t);
+}
 // the 8 f16x2 A-fragment registers (two fragments) carried by one code word
 __device__ __forceinline__ void unpack_word(unsigned w, unsigned (&a)[8]) {
   const unsigned t0 = w & 0x33333333u, t1 = (w >> 2) & 0x33333333u;
@@ -281,7 +292,7 @@ __device__ __forceinline__ void unpack_word(unsigned w, unsigned (&a)[8]) {
 }
 __device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
                                         unsigned b0, unsigned b1) {
-  asm volatile(
+  asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));

@@ -38,7 +38,6 @@ struct qe_handle_s {
   float* part_o = nullptr;
   float2* part_ml = nullptr;
   float* lse = nullptr;
-  int* lay_buf = nullptr;     // [n_layers][4] counts handed from attention to combine
   int pslots_cap = 0;         // partial slots per unit
   int attn_grid = 0;          // CTAs of every attention launch (fixed)
   int ntiles_cap = 0;

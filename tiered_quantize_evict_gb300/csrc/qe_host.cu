@@ -106,7 +106,7 @@ void free_all(qe_handle h) {
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_top, s.qfree,
                   s.qfree_top, s.sfree, s.sfree_top, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
-                  h->lay_buf, h->tok_stage};
+                  h->tok_stage};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -217,7 +217,6 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(h->part_o, (size_t)h->units * h->pslots_cap * G * c.head_dim, "partials");
   QE_ALLOC(h->part_ml, (size_t)h->units * h->pslots_cap * G, "partial stats");
   QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
-  QE_ALLOC(h->lay_buf, (size_t)c.n_layers * 4, "layer counts");
   QE_ALLOC(h->tok_stage, (size_t)c.n_layers * 2 * h->units * c.head_dim, "token staging");
   h->max_moves = h->units * st.caps + 16;
   {
@@ -374,7 +373,6 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   p.pend = m.pending;
   p.knew = m.pk;
   p.vnew = m.pv;
-  p.lay_out = h->lay_buf + 4 * layer;
   m.pending = 0;
   m.pk = m.pv = nullptr;
   p.cb = h->cost_b;
@@ -415,7 +413,7 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   qe::CombineParams cp{};
   cp.st = h->st;
   cp.layer = layer;
-  cp.lay_in = h->lay_buf + 4 * layer;
+  cp.pend = p.pend;
   cp.cb = p.cb;
   cp.cq = p.cq;
   cp.NW = grid * qe::attn_warps_per_cta();

@@ -17,7 +17,6 @@ struct AttnParams {
   int pend;              // single-token appends not yet counted in the header's length (0 or 1)
   const uint16_t* knew;  // pend = 1: the token's K and V [B][Hkv][D] bf16, written by this launch
   const uint16_t* vnew;
-  int* lay_out;          // [4]: length, bf16 entries, 2-bit entries, tiles per unit, for the combine
   int cb, cq;            // cost of one 16-token bf16 tile and of one 2-bit window
   int pslots;            // partial slots per unit (>= warps whose range meets one unit)
   const uint16_t* q;     // [B][Hq][D] bf16
@@ -31,7 +30,7 @@ struct AttnParams {
 struct CombineParams {
   State st;
   int layer;
-  const int* lay_in;     // written by the attention launch; the combine commits the length
+  int pend;              // as in the attention launch; the combine commits the length
   int cb, cq;
   int NW, pslots;        // warps of the attention launch, partial slots per unit
   const float* part_o;

@@ -7,7 +7,7 @@
 // allocating CUDA calls at all.  qe_decode_step itself allocates nothing per call once its
 // handle exists, except the staging buffers it creates on first use for host pointers; this
 // entry point accepts device pointers only and takes the split-K scratch of the attention
-// (per-warp partial outputs, per-tile log-sum-exps, the counts handed to the combine) from a
+// (per-warp partial outputs and per-tile log-sum-exps) from a
 // fixed array compiled into the library instead of the handle's own scratch.  The kernels are
 // the same two the handle's decode step launches.
 //
@@ -37,8 +37,7 @@ constexpr int NA_MAX_D = 128;
 constexpr size_t NA_PART_O = (size_t)NA_MAX_UNITS * NA_PSLOTS * NA_MAX_G * NA_MAX_D * sizeof(float);
 constexpr size_t NA_PART_ML = (size_t)NA_MAX_UNITS * NA_PSLOTS * NA_MAX_G * sizeof(float2);
 constexpr size_t NA_LSE = (size_t)NA_MAX_UNITS * NA_MAX_TILES * NA_MAX_G * sizeof(float);
-constexpr size_t NA_LAY = 256;
-constexpr size_t NA_BYTES = NA_PART_O + NA_PART_ML + NA_LSE + NA_LAY;
+constexpr size_t NA_BYTES = NA_PART_O + NA_PART_ML + NA_LSE;
 
 static __device__ __align__(256) unsigned char g_na_scratch[NA_BYTES];
 
@@ -98,7 +97,6 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   float* part_o = reinterpret_cast<float*>(base);
   float2* part_ml = reinterpret_cast<float2*>(base + NA_PART_O);
   float* lse = reinterpret_cast<float*>(base + NA_PART_O + NA_PART_ML);
-  int* lay = reinterpret_cast<int*>(base + NA_PART_O + NA_PART_ML + NA_LSE);
 
   qe::AttnParams p{};
   p.st = h->st;
@@ -106,7 +104,6 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   p.pend = m.pending;
   p.knew = m.pk;
   p.vnew = m.pv;
-  p.lay_out = lay;
   p.cb = h->cost_b;
   p.cq = h->cost_q;
   p.pslots = NA_PSLOTS;
@@ -123,7 +120,7 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   qe::CombineParams cp{};
   cp.st = h->st;
   cp.layer = layer;
-  cp.lay_in = lay;
+  cp.pend = p.pend;
   cp.cb = p.cb;
   cp.cq = p.cq;
   cp.NW = grid * qe::attn_warps_per_cta();
