@@ -288,10 +288,11 @@ struct Shape {
   static constexpr int STAGE = SUB_BYTES > QSLOT ? SUB_BYTES : QSLOT;
   static constexpr int NST = ATTN_SMEM_STAGES_BYTES / (ATTN_WARPS * STAGE);
   static constexpr int KCODE = W * D / 4;
-  static constexpr int OFF_KMIN = 2 * KCODE;
-  static constexpr int OFF_KSCALE = 2 * KCODE + 4 * D;
-  static constexpr int OFF_VMIN = 2 * KCODE + 8 * D;
-  static constexpr int OFF_VSCALE = 2 * KCODE + 8 * D + 4 * W;
+  static constexpr int OFF_KMIN = KCODE;
+  static constexpr int OFF_KSCALE = KCODE + 4 * D;
+  static constexpr int OFF_VCODE = KCODE + 8 * D;
+  static constexpr int OFF_VMIN = OFF_VCODE + KCODE;
+  static constexpr int OFF_VSCALE = OFF_VCODE + KCODE + 4 * W;
 };
 
 __device__ __forceinline__ uint4 lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
@@ -684,7 +685,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       // the outer loop, so consecutive mma go to the MC independent accumulators
       {
         unsigned wv[WPL];
-        load_words<WPL, CW>(sp + S::KCODE, lane, wv);
+        load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
 #pragma unroll
         for (int kt = 0; kt < KT; ++kt)
 #pragma unroll
@@ -715,12 +716,24 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
 }
 
 // ------------------------------------------------------------------------------ combine
-// Grid (units, G + 1).  CTA (u, h < G) merges the partials of unit u for query head h and
-// writes o_h = sum / l; CTA (u, G) recomputes every head's log-sum-exp, turns each tile's
-// log2-sum-exp into mass, sums it over the G heads and adds it to the window's float32 score
-// (eq. (1) with the GQA group sum).  The partial list comes from the attention launch.
-constexpr int COMBINE_THREADS = 128;
+// One CTA per unit (COMBINE_THREADS = 4 x 128 threads).  Thread (h, c) = (tid / D, tid % D)
+// merges the partials of query head h < G at channel c and writes o_h = sum / l; every thread
+// also takes list entries (bf16 windows, then 2-bit ones), turns their tiles' log2-sum-exps into
+// mass, sums it over the G heads and adds it to the window's float32 score (eq. (1) with the GQA
+// group sum).  Warps 0..G-1 compute each head's global statistics.  The partial slots follow
+// from the attention launch's warp ranges.
+//
+// The combine is launched as a programmatic dependent of the attention launch: its CTAs start
+// as attention CTAs leave, compute the layer's counts from the header (the attention read the
+// same header and does not change it), load what the attention does not write (list entries
+// and scores of windows that existed before this step), then wait for the attention grid
+// (griddepcontrol.wait: completion and memory flush) and issue every load of partials and
+// tile log-sum-exps at once.  The last CTA to finish commits the new length.
+constexpr int COMBINE_THREADS = 512;
 constexpr int MAXP = COMBINE_MAXP;
+constexpr int COMBINE_PR = 32;     // partials per thread held in registers (more are re-read)
+constexpr int COMBINE_EPT = 2;     // list entries per thread per round
+constexpr int COMBINE_MAXSUB = 4;  // 16-token sub-tiles per bf16 window (w <= 64)
 
 // partial slots of unit u: one per warp whose position range meets [u Cu, (u+1) Cu)
 __device__ __forceinline__ int unit_partials(const CombineParams& p, const Lay& y, int u) {
@@ -754,7 +767,7 @@ __device__ __forceinline__ void head_stats(const CombineParams& p, int u, int np
   for (int j = 0; j < MAXP / 32; ++j) {
     const int k = lane + 32 * j;
     const float sc = ml[j].y > 0.f ? ex2(ml[j].x - Mu) : 0.f;
-    if (s_sc && k < np) s_sc[k] = sc;
+    if (k < np) s_sc[k] = sc;
     Ls = fmaf(ml[j].y, sc, Ls);
   }
   for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
@@ -762,131 +775,142 @@ __device__ __forceinline__ void head_stats(const CombineParams& p, int u, int np
   lse = Mu + lg2(Ls);
 }
 
-// The combine is launched as a programmatic dependent of the attention launch: its CTAs start
-// as attention CTAs leave, compute the layer's counts from the header (the attention read the
-// same header and does not change it), load what the attention does not write (list entries
-// and scores of windows that existed before this step), then wait for the attention grid
-// (griddepcontrol.wait: completion and memory flush) before reading the partials.
 template <int D>
 __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const CombineParams p) {
-  const int u = blockIdx.x, part = blockIdx.y;
+  const int u = blockIdx.x;
   const int G = p.st.G;
   const long long gu = (long long)p.layer * p.st.units + u;
-  __shared__ float s_sc[MAXP];
+  __shared__ float s_sc[4][MAXP];
   __shared__ float s_inv[4], s_lse[4];
   const int tid = threadIdx.x, warp = tid >> 5;
   const Lay y = make_lay(p.st, p.layer, p.pend, p.cb, p.cq, p.NW);   // counts incl. the pending token
   const int np = unit_partials(p, y, u);
-  if (part < G) {
-    // ---- output of head h = part: every partial of this thread's channels is loaded at once
-    const int h = part;
-    const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
-    const float* po = p.part_o + ((size_t)u * p.pslots * G + h) * D;
-    griddep_wait();
-    constexpr int PR = 32;   // partials held in registers per round
-    float v[PR];
-    const int c = tid;       // COMBINE_THREADS >= D
-    if (c < D) {
-#pragma unroll
-      for (int k = 0; k < PR; ++k) v[k] = k < np ? po[(size_t)k * G * D + c] : 0.f;
-    }
-    if (warp == 0) {
-      float inv, lse;
-      head_stats(p, u, np, h, s_sc, inv, lse);
-      if (tid == 0) s_inv[0] = inv;
-    }
-    __syncthreads();
-    if (c < D) {
-      float acc = 0.f;
-#pragma unroll
-      for (int k = 0; k < PR; ++k)
-        if (k < np && s_sc[k] != 0.f) acc = fmaf(v[k], s_sc[k], acc);
-      for (int k = PR; k < np; ++k)
-        if (s_sc[k] != 0.f) acc = fmaf(po[(size_t)k * G * D + c], s_sc[k], acc);
-      const float o = acc * s_inv[0];
-      const size_t oi = ((size_t)bb * p.st.Hq + kvh * G + h) * D + c;
-      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
-      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
-    }
-    return;
-  }
-  // ---- scores: this thread's list entries and their scores before the wait (a window this
-  //      step opened, the last bf16 entry, is read after it: the attention launch wrote it)
   const int W = p.st.geo.W, sub_tiles = W / 16;
   const int nent = y.nbw + y.nq;
   const bool opens = p.pend > 0 && (y.L - 1) % W == 0;
-  constexpr int EPT = 4;   // entries per thread per round
-  int2 ent[EPT];
-  float sc[EPT];
-  const int e0 = tid;
+  constexpr int EPT = COMBINE_EPT, MAXSUB = COMBINE_MAXSUB;
   auto load_ent = [&](int e) -> int2 {
     if (e < y.nbw) return p.st.blist[gu * p.st.capb + e];
     if (e < nent) return p.st.qlist[gu * p.st.capq + (e - y.nbw)];
     return make_int2(-1, -1);
   };
-  const bool fits = nent <= COMBINE_THREADS * EPT;
+  // first round of this thread's entries and their scores (before the wait)
+  int2 ent[EPT];
+  float sc[EPT];
 #pragma unroll
   for (int j = 0; j < EPT; ++j) {
-    const int e = e0 + j * COMBINE_THREADS;
+    const int e = tid + j * COMBINE_THREADS;
     const bool late = opens && e == y.nbw - 1;
-    ent[j] = (fits && !late) ? load_ent(e) : make_int2(-1, -1);
-    sc[j] = 0.f;
-    if (fits && !late && ent[j].x >= 0 && ent[j].x < p.st.maxw) sc[j] = p.st.score[gu * p.st.maxw + ent[j].x];
+    ent[j] = (e < nent && !late) ? load_ent(e) : make_int2(-1, -1);
+    sc[j] = (ent[j].x >= 0 && ent[j].x < p.st.maxw) ? p.st.score[gu * p.st.maxw + ent[j].x] : 0.f;
   }
   griddep_wait();
-  if (u == 0 && tid == 0) p.st.ldev[p.layer].L = y.L;   // commit the length (the attention has finished)
+  // ---- loads of this thread's partial outputs (head h, channel c) and tile log-sum-exps
+  const int h = tid / D, c = tid - h * D;
+  const bool out_thread = h < G;
+  const float* po = p.part_o + ((size_t)u * p.pslots * G + h) * D + c;
+  float v[COMBINE_PR];
+#pragma unroll
+  for (int k = 0; k < COMBINE_PR; ++k) v[k] = (out_thread && k < np) ? po[(size_t)k * G * D] : 0.f;
+  auto load_lse = [&](int e, const int2 en, float (&ls)[MAXSUB][4]) {
+#pragma unroll
+    for (int s2 = 0; s2 < MAXSUB; ++s2)
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh) ls[s2][hh] = -INFINITY;
+    if (e >= nent || en.x < 0) return;
+    if (e < y.nbw) {
+      const int lo = (en.x == 0) ? p.st.n_sink : 0;
+      int hi = y.L - en.x * W;
+      hi = hi < W ? hi : W;
+#pragma unroll
+      for (int s2 = 0; s2 < MAXSUB; ++s2) {
+        if (s2 >= sub_tiles) break;
+        const int tl = lo - 16 * s2, th = hi - 16 * s2;
+        if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
+        const float* lp = p.lse + ((size_t)u * y.ntiles + e * sub_tiles + s2) * G;
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+          if (hh < G) ls[s2][hh] = lp[hh];
+      }
+    } else {
+      const float* lp = p.lse + ((size_t)u * y.ntiles + y.nbt + (e - y.nbw)) * G;
+#pragma unroll
+      for (int hh = 0; hh < 4; ++hh)
+        if (hh < G) ls[0][hh] = lp[hh];
+    }
+  };
+  if (opens) {   // the window this step opened: its entry now, its score is 0
+#pragma unroll
+    for (int j = 0; j < EPT; ++j)
+      if (tid + j * COMBINE_THREADS == y.nbw - 1) {
+        ent[j] = load_ent(y.nbw - 1);
+        sc[j] = 0.f;
+      }
+  }
+  float ls[EPT][MAXSUB][4];
+#pragma unroll
+  for (int j = 0; j < EPT; ++j) load_lse(tid + j * COMBINE_THREADS, ent[j], ls[j]);
+  // ---- head statistics
   if (warp < G) {
     float inv, lse;
-    head_stats(p, u, np, warp, nullptr, inv, lse);
-    if ((tid & 31) == 0) s_lse[warp] = lse;
+    head_stats(p, u, np, warp, s_sc[warp], inv, lse);
+    if ((tid & 31) == 0) {
+      s_inv[warp] = inv;
+      s_lse[warp] = lse;
+    }
   }
   __syncthreads();
+  // ---- outputs
+  if (out_thread) {
+    float acc = 0.f;
+#pragma unroll
+    for (int k = 0; k < COMBINE_PR; ++k)
+      if (k < np && s_sc[h][k] != 0.f) acc = fmaf(v[k], s_sc[h][k], acc);
+    for (int k = COMBINE_PR; k < np; ++k)
+      if (s_sc[h][k] != 0.f) acc = fmaf(po[(size_t)k * G * D], s_sc[h][k], acc);
+    const float o = acc * s_inv[h];
+    const int bb = u / p.st.Hkv, kvh = u - bb * p.st.Hkv;
+    const size_t oi = ((size_t)bb * p.st.Hq + kvh * G + h) * D + c;
+    if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+    else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+  }
+  // ---- scores
   for (int r0 = 0; r0 < nent; r0 += COMBINE_THREADS * EPT) {
-    if (!fits || r0 > 0) {   // entries beyond the preloaded round (or all of them): load now
+    if (r0 > 0) {   // later rounds (a unit with more entries than one round holds)
 #pragma unroll
       for (int j = 0; j < EPT; ++j) {
-        const int e = r0 + e0 + j * COMBINE_THREADS;
-        ent[j] = load_ent(e);
+        const int e = r0 + tid + j * COMBINE_THREADS;
+        ent[j] = e < nent ? load_ent(e) : make_int2(-1, -1);
         sc[j] = (ent[j].x >= 0 && ent[j].x < p.st.maxw) ? p.st.score[gu * p.st.maxw + ent[j].x] : 0.f;
-      }
-    } else if (opens) {
-#pragma unroll
-      for (int j = 0; j < EPT; ++j)
-        if (e0 + j * COMBINE_THREADS == y.nbw - 1) {
-          ent[j] = load_ent(y.nbw - 1);
-          sc[j] = 0.f;   // opened by this step's attention launch with score 0
-        }
-    }
-    float dS[EPT];
-#pragma unroll
-    for (int j = 0; j < EPT; ++j) {
-      const int e = r0 + e0 + j * COMBINE_THREADS;
-      dS[j] = 0.f;
-      if (e >= nent || ent[j].x < 0) continue;
-      if (e < y.nbw) {
-        const int lo = (ent[j].x == 0) ? p.st.n_sink : 0;
-        int hi = y.L - ent[j].x * W;
-        hi = hi < W ? hi : W;
-        for (int s2 = 0; s2 < sub_tiles; ++s2) {
-          const int tl = lo - 16 * s2, th = hi - 16 * s2;
-          if ((th > 16 ? 16 : th) <= (tl < 0 ? 0 : tl)) continue;
-          const float* ls = p.lse + ((size_t)u * y.ntiles + e * sub_tiles + s2) * G;
-          for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
-        }
-      } else {
-        const float* ls = p.lse + ((size_t)u * y.ntiles + y.nbt + (e - y.nbw)) * G;
-        for (int h = 0; h < G; ++h) dS[j] += ex2(ls[h] - s_lse[h]);
+        if (opens && e == y.nbw - 1) sc[j] = 0.f;
+        load_lse(e, ent[j], ls[j]);
       }
     }
 #pragma unroll
     for (int j = 0; j < EPT; ++j) {
-      const int e = r0 + e0 + j * COMBINE_THREADS;
+      const int e = r0 + tid + j * COMBINE_THREADS;
       if (e >= nent || ent[j].x < 0) continue;
       if (ent[j].x >= p.st.maxw) {
         atomicOr(p.st.err, ERR_TABLE);
         continue;
       }
-      p.st.score[gu * p.st.maxw + ent[j].x] = sc[j] + dS[j];
+      float dS = 0.f;
+#pragma unroll
+      for (int s2 = 0; s2 < MAXSUB; ++s2)
+#pragma unroll
+        for (int hh = 0; hh < 4; ++hh)
+          if (hh < G) dS += ex2(ls[j][s2][hh] - s_lse[hh]);
+      p.st.score[gu * p.st.maxw + ent[j].x] = sc[j] + dS;
+    }
+  }
+  // The last CTA to finish commits the new length: every CTA read the header when it started,
+  // before its count.
+  __syncthreads();
+  if (tid == 0) {
+    LayerDev* hd = p.st.ldev + p.layer;
+    if (atomicAdd(&hd->done, 1u) == gridDim.x - 1) {
+      hd->L = y.L;
+      hd->done = 0;
     }
   }
 }
@@ -935,7 +959,7 @@ cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t strea
 // programmatic dependent of the attention launch before it on the stream (see the kernel)
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream) {
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(p.st.units, p.st.G + 1);
+  cfg.gridDim = dim3(p.st.units);
   cfg.blockDim = dim3(COMBINE_THREADS);
   cfg.dynamicSmemBytes = 0;
   cfg.stream = stream;

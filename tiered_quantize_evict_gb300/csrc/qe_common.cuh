@@ -10,9 +10,9 @@
 // rows) followed by the value fragments (d/16 of 512 B, A operand of V^T P^T
 // with channels as rows).
 //
-// 2-bit window slot: key codes (w d / 4 B), value codes (w d / 4 B), key
-// min[d], key scale[d], value min[w], value scale[w] (float32; the parameter
-// arrays are permuted so each lane reads its own as 16-byte vectors).  Codes
+// 2-bit window slot: key codes (w d / 4 B), key min[d], key scale[d], then value
+// codes (w d / 4 B), value min[w], value scale[w] (float32; the parameter arrays
+// are permuted so each lane reads its own as 16-byte vectors).  Codes
 // are grouped per lane in 32-bit words; a word carries two fragments of 8
 // codes; fragment f, register r, element e sits at bit 8 r + 2 f + 4 e.  Then
 // (word >> 2f) & 0x33333333 holds, in byte r, the register's two codes as two
@@ -43,10 +43,15 @@ struct Geo {
   QE_HD int qslot_bytes() const { return 2 * (W * D / 4) + 8 * D + 8 * W; }
   QE_HD int wpl() const { return (W / 16) * (D / 16) / 2; }       // code words per lane (K or V)
   QE_HD int cw() const { return wpl() < 4 ? wpl() : 4; }          // words per lane per chunk
-  QE_HD int off_kmin() const { return 2 * kcode_bytes(); }
-  QE_HD int off_kscale() const { return 2 * kcode_bytes() + 4 * D; }
-  QE_HD int off_vmin() const { return 2 * kcode_bytes() + 8 * D; }
-  QE_HD int off_vscale() const { return 2 * kcode_bytes() + 8 * D + 4 * W; }
+  // 2-bit slot: the key half (codes, min[D], scale[D]) then the value half (codes, min[W],
+  // scale[W]); each half is one contiguous 16-byte-aligned block
+  QE_HD int khalf_bytes() const { return kcode_bytes() + 8 * D; }
+  QE_HD int vhalf_bytes() const { return kcode_bytes() + 8 * W; }
+  QE_HD int off_kmin() const { return kcode_bytes(); }
+  QE_HD int off_kscale() const { return kcode_bytes() + 4 * D; }
+  QE_HD int off_vcode() const { return khalf_bytes(); }
+  QE_HD int off_vmin() const { return khalf_bytes() + kcode_bytes(); }
+  QE_HD int off_vscale() const { return khalf_bytes() + kcode_bytes() + 4 * W; }
 };
 
 // byte offset of K[r][c] inside a bf16 slot (r < W)
@@ -87,7 +92,7 @@ QE_HD CodePos vcode_pos(const Geo& g, int r, int c) {
   int lane = (rc & 7) * 4 + ((rt & 7) >> 1);
   int reg = (rc >> 3) + 2 * (rt >> 3);
   CodePos p = code_word(g, mc * (g.W / 16) + kt, lane, reg, rt & 1);
-  p.byte += g.kcode_bytes();
+  p.byte += g.off_vcode();
   return p;
 }
 

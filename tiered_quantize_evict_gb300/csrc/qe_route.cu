@@ -613,7 +613,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
           }
         }
       }
-      const int wo = (value ? g.kcode_bytes() / 4 : 0) + widx;
+      const int wo = (value ? g.off_vcode() / 4 : 0) + widx;
       reinterpret_cast<unsigned*>(qs)[wo] = word;
       reinterpret_cast<unsigned*>(hl)[wo] = word;
     }
