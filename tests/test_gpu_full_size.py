@@ -1,8 +1,9 @@
-"""Full-size sampled parity on the 32K-context throughput workload (GPU).
+"""Full-size sampled parity on the 32-layer workloads (GPU).
 
-The cache holds the whole workload: 32 layers, batch 16, GQA 32q/8kv, d 128, 32,768-token
-prefill, w 32, Omega 32, 8 % bf16 / 25 % 2-bit tokens. It is driven in the launch configuration
-the benchmark times:
+Each test holds a whole workload in the cache and checks a few sampled units against the oracle.
+The headline one is the 32K-context throughput workload: 32 layers, batch 16, GQA 32q/8kv, d 128,
+32,768-token prefill, w 32, Omega 32, 8 % bf16 / 25 % 2-bit tokens. It is driven in the launch
+configuration the benchmark times:
 
 - direct calls up to the first routing event;
 - then one decode step of the whole stack captured as a CUDA graph, plus a variant that ends
@@ -16,6 +17,9 @@ generator. For those units the test compares:
   replayed graph);
 - every 2-bit window's codes and parameters, bit for bit;
 - every Full window's bf16 contents.
+
+The Llama-shaped byte-budget stack (all 256 steps, 16 routing events) and the 131K-context
+workload (one routing event over about 2,050 candidate windows per unit) run with direct calls.
 """
 import numpy as np
 import pytest
@@ -96,3 +100,46 @@ def test_throughput_32k_sampled_units_graph_replay():
           f"2-bit windows compared {run.codes_checked}, Full windows compared {full_checked}, "
           f"tie-ambiguous units {run.ambiguous} {[tr.note for tr in run.tracked if tr.note]}")
     assert run.codes_checked > 0 and full_checked > 0
+
+
+def _direct_trajectory(wl, track, steps):
+    """Drive the whole workload with direct calls for `steps` decode steps, comparing the
+    sampled units every step and at every routing event; returns the run."""
+    import torch
+    dev = torch.device("cuda:0")
+    torch.cuda.set_stream(torch.cuda.Stream(dev))
+    run = ParityRun(wl, wl.batch, wl.n_layers, track, device_inputs=True)
+    run.prefill()
+    for _ in range(steps):
+        run.step()
+    return run
+
+
+def test_llama8b_stack_byte_budget_sampled_units():
+    """32 layers, GQA 32q/8kv, d 128, batch 1, 512-token prefill and all 256 decode steps, w 16,
+    Omega 16 (16 routing events), 20 % KV byte budget with 10 % of tokens bf16."""
+    wl = gen.WORKLOADS["llama8b_stack"]
+    run = _direct_trajectory(wl, [(0, 0, 0), (0, 13, 5), (0, 31, 7)], wl.decode_steps)
+    assert run.route_events == wl.decode_steps // wl.route_period
+    full_checked = sum(run.check_bf16_windows(tr) for tr in run.tracked if tr.live)
+    print(f"llama8b_stack: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
+          f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}, "
+          f"tie-ambiguous {run.ambiguous} {[tr.note for tr in run.tracked if tr.note]}")
+    assert run.codes_checked > 0
+
+
+def test_long_131k_sampled_units():
+    """32 layers, GQA 32q/8kv, d 128, batch 1, 131,072-token prefill, w 64, Omega 64, 5 % bf16 /
+    30 % 2-bit tokens: the routing event at step 64 ranks about 2,050 candidate windows per unit;
+    eight more steps attend over the routed cache."""
+    import dataclasses
+    wl = dataclasses.replace(gen.WORKLOADS["long_131k"], decode_steps=72)
+    run = _direct_trajectory(wl, [(0, 0, 0), (0, 31, 7)], 72)
+    assert run.route_events == 1
+    full_checked = sum(run.check_bf16_windows(tr) for tr in run.tracked if tr.live)
+    info = run.cache.layer_info(31)
+    assert (info.n_full, info.n_quant) == (info.kf, info.kq)
+    print(f"long_131k: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
+          f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}, Kf {info.kf}, Kq {info.kq}, "
+          f"tie-ambiguous {run.ambiguous}")
+    assert run.codes_checked > 0
