@@ -204,6 +204,10 @@ typedef struct {
   long long ledger_reuses; /* demotions that reused stored codes */
   long long promotions;    /* Quantized -> Full */
   long long evictions;
+  long long bf16_reclaims; /* promotions that took back their previous bf16 slot, whose
+                              contents no other window had overwritten (no host read) */
+  long long int2_reclaims; /* re-demotions that took back their previous 2-bit slot (no
+                              host read of the ledger) */
 } qe_route_stats;
 
 /* Cumulative routing counters of one layer (layer = -1: summed); synchronous. */

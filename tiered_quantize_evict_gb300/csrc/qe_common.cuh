@@ -30,6 +30,10 @@ namespace qe {
 
 enum : int { TIER_NONE = 0, TIER_PINNED = 1, TIER_FULL = 2, TIER_QUANT = 3, TIER_EVICTED = 4 };
 
+// routing counters per layer: routes, first packs, ledger reuses, promotions, evictions, and
+// promotions / re-demotions that took their previous slot back (no host transfer)
+constexpr int N_STATS = 7;
+
 enum : unsigned { ERR_FREELIST = 1u, ERR_TABLE = 2u, ERR_TIMEOUT = 4u, ERR_COUNT = 8u, ERR_MOVES = 16u,
                   ERR_CAPACITY = 32u };
 
@@ -165,15 +169,24 @@ struct State {
   float* score;       // [GU][maxw]
   int2* blist;        // [GU][capb] {window, slot}; entry 0 is the sink {-1, 0}
   int2* qlist;        // [GU][capq]
-  int* bfree; int* bfree_top;   // [GU][capb], [GU]
-  int* qfree; int* qfree_top;   // [GU][capq], [GU]
-  int* sfree; int* sfree_top;   // [GU][caps], [GU]
+  // Free bf16 and 2-bit slots, next to hand out first: entries [bfree_head, bfree_top) and
+  // [0, qfree_top).  A slot freed by a demotion (bf16) or a promotion (2-bit) still holds that
+  // window's exact data (bvictim / qvictim name the window, bprev / qprev the window's last
+  // slot): it goes to the back, so it is handed out late, and the window takes it back without a
+  // host transfer if nobody has taken it meanwhile.  Slots of evicted windows go to the front.
+  int* bfree; int* bfree_head; int* bfree_top;   // [GU][capb], [GU], [GU]
+  int* qfree; int* qfree_top;                    // [GU][capq], [GU]
+  int* sfree; int* sfree_top;                    // [GU][caps], [GU] (store entries, a stack)
+  int* bvictim;       // [GU][capb] window whose exact bf16 the slot holds, -1 if none
+  int* qvictim;       // [GU][capq] window whose 2-bit codes the slot holds, -1 if none
+  int* bprev;         // [GU][maxw] last bf16 slot of the window, -1 if none
+  int* qprev;         // [GU][maxw] last 2-bit slot of the window, -1 if none
   uint8_t* bslab;     // [GU][capb][bslot_bytes]
   uint8_t* qslab;     // [GU][capq][qslot_bytes]
   uint8_t* hstore;    // device pointer to pinned host [GU][caps][bslot_bytes]
   uint8_t* hledger;   // device pointer to pinned host [GU][caps][qslot_bytes]
   unsigned* err;      // sticky flag
-  unsigned long long* stats;  // [layers][5]
+  unsigned long long* stats;  // [layers][N_STATS]
   LayerDev* ldev;     // [layers]
   CapCfg cap;
   int max_context;

@@ -103,8 +103,8 @@ int nbw_of(const qe_handle h, const LayerMirror& m) {
 
 void free_all(qe_handle h) {
   qe::State& s = h->st;
-  void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_top, s.qfree,
-                  s.qfree_top, s.sfree, s.sfree_top, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
+  void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_head, s.bfree_top,
+                  s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
                   h->tok_stage};
   for (void* p : ptrs)
@@ -196,7 +196,12 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(st.blist, GU * st.capb, "blist");
   QE_ALLOC(st.qlist, GU * st.capq, "qlist");
   QE_ALLOC(st.bfree, GU * st.capb, "bfree");
+  QE_ALLOC(st.bfree_head, GU, "bfree_head");
   QE_ALLOC(st.bfree_top, GU, "bfree_top");
+  QE_ALLOC(st.bvictim, GU * st.capb, "bvictim");
+  QE_ALLOC(st.qvictim, GU * st.capq, "qvictim");
+  QE_ALLOC(st.bprev, GU * maxw, "bprev");
+  QE_ALLOC(st.qprev, GU * maxw, "qprev");
   QE_ALLOC(st.qfree, GU * st.capq, "qfree");
   QE_ALLOC(st.qfree_top, GU, "qfree_top");
   QE_ALLOC(st.sfree, GU * st.caps, "sfree");
@@ -204,7 +209,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(st.bslab, GU * st.capb * bslot_b, "bf16 window pool");
   QE_ALLOC(st.qslab, GU * st.capq * qslot_b, "2-bit window pool");
   QE_ALLOC(st.err, 1, "error flag");
-  QE_ALLOC(st.stats, (size_t)c.n_layers * 5, "stats");
+  QE_ALLOC(st.stats, (size_t)c.n_layers * qe::N_STATS, "stats");
   QE_ALLOC(st.ldev, (size_t)c.n_layers, "layer headers");
 
   // split-K scratch: one CTA per SM, attn_warps_per_cta() warps each; a unit meets at most
@@ -259,19 +264,24 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   set(cudaMemsetAsync(st.bslab, 0, GU * st.capb * bslot_b, h->stream));
   set(cudaMemsetAsync(st.qslab, 0, GU * st.capq * qslot_b, h->stream));
   set(cudaMemsetAsync(st.err, 0, 4, h->stream));
-  set(cudaMemsetAsync(st.stats, 0, (size_t)c.n_layers * 5 * 8, h->stream));
+  set(cudaMemsetAsync(st.stats, 0, (size_t)c.n_layers * qe::N_STATS * 8, h->stream));
+  set(cudaMemsetAsync(st.bvictim, 0xFF, GU * st.capb * 4, h->stream));
+  set(cudaMemsetAsync(st.qvictim, 0xFF, GU * st.capq * 4, h->stream));
+  set(cudaMemsetAsync(st.bprev, 0xFF, GU * maxw * 4, h->stream));
+  set(cudaMemsetAsync(st.qprev, 0xFF, GU * maxw * 4, h->stream));
+  set(cudaMemsetAsync(st.bfree_head, 0, GU * 4, h->stream));
   set(cudaMemsetAsync(st.ldev, 0, (size_t)c.n_layers * sizeof(qe::LayerDev), h->stream));
   {
     std::vector<int> tmp;
     tmp.resize((size_t)GU * st.capb);
     for (long long gu = 0; gu < GU; ++gu)
-      for (int i = 0; i < st.capb - 1; ++i) tmp[gu * st.capb + i] = st.capb - 1 - i;
+      for (int i = 0; i < st.capb - 1; ++i) tmp[gu * st.capb + i] = 1 + i;   // slot 0 is the sink's
     set(cudaMemcpy(st.bfree, tmp.data(), tmp.size() * 4, cudaMemcpyHostToDevice));
     std::vector<int> top(GU, st.capb - 1);
     set(cudaMemcpy(st.bfree_top, top.data(), GU * 4, cudaMemcpyHostToDevice));
     tmp.assign((size_t)GU * st.capq, 0);
     for (long long gu = 0; gu < GU; ++gu)
-      for (int i = 0; i < st.capq; ++i) tmp[gu * st.capq + i] = st.capq - 1 - i;
+      for (int i = 0; i < st.capq; ++i) tmp[gu * st.capq + i] = i;
     set(cudaMemcpy(st.qfree, tmp.data(), tmp.size() * 4, cudaMemcpyHostToDevice));
     top.assign(GU, st.capq);
     set(cudaMemcpy(st.qfree_top, top.data(), GU * 4, cudaMemcpyHostToDevice));
@@ -647,17 +657,19 @@ qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out) {
   if (!h || !out) return QE_ERR_INVALID_ARG;
   if (layer < -1 || layer >= h->cfg.n_layers) return fail(h, QE_ERR_INVALID_ARG, "layer out of range");
   QE_CK(h, cudaStreamSynchronize(h->stream));
-  std::vector<unsigned long long> v((size_t)h->cfg.n_layers * 5);
+  std::vector<unsigned long long> v((size_t)h->cfg.n_layers * qe::N_STATS);
   QE_CK(h, cudaMemcpy(v.data(), h->st.stats, v.size() * 8, cudaMemcpyDeviceToHost));
-  long long a[5] = {0, 0, 0, 0, 0};
+  long long a[qe::N_STATS] = {};
   for (int l = 0; l < h->cfg.n_layers; ++l)
     if (layer == -1 || l == layer)
-      for (int i = 0; i < 5; ++i) a[i] += (long long)v[(size_t)l * 5 + i];
+      for (int i = 0; i < qe::N_STATS; ++i) a[i] += (long long)v[(size_t)l * qe::N_STATS + i];
   out->routes = a[0];
   out->first_packs = a[1];
   out->ledger_reuses = a[2];
   out->promotions = a[3];
   out->evictions = a[4];
+  out->bf16_reclaims = a[5];
+  out->int2_reclaims = a[6];
   return QE_OK;
 }
 

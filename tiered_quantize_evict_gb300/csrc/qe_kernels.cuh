@@ -65,16 +65,18 @@ struct Move {
 constexpr int SENT_LEDGER = 1 << 30;
 
 #if defined(__CUDACC__)
-// Open window j of unit gu when its first token arrives: pop a bf16 slot, Pinned, score 0,
-// entry nb of the bf16 list.  Returns the slot (-1 and the error flag if the pool is empty).
+// Open window j of unit gu when its first token arrives: take the next free bf16 slot, Pinned,
+// score 0, entry nb of the bf16 list.  Returns the slot (-1 and the error flag if the pool is
+// empty).
 __device__ __forceinline__ int open_window(const State& st, long long gu, int j, int nb) {
-  int top = st.bfree_top[gu];
-  if (top <= 0 || nb >= st.capb) {
+  const int head = st.bfree_head[gu];
+  if (head >= st.bfree_top[gu] || nb >= st.capb) {
     atomicOr(st.err, ERR_FREELIST);
     return -1;
   }
-  const int s = st.bfree[gu * st.capb + (--top)];
-  st.bfree_top[gu] = top;
+  const int s = st.bfree[gu * st.capb + head];
+  st.bfree_head[gu] = head + 1;
+  st.bvictim[gu * st.capb + s] = j;
   st.bslot[gu * st.maxw + j] = s;
   st.tier[gu * st.maxw + j] = TIER_PINNED;
   st.score[gu * st.maxw + j] = 0.f;

@@ -135,7 +135,44 @@ __global__ void qe_append_kernel(State st, int layer, int n, const uint16_t* __r
 constexpr int ROUTE_THREADS = 256;
 constexpr int ROUTE_MAX_CAND = 4096;
 
-// One CTA per unit.  Shared memory: sort keys, per-kind change lists, the three free stacks.
+// Block-wide: write front[0, nf) and then the entries of rest[0, nr) whose slot is flagged free,
+// in order, to dst (at most cap entries; more is a free-list error).  Returns the count on every
+// thread.
+__device__ int compact_free(const int* front, int nf, const int* rest, int nr, const uint8_t* flag, int* dst,
+                            int cap, int* s_cnt, unsigned* err) {
+  __shared__ int s_total;
+  const int tid = threadIdx.x;
+  const int per = (nr + ROUTE_THREADS - 1) / ROUTE_THREADS;
+  const int i0 = tid * per, i1 = min(i0 + per, nr);
+  auto keep = [&](int sl) { return sl >= 0 && sl < cap && flag[sl] != 0; };
+  int cnt = 0;
+  for (int i = i0; i < i1; ++i) cnt += keep(rest[i]);
+  s_cnt[tid] = cnt;
+  __syncthreads();
+  if (tid == 0) {
+    int acc = nf;
+    for (int t = 0; t < ROUTE_THREADS; ++t) {
+      const int c = s_cnt[t];
+      s_cnt[t] = acc;
+      acc += c;
+    }
+    if (acc > cap) atomicOr(err, ERR_FREELIST);
+    s_total = acc < cap ? acc : cap;
+  }
+  __syncthreads();
+  for (int i = tid; i < nf && i < cap; i += ROUTE_THREADS) dst[i] = front[i];
+  int o = s_cnt[tid];
+  for (int i = i0; i < i1; ++i)
+    if (keep(rest[i])) {
+      if (o < cap) dst[o] = rest[i];
+      ++o;
+    }
+  const int total = s_total;
+  __syncthreads();   // s_cnt and s_total are reused by the next call
+  return total;
+}
+
+// One CTA per unit.  Shared memory: sort keys, the changed windows' table entries, the free lists.
 __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RouteParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const State& st = p.st;
@@ -148,12 +185,21 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   int* ch_b = ch_win + ROUTE_MAX_CAND;                                               // ROUTE_MAX_CAND
   int* ch_q = ch_b + ROUTE_MAX_CAND;                                                 // ROUTE_MAX_CAND
   int* ch_s = ch_q + ROUTE_MAX_CAND;                                                 // ROUTE_MAX_CAND
-  uint8_t* ch_new = reinterpret_cast<uint8_t*>(ch_s + ROUTE_MAX_CAND);               // ROUTE_MAX_CAND
+  int* ch_bv = ch_s + ROUTE_MAX_CAND;      // previous bf16 slot still holding the window, or -1
+  int* ch_qv = ch_bv + ROUTE_MAX_CAND;     // previous 2-bit slot still holding the window, or -1
+  uint8_t* ch_new = reinterpret_cast<uint8_t*>(ch_qv + ROUTE_MAX_CAND);              // ROUTE_MAX_CAND
   uint8_t* ch_old = ch_new + ROUTE_MAX_CAND;                                         // ROUTE_MAX_CAND
-  int* bstack = reinterpret_cast<int*>(ch_old + ROUTE_MAX_CAND);                     // capb
-  int* qstack = bstack + st.capb;                                                    // capq
-  int* sstack = qstack + st.capq;                                                    // caps
-  __shared__ int s_n, s_nch, s_pos[3];
+  // free lists: the current entries (next to hand out first), then slots freed at the back;
+  // slots freed at the front apart; a flag per slot says whether it is free
+  int* bfa = reinterpret_cast<int*>(ch_old + ROUTE_MAX_CAND);                        // 2 capb
+  int* bfront = bfa + 2 * st.capb;                                                   // capb
+  int* qfa = bfront + st.capb;                                                       // 2 capq
+  int* qfront = qfa + 2 * st.capq;                                                   // capq
+  int* sstack = qfront + st.capq;                                                    // caps
+  uint8_t* bflag = reinterpret_cast<uint8_t*>(sstack + st.caps);                     // capb
+  uint8_t* qflag = bflag + st.capb;                                                  // capq
+  __shared__ int s_n, s_nch, s_pos[8];
+  __shared__ int s_cnt2[ROUTE_THREADS];
 
   const int tid = threadIdx.x;
   // this event's geometry and capacities, from the device-resident header (identical in every CTA)
@@ -228,45 +274,126 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
         ch_b[c] = bsl[j];
         ch_q[c] = qsl[j];
         ch_s[c] = sen[j];
+        // the slot the window last held, if its contents are still the window's
+        int bv = -1, qv = -1;
+        if (nt == TIER_FULL && ot == TIER_QUANT) {
+          const int sb = st.bprev[gu * st.maxw + j];
+          if (sb > 0 && sb < st.capb && st.bvictim[gu * st.capb + sb] == j) bv = sb;
+        }
+        if (nt == TIER_QUANT) {
+          const int sq = st.qprev[gu * st.maxw + j];
+          if (sq >= 0 && sq < st.capq && st.qvictim[gu * st.capq + sq] == j) qv = sq;
+        }
+        ch_bv[c] = bv;
+        ch_qv[c] = qv;
       }
     }
   }
-  // free stacks into shared memory
-  const int btop = st.bfree_top[gu], qtop = st.qfree_top[gu], stop = st.sfree_top[gu];
-  for (int i = tid; i < btop; i += ROUTE_THREADS) bstack[i] = st.bfree[gu * st.capb + i];
-  for (int i = tid; i < qtop; i += ROUTE_THREADS) qstack[i] = st.qfree[gu * st.capq + i];
+  // free lists into shared memory
+  const int bhead = st.bfree_head[gu], btop = st.bfree_top[gu], qtop = st.qfree_top[gu], stop = st.sfree_top[gu];
+  const int nbf = btop > bhead ? btop - bhead : 0;
+  for (int i = tid; i < st.capb; i += ROUTE_THREADS) bflag[i] = 0;
+  for (int i = tid; i < st.capq; i += ROUTE_THREADS) qflag[i] = 0;
+  __syncthreads();
+  for (int i = tid; i < nbf; i += ROUTE_THREADS) {
+    const int sl = st.bfree[gu * st.capb + bhead + i];
+    bfa[i] = sl;
+    if (sl >= 0 && sl < st.capb) bflag[sl] = 1;
+  }
+  for (int i = tid; i < qtop; i += ROUTE_THREADS) {
+    const int sl = st.qfree[gu * st.capq + i];
+    qfa[i] = sl;
+    if (sl >= 0 && sl < st.capq) qflag[sl] = 1;
+  }
   for (int i = tid; i < stop; i += ROUTE_THREADS) sstack[i] = st.sfree[gu * st.caps + i];
   __syncthreads();
   const int nch = s_nch;
   // 4. bookkeeping, one thread, on the shared copies, in an order that never hands out a slot
-  //    whose data a move still has to read: 2-bit and store frees first (their contents are not
-  //    needed), bf16 slots for promotions next, then demotions, then the bf16 frees.
+  //    whose data a move still has to read: slots of evicted windows and 2-bit slots first
+  //    (their contents are not needed), then promotions (taking back their previous slot when
+  //    it still holds them), then demotions, then the bf16 slots of demoted windows (at the back).
   if (tid == 0) {
-    int bt = btop, qt = qtop, stt = stop;
+    int bh = 0, bn = nbf, bf_n = 0, bf_i = 0;   // bf16: pop cursor, end, front count, front cursor
+    int qh = 0, qn = qtop, qf_n = 0, qf_i = 0;
+    int stt = stop;
     unsigned err = 0;
     int nm = 0;
-    // (a) leaving the 2-bit pool: promotions and evictions of Quantized windows
+    // every list entry is a slot in range (only in-range slots are ever added)
+    auto pop_b = [&]() -> int {
+      if (bf_i < bf_n) { const int sl = bfront[bf_i++]; bflag[sl] = 0; return sl; }
+      while (bh < bn && !(bfa[bh] > 0 && bfa[bh] < st.capb && bflag[bfa[bh]])) ++bh;
+      if (bh >= bn) return -1;
+      const int sl = bfa[bh++];
+      bflag[sl] = 0;
+      return sl;
+    };
+    auto pop_q = [&]() -> int {
+      if (qf_i < qf_n) { const int sl = qfront[qf_i++]; qflag[sl] = 0; return sl; }
+      while (qh < qn && !(qfa[qh] >= 0 && qfa[qh] < st.capq && qflag[qfa[qh]])) ++qh;
+      if (qh >= qn) return -1;
+      const int sl = qfa[qh++];
+      qflag[sl] = 0;
+      return sl;
+    };
+    unsigned long long nfirst = 0, nreuse = 0, nprom = 0, nev = 0, brec = 0, qrec = 0;
+    // (a) leaving the 2-bit pool: a promoted window's slot keeps its codes (back), an evicted
+    //     window's slot goes to the front
     for (int c = 0; c < nch; ++c) {
-      if (ch_old[c] == TIER_QUANT) {
-        const int s = ch_q[c];
-        if (s < 0 || qt >= st.capq) err |= ERR_FREELIST; else qstack[qt++] = s;
-        ch_q[c] = -1;
+      if (ch_old[c] != TIER_QUANT) continue;
+      const int sl = ch_q[c];
+      if (sl < 0 || sl >= st.capq) { err |= ERR_FREELIST; ch_q[c] = -1; continue; }
+      if (ch_new[c] == TIER_EVICTED) {
+        qfront[qf_n++] = sl;
+        st.qvictim[gu * st.capq + sl] = -1;
+      } else {
+        qfa[qn++] = sl;
+        st.qprev[gu * st.maxw + ch_win[c]] = sl;
       }
+      qflag[sl] = 1;
+      ch_q[c] = -1;
     }
-    // (b) evictions release their store / ledger entry
+    // (b) evictions release their store / ledger entry and their bf16 slot (front)
     for (int c = 0; c < nch; ++c) {
-      if (ch_new[c] == TIER_EVICTED && ch_s[c] >= 0) {
+      if (ch_new[c] != TIER_EVICTED) continue;
+      ++nev;
+      if (ch_s[c] >= 0) {
         if (stt >= st.caps) err |= ERR_FREELIST; else sstack[stt++] = ch_s[c] & ~SENT_LEDGER;
         ch_s[c] = -1;
       }
+      if (ch_old[c] == TIER_PINNED || ch_old[c] == TIER_FULL) {
+        const int sl = ch_b[c];
+        if (sl <= 0 || sl >= st.capb) err |= ERR_FREELIST;
+        else {
+          bfront[bf_n++] = sl;
+          bflag[sl] = 1;
+          st.bvictim[gu * st.capb + sl] = -1;
+        }
+        ch_b[c] = -1;
+      }
     }
-    // (c) promotions: a bf16 slot, filled from the exact host copy; Pinned windows kept Full
-    //     get a store entry and their exact copy is written now
+    // (c) promotions: the previous slot if it still holds the window, else a free slot filled
+    //     from the exact host copy; Pinned windows kept Full get a store entry and their exact
+    //     copy is written now
+    for (int c = 0; c < nch; ++c) {
+      if (ch_new[c] != TIER_FULL || ch_old[c] != TIER_QUANT) continue;
+      const int sv = ch_bv[c];
+      if (sv > 0 && bflag[sv]) {
+        bflag[sv] = 0;
+        ch_b[c] = sv;
+        ch_bv[c] = -2;   // taken back: no move
+        ++brec;
+      }
+    }
     for (int c = 0; c < nch; ++c) {
       if (ch_new[c] != TIER_FULL) continue;
       if (ch_old[c] == TIER_QUANT) {
-        if (bt <= 0 || ch_s[c] < 0) { err |= ERR_FREELIST; continue; }
-        ch_b[c] = bstack[--bt];
+        ++nprom;
+        if (ch_bv[c] == -2) continue;
+        if (ch_s[c] < 0) { err |= ERR_FREELIST; continue; }
+        const int sl = pop_b();
+        if (sl <= 0) { err |= ERR_FREELIST; continue; }
+        ch_b[c] = sl;
+        st.bvictim[gu * st.capb + sl] = ch_win[c];
         keys[nm++] = ((unsigned long long)MOVE_PROMOTE << 56) | ((unsigned long long)(unsigned)c << 24);
       } else if (ch_s[c] < 0) {
         if (stt <= 0) { err |= ERR_FREELIST; continue; }
@@ -274,28 +401,41 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
         keys[nm++] = ((unsigned long long)MOVE_COPY << 56) | ((unsigned long long)(unsigned)c << 24);
       }
     }
-    // (d) demotions: a 2-bit slot; the first demotion packs (and, from Pinned, takes a store
-    //     entry for the exact copy), later ones reuse the ledger
+    // (d) demotions: the previous 2-bit slot if it still holds the window's codes, else a free
+    //     slot: the first demotion packs (and, from Pinned, takes a store entry for the exact
+    //     copy), later ones reuse the ledger
     for (int c = 0; c < nch; ++c) {
-      if (ch_new[c] == TIER_QUANT) {
-        if (qt <= 0) { err |= ERR_FREELIST; continue; }
-        ch_q[c] = qstack[--qt];
-        int kind;
-        if (ch_s[c] < 0) {
-          if (stt <= 0) { err |= ERR_FREELIST; continue; }
-          ch_s[c] = sstack[--stt];
-          kind = MOVE_PACK_COPY;
-        } else {
-          kind = (ch_s[c] & SENT_LEDGER) ? MOVE_REUSE : MOVE_PACK;
-        }
-        ch_s[c] |= SENT_LEDGER;
-        keys[nm++] = ((unsigned long long)kind << 56) | ((unsigned long long)(unsigned)c << 24);
+      if (ch_new[c] != TIER_QUANT) continue;
+      const int qv = ch_qv[c];
+      if (qv >= 0 && (ch_s[c] & SENT_LEDGER) && qflag[qv]) {
+        qflag[qv] = 0;
+        ch_q[c] = qv;
+        ch_qv[c] = -2;
+        ++qrec;
       }
+    }
+    for (int c = 0; c < nch; ++c) {
+      if (ch_new[c] != TIER_QUANT) continue;
+      if (ch_qv[c] == -2) { ++nreuse; continue; }
+      const int sl = pop_q();
+      if (sl < 0) { err |= ERR_FREELIST; continue; }
+      ch_q[c] = sl;
+      st.qvictim[gu * st.capq + sl] = ch_win[c];
+      int kind;
+      if (ch_s[c] < 0) {
+        if (stt <= 0) { err |= ERR_FREELIST; continue; }
+        ch_s[c] = sstack[--stt];
+        kind = MOVE_PACK_COPY;
+      } else {
+        kind = (ch_s[c] & SENT_LEDGER) ? MOVE_REUSE : MOVE_PACK;
+      }
+      if (kind == MOVE_REUSE) ++nreuse; else ++nfirst;
+      ch_s[c] |= SENT_LEDGER;
+      keys[nm++] = ((unsigned long long)kind << 56) | ((unsigned long long)(unsigned)c << 24);
     }
     // move records (slot numbers captured before the bf16 frees below clear them)
     int base = 0;
     if (nm > 0) base = atomicAdd(p.n_moves, nm);
-    unsigned long long nfirst = 0, nreuse = 0, nprom = 0, nev = 0;
     for (int k = 0; k < nm; ++k) {
       const int kind = (int)(keys[k] >> 56);
       const int c = (int)((keys[k] >> 24) & 0xFFFFFFFF);
@@ -305,38 +445,47 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       mv.gu = (int)gu;
       mv.win = ch_win[c];
       mv.sent = ent;
-      if (kind == MOVE_PACK_COPY || kind == MOVE_PACK) { mv.src = ch_b[c]; mv.dst = ch_q[c]; ++nfirst; }
-      else if (kind == MOVE_REUSE) { mv.src = ent; mv.dst = ch_q[c]; ++nreuse; }
-      else if (kind == MOVE_PROMOTE) { mv.src = ent; mv.dst = ch_b[c]; ++nprom; }
+      if (kind == MOVE_PACK_COPY || kind == MOVE_PACK) { mv.src = ch_b[c]; mv.dst = ch_q[c]; }
+      else if (kind == MOVE_REUSE) { mv.src = ent; mv.dst = ch_q[c]; }
+      else if (kind == MOVE_PROMOTE) { mv.src = ent; mv.dst = ch_b[c]; }
       else { mv.src = ch_b[c]; mv.dst = ent; }
       if (base + k < p.max_moves) p.moves[base + k] = mv; else err |= ERR_MOVES;
     }
-    // (e) bf16 frees (after the moves above were decided; the move kernel reads them first)
+    // (e) bf16 slots of demoted windows go to the back and keep the window's data (the move
+    //     kernel reads them first)
     for (int c = 0; c < nch; ++c) {
-      const int ot = ch_old[c];
-      if ((ot == TIER_PINNED || ot == TIER_FULL) && ch_new[c] != TIER_FULL) {
-        if (ch_b[c] < 0 || bt >= st.capb) err |= ERR_FREELIST; else bstack[bt++] = ch_b[c];
-        ch_b[c] = -1;
+      if (ch_new[c] != TIER_QUANT || (ch_old[c] != TIER_PINNED && ch_old[c] != TIER_FULL)) continue;
+      const int sl = ch_b[c];
+      if (sl <= 0 || sl >= st.capb) err |= ERR_FREELIST;
+      else {
+        bfa[bn++] = sl;
+        bflag[sl] = 1;
+        st.bprev[gu * st.maxw + ch_win[c]] = sl;
       }
-      if (ch_new[c] == TIER_EVICTED) ++nev;
+      ch_b[c] = -1;
     }
-    unsigned long long* sp = st.stats + (size_t)p.layer * 5;
+    unsigned long long* sp = st.stats + (size_t)p.layer * N_STATS;
     if (u == 0) atomicAdd(sp + 0, 1ull);
     if (nfirst) atomicAdd(sp + 1, nfirst);
     if (nreuse) atomicAdd(sp + 2, nreuse);
     if (nprom) atomicAdd(sp + 3, nprom);
     if (nev) atomicAdd(sp + 4, nev);
-    st.bfree_top[gu] = bt;
-    st.qfree_top[gu] = qt;
+    if (brec) atomicAdd(sp + 5, brec);
+    if (qrec) atomicAdd(sp + 6, qrec);
     st.sfree_top[gu] = stt;
-    s_pos[0] = bt;
-    s_pos[1] = qt;
-    s_pos[2] = stt;
+    s_pos[0] = bh;
+    s_pos[1] = bn;
+    s_pos[2] = bf_i;
+    s_pos[3] = bf_n;
+    s_pos[4] = qh;
+    s_pos[5] = qn;
+    s_pos[6] = qf_i;
+    s_pos[7] = qf_n;
     if (err) atomicOr(st.err, err);
   }
   __syncthreads();
   {
-    // table entries and tiers of the changed windows, and the free stacks, back to global memory
+    // table entries and tiers of the changed windows, and the store stack, back to global memory
     for (int c = tid; c < nch; c += ROUTE_THREADS) {
       const int j = ch_win[c];
       bsl[j] = ch_b[c];
@@ -344,10 +493,21 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       sen[j] = ch_s[c];
       st.tier[gu * st.maxw + j] = ch_new[c];
     }
-    const int bt = s_pos[0], qt = s_pos[1], stt = s_pos[2];
-    for (int i = tid; i < bt; i += ROUTE_THREADS) st.bfree[gu * st.capb + i] = bstack[i];
-    for (int i = tid; i < qt; i += ROUTE_THREADS) st.qfree[gu * st.capq + i] = qstack[i];
-    for (int i = tid; i < stt; i += ROUTE_THREADS) st.sfree[gu * st.caps + i] = sstack[i];
+    for (int i = tid; i < st.sfree_top[gu]; i += ROUTE_THREADS) st.sfree[gu * st.caps + i] = sstack[i];
+  }
+  // the free lists, compacted: front entries not handed out, then the free entries in order
+  {
+    const int bh = s_pos[0], bn = s_pos[1], bf_i = s_pos[2], bf_n = s_pos[3];
+    const int nb = compact_free(bfront + bf_i, bf_n - bf_i, bfa + bh, bn - bh, bflag, st.bfree + gu * st.capb,
+                                st.capb, s_cnt2, st.err);
+    const int qh = s_pos[4], qn = s_pos[5], qf_i = s_pos[6], qf_n = s_pos[7];
+    const int nq2 = compact_free(qfront + qf_i, qf_n - qf_i, qfa + qh, qn - qh, qflag, st.qfree + gu * st.capq,
+                                 st.capq, s_cnt2, st.err);
+    if (tid == 0) {
+      st.bfree_head[gu] = 0;
+      st.bfree_top[gu] = nb;
+      st.qfree_top[gu] = nq2;
+    }
   }
   __syncthreads();
   // 5. rebuild the tile lists: bf16 = sink + Pinned/Full windows, 2-bit = Quantized windows,
@@ -659,7 +819,8 @@ cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t
 }
 
 size_t route_smem_bytes(const State& st) {
-  return (size_t)ROUTE_MAX_CAND * (8 + 4 * 4 + 2) + (size_t)(st.capb + st.capq + st.caps) * 4 + 16;
+  return (size_t)ROUTE_MAX_CAND * (8 + 4 * 6 + 2) + (size_t)(3 * st.capb + 3 * st.capq + st.caps) * 4 +
+         (size_t)(st.capb + st.capq) + 16;
 }
 
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
