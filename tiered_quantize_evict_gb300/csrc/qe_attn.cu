@@ -22,10 +22,10 @@
 //    one head (its accumulator pair is that head's hi and lo), so the softmax needs no
 //    cross-lane merging and no lane duplicates another's work.
 //  * 2-bit codes are unpacked in registers straight into mma fragments (the slots are stored
-//    in fragment order): a code is the low half of an FP4 (e2m1) nibble, value code / 2, and
-//    one cvt.f16x2.e2m1x2 turns two codes into an f16 pair; the factor 2 is folded into the
-//    B operand (2 q s_K for keys, 2 p s_V for values).  Dequantized values never exist in
-//    memory.
+//    in fragment order): one shift and one and-or turn a register's two codes into the f16 pair
+//    (1 + code / 4).  The factor 4 goes into the logit scale (keys) and the B operand
+//    (4 p s_V for values); the constant 1 into the key bias (q . (z_K / 4 - s_K)) and the value
+//    offset (p . (z_V - 4 s_V)).  Dequantized values never exist in memory.
 //  * Per-window mass leaves the kernel as a log-sum-exp per (tile, head); the combine kernel
 //    turns it into a probability mass once the unit's global softmax normaliser is known.
 #include <cstdint>
@@ -634,10 +634,12 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       // ---- 2-bit window: W tokens
       const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
       const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
-      // B fragments 2 q s_K in f16: trunc part in even columns, remainder in odd ones; bias q . z_K
-      // (the codes arrive as code / 2: the logit scale below carries the factor 2)
+      // B fragments q s_K in f16: trunc part in even columns, remainder in odd ones.  The codes
+      // arrive as 1 + code / 4, so logit / 4 = q s_K . A + q . (z_K - 4 s_K) / 4: the bias
+      // accumulates q . (z_K - 4 s_K), the logit scale below carries the factor 4.
       unsigned qp[KS][2];
       unsigned long long bp2 = 0ull;
+      const unsigned long long neg4 = f2_pack(-4.f, -4.f);
       const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
@@ -646,20 +648,26 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         bp2 = f2_fma(qf[ks][0], zc.x, bp2);
         bp2 = f2_fma(qf[ks][1], zc.y, bp2);
         const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
+        bp2 = f2_fma(y01, neg4, bp2);   // q . (z_K - 4 s_K)
+        bp2 = f2_fma(y23, neg4, bp2);
         const unsigned long long k2 = ((unsigned long long)keep << 32) | keep;
         const unsigned long long r01 = f2_sub(y01, y01 & k2), r23 = f2_sub(y23, y23 & k2);
         qp[ks][0] = pack_f16x2_rz(f2_lo(r01), f2_hi(r01));
         qp[ks][1] = pack_f16x2_rz(f2_lo(r23), f2_hi(r23));
       }
-      float bpart = f2_lo(bp2) + f2_hi(bp2);
+      float bpart = 0.25f * (f2_lo(bp2) + f2_hi(bp2));
       bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
       bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-      const float bias = 0.5f * __shfl_sync(0xffffffffu, bpart, 8 * t);   // half of q . z_K of head t
+      const float bias = __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . (z_K / 4 - s_K) of head t
       float vz[2 * MT], vs[2 * MT];
       load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
       load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
+      // codes arrive as 1 + code / 4: B = 4 p s_V, and the offset p . (z_V - 4 s_V) per token
 #pragma unroll
-      for (int i = 0; i < 2 * MT; ++i) vs[i] *= 2.f;   // codes arrive as code / 2
+      for (int i = 0; i < 2 * MT; ++i) {
+        vs[i] *= 4.f;
+        vz[i] -= vs[i];
+      }
       // Q K^T over the unpacked key codes (fragment F = mt KS + ks is half F % 2 of word F / 2);
       // channel-step parity splits the accumulators, and consecutive mma go to different
       // accumulators (2 MT independent chains)
@@ -679,7 +687,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
           }
       }
       unsigned Bp[MT][2];
-      softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 2.f * p.scale_log2, rs, Bp, lse_out,
+      softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 4.f * p.scale_log2, rs, Bp, lse_out,
                                     G, lane);
       // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
       // the outer loop, so consecutive mma go to the MC independent accumulators

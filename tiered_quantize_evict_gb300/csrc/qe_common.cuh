@@ -14,10 +14,11 @@
 // codes (w d / 4 B), value min[w], value scale[w] (float32; the parameter arrays
 // are permuted so each lane reads its own as 16-byte vectors).  Codes
 // are grouped per lane in 32-bit words; a word carries two fragments of 8
-// codes; fragment f, register r, element e sits at bit 8 r + 2 f + 4 e.  Then
-// (word >> 2f) & 0x33333333 holds, in byte r, the register's two codes as two
-// FP4 (e2m1) nibbles whose values are code / 2, and one cvt.f16x2.e2m1x2 per
-// register turns them into the f16 pair the tensor core consumes.
+// codes: fragment f, register r (R = 4 f + r), element e sits at bit 2 R + 16 e.
+// Shifting the word by 8 - 2R brings the register's two codes to bits 8 and 24,
+// and one and-or with 0x03000300 / 0x3C003C00 makes them the f16 pair
+// (1 + code / 4) the tensor core consumes; the constant 1 is removed through
+// the key bias and the value offset.
 #pragma once
 #include <cstdint>
 #include <cuda_runtime.h>
@@ -80,7 +81,7 @@ QE_HD CodePos code_word(const Geo& g, int F, int lane, int reg, int e) {
   int cw = g.cw();
   CodePos p;
   p.byte = ((wi / cw) * 32 + lane) * (cw * 4) + (wi % cw) * 4;
-  p.bit = 8 * reg + 2 * f + 4 * e;
+  p.bit = 8 * f + 2 * reg + 16 * e;
   return p;
 }
 // key code of token r, channel c (fragments ordered token-tile major, channel-step minor)
@@ -101,7 +102,7 @@ QE_HD CodePos vcode_pos(const Geo& g, int r, int c) {
 }
 
 // Inverse of kcode_pos / vcode_pos: the (token r, channel c) whose code sits at bit
-// 8 reg + 2 f + 4 e of word widx of the key code block (value = false) or of the value code
+// 8 f + 2 reg + 16 e of word widx of the key code block (value = false) or of the value code
 // block (value = true; widx counted from the start of that block).
 struct RC { int r, c; };
 QE_HD RC code_rc(const Geo& g, bool value, int widx, int reg, int f, int e) {
@@ -283,30 +284,24 @@ __device__ __forceinline__ unsigned movmatrix_t(unsigned a) {
   asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
   return d;
 }
-// byte `b` of x holds two FP4 (e2m1) nibbles -> f16x2 (low nibble -> low half).  2-bit codes
-// sit in the low two bits of each nibble, so the values are code / 2, exactly.
-template <int B>
-__device__ __forceinline__ unsigned e2m1x2_to_f16x2(unsigned x) {
+// Register R (0..7) of a code word as an f16 pair (1 + code / 4): its codes sit at bits 2R and
+// 2R + 16; the shift brings them to bits 8 and 24, the f16 mantissa's top two bits under the
+// exponent of 1.0.
+template <int R>
+__device__ __forceinline__ unsigned code_pair_f16(unsigned w) {
+  constexpr int SH = 8 - 2 * R;
+  const unsigned x = SH >= 0 ? (w << (SH >= 0 ? SH : 0)) : (w >> (SH < 0 ? -SH : 0));
   unsigned d;
-  asm("{\n\t.reg .b16 s;\n\t.reg .b8 t;\n\tcvt.u16.u32 s, %1;\n\tcvt.u8.u16 t, s;\n\t"
-      "cvt.rn.f16x2.e2m1x2 %0, t;\n\t}"
-      : "=r"(d) : "r"(x >> (8 * B)));
+  asm("lop3.b32 %0, %1, 0x03000300, 0x3C003C00, 0xEA;" : "=r"(d) : "r"(x));   // (a & b) | c
   return d;
 }
-// the 4 f16x2 A-fragment registers of fragment f (0 or 1) of a code word
+// the 4 f16x2 A-fragment registers of fragment F (0 or 1) of a code word
 template <int F>
 __device__ __forceinline__ void unpack_half(unsigned w, unsigned (&a)[4]) {
-  const unsigned t = (F ? (w >> 2) : w) & 0x33333333u;
-  a[0] = e2m1x2_to_f16x2<0>(t); a[1] = e2m1x2_to_f16x2<1>(t);
-  a[2] = e2m1x2_to_f16x2<2>(t); a[3] = e2m1x2_to_f16x2<3>(t);
-}
-// the 8 f16x2 A-fragment registers (two fragments) carried by one code word
-__device__ __forceinline__ void unpack_word(unsigned w, unsigned (&a)[8]) {
-  const unsigned t0 = w & 0x33333333u, t1 = (w >> 2) & 0x33333333u;
-  a[0] = e2m1x2_to_f16x2<0>(t0); a[1] = e2m1x2_to_f16x2<1>(t0);
-  a[2] = e2m1x2_to_f16x2<2>(t0); a[3] = e2m1x2_to_f16x2<3>(t0);
-  a[4] = e2m1x2_to_f16x2<0>(t1); a[5] = e2m1x2_to_f16x2<1>(t1);
-  a[6] = e2m1x2_to_f16x2<2>(t1); a[7] = e2m1x2_to_f16x2<3>(t1);
+  a[0] = code_pair_f16<4 * F + 0>(w);
+  a[1] = code_pair_f16<4 * F + 1>(w);
+  a[2] = code_pair_f16<4 * F + 2>(w);
+  a[3] = code_pair_f16<4 * F + 3>(w);
 }
 __device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
                                         unsigned b0, unsigned b1) {
@@ -335,6 +330,11 @@ __device__ __forceinline__ unsigned long long f2_mul(unsigned long long a, unsig
 __device__ __forceinline__ unsigned long long f2_fma(unsigned long long a, unsigned long long b, unsigned long long c) {
   unsigned long long d;
   asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ unsigned long long f2_add(unsigned long long a, unsigned long long b) {
+  unsigned long long d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
 __device__ __forceinline__ unsigned long long f2_sub(unsigned long long a, unsigned long long b) {

@@ -730,7 +730,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
     // codes: each thread assembles whole 32-bit words.  Word (lane, wi) of a code block holds
     // fragments 2 wi and 2 wi + 1 of that lane; the bf16 slot stores the same fragment of the
     // same lane as one 16-byte vector (element (reg, e) at bits 32 reg + 16 e), so a word needs
-    // two vector loads and its code (reg, f, e) goes to bit 8 reg + 2 f + 4 e.
+    // two vector loads and its code (reg, f, e) goes to bit 8 f + 2 reg + 16 e.
     const int wpl = g.wpl(), cw = g.cw(), KS = D / 16, KT = W / 16;
     for (int t = tid; t < 64 * wpl; t += MOVE_THREADS) {
       const bool value = t >= 32 * wpl;
@@ -769,7 +769,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
               const int r = r0 + e + 8 * (reg >> 1);
               code = r >= lo ? quant_code(xv, vz[r], vs[r]) : 0u;
             }
-            word |= code << (8 * reg + 2 * f + 4 * e);
+            word |= code << (8 * f + 2 * reg + 16 * e);
           }
         }
       }
