@@ -145,7 +145,6 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
     delete h;
     return fail(nullptr, QE_ERR_CUDA, "no CUDA device: %s", cudaGetErrorString(e));
   }
-  if (const char* s = getenv("QE_TILE_COSTS")) sscanf(s, "%d,%d", &h->cost_b, &h->cost_q);
   h->cost_q = h->cost_q * c.window / 32 > 0 ? h->cost_q * c.window / 32 : 1;
 
   const int maxw = ceil_div(c.max_context, c.window);
@@ -400,6 +399,7 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   }
   const int grid = h->attn_grid;
   cudaEvent_t e0 = nullptr, e1 = nullptr;
+  unsigned ev_flags = cudaEventRecordDefault;
   if (h->timing) {
     while (h->ev_pool.size() < h->ev_used + 2) {
       cudaEvent_t ev;
@@ -409,12 +409,16 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
     e0 = h->ev_pool[h->ev_used];
     e1 = h->ev_pool[h->ev_used + 1];
     h->ev_used += 2;
-    QE_CK(h, cudaEventRecord(e0, h->stream));
+    // inside a stream capture the records must be external to happen when the graph runs
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    QE_CK(h, cudaStreamIsCapturing(h->stream, &cs));
+    ev_flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    QE_CK(h, cudaEventRecordWithFlags(e0, h->stream, ev_flags));
   }
   QE_CK(h, qe::launch_decode_attn(p, grid, h->stream));
   ++h->launches;
   if (h->timing) {
-    QE_CK(h, cudaEventRecord(e1, h->stream));
+    QE_CK(h, cudaEventRecordWithFlags(e1, h->stream, ev_flags));
     h->timed_launches += 1;
     qe_layer_info info;
     fill_info(h, m, &info);   // host shadow: no synchronisation inside the timed path
