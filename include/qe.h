@@ -213,6 +213,29 @@ typedef struct {
 /* Cumulative routing counters of one layer (layer = -1: summed); synchronous. */
 qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out);
 
+/* One unit's record of the layer's latest routing event (diagnostics; QEvict reading notes §3
+ * define selection churn as the Jaccard distance between the kept sets of consecutive routing
+ * events, H2O page §5.1 the cutoff margin as the lowest kept score minus the highest dropped
+ * one).  "Old" is the tier map before the event; windows entering the candidate pool from
+ * Pinned are in no old set.  A cut score is -1 when that side of the cut is empty. */
+typedef struct {
+  int kf, kq;            /* capacities at the event */
+  int full_old, full_new, full_both;   /* |F|, |F'|, |F and F'| (Full sets) */
+  int kept_old, kept_new, kept_both;   /* the same for Full or Quantized */
+  int promotions;        /* Quantized -> Full */
+  int demotions;         /* Full -> Quantized */
+  int evictions;         /* -> Evicted */
+  float full_cut_kept;   /* score of the candidate ranked K_f (the lowest Full one) */
+  float full_cut_next;   /* score of the candidate ranked K_f + 1 */
+  float kept_cut_kept;   /* score of the candidate ranked K_f + K_q (the lowest kept one) */
+  float kept_cut_next;   /* score of the candidate ranked K_f + K_q + 1 */
+} qe_route_diag;
+
+/* Copy the records of the layer's latest routing event for units [0, n_units) (unit = batch
+ * element x KV head, in that order) into out; synchronous.  Records of a layer that has not
+ * been routed are zero. */
+qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n_units);
+
 /* Time every qe_decode_step attention launch with CUDA events on the handle's
  * stream (enable = 1) or stop (0).  qe_get_timing returns the summed device
  * time in ms, the number of launches and the summed algorithmic bytes of

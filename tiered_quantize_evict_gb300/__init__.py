@@ -27,7 +27,7 @@ EXPORTED = [
     "qe_init", "qe_destroy", "qe_last_error", "qe_append", "qe_decode_step", "qe_route",
     "qe_synchronize", "qe_get_layer_info", "qe_get_tiers", "qe_get_scores", "qe_set_scores",
     "qe_get_quant_window", "qe_get_bf16_window", "qe_get_route_stats", "qe_set_timing",
-    "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc",
+    "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc", "qe_get_route_diag",
 ]
 
 
@@ -56,6 +56,13 @@ class QERouteStats(ctypes.Structure):
                 ("ledger_reuses", ctypes.c_longlong), ("promotions", ctypes.c_longlong),
                 ("evictions", ctypes.c_longlong), ("bf16_reclaims", ctypes.c_longlong),
                 ("int2_reclaims", ctypes.c_longlong)]
+
+
+class QERouteDiag(ctypes.Structure):
+    """One unit's record of a layer's latest routing event (see qe_route_diag in qe.h)."""
+    _fields_ = [(n, ctypes.c_int) for n in ("kf", "kq", "full_old", "full_new", "full_both", "kept_old",
+                                             "kept_new", "kept_both", "promotions", "demotions", "evictions")] + \
+               [(n, ctypes.c_float) for n in ("full_cut_kept", "full_cut_next", "kept_cut_kept", "kept_cut_next")]
 
 
 class QEError(RuntimeError):
@@ -95,6 +102,7 @@ def load_library() -> ctypes.CDLL:
         "qe_get_timing": ([P, ctypes.POINTER(D), ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(D)], I),
         "qe_kernel_launches": ([P], ctypes.c_longlong),
         "qe_decode_step_noalloc": ([P, I, P, P], I),
+        "qe_get_route_diag": ([P, I, ctypes.POINTER(QERouteDiag), S], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -219,6 +227,13 @@ class QECache:
         s = QERouteStats()
         self._check(self._lib.qe_get_route_stats(self.h, layer, ctypes.byref(s)))
         return s
+
+    def route_diag(self, layer: int):
+        """Records of the layer's latest routing event, one per unit."""
+        units = self.cfg.batch * self.cfg.n_kv_heads
+        arr = (QERouteDiag * units)()
+        self._check(self._lib.qe_get_route_diag(self.h, layer, arr, units))
+        return list(arr)
 
     def set_timing(self, enable: bool):
         self._check(self._lib.qe_set_timing(self.h, 1 if enable else 0))

@@ -45,6 +45,7 @@ struct qe_handle_s {
   qe::Move* moves = nullptr;
   int* n_moves = nullptr;
   int max_moves = 0;
+  qe::RouteDiag* diag = nullptr;   // [n_layers][units] latest routing event of each layer
   // staging for host pointers
   uint16_t* tok_stage = nullptr;   // [n_layers][2][units][D]: single-token appends from host memory
   void* stage[4] = {nullptr, nullptr, nullptr, nullptr};

@@ -106,7 +106,7 @@ void free_all(qe_handle h) {
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_head, s.bfree_top,
                   s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
-                  h->tok_stage};
+                  h->tok_stage, h->diag};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -221,6 +221,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(h->part_o, (size_t)h->units * h->pslots_cap * G * c.head_dim, "partials");
   QE_ALLOC(h->part_ml, (size_t)h->units * h->pslots_cap * G, "partial stats");
   QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
+  QE_ALLOC(h->diag, (size_t)c.n_layers * h->units, "routing records");
   QE_ALLOC(h->tok_stage, (size_t)c.n_layers * 2 * h->units * c.head_dim, "token staging");
   h->max_moves = h->units * st.caps + 16;
   {
@@ -263,6 +264,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   set(cudaMemsetAsync(st.bslab, 0, GU * st.capb * bslot_b, h->stream));
   set(cudaMemsetAsync(st.qslab, 0, GU * st.capq * qslot_b, h->stream));
   set(cudaMemsetAsync(st.err, 0, 4, h->stream));
+  set(cudaMemsetAsync(h->diag, 0, (size_t)c.n_layers * h->units * sizeof(qe::RouteDiag), h->stream));
   set(cudaMemsetAsync(st.stats, 0, (size_t)c.n_layers * qe::N_STATS * 8, h->stream));
   set(cudaMemsetAsync(st.bvictim, 0xFF, GU * st.capb * 4, h->stream));
   set(cudaMemsetAsync(st.qvictim, 0xFF, GU * st.capq * 4, h->stream));
@@ -463,6 +465,7 @@ static qe_status route_layer(qe_handle h, int layer) {
   p.moves = h->moves;
   p.n_moves = h->n_moves;
   p.max_moves = h->max_moves;
+  p.diag = h->diag;
   QE_CK(h, cudaMemsetAsync(h->n_moves, 0, 4, h->stream));
   QE_CK(h, qe::launch_route(p, h->stream));
   QE_CK(h, qe::launch_moves(h->st, h->moves, h->n_moves, h->n_sm, h->stream));
@@ -674,6 +677,18 @@ qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out) {
   out->evictions = a[4];
   out->bf16_reclaims = a[5];
   out->int2_reclaims = a[6];
+  return QE_OK;
+}
+
+qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n_units) {
+  if (!h || !out) return QE_ERR_INVALID_ARG;
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  if (n_units > (size_t)h->units) return fail(h, QE_ERR_INVALID_ARG, "n_units %zu > %d units", n_units, h->units);
+  static_assert(sizeof(qe_route_diag) == sizeof(qe::RouteDiag), "routing record layout");
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  QE_CK(h, cudaMemcpy(out, h->diag + (size_t)layer * h->units, n_units * sizeof(qe_route_diag),
+                      cudaMemcpyDeviceToHost));
   return QE_OK;
 }
 

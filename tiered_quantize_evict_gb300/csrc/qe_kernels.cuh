@@ -85,12 +85,19 @@ __device__ __forceinline__ int open_window(const State& st, long long gu, int j,
 }
 #endif
 
+// per-unit record of a routing event (same layout as qe_route_diag)
+struct RouteDiag {
+  int kf, kq, full_old, full_new, full_both, kept_old, kept_new, kept_both, promotions, demotions, evictions;
+  float full_cut_kept, full_cut_next, kept_cut_kept, kept_cut_next;
+};
+
 struct RouteParams {
   State st;
   int layer;
   Move* moves;
   int* n_moves;
   int max_moves;
+  RouteDiag* diag;   // [layers][units]
 };
 
 cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t stream);

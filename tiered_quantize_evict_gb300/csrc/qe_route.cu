@@ -199,6 +199,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   uint8_t* bflag = reinterpret_cast<uint8_t*>(sstack + st.caps);                     // capb
   uint8_t* qflag = bflag + st.capb;                                                  // capq
   __shared__ int s_n, s_nch, s_pos[8];
+  __shared__ int s_diag[9];   // full old/new/both, kept old/new/both, promotions, demotions, evictions
+  __shared__ float s_cut[4];  // scores at the two cuts (read before the keys are reused)
   __shared__ int s_cnt2[ROUTE_THREADS];
 
   const int tid = threadIdx.x;
@@ -216,6 +218,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   const int exp_nquant = kq < ncand - exp_nfull ? kq : ncand - exp_nfull;
   const bool fits = exp_nquant <= st.capq && exp_nfull + exp_nquant <= st.caps && ncand <= ROUTE_MAX_CAND;
   if (tid == 0) { s_n = 0; s_nch = 0; }
+  if (tid < 9) s_diag[tid] = 0;
   __syncthreads();
   if (!fits) {   // the pools cannot hold this event's result: flag and leave the layer unchanged
     if (tid == 0 && u == 0) atomicOr(st.err, ERR_CAPACITY);
@@ -257,14 +260,26 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       __syncthreads();
     }
   }
+  if (tid < 4) {
+    const int r = tid < 2 ? kf - 1 + tid : kf + kq - 1 + (tid - 2);
+    s_cut[tid] = (r >= 0 && r < n) ? __uint_as_float(0xFFFFFFFFu - (unsigned)(keys[r] >> 32)) : -1.f;
+  }
   // 3. eq. (5): rank -> tier; collect the windows whose tier changes
   int* bsl = st.bslot + gu * st.maxw;
   int* qsl = st.qslot + gu * st.maxw;
   int* sen = st.sent + gu * st.maxw;
+  int dg[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // this thread's share of the event record
   for (int r = tid; r < n; r += ROUTE_THREADS) {
     const int j = (int)(keys[r] & 0xFFFFFFFFu);
     const int nt = r < kf ? TIER_FULL : (r < kf + kq ? TIER_QUANT : TIER_EVICTED);
     const int ot = tier[j];
+    const bool fo = ot == TIER_FULL, fn = nt == TIER_FULL;
+    const bool ko = fo || ot == TIER_QUANT, kn = fn || nt == TIER_QUANT;
+    dg[0] += fo; dg[1] += fn; dg[2] += fo && fn;
+    dg[3] += ko; dg[4] += kn; dg[5] += ko && kn;
+    dg[6] += ot == TIER_QUANT && fn;
+    dg[7] += fo && nt == TIER_QUANT;
+    dg[8] += nt == TIER_EVICTED;
     if (nt != ot) {
       {
         const int c = atomicAdd(&s_nch, 1);
@@ -289,6 +304,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       }
     }
   }
+  for (int i = 0; i < 9; ++i)
+    if (dg[i]) atomicAdd(&s_diag[i], dg[i]);
   // free lists into shared memory
   const int bhead = st.bfree_head[gu], btop = st.bfree_top[gu], qtop = st.qfree_top[gu], stop = st.sfree_top[gu];
   const int nbf = btop > bhead ? btop - bhead : 0;
@@ -510,6 +527,20 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     }
   }
   __syncthreads();
+  // the event's record of this unit
+  if (tid == 0 && p.diag) {
+    RouteDiag d;
+    d.kf = kf;
+    d.kq = kq;
+    d.full_old = s_diag[0]; d.full_new = s_diag[1]; d.full_both = s_diag[2];
+    d.kept_old = s_diag[3]; d.kept_new = s_diag[4]; d.kept_both = s_diag[5];
+    d.promotions = s_diag[6]; d.demotions = s_diag[7]; d.evictions = s_diag[8];
+    d.full_cut_kept = s_cut[0];
+    d.full_cut_next = s_cut[1];
+    d.kept_cut_kept = s_cut[2];
+    d.kept_cut_next = s_cut[3];
+    p.diag[(size_t)p.layer * st.units + u] = d;
+  }
   // 5. rebuild the tile lists: bf16 = sink + Pinned/Full windows, 2-bit = Quantized windows,
   //    both in ascending window order (block-wide stream compaction)
   __shared__ int s_cnt[ROUTE_THREADS][2];
@@ -839,11 +870,22 @@ cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves,
 }
 
 // kernel attributes, set once (outside any stream capture)
+// The limit is a property of the kernel, shared by every handle of the process: it is raised to
+// the device's opt-in maximum (never lowered for a smaller handle), and a handle whose routing
+// needs more is refused.
 cudaError_t prepare_route_kernels(const State& st) {
-  cudaError_t e = cudaFuncSetAttribute(qe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       (int)route_smem_bytes(st));
+  int dev = 0, optin = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(qe_move_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)move_smem_bytes(st));
+  cudaFuncAttributes ra{}, ma{};
+  if ((e = cudaFuncGetAttributes(&ra, qe_route_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&ma, qe_move_kernel)) != cudaSuccess) return e;
+  const int rmax = optin - (int)ra.sharedSizeBytes, mmax = optin - (int)ma.sharedSizeBytes;
+  if (route_smem_bytes(st) > (size_t)rmax || move_smem_bytes(st) > (size_t)mmax) return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(qe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rmax);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(qe_move_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mmax);
 }
 
 }  // namespace qe
