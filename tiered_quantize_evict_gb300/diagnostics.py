@@ -184,6 +184,14 @@ def summary(records: List[EventRecord], dropped: Dict[int, np.ndarray], fmm: Dic
         s[f"layer{layer}_dropped_mass_p99"] = float(np.percentile(d, 99)) if d.size else 0.0
         if fmm.get(layer):
             s[f"layer{layer}_fmm_mean"] = float(np.mean([e.mean() for e in fmm[layer]]))
+    if dropped:
+        alld = np.concatenate([d.ravel() for d in dropped.values() if d.size]) if any(
+            d.size for d in dropped.values()) else np.zeros(0)
+        s["dropped_mass_mean"] = float(alld.mean()) if alld.size else 0.0
+        s["dropped_mass_p50"] = float(np.percentile(alld, 50)) if alld.size else 0.0
+        s["dropped_mass_p99"] = float(np.percentile(alld, 99)) if alld.size else 0.0
+        f_all = [e.mean() for l in fmm for e in fmm[l]]
+        s["fmm_mean"] = float(np.mean(f_all)) if f_all else 0.0
     return s
 
 
@@ -199,4 +207,5 @@ if __name__ == "__main__":
     wl = gen.WORKLOADS[a.workload]
     rec, dropped, fmm = run(wl, n_layers=a.layers or None, steps=a.steps or None,
                             layers_report=tuple(range(a.layers or wl.n_layers)))
-    print(json.dumps({"workload": a.workload, **summary(rec, dropped, fmm)}))
+    full = summary(rec, dropped, fmm)
+    print(json.dumps({"workload": a.workload, **{k: v for k, v in full.items() if not k.startswith("layer")}}))
