@@ -320,7 +320,9 @@ def run_ours(args):
             "measured_on": "the next K decode steps launched directly, CUDA events around each launch",
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h},
+                "d2h_bytes_per_step": d2h,
+                "path": "direct C-ABI calls on pinned host buffers: queries copied in, new K/V read "
+                        "and outputs written in place by the kernels over the host link"},
         "gpu_launches": launches,
         "clocks": clk,
     }

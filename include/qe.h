@@ -100,8 +100,12 @@ typedef struct {
 /* Pointer-location flags for qe_append / qe_decode_step. */
 enum {
   QE_DEVICE_PTRS = 0,  /* all buffers are device memory */
-  QE_HOST_PTRS = 1     /* all buffers are host memory (pinned for async copies; pageable works
-                          but the copies then block the calling thread) */
+  QE_HOST_PTRS = 1     /* all buffers are host memory.  Page-locked, device-mapped buffers
+                          (cudaHostAlloc, or registered as mapped) stay asynchronous: a
+                          single-token append's K and V are read, and decode outputs written,
+                          by the kernels in place over the host link; queries and multi-token
+                          appends are copied in.  Pageable buffers are copied both ways, and
+                          the copies then block the calling thread. */
 };
 
 /* Create a cache for cfg on the current CUDA device.  Allocates the device
@@ -126,9 +130,9 @@ const char* qe_last_error(qe_handle h);
  * with n_tokens = prompt length; a decode step appends 1 token.
  * A single-token append launches nothing: the next qe_decode_step of the layer
  * writes the token inside its attention launch (any other call on the layer
- * writes it first).  Device k and v must therefore stay valid until the
- * stream reaches that call; host k and v are copied to the layer's own
- * staging buffers at once.
+ * writes it first).  Device and pinned host k and v must therefore stay valid
+ * and unchanged until the stream reaches that call; pageable host k and v are
+ * copied to the layer's own staging buffers at once.
  * Errors: QE_ERR_CAPACITY if the length would pass max_context. */
 qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_tokens, int flags);
 
@@ -140,7 +144,8 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
  * Full bf16 windows and the dequantized INT2 windows (x = code * s + z), and
  * adds each window's mass, summed over the unit's query heads, to its
  * float32 score (eq. (1) with the GQA group sum).  Sink tokens are never
- * scored. */
+ * scored.  A pinned host out is written by the combine kernel in place and
+ * is complete once the stream has passed the call. */
 qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int flags);
 
 /* Routing event of one layer (layer = -1: all layers), QEvict notes §4.4

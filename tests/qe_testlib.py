@@ -71,7 +71,9 @@ class ParityRun:
     """A cache on the GPU plus oracle units for a chosen set of (b, layer, kvh)."""
 
     def __init__(self, wl, batch: int, n_layers: int, track: Sequence[Tuple[int, int, int]],
-                 device_inputs: bool = False):
+                 device_inputs: bool = False, host: Optional[str] = None):
+        """host: None (device buffers), "pinned" (page-locked torch tensors) or "pageable"
+        (numpy arrays): where the inputs and the outputs of every call live."""
         import tiered_quantize_evict_gb300 as qe
         torch, dev = torch_dev()
         self.torch, self.dev = torch, dev
@@ -92,7 +94,28 @@ class ParityRun:
         self.ambiguous = 0
         self.codes_checked = 0
         self.route_events = 0
-        self.out = torch.empty(batch, wl.n_q_heads, wl.head_dim, device=dev, dtype=torch.float32)
+        assert host in (None, "pinned", "pageable") and not (host and device_inputs)
+        self.host = host
+        if host == "pinned":
+            self.out = torch.empty(batch, wl.n_q_heads, wl.head_dim, dtype=torch.float32).pin_memory()
+        elif host == "pageable":
+            self.out = np.zeros((batch, wl.n_q_heads, wl.head_dim), np.float32)
+        else:
+            self.out = torch.empty(batch, wl.n_q_heads, wl.head_dim, device=dev, dtype=torch.float32)
+
+    def _place(self, a: np.ndarray):
+        a = np.ascontiguousarray(a).view(np.int16)
+        if self.host == "pinned":
+            return self.torch.from_numpy(a).pin_memory()
+        if self.host == "pageable":
+            return a.copy()
+        return to_dev(a)
+
+    def _read_out(self):
+        if self.host:   # host buffers are complete once the stream has passed the call
+            self.cache.qe_synchronize()
+            return np.array(self.out, copy=True) if self.host == "pageable" else self.out.numpy().copy()
+        return self.out.cpu().numpy().copy()
 
     # ------------------------------------------------------------------ inputs
     def _kv(self, layer, pos0, n):
@@ -103,7 +126,7 @@ class ParityRun:
             self.gdev.keys_values(layer, pos0, n, k, v, torch.cuda.current_stream().cuda_stream)
             return k, v
         K, V = host_kv(self.wl, layer, pos0, n, self.batch)
-        return to_dev(K), to_dev(V)
+        return self._place(K), self._place(V)
 
     def _q(self, layer, step):
         torch = self.torch
@@ -111,7 +134,7 @@ class ParityRun:
             q = torch.empty(self.batch, self.wl.n_q_heads, self.wl.head_dim, device=self.dev, dtype=torch.int16)
             self.gdev.queries(layer, step, q, torch.cuda.current_stream().cuda_stream)
             return q
-        return to_dev(host_q(self.wl, layer, step, self.batch))
+        return self._place(host_q(self.wl, layer, step, self.batch))
 
     # ------------------------------------------------------------------ driving
     def prefill(self):
@@ -119,6 +142,8 @@ class ParityRun:
         for layer in range(self.n_layers):
             k, v = self._kv(layer, 0, wl.prefill)
             self.cache.qe_append(layer, k, v, wl.prefill)
+            if self.host:   # the copies read host memory in stream order
+                self.cache.qe_synchronize()
             del k, v
         for tr in self.tracked:
             kb, vb = gen.gen_keys_values(wl, tr.b, tr.layer, tr.kvh, 0, wl.prefill)
@@ -136,8 +161,9 @@ class ParityRun:
             self.cache.qe_append(layer, k, v, 1)
             q = self._q(layer, t)
             self.cache.qe_decode_step(layer, q, self.out)
-            if any(tr.layer == layer and tr.live for tr in self.tracked):
-                outs[layer] = self.out.cpu().numpy().copy()
+            if self.host or any(tr.layer == layer and tr.live for tr in self.tracked):
+                # host inputs stay referenced (and unchanged) until the stream has read them
+                outs[layer] = self._read_out()
         for tr in self.tracked:
             if not tr.live:
                 continue

@@ -55,3 +55,22 @@ def test_trajectory_parity(name):
             run.check_bf16_windows(tr)
     print(f"{name}: out err {run.max_out_err:.2e}, score rel err {run.max_score_err:.2e}, "
           f"codes {run.codes_checked}, ambiguous {run.ambiguous}")
+
+
+@pytest.mark.parametrize("host", ["pinned", "pageable"])
+def test_host_buffers_trajectory(host):
+    """The same path with every input and output in host memory: the kernels read pinned new
+    tokens and write pinned outputs in place, pageable buffers go through copies, queries and the
+    prefill are copied in; every unit still follows the oracle."""
+    wl = dataclasses.replace(CASES["d128_w32_g4"], name="host_" + host, n_layers=2, decode_steps=24)
+    track = [(b, l, h) for b in range(wl.batch) for l in range(wl.n_layers) for h in range(wl.n_kv_heads)]
+    run = ParityRun(wl, wl.batch, wl.n_layers, track, host=host)
+    run.prefill()
+    for _ in range(wl.decode_steps):
+        run.step()
+    run.check_scores()
+    run.cache.qe_synchronize()
+    assert sum(tr.live for tr in run.tracked) >= len(run.tracked) - 1
+    assert run.codes_checked > 0 and run.route_events == wl.decode_steps // wl.route_period
+    print(f"host {host}: out err {run.max_out_err:.2e}, score rel err {run.max_score_err:.2e}, "
+          f"codes {run.codes_checked}")

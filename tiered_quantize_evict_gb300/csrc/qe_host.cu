@@ -6,6 +6,7 @@
 // device.  Window identities, slots, scores and codes live only on the device.
 #include <cmath>
 #include <cstdarg>
+#include <cstdint>
 #include <cstdio>
 #include <cstdlib>
 #include <cstring>
@@ -82,6 +83,20 @@ qe_status ensure_stage(qe_handle h, int i, size_t bytes) {
 }
 
 void fill_info(qe_handle h, const LayerMirror& m, qe_layer_info* info);
+
+// The device address of a page-locked, device-mapped host buffer, aligned to `align` bytes;
+// nullptr for pageable memory (which goes through copies).  Kernels read and write such a buffer
+// over the host link in stream order, exactly where a copy would have run.
+const void* mapped_view(const void* p, size_t align) {
+  cudaPointerAttributes a{};
+  if (cudaPointerGetAttributes(&a, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  if (a.type != cudaMemoryTypeHost || !a.devicePointer) return nullptr;
+  if (reinterpret_cast<uintptr_t>(a.devicePointer) % align) return nullptr;
+  return a.devicePointer;
+}
 
 // a single-token append that no decode step consumed: write the token and advance the device
 // length now
@@ -332,14 +347,22 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
   const uint16_t* vd = static_cast<const uint16_t*>(v);
   if (n_tokens == 1) {
     // The next decode step of this layer writes the token (inside its attention launch) and its
-    // combine commits the length; host tokens wait in the layer's own staging slots.
+    // combine commits the length.  That launch reads a pinned host token in place; a pageable
+    // one waits in the layer's own staging slots.
     if (flags & QE_HOST_PTRS) {
-      uint16_t* ks = h->tok_stage + (size_t)layer * 2 * h->units * h->cfg.head_dim;
-      uint16_t* vs = ks + (size_t)h->units * h->cfg.head_dim;
-      QE_CK(h, cudaMemcpyAsync(ks, k, bytes, cudaMemcpyHostToDevice, h->stream));
-      QE_CK(h, cudaMemcpyAsync(vs, v, bytes, cudaMemcpyHostToDevice, h->stream));
-      kd = ks;
-      vd = vs;
+      const void* mk = mapped_view(k, 4);
+      const void* mv = mapped_view(v, 2);
+      if (mk && mv) {
+        kd = static_cast<const uint16_t*>(mk);
+        vd = static_cast<const uint16_t*>(mv);
+      } else {
+        uint16_t* ks = h->tok_stage + (size_t)layer * 2 * h->units * h->cfg.head_dim;
+        uint16_t* vs = ks + (size_t)h->units * h->cfg.head_dim;
+        QE_CK(h, cudaMemcpyAsync(ks, k, bytes, cudaMemcpyHostToDevice, h->stream));
+        QE_CK(h, cudaMemcpyAsync(vs, v, bytes, cudaMemcpyHostToDevice, h->stream));
+        kd = ks;
+        vd = vs;
+      }
     }
     m.pending = 1;
     m.pk = kd;
@@ -372,11 +395,22 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   const size_t obytes = (size_t)c.batch * c.n_q_heads * D * (c.out_fp32 ? 4 : 2);
   const uint16_t* qd = static_cast<const uint16_t*>(q);
   void* od = out;
+  bool out_copy = false;   // pageable output: combine into staging, then copy out
   if (flags & QE_HOST_PTRS) {
-    if ((s = ensure_stage(h, 2, qbytes)) != QE_OK || (s = ensure_stage(h, 3, obytes)) != QE_OK) return s;
-    QE_CK(h, cudaMemcpyAsync(h->stage[2], q, qbytes, cudaMemcpyHostToDevice, h->stream));
-    qd = static_cast<const uint16_t*>(h->stage[2]);
-    od = h->stage[3];
+    if (const void* mq = mapped_view(q, 4)) {
+      qd = static_cast<const uint16_t*>(mq);   // the attention warps read a pinned query in place
+    } else {
+      if ((s = ensure_stage(h, 2, qbytes)) != QE_OK) return s;
+      QE_CK(h, cudaMemcpyAsync(h->stage[2], q, qbytes, cudaMemcpyHostToDevice, h->stream));
+      qd = static_cast<const uint16_t*>(h->stage[2]);
+    }
+    if (const void* mo = mapped_view(out, c.out_fp32 ? 4 : 2)) {
+      od = const_cast<void*>(mo);   // the combine writes a pinned output in place
+    } else {
+      if ((s = ensure_stage(h, 3, obytes)) != QE_OK) return s;
+      od = h->stage[3];
+      out_copy = true;
+    }
   }
   qe::AttnParams p{};
   p.st = h->st;
@@ -441,7 +475,7 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   cp.out_fp32 = c.out_fp32;
   QE_CK(h, qe::launch_attn_combine(cp, h->stream));
   ++h->launches;
-  if (flags & QE_HOST_PTRS) QE_CK(h, cudaMemcpyAsync(out, od, obytes, cudaMemcpyDeviceToHost, h->stream));
+  if (out_copy) QE_CK(h, cudaMemcpyAsync(out, od, obytes, cudaMemcpyDeviceToHost, h->stream));
   return QE_OK;
 }
 
