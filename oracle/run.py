@@ -17,11 +17,16 @@ import numpy as np
 import qe_inputs as gen
 
 from .budget import capacities
+from .hqekv import HqeUnit
 from .qevict import QEvictUnit
 from .router import RouteResult
 
 
-def make_unit(wl, max_context: Optional[int] = None) -> QEvictUnit:
+def make_unit(wl, max_context: Optional[int] = None):
+    """A QEvict unit, or a five-tier per-token unit for workloads with tiering "tokens"."""
+    if wl.tiering == "tokens":
+        return HqeUnit(wl.head_dim, wl.group, wl.n_sink, wl.n_recent, wl.route_period, wl.score_window,
+                       (wl.frac_bf16, wl.frac_int4, wl.frac_int2, wl.frac_nq1), max_context or wl.max_context)
     return QEvictUnit(wl.window, wl.n_sink, wl.n_recent, wl.head_dim, wl.group,
                       lambda L: capacities(wl, L), max_context or wl.max_context)
 

@@ -133,6 +133,13 @@ class Workload:
     plant_step: int = 0                # decode step from which queries carry u
     plant_amp: float = 3.0
     drift_period: int = 0              # 0 = no drift
+    # five-tier per-token variant (tiering "tokens"): token fractions of the BF16 / INT4 / INT2 /
+    # 1-bit tiers (the rest evicted) and the number of last steps before a re-rank whose
+    # attention is counted (0 = every step); route_period is the re-rank period
+    tiering: str = "windows"
+    frac_int4: float = 0.0
+    frac_nq1: float = 0.0
+    score_window: int = 0
 
     @property
     def group(self) -> int:
@@ -163,6 +170,20 @@ WORKLOADS = {
         prefill=32768, decode_steps=128, window=32, route_period=32, n_sink=5, n_recent=32,
         cap_mode=1, frac_bf16=0.08, frac_int2=0.25, seed=20261202 + 3,
         drift_period=64),
+    # five-tier per-token variant: 10 % BF16 / 20 % INT4 / 30 % INT2 / 30 % 1-bit / 10 % evicted,
+    # re-ranked every 64 steps over the attention of the last 20 steps (w = 32 is the drift epoch's
+    # window grid only)
+    "hqe_16k": Workload(
+        name="hqe_16k", batch=8, n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        prefill=16384, decode_steps=128, window=32, route_period=64, n_sink=5, n_recent=32,
+        cap_mode=1, frac_bf16=0.10, frac_int2=0.30, seed=20261202 + 5, drift_period=64,
+        tiering="tokens", frac_int4=0.20, frac_nq1=0.30, score_window=20),
+    # the same rule at a size the oracle follows through every step
+    "tiny_hqe": Workload(
+        name="tiny_hqe", batch=2, n_layers=2, n_q_heads=8, n_kv_heads=2, head_dim=128,
+        prefill=300, decode_steps=48, window=32, route_period=16, n_sink=5, n_recent=16,
+        cap_mode=1, frac_bf16=0.10, frac_int2=0.30, seed=20261202 + 6, drift_period=64,
+        tiering="tokens", frac_int4=0.20, frac_nq1=0.30, score_window=6),
     "long_131k": Workload(
         name="long_131k", batch=1, n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128,
         prefill=131072, decode_steps=64, window=64, route_period=64, n_sink=5, n_recent=32,
