@@ -95,7 +95,34 @@ typedef struct {
   double frac_int2;    /* cap_mode 1 */
   double budget_frac;  /* cap_mode 2 */
   int out_fp32;        /* 1: qe_decode_step writes float32, 0: bf16 */
+  /* Tiering (QE_TIERING_*).  QE_TIERING_TOKENS is the five-tier per-token cache of the HqeKV
+   * reading notes (§3.1): every token is BF16, 4-bit or 2-bit uniform (eq. (2), per-token
+   * min/scale for its key and its value), 1-bit normal (eqs. (3)-(4): per-token mean and
+   * population std, centers +-Phi^-1(3/4), code 1 when x > mean) or evicted.  qe_route then
+   * re-ranks (§3.5): the n_sink first and n_recent last tokens stay BF16; the others are
+   * ranked by score (descending, ties to the lower position) and the ranks give the tiers in
+   * the order BF16, 4-bit, 2-bit, 1-bit, evicted with counts
+   *   max(0, floor(frac_bf16 L) - n_sink - n_recent), floor(frac_int4 L),
+   *   floor(frac_int2 L), floor(frac_nq1 L), the rest
+   * (double precision); a token only moves down (a token whose rank asks for a higher tier
+   * keeps its own), and a token that moves is re-quantized from what its tier held (one
+   * float32 fma per value).  Scores add each token's attention mass summed over the KV head's
+   * query heads, on the last score_window decode steps before a re-rank (0: every step), and
+   * restart at 0 after it when score_window > 0.  window, cap_mode, kf, kq and budget_frac are
+   * unused; route_period is the re-rank period. */
+  int tiering;
+  double frac_int4;
+  double frac_nq1;
+  int score_window;
 } qe_config;
+
+enum { QE_TIERING_WINDOWS = 0, QE_TIERING_TOKENS = 1 };
+
+/* Token tiers of the five-tier mode (qe_get_token_tiers). */
+enum {
+  QE_TOK_BF16 = 0, QE_TOK_INT4 = 1, QE_TOK_INT2 = 2, QE_TOK_NQ1 = 3, QE_TOK_EVICTED = 4,
+  QE_TOK_ABSENT = 255    /* position not appended yet */
+};
 
 /* Pointer-location flags for qe_append / qe_decode_step. */
 enum {
@@ -247,6 +274,26 @@ qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n
  * the timed launches since the last enable, and resets nothing. */
 qe_status qe_set_timing(qe_handle h, int enable);
 qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, double* attn_bytes);
+
+/* ---------------------------------------------------------------- five-tier introspection
+ * (QE_TIERING_TOKENS handles; all synchronous; QE_ERR_STATE on a window-tiered handle) */
+
+/* Tier of every position [units][max_context] uint8 (QE_TOK_*). */
+qe_status qe_get_token_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes);
+
+/* Score of every position [units][max_context] float32 (0 for evicted and absent ones). */
+qe_status qe_get_token_scores(qe_handle h, int layer, float* host, size_t bytes);
+
+/* Tokens per unit [units][5] int32: ranked BF16, 4-bit, 2-bit, 1-bit, and the BF16 tail
+ * (sink, recent and the tokens appended since the last re-rank). */
+qe_status qe_get_token_counts(qe_handle h, int layer, int* host, size_t bytes);
+
+/* One token: *tier (QE_TOK_*); for BF16 its key and value bf16 bits [head_dim] each; for a
+ * quantized tier its codes [head_dim] each and params = {key p0, key p1, value p0, value p1}
+ * (min and scale, or mean and std for the 1-bit tier).  Pointers of the kind that does not
+ * apply may be null. */
+qe_status qe_get_token(qe_handle h, int layer, int unit, int pos, int* tier, uint16_t* k_bf16, uint16_t* v_bf16,
+                       uint8_t* k_codes, uint8_t* v_codes, float* params);
 
 /* Number of kernel launches the handle has enqueued since qe_init. */
 long long qe_kernel_launches(qe_handle h);

@@ -281,6 +281,7 @@ class HqeUnit:
         self.tier = np.zeros(max_context, np.int64)          # BF16 for every position at first
         self.S = np.zeros(max_context, F32)
         self.codes: Dict[int, TokenCodes] = {}
+        self._deq: Dict[int, Tuple[np.ndarray, np.ndarray]] = {}
         self.history: List[RerankResult] = []
 
     def append(self, k_rows, v_rows):
@@ -298,7 +299,9 @@ class HqeUnit:
         z = self.tier[p]
         if z == BF16:
             return self.K[p], self.V[p]
-        return dequantize_token(self.codes[p])
+        if p not in self._deq:
+            self._deq[p] = dequantize_token(self.codes[p])
+        return self._deq[p]
 
     def accessible(self):
         pos = [p for p in range(self.L) if self.tier[p] != EVICT]
@@ -313,8 +316,9 @@ class HqeUnit:
         """Whether decode step t (1-based) adds to the scores."""
         return self.m == 0 or (t - 1) % self.T >= self.T - self.m
 
-    def decode_step(self, q, k_row, v_row):
-        """append -> attend -> (scoring steps) accumulate -> (every T steps) re-rank.
+    def decode_step(self, q, k_row, v_row, auto_rerank: bool = True):
+        """append -> attend -> (scoring steps) accumulate -> (every T steps, when auto_rerank)
+        re-rank.
 
         Returns (o [G, d] float64, mass {position: float64} of this step)."""
         self.append(k_row, v_row)
@@ -326,7 +330,7 @@ class HqeUnit:
         if self.scoring_step(self.t):
             for q_, mval in mass.items():
                 self.S[q_] = F32(self.S[q_] + F32(mval))
-        if self.t % self.T == 0:
+        if auto_rerank and self.t % self.T == 0:
             self.rerank()
         return o, mass
 
@@ -347,6 +351,7 @@ class HqeUnit:
             else:
                 k, v = self.values(p)               # re-quantize what the token holds now
                 self.codes[p] = quantize_token(zn, k, v)
+            self._deq.pop(p, None)
             self.tier[p] = zn
         if self.m > 0:
             self.S[:L] = 0

@@ -1,0 +1,158 @@
+"""Five-tier per-token cache (HqeKV reading notes) on the GPU against the oracle, every unit of
+small workloads through whole trajectories.
+
+Each decode step compares every unit's attention outputs.  At each re-rank the test compares:
+- every position's score;
+- the tiers after both sides re-rank on the GPU's scores;
+- every quantized token's codes and float32 parameters, bit for bit;
+- every BF16 token's values.
+
+Ranking parity is asserted on identical scores: the GPU's float32 scores are handed to the oracle
+before it re-ranks, because near-ties make both rankings correct when the scores differ in the
+last bits.
+"""
+import dataclasses
+
+import numpy as np
+import pytest
+
+import qe_inputs as gen
+from oracle import hqekv as H
+from oracle.run import make_unit
+from qe_testlib import OUT_TOL, SCORE_ATOL, SCORE_RTOL, host_kv, host_q, to_dev, torch_dev
+
+pytestmark = pytest.mark.gpu
+
+BASE = gen.WORKLOADS["tiny_hqe"]
+CASES = {
+    "d128_g4": BASE,
+    "d64_g2_m0": dataclasses.replace(BASE, name="d64_g2_m0", head_dim=64, n_q_heads=6, n_kv_heads=3, batch=1,
+                                     prefill=203, decode_steps=40, route_period=10, score_window=0, n_sink=3,
+                                     n_recent=9, seed=31),
+    "d128_g1_long_window": dataclasses.replace(BASE, name="d128_g1", n_q_heads=2, n_kv_heads=2, batch=2, n_layers=1,
+                                               prefill=520, decode_steps=36, route_period=12, score_window=12,
+                                               frac_bf16=0.05, frac_int4=0.15, frac_int2=0.25, frac_nq1=0.45,
+                                               seed=32),
+}
+
+
+class TokRun:
+    def __init__(self, wl):
+        import tiered_quantize_evict_gb300 as qe
+        torch, dev = torch_dev()
+        self.torch, self.dev, self.wl = torch, dev, wl
+        self.cache = qe.QECache(qe.config_from_workload(wl), torch.cuda.current_stream().cuda_stream)
+        self.units = {(b, l, h): make_unit(wl) for b in range(wl.batch) for l in range(wl.n_layers)
+                      for h in range(wl.n_kv_heads)}
+        self.t = 0
+        self.max_out = 0.0
+        self.max_score = 0.0
+        self.codes_checked = 0
+        self.bf16_checked = 0
+        self.out = torch.empty(wl.batch, wl.n_q_heads, wl.head_dim, device=dev, dtype=torch.float32)
+
+    def u_index(self, b, h):
+        return b * self.wl.n_kv_heads + h
+
+    def prefill(self):
+        wl = self.wl
+        for layer in range(wl.n_layers):
+            K, V = host_kv(wl, layer, 0, wl.prefill, wl.batch)
+            self.cache.qe_append(layer, to_dev(K), to_dev(V), wl.prefill)
+            for b in range(wl.batch):
+                for h in range(wl.n_kv_heads):
+                    self.units[(b, layer, h)].append(gen.bf16_bits_to_f32(K[b, h]), gen.bf16_bits_to_f32(V[b, h]))
+
+    def step(self):
+        wl = self.wl
+        self.t += 1
+        t = self.t
+        pos = wl.prefill + t - 1
+        for layer in range(wl.n_layers):
+            K, V = host_kv(wl, layer, pos, 1, wl.batch)
+            Q = host_q(wl, layer, t, wl.batch)
+            self.cache.qe_append(layer, to_dev(K), to_dev(V), 1)
+            self.cache.qe_decode_step(layer, to_dev(Q), self.out)
+            got = self.out.cpu().numpy().astype(np.float64)
+            for b in range(wl.batch):
+                for h in range(wl.n_kv_heads):
+                    heads = slice(h * wl.group, (h + 1) * wl.group)
+                    q = gen.bf16_bits_to_f32(Q[b, heads])
+                    o, _ = self.units[(b, layer, h)].decode_step(q, gen.bf16_bits_to_f32(K[b, h]),
+                                                                 gen.bf16_bits_to_f32(V[b, h]), auto_rerank=False)
+                    for i in range(wl.group):
+                        err = np.linalg.norm(got[b, h * wl.group + i] - o[i]) / np.linalg.norm(o[i])
+                        self.max_out = max(self.max_out, err)
+                        assert err <= OUT_TOL, f"step {t} layer {layer} unit {(b, h)} head {i}: rel-L2 {err:.2e}"
+        if t % wl.route_period == 0:
+            self.rerank_and_check()
+
+    def rerank_and_check(self):
+        wl = self.wl
+        for layer in range(wl.n_layers):
+            S = self.cache.token_scores(layer)
+            for b in range(wl.batch):
+                for h in range(wl.n_kv_heads):
+                    un = self.units[(b, layer, h)]
+                    u = self.u_index(b, h)
+                    live = (un.tier[:un.L] != H.EVICT) & (np.arange(un.L) >= wl.n_sink)
+                    ref = un.S[:un.L][live].astype(np.float64)
+                    got = S[u, :un.L][live].astype(np.float64)
+                    err = np.abs(got - ref)
+                    assert np.all(err <= SCORE_RTOL * ref + SCORE_ATOL), \
+                        f"t {self.t} layer {layer} unit {u}: score error {err.max():.2e}"
+                    self.max_score = max(self.max_score, float(np.max(err / np.maximum(ref, 1e-30))) if ref.size else 0)
+                    un.S[:un.L] = np.where(np.arange(un.L) < wl.n_sink, 0, S[u, :un.L])   # route on the GPU's scores
+        self.cache.qe_route(-1)
+        for un in self.units.values():
+            un.rerank()
+        self.check_state()
+
+    def check_state(self):
+        wl = self.wl
+        for layer in range(wl.n_layers):
+            tiers = self.cache.token_tiers(layer)
+            for b in range(wl.batch):
+                for h in range(wl.n_kv_heads):
+                    un = self.units[(b, layer, h)]
+                    u = self.u_index(b, h)
+                    ref = un.tier[:un.L]
+                    bad = np.flatnonzero(tiers[u, :un.L] != ref)
+                    assert bad.size == 0, f"t {self.t} layer {layer} unit {u}: tiers differ at {bad[:8].tolist()} " \
+                                          f"(gpu {tiers[u, bad[:8]].tolist()}, oracle {ref[bad[:8]].tolist()})"
+                    assert np.all(tiers[u, un.L:] == 255)
+                    for p in range(un.L):
+                        z = int(ref[p])
+                        if z == H.EVICT:
+                            continue
+                        tier, kb, vb, kc, vc, par = self.cache.token(layer, u, p)
+                        assert tier == z
+                        if z == H.BF16:
+                            if p % 7 == 0:   # a sample of the BF16 tokens
+                                assert np.array_equal(gen.bf16_bits_to_f32(kb), un.K[p])
+                                assert np.array_equal(gen.bf16_bits_to_f32(vb), un.V[p])
+                                self.bf16_checked += 1
+                            continue
+                        tc = un.codes[p]
+                        assert np.array_equal(kc, tc.k_codes), f"layer {layer} unit {u} pos {p} tier {z}: key codes"
+                        assert np.array_equal(vc, tc.v_codes), f"layer {layer} unit {u} pos {p} tier {z}: value codes"
+                        ref_par = np.array([tc.k_p0, tc.k_p1, tc.v_p0, tc.v_p1], np.float32)
+                        assert np.array_equal(par.view(np.uint32), ref_par.view(np.uint32)), \
+                            f"layer {layer} unit {u} pos {p} tier {z}: params {par} vs {ref_par}"
+                        self.codes_checked += 1
+
+
+@pytest.mark.parametrize("name", sorted(CASES))
+def test_five_tier_trajectory(name):
+    wl = CASES[name]
+    run = TokRun(wl)
+    run.prefill()
+    run.check_state()
+    for _ in range(wl.decode_steps):
+        run.step()
+    run.cache.qe_synchronize()
+    counts = run.cache.token_counts(0)
+    print(f"{name}: max out rel-L2 {run.max_out:.2e}, max score rel {run.max_score:.2e}, codes {run.codes_checked}, "
+          f"bf16 {run.bf16_checked}, counts unit 0 {counts[0].tolist()}")
+    assert run.codes_checked > 0
+    assert (counts[:, 1:4] > 0).all()

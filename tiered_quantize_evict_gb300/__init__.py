@@ -28,7 +28,10 @@ EXPORTED = [
     "qe_synchronize", "qe_get_layer_info", "qe_get_tiers", "qe_get_scores", "qe_set_scores",
     "qe_get_quant_window", "qe_get_bf16_window", "qe_get_route_stats", "qe_set_timing",
     "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc", "qe_get_route_diag",
+    "qe_get_token_tiers", "qe_get_token_scores", "qe_get_token_counts", "qe_get_token",
 ]
+QE_TIERING_WINDOWS, QE_TIERING_TOKENS = 0, 1
+TOK_BF16, TOK_INT4, TOK_INT2, TOK_NQ1, TOK_EVICTED, TOK_ABSENT = 0, 1, 2, 3, 4, 255
 
 
 class QEConfig(ctypes.Structure):
@@ -39,6 +42,8 @@ class QEConfig(ctypes.Structure):
         ("max_context", ctypes.c_int), ("cap_mode", ctypes.c_int), ("kf", ctypes.c_int),
         ("kq", ctypes.c_int), ("frac_bf16", ctypes.c_double), ("frac_int2", ctypes.c_double),
         ("budget_frac", ctypes.c_double), ("out_fp32", ctypes.c_int),
+        ("tiering", ctypes.c_int), ("frac_int4", ctypes.c_double), ("frac_nq1", ctypes.c_double),
+        ("score_window", ctypes.c_int),
     ]
 
 
@@ -103,6 +108,10 @@ def load_library() -> ctypes.CDLL:
         "qe_kernel_launches": ([P], ctypes.c_longlong),
         "qe_decode_step_noalloc": ([P, I, P, P], I),
         "qe_get_route_diag": ([P, I, ctypes.POINTER(QERouteDiag), S], I),
+        "qe_get_token_tiers": ([P, I, P, S], I),
+        "qe_get_token_scores": ([P, I, P, S], I),
+        "qe_get_token_counts": ([P, I, P, S], I),
+        "qe_get_token": ([P, I, I, I, ctypes.POINTER(I), P, P, P, P, P], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -235,6 +244,35 @@ class QECache:
         self._check(self._lib.qe_get_route_diag(self.h, layer, arr, units))
         return list(arr)
 
+    # ---------------------------------------------------------------- five-tier mode
+    def token_tiers(self, layer: int) -> np.ndarray:
+        """[units][max_context] uint8 tier of every position (TOK_*)."""
+        out = np.zeros((self.cfg.batch * self.cfg.n_kv_heads, self.cfg.max_context), np.uint8)
+        self._check(self._lib.qe_get_token_tiers(self.h, layer, out.ctypes.data, out.nbytes))
+        return out
+
+    def token_scores(self, layer: int) -> np.ndarray:
+        out = np.zeros((self.cfg.batch * self.cfg.n_kv_heads, self.cfg.max_context), np.float32)
+        self._check(self._lib.qe_get_token_scores(self.h, layer, out.ctypes.data, out.nbytes))
+        return out
+
+    def token_counts(self, layer: int) -> np.ndarray:
+        """[units][5]: ranked BF16, INT4, INT2, 1-bit, BF16 tail."""
+        out = np.zeros((self.cfg.batch * self.cfg.n_kv_heads, 5), np.int32)
+        self._check(self._lib.qe_get_token_counts(self.h, layer, out.ctypes.data, out.nbytes))
+        return out
+
+    def token(self, layer: int, unit: int, pos: int):
+        """(tier, k_bf16 bits, v_bf16 bits, k_codes, v_codes, params[4]) of one position."""
+        d = self.cfg.head_dim
+        tier = ctypes.c_int()
+        kb, vb = np.zeros(d, np.uint16), np.zeros(d, np.uint16)
+        kc, vc = np.zeros(d, np.uint8), np.zeros(d, np.uint8)
+        par = np.zeros(4, np.float32)
+        self._check(self._lib.qe_get_token(self.h, layer, unit, pos, ctypes.byref(tier), kb.ctypes.data, vb.ctypes.data,
+                                           kc.ctypes.data, vc.ctypes.data, par.ctypes.data))
+        return tier.value, kb, vb, kc, vc, par
+
     def set_timing(self, enable: bool):
         self._check(self._lib.qe_set_timing(self.h, 1 if enable else 0))
 
@@ -256,4 +294,7 @@ def config_from_workload(wl, out_fp32: bool = True, max_context: Optional[int] =
         route_period=wl.route_period, n_sink=wl.n_sink, n_recent=wl.n_recent,
         max_context=max_context or wl.max_context, cap_mode=wl.cap_mode, kf=wl.kf, kq=wl.kq,
         frac_bf16=wl.frac_bf16, frac_int2=wl.frac_int2, budget_frac=wl.budget_frac,
-        out_fp32=1 if out_fp32 else 0)
+        out_fp32=1 if out_fp32 else 0,
+        tiering=QE_TIERING_TOKENS if getattr(wl, "tiering", "windows") == "tokens" else QE_TIERING_WINDOWS,
+        frac_int4=getattr(wl, "frac_int4", 0.0), frac_nq1=getattr(wl, "frac_nq1", 0.0),
+        score_window=getattr(wl, "score_window", 0))

@@ -7,6 +7,7 @@
 
 #include "qe.h"
 #include "qe_kernels.cuh"
+#include "qe_tok.cuh"
 
 namespace qe {
 
@@ -21,6 +22,13 @@ struct LayerMirror {
   int n_full = 0;
   int n_quant = 0;
   int kf = 0, kq = 0;
+};
+
+// Host shadow of a five-tier layer.
+struct TokMirror {
+  int L = 0;
+  int n_tail = 0;     // tail tokens, the pending one included
+  int pending = 0;    // appended token whose length the next decode step's merge commits
 };
 
 }  // namespace qe
@@ -63,4 +71,24 @@ struct qe_handle_s {
   long long timed_launches = 0;
   long long launches = 0;
   std::string err;
+  // five-tier per-token mode (cfg.tiering == QE_TIERING_TOKENS)
+  bool tok = false;
+  qe::TokState ts{};
+  std::vector<qe::TokMirror> tlay;
+  float* tk_part_o = nullptr;
+  float2* tk_part_ml = nullptr;
+  float* tk_logits = nullptr;
+  int tk_grid = 0;
+  int tk_lgcap = 0;
+  std::vector<void*> tk_allocs;   // every device allocation of the mode
 };
+
+namespace qe {
+// five-tier mode (qe_tok_host.cu)
+qe_status tok_init(const qe_config& c, cudaStream_t stream, qe_handle* out, std::string& err);
+void tok_free(qe_handle h);
+qe_status tok_append(qe_handle h, int layer, const void* k, const void* v, int n, int flags);
+qe_status tok_decode(qe_handle h, int layer, const void* q, void* out, int flags);
+qe_status tok_route(qe_handle h, int layer);
+qe_status tok_layer_info(qe_handle h, int layer, qe_layer_info* info);
+}  // namespace qe

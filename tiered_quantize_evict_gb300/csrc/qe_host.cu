@@ -145,6 +145,15 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   const int G = c.n_q_heads / c.n_kv_heads;
   if (G != 1 && G != 2 && G != 4) return fail(nullptr, QE_ERR_INVALID_ARG, "query heads per KV head must be 1, 2 or 4");
   if (c.head_dim != 64 && c.head_dim != 128) return fail(nullptr, QE_ERR_INVALID_ARG, "head_dim must be 64 or 128");
+  if (c.tiering != QE_TIERING_WINDOWS && c.tiering != QE_TIERING_TOKENS)
+    return fail(nullptr, QE_ERR_INVALID_ARG, "tiering must be QE_TIERING_WINDOWS or QE_TIERING_TOKENS");
+  if (c.max_context < 1) return fail(nullptr, QE_ERR_INVALID_ARG, "bad max_context");
+  if (c.tiering == QE_TIERING_TOKENS) {
+    std::string err;
+    qe_status ts = qe::tok_init(c, static_cast<cudaStream_t>(cuda_stream), out, err);
+    if (ts != QE_OK) g_init_error = err;
+    return ts;
+  }
   if (c.window != 16 && c.window != 32 && c.window != 64) return fail(nullptr, QE_ERR_INVALID_ARG, "window must be 16, 32 or 64");
   if (c.n_sink < 0 || c.n_sink >= c.window || c.n_sink >= 16) return fail(nullptr, QE_ERR_INVALID_ARG, "need 0 <= n_sink < min(window, 16)");
   if (c.n_recent < 1) return fail(nullptr, QE_ERR_INVALID_ARG, "n_recent must be >= 1");
@@ -328,12 +337,18 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
 qe_status qe_destroy(qe_handle h) {
   if (!h) return QE_ERR_INVALID_ARG;
   cudaStreamSynchronize(h->stream);
+  if (h->tok) {
+    qe::tok_free(h);
+    delete h;
+    return QE_OK;
+  }
   free_all(h);
   delete h;
   return QE_OK;
 }
 
 qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_tokens, int flags) {
+  if (h && h->tok) return qe::tok_append(h, layer, k, v, n_tokens, flags);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if (!k || !v || n_tokens < 1) return fail(h, QE_ERR_INVALID_ARG, "append needs K, V and n_tokens >= 1");
@@ -384,6 +399,7 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
 }
 
 qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int flags) {
+  if (h && h->tok) return qe::tok_decode(h, layer, q, out, flags);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if (!q || !out) return fail(h, QE_ERR_INVALID_ARG, "decode needs q and out");
@@ -514,6 +530,7 @@ static qe_status route_layer(qe_handle h, int layer) {
 
 qe_status qe_route(qe_handle h, int layer) {
   if (!h) return QE_ERR_INVALID_ARG;
+  if (h->tok) return qe::tok_route(h, layer);
   if (layer == -1) {
     for (int l = 0; l < h->cfg.n_layers; ++l) {
       qe_status s = route_layer(h, l);
@@ -570,6 +587,10 @@ void fill_info(qe_handle h, const LayerMirror& m, qe_layer_info* info) {
 extern "C" {
 
 qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
+  if (h && h->tok) {
+    if (!info) return fail(h, QE_ERR_INVALID_ARG, "null info");
+    return qe::tok_layer_info(h, layer, info);
+  }
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if ((s = commit_pending(h, layer)) != QE_OK) return s;
@@ -591,6 +612,7 @@ qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
 }
 
 qe_status qe_get_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if ((s = commit_pending(h, layer)) != QE_OK) return s;
@@ -602,6 +624,7 @@ qe_status qe_get_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes) {
 }
 
 qe_status qe_get_scores(qe_handle h, int layer, float* host, size_t bytes) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if ((s = commit_pending(h, layer)) != QE_OK) return s;
@@ -613,6 +636,7 @@ qe_status qe_get_scores(qe_handle h, int layer, float* host, size_t bytes) {
 }
 
 qe_status qe_set_scores(qe_handle h, int layer, const float* host, size_t bytes) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if ((s = commit_pending(h, layer)) != QE_OK) return s;
@@ -630,6 +654,7 @@ static qe_status read_int(qe_handle h, const int* dptr, int* out) {
 
 qe_status qe_get_quant_window(qe_handle h, int layer, int unit, int window, uint8_t* k_codes, uint8_t* v_codes,
                               float* k_min, float* k_scale, float* v_min, float* v_scale) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if (unit < 0 || unit >= h->units || window < 0 || window >= h->st.maxw)
@@ -667,6 +692,7 @@ qe_status qe_get_quant_window(qe_handle h, int layer, int unit, int window, uint
 }
 
 qe_status qe_get_bf16_window(qe_handle h, int layer, int unit, int window, uint16_t* k, uint16_t* v) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   if (unit < 0 || unit >= h->units || window < -1 || window >= h->st.maxw)
@@ -695,6 +721,7 @@ qe_status qe_get_bf16_window(qe_handle h, int layer, int unit, int window, uint1
 }
 
 qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   if (!h || !out) return QE_ERR_INVALID_ARG;
   if (layer < -1 || layer >= h->cfg.n_layers) return fail(h, QE_ERR_INVALID_ARG, "layer out of range");
   QE_CK(h, cudaStreamSynchronize(h->stream));
@@ -715,6 +742,7 @@ qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out) {
 }
 
 qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n_units) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "a window-tier call on a token-tiered handle");
   if (!h || !out) return QE_ERR_INVALID_ARG;
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;

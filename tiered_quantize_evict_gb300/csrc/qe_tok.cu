@@ -1,0 +1,1241 @@
+// qe_tok.cu -- kernels of the five-tier per-token cache (HqeKV reading notes §3.1-§3.5; layout in
+// qe_tok.cuh): the single-token append, the split-K decode attention over BF16 / 4-bit / 2-bit /
+// 1-bit tiles with per-token logits for the importance, the split merge with the score update,
+// and the demote-only re-rank that rebuilds the pools.
+//
+// Attention (what it computes): for each unit and its G query heads, o_h = softmax(q_h K^T /
+// sqrt(d)) V over the kept tokens, every quantized token dequantized as x = code * s + z (uniform,
+// eq. (2)) or x = c_code * s + m (normal, eq. (4) centers +-Phi^-1(3/4)); on the steps that
+// count towards the importance, each token's attention mass summed over the G heads is added to
+// its float32 score.
+//
+// GB300 design:
+//  * persistent grid of 12-warp CTAs; the layer's units x tiles sequence is cut into one
+//    cost-weighted range per warp (stream-K over per-unit costs that differ after re-ranking); a
+//    warp streams its range through a private two-stage ring filled by cp.async.bulk;
+//  * Q K^T and P V run on the tensor cores (mma.m16n8k16, fp32 accumulate): b-bit codes are
+//    turned into the operands 1 + code / 2^b with one shift and one and-or per register (bf16 for
+//    keys, which meet the bf16 queries exactly; f16 for values, which meet P split into a
+//    truncated and a remainder column); the per-token key scale and offset are applied to the
+//    logits, the value scale goes into P and the value offset into a running sum;
+//  * the per-token importance leaves the attention as log2-domain logits; the merge kernel
+//    turns them into probability mass once the unit's normaliser is known.
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "qe_tok.cuh"
+#include "qe_tok_kernels.h"
+
+namespace qe {
+
+constexpr int TK_WARPS = 12;
+constexpr int TK_STAGE_TOTAL = 196608;
+constexpr unsigned long long TK_WAIT_NS = 200000000ull;   // 0.2 s
+constexpr float TK_NQ1_C = 0.67448975f;                   // Phi^-1(3/4) rounded to float32
+constexpr int TK_MERGE_THREADS = 512;
+constexpr int TK_RERANK_THREADS = 512;
+constexpr int TK_RERANK_WARPS = TK_RERANK_THREADS / 32;
+
+// ------------------------------------------------------------------------------ unit geometry
+struct TkUnit {
+  int t[5];            // tiles per segment (pools BF16, INT4, INT2, 1-bit, then the tail)
+  int n[5];            // tokens per segment
+  long long s0[6];     // cost offset of each segment; s0[5] = the unit's cost
+  int tok0[5];         // token-slot offset of each segment (16 x tiles before it)
+};
+
+__device__ __forceinline__ TkUnit tk_unit(const TokState& s, int layer, int u, int n_tail) {
+  const int4 c = *reinterpret_cast<const int4*>(s.cnt + ((long long)layer * s.units + u) * 4);
+  TkUnit g;
+  g.n[0] = c.x; g.n[1] = c.y; g.n[2] = c.z; g.n[3] = c.w; g.n[4] = n_tail;
+  long long x = 0;
+  int tk = 0;
+#pragma unroll
+  for (int z = 0; z < 5; ++z) {
+    g.t[z] = (g.n[z] + 15) >> 4;
+    g.s0[z] = x;
+    g.tok0[z] = tk;
+    x += (long long)g.t[z] * s.cost[z];
+    tk += 16 * g.t[z];
+  }
+  g.s0[5] = x;
+  return g;
+}
+
+// cost offset of unit u: ranked prefix plus u tails
+__device__ __forceinline__ long long tk_X(const long long* cum, int u, long long tail_cost) {
+  return cum[u] + (long long)u * tail_cost;
+}
+
+// unit holding cost position x (largest u with X(u) <= x)
+__device__ __forceinline__ int tk_unit_of(const long long* cum, int units, long long tail_cost, long long x) {
+  int lo = 0, hi = units - 1;
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (tk_X(cum, mid, tail_cost) <= x) lo = mid;
+    else hi = mid - 1;
+  }
+  return lo;
+}
+
+__device__ __forceinline__ const uint8_t* tk_tile_src(const TokState& s, int layer, int buf, int u, int z, int k) {
+  if (z == 4) return s.tail + (tk_tail_tok_index(s, layer, buf, u) / 16 + k) * (long long)s.g.bf_tile();
+  return s.pool[z] + (tk_pool_tile_index(s, z, layer, buf, u) + k) * (long long)tk_tile_bytes(s, z);
+}
+
+// ------------------------------------------------------------------------------ helpers
+__device__ __forceinline__ uint4 tk_lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+template <int WPL>
+__device__ __forceinline__ void tk_load_words(const uint8_t* blk, int lane, unsigned (&w)[WPL]) {
+  constexpr int CW = WPL < 4 ? WPL : 4;
+#pragma unroll
+  for (int c = 0; c < WPL / CW; ++c) {
+    const uint8_t* src = blk + (c * 32 + lane) * (CW * 4);
+    if constexpr (CW == 4) {
+      const uint4 v = tk_lds128(src);
+      w[c * 4 + 0] = v.x; w[c * 4 + 1] = v.y; w[c * 4 + 2] = v.z; w[c * 4 + 3] = v.w;
+    } else if constexpr (CW == 2) {
+      const uint2 v = *reinterpret_cast<const uint2*>(src);
+      w[c * 2 + 0] = v.x; w[c * 2 + 1] = v.y;
+    } else {
+      w[c] = *reinterpret_cast<const unsigned*>(src);
+    }
+  }
+}
+
+// register r of step k (inside a word) as the operand pair 1 + code / 2^B: bf16 (EB = 7 mantissa
+// bits, ONE = 0x3F80) or f16 (EB = 10, ONE = 0x3C00)
+template <int B, int EB, unsigned ONE>
+__device__ __forceinline__ unsigned tk_pair(unsigned w, int k, int r) {
+  const int sh = (EB - B) - B * (4 * k + r);
+  const unsigned x = sh >= 0 ? (w << sh) : (w >> (-sh));
+  constexpr unsigned MASK = (((1u << B) - 1u) << (EB - B)) * 0x00010001u;
+  return (x & MASK) | (ONE * 0x00010001u);
+}
+
+template <int MC>
+struct TkRun {
+  float mref, l, zs;
+  float O[MC][4];
+};
+
+// Online softmax of one 16-token tile (rows g, g + 8 of this lane, head t).  Q: per-row key
+// scale and offset (logit = ks v + kb) and per-row value scale (into P) and offset (into zs).
+// lg: this tile's per-token logits (row * G + head), or null.
+template <int MC, bool Q>
+__device__ __forceinline__ void tk_softmax(float (&acc)[2][4], int nvalid, const float (&ksc)[2], const float (&kbi)[2],
+                                           const float (&vz)[2], const float (&vs)[2], float scale_log2, TkRun<MC>& st,
+                                           unsigned (&Bp)[2], float* lg, int G, int lane) {
+  const int g = lane >> 2, t = lane & 3;
+  float x[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float v = (acc[0][2 * j] + acc[0][2 * j + 1]) + (acc[1][2 * j] + acc[1][2 * j + 1]);
+    x[j] = (Q ? fmaf(v, ksc[j], kbi[j]) : v) * scale_log2;
+    if (g + 8 * j >= nvalid) x[j] = -INFINITY;
+  }
+  if (lg != nullptr && t < G) {
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+      if (g + 8 * j < nvalid) lg[(g + 8 * j) * G + t] = x[j];
+  }
+  float mx = fmaxf(x[0], x[1]);
+  if (__any_sync(0xffffffffu, mx > st.mref + 8.f)) {
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(st.mref, mx);
+    const float alpha = (st.mref == -INFINITY) ? 0.f : ex2(st.mref - mn);
+    st.mref = mn;
+    st.l *= alpha;
+    st.zs *= alpha;
+#pragma unroll
+    for (int mc = 0; mc < MC; ++mc)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) st.O[mc][r] *= alpha;
+  }
+  const float muse = st.mref == -INFINITY ? 0.f : st.mref;
+  float pr[2];
+  float mass = 0.f, zadd = 0.f;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    pr[j] = ex2(x[j] - muse);
+    mass += pr[j];
+    if constexpr (Q) zadd = fmaf(pr[j], vz[j], zadd);
+  }
+  if constexpr (Q) st.zs += zadd;
+  mass += __shfl_xor_sync(0xffffffffu, mass, 4);
+  mass += __shfl_xor_sync(0xffffffffu, mass, 8);
+  mass += __shfl_xor_sync(0xffffffffu, mass, 16);
+  st.l += mass;
+  constexpr unsigned KEEP = Q ? 0xFFFFE000u : 0xFFFF0000u;
+  unsigned rr[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float y = pr[j];
+    if constexpr (Q) y *= vs[j];
+    const float yh = __uint_as_float(__float_as_uint(y) & KEEP);
+    rr[j] = Q ? pack_f16x2_rz(yh, y - yh) : pack_bf16x2_rz(yh, y - yh);
+  }
+  Bp[0] = movmatrix_t(rr[0]);
+  Bp[1] = movmatrix_t(rr[1]);
+}
+
+// (z_eff, s_eff) with x = z_eff + s_eff code: uniform (min, scale) as stored; normal (mean, std)
+// with centers -+c: (m - c s, 2 c s)
+__device__ __forceinline__ float2 tk_affine(float2 p, bool normal) {
+  if (!normal) return p;
+  return make_float2(fmaf(-TK_NQ1_C, p.y, p.x), 2.f * TK_NQ1_C * p.y);
+}
+
+struct TkDesc {
+  int u, kind, nvalid, tokslot;
+};
+
+struct TkAttnArgs {
+  TokState st;
+  int layer, pend;
+  const uint16_t* q;
+  float scale_log2;
+  float* part_o;
+  float2* part_ml;
+  float* logits;
+  int lg_cap;
+};
+
+template <int D>
+__device__ __forceinline__ void tk_tile_bf16(const uint8_t* sp, int nvalid, const unsigned (&qb)[D / 16][2],
+                                             TkRun<D / 16>& rs, float* lg, float scale_log2, int G, int lane) {
+  constexpr int KS = D / 16, MC = D / 16;
+  float acc[2][4] = {};
+#pragma unroll
+  for (int ks = 0; ks < KS; ++ks) {
+    const uint4 a = tk_lds128(sp + ks * 512 + lane * 16);
+    mma_bf16(acc[ks & 1], a.x, a.y, a.z, a.w, qb[ks][0], qb[ks][1]);
+  }
+  const float none[2] = {0.f, 0.f};
+  unsigned Bp[2];
+  tk_softmax<MC, false>(acc, nvalid, none, none, none, none, scale_log2, rs, Bp, lg, G, lane);
+#pragma unroll
+  for (int mc = 0; mc < MC; ++mc) {
+    const uint4 a = tk_lds128(sp + 32 * D + mc * 512 + lane * 16);
+    mma_bf16(rs.O[mc], a.x, a.y, a.z, a.w, Bp[0], Bp[1]);
+  }
+}
+
+template <int D, int B>
+__device__ __forceinline__ void tk_tile_q(const uint8_t* sp, int nvalid, bool normal, const unsigned (&qb)[D / 16][2],
+                                          float qsum, TkRun<D / 16>& rs, float* lg, float scale_log2, int G, int lane) {
+  constexpr int KS = D / 16, MC = D / 16, WPL = D * B / 64, PW = 4 / B;
+  constexpr float TWO_B = (float)(1 << B);
+  const TokGeo geo{D};
+  const int g = lane >> 2;
+  // per-row parameters (rows g, g + 8)
+  const float2* kp = reinterpret_cast<const float2*>(sp + geo.off_kpar(B));
+  const float2* vp = reinterpret_cast<const float2*>(sp + geo.off_vpar(B));
+  float ksc[2], kbi[2], vz[2], vs[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float2 ka = tk_affine(kp[g + 8 * j], normal);
+    const float2 va = tk_affine(vp[g + 8 * j], normal);
+    ksc[j] = TWO_B * ka.y;
+    kbi[j] = fmaf(-TWO_B, ka.y, ka.x) * qsum;
+    vs[j] = TWO_B * va.y;
+    vz[j] = fmaf(-TWO_B, va.y, va.x);
+  }
+  float acc[2][4] = {};
+  {
+    unsigned wk[WPL];
+    tk_load_words<WPL>(sp, lane, wk);
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      const unsigned w = wk[ks / PW];
+      const int k = ks % PW;
+      mma_bf16(acc[ks & 1], tk_pair<B, 7, 0x3F80u>(w, k, 0), tk_pair<B, 7, 0x3F80u>(w, k, 1),
+               tk_pair<B, 7, 0x3F80u>(w, k, 2), tk_pair<B, 7, 0x3F80u>(w, k, 3), qb[ks][0], qb[ks][1]);
+    }
+  }
+  unsigned Bp[2];
+  tk_softmax<MC, true>(acc, nvalid, ksc, kbi, vz, vs, scale_log2, rs, Bp, lg, G, lane);
+  {
+    unsigned wv[WPL];
+    tk_load_words<WPL>(sp + geo.off_vcode(B), lane, wv);
+#pragma unroll
+    for (int mc = 0; mc < MC; ++mc) {
+      const unsigned w = wv[mc / PW];
+      const int k = mc % PW;
+      mma_f16(rs.O[mc], tk_pair<B, 10, 0x3C00u>(w, k, 0), tk_pair<B, 10, 0x3C00u>(w, k, 1),
+              tk_pair<B, 10, 0x3C00u>(w, k, 2), tk_pair<B, 10, 0x3C00u>(w, k, 3), Bp[0], Bp[1]);
+    }
+  }
+}
+
+// whether this decode step adds to the importance (the last score_window steps of a period)
+__device__ __forceinline__ bool tk_scoring(const TokState& s, int step_before) {
+  const int sidx = step_before + 1;
+  return s.score_window == 0 || sidx > s.period - s.score_window;
+}
+
+template <int D>
+__global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnArgs p) {
+  constexpr int KS = D / 16, MC = D / 16;
+  constexpr int STAGE = 64 * D;   // a BF16 tile, the largest
+  constexpr int NST = TK_STAGE_TOTAL / (TK_WARPS * STAGE) < 4 ? TK_STAGE_TOTAL / (TK_WARPS * STAGE) : 4;
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ __align__(8) unsigned long long bars[TK_WARPS][NST];
+  __shared__ TkDesc descs[TK_WARPS][NST];
+  const TokState& S = p.st;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int g = lane >> 2, t = lane & 3;
+  const int G = S.G;
+  const int NW = gridDim.x * TK_WARPS;
+  const int wg = blockIdx.x * TK_WARPS + warp;
+  const TokLayer hd = S.hdr[p.layer];
+  const int n_tail = hd.n_tail + p.pend;
+  const int buf = hd.buf;
+  const bool scoring = tk_scoring(S, hd.step);
+  griddep_launch_dependents();
+  const long long* cum = S.cum + (long long)p.layer * (S.units + 1);
+  const long long tail_cost = (long long)S.cost[4] * ((n_tail + 15) >> 4);
+  const long long C = tk_X(cum, S.units, tail_cost);
+  const long long x_lo = ((long long)wg * C + NW - 1) / NW;
+  const long long x_hi = (((long long)wg + 1) * C + NW - 1) / NW;
+  if (x_lo >= x_hi) {   // empty range: an empty partial in the unit it falls into
+    if (x_lo < C) {
+      const int u = tk_unit_of(cum, S.units, tail_cost, x_lo);
+      if (lane < G) p.part_ml[((long long)wg + u) * G + lane] = make_float2(-INFINITY, 0.f);
+    }
+    return;
+  }
+  const int u_first = tk_unit_of(cum, S.units, tail_cost, x_lo);
+  const int u_last = tk_unit_of(cum, S.units, tail_cost, x_hi - 1);
+
+  uint8_t* stage_base = smem + (size_t)warp * NST * STAGE;
+  if (lane == 0) {
+    for (int s = 0; s < NST; ++s) mbar_init(smem_u32(&bars[warp][s]), 1);
+    mbar_fence_init();
+  }
+  __syncwarp();
+
+  // ---- producer cursor (lane-uniform): unit cu, segment cz, tile ck
+  int cu = u_first;
+  TkUnit un = tk_unit(S, p.layer, cu, n_tail);
+  long long ux = tk_X(cum, cu, tail_cost);
+  int cz = 0, ck = 0;
+  bool cvalid = true;
+  {
+    // first tile whose start >= x_lo
+    const long long r = x_lo - ux;
+    cz = 5;
+    for (int z = 0; z < 5; ++z) {
+      if (un.t[z] == 0) continue;
+      const long long last = un.s0[z] + (long long)(un.t[z] - 1) * S.cost[z];
+      if (r <= last) {
+        cz = z;
+        ck = r <= un.s0[z] ? 0 : (int)((r - un.s0[z] + S.cost[z] - 1) / S.cost[z]);
+        break;
+      }
+    }
+    if (cz == 5) {   // past the unit's last tile start: the next unit's first tile
+      ++cu;
+      if (cu >= S.units) cvalid = false;
+      else {
+        un = tk_unit(S, p.layer, cu, n_tail);
+        ux = tk_X(cum, cu, tail_cost);
+        cz = 0;
+        ck = 0;
+        while (cz < 5 && un.t[cz] == 0) ++cz;
+      }
+    }
+  }
+  auto advance = [&]() {
+    ++ck;
+    if (ck < un.t[cz]) return;
+    ck = 0;
+    ++cz;
+    while (cz < 5 && un.t[cz] == 0) ++cz;
+    if (cz < 5) return;
+    ++cu;
+    if (cu >= S.units) {
+      cvalid = false;
+      return;
+    }
+    un = tk_unit(S, p.layer, cu, n_tail);
+    ux = tk_X(cum, cu, tail_cost);
+    cz = 0;
+    while (cz < 5 && un.t[cz] == 0) ++cz;
+  };
+  auto issue_next = [&](int stage) -> bool {
+    if (!cvalid || cz >= 5) return false;
+    const long long start = ux + un.s0[cz] + (long long)ck * S.cost[cz];
+    if (start >= x_hi) return false;
+    if (lane == 0) {
+      const int kind = cz;
+      const unsigned bytes = (unsigned)tk_tile_bytes(S, kind == 4 ? TK_TAIL : kind);
+      TkDesc d;
+      d.u = cu;
+      d.kind = kind;
+      const int rem = un.n[cz] - 16 * ck;
+      d.nvalid = rem < 16 ? rem : 16;
+      d.tokslot = un.tok0[cz] + 16 * ck;
+      descs[warp][stage] = d;
+      const unsigned bar = smem_u32(&bars[warp][stage]);
+      mbar_expect_tx(bar, bytes);
+      bulk_g2s(smem_u32(stage_base + (size_t)stage * STAGE), tk_tile_src(S, p.layer, buf, cu, kind, ck), bytes, bar);
+    }
+    advance();
+    return true;
+  };
+  int issued = 0;
+  for (int s = 0; s < NST; ++s) {
+    if (!issue_next(s)) break;
+    ++issued;
+  }
+  __syncwarp();
+
+  // ---- consumer
+  TkRun<MC> rs;
+  unsigned qb[KS][2];
+  float qsum = 0.f;
+  int cur_u = u_first, q_unit = -1;
+  const int hh = g >> 1;
+  const bool lo_col = (g & 1) != 0;
+  auto reset = [&]() {
+    rs.mref = -INFINITY;
+    rs.l = 0.f;
+    rs.zs = 0.f;
+#pragma unroll
+    for (int mc = 0; mc < MC; ++mc)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) rs.O[mc][r] = 0.f;
+  };
+  auto flush = [&](int u) {
+    const long long slot = (long long)wg + u;
+    float z = rs.zs;
+    z += __shfl_xor_sync(0xffffffffu, z, 4);
+    z += __shfl_xor_sync(0xffffffffu, z, 8);
+    z += __shfl_xor_sync(0xffffffffu, z, 16);
+    if (t < G) {
+      float* po = p.part_o + (slot * G + t) * D;
+#pragma unroll
+      for (int mc = 0; mc < MC; ++mc) {
+        po[mc * 16 + g] = rs.O[mc][0] + rs.O[mc][1] + z;
+        po[mc * 16 + g + 8] = rs.O[mc][2] + rs.O[mc][3] + z;
+      }
+      if (g == 0) p.part_ml[slot * G + t] = make_float2(rs.mref, rs.l);
+    }
+  };
+  reset();
+  auto wait_tile = [&](int k) -> bool {
+    const unsigned bar = smem_u32(&bars[warp][k % NST]);
+    const unsigned parity = (k / NST) & 1;
+    unsigned long long t0 = 0;
+    int spins = 0;
+    bool ok = true;
+    while (!mbar_try_wait(bar, parity)) {
+      if (++spins == 64) {
+        spins = 0;
+        const unsigned long long now = globaltimer_ns();
+        if (t0 == 0) t0 = now;
+        else if (now - t0 > TK_WAIT_NS) { ok = false; break; }
+      }
+    }
+    return __all_sync(0xffffffffu, ok);
+  };
+  bool timed_out = false;
+  int k = 0;
+  for (; k < issued; ++k) {
+    const int s = k % NST;
+    if (!wait_tile(k)) { timed_out = true; break; }
+    const TkDesc d = descs[warp][s];
+    const uint8_t* sp = stage_base + (size_t)s * STAGE;
+    while (d.u > cur_u) {
+      flush(cur_u);
+      reset();
+      ++cur_u;
+    }
+    if (q_unit != cur_u) {
+      q_unit = cur_u;
+      const int b = cur_u / S.Hkv, kvh = cur_u - b * S.Hkv;
+      const uint16_t* qh = p.q + ((size_t)b * S.Hq + kvh * G + hh) * D;
+      const bool act = hh < G;
+      float part = 0.f;
+#pragma unroll
+      for (int ks = 0; ks < KS; ++ks) {
+        const unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
+        const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
+        part += (bf16lo_to_f32(a0) + bf16hi_to_f32(a0)) + (bf16lo_to_f32(a1) + bf16hi_to_f32(a1));
+        qb[ks][0] = lo_col ? 0u : a0;
+        qb[ks][1] = lo_col ? 0u : a1;
+      }
+      part += __shfl_xor_sync(0xffffffffu, part, 1);
+      part += __shfl_xor_sync(0xffffffffu, part, 2);
+      qsum = __shfl_sync(0xffffffffu, part, 8 * t);   // sum of q over the channels, head t
+    }
+    float* lg = scoring ? p.logits + ((long long)d.u * p.lg_cap + d.tokslot) * G : nullptr;
+    switch (d.kind) {
+      case 0:
+      case 4: tk_tile_bf16<D>(sp, d.nvalid, qb, rs, lg, p.scale_log2, G, lane); break;
+      case 1: tk_tile_q<D, 4>(sp, d.nvalid, false, qb, qsum, rs, lg, p.scale_log2, G, lane); break;
+      case 2: tk_tile_q<D, 2>(sp, d.nvalid, false, qb, qsum, rs, lg, p.scale_log2, G, lane); break;
+      default: tk_tile_q<D, 1>(sp, d.nvalid, true, qb, qsum, rs, lg, p.scale_log2, G, lane); break;
+    }
+    __syncwarp();
+    if (issue_next(s)) ++issued;
+    __syncwarp();
+  }
+  if (timed_out) {
+    if (lane == 0) atomicOr(S.err, ERR_TIMEOUT);
+    for (int kk = k + 1; kk < issued; ++kk) wait_tile(kk);
+    return;
+  }
+  while (cur_u <= u_last) {
+    flush(cur_u);
+    reset();
+    ++cur_u;
+  }
+}
+
+// ------------------------------------------------------------------------------ append
+// Single-token append: the token goes to the tail at index n_tail (its length is committed by
+// the decode step's merge, or by tk_commit_kernel).
+__global__ void tk_append1_kernel(TokState s, int layer, const uint16_t* __restrict__ k, const uint16_t* __restrict__ v) {
+  const TokLayer hd = s.hdr[layer];
+  const int D = s.g.D;
+  const int u = blockIdx.x;
+  const int c = 2 * threadIdx.x;
+  if (c >= D) return;
+  const int idx = hd.n_tail;
+  if (idx >= s.cap_tail) {
+    if (threadIdx.x == 0) atomicOr(s.err, ERR_CAPACITY);
+    return;
+  }
+  const long long tb = tk_tail_tok_index(s, layer, hd.buf, u);
+  uint8_t* tile = s.tail + (tb / 16 + idx / 16) * (long long)s.g.bf_tile();
+  const Geo g16{D, 16};
+  const int row = idx & 15;
+  const size_t src = (size_t)u * D + c;
+  *reinterpret_cast<unsigned*>(tile + bf16_k_off(g16, row, c)) = *reinterpret_cast<const unsigned*>(k + src);
+  *reinterpret_cast<uint16_t*>(tile + bf16_v_off(g16, row, c)) = v[src];
+  *reinterpret_cast<uint16_t*>(tile + bf16_v_off(g16, row, c + 1)) = v[src + 1];
+  if (threadIdx.x == 0) {
+    s.tail_pos[tb + idx] = hd.L;
+    s.tail_score[tb + idx] = 0.f;
+  }
+}
+
+// Multi-token append of n tokens at length L0 = hd.L.  prefill (L0 == 0): the sink and the last
+// n_recent tokens go to the tail, the rest to the ranked BF16 pool; otherwise all to the tail.
+__global__ void tk_append_kernel(TokState s, int layer, int n, int prefill, const uint16_t* __restrict__ k,
+                                 const uint16_t* __restrict__ v) {
+  const TokLayer hd = s.hdr[layer];
+  const int D = s.g.D;
+  const Geo g16{D, 16};
+  const long long total = (long long)s.units * n * (D / 2);
+  const int mid_lo = s.n_sink < n ? s.n_sink : n;
+  int mid_hi = n - s.n_recent;
+  if (mid_hi < mid_lo) mid_hi = mid_lo;
+  for (long long e = blockIdx.x * (long long)blockDim.x + threadIdx.x; e < total; e += (long long)gridDim.x * blockDim.x) {
+    const int c = 2 * (int)(e % (D / 2));
+    const long long ti = e / (D / 2);
+    const int i = (int)(ti % n);
+    const int u = (int)(ti / n);
+    uint8_t* tile;
+    int row, idx;
+    int* posp;
+    float* scp;
+    if (prefill && i >= mid_lo && i < mid_hi) {
+      idx = i - mid_lo;
+      if (idx >= s.cap[0]) { atomicOr(s.err, ERR_CAPACITY); continue; }
+      const long long b0 = tk_pool_tok_index(s, 0, layer, hd.buf, u);
+      tile = s.pool[0] + (tk_pool_tile_index(s, 0, layer, hd.buf, u) + idx / 16) * (long long)s.g.bf_tile();
+      posp = s.pos[0] + b0 + idx;
+      scp = s.score[0] + b0 + idx;
+    } else {
+      idx = prefill ? (i < mid_lo ? i : mid_lo + (i - mid_hi)) : hd.n_tail + i;
+      if (idx >= s.cap_tail) { atomicOr(s.err, ERR_CAPACITY); continue; }
+      const long long tb = tk_tail_tok_index(s, layer, hd.buf, u);
+      tile = s.tail + (tb / 16 + idx / 16) * (long long)s.g.bf_tile();
+      posp = s.tail_pos + tb + idx;
+      scp = s.tail_score + tb + idx;
+    }
+    row = idx & 15;
+    const size_t src = ((size_t)u * n + i) * D + c;
+    *reinterpret_cast<unsigned*>(tile + bf16_k_off(g16, row, c)) = *reinterpret_cast<const unsigned*>(k + src);
+    *reinterpret_cast<uint16_t*>(tile + bf16_v_off(g16, row, c)) = v[src];
+    *reinterpret_cast<uint16_t*>(tile + bf16_v_off(g16, row, c + 1)) = v[src + 1];
+    if (c == 0) {
+      *posp = hd.L + i;
+      *scp = 0.f;
+    }
+  }
+}
+
+// Header update after a multi-token append (one thread): length, tail count and, after a
+// prefill, the ranked BF16 count of every unit and the cost prefix.
+__global__ void tk_commit_kernel(TokState s, int layer, int n, int prefill) {
+  if (threadIdx.x != 0 || blockIdx.x != 0) return;
+  TokLayer& hd = s.hdr[layer];
+  int* cnt = s.cnt + (long long)layer * s.units * 4;
+  long long* cum = s.cum + (long long)layer * (s.units + 1);
+  if (prefill) {
+    const int mid_lo = s.n_sink < n ? s.n_sink : n;
+    int mid_hi = n - s.n_recent;
+    if (mid_hi < mid_lo) mid_hi = mid_lo;
+    hd.n_tail = mid_lo + (n - mid_hi);
+    const long long c0 = (long long)s.cost[0] * ((mid_hi - mid_lo + 15) >> 4);
+    cum[0] = 0;
+    for (int u = 0; u < s.units; ++u) {
+      cnt[u * 4 + 0] = mid_hi - mid_lo;
+      cnt[u * 4 + 1] = cnt[u * 4 + 2] = cnt[u * 4 + 3] = 0;
+      cum[u + 1] = cum[u] + c0;
+    }
+  } else {
+    hd.n_tail += n;
+  }
+  hd.L += n;
+}
+
+// ------------------------------------------------------------------------------ merge
+struct TkMergeArgs {
+  TokState st;
+  int layer, pend, NW;
+  const float* part_o;
+  const float2* part_ml;
+  const float* logits;
+  int lg_cap;
+  void* out;
+  int out_fp32;
+};
+
+// One CTA per unit: merge the partials of the warps whose ranges met the unit, write o_h, and on
+// scoring steps add each token's mass (sum over the G heads of 2^(logit - lse_h)) to its score.
+// A programmatic dependent of the attention launch.  The last CTA commits the appended token.
+template <int D>
+__global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMergeArgs p) {
+  extern __shared__ float s_sc[];   // [G][np]
+  __shared__ float s_inv[4], s_lse[4];
+  __shared__ bool s_last;
+  const TokState& S = p.st;
+  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int G = S.G;
+  const TokLayer hd = S.hdr[p.layer];
+  const int n_tail = hd.n_tail + p.pend;
+  const bool scoring = tk_scoring(S, hd.step);
+  const long long* cum = S.cum + (long long)p.layer * (S.units + 1);
+  const long long tail_cost = (long long)S.cost[4] * ((n_tail + 15) >> 4);
+  const long long C = tk_X(cum, S.units, tail_cost);
+  const long long X0 = tk_X(cum, u, tail_cost), X1 = tk_X(cum, u + 1, tail_cost);
+  const long long w0 = X0 * p.NW / C, w1 = (X1 - 1) * p.NW / C;
+  const int np = (int)(w1 - w0 + 1);
+  const long long slot0 = w0 + u;
+  const TkUnit un = tk_unit(S, p.layer, u, n_tail);
+  griddep_wait();
+  if (warp < G) {
+    const int h = warp;
+    float M = -INFINITY;
+    for (int k = lane; k < np; k += 32) M = fmaxf(M, p.part_ml[(slot0 + k) * G + h].x);
+    for (int o = 16; o; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float Mu = M == -INFINITY ? 0.f : M;
+    float Ls = 0.f;
+    for (int k = lane; k < np; k += 32) {
+      const float2 ml = p.part_ml[(slot0 + k) * G + h];
+      const float sc = ml.y > 0.f ? ex2(ml.x - Mu) : 0.f;
+      s_sc[h * np + k] = sc;
+      Ls = fmaf(ml.y, sc, Ls);
+    }
+    for (int o = 16; o; o >>= 1) Ls += __shfl_xor_sync(0xffffffffu, Ls, o);
+    if (lane == 0) {
+      s_inv[h] = 1.f / Ls;
+      s_lse[h] = Mu + lg2(Ls);
+    }
+  }
+  __syncthreads();
+  for (int e = tid; e < G * D; e += TK_MERGE_THREADS) {
+    const int h = e / D, c = e - h * D;
+    float acc = 0.f;
+    for (int k = 0; k < np; ++k) {
+      const float sc = s_sc[h * np + k];
+      if (sc != 0.f) acc = fmaf(p.part_o[((slot0 + k) * G + h) * D + c], sc, acc);
+    }
+    const float o = acc * s_inv[h];
+    const int bb = u / S.Hkv, kvh = u - bb * S.Hkv;
+    const size_t oi = ((size_t)bb * S.Hq + kvh * G + h) * D + c;
+    if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+    else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+  }
+  if (scoring) {
+    const float* lgu = p.logits + (long long)u * p.lg_cap * G;
+    for (int z = 0; z < 5; ++z) {
+      float* sc;
+      if (z < 4) sc = S.score[z] + tk_pool_tok_index(S, z, p.layer, hd.buf, u);
+      else sc = S.tail_score + tk_tail_tok_index(S, p.layer, hd.buf, u);
+      const int first = z < 4 ? 0 : S.n_sink;   // sink tokens are never scored
+      for (int i = first + tid; i < un.n[z]; i += TK_MERGE_THREADS) {
+        const float* lg = lgu + (long long)(un.tok0[z] + i) * G;
+        float m = 0.f;
+        for (int h = 0; h < G; ++h) m += ex2(lg[h] - s_lse[h]);
+        sc[i] += m;
+      }
+    }
+  }
+  // commit: the last CTA advances the header
+  __syncthreads();
+  if (tid == 0) {
+    __threadfence();
+    const unsigned prev = atomicAdd(S.done + p.layer, 1u);
+    s_last = prev == (unsigned)S.units - 1;
+  }
+  __syncthreads();
+  if (s_last && tid == 0) {
+    TokLayer& h = S.hdr[p.layer];
+    h.L += p.pend;
+    h.n_tail += p.pend;
+    h.step += 1;
+    S.done[p.layer] = 0;
+  }
+}
+
+// ------------------------------------------------------------------------------ re-rank
+// a value of a token held by pool/tail `sz` at index `si` (buffer buf), channel c
+__device__ __forceinline__ const uint8_t* tk_src_tile(const TokState& s, int layer, int buf, int u, int sz, int si) {
+  if (sz == TK_TAIL) return s.tail + (tk_tail_tok_index(s, layer, buf, u) / 16 + si / 16) * (long long)s.g.bf_tile();
+  return s.pool[sz] + (tk_pool_tile_index(s, sz, layer, buf, u) + si / 16) * (long long)tk_tile_bytes(s, sz);
+}
+
+__device__ __forceinline__ unsigned tk_code_at(const TokGeo& g, const uint8_t* tile, int b, int row, int c, bool value) {
+  const CodePos cp = value ? tk_vcode_pos(g, b, row, c) : tk_kcode_pos(g, b, row, c);
+  const unsigned w = *reinterpret_cast<const unsigned*>(tile + cp.byte);
+  return (w >> cp.bit) & ((1u << b) - 1u);
+}
+
+__device__ __forceinline__ float tk_value_at(const TokState& s, const uint8_t* tile, int sz, int row, int c, bool value) {
+  const Geo g16{s.g.D, 16};
+  if (sz == TK_BF16 || sz == TK_TAIL) {
+    const int off = value ? bf16_v_off(g16, row, c) : bf16_k_off(g16, row, c);
+    return __uint_as_float((unsigned)*reinterpret_cast<const uint16_t*>(tile + off) << 16);
+  }
+  const int b = tk_bits(sz);
+  const unsigned code = tk_code_at(s.g, tile, b, row, c, value);
+  const float2 par = reinterpret_cast<const float2*>(tile + (value ? s.g.off_vpar(b) : s.g.off_kpar(b)))[row];
+  if (sz == TK_NQ1) return fmaf(code ? TK_NQ1_C : -TK_NQ1_C, par.y, par.x);
+  return fmaf((float)code, par.y, par.x);
+}
+
+// eq. (2) decision, as IEEE float32 division decides it (fast estimate, exact division within
+// 1e-5 of a half-integer or for scales outside [1e-30, 1e30])
+__device__ __forceinline__ unsigned tk_quant_code(float x, float z, float s, float levels) {
+  if (s == 0.f) return 0u;
+  const float d = __fsub_rn(x, z);
+  float qv = __fdividef(d, s);
+  const float fr = qv - floorf(qv);
+  if (fabsf(fr - 0.5f) < 1e-5f || !(s >= 1e-30f && s <= 1e30f)) qv = __fdiv_rn(d, s);
+  qv = rintf(qv);
+  qv = fminf(fmaxf(qv, 0.f), levels);
+  return (unsigned)qv;
+}
+
+constexpr int TK_VROW = 129;   // padded row of the value buffer (floats), D <= 128
+
+struct TkWarpBuf {
+  float vals[16 * TK_VROW];
+  uint8_t codes[16 * 128];
+  float2 par[16];
+  int need[16];
+};
+
+template <int D>
+__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const TokState s, int layer) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  __shared__ unsigned hist[4][256];
+  __shared__ unsigned long long pref[4];
+  __shared__ long long need_rank[4];
+  __shared__ int cut_mode[4];   // 0 select, 1 every key is past the cut, 2 no key is
+  __shared__ int scan[4][TK_RERANK_THREADS];
+  __shared__ int s_cnt[4];
+  TkWarpBuf* wb = reinterpret_cast<TkWarpBuf*>(smem);
+  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const TokGeo geo = s.g;
+  const Geo g16{D, 16};
+  const TokLayer hd = s.hdr[layer];
+  const int L = hd.L, nt = hd.n_tail, buf = hd.buf, nb = buf ^ 1;
+  const int4 c4 = *reinterpret_cast<const int4*>(s.cnt + ((long long)layer * s.units + u) * 4);
+  const int cnt[4] = {c4.x, c4.y, c4.z, c4.w};
+  int n_aged = nt - s.n_sink - s.n_recent;
+  if (n_aged < 0) n_aged = 0;
+  const int ncand = cnt[0] + cnt[1] + cnt[2] + cnt[3] + n_aged;
+  const size_t mc = (size_t)s.max_context;
+  unsigned long long* key = s.ckey + u * mc;
+  int* src = s.csrc + u * mc;
+  uint8_t* newt = s.newt + u * mc;
+  int* src_of = s.src_of + u * mc;
+  int* order = s.order + u * 4 * mc;
+  const bool reset = s.score_window > 0;
+  // cut ranks (cumulative), double arithmetic without contraction as the host and oracle do
+  long long cuts[4];
+  {
+    long long acc = 0;
+    for (int z = 0; z < 4; ++z) {
+      long long n = (long long)floor(__dmul_rn(s.frac[z], (double)L));
+      if (z == 0) n -= s.n_sink + s.n_recent;
+      if (n < 0) n = 0;
+      acc += n;
+      cuts[z] = acc;
+    }
+  }
+  // ---- candidates
+  for (int i = tid; i < L; i += TK_RERANK_THREADS) newt[i] = 0xFF;
+  for (int i = tid; i < ncand; i += TK_RERANK_THREADS) {
+    int z = 0, idx = i;
+    while (z < 4 && idx >= cnt[z]) { idx -= cnt[z]; ++z; }
+    int pos;
+    float sc;
+    if (z < 4) {
+      const long long b = tk_pool_tok_index(s, z, layer, buf, u);
+      pos = s.pos[z][b + idx];
+      sc = s.score[z][b + idx];
+    } else {
+      z = TK_TAIL;
+      idx += s.n_sink;
+      const long long b = tk_tail_tok_index(s, layer, buf, u);
+      pos = s.tail_pos[b + idx];
+      sc = s.tail_score[b + idx];
+    }
+    key[i] = ((unsigned long long)(~__float_as_uint(fmaxf(sc, 0.f))) << 32) | (unsigned)pos;
+    src[i] = (z << 28) | idx;
+  }
+  if (tid < 4) {
+    const long long c = cuts[tid];
+    cut_mode[tid] = c <= 0 ? 1 : (c >= ncand ? 2 : 0);
+    pref[tid] = 0ull;
+    need_rank[tid] = c - 1;
+  }
+  __syncthreads();
+  // ---- the key at rank cuts[k] - 1, one radix digit (8 bits) per pass, all cuts at once
+  for (int shift = 56; shift >= 0; shift -= 8) {
+    for (int i = tid; i < 4 * 256; i += TK_RERANK_THREADS) hist[i >> 8][i & 255] = 0;
+    __syncthreads();
+    for (int i = tid; i < ncand; i += TK_RERANK_THREADS) {
+      const unsigned long long kk = key[i];
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        if (cut_mode[c] != 0) continue;
+        const bool match = shift == 56 ? true : ((kk ^ pref[c]) >> (shift + 8)) == 0ull;
+        if (match) atomicAdd(&hist[c][(kk >> shift) & 255u], 1u);
+      }
+    }
+    __syncthreads();
+    if (tid < 4 && cut_mode[tid] == 0) {
+      long long r = need_rank[tid];
+      int d = 0;
+      for (; d < 256; ++d) {
+        const long long h = hist[tid][d];
+        if (r < h) break;
+        r -= h;
+      }
+      if (d > 255) d = 255;
+      pref[tid] |= (unsigned long long)d << shift;
+      need_rank[tid] = r;
+    }
+    __syncthreads();
+  }
+  // ---- new tiers: the rank's tier, never above the current one
+  for (int i = tid; i < ncand; i += TK_RERANK_THREADS) {
+    const unsigned long long kk = key[i];
+    int d = 0;
+#pragma unroll
+    for (int c = 0; c < 4; ++c) d += cut_mode[c] == 1 || (cut_mode[c] == 0 && kk > pref[c]);
+    const int sr = src[i];
+    const int z = sr >> 28;
+    const int old = z == TK_TAIL ? TK_BF16 : z;
+    const int nw = d > old ? d : old;
+    const int pos = (int)(unsigned)kk;
+    if (pos >= 0 && pos < L) {
+      newt[pos] = (uint8_t)nw;
+      src_of[pos] = sr;
+    } else {
+      atomicOr(s.err, ERR_TABLE);
+    }
+  }
+  __syncthreads();
+  // ---- positional order of every kept tier
+  {
+    const int chunk = (L + TK_RERANK_THREADS - 1) / TK_RERANK_THREADS;
+    const int p0 = tid * chunk, p1 = p0 + chunk < L ? p0 + chunk : L;
+    int c[4] = {0, 0, 0, 0};
+    for (int q = p0; q < p1; ++q) {
+      const int z = newt[q];
+      if (z < 4) ++c[z];
+    }
+    for (int z = 0; z < 4; ++z) scan[z][tid] = c[z];
+    __syncthreads();
+    if (tid < 4) {
+      int acc = 0;
+      for (int i = 0; i < TK_RERANK_THREADS; ++i) {
+        const int v = scan[tid][i];
+        scan[tid][i] = acc;
+        acc += v;
+      }
+      s_cnt[tid] = acc;
+      if (acc > s.cap[tid]) atomicOr(s.err, ERR_CAPACITY);
+    }
+    __syncthreads();
+    int o[4] = {scan[0][tid], scan[1][tid], scan[2][tid], scan[3][tid]};
+    for (int q = p0; q < p1; ++q) {
+      const int z = newt[q];
+      if (z < 4) {
+        if (o[z] < s.cap[z]) order[z * mc + o[z]] = q;
+        ++o[z];
+      }
+    }
+  }
+  __syncthreads();
+  int ncnt[4];
+  for (int z = 0; z < 4; ++z) ncnt[z] = s_cnt[z] < s.cap[z] ? s_cnt[z] : s.cap[z];
+  // ---- rebuild the pools of the other buffer, one destination tile per warp at a time
+  const int T0 = (ncnt[0] + 15) >> 4, T1 = (ncnt[1] + 15) >> 4, T2 = (ncnt[2] + 15) >> 4, T3 = (ncnt[3] + 15) >> 4;
+  const int Ttot = T0 + T1 + T2 + T3;
+  TkWarpBuf& W = wb[warp];
+  for (int tt = warp; tt < Ttot; tt += TK_RERANK_WARPS) {
+    int z, kt;
+    if (tt < T0) { z = 0; kt = tt; }
+    else if (tt < T0 + T1) { z = 1; kt = tt - T0; }
+    else if (tt < T0 + T1 + T2) { z = 2; kt = tt - T0 - T1; }
+    else { z = 3; kt = tt - T0 - T1 - T2; }
+    const long long pb = tk_pool_tok_index(s, z, layer, nb, u);
+    uint8_t* dst = s.pool[z] + (tk_pool_tile_index(s, z, layer, nb, u) + kt) * (long long)tk_tile_bytes(s, z);
+    // positions and scores
+    if (lane < 16) {
+      const int idx = 16 * kt + lane;
+      if (idx < ncnt[z]) {
+        const int q = order[z * mc + idx];
+        const int sr = src_of[q];
+        const int sz = sr >> 28, si = sr & 0x0FFFFFFF;
+        float sc = 0.f;
+        if (!reset) {
+          sc = sz == TK_TAIL ? s.tail_score[tk_tail_tok_index(s, layer, buf, u) + si]
+                             : s.score[sz][tk_pool_tok_index(s, sz, layer, buf, u) + si];
+        }
+        s.pos[z][pb + idx] = q;
+        s.score[z][pb + idx] = sc;
+      }
+    }
+    if (z == 0) {
+      // BF16 -> BF16: copy the rows into their new places
+      for (int row = 0; row < 16; ++row) {
+        const int idx = 16 * kt + row;
+        const bool valid = idx < ncnt[0];
+        const uint8_t* st = nullptr;
+        int srow = 0;
+        if (valid) {
+          const int sr = src_of[order[idx]];
+          const int sz = sr >> 28, si = sr & 0x0FFFFFFF;
+          st = tk_src_tile(s, layer, buf, u, sz, si);
+          srow = si & 15;
+        }
+        for (int c = 2 * lane; c < D; c += 64) {
+          unsigned kk = 0u;
+          uint16_t v0 = 0, v1 = 0;
+          if (valid) {
+            kk = *reinterpret_cast<const unsigned*>(st + bf16_k_off(g16, srow, c));
+            v0 = *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c));
+            v1 = *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c + 1));
+          }
+          *reinterpret_cast<unsigned*>(dst + bf16_k_off(g16, row, c)) = kk;
+          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c)) = v0;
+          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c + 1)) = v1;
+        }
+      }
+      __syncwarp();
+      continue;
+    }
+    const int b = tk_bits(z);
+    const float levels = (float)((1 << b) - 1);
+    for (int half = 0; half < 2; ++half) {   // keys, then values
+      const bool value = half == 1;
+      // 1. gather: codes of tokens that keep their tier, values of the others
+      for (int row = 0; row < 16; ++row) {
+        const int idx = 16 * kt + row;
+        int mode = 0;   // 0 empty row, 1 copy codes, 2 quantize values
+        const uint8_t* st = nullptr;
+        int sz = 0, srow = 0;
+        if (idx < ncnt[z]) {
+          const int sr = src_of[order[z * mc + idx]];
+          sz = sr >> 28;
+          const int si = sr & 0x0FFFFFFF;
+          st = tk_src_tile(s, layer, buf, u, sz, si);
+          srow = si & 15;
+          mode = sz == z ? 1 : 2;
+        }
+        if (mode == 1) {
+          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)tk_code_at(geo, st, b, srow, c, value);
+          if (lane == 0)
+            W.par[row] = reinterpret_cast<const float2*>(st + (value ? geo.off_vpar(b) : geo.off_kpar(b)))[srow];
+        } else if (mode == 2) {
+          for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_at(s, st, sz, srow, c, value);
+        } else {
+          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = 0;
+          if (lane == 0) W.par[row] = make_float2(0.f, 0.f);
+        }
+        if (lane == 0) W.need[row] = mode == 2;
+      }
+      __syncwarp();
+      // 2. quantize the rows that need it
+      if (z == TK_NQ1) {
+        // eqs. (3)-(4), b = 1: mean and population std in float64, channel order, one lane per row
+        if (lane < 16 && W.need[lane]) {
+          const float* x = W.vals + lane * TK_VROW;
+          double acc = 0.0;
+          for (int c = 0; c < D; ++c) acc = __dadd_rn(acc, (double)x[c]);
+          const double m = __ddiv_rn(acc, (double)D);
+          double a2 = 0.0;
+          for (int c = 0; c < D; ++c) {
+            const double dl = __dsub_rn((double)x[c], m);
+            a2 = __dadd_rn(a2, __dmul_rn(dl, dl));
+          }
+          const double sd = __dsqrt_rn(__ddiv_rn(a2, (double)D));
+          W.par[lane] = make_float2(__double2float_rn(m), __double2float_rn(sd));
+        }
+        __syncwarp();
+        for (int row = 0; row < 16; ++row) {
+          if (!W.need[row]) continue;
+          const float2 pr = W.par[row];
+          for (int c = lane; c < D; c += 32)
+            W.codes[row * 128 + c] = (uint8_t)(pr.y > 0.f && W.vals[row * TK_VROW + c] > pr.x);
+        }
+      } else {
+        // eq. (2) per token: z = min, s = (max - min) / (2^b - 1) in float32
+        for (int row = 0; row < 16; ++row) {
+          if (!W.need[row]) continue;
+          float mn = INFINITY, mx = -INFINITY;
+          for (int c = lane; c < D; c += 32) {
+            const float x = W.vals[row * TK_VROW + c];
+            mn = fminf(mn, x);
+            mx = fmaxf(mx, x);
+          }
+          for (int o = 16; o; o >>= 1) {
+            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+          }
+          const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
+          for (int c = lane; c < D; c += 32)
+            W.codes[row * 128 + c] = (uint8_t)tk_quant_code(W.vals[row * TK_VROW + c], mn, sc, levels);
+          if (lane == 0) W.par[row] = make_float2(mn, sc);
+        }
+      }
+      __syncwarp();
+      // 3. pack this lane's words and write the block and its parameters
+      {
+        const int wpl = geo.wpl(b), cw = geo.cw(b), per_word = 4 / b;
+        uint8_t* blk = dst + (value ? geo.off_vcode(b) : 0);
+        for (int j = 0; j < wpl; ++j) {
+          unsigned word = 0u;
+          for (int kk = 0; kk < per_word; ++kk) {
+            const int step = j * per_word + kk;
+            for (int r = 0; r < 4; ++r)
+              for (int hf = 0; hf < 2; ++hf) {
+                const int row16 = (lane >> 2) + 8 * (r & 1);
+                const int col16 = ((lane & 3) << 1) + hf + 8 * (r >> 1);
+                const int tok = value ? col16 : row16;
+                const int ch = 16 * step + (value ? row16 : col16);
+                const unsigned code = W.codes[tok * 128 + ch];
+                word |= code << (16 * hf + b * (4 * kk + r));
+              }
+          }
+          *reinterpret_cast<unsigned*>(blk + ((j / cw) * 32 + lane) * (cw * 4) + (j % cw) * 4) = word;
+        }
+        if (lane < 16)
+          reinterpret_cast<float2*>(dst + (value ? geo.off_vpar(b) : geo.off_kpar(b)))[lane] = W.par[lane];
+      }
+      __syncwarp();
+    }
+  }
+  // ---- the new tail: the sink and the recent tokens, moved up over the aged ones
+  {
+    const int ntn = nt - n_aged;
+    const long long ob = tk_tail_tok_index(s, layer, buf, u), nbb = tk_tail_tok_index(s, layer, nb, u);
+    const int tiles = (ntn + 15) >> 4;
+    for (int tt = warp; tt < tiles; tt += TK_RERANK_WARPS) {
+      uint8_t* dst = s.tail + (nbb / 16 + tt) * (long long)geo.bf_tile();
+      for (int row = 0; row < 16; ++row) {
+        const int i = 16 * tt + row;
+        const bool valid = i < ntn;
+        const int si = i < s.n_sink ? i : i + n_aged;
+        const uint8_t* st = s.tail + (ob / 16 + si / 16) * (long long)geo.bf_tile();
+        const int srow = si & 15;
+        for (int c = 2 * lane; c < D; c += 64) {
+          unsigned kk = 0u;
+          uint16_t v0 = 0, v1 = 0;
+          if (valid) {
+            kk = *reinterpret_cast<const unsigned*>(st + bf16_k_off(g16, srow, c));
+            v0 = *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c));
+            v1 = *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c + 1));
+          }
+          *reinterpret_cast<unsigned*>(dst + bf16_k_off(g16, row, c)) = kk;
+          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c)) = v0;
+          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c + 1)) = v1;
+        }
+        if (lane == 0 && valid) {
+          s.tail_pos[nbb + i] = s.tail_pos[ob + si];
+          s.tail_score[nbb + i] = reset ? 0.f : s.tail_score[ob + si];
+        }
+      }
+    }
+  }
+  if (tid == 0) {
+    int4 nc;
+    nc.x = ncnt[0]; nc.y = ncnt[1]; nc.z = ncnt[2]; nc.w = ncnt[3];
+    *reinterpret_cast<int4*>(s.cnt + ((long long)layer * s.units + u) * 4) = nc;
+  }
+}
+
+// After the re-rank of a layer: cost prefix of the new counts and the header switch.
+__global__ void tk_finish_kernel(TokState s, int layer) {
+  __shared__ long long part[256];
+  const int tid = threadIdx.x;
+  const int* cnt = s.cnt + (long long)layer * s.units * 4;
+  long long* cum = s.cum + (long long)layer * (s.units + 1);
+  // each thread sums a contiguous run of units, then a serial prefix over the threads
+  const int per = (s.units + 255) / 256;
+  const int u0 = tid * per, u1 = u0 + per < s.units ? u0 + per : s.units;
+  long long acc = 0;
+  for (int u = u0; u < u1; ++u)
+    for (int z = 0; z < 4; ++z) acc += (long long)s.cost[z] * ((cnt[u * 4 + z] + 15) >> 4);
+  part[tid] = acc;
+  __syncthreads();
+  if (tid == 0) {
+    long long run = 0;
+    for (int i = 0; i < 256; ++i) {
+      const long long v = part[i];
+      part[i] = run;
+      run += v;
+    }
+  }
+  __syncthreads();
+  long long run = part[tid];
+  for (int u = u0; u < u1; ++u) {
+    cum[u] = run;
+    for (int z = 0; z < 4; ++z) run += (long long)s.cost[z] * ((cnt[u * 4 + z] + 15) >> 4);
+  }
+  if (u1 == s.units && u0 < u1) cum[s.units] = run;
+  if (s.units == 0 && tid == 0) cum[0] = 0;
+  __syncthreads();
+  if (tid == 0) {
+    TokLayer& hd = s.hdr[layer];
+    int n_aged = hd.n_tail - s.n_sink - s.n_recent;
+    if (n_aged < 0) n_aged = 0;
+    hd.n_tail -= n_aged;
+    hd.buf ^= 1;
+    hd.step = 0;
+  }
+}
+
+// ------------------------------------------------------------------------------ launchers
+size_t tk_rerank_smem(int D) { return (size_t)TK_RERANK_WARPS * sizeof(TkWarpBuf) + 0 * D; }
+
+template <int D>
+static cudaError_t tk_prepare_t() {
+  constexpr int STAGE = 64 * D;
+  constexpr int NST = TK_STAGE_TOTAL / (TK_WARPS * STAGE) < 4 ? TK_STAGE_TOTAL / (TK_WARPS * STAGE) : 4;
+  cudaError_t e = cudaFuncSetAttribute(tk_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TK_WARPS * NST * STAGE);
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(tk_rerank_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                              (int)tk_rerank_smem(D));
+}
+
+cudaError_t tk_prepare(int D) { return D == 128 ? tk_prepare_t<128>() : tk_prepare_t<64>(); }
+
+int tk_attn_warps() { return TK_WARPS; }
+
+cudaError_t tk_launch_append1(const TokState& s, int layer, const uint16_t* k, const uint16_t* v, cudaStream_t st) {
+  tk_append1_kernel<<<s.units, s.g.D / 2, 0, st>>>(s, layer, k, v);
+  return cudaGetLastError();
+}
+
+cudaError_t tk_launch_append(const TokState& s, int layer, int n, bool prefill, const uint16_t* k, const uint16_t* v,
+                             int n_sm, cudaStream_t st) {
+  const long long total = (long long)s.units * n * (s.g.D / 2);
+  long long blocks = (total + 255) / 256;
+  if (blocks > (long long)n_sm * 16) blocks = (long long)n_sm * 16;
+  if (blocks < 1) blocks = 1;
+  tk_append_kernel<<<(int)blocks, 256, 0, st>>>(s, layer, n, prefill ? 1 : 0, k, v);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  tk_commit_kernel<<<1, 32, 0, st>>>(s, layer, n, prefill ? 1 : 0);
+  return cudaGetLastError();
+}
+
+__global__ void tk_commit_pending_kernel(TokState s, int layer, int pend) {
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    s.hdr[layer].L += pend;
+    s.hdr[layer].n_tail += pend;
+  }
+}
+
+cudaError_t tk_launch_commit_pending(const TokState& s, int layer, int pend, cudaStream_t st) {
+  tk_commit_pending_kernel<<<1, 32, 0, st>>>(s, layer, pend);
+  return cudaGetLastError();
+}
+
+cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* q, float scale_log2, float* part_o,
+                           float2* part_ml, float* logits, int lg_cap, int grid, cudaStream_t st) {
+  const int D = s.g.D;
+  TkAttnArgs a;
+  a.st = s;
+  a.layer = layer;
+  a.pend = pend;
+  a.q = q;
+  a.scale_log2 = scale_log2;
+  a.part_o = part_o;
+  a.part_ml = part_ml;
+  a.logits = logits;
+  a.lg_cap = lg_cap;
+  const int stage = 64 * D;
+  const int nst = TK_STAGE_TOTAL / (TK_WARPS * stage) < 4 ? TK_STAGE_TOTAL / (TK_WARPS * stage) : 4;
+  if (D == 128) tk_attn_kernel<128><<<grid, TK_WARPS * 32, TK_WARPS * nst * stage, st>>>(a);
+  else tk_attn_kernel<64><<<grid, TK_WARPS * 32, TK_WARPS * nst * stage, st>>>(a);
+  return cudaGetLastError();
+}
+
+// programmatic dependent of the attention launch before it on the stream
+cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float* part_o, const float2* part_ml,
+                            const float* logits, int lg_cap, int grid, void* out, int out_fp32, cudaStream_t st) {
+  TkMergeArgs m;
+  m.st = s;
+  m.layer = layer;
+  m.pend = pend;
+  m.NW = grid * TK_WARPS;
+  m.part_o = part_o;
+  m.part_ml = part_ml;
+  m.logits = logits;
+  m.lg_cap = lg_cap;
+  m.out = out;
+  m.out_fp32 = out_fp32;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(s.units);
+  cfg.blockDim = dim3(TK_MERGE_THREADS);
+  cfg.dynamicSmemBytes = (size_t)s.G * (m.NW + 2) * sizeof(float);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (s.g.D == 128) return cudaLaunchKernelEx(&cfg, tk_merge_kernel<128>, m);
+  return cudaLaunchKernelEx(&cfg, tk_merge_kernel<64>, m);
+}
+
+cudaError_t tk_launch_rerank(const TokState& s, int layer, cudaStream_t st) {
+  const size_t sm = tk_rerank_smem(s.g.D);
+  if (s.g.D == 128) tk_rerank_kernel<128><<<s.units, TK_RERANK_THREADS, sm, st>>>(s, layer);
+  else tk_rerank_kernel<64><<<s.units, TK_RERANK_THREADS, sm, st>>>(s, layer);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  tk_finish_kernel<<<1, 256, 0, st>>>(s, layer);
+  return cudaGetLastError();
+}
+
+}  // namespace qe
