@@ -64,12 +64,17 @@ def whole_job_rate(tokens_per_rank: float, world: int, ms: float) -> float:
 
 def workload_config(wl, world: int) -> dict:
     """The `config` object of the JSON line (shared by both arms)."""
-    return {
+    c = {
         "workload": wl.name, "batch": wl.batch, "context": wl.prefill, "layers": wl.n_layers,
         "q_heads": wl.n_q_heads, "kv_heads": wl.n_kv_heads, "head_dim": wl.head_dim, "window": wl.window,
         "route_period": wl.route_period, "bf16_token_share": wl.frac_bf16, "int2_token_share": wl.frac_int2,
         "n_sink": wl.n_sink, "n_recent": wl.n_recent, "parallelism": f"replicas{world}",
     }
+    if getattr(wl, "tiering", "windows") == "tokens":
+        del c["window"]
+        c.update({"tiering": "per-token five tiers", "int4_token_share": wl.frac_int4,
+                  "nq1_token_share": wl.frac_nq1, "score_window": wl.score_window})
+    return c
 
 
 # ---------------------------------------------------------------------------- clocks
@@ -211,6 +216,7 @@ def run_ours(args):
     timed = [make_inputs(t + 1 + i) for i in range(K)]
     torch.cuda.synchronize(dev)
     n_routes = 0
+    launches_before = cache.kernel_launches()
     g_all = torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_all, stream=stream, capture_error_mode="thread_local"):
         for i in range(K):
@@ -222,7 +228,7 @@ def run_ours(args):
             if tt % omega == 0:
                 cache.qe_route(-1)
                 n_routes += 1
-    launches_per_step = 2 * Lyr                    # attention (with the append) and combine per layer
+    graph_launches = cache.kernel_launches() - launches_before   # kernels the graph holds
     clocks = ClockSampler(local)
     clocks.start()
     time.sleep(0.3)
@@ -240,7 +246,7 @@ def run_ours(args):
         dist.barrier()
     clk = clocks.stop()
     ms_total = e0.elapsed_time(e1)
-    launches = K * launches_per_step + n_routes * 2 * Lyr
+    launches = graph_launches
     cache.qe_synchronize()
     cache.qe_layer_info_sync()
     del timed
@@ -295,6 +301,13 @@ def run_ours(args):
     peak, peak_kind = _peaks()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
     info = cache.layer_info(0)
+    tok = getattr(wl, "tiering", "windows") == "tokens"
+    if tok:
+        cnt = cache.token_counts(0).mean(axis=0)
+        kv_unit = {"bf16_ranked": round(float(cnt[0]), 1), "int4": round(float(cnt[1]), 1),
+                   "int2": round(float(cnt[2]), 1), "nq1": round(float(cnt[3]), 1), "bf16_tail": round(float(cnt[4]), 1)}
+    else:
+        kv_unit = {"full": info.n_full, "quant": info.n_quant, "pinned": info.n_pinned}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "tokens/s", "n_gpus": world, "steps": K,
         "warmup": W, "ms_per_step": round(ms_total / K, 4), "higher_is_better": True, "scaling": "weak",
@@ -302,15 +315,18 @@ def run_ours(args):
         "config": {
             **workload_config(wl, world),
             "timed_decode_steps": [omega + W + 1, omega + W + K],
-            "launch": "the K timed steps as one CUDA graph (per step %d layers x attention with the token "
-                      "append, combine; routing every Omega)" % Lyr,
-            "kv_per_layer_unit": {"full": info.n_full, "quant": info.n_quant, "pinned": info.n_pinned},
-            "l2": "inputs larger than L2: %.0f MB read per layer launch, %.1f GB per step" % (
-                info.attn_bytes / 1e6, info.attn_bytes * Lyr / 1e9),
-            "kv_dtypes": "bf16 tiles + 2-bit codes (fp32 min/scale); fp32 accumulate",
+            "launch": ("the K timed steps as one CUDA graph (per step %d layers x token append, attention, merge; "
+                       "re-rank every Omega)" % Lyr) if tok else
+                      ("the K timed steps as one CUDA graph (per step %d layers x attention with the token "
+                       "append, combine; routing every Omega)" % Lyr),
+            ("kv_tokens_per_layer_unit" if tok else "kv_per_layer_unit"): kv_unit,
+            "l2": "inputs larger than L2: %.0f MB read per layer launch, %.1f GB per step (a layer's data is "
+                  "read again only after the other layers' data)" % (info.attn_bytes / 1e6, info.attn_bytes * Lyr / 1e9),
+            "kv_dtypes": ("bf16 + per-token 4/2-bit uniform and 1-bit normal codes (fp32 params); fp32 accumulate"
+                          if tok else "bf16 tiles + 2-bit codes (fp32 min/scale); fp32 accumulate"),
         },
         "roofline": {
-            "bound": "hbm", "kernel": "qe_decode_attn", "achieved": round(achieved, 1) if achieved else None,
+            "bound": "hbm", "kernel": "tk_attn" if tok else "qe_decode_attn", "achieved": round(achieved, 1) if achieved else None,
             "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4) if achieved else None,
             "traffic": _traffic(wl.name),
@@ -342,17 +358,18 @@ def _oracle_worker(a):
     wl = gen.WORKLOADS[name]
     unit = make_unit(wl, max_context=wl.prefill + first_step + n_steps + 1)
     prefill(wl, unit, b, layer, kvh)
+    routes = hasattr(unit, "route")          # window tiers route explicitly; token tiers re-rank in the step
     for t in range(1, first_step):
         q, k, v = step_inputs(wl, b, layer, kvh, t)
         unit.decode_step(q, k, v)
-        if t % wl.route_period == 0:
+        if routes and t % wl.route_period == 0:
             unit.route()
     times = []
     for t in range(first_step, first_step + n_steps):
         q, k, v = step_inputs(wl, b, layer, kvh, t)
         t0 = time.perf_counter()
         unit.decode_step(q, k, v)
-        if t % wl.route_period == 0:
+        if routes and t % wl.route_period == 0:
             unit.route()
         times.append(time.perf_counter() - t0)
     return times

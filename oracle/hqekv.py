@@ -31,8 +31,11 @@ Readings where the pages leave a step open
   Phi^-1((j + 1) / 2^b), where the two probability masses are equal, and a
   value on a boundary takes the lower center.  For b = 1 the centers are
   +-0.6745 and the boundary is 0: the code is 1 exactly when x > m.
-* Mean and population standard deviation are accumulated in float64 in channel
-  order (two passes), then stored as float32; s = 0 gives all-zero codes.
+* Mean and population standard deviation are computed in float32 (the precision the
+  pages leave open; the CUDA path decides codes in it): two passes, each sum in one
+  fixed order (per-lane partials over channels l, l + 32, ..., then a pairwise
+  butterfly over the 32 partials), every operation rounded once; s = 0 gives all-zero
+  codes.
 * Uniform decisions are eq. (2) in float32 as in ``oracle.quant``.
 * Dequantization is one float32 fused multiply-add, code * s + z (uniform) or
   c_j * s + m (normal); re-quantization to a lower tier starts from those
@@ -143,26 +146,36 @@ def normal_boundaries(bits: int) -> np.ndarray:
     return _symmetric([(j + 1) / n for j in range(n - 1)])
 
 
-def mean_std_f64(x):
-    """Per-row mean and population std of x [n, D] (float32), float64 sums in channel order."""
-    x = np.asarray(x, np.float32).astype(np.float64)
+def _lane_sum(x):
+    """float32 sum of each row of x [n, D] (D a multiple of 32) in a fixed order: partial j of
+    32 is x[j] + x[j + 32] + ... left to right, then the partials are combined pairwise, each
+    partial j with partial j xor o for o = 16, 8, 4, 2, 1 (every step one float32 add)."""
+    x = np.asarray(x, np.float32)
     n, D = x.shape
-    acc = np.zeros(n, np.float64)
-    for c in range(D):
-        acc = acc + x[:, c]
-    m = acc / D
-    acc2 = np.zeros(n, np.float64)
-    for c in range(D):
-        dlt = x[:, c] - m
-        acc2 = acc2 + dlt * dlt
-    return m, np.sqrt(acc2 / D)
+    a = x[:, 0:32].copy()
+    for k in range(1, D // 32):
+        a = (a + x[:, 32 * k:32 * (k + 1)]).astype(np.float32)
+    lanes = np.arange(32)
+    for o in (16, 8, 4, 2, 1):
+        a = (a + a[:, lanes ^ o]).astype(np.float32)
+    return a[:, 0]
+
+
+def mean_std_f32(x):
+    """Per-row mean and population std of x [n, D] (float32) in float32: m = sum / D,
+    s = sqrt(sum((x - m)^2) / D), the sums in the order of ``_lane_sum``, every operation
+    rounded once (no fused multiply-add)."""
+    x = np.asarray(x, np.float32)
+    n, D = x.shape
+    m = (_lane_sum(x) / np.float32(D)).astype(np.float32)
+    d = (x - m[:, None]).astype(np.float32)
+    q = _lane_sum((d * d).astype(np.float32))
+    return m, np.sqrt((q / np.float32(D)).astype(np.float32)).astype(np.float32)
 
 
 def normal_quantize(x, bits: int = 1):
     """eqs. (3)-(4) per row of x [n, D] (float32): (codes uint8 [n, D], m float32 [n], s float32 [n])."""
-    m64, s64 = mean_std_f64(x)
-    m = m64.astype(F32)
-    s = s64.astype(F32)
+    m, s = mean_std_f32(x)
     x = np.asarray(x, np.float32).astype(np.float64)
     safe = np.where(s == 0, 1.0, s.astype(np.float64))
     xp = (x - m.astype(np.float64)[:, None]) / safe[:, None]          # eq. (3)

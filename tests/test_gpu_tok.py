@@ -156,3 +156,141 @@ def test_five_tier_trajectory(name):
           f"bf16 {run.bf16_checked}, counts unit 0 {counts[0].tolist()}")
     assert run.codes_checked > 0
     assert (counts[:, 1:4] > 0).all()
+
+
+def test_hqe_16k_sampled_units_graph_replay():
+    """The 16K five-tier workload at full size (32 layers, batch 8, GQA 32q/8kv, d 128, 16,384-token
+    prefill, re-rank every 64 steps over the last 20 steps' attention), in the benchmark's launch
+    configuration: direct calls through the first re-rank, then one decode step of the whole stack
+    captured as a CUDA graph (plus the variant that ends with the re-rank) and replayed with fresh
+    inputs.  Three sampled units follow the oracle: outputs every step, scores, tiers, codes and
+    parameters at both re-ranks."""
+    import torch
+    import qe_inputs.cuda as gc
+    import tiered_quantize_evict_gb300 as qe
+    wl = gen.WORKLOADS["hqe_16k"]
+    dev = torch.device("cuda:0")
+    stream = torch.cuda.Stream(dev)
+    torch.cuda.set_stream(stream)
+    cache = qe.QECache(qe.config_from_workload(wl), stream.cuda_stream)
+    g = gc.DeviceGenerator(wl, device=dev)
+    Lyr, B, D, Hq, Hkv = wl.n_layers, wl.batch, wl.head_dim, wl.n_q_heads, wl.n_kv_heads
+    sampled = [(0, 0, 0), (3, 17, 5), (7, 31, 7)]
+    units = {s: make_unit(wl) for s in sampled}
+    kbuf = torch.empty(B, Hkv, wl.prefill, D, device=dev, dtype=torch.int16)
+    vbuf = torch.empty_like(kbuf)
+    for layer in range(Lyr):
+        g.keys_values(layer, 0, wl.prefill, kbuf, vbuf, stream.cuda_stream)
+        cache.qe_append(layer, kbuf, vbuf, wl.prefill)
+    del kbuf, vbuf
+    for (b, layer, h), un in units.items():
+        kb, vb = gen.gen_keys_values(wl, b, layer, h, 0, wl.prefill)
+        un.append(gen.bf16_bits_to_f32(kb), gen.bf16_bits_to_f32(vb))
+    kin = torch.empty(Lyr, B, Hkv, 1, D, device=dev, dtype=torch.int16)
+    vin = torch.empty_like(kin)
+    qin = torch.empty(Lyr, B, Hq, D, device=dev, dtype=torch.int16)
+    out = torch.empty(Lyr, B, Hq, D, device=dev, dtype=torch.float32)
+    stats = {"out": 0.0, "score": 0.0, "codes": 0}
+
+    def inputs(t):
+        for layer in range(Lyr):
+            g.keys_values(layer, wl.prefill + t - 1, 1, kin[layer], vin[layer], stream.cuda_stream)
+            g.queries(layer, t, qin[layer], stream.cuda_stream)
+
+    def compare(t):
+        got = out.cpu().numpy().astype(np.float64)
+        for (b, layer, h), un in units.items():
+            heads = range(h * wl.group, (h + 1) * wl.group)
+            q = gen.bf16_bits_to_f32(gen.gen_queries(wl, b, layer, heads, t))
+            kb, vb = gen.gen_keys_values(wl, b, layer, h, wl.prefill + t - 1, 1)
+            o, _ = un.decode_step(q, gen.bf16_bits_to_f32(kb), gen.bf16_bits_to_f32(vb), auto_rerank=False)
+            for i, hq in enumerate(heads):
+                err = np.linalg.norm(got[layer, b, hq] - o[i]) / np.linalg.norm(o[i])
+                stats["out"] = max(stats["out"], err)
+                assert err <= OUT_TOL, f"step {t} unit {(b, layer, h)} head {hq}: rel-L2 {err:.2e}"
+
+    def scores_then_rerank(t, gpu_routed):
+        for (b, layer, h), un in units.items():
+            u = b * Hkv + h
+            S = cache.token_scores(layer)[u]
+            live = (un.tier[:un.L] != H.EVICT) & (np.arange(un.L) >= wl.n_sink)
+            ref = un.S[:un.L][live].astype(np.float64)
+            err = np.abs(S[:un.L][live] - ref)
+            assert np.all(err <= SCORE_RTOL * ref + SCORE_ATOL), f"t {t} unit {(b, layer, h)}: score {err.max():.2e}"
+            stats["score"] = max(stats["score"], float(np.max(err / np.maximum(ref, 1e-30))))
+            un.S[:un.L] = np.where(np.arange(un.L) < wl.n_sink, 0, S[:un.L])
+        if not gpu_routed:
+            cache.qe_route(-1)
+        for un in units.values():
+            un.rerank()
+        for (b, layer, h), un in units.items():
+            u = b * Hkv + h
+            tiers = cache.token_tiers(layer)[u]
+            assert np.array_equal(tiers[:un.L], un.tier[:un.L]), f"t {t} unit {(b, layer, h)}: tiers"
+            quant = [p for p in range(un.L) if un.tier[p] in (H.INT4, H.INT2, H.NQ1)]
+            for p in quant[::37]:   # every 37th quantized token
+                tier, _, _, kc, vc, par = cache.token(layer, u, p)
+                tc = un.codes[p]
+                assert tier == tc.tier and np.array_equal(kc, tc.k_codes) and np.array_equal(vc, tc.v_codes), \
+                    f"t {t} unit {(b, layer, h)} pos {p}: codes"
+                ref_par = np.array([tc.k_p0, tc.k_p1, tc.v_p0, tc.v_p1], np.float32)
+                assert np.array_equal(par.view(np.uint32), ref_par.view(np.uint32)), f"pos {p}: params"
+                stats["codes"] += 1
+
+    omega = wl.route_period
+    for t in range(1, omega + 1):            # direct calls through the first re-rank
+        inputs(t)
+        for layer in range(Lyr):
+            cache.qe_append(layer, kin[layer], vin[layer], 1)
+            cache.qe_decode_step(layer, qin[layer], out[layer])
+        torch.cuda.synchronize(dev)
+        compare(t)
+        if t == omega:
+            scores_then_rerank(t, gpu_routed=False)
+    # one decode step of the stack and one re-rank of every layer, each captured once
+    g_step, g_route = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_step, stream=stream, capture_error_mode="thread_local"):
+        for layer in range(Lyr):
+            cache.qe_append(layer, kin[layer], vin[layer], 1)
+            cache.qe_decode_step(layer, qin[layer], out[layer])
+    with torch.cuda.graph(g_route, stream=stream, capture_error_mode="thread_local"):
+        cache.qe_route(-1)
+    for t in range(omega + 1, 2 * omega + 1):   # graph replays through the second re-rank
+        inputs(t)
+        g_step.replay()
+        torch.cuda.synchronize(dev)
+        compare(t)
+        if t % omega == 0:
+            cache.qe_layer_info_sync()
+            g_route_run = lambda: g_route.replay()
+            # scores before the re-rank go to the oracle, then the captured re-rank runs
+            for (b, layer, h), un in units.items():
+                u = b * Hkv + h
+                S = cache.token_scores(layer)[u]
+                live = (un.tier[:un.L] != H.EVICT) & (np.arange(un.L) >= wl.n_sink)
+                ref = un.S[:un.L][live].astype(np.float64)
+                err = np.abs(S[:un.L][live] - ref)
+                assert np.all(err <= SCORE_RTOL * ref + SCORE_ATOL), f"t {t}: score {err.max():.2e}"
+                stats["score"] = max(stats["score"], float(np.max(err / np.maximum(ref, 1e-30))))
+                un.S[:un.L] = np.where(np.arange(un.L) < wl.n_sink, 0, S[:un.L])
+            g_route_run()
+            torch.cuda.synchronize(dev)
+            cache.qe_layer_info_sync()
+            for un in units.values():
+                un.rerank()
+            for (b, layer, h), un in units.items():
+                u = b * Hkv + h
+                tiers = cache.token_tiers(layer)[u]
+                assert np.array_equal(tiers[:un.L], un.tier[:un.L]), f"t {t} unit {(b, layer, h)}: tiers"
+                quant = [p for p in range(un.L) if un.tier[p] in (H.INT4, H.INT2, H.NQ1)]
+                for p in quant[::37]:
+                    tier, _, _, kc, vc, par = cache.token(layer, u, p)
+                    tc = un.codes[p]
+                    assert tier == tc.tier and np.array_equal(kc, tc.k_codes) and np.array_equal(vc, tc.v_codes)
+                    ref_par = np.array([tc.k_p0, tc.k_p1, tc.v_p0, tc.v_p1], np.float32)
+                    assert np.array_equal(par.view(np.uint32), ref_par.view(np.uint32))
+                    stats["codes"] += 1
+    cache.qe_synchronize()
+    print(f"hqe_16k: max out rel-L2 {stats['out']:.2e}, max score rel {stats['score']:.2e}, codes {stats['codes']}, "
+          f"counts layer 0 unit 0 {cache.token_counts(0)[0].tolist()}")
+    assert stats["codes"] > 0

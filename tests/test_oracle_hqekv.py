@@ -81,11 +81,27 @@ def test_one_bit_code_is_the_sign_against_the_mean():
 
 def test_mean_std_match_the_closed_form():
     rng = np.random.default_rng(5)
-    x = (rng.standard_normal((50, 128)) * 3 + 1).astype(np.float32)
-    m, s = H.mean_std_f64(x)
-    xd = x.astype(np.float64)
-    assert np.allclose(m, xd.mean(axis=1), rtol=1e-14, atol=1e-15)
-    assert np.allclose(s, xd.std(axis=1), rtol=1e-13)
+    for D in (64, 128):
+        x = (rng.standard_normal((50, D)) * 3 + 1).astype(np.float32)
+        m, s = H.mean_std_f32(x)
+        xd = x.astype(np.float64)
+        assert m.dtype == np.float32 and s.dtype == np.float32
+        assert np.allclose(m, xd.mean(axis=1), rtol=1e-6, atol=1e-6)
+        assert np.allclose(s, xd.std(axis=1), rtol=1e-6)
+
+
+def test_mean_std_exact_when_every_step_is_exact():
+    # integer rows with a sum divisible by D: every add, the division by D, x - m and (x - m)^2
+    # are exact in float32, so m and the variance are exact and s is the rounded square root
+    rng = np.random.default_rng(11)
+    for D in (64, 128):
+        x = rng.integers(-100, 101, (40, D)).astype(np.int64)
+        x[:, -1] -= x.sum(axis=1) % D          # sum divisible by D (the last value moves a little)
+        m, s = H.mean_std_f32(x.astype(np.float32))
+        me = x.sum(axis=1) // D
+        var = ((x - me[:, None]) ** 2).sum(axis=1) / D
+        assert np.array_equal(m, me.astype(np.float32))
+        assert np.array_equal(s, np.sqrt(var).astype(np.float32))
 
 
 def test_fmaf32_rounds_once():
@@ -197,5 +213,5 @@ def test_requantization_starts_from_the_current_codes():
     # the chain keeps min and max of the 4-bit reconstruction: min exactly, codes mostly agree
     assert via.k_p0 == q4.k_p0 and np.mean(via.k_codes == direct.k_codes) > 0.8
     k1, _ = H.dequantize_token(H.quantize_token(H.NQ1, k4, v4))
-    m, s = H.mean_std_f64(k4[None, :])
+    m, s = H.mean_std_f32(k4[None, :])
     assert set(np.round((k1.astype(np.float64) - m[0]) / s[0], 4)) <= {-0.6745, 0.6745}

@@ -34,7 +34,7 @@ constexpr int TK_STAGE_TOTAL = 196608;
 constexpr unsigned long long TK_WAIT_NS = 200000000ull;   // 0.2 s
 constexpr float TK_NQ1_C = 0.67448975f;                   // Phi^-1(3/4) rounded to float32
 constexpr int TK_MERGE_THREADS = 512;
-constexpr int TK_RERANK_THREADS = 512;
+constexpr int TK_RERANK_THREADS = 256;
 constexpr int TK_RERANK_WARPS = TK_RERANK_THREADS / 32;
 
 // ------------------------------------------------------------------------------ unit geometry
@@ -191,8 +191,20 @@ __device__ __forceinline__ float2 tk_affine(float2 p, bool normal) {
 }
 
 struct TkDesc {
-  int u, kind, nvalid, tokslot;
+  int u, kind;
+  int ntile;       // tiles in this stage (consecutive tiles of one segment)
+  int rem;         // tokens of the segment from the stage's first tile on
+  int tokslot;     // token slot of the first tile
+  int pad[3];
 };
+
+// Tiles one stage carries: a BF16 tile fills it; quantized tiles of a segment are staged
+// together (up to 64 d bytes), so every stage moves about as many bytes.
+template <int D>
+__device__ __forceinline__ int tk_per_stage(int z) {
+  if (z == 0 || z == 4) return 1;
+  return (64 * D) / (4 * D * tk_bits(z) + 256);
+}
 
 struct TkAttnArgs {
   TokState st;
@@ -325,20 +337,24 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   long long ux = tk_X(cum, cu, tail_cost);
   int cz = 0, ck = 0;
   bool cvalid = true;
+  // the cursor walks stages: stage k of segment z holds tiles [k pc, (k + 1) pc) (pc tiles per
+  // stage) and starts at cost s0[z] + k pc cost[z]
+  auto nstages = [&](int z) -> int { const int pc = tk_per_stage<D>(z); return (un.t[z] + pc - 1) / pc; };
   {
-    // first tile whose start >= x_lo
+    // first stage whose start >= x_lo
     const long long r = x_lo - ux;
     cz = 5;
     for (int z = 0; z < 5; ++z) {
       if (un.t[z] == 0) continue;
-      const long long last = un.s0[z] + (long long)(un.t[z] - 1) * S.cost[z];
+      const long long step = (long long)tk_per_stage<D>(z) * S.cost[z];
+      const long long last = un.s0[z] + (long long)(nstages(z) - 1) * step;
       if (r <= last) {
         cz = z;
-        ck = r <= un.s0[z] ? 0 : (int)((r - un.s0[z] + S.cost[z] - 1) / S.cost[z]);
+        ck = r <= un.s0[z] ? 0 : (int)((r - un.s0[z] + step - 1) / step);
         break;
       }
     }
-    if (cz == 5) {   // past the unit's last tile start: the next unit's first tile
+    if (cz == 5) {   // past the unit's last stage start: the next unit's first stage
       ++cu;
       if (cu >= S.units) cvalid = false;
       else {
@@ -352,7 +368,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   }
   auto advance = [&]() {
     ++ck;
-    if (ck < un.t[cz]) return;
+    if (ck < nstages(cz)) return;
     ck = 0;
     ++cz;
     while (cz < 5 && un.t[cz] == 0) ++cz;
@@ -369,21 +385,24 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   };
   auto issue_next = [&](int stage) -> bool {
     if (!cvalid || cz >= 5) return false;
-    const long long start = ux + un.s0[cz] + (long long)ck * S.cost[cz];
+    const int pc = tk_per_stage<D>(cz);
+    const long long start = ux + un.s0[cz] + (long long)ck * pc * S.cost[cz];
     if (start >= x_hi) return false;
     if (lane == 0) {
       const int kind = cz;
-      const unsigned bytes = (unsigned)tk_tile_bytes(S, kind == 4 ? TK_TAIL : kind);
+      const int t0 = ck * pc;
+      const int nt = un.t[cz] - t0 < pc ? un.t[cz] - t0 : pc;
+      const unsigned bytes = (unsigned)(nt * tk_tile_bytes(S, kind == 4 ? TK_TAIL : kind));
       TkDesc d;
       d.u = cu;
       d.kind = kind;
-      const int rem = un.n[cz] - 16 * ck;
-      d.nvalid = rem < 16 ? rem : 16;
-      d.tokslot = un.tok0[cz] + 16 * ck;
+      d.ntile = nt;
+      d.rem = un.n[cz] - 16 * t0;
+      d.tokslot = un.tok0[cz] + 16 * t0;
       descs[warp][stage] = d;
       const unsigned bar = smem_u32(&bars[warp][stage]);
       mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_u32(stage_base + (size_t)stage * STAGE), tk_tile_src(S, p.layer, buf, cu, kind, ck), bytes, bar);
+      bulk_g2s(smem_u32(stage_base + (size_t)stage * STAGE), tk_tile_src(S, p.layer, buf, cu, kind, t0), bytes, bar);
     }
     advance();
     return true;
@@ -475,12 +494,27 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
       qsum = __shfl_sync(0xffffffffu, part, 8 * t);   // sum of q over the channels, head t
     }
     float* lg = scoring ? p.logits + ((long long)d.u * p.lg_cap + d.tokslot) * G : nullptr;
+    const int nv0 = d.rem < 16 ? d.rem : 16;
     switch (d.kind) {
       case 0:
-      case 4: tk_tile_bf16<D>(sp, d.nvalid, qb, rs, lg, p.scale_log2, G, lane); break;
-      case 1: tk_tile_q<D, 4>(sp, d.nvalid, false, qb, qsum, rs, lg, p.scale_log2, G, lane); break;
-      case 2: tk_tile_q<D, 2>(sp, d.nvalid, false, qb, qsum, rs, lg, p.scale_log2, G, lane); break;
-      default: tk_tile_q<D, 1>(sp, d.nvalid, true, qb, qsum, rs, lg, p.scale_log2, G, lane); break;
+      case 4: tk_tile_bf16<D>(sp, nv0, qb, rs, lg, p.scale_log2, G, lane); break;
+      case 1:
+      case 2:
+      case 3: {
+        const int b = tk_bits(d.kind);
+        const int tb = 4 * D * b + 256;
+        for (int i = 0; i < d.ntile; ++i) {
+          const int r = d.rem - 16 * i;
+          const int nv = r < 16 ? r : 16;
+          const uint8_t* ti = sp + i * tb;
+          float* lgi = lg ? lg + 16 * i * G : nullptr;
+          if (d.kind == 1) tk_tile_q<D, 4>(ti, nv, false, qb, qsum, rs, lgi, p.scale_log2, G, lane);
+          else if (d.kind == 2) tk_tile_q<D, 2>(ti, nv, false, qb, qsum, rs, lgi, p.scale_log2, G, lane);
+          else tk_tile_q<D, 1>(ti, nv, true, qb, qsum, rs, lgi, p.scale_log2, G, lane);
+        }
+        break;
+      }
+      default: break;
     }
     __syncwarp();
     if (issue_next(s)) ++issued;
@@ -656,9 +690,16 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
   for (int e = tid; e < G * D; e += TK_MERGE_THREADS) {
     const int h = e / D, c = e - h * D;
     float acc = 0.f;
-    for (int k = 0; k < np; ++k) {
-      const float sc = s_sc[h * np + k];
-      if (sc != 0.f) acc = fmaf(p.part_o[((slot0 + k) * G + h) * D + c], sc, acc);
+    for (int k0 = 0; k0 < np; k0 += 16) {   // 16 partial loads in flight
+      float v[16];
+#pragma unroll
+      for (int j = 0; j < 16; ++j) {
+        const int k = k0 + j;
+        v[j] = (k < np && s_sc[h * np + k] != 0.f) ? __ldg(p.part_o + ((slot0 + k) * G + h) * D + c) : 0.f;
+      }
+#pragma unroll
+      for (int j = 0; j < 16; ++j)
+        if (k0 + j < np) acc = fmaf(v[j], s_sc[h * np + k0 + j], acc);
     }
     const float o = acc * s_inv[h];
     const int bb = u / S.Hkv, kvh = u - bb * S.Hkv;
@@ -673,11 +714,24 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
       if (z < 4) sc = S.score[z] + tk_pool_tok_index(S, z, p.layer, hd.buf, u);
       else sc = S.tail_score + tk_tail_tok_index(S, p.layer, hd.buf, u);
       const int first = z < 4 ? 0 : S.n_sink;   // sink tokens are never scored
-      for (int i = first + tid; i < un.n[z]; i += TK_MERGE_THREADS) {
-        const float* lg = lgu + (long long)(un.tok0[z] + i) * G;
-        float m = 0.f;
-        for (int h = 0; h < G; ++h) m += ex2(lg[h] - s_lse[h]);
-        sc[i] += m;
+      for (int i0 = first + tid; i0 < un.n[z]; i0 += 4 * TK_MERGE_THREADS) {   // 4 tokens in flight
+        float m[4], old[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * TK_MERGE_THREADS;
+          m[j] = 0.f;
+          old[j] = 0.f;
+          if (i < un.n[z]) {
+            const float* lg = lgu + (long long)(un.tok0[z] + i) * G;
+            for (int h = 0; h < G; ++h) m[j] += ex2(__ldg(lg + h) - s_lse[h]);
+            old[j] = sc[i];
+          }
+        }
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int i = i0 + j * TK_MERGE_THREADS;
+          if (i < un.n[z]) sc[i] = old[j] + m[j];
+        }
       }
     }
   }
@@ -740,10 +794,13 @@ __device__ __forceinline__ unsigned tk_quant_code(float x, float z, float s, flo
 constexpr int TK_VROW = 129;   // padded row of the value buffer (floats), D <= 128
 
 struct TkWarpBuf {
+  uint8_t src[8192];     // the source tile last read (a BF16 tile of d = 128 is the largest)
   float vals[16 * TK_VROW];
   uint8_t codes[16 * 128];
   float2 par[16];
   int need[16];
+  int src_id;            // (pool or tail) << 28 | tile index of src, -1 for none
+  int pad[3];
 };
 
 template <int D>
@@ -755,12 +812,9 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
   __shared__ int cut_mode[4];   // 0 select, 1 every key is past the cut, 2 no key is
   __shared__ int scan[4][TK_RERANK_THREADS];
   __shared__ int s_cnt[4];
-  TkWarpBuf* wb = reinterpret_cast<TkWarpBuf*>(smem);
-  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const TokGeo geo = s.g;
-  const Geo g16{D, 16};
+  const int u = blockIdx.x, tid = threadIdx.x;
   const TokLayer hd = s.hdr[layer];
-  const int L = hd.L, nt = hd.n_tail, buf = hd.buf, nb = buf ^ 1;
+  const int L = hd.L, nt = hd.n_tail, buf = hd.buf;
   const int4 c4 = *reinterpret_cast<const int4*>(s.cnt + ((long long)layer * s.units + u) * 4);
   const int cnt[4] = {c4.x, c4.y, c4.z, c4.w};
   int n_aged = nt - s.n_sink - s.n_recent;
@@ -772,7 +826,6 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
   uint8_t* newt = s.newt + u * mc;
   int* src_of = s.src_of + u * mc;
   int* order = s.order + u * 4 * mc;
-  const bool reset = s.score_window > 0;
   // cut ranks (cumulative), double arithmetic without contraction as the host and oracle do
   long long cuts[4];
   {
@@ -892,13 +945,55 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
     }
   }
   __syncthreads();
+  if (tid < 4) s.ncnt[u * 4 + tid] = s_cnt[tid] < s.cap[tid] ? s_cnt[tid] : s.cap[tid];
+}
+
+// Rebuild of one unit's pools and tail in the other buffer after tk_rerank_kernel chose the new
+// tiers: TK_REBUILD_SPLIT CTAs per unit share its destination tiles, one tile per warp at a time.
+// A destination tile's rows (position order) come from few source tiles: the warp stages each
+// distinct source tile once in shared memory and serves every row that reads from it.
+constexpr int TK_REBUILD_SPLIT = 4;
+
+template <int D>
+__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const TokState s, int layer) {
+  extern __shared__ __align__(1024) uint8_t smem[];
+  TkWarpBuf* wb = reinterpret_cast<TkWarpBuf*>(smem);
+  const int u = blockIdx.x / TK_REBUILD_SPLIT, part = blockIdx.x - u * TK_REBUILD_SPLIT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int wall = part * TK_RERANK_WARPS + warp, nwall = TK_REBUILD_SPLIT * TK_RERANK_WARPS;
+  const TokGeo geo = s.g;
+  const Geo g16{D, 16};
+  const TokLayer hd = s.hdr[layer];
+  const int nt = hd.n_tail, buf = hd.buf, nb = buf ^ 1;
+  int n_aged = nt - s.n_sink - s.n_recent;
+  if (n_aged < 0) n_aged = 0;
+  const size_t mc = (size_t)s.max_context;
+  const int* order = s.order + u * 4 * mc;
+  const int* src_of = s.src_of + u * mc;
+  const bool reset = s.score_window > 0;
   int ncnt[4];
-  for (int z = 0; z < 4; ++z) ncnt[z] = s_cnt[z] < s.cap[z] ? s_cnt[z] : s.cap[z];
-  // ---- rebuild the pools of the other buffer, one destination tile per warp at a time
+  for (int z = 0; z < 4; ++z) ncnt[z] = s.ncnt[u * 4 + z];
+  TkWarpBuf& W = wb[warp];
+  if (lane == 0) W.src_id = -1;
+  __syncwarp();
+  // stage source tile `id` ((pool or tail) << 28 | tile) in shared memory
+  auto stage_src = [&](int id) -> const uint8_t* {
+    if (W.src_id != id) {
+      __syncwarp();
+      const int sz = id >> 28, ti = id & 0x0FFFFFFF;
+      const uint8_t* g = tk_src_tile(s, layer, buf, u, sz, ti * 16);
+      const int bytes = tk_tile_bytes(s, sz);
+      for (int off = lane * 16; off < bytes; off += 512)
+        *reinterpret_cast<uint4*>(W.src + off) = *reinterpret_cast<const uint4*>(g + off);
+      __syncwarp();
+      if (lane == 0) W.src_id = id;
+      __syncwarp();
+    }
+    return W.src;
+  };
   const int T0 = (ncnt[0] + 15) >> 4, T1 = (ncnt[1] + 15) >> 4, T2 = (ncnt[2] + 15) >> 4, T3 = (ncnt[3] + 15) >> 4;
   const int Ttot = T0 + T1 + T2 + T3;
-  TkWarpBuf& W = wb[warp];
-  for (int tt = warp; tt < Ttot; tt += TK_RERANK_WARPS) {
+  for (int tt = wall; tt < Ttot; tt += nwall) {
     int z, kt;
     if (tt < T0) { z = 0; kt = tt; }
     else if (tt < T0 + T1) { z = 1; kt = tt - T0; }
@@ -906,46 +1001,53 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
     else { z = 3; kt = tt - T0 - T1 - T2; }
     const long long pb = tk_pool_tok_index(s, z, layer, nb, u);
     uint8_t* dst = s.pool[z] + (tk_pool_tile_index(s, z, layer, nb, u) + kt) * (long long)tk_tile_bytes(s, z);
-    // positions and scores
+    // lane r < 16: row r's source (pool or tail, index) and its tile id; positions and scores
+    int my_sz = -1, my_si = 0, my_id = -1;
     if (lane < 16) {
       const int idx = 16 * kt + lane;
       if (idx < ncnt[z]) {
         const int q = order[z * mc + idx];
         const int sr = src_of[q];
-        const int sz = sr >> 28, si = sr & 0x0FFFFFFF;
+        my_sz = sr >> 28;
+        my_si = sr & 0x0FFFFFFF;
+        my_id = (my_sz << 28) | (my_si >> 4);
         float sc = 0.f;
         if (!reset) {
-          sc = sz == TK_TAIL ? s.tail_score[tk_tail_tok_index(s, layer, buf, u) + si]
-                             : s.score[sz][tk_pool_tok_index(s, sz, layer, buf, u) + si];
+          sc = my_sz == TK_TAIL ? s.tail_score[tk_tail_tok_index(s, layer, buf, u) + my_si]
+                                : s.score[my_sz][tk_pool_tok_index(s, my_sz, layer, buf, u) + my_si];
         }
         s.pos[z][pb + idx] = q;
         s.score[z][pb + idx] = sc;
       }
     }
+    const unsigned valid = __ballot_sync(0xffffffffu, my_id >= 0);
     if (z == 0) {
-      // BF16 -> BF16: copy the rows into their new places
-      for (int row = 0; row < 16; ++row) {
-        const int idx = 16 * kt + row;
-        const bool valid = idx < ncnt[0];
-        const uint8_t* st = nullptr;
-        int srow = 0;
-        if (valid) {
-          const int sr = src_of[order[idx]];
-          const int sz = sr >> 28, si = sr & 0x0FFFFFFF;
-          st = tk_src_tile(s, layer, buf, u, sz, si);
-          srow = si & 15;
-        }
-        for (int c = 2 * lane; c < D; c += 64) {
-          unsigned kk = 0u;
-          uint16_t v0 = 0, v1 = 0;
-          if (valid) {
-            kk = *reinterpret_cast<const unsigned*>(st + bf16_k_off(g16, srow, c));
-            v0 = *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c));
-            v1 = *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c + 1));
+      // BF16 -> BF16: rows move to their new places (empty rows become zeros)
+      unsigned todo = valid;
+      while (todo) {
+        const int id = __shfl_sync(0xffffffffu, my_id, __ffs(todo) - 1);
+        const unsigned grp = __ballot_sync(0xffffffffu, my_id == id) & todo;
+        const uint8_t* st = stage_src(id);
+        for (unsigned m = grp; m; m &= m - 1) {
+          const int row = __ffs(m) - 1;
+          const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
+          for (int c = 2 * lane; c < D; c += 64) {
+            *reinterpret_cast<unsigned*>(dst + bf16_k_off(g16, row, c)) =
+                *reinterpret_cast<const unsigned*>(st + bf16_k_off(g16, srow, c));
+            *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c)) =
+                *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c));
+            *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c + 1)) =
+                *reinterpret_cast<const uint16_t*>(st + bf16_v_off(g16, srow, c + 1));
           }
-          *reinterpret_cast<unsigned*>(dst + bf16_k_off(g16, row, c)) = kk;
-          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c)) = v0;
-          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c + 1)) = v1;
+        }
+        todo &= ~grp;
+      }
+      for (unsigned m = ~valid & 0xFFFFu; m; m &= m - 1) {
+        const int row = __ffs(m) - 1;
+        for (int c = 2 * lane; c < D; c += 64) {
+          *reinterpret_cast<unsigned*>(dst + bf16_k_off(g16, row, c)) = 0u;
+          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c)) = 0;
+          *reinterpret_cast<uint16_t*>(dst + bf16_v_off(g16, row, c + 1)) = 0;
         }
       }
       __syncwarp();
@@ -955,55 +1057,55 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
     const float levels = (float)((1 << b) - 1);
     for (int half = 0; half < 2; ++half) {   // keys, then values
       const bool value = half == 1;
-      // 1. gather: codes of tokens that keep their tier, values of the others
-      for (int row = 0; row < 16; ++row) {
-        const int idx = 16 * kt + row;
-        int mode = 0;   // 0 empty row, 1 copy codes, 2 quantize values
-        const uint8_t* st = nullptr;
-        int sz = 0, srow = 0;
-        if (idx < ncnt[z]) {
-          const int sr = src_of[order[z * mc + idx]];
-          sz = sr >> 28;
-          const int si = sr & 0x0FFFFFFF;
-          st = tk_src_tile(s, layer, buf, u, sz, si);
-          srow = si & 15;
-          mode = sz == z ? 1 : 2;
+      // 1. gather: codes of rows that keep their tier, values of the others, source by source
+      if (lane < 16) W.need[lane] = my_id >= 0 && my_sz != z;
+      for (unsigned m = ~valid & 0xFFFFu; m; m &= m - 1) {
+        const int row = __ffs(m) - 1;
+        for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = 0;
+        if (lane == 0) W.par[row] = make_float2(0.f, 0.f);
+      }
+      unsigned todo = valid;
+      while (todo) {
+        const int id = __shfl_sync(0xffffffffu, my_id, __ffs(todo) - 1);
+        const unsigned grp = __ballot_sync(0xffffffffu, my_id == id) & todo;
+        const uint8_t* st = stage_src(id);
+        const int sz = id >> 28;
+        for (unsigned m = grp; m; m &= m - 1) {
+          const int row = __ffs(m) - 1;
+          const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
+          if (sz == z) {
+            for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)tk_code_at(geo, st, b, srow, c, value);
+            if (lane == 0)
+              W.par[row] = reinterpret_cast<const float2*>(st + (value ? geo.off_vpar(b) : geo.off_kpar(b)))[srow];
+          } else {
+            for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_at(s, st, sz, srow, c, value);
+          }
         }
-        if (mode == 1) {
-          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)tk_code_at(geo, st, b, srow, c, value);
-          if (lane == 0)
-            W.par[row] = reinterpret_cast<const float2*>(st + (value ? geo.off_vpar(b) : geo.off_kpar(b)))[srow];
-        } else if (mode == 2) {
-          for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_at(s, st, sz, srow, c, value);
-        } else {
-          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = 0;
-          if (lane == 0) W.par[row] = make_float2(0.f, 0.f);
-        }
-        if (lane == 0) W.need[row] = mode == 2;
+        todo &= ~grp;
       }
       __syncwarp();
       // 2. quantize the rows that need it
       if (z == TK_NQ1) {
-        // eqs. (3)-(4), b = 1: mean and population std in float64, channel order, one lane per row
-        if (lane < 16 && W.need[lane]) {
-          const float* x = W.vals + lane * TK_VROW;
-          double acc = 0.0;
-          for (int c = 0; c < D; ++c) acc = __dadd_rn(acc, (double)x[c]);
-          const double m = __ddiv_rn(acc, (double)D);
-          double a2 = 0.0;
-          for (int c = 0; c < D; ++c) {
-            const double dl = __dsub_rn((double)x[c], m);
-            a2 = __dadd_rn(a2, __dmul_rn(dl, dl));
-          }
-          const double sd = __dsqrt_rn(__ddiv_rn(a2, (double)D));
-          W.par[lane] = make_float2(__double2float_rn(m), __double2float_rn(sd));
-        }
-        __syncwarp();
+        // eqs. (3)-(4), b = 1: mean and population std in float32, each sum as per-lane partials
+        // over channels lane, lane + 32, ... and then a xor butterfly, every operation rounded
+        // once (no contraction); code 1 where x > mean
         for (int row = 0; row < 16; ++row) {
           if (!W.need[row]) continue;
-          const float2 pr = W.par[row];
-          for (int c = lane; c < D; c += 32)
-            W.codes[row * 128 + c] = (uint8_t)(pr.y > 0.f && W.vals[row * TK_VROW + c] > pr.x);
+          const float* x = W.vals + row * TK_VROW;
+          float a = x[lane];
+          for (int c = lane + 32; c < D; c += 32) a = __fadd_rn(a, x[c]);
+          for (int o = 16; o; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
+          const float m = __fdiv_rn(a, (float)D);
+          float dl = __fsub_rn(x[lane], m);
+          float q = __fmul_rn(dl, dl);
+          for (int c = lane + 32; c < D; c += 32) {
+            dl = __fsub_rn(x[c], m);
+            q = __fadd_rn(q, __fmul_rn(dl, dl));
+          }
+          for (int o = 16; o; o >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, o));
+          const float sd = __fsqrt_rn(__fdiv_rn(q, (float)D));
+          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)(sd > 0.f && x[c] > m);
+          if (lane == 0) W.par[row] = make_float2(m, sd);
         }
       } else {
         // eq. (2) per token: z = min, s = (max - min) / (2^b - 1) in float32
@@ -1057,7 +1159,7 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
     const int ntn = nt - n_aged;
     const long long ob = tk_tail_tok_index(s, layer, buf, u), nbb = tk_tail_tok_index(s, layer, nb, u);
     const int tiles = (ntn + 15) >> 4;
-    for (int tt = warp; tt < tiles; tt += TK_RERANK_WARPS) {
+    for (int tt = wall; tt < tiles; tt += nwall) {
       uint8_t* dst = s.tail + (nbb / 16 + tt) * (long long)geo.bf_tile();
       for (int row = 0; row < 16; ++row) {
         const int i = 16 * tt + row;
@@ -1084,18 +1186,15 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
       }
     }
   }
-  if (tid == 0) {
-    int4 nc;
-    nc.x = ncnt[0]; nc.y = ncnt[1]; nc.z = ncnt[2]; nc.w = ncnt[3];
-    *reinterpret_cast<int4*>(s.cnt + ((long long)layer * s.units + u) * 4) = nc;
-  }
 }
 
 // After the re-rank of a layer: cost prefix of the new counts and the header switch.
 __global__ void tk_finish_kernel(TokState s, int layer) {
   __shared__ long long part[256];
   const int tid = threadIdx.x;
-  const int* cnt = s.cnt + (long long)layer * s.units * 4;
+  int* cnt = s.cnt + (long long)layer * s.units * 4;
+  for (int i = tid; i < s.units * 4; i += 256) cnt[i] = s.ncnt[i];
+  __syncthreads();
   long long* cum = s.cum + (long long)layer * (s.units + 1);
   // each thread sums a contiguous run of units, then a serial prefix over the threads
   const int per = (s.units + 255) / 256;
@@ -1142,7 +1241,7 @@ static cudaError_t tk_prepare_t() {
   cudaError_t e = cudaFuncSetAttribute(tk_attn_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        TK_WARPS * NST * STAGE);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(tk_rerank_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  return cudaFuncSetAttribute(tk_rebuild_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)tk_rerank_smem(D));
 }
 
@@ -1230,9 +1329,13 @@ cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float*
 
 cudaError_t tk_launch_rerank(const TokState& s, int layer, cudaStream_t st) {
   const size_t sm = tk_rerank_smem(s.g.D);
-  if (s.g.D == 128) tk_rerank_kernel<128><<<s.units, TK_RERANK_THREADS, sm, st>>>(s, layer);
-  else tk_rerank_kernel<64><<<s.units, TK_RERANK_THREADS, sm, st>>>(s, layer);
+  if (s.g.D == 128) tk_rerank_kernel<128><<<s.units, TK_RERANK_THREADS, 0, st>>>(s, layer);
+  else tk_rerank_kernel<64><<<s.units, TK_RERANK_THREADS, 0, st>>>(s, layer);
   cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+  if (s.g.D == 128) tk_rebuild_kernel<128><<<s.units * TK_REBUILD_SPLIT, TK_RERANK_THREADS, sm, st>>>(s, layer);
+  else tk_rebuild_kernel<64><<<s.units * TK_REBUILD_SPLIT, TK_RERANK_THREADS, sm, st>>>(s, layer);
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   tk_finish_kernel<<<1, 256, 0, st>>>(s, layer);
   return cudaGetLastError();

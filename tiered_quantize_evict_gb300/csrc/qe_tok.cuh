@@ -100,6 +100,7 @@ struct TokState {
   uint8_t* newt;
   int* order;              // [units][4][max_context]
   int* src_of;             // [units][max_context]
+  int* ncnt;               // [units][4] ranked pool counts after the re-rank being applied
   unsigned* done;          // [layers] combine completion counters
 };
 

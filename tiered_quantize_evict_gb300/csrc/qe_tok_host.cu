@@ -192,6 +192,7 @@ qe_status tok_init(const qe_config& c, cudaStream_t stream, qe_handle* out, std:
   A(talloc(h, &s.newt, (size_t)s.units * mc));
   A(talloc(h, &s.order, (size_t)s.units * 4 * mc));
   A(talloc(h, &s.src_of, (size_t)s.units * mc));
+  A(talloc(h, &s.ncnt, (size_t)s.units * 4));
   A(talloc(h, &s.done, (size_t)c.n_layers));
   A(talloc(h, &h->tk_part_o, (size_t)(NW + s.units) * G * c.head_dim));
   A(talloc(h, &h->tk_part_ml, (size_t)(NW + s.units) * G));
@@ -363,7 +364,9 @@ qe_status tok_layer_info(qe_handle h, int layer, qe_layer_info* info) {
   TokLayer hd;
   if ((st = fetch_counts(h, layer, cnt, hd)) != QE_OK) return st;
   std::memset(info, 0, sizeof *info);
-  const TokMirror& m = h->tlay[layer];
+  TokMirror& m = h->tlay[layer];
+  m.L = hd.L + m.pending;              // the device header also advances under CUDA-graph replays
+  m.n_tail = hd.n_tail + m.pending;
   info->length = m.L;
   info->units = h->ts.units;
   info->max_windows = h->cfg.max_context;
@@ -424,8 +427,9 @@ static qe_status tok_snapshot(qe_handle h, int layer, TokSnapshot& sn, bool scor
 
 static int tok_count(const qe_handle h, const TokSnapshot& sn, int layer, int u, int z) {
   if (z < 4) return sn.cnt[(size_t)u * 4 + z];
-  return h->tlay[layer].n_tail;   // the pending token is written already
+  return sn.hd.n_tail + h->tlay[layer].pending;   // the pending token is written already
 }
+static int tok_length(const qe_handle h, const TokSnapshot& sn, int layer) { return sn.hd.L + h->tlay[layer].pending; }
 
 qe_status qe_get_token_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes) {
   qe_status st = tok_only(h, layer);
@@ -438,7 +442,7 @@ qe_status qe_get_token_tiers(qe_handle h, int layer, uint8_t* host, size_t bytes
   }
   TokSnapshot sn;
   if ((st = tok_snapshot(h, layer, sn, false)) != QE_OK) return st;
-  const int L = h->tlay[layer].L;
+  const int L = tok_length(h, sn, layer);
   for (int u = 0; u < s.units; ++u) {
     uint8_t* row = host + u * mc;
     for (size_t p = 0; p < mc; ++p) row[p] = (int)p < L ? QE_TOK_EVICTED : QE_TOK_ABSENT;
@@ -506,7 +510,7 @@ qe_status qe_get_token(qe_handle h, int layer, int unit, int pos, int* tier, uin
   }
   TokSnapshot sn;
   if ((st = tok_snapshot(h, layer, sn, false)) != QE_OK) return st;
-  *tier = pos >= 0 && pos < h->tlay[layer].L ? QE_TOK_EVICTED : QE_TOK_ABSENT;
+  *tier = pos >= 0 && pos < tok_length(h, sn, layer) ? QE_TOK_EVICTED : QE_TOK_ABSENT;
   const int D = s.g.D;
   for (int z = 0; z < 5; ++z) {
     const int cap = z < 4 ? s.cap[z] : s.cap_tail;
