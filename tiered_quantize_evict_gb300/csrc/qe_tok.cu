@@ -948,6 +948,180 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
   if (tid < 4) s.ncnt[u * 4 + tid] = s_cnt[tid] < s.cap[tid] ? s_cnt[tid] : s.cap[tid];
 }
 
+// stage source tile `id` ((pool or tail) << 28 | tile) of unit u in the warp's shared buffer
+__device__ __forceinline__ const uint8_t* tk_stage(TkWarpBuf& W, const TokState& s, int layer, int buf, int u, int id,
+                                                   int lane) {
+  if (W.src_id != id) {
+    __syncwarp();
+    const int sz = id >> 28, ti = id & 0x0FFFFFFF;
+    const uint8_t* g = tk_src_tile(s, layer, buf, u, sz, ti * 16);
+    const int bytes = tk_tile_bytes(s, sz);
+    for (int off = lane * 16; off < bytes; off += 512)
+      *reinterpret_cast<uint4*>(W.src + off) = *reinterpret_cast<const uint4*>(g + off);
+    __syncwarp();
+    if (lane == 0) W.src_id = id;
+    __syncwarp();
+  }
+  return W.src;
+}
+
+// byte offset (in the tile) and bit of the code of token `tok`, channel c, in a B-bit tile
+template <int D, int B>
+__device__ __forceinline__ void tk_code_loc(int tok, int c, bool value, int& byte, int& bit) {
+  constexpr int PW = 4 / B, WPL = D * B / 64, CW = WPL < 4 ? WPL : 4;
+  const int step = c >> 4;
+  const int row16 = value ? (c & 15) : tok, col16 = value ? tok : (c & 15);
+  const int ln = (row16 & 7) * 4 + ((col16 & 7) >> 1);
+  const int reg = (row16 >> 3) + 2 * (col16 >> 3);
+  const int j = step / PW, k = step % PW;
+  byte = ((j / CW) * 32 + ln) * (CW * 4) + (j % CW) * 4 + (value ? 2 * D * B : 0);
+  bit = 16 * (col16 & 1) + B * (4 * k + reg);
+}
+
+template <int D, int B>
+__device__ __forceinline__ unsigned tk_code_t(const uint8_t* tile, int tok, int c, bool value) {
+  int byte, bit;
+  tk_code_loc<D, B>(tok, c, value, byte, bit);
+  return (*reinterpret_cast<const unsigned*>(tile + byte) >> bit) & ((1u << B) - 1u);
+}
+
+// the value a B-bit tile (normal for the 1-bit tier) reconstructs: one float32 fma
+template <int D, int B>
+__device__ __forceinline__ float tk_value_t(const uint8_t* tile, int tok, int c, bool value) {
+  const unsigned code = tk_code_t<D, B>(tile, tok, c, value);
+  const float2 par = reinterpret_cast<const float2*>(tile + 4 * D * B + (value ? 128 : 0))[tok];
+  if (B == 1) return fmaf(code ? TK_NQ1_C : -TK_NQ1_C, par.y, par.x);
+  return fmaf((float)code, par.y, par.x);
+}
+
+// Rows of one destination tile of the B-bit tier (1-bit: the normal quantizer): codes of rows that
+// keep their tier are moved, rows arriving from another tier are re-quantized from the values it
+// held.  Lane r < 16 holds row r's source (my_sz, my_si, my_id); `valid` marks rows present.
+template <int D, int B>
+__device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, TkWarpBuf& W, uint8_t* dst,
+                                 unsigned valid, int my_sz, int my_si, int my_id, int lane) {
+  constexpr int Z = B == 4 ? TK_INT4 : B == 2 ? TK_INT2 : TK_NQ1;
+  constexpr float LEVELS = (float)((1 << B) - 1);
+  constexpr int WPL = D * B / 64, CW = WPL < 4 ? WPL : 4, PW = 4 / B;
+  const Geo g16{D, 16};
+#pragma unroll 1
+  for (int half = 0; half < 2; ++half) {   // keys, then values
+    const bool value = half == 1;
+    if (lane < 16) W.need[lane] = my_id >= 0 && my_sz != Z;
+    for (unsigned m = ~valid & 0xFFFFu; m; m &= m - 1) {
+      const int row = __ffs(m) - 1;
+      for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = 0;
+      if (lane == 0) W.par[row] = make_float2(0.f, 0.f);
+    }
+    // 1. gather, one staged source tile at a time
+    unsigned todo = valid;
+    while (todo) {
+      const int id = __shfl_sync(0xffffffffu, my_id, __ffs(todo) - 1);
+      const unsigned grp = __ballot_sync(0xffffffffu, my_id == id) & todo;
+      const uint8_t* st = tk_stage(W, s, layer, buf, u, id, lane);
+      const int sz = id >> 28;
+      for (unsigned m = grp; m; m &= m - 1) {
+        const int row = __ffs(m) - 1;
+        const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
+        if (sz == Z) {
+#pragma unroll
+          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)tk_code_t<D, B>(st, srow, c, value);
+          if (lane == 0) W.par[row] = reinterpret_cast<const float2*>(st + 4 * D * B + (value ? 128 : 0))[srow];
+        } else if (sz == TK_BF16 || sz == TK_TAIL) {
+#pragma unroll
+          for (int c = lane; c < D; c += 32) {
+            const int off = value ? bf16_v_off(g16, srow, c) : bf16_k_off(g16, srow, c);
+            W.vals[row * TK_VROW + c] = __uint_as_float((unsigned)*reinterpret_cast<const uint16_t*>(st + off) << 16);
+          }
+        } else if (sz == TK_INT4) {
+#pragma unroll
+          for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_t<D, 4>(st, srow, c, value);
+        } else {   // 2-bit (a token only moves down, so a 1-bit source never reaches another tier)
+#pragma unroll
+          for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_t<D, 2>(st, srow, c, value);
+        }
+      }
+      todo &= ~grp;
+    }
+    __syncwarp();
+    // 2. quantize the rows arriving from another tier
+    if (B == 1) {
+      // eqs. (3)-(4), b = 1: mean and population std in float32, each sum as per-lane partials
+      // over channels lane, lane + 32, ... then a xor butterfly, every operation rounded once
+      // (no contraction); code 1 where x > mean
+      for (int row = 0; row < 16; ++row) {
+        if (!W.need[row]) continue;
+        const float* x = W.vals + row * TK_VROW;
+        float a = x[lane];
+#pragma unroll
+        for (int c = lane + 32; c < D; c += 32) a = __fadd_rn(a, x[c]);
+#pragma unroll
+        for (int o = 16; o; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
+        const float m = __fdiv_rn(a, (float)D);
+        float dl = __fsub_rn(x[lane], m);
+        float q = __fmul_rn(dl, dl);
+#pragma unroll
+        for (int c = lane + 32; c < D; c += 32) {
+          dl = __fsub_rn(x[c], m);
+          q = __fadd_rn(q, __fmul_rn(dl, dl));
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, o));
+        const float sd = __fsqrt_rn(__fdiv_rn(q, (float)D));
+#pragma unroll
+        for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)(sd > 0.f && x[c] > m);
+        if (lane == 0) W.par[row] = make_float2(m, sd);
+      }
+    } else {
+      // eq. (2) per token: z = min, s = (max - min) / (2^b - 1) in float32
+      for (int row = 0; row < 16; ++row) {
+        if (!W.need[row]) continue;
+        float mn = INFINITY, mx = -INFINITY;
+#pragma unroll
+        for (int c = lane; c < D; c += 32) {
+          const float x = W.vals[row * TK_VROW + c];
+          mn = fminf(mn, x);
+          mx = fmaxf(mx, x);
+        }
+#pragma unroll
+        for (int o = 16; o; o >>= 1) {
+          mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+        }
+        const float sc = __fdiv_rn(__fsub_rn(mx, mn), LEVELS);
+#pragma unroll
+        for (int c = lane; c < D; c += 32)
+          W.codes[row * 128 + c] = (uint8_t)tk_quant_code(W.vals[row * TK_VROW + c], mn, sc, LEVELS);
+        if (lane == 0) W.par[row] = make_float2(mn, sc);
+      }
+    }
+    __syncwarp();
+    // 3. pack this lane's words and write the block and its parameters
+    uint8_t* blk = dst + (value ? 2 * D * B : 0);
+#pragma unroll
+    for (int j = 0; j < WPL; ++j) {
+      unsigned word = 0u;
+#pragma unroll
+      for (int kk = 0; kk < PW; ++kk) {
+        const int step = j * PW + kk;
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+          for (int hf = 0; hf < 2; ++hf) {
+            const int row16 = (lane >> 2) + 8 * (r & 1);
+            const int col16 = ((lane & 3) << 1) + hf + 8 * (r >> 1);
+            const int tok = value ? col16 : row16;
+            const int ch = 16 * step + (value ? row16 : col16);
+            word |= (unsigned)W.codes[tok * 128 + ch] << (16 * hf + B * (4 * kk + r));
+          }
+      }
+      *reinterpret_cast<unsigned*>(blk + ((j / CW) * 32 + lane) * (CW * 4) + (j % CW) * 4) = word;
+    }
+    if (lane < 16) reinterpret_cast<float2*>(dst + 4 * D * B + (value ? 128 : 0))[lane] = W.par[lane];
+    __syncwarp();
+  }
+}
+
 // Rebuild of one unit's pools and tail in the other buffer after tk_rerank_kernel chose the new
 // tiers: TK_REBUILD_SPLIT CTAs per unit share its destination tiles, one tile per warp at a time.
 // A destination tile's rows (position order) come from few source tiles: the warp stages each
@@ -976,21 +1150,6 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const 
   TkWarpBuf& W = wb[warp];
   if (lane == 0) W.src_id = -1;
   __syncwarp();
-  // stage source tile `id` ((pool or tail) << 28 | tile) in shared memory
-  auto stage_src = [&](int id) -> const uint8_t* {
-    if (W.src_id != id) {
-      __syncwarp();
-      const int sz = id >> 28, ti = id & 0x0FFFFFFF;
-      const uint8_t* g = tk_src_tile(s, layer, buf, u, sz, ti * 16);
-      const int bytes = tk_tile_bytes(s, sz);
-      for (int off = lane * 16; off < bytes; off += 512)
-        *reinterpret_cast<uint4*>(W.src + off) = *reinterpret_cast<const uint4*>(g + off);
-      __syncwarp();
-      if (lane == 0) W.src_id = id;
-      __syncwarp();
-    }
-    return W.src;
-  };
   const int T0 = (ncnt[0] + 15) >> 4, T1 = (ncnt[1] + 15) >> 4, T2 = (ncnt[2] + 15) >> 4, T3 = (ncnt[3] + 15) >> 4;
   const int Ttot = T0 + T1 + T2 + T3;
   for (int tt = wall; tt < Ttot; tt += nwall) {
@@ -1027,7 +1186,7 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const 
       while (todo) {
         const int id = __shfl_sync(0xffffffffu, my_id, __ffs(todo) - 1);
         const unsigned grp = __ballot_sync(0xffffffffu, my_id == id) & todo;
-        const uint8_t* st = stage_src(id);
+        const uint8_t* st = tk_stage(W, s, layer, buf, u, id, lane);
         for (unsigned m = grp; m; m &= m - 1) {
           const int row = __ffs(m) - 1;
           const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
@@ -1053,106 +1212,9 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const 
       __syncwarp();
       continue;
     }
-    const int b = tk_bits(z);
-    const float levels = (float)((1 << b) - 1);
-    for (int half = 0; half < 2; ++half) {   // keys, then values
-      const bool value = half == 1;
-      // 1. gather: codes of rows that keep their tier, values of the others, source by source
-      if (lane < 16) W.need[lane] = my_id >= 0 && my_sz != z;
-      for (unsigned m = ~valid & 0xFFFFu; m; m &= m - 1) {
-        const int row = __ffs(m) - 1;
-        for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = 0;
-        if (lane == 0) W.par[row] = make_float2(0.f, 0.f);
-      }
-      unsigned todo = valid;
-      while (todo) {
-        const int id = __shfl_sync(0xffffffffu, my_id, __ffs(todo) - 1);
-        const unsigned grp = __ballot_sync(0xffffffffu, my_id == id) & todo;
-        const uint8_t* st = stage_src(id);
-        const int sz = id >> 28;
-        for (unsigned m = grp; m; m &= m - 1) {
-          const int row = __ffs(m) - 1;
-          const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
-          if (sz == z) {
-            for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)tk_code_at(geo, st, b, srow, c, value);
-            if (lane == 0)
-              W.par[row] = reinterpret_cast<const float2*>(st + (value ? geo.off_vpar(b) : geo.off_kpar(b)))[srow];
-          } else {
-            for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_at(s, st, sz, srow, c, value);
-          }
-        }
-        todo &= ~grp;
-      }
-      __syncwarp();
-      // 2. quantize the rows that need it
-      if (z == TK_NQ1) {
-        // eqs. (3)-(4), b = 1: mean and population std in float32, each sum as per-lane partials
-        // over channels lane, lane + 32, ... and then a xor butterfly, every operation rounded
-        // once (no contraction); code 1 where x > mean
-        for (int row = 0; row < 16; ++row) {
-          if (!W.need[row]) continue;
-          const float* x = W.vals + row * TK_VROW;
-          float a = x[lane];
-          for (int c = lane + 32; c < D; c += 32) a = __fadd_rn(a, x[c]);
-          for (int o = 16; o; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
-          const float m = __fdiv_rn(a, (float)D);
-          float dl = __fsub_rn(x[lane], m);
-          float q = __fmul_rn(dl, dl);
-          for (int c = lane + 32; c < D; c += 32) {
-            dl = __fsub_rn(x[c], m);
-            q = __fadd_rn(q, __fmul_rn(dl, dl));
-          }
-          for (int o = 16; o; o >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, o));
-          const float sd = __fsqrt_rn(__fdiv_rn(q, (float)D));
-          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)(sd > 0.f && x[c] > m);
-          if (lane == 0) W.par[row] = make_float2(m, sd);
-        }
-      } else {
-        // eq. (2) per token: z = min, s = (max - min) / (2^b - 1) in float32
-        for (int row = 0; row < 16; ++row) {
-          if (!W.need[row]) continue;
-          float mn = INFINITY, mx = -INFINITY;
-          for (int c = lane; c < D; c += 32) {
-            const float x = W.vals[row * TK_VROW + c];
-            mn = fminf(mn, x);
-            mx = fmaxf(mx, x);
-          }
-          for (int o = 16; o; o >>= 1) {
-            mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
-            mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
-          }
-          const float sc = __fdiv_rn(__fsub_rn(mx, mn), levels);
-          for (int c = lane; c < D; c += 32)
-            W.codes[row * 128 + c] = (uint8_t)tk_quant_code(W.vals[row * TK_VROW + c], mn, sc, levels);
-          if (lane == 0) W.par[row] = make_float2(mn, sc);
-        }
-      }
-      __syncwarp();
-      // 3. pack this lane's words and write the block and its parameters
-      {
-        const int wpl = geo.wpl(b), cw = geo.cw(b), per_word = 4 / b;
-        uint8_t* blk = dst + (value ? geo.off_vcode(b) : 0);
-        for (int j = 0; j < wpl; ++j) {
-          unsigned word = 0u;
-          for (int kk = 0; kk < per_word; ++kk) {
-            const int step = j * per_word + kk;
-            for (int r = 0; r < 4; ++r)
-              for (int hf = 0; hf < 2; ++hf) {
-                const int row16 = (lane >> 2) + 8 * (r & 1);
-                const int col16 = ((lane & 3) << 1) + hf + 8 * (r >> 1);
-                const int tok = value ? col16 : row16;
-                const int ch = 16 * step + (value ? row16 : col16);
-                const unsigned code = W.codes[tok * 128 + ch];
-                word |= code << (16 * hf + b * (4 * kk + r));
-              }
-          }
-          *reinterpret_cast<unsigned*>(blk + ((j / cw) * 32 + lane) * (cw * 4) + (j % cw) * 4) = word;
-        }
-        if (lane < 16)
-          reinterpret_cast<float2*>(dst + (value ? geo.off_vpar(b) : geo.off_kpar(b)))[lane] = W.par[lane];
-      }
-      __syncwarp();
-    }
+    if (z == TK_INT4) tk_rebuild_qtile<D, 4>(s, layer, buf, u, W, dst, valid, my_sz, my_si, my_id, lane);
+    else if (z == TK_INT2) tk_rebuild_qtile<D, 2>(s, layer, buf, u, W, dst, valid, my_sz, my_si, my_id, lane);
+    else tk_rebuild_qtile<D, 1>(s, layer, buf, u, W, dst, valid, my_sz, my_si, my_id, lane);
   }
   // ---- the new tail: the sink and the recent tokens, moved up over the aged ones
   {
