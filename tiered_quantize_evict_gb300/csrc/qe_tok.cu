@@ -166,10 +166,7 @@ __device__ __forceinline__ void tk_softmax(float (&acc)[2][4], int nvalid, const
     if constexpr (Q) zadd = fmaf(pr[j], vz[j], zadd);
   }
   if constexpr (Q) st.zs += zadd;
-  mass += __shfl_xor_sync(0xffffffffu, mass, 4);
-  mass += __shfl_xor_sync(0xffffffffu, mass, 8);
-  mass += __shfl_xor_sync(0xffffffffu, mass, 16);
-  st.l += mass;
+  st.l += mass;   // this lane's rows only: the flush sums the partial normalisers of a head
   constexpr unsigned KEEP = Q ? 0xFFFFE000u : 0xFFFF0000u;
   unsigned rr[2];
 #pragma unroll
@@ -432,10 +429,13 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   };
   auto flush = [&](int u) {
     const long long slot = (long long)wg + u;
-    float z = rs.zs;
+    float z = rs.zs, l = rs.l;
     z += __shfl_xor_sync(0xffffffffu, z, 4);
     z += __shfl_xor_sync(0xffffffffu, z, 8);
     z += __shfl_xor_sync(0xffffffffu, z, 16);
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
     if (t < G) {
       float* po = p.part_o + (slot * G + t) * D;
 #pragma unroll
@@ -443,7 +443,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
         po[mc * 16 + g] = rs.O[mc][0] + rs.O[mc][1] + z;
         po[mc * 16 + g + 8] = rs.O[mc][2] + rs.O[mc][3] + z;
       }
-      if (g == 0) p.part_ml[slot * G + t] = make_float2(rs.mref, rs.l);
+      if (g == 0) p.part_ml[slot * G + t] = make_float2(rs.mref, l);
     }
   };
   reset();
