@@ -37,9 +37,12 @@ CASES = {
 
 
 class TokRun:
-    def __init__(self, wl):
+    def __init__(self, wl, host=None):
+        """host: None (device buffers), "pinned" or "pageable": where every call's inputs and
+        outputs live."""
         import tiered_quantize_evict_gb300 as qe
         torch, dev = torch_dev()
+        self.host = host
         self.torch, self.dev, self.wl = torch, dev, wl
         self.cache = qe.QECache(qe.config_from_workload(wl), torch.cuda.current_stream().cuda_stream)
         self.units = {(b, l, h): make_unit(wl) for b in range(wl.batch) for l in range(wl.n_layers)
@@ -49,7 +52,26 @@ class TokRun:
         self.max_score = 0.0
         self.codes_checked = 0
         self.bf16_checked = 0
-        self.out = torch.empty(wl.batch, wl.n_q_heads, wl.head_dim, device=dev, dtype=torch.float32)
+        if host == "pinned":
+            self.out = torch.empty(wl.batch, wl.n_q_heads, wl.head_dim, dtype=torch.float32).pin_memory()
+        elif host == "pageable":
+            self.out = np.zeros((wl.batch, wl.n_q_heads, wl.head_dim), np.float32)
+        else:
+            self.out = torch.empty(wl.batch, wl.n_q_heads, wl.head_dim, device=dev, dtype=torch.float32)
+
+    def place(self, a):
+        a = np.ascontiguousarray(a).view(np.int16)
+        if self.host == "pinned":
+            return self.torch.from_numpy(a).pin_memory()
+        if self.host == "pageable":
+            return a.copy()
+        return to_dev(a)
+
+    def read_out(self):
+        if self.host:
+            self.cache.qe_synchronize()
+            return np.array(self.out, dtype=np.float64) if self.host == "pageable" else self.out.numpy().astype(np.float64)
+        return self.out.cpu().numpy().astype(np.float64)
 
     def u_index(self, b, h):
         return b * self.wl.n_kv_heads + h
@@ -58,7 +80,9 @@ class TokRun:
         wl = self.wl
         for layer in range(wl.n_layers):
             K, V = host_kv(wl, layer, 0, wl.prefill, wl.batch)
-            self.cache.qe_append(layer, to_dev(K), to_dev(V), wl.prefill)
+            kt, vt = self.place(K), self.place(V)
+            self.cache.qe_append(layer, kt, vt, wl.prefill)
+            self.cache.qe_synchronize()
             for b in range(wl.batch):
                 for h in range(wl.n_kv_heads):
                     self.units[(b, layer, h)].append(gen.bf16_bits_to_f32(K[b, h]), gen.bf16_bits_to_f32(V[b, h]))
@@ -71,9 +95,10 @@ class TokRun:
         for layer in range(wl.n_layers):
             K, V = host_kv(wl, layer, pos, 1, wl.batch)
             Q = host_q(wl, layer, t, wl.batch)
-            self.cache.qe_append(layer, to_dev(K), to_dev(V), 1)
-            self.cache.qe_decode_step(layer, to_dev(Q), self.out)
-            got = self.out.cpu().numpy().astype(np.float64)
+            kt, vt, qt = self.place(K), self.place(V), self.place(Q)   # alive until read_out syncs
+            self.cache.qe_append(layer, kt, vt, 1)
+            self.cache.qe_decode_step(layer, qt, self.out)
+            got = self.read_out()
             for b in range(wl.batch):
                 for h in range(wl.n_kv_heads):
                     heads = slice(h * wl.group, (h + 1) * wl.group)
@@ -156,6 +181,20 @@ def test_five_tier_trajectory(name):
           f"bf16 {run.bf16_checked}, counts unit 0 {counts[0].tolist()}")
     assert run.codes_checked > 0
     assert (counts[:, 1:4] > 0).all()
+
+
+@pytest.mark.parametrize("host", ["pinned", "pageable"])
+def test_five_tier_host_buffers(host):
+    """Host inputs and outputs: pinned tokens and queries are read, outputs written, in place by
+    the kernels; pageable ones go through copies; the trajectory still follows the oracle."""
+    wl = dataclasses.replace(CASES["d128_g4"], decode_steps=32)
+    run = TokRun(wl, host=host)
+    run.prefill()
+    for _ in range(wl.decode_steps):
+        run.step()
+    run.cache.qe_synchronize()
+    print(f"five-tier host {host}: max out rel-L2 {run.max_out:.2e}, codes {run.codes_checked}")
+    assert run.codes_checked > 0
 
 
 def test_hqe_16k_sampled_units_graph_replay():
