@@ -128,15 +128,17 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- ncu traffic record
-def _traffic(workload: str):
-    """DRAM bytes per launch of qe_decode_attn from the committed ncu summary, if the kernel
-    source is unchanged since it was captured (else None)."""
-    path = os.path.join(ROOT, "profiles", f"qe_decode_attn_{workload}.json")
+def _traffic(workload: str, kernel: str = "qe_decode_attn"):
+    """DRAM bytes per launch of the attention kernel from the committed ncu summary, if the
+    kernel source is unchanged since it was captured (else None)."""
+    src_file = {"qe_decode_attn": "qe_attn.cu", "tk_attn": "qe_tok.cu"}[kernel]
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        src = open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", "qe_attn.cu"), "rb").read()
-        if rec.get("qe_attn_sha256") != hashlib.sha256(src).hexdigest():
+        src = open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", src_file), "rb").read()
+        sha = rec.get("source_sha256", rec.get("qe_attn_sha256"))
+        if sha != hashlib.sha256(src).hexdigest():
             return None
         return rec.get("dram_bytes_per_launch_full")
     except Exception:
@@ -329,7 +331,7 @@ def run_ours(args):
             "bound": "hbm", "kernel": "tk_attn" if tok else "qe_decode_attn", "achieved": round(achieved, 1) if achieved else None,
             "peak": peak, "peak_kind": peak_kind, "unit": "GB/s",
             "frac": round(achieved / peak, 4) if achieved else None,
-            "traffic": _traffic(wl.name),
+            "traffic": _traffic(wl.name, "tk_attn" if tok else "qe_decode_attn"),
             "algorithmic_bytes_per_launch": round(attn_bytes / max(attn_launches, 1)),
             "avg_launch_us": round(attn_ms * 1e3 / max(attn_launches, 1), 2),
             "attn_share_of_step": round(attn_ms / ms_total, 4) if ms_total > 0 else None,
