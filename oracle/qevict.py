@@ -38,6 +38,7 @@ import numpy as np
 
 from .attention import group_mass, softmax_attention
 from .quant import QuantizedWindow, kivi_quantize_window
+from .rope import apply_rope
 from .router import EVICTED, FULL, PINNED, QUANT, RouteResult, assign, candidate_pool
 
 F32 = np.float32
@@ -48,7 +49,9 @@ class QEvictUnit:
 
     def __init__(self, window: int, n_sink: int, n_recent: int, head_dim: int, group: int,
                  capacity: Callable[[int], Tuple[int, int]], max_context: int,
-                 v_group: Optional[int] = None):
+                 v_group: Optional[int] = None, rope_base: float = 0.0):
+        """rope_base > 0: keys are stored pre-RoPE and rotated at their original positions when
+        attended to (``oracle.rope``)."""
         assert 0 <= n_sink < window
         self.w, self.n_sink, self.n_recent = window, n_sink, n_recent
         self.d, self.G = head_dim, group
@@ -63,6 +66,7 @@ class QEvictUnit:
         self.ledger: Dict[int, QuantizedWindow] = {}
         self._deq: Dict[int, Tuple[np.ndarray, np.ndarray]] = {}
         self.history: List[RouteResult] = []
+        self.rope_base = float(rope_base)
 
     # ------------------------------------------------------------------ geometry
     def window_range(self, j: int) -> Tuple[int, int]:
@@ -93,9 +97,10 @@ class QEvictUnit:
 
     def accessible(self):
         """(K_acc, V_acc, window of each token): sink, Pinned/Full originals, dequantized INT2."""
-        ks, vs, ws = [], [], []
+        ks, vs, ws, ps = [], [], [], []
         ns = min(self.n_sink, self.L)
         ks.append(self.K[:ns].astype(np.float64))
+        ps.append(np.arange(ns))
         vs.append(self.V[:ns].astype(np.float64))
         ws.append(np.full(ns, -1))
         for j in sorted(self.tier):
@@ -110,7 +115,11 @@ class QEvictUnit:
             ks.append(k)
             vs.append(v)
             ws.append(np.full(hi - lo, j))
-        return np.concatenate(ks), np.concatenate(vs), np.concatenate(ws)
+            ps.append(np.arange(lo, hi))
+        K = np.concatenate(ks)
+        if self.rope_base > 0:                   # pre-RoPE keys, rotated at their original positions
+            K = apply_rope(K, np.concatenate(ps), self.rope_base)
+        return K, np.concatenate(vs), np.concatenate(ws)
 
     def attend(self, q):
         """Attention of the group's queries q [G, d] over the accessible set.

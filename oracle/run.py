@@ -28,7 +28,8 @@ def make_unit(wl, max_context: Optional[int] = None):
         return HqeUnit(wl.head_dim, wl.group, wl.n_sink, wl.n_recent, wl.route_period, wl.score_window,
                        (wl.frac_bf16, wl.frac_int4, wl.frac_int2, wl.frac_nq1), max_context or wl.max_context)
     return QEvictUnit(wl.window, wl.n_sink, wl.n_recent, wl.head_dim, wl.group,
-                      lambda L: capacities(wl, L), max_context or wl.max_context)
+                      lambda L: capacities(wl, L), max_context or wl.max_context,
+                      rope_base=getattr(wl, "rope_theta", 0.0))
 
 
 def prefill(wl, unit: QEvictUnit, b: int, layer: int, kvh: int, n: Optional[int] = None):

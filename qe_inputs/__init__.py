@@ -140,6 +140,8 @@ class Workload:
     frac_int4: float = 0.0
     frac_nq1: float = 0.0
     score_window: int = 0
+    # rotary embedding base for keys stored pre-RoPE (0 = keys carry no rotation)
+    rope_theta: float = 0.0
 
     @property
     def group(self) -> int:
@@ -170,6 +172,13 @@ WORKLOADS = {
         prefill=32768, decode_steps=128, window=32, route_period=32, n_sink=5, n_recent=32,
         cap_mode=1, frac_bf16=0.08, frac_int2=0.25, seed=20261202 + 3,
         drift_period=64),
+    # the throughput workload with keys stored pre-RoPE (rotary base 10000), rotated in the
+    # attention at their original positions
+    "throughput_32k_rope": Workload(
+        name="throughput_32k_rope", batch=16, n_layers=32, n_q_heads=32, n_kv_heads=8, head_dim=128,
+        prefill=32768, decode_steps=128, window=32, route_period=32, n_sink=5, n_recent=32,
+        cap_mode=1, frac_bf16=0.08, frac_int2=0.25, seed=20261202 + 3,
+        drift_period=64, rope_theta=10000.0),
     # five-tier per-token variant: 10 % BF16 / 20 % INT4 / 30 % INT2 / 30 % 1-bit / 10 % evicted,
     # re-ranked every 64 steps over the attention of the last 20 steps (w = 32 is the drift epoch's
     # window grid only)
