@@ -114,6 +114,13 @@ typedef struct {
   double frac_int4;
   double frac_nq1;
   int score_window;
+  /* Keys stored pre-RoPE (window tiering; QEvict notes §4.4: keys are quantized before the
+   * rotary embedding and rotated again at their original positions).  rope_theta > 0: the
+   * K passed to qe_append is pre-RoPE and every cached key (bf16, or dequantized 2-bit) is
+   * rotated at its original position p before q . k: channel pairs (2i, 2i + 1) by the angle
+   * p * rope_theta^(-2i / head_dim).  q is passed already rotated at its own position.
+   * 0: keys are used as stored. */
+  double rope_theta;
 } qe_config;
 
 enum { QE_TIERING_WINDOWS = 0, QE_TIERING_TOKENS = 1 };

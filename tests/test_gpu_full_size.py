@@ -143,3 +143,16 @@ def test_long_131k_sampled_units():
           f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}, Kf {info.kf}, Kq {info.kq}, "
           f"tie-ambiguous {run.ambiguous}")
     assert run.codes_checked > 0
+
+
+def test_throughput_32k_pre_rope_sampled_units():
+    """The 32K throughput workload with keys stored pre-RoPE (rotary base 10000): 40 steps of
+    direct calls through the first routing event, three sampled units against the oracle."""
+    import dataclasses
+    wl = dataclasses.replace(gen.WORKLOADS["throughput_32k_rope"], decode_steps=40)
+    run = _direct_trajectory(wl, SAMPLED, 40)
+    assert run.route_events == 1
+    full_checked = sum(run.check_bf16_windows(tr) for tr in run.tracked if tr.live)
+    print(f"throughput_32k_rope: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
+          f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}")
+    assert run.codes_checked > 0

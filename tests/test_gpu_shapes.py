@@ -74,3 +74,32 @@ def test_host_buffers_trajectory(host):
     assert run.codes_checked > 0 and run.route_events == wl.decode_steps // wl.route_period
     print(f"host {host}: out err {run.max_out_err:.2e}, score rel err {run.max_score_err:.2e}, "
           f"codes {run.codes_checked}")
+
+
+ROPE_CASES = {
+    "rope_d128_w32_g4": dataclasses.replace(CASES["d128_w32_g4"], name="rope_d128_w32_g4", rope_theta=10000.0,
+                                            prefill=700, seed=41),
+    "rope_d64_w16_g2": dataclasses.replace(CASES["d64_w64_g2"], name="rope_d64_w16_g2", window=16, route_period=8,
+                                           n_sink=3, rope_theta=500.0, seed=42),
+}
+
+
+@pytest.mark.parametrize("name", sorted(ROPE_CASES))
+def test_pre_rope_keys_trajectory(name):
+    """Keys stored pre-RoPE (bf16 windows, 2-bit codes and the host store), rotated at their
+    original positions inside the attention: every unit follows the oracle, which rotates the
+    same stored keys in float64."""
+    wl = ROPE_CASES[name]
+    track = [(b, l, h) for b in range(wl.batch) for l in range(wl.n_layers) for h in range(wl.n_kv_heads)]
+    run = ParityRun(wl, wl.batch, wl.n_layers, track)
+    run.prefill()
+    for _ in range(wl.decode_steps):
+        run.step()
+    run.check_scores()
+    run.cache.qe_synchronize()
+    assert sum(tr.live for tr in run.tracked) >= len(run.tracked) - 1
+    assert run.codes_checked > 0
+    for tr in run.tracked:
+        if tr.live:
+            run.check_bf16_windows(tr)
+    print(f"{name}: out err {run.max_out_err:.2e}, score rel err {run.max_score_err:.2e}, codes {run.codes_checked}")

@@ -422,7 +422,26 @@ __device__ __forceinline__ void softmax_tile(float (&acc)[MT][NF][4], bool full,
   }
 }
 
-template <int D, int W>
+// Keys stored pre-RoPE (QEvict reading notes, §4.4: quantized before the rotation, rotated again
+// at their original positions): cos / sin of the angle (16 b + r) theta_i by angle addition from
+// the block table (b) and the row-offset table (r).
+__device__ __forceinline__ float2 rope_cs(float2 b, float2 o) {
+  return make_float2(fmaf(b.x, o.x, -b.y * o.y), fmaf(b.y, o.x, b.x * o.y));
+}
+// the channel pair (x0, x1) rotated by (cos, sin), as an f16x2 truncated part and an f16x2
+// remainder: 22 bits of the rotated key reach the f16 mma against the query (the bf16 query is
+// exact in f16 inside the f16 range)
+__device__ __forceinline__ void rope_rot_split(float x0, float x1, float2 cs, unsigned& hi, unsigned& lo) {
+  const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
+  const float y1 = fmaf(x0, cs.y, x1 * cs.x);
+  const float h0 = __uint_as_float(__float_as_uint(y0) & 0xFFFFE000u);
+  const float h1 = __uint_as_float(__float_as_uint(y1) & 0xFFFFE000u);
+  hi = pack_f16x2_rz(h0, h1);
+  lo = pack_f16x2_rz(y0 - h0, y1 - h1);
+}
+constexpr int ROPE_OFF_STRIDE_PAD = 4;   // float2 padding of a row of the offset table in shared memory
+
+template <int D, int W, bool ROPE = false>
 __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(const AttnParams p) {
   using S = Shape<D, W>;
   constexpr int KS = S::KS, MC = S::MC, MT = S::MT, KT = S::KT, WPL = S::WPL, CW = S::CW, NST = S::NST;
@@ -440,6 +459,11 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   // described), not in registers the tile loop needs
   __shared__ Lay s_lay;
   if (threadIdx.x == 0) s_lay = make_lay(p.st, p.layer, p.pend, p.cb, p.cq, gridDim.x * ATTN_WARPS);
+  constexpr int ROS = D / 2 + ROPE_OFF_STRIDE_PAD;
+  __shared__ float2 s_roff[ROPE ? 16 * ROS : 1];
+  if constexpr (ROPE) {
+    for (int i = threadIdx.x; i < 16 * (D / 2); i += blockDim.x) s_roff[(i / (D / 2)) * ROS + i % (D / 2)] = p.rope_off[i];
+  }
   // the combine launch may start as CTAs of this one leave (it waits for this grid's completion)
   griddep_launch_dependents();
   __syncthreads();
@@ -497,7 +521,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         bd.sd.u = u;
         bd.sd.lse_off = (u * y.ntiles + d.i) * G;
         bd.sd.meta = d.lo | (d.hi << 8) | (d.kind << 16);
-        bd.sd.pad = 0;
+        // 16-token block of the tile's first row (its position / 16; the sink tile is block 0)
+        bd.sd.pad = ROPE ? (d.win < 0 ? 0 : d.win * (W / 16) + (d.kind == 0 ? d.sub : 0)) : 0;
         bd.pad = 0;
         batch[__popc(vb & ((1u << lane) - 1))] = bd;
       }
@@ -608,18 +633,42 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
         qf[ks][0] = f2_pack(bf16lo_to_f32(a0), bf16hi_to_f32(a0));
         qf[ks][1] = f2_pack(bf16lo_to_f32(a1), bf16hi_to_f32(a1));
-        qb[ks][0] = lo_col ? 0u : a0;
-        qb[ks][1] = lo_col ? 0u : a1;
+        if constexpr (ROPE) {   // f16 B fragments (exact for queries inside the f16 range)
+          qb[ks][0] = lo_col ? 0u : pack_f16x2_rz(bf16lo_to_f32(a0), bf16hi_to_f32(a0));
+          qb[ks][1] = lo_col ? 0u : pack_f16x2_rz(bf16lo_to_f32(a1), bf16hi_to_f32(a1));
+        } else {
+          qb[ks][0] = lo_col ? 0u : a0;
+          qb[ks][1] = lo_col ? 0u : a1;
+        }
       }
     }
     float* lse_out = p.lse + sd.lse_off;
     if (d_kind == 0) {
       // ---- bf16 sub-tile: 16 tokens; two accumulators halve the mma dependency chain
       float acc[1][2][4] = {};
+      if constexpr (ROPE) {
+        // registers: (row g, pair 8 ks + t), (row g + 8, same), (row g, pair 8 ks + 4 + t), (row g + 8, same);
+        // rotated keys meet the query as f16 truncated + remainder parts
+        const float2* bt = p.rope_blk + (size_t)sd.pad * (D / 2);
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const uint4 a = lds128(sp + ks * 512 + lane * 16);
-        mma_bf16(acc[0][ks & 1], a.x, a.y, a.z, a.w, qb[ks][0], qb[ks][1]);
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint4 a = lds128(sp + ks * 512 + lane * 16);
+          const int i0 = 8 * ks + t, i1 = i0 + 4;
+          const float2 b0 = bt[i0], b1 = bt[i1];
+          unsigned h[4], l[4];
+          rope_rot_split(bf16lo_to_f32(a.x), bf16hi_to_f32(a.x), rope_cs(b0, s_roff[g * ROS + i0]), h[0], l[0]);
+          rope_rot_split(bf16lo_to_f32(a.y), bf16hi_to_f32(a.y), rope_cs(b0, s_roff[(g + 8) * ROS + i0]), h[1], l[1]);
+          rope_rot_split(bf16lo_to_f32(a.z), bf16hi_to_f32(a.z), rope_cs(b1, s_roff[g * ROS + i1]), h[2], l[2]);
+          rope_rot_split(bf16lo_to_f32(a.w), bf16hi_to_f32(a.w), rope_cs(b1, s_roff[(g + 8) * ROS + i1]), h[3], l[3]);
+          mma_f16(acc[0][ks & 1], h[0], h[1], h[2], h[3], qb[ks][0], qb[ks][1]);
+          mma_f16(acc[0][ks & 1], l[0], l[1], l[2], l[3], qb[ks][0], qb[ks][1]);
+        }
+      } else {
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const uint4 a = lds128(sp + ks * 512 + lane * 16);
+          mma_bf16(acc[0][ks & 1], a.x, a.y, a.z, a.w, qb[ks][0], qb[ks][1]);
+        }
       }
       const float vnone[2] = {0.f, 0.f};
       unsigned Bp[1][2];
@@ -631,79 +680,147 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         mma_bf16(rs.O[mc], a.x, a.y, a.z, a.w, Bp[0][0], Bp[0][1]);
       }
     } else {
-      // ---- 2-bit window: W tokens
-      const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
-      const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
-      // B fragments q s_K in f16: trunc part in even columns, remainder in odd ones.  The codes
-      // arrive as 1 + code / 4, so logit / 4 = q s_K . A + q . (z_K - 4 s_K) / 4: the bias
-      // accumulates q . (z_K - 4 s_K), the logit scale below carries the factor 4.
-      unsigned qp[KS][2];
-      unsigned long long bp2 = 0ull;
-      const unsigned long long neg4 = f2_pack(-4.f, -4.f);
-      const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
+      if constexpr (ROPE) {
+        // ---- 2-bit window, keys stored pre-RoPE: W tokens
+        const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
+        const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
+        float vz[2 * MT], vs[2 * MT];
+        load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
+        load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
+        // codes arrive as 1 + code / 4: B = 4 p s_V, and the offset p . (z_V - 4 s_V) per token
 #pragma unroll
-      for (int ks = 0; ks < KS; ++ks) {
-        const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
-        const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
-        bp2 = f2_fma(qf[ks][0], zc.x, bp2);
-        bp2 = f2_fma(qf[ks][1], zc.y, bp2);
-        const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
-        bp2 = f2_fma(y01, neg4, bp2);   // q . (z_K - 4 s_K)
-        bp2 = f2_fma(y23, neg4, bp2);
-        const unsigned long long k2 = ((unsigned long long)keep << 32) | keep;
-        const unsigned long long r01 = f2_sub(y01, y01 & k2), r23 = f2_sub(y23, y23 & k2);
-        qp[ks][0] = pack_f16x2_rz(f2_lo(r01), f2_hi(r01));
-        qp[ks][1] = pack_f16x2_rz(f2_lo(r23), f2_hi(r23));
-      }
-      float bpart = 0.25f * (f2_lo(bp2) + f2_hi(bp2));
-      bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
-      bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-      const float bias = __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . (z_K / 4 - s_K) of head t
-      float vz[2 * MT], vs[2 * MT];
-      load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
-      load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
-      // codes arrive as 1 + code / 4: B = 4 p s_V, and the offset p . (z_V - 4 s_V) per token
+        for (int i = 0; i < 2 * MT; ++i) {
+          vs[i] *= 4.f;
+          vz[i] -= vs[i];
+        }
+        float acc[MT][2][4] = {};
+          // keys dequantized per element (one float32 fma), rotated at their positions, then split
+          // into f16 truncated and remainder parts against the f16 query; register r of fragment
+          // F holds the codes of channels 2i, 2i + 1 at bits 8 (F & 1) + 2 r and 16 above
+          unsigned wk[WPL];
+          load_words<WPL, CW>(sp, lane, wk);
 #pragma unroll
-      for (int i = 0; i < 2 * MT; ++i) {
-        vs[i] *= 4.f;
-        vz[i] -= vs[i];
-      }
-      // Q K^T over the unpacked key codes (fragment F = mt KS + ks is half F % 2 of word F / 2);
-      // channel-step parity splits the accumulators, and consecutive mma go to different
-      // accumulators (2 MT independent chains)
-      float acc[MT][2][4] = {};
-      {
-        unsigned wk[WPL];
-        load_words<WPL, CW>(sp, lane, wk);
+          for (int ks = 0; ks < KS; ++ks) {
+            const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
+            const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
+            const float ksv[4] = {f2_lo(sc.x), f2_hi(sc.x), f2_lo(sc.y), f2_hi(sc.y)};
+            const float kzv[4] = {f2_lo(zc.x), f2_hi(zc.x), f2_lo(zc.y), f2_hi(zc.y)};
+            const int i0 = 8 * ks + t, i1 = i0 + 4;
+            const float2 o[4] = {s_roff[g * ROS + i0], s_roff[(g + 8) * ROS + i0], s_roff[g * ROS + i1],
+                                 s_roff[(g + 8) * ROS + i1]};
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks)
+            for (int mt = 0; mt < MT; ++mt) {
+              const int F = mt * KS + ks;
+              const unsigned w = wk[F >> 1];
+              const float2* bt = p.rope_blk + (size_t)(sd.pad + mt) * (D / 2);
+              const float2 b0 = bt[i0], b1 = bt[i1];
+              unsigned h[4], l[4];
 #pragma unroll
-          for (int mt = 0; mt < MT; ++mt) {
-            const int F = mt * KS + ks;
-            unsigned a[4];
-            if (F & 1) unpack_half<1>(wk[F >> 1], a);
-            else unpack_half<0>(wk[F >> 1], a);
-            mma_f16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qp[ks][0], qp[ks][1]);
+              for (int r = 0; r < 4; ++r) {
+                const int sh = 8 * (F & 1) + 2 * r;
+                const int pc = (r >> 1) * 2;   // channel pair (2t, 2t+1) or (2t+8, 2t+9)
+                const float x0 = fmaf((float)((w >> sh) & 3u), ksv[pc], kzv[pc]);
+                const float x1 = fmaf((float)((w >> (sh + 16)) & 3u), ksv[pc + 1], kzv[pc + 1]);
+                rope_rot_split(x0, x1, rope_cs(r < 2 ? b0 : b1, o[r]), h[r], l[r]);
+              }
+              mma_f16(acc[mt][ks & 1], h[0], h[1], h[2], h[3], qb[ks][0], qb[ks][1]);
+              mma_f16(acc[mt][ks & 1], l[0], l[1], l[2], l[3], qb[ks][0], qb[ks][1]);
+            }
           }
-      }
-      unsigned Bp[MT][2];
-      softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 4.f * p.scale_log2, rs, Bp, lse_out,
-                                    G, lane);
-      // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
-      // the outer loop, so consecutive mma go to the MC independent accumulators
-      {
-        unsigned wv[WPL];
-        load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
+        unsigned Bp[MT][2];
+        softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, 0.f, vz, vs, p.scale_log2, rs, Bp, lse_out, G,
+                                      lane);
+        // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
+        // the outer loop, so consecutive mma go to the MC independent accumulators
+        {
+          unsigned wv[WPL];
+          load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
 #pragma unroll
-        for (int kt = 0; kt < KT; ++kt)
+          for (int kt = 0; kt < KT; ++kt)
 #pragma unroll
-          for (int mc = 0; mc < MC; ++mc) {
-            const int F = mc * KT + kt;
-            unsigned a[4];
-            if (F & 1) unpack_half<1>(wv[F >> 1], a);
-            else unpack_half<0>(wv[F >> 1], a);
-            mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
-          }
+            for (int mc = 0; mc < MC; ++mc) {
+              const int F = mc * KT + kt;
+              unsigned a[4];
+              if (F & 1) unpack_half<1>(wv[F >> 1], a);
+              else unpack_half<0>(wv[F >> 1], a);
+              mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
+            }
+        }
+      } else {
+        // ---- 2-bit window: W tokens
+        const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
+        const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
+        // B fragments q s_K in f16: trunc part in even columns, remainder in odd ones.  The codes
+        // arrive as 1 + code / 4, so logit / 4 = q s_K . A + q . (z_K - 4 s_K) / 4: the bias
+        // accumulates q . (z_K - 4 s_K), the logit scale below carries the factor 4.
+        unsigned qp[KS][2];
+        unsigned long long bp2 = 0ull;
+        const unsigned long long neg4 = f2_pack(-4.f, -4.f);
+        const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
+          const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
+          bp2 = f2_fma(qf[ks][0], zc.x, bp2);
+          bp2 = f2_fma(qf[ks][1], zc.y, bp2);
+          const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
+          bp2 = f2_fma(y01, neg4, bp2);   // q . (z_K - 4 s_K)
+          bp2 = f2_fma(y23, neg4, bp2);
+          const unsigned long long k2 = ((unsigned long long)keep << 32) | keep;
+          const unsigned long long r01 = f2_sub(y01, y01 & k2), r23 = f2_sub(y23, y23 & k2);
+          qp[ks][0] = pack_f16x2_rz(f2_lo(r01), f2_hi(r01));
+          qp[ks][1] = pack_f16x2_rz(f2_lo(r23), f2_hi(r23));
+        }
+        float bpart = 0.25f * (f2_lo(bp2) + f2_hi(bp2));
+        bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
+        bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
+        const float bias = __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . (z_K / 4 - s_K) of head t
+        float vz[2 * MT], vs[2 * MT];
+        load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
+        load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
+        // codes arrive as 1 + code / 4: B = 4 p s_V, and the offset p . (z_V - 4 s_V) per token
+#pragma unroll
+        for (int i = 0; i < 2 * MT; ++i) {
+          vs[i] *= 4.f;
+          vz[i] -= vs[i];
+        }
+        // Q K^T over the unpacked key codes (fragment F = mt KS + ks is half F % 2 of word F / 2);
+        // channel-step parity splits the accumulators, and consecutive mma go to different
+        // accumulators (2 MT independent chains)
+        float acc[MT][2][4] = {};
+        {
+          unsigned wk[WPL];
+          load_words<WPL, CW>(sp, lane, wk);
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks)
+#pragma unroll
+            for (int mt = 0; mt < MT; ++mt) {
+              const int F = mt * KS + ks;
+              unsigned a[4];
+              if (F & 1) unpack_half<1>(wk[F >> 1], a);
+              else unpack_half<0>(wk[F >> 1], a);
+              mma_f16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qp[ks][0], qp[ks][1]);
+            }
+        }
+        unsigned Bp[MT][2];
+        softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 4.f * p.scale_log2, rs, Bp, lse_out,
+                                      G, lane);
+        // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
+        // the outer loop, so consecutive mma go to the MC independent accumulators
+        {
+          unsigned wv[WPL];
+          load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
+#pragma unroll
+          for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+            for (int mc = 0; mc < MC; ++mc) {
+              const int F = mc * KT + kt;
+              unsigned a[4];
+              if (F & 1) unpack_half<1>(wv[F >> 1], a);
+              else unpack_half<0>(wv[F >> 1], a);
+              mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
+            }
+        }
       }
     }
     __syncwarp();
@@ -932,13 +1049,17 @@ static size_t attn_smem_bytes() {
 
 template <int D, int W>
 static cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t stream) {
-  qe_decode_attn_kernel<D, W><<<grid, ATTN_WARPS * 32, attn_smem_bytes<D, W>(), stream>>>(p);
+  if (p.rope_blk) qe_decode_attn_kernel<D, W, true><<<grid, ATTN_WARPS * 32, attn_smem_bytes<D, W>(), stream>>>(p);
+  else qe_decode_attn_kernel<D, W, false><<<grid, ATTN_WARPS * 32, attn_smem_bytes<D, W>(), stream>>>(p);
   return cudaGetLastError();
 }
 
 template <int D, int W>
 static cudaError_t prepare_attn_t() {
-  return cudaFuncSetAttribute(qe_decode_attn_kernel<D, W>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(qe_decode_attn_kernel<D, W, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)attn_smem_bytes<D, W>());
+  if (e != cudaSuccess) return e;
+  return cudaFuncSetAttribute(qe_decode_attn_kernel<D, W, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                               (int)attn_smem_bytes<D, W>());
 }
 

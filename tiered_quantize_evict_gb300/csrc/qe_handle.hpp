@@ -61,6 +61,9 @@ struct qe_handle_s {
   // pinned host store
   void* hstore_host = nullptr;
   void* hledger_host = nullptr;
+  // keys stored pre-RoPE: angle tables (null when rope_theta == 0)
+  float2* rope_blk = nullptr;   // [ceil(max_context / 16)][D/2] cos, sin of 16 b theta_i
+  float2* rope_off = nullptr;   // [16][D/2] cos, sin of r theta_i
   // tile costs of the split-K partition
   int cost_b = 8, cost_q = 6;
   // timing

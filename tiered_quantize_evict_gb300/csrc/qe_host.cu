@@ -121,7 +121,7 @@ void free_all(qe_handle h) {
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_head, s.bfree_top,
                   s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
-                  h->tok_stage, h->diag};
+                  h->tok_stage, h->diag, h->rope_blk, h->rope_off};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -148,6 +148,9 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   if (c.tiering != QE_TIERING_WINDOWS && c.tiering != QE_TIERING_TOKENS)
     return fail(nullptr, QE_ERR_INVALID_ARG, "tiering must be QE_TIERING_WINDOWS or QE_TIERING_TOKENS");
   if (c.max_context < 1) return fail(nullptr, QE_ERR_INVALID_ARG, "bad max_context");
+  if (!(c.rope_theta >= 0.0)) return fail(nullptr, QE_ERR_INVALID_ARG, "rope_theta must be >= 0");
+  if (c.tiering == QE_TIERING_TOKENS && c.rope_theta != 0.0)
+    return fail(nullptr, QE_ERR_INVALID_ARG, "pre-RoPE keys are served by the window tiering only");
   if (c.tiering == QE_TIERING_TOKENS) {
     std::string err;
     qe_status ts = qe::tok_init(c, static_cast<cudaStream_t>(cuda_stream), out, err);
@@ -320,6 +323,29 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
     for (long long gu = 0; gu < GU; ++gu) bl[gu * st.capb] = make_int2(-1, 0);
     set(cudaMemcpy(st.blist, bl.data(), bl.size() * sizeof(int2), cudaMemcpyHostToDevice));
   }
+  if (c.rope_theta > 0.0) {
+    // angle tables in double precision, rounded once: theta_i = base^(-2i/d); block b holds
+    // the angle 16 b theta_i, offset r the angle r theta_i
+    // every 16-token block of every window slot (a tile is only read where it holds a valid row)
+    const int half = c.head_dim / 2, nblk = ceil_div(c.max_context, c.window) * (c.window / 16) + 1;
+    std::vector<float2> blk((size_t)nblk * half), off(16 * (size_t)half);
+    for (int i = 0; i < half; ++i) {
+      const double th = std::pow(c.rope_theta, -2.0 * i / c.head_dim);
+      for (int b = 0; b < nblk; ++b) {
+        const double a = 16.0 * b * th;
+        blk[(size_t)b * half + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+      }
+      for (int r = 0; r < 16; ++r) off[(size_t)r * half + i] = make_float2((float)std::cos(r * th), (float)std::sin(r * th));
+    }
+    void* pb = nullptr;
+    void* po = nullptr;
+    set(cudaMalloc(&pb, blk.size() * sizeof(float2)));
+    set(cudaMalloc(&po, off.size() * sizeof(float2)));
+    h->rope_blk = static_cast<float2*>(pb);
+    h->rope_off = static_cast<float2*>(po);
+    if (ie == cudaSuccess) set(cudaMemcpy(pb, blk.data(), blk.size() * sizeof(float2), cudaMemcpyHostToDevice));
+    if (ie == cudaSuccess) set(cudaMemcpy(po, off.data(), off.size() * sizeof(float2), cudaMemcpyHostToDevice));
+  }
   set(qe::prepare_attn_kernels(c.head_dim, c.window));
   set(qe::prepare_route_kernels(st));
   set(cudaStreamSynchronize(h->stream));
@@ -444,6 +470,8 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   p.part_o = h->part_o;
   p.part_ml = h->part_ml;
   p.lse = h->lse;
+  p.rope_blk = h->rope_blk;
+  p.rope_off = h->rope_off;
   {
     const int sub = c.window / 16;
     const int ntiles = nbw_of(h, m) * sub + m.n_quant;

@@ -24,6 +24,10 @@ struct AttnParams {
   float* part_o;         // [units][pslots][G][D] unnormalised output
   float2* part_ml;       // [units][pslots][G] (reference max, sum) in the log2 domain
   float* lse;            // [units][ntiles][G] per-tile log2-sum-exp
+  // keys stored pre-RoPE (null: no rotation): cos / sin of 16 b theta_i per 16-token block b
+  // [blocks][D/2], and of r theta_i per row offset r < 16 [16][D/2]
+  const float2* rope_blk;
+  const float2* rope_off;
 };
 
 // qe_attn_combine
