@@ -146,6 +146,38 @@ class QEvictUnit:
         self.t += 1
         return o, mass, sink_mass
 
+    # ------------------------------------------------------------------ speculative verify
+    def verify(self, qs, k_rows, v_rows):
+        """Draft tokens j = 0 .. n-1 are appended one by one and query j attends over the cache
+        and drafts 0 .. j; the masses are held back (H2O page §5, speculative decoding: a
+        rejected draft's score increments must not reach the scores).  Returns ([o_j], [mass_j])."""
+        n = len(qs)
+        self._verify = (self.L, n, [])
+        outs = []
+        for j in range(n):
+            self.append(k_rows[j], v_rows[j])
+            o, mass, _ = self.attend(qs[j])
+            outs.append(o)
+            self._verify[2].append(mass)
+        return outs, list(self._verify[2])
+
+    def commit(self, n_accept: int):
+        """Keep drafts 0 .. n_accept-1: the length becomes L0 + n_accept, windows opened by rejected
+        drafts close, and the accepted queries' masses are added in order (eq. (1), float32)."""
+        L0, n, masses = self._verify
+        assert 0 <= n_accept <= n
+        new_L = L0 + n_accept
+        last = (new_L + self.w - 1) // self.w          # windows [0, last) hold a token
+        for j in sorted(self.tier, reverse=True):
+            if j >= last and j * self.w >= L0:           # opened by a rejected draft
+                del self.tier[j]
+                self.S.pop(j, None)
+        self.L = new_L
+        for m in masses[:n_accept]:
+            self.accumulate(m)
+        self.t += n_accept
+        self._verify = None
+
     # ------------------------------------------------------------------ routing
     def quantize_window(self, j: int) -> QuantizedWindow:
         lo, hi = self.window_range(j)
