@@ -167,9 +167,12 @@ def run_ours(args):
     B, Lyr, Hq, Hkv, D = wl.batch, wl.n_layers, wl.n_q_heads, wl.n_kv_heads, wl.head_dim
     omega = wl.route_period
     K, W = args.steps, args.warmup
-    # decode steps: Omega pre-roll (all-bf16 cache, first routing event), W warm-up, K timed, K e2e
-    total_steps = omega + W + 3 * K
-    max_ctx = wl.prefill + max(wl.decode_steps, total_steps + omega)
+    NQ = max(1, args.verify)          # tokens per step: a speculative verify of NQ drafts, all kept
+    verify = args.verify > 0
+    pre = (omega + NQ - 1) // NQ      # steps through the first routing event
+    # steps: pre-roll (all-bf16 cache, first routing event), W warm-up, K timed, K roofline, K e2e
+    total_steps = pre + W + 3 * K
+    max_ctx = wl.prefill + max(wl.decode_steps, (total_steps + pre + 1) * NQ)
     stream = torch.cuda.Stream(dev)     # capturable: all work of this run is ordered on it
     torch.cuda.set_stream(stream)
     cache = qe.QECache(qe.config_from_workload(wl, max_context=max_ctx), stream.cuda_stream)
@@ -187,25 +190,45 @@ def run_ours(args):
 
     # per-step inputs, device resident
     def make_inputs(t):
-        k = torch.empty(Lyr, B, Hkv, 1, D, device=dev, dtype=torch.int16)
+        """Inputs of step t (1-based): tokens (t-1) NQ + j and their queries, j < NQ."""
+        if not verify:
+            k = torch.empty(Lyr, B, Hkv, 1, D, device=dev, dtype=torch.int16)
+            v = torch.empty_like(k)
+            q = torch.empty(Lyr, B, Hq, D, device=dev, dtype=torch.int16)
+            for layer in range(Lyr):
+                g.keys_values(layer, wl.prefill + t - 1, 1, k[layer], v[layer], stream.cuda_stream)
+                g.queries(layer, t, q[layer], stream.cuda_stream)
+            return k, v, q
+        k = torch.empty(Lyr, NQ, B, Hkv, D, device=dev, dtype=torch.int16)   # draft-major
         v = torch.empty_like(k)
-        q = torch.empty(Lyr, B, Hq, D, device=dev, dtype=torch.int16)
+        q = torch.empty(Lyr, NQ, B, Hq, D, device=dev, dtype=torch.int16)
         for layer in range(Lyr):
-            g.keys_values(layer, wl.prefill + t - 1, 1, k[layer], v[layer], stream.cuda_stream)
-            g.queries(layer, t, q[layer], stream.cuda_stream)
+            for j in range(NQ):
+                i = (t - 1) * NQ + j
+                g.keys_values(layer, wl.prefill + i, 1, k[layer, j].view(B, Hkv, 1, D),
+                              v[layer, j].view(B, Hkv, 1, D), stream.cuda_stream)
+                g.queries(layer, i + 1, q[layer, j], stream.cuda_stream)
         return k, v, q
 
-    out = torch.empty(B, Hq, D, device=dev, dtype=torch.float32)
+    out = torch.empty(NQ, B, Hq, D, device=dev, dtype=torch.float32) if verify else \
+        torch.empty(B, Hq, D, device=dev, dtype=torch.float32)
+
+    def routes_at(t):
+        return (t * NQ) // omega > ((t - 1) * NQ) // omega
 
     def step(t, k, v, q, o=out):
         for layer in range(Lyr):
-            cache.qe_append(layer, k[layer], v[layer], 1)
-            cache.qe_decode_step(layer, q[layer], o)
-        if t % omega == 0:
+            if verify:
+                cache.qe_verify(layer, q[layer], k[layer], v[layer], o, NQ)
+                cache.qe_verify_commit(layer, NQ)
+            else:
+                cache.qe_append(layer, k[layer], v[layer], 1)
+                cache.qe_decode_step(layer, q[layer], o)
+        if routes_at(t):
             cache.qe_route(-1)
 
     t = 0
-    for _ in range(omega + W):          # pre-roll through the first routing event, then warm-up
+    for _ in range(pre + W):            # pre-roll through the first routing event, then warm-up
         t += 1
         k, v, q = make_inputs(t)
         step(t, k, v, q)
@@ -223,13 +246,8 @@ def run_ours(args):
     with torch.cuda.graph(g_all, stream=stream, capture_error_mode="thread_local"):
         for i in range(K):
             tt = t + 1 + i
-            k, v, q = timed[i]
-            for layer in range(Lyr):
-                cache.qe_append(layer, k[layer], v[layer], 1)
-                cache.qe_decode_step(layer, q[layer], out)
-            if tt % omega == 0:
-                cache.qe_route(-1)
-                n_routes += 1
+            step(tt, *timed[i])
+            n_routes += routes_at(tt)
     graph_launches = cache.kernel_launches() - launches_before   # kernels the graph holds
     clocks = ClockSampler(local)
     clocks.start()
@@ -273,7 +291,7 @@ def run_ours(args):
     for i in range(K):
         k, v, q = make_inputs(t + 1 + i)
         host_in.append((k.cpu().pin_memory(), v.cpu().pin_memory(), q.cpu().pin_memory()))
-    host_out = torch.empty(B, Hq, D, dtype=torch.float32).pin_memory()
+    host_out = torch.empty(tuple(out.shape), dtype=torch.float32).pin_memory()
     h2d = sum(x.numel() * x.element_size() for x in host_in[0])
     d2h = host_out.numel() * host_out.element_size() * Lyr
     torch.cuda.synchronize(dev)
@@ -285,12 +303,7 @@ def run_ours(args):
     e2.record(stream)
     for i in range(K):
         t += 1
-        kh, vh, qh = host_in[i]
-        for layer in range(Lyr):
-            cache.qe_append(layer, kh[layer], vh[layer], 1)
-            cache.qe_decode_step(layer, qh[layer], host_out)
-        if t % omega == 0:
-            cache.qe_route(-1)
+        step(t, *host_in[i], o=host_out)
     e3.record(stream)
     torch.cuda.synchronize(dev)
     e2e_ms = max(e2.elapsed_time(e3), (time.perf_counter() - t_e2e0) * 1e3)
@@ -298,8 +311,8 @@ def run_ours(args):
 
     ms_total = max_over_ranks(ms_total, world, dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
-    value = whole_job_rate(B * K, world, ms_total)
-    e2e_val = whole_job_rate(B * K, world, e2e_ms)
+    value = whole_job_rate(B * NQ * K, world, ms_total)
+    e2e_val = whole_job_rate(B * NQ * K, world, e2e_ms)
     peak, peak_kind = _peaks()
     achieved = attn_bytes / (attn_ms / 1e3) / 1e9 if attn_ms > 0 else None
     info = cache.layer_info(0)
@@ -316,7 +329,7 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded qe_inputs generator, device-side)",
         "config": {
             **workload_config(wl, world),
-            "timed_decode_steps": [omega + W + 1, omega + W + K],
+            "timed_decode_steps": [pre + W + 1, pre + W + K],
             "launch": ("the K timed steps as one CUDA graph (per step %d layers x token append, attention, merge; "
                        "re-rank every Omega)" % Lyr) if tok else
                       ("the K timed steps as one CUDA graph (per step %d layers x attention with the token "
@@ -344,6 +357,11 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    if verify:
+        line["config"]["verify"] = {
+            "drafts_per_step": NQ, "accepted": "all",
+            "step": "per layer qe_verify of the drafts (each draft query attends over the cache and the "
+                    "drafts before it; masses held per query) then qe_verify_commit; value counts every draft"}
     cache.close()
     if world > 1:
         dist.destroy_process_group()
@@ -443,6 +461,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="profiling only: fewer layers than the workload")
     ap.add_argument("--batch", type=int, default=0, help="profiling only: other batch than the workload")
+    ap.add_argument("--verify", type=int, default=0,
+                    help="steps are speculative verifies of this many drafts per layer, all accepted")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

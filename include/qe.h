@@ -195,6 +195,30 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
  * All moves complete on the handle's stream before it runs anything else. */
 qe_status qe_route(qe_handle h, int layer);
 
+/* ---------------------------------------------------------------- speculative verify
+ * (window tiering; H2O page §5, speculative decoding: each draft query adds attention mass to
+ * older positions, so a rejected draft's score increments must be rolled back; here they are
+ * held aside and only the accepted ones are added).
+ *
+ * qe_verify appends n_q draft tokens one by one and runs draft query j over the cache and
+ * drafts 0..j, exactly as n_q decode steps would, except that each query's window masses are
+ * kept per query instead of being added to the scores.
+ *   q:   [n_q][batch][n_q_heads][head_dim] bf16 (draft-major: draft j's queries are contiguous)
+ *   k,v: [n_q][batch][n_kv_heads][head_dim] bf16
+ *   out: [n_q][batch][n_q_heads][head_dim] float32 (out_fp32) or bf16
+ * The layer then awaits qe_verify_commit; qe_append, qe_decode_step and qe_route on it fail
+ * with QE_ERR_STATE until then.  Pointer rules and flags as for qe_append / qe_decode_step.
+ * Errors: QE_ERR_INVALID_ARG (n_q outside 1..QE_VERIFY_MAX), QE_ERR_CAPACITY, QE_ERR_STATE. */
+#define QE_VERIFY_MAX 16
+qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const void* v, void* out, int n_q,
+                    int flags);
+
+/* Keep drafts 0..n_accept-1 of the pending verify (0 <= n_accept <= n_q): the length becomes
+ * L0 + n_accept, windows opened by rejected drafts close (their slots return to the free
+ * list), and the accepted queries' window masses are added to the scores in draft order
+ * (float32, as n_accept decode steps would have added them).  Stream-ordered. */
+qe_status qe_verify_commit(qe_handle h, int layer, int n_accept);
+
 /* Wait for the handle's stream and report the sticky device flag. */
 qe_status qe_synchronize(qe_handle h);
 

@@ -29,7 +29,9 @@ EXPORTED = [
     "qe_get_quant_window", "qe_get_bf16_window", "qe_get_route_stats", "qe_set_timing",
     "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc", "qe_get_route_diag",
     "qe_get_token_tiers", "qe_get_token_scores", "qe_get_token_counts", "qe_get_token",
+    "qe_verify", "qe_verify_commit",
 ]
+QE_VERIFY_MAX = 16
 QE_TIERING_WINDOWS, QE_TIERING_TOKENS = 0, 1
 TOK_BF16, TOK_INT4, TOK_INT2, TOK_NQ1, TOK_EVICTED, TOK_ABSENT = 0, 1, 2, 3, 4, 255
 
@@ -112,6 +114,8 @@ def load_library() -> ctypes.CDLL:
         "qe_get_token_scores": ([P, I, P, S], I),
         "qe_get_token_counts": ([P, I, P, S], I),
         "qe_get_token": ([P, I, I, I, ctypes.POINTER(I), P, P, P, P, P], I),
+        "qe_verify": ([P, I, P, P, P, P, I, I], I),
+        "qe_verify_commit": ([P, I, I], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -179,6 +183,14 @@ class QECache:
         if _is_host(q) or _is_host(out):
             raise ValueError("qe_decode_step_noalloc takes device tensors only")
         self._check(self._lib.qe_decode_step_noalloc(self.h, layer, _ptr(q), _ptr(out)))
+
+    def qe_verify(self, layer: int, q, k, v, out, n_q: int):
+        """Speculative verify of n_q drafts: q [n_q][B][Hq][D], k/v [n_q][B][Hkv][D], out [n_q][B][Hq][D]."""
+        flags = QE_HOST_PTRS if _is_host(q) else QE_DEVICE_PTRS
+        self._check(self._lib.qe_verify(self.h, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(out), n_q, flags))
+
+    def qe_verify_commit(self, layer: int, n_accept: int):
+        self._check(self._lib.qe_verify_commit(self.h, layer, n_accept))
 
     def qe_route(self, layer: int = -1):
         self._check(self._lib.qe_route(self.h, layer))

@@ -1025,7 +1025,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
 #pragma unroll
         for (int hh = 0; hh < 4; ++hh)
           if (hh < G) dS += ex2(ls[j][s2][hh] - s_lse[hh]);
-      p.st.score[gu * p.st.maxw + ent[j].x] = sc[j] + dS;
+      if (p.delta) p.delta[(long long)u * p.st.maxw + ent[j].x] = dS;
+      else p.st.score[gu * p.st.maxw + ent[j].x] = sc[j] + dS;
     }
   }
   // The last CTA to finish commits the new length: every CTA read the header when it started,

@@ -22,6 +22,8 @@ struct LayerMirror {
   int n_full = 0;
   int n_quant = 0;
   int kf = 0, kq = 0;
+  int verify_n = 0;    // > 0: a speculative verify of that many drafts awaits qe_verify_commit
+  int verify_L0 = 0;   // length before the drafts
 };
 
 // Host shadow of a five-tier layer.
@@ -61,6 +63,9 @@ struct qe_handle_s {
   // pinned host store
   void* hstore_host = nullptr;
   void* hledger_host = nullptr;
+  // speculative verify: window masses of each draft query, [n_layers][verify_cap][units][maxw]
+  float* vdelta = nullptr;
+  int verify_cap = 0;
   // keys stored pre-RoPE: angle tables (null when rope_theta == 0)
   float2* rope_blk = nullptr;   // [ceil(max_context / 16)][D/2] cos, sin of 16 b theta_i
   float2* rope_off = nullptr;   // [16][D/2] cos, sin of r theta_i

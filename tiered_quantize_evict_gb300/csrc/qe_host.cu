@@ -121,7 +121,7 @@ void free_all(qe_handle h) {
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_head, s.bfree_top,
                   s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
-                  h->tok_stage, h->diag, h->rope_blk, h->rope_off};
+                  h->tok_stage, h->diag, h->rope_blk, h->rope_off, h->vdelta};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -377,6 +377,7 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
   if (h && h->tok) return qe::tok_append(h, layer, k, v, n_tokens, flags);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
+  if (h->lay[layer].verify_n) return fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", layer);
   if (!k || !v || n_tokens < 1) return fail(h, QE_ERR_INVALID_ARG, "append needs K, V and n_tokens >= 1");
   LayerMirror& m = h->lay[layer];
   if (m.L + n_tokens > h->cfg.max_context)
@@ -424,10 +425,19 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
   return QE_OK;
 }
 
+static qe_status decode_impl(qe_handle h, int layer, const void* q, void* out, int flags, float* delta);
+
 qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int flags) {
   if (h && h->tok) return qe::tok_decode(h, layer, q, out, flags);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
+  if (h->lay[layer].verify_n) return fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", layer);
+  return decode_impl(h, layer, q, out, flags, nullptr);
+}
+
+// one decode step; delta non-null: the window masses go to delta (a speculative query)
+static qe_status decode_impl(qe_handle h, int layer, const void* q, void* out, int flags, float* delta) {
+  qe_status s;
   if (!q || !out) return fail(h, QE_ERR_INVALID_ARG, "decode needs q and out");
   LayerMirror& m = h->lay[layer];
   if (m.L < 1) return fail(h, QE_ERR_STATE, "decode on an empty layer");
@@ -517,13 +527,73 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
   cp.lse = h->lse;
   cp.out = od;
   cp.out_fp32 = c.out_fp32;
+  cp.delta = delta;
   QE_CK(h, qe::launch_attn_combine(cp, h->stream));
   ++h->launches;
   if (out_copy) QE_CK(h, cudaMemcpyAsync(out, od, obytes, cudaMemcpyDeviceToHost, h->stream));
   return QE_OK;
 }
 
+qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const void* v, void* out, int n_q,
+                    int flags) {
+  if (h && h->tok) return fail(h, QE_ERR_STATE, "speculative verify serves window-tiered handles");
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  LayerMirror& m = h->lay[layer];
+  if (m.verify_n) return fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", layer);
+  if (!q || !k || !v || !out || n_q < 1 || n_q > QE_VERIFY_MAX)
+    return fail(h, QE_ERR_INVALID_ARG, "verify needs q, k, v, out and 1 <= n_q <= %d", QE_VERIFY_MAX);
+  if (m.L < 1) return fail(h, QE_ERR_STATE, "verify on an empty layer");
+  const qe_config& c = h->cfg;
+  if (m.L + m.pending + n_q > c.max_context)
+    return fail(h, QE_ERR_CAPACITY, "%d drafts pass max_context %d", n_q, c.max_context);
+  if ((s = commit_pending(h, layer)) != QE_OK) return s;
+  if (n_q > h->verify_cap) {
+    // window masses of each draft query; grown outside any stream capture
+    if (h->vdelta) cudaFree(h->vdelta);
+    h->vdelta = nullptr;
+    h->verify_cap = 0;
+    QE_CK(h, cudaMalloc(&h->vdelta, (size_t)c.n_layers * n_q * h->units * h->st.maxw * sizeof(float)));
+    h->verify_cap = n_q;
+  }
+  const long long qstride = (long long)h->units * h->st.maxw;
+  float* dl = h->vdelta + (size_t)layer * h->verify_cap * qstride;
+  QE_CK(h, cudaMemsetAsync(dl, 0, (size_t)n_q * qstride * sizeof(float), h->stream));
+  const int D = c.head_dim;
+  const size_t kv_tok = (size_t)h->units * D * 2;                       // one draft's K (or V)
+  const size_t q_tok = (size_t)c.batch * c.n_q_heads * D * 2;           // one draft's queries
+  const size_t o_tok = (size_t)c.batch * c.n_q_heads * D * (c.out_fp32 ? 4 : 2);
+  m.verify_L0 = m.L;
+  for (int j = 0; j < n_q; ++j) {
+    const char* kj = static_cast<const char*>(k) + j * kv_tok;
+    const char* vj = static_cast<const char*>(v) + j * kv_tok;
+    if ((s = qe_append(h, layer, kj, vj, 1, flags)) != QE_OK) return s;
+    if ((s = decode_impl(h, layer, static_cast<const char*>(q) + j * q_tok, static_cast<char*>(out) + j * o_tok, flags,
+                         dl + j * qstride)) != QE_OK)
+      return s;
+  }
+  m.verify_n = n_q;
+  return QE_OK;
+}
+
+qe_status qe_verify_commit(qe_handle h, int layer, int n_accept) {
+  qe_status s = check_layer(h, layer);
+  if (s != QE_OK) return s;
+  LayerMirror& m = h->lay[layer];
+  if (!m.verify_n) return fail(h, QE_ERR_STATE, "layer %d has no verify to commit", layer);
+  if (n_accept < 0 || n_accept > m.verify_n)
+    return fail(h, QE_ERR_INVALID_ARG, "n_accept %d outside [0, %d]", n_accept, m.verify_n);
+  const long long qstride = (long long)h->units * h->st.maxw;
+  QE_CK(h, qe::launch_verify_commit(h->st, layer, m.verify_L0, m.verify_n, n_accept,
+                                    h->vdelta + (size_t)layer * h->verify_cap * qstride, qstride, h->stream));
+  ++h->launches;
+  m.L = m.verify_L0 + n_accept;
+  m.verify_n = 0;
+  return QE_OK;
+}
+
 static qe_status route_layer(qe_handle h, int layer) {
+  if (h->lay[layer].verify_n) return fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", layer);
   qe_status s0 = commit_pending(h, layer);
   if (s0 != QE_OK) return s0;
   LayerMirror& m = h->lay[layer];
@@ -634,6 +704,8 @@ qe_status qe_get_layer_info(qe_handle h, int layer, qe_layer_info* info) {
   m.n_quant = d.n_quant;
   m.kf = d.kf;
   m.kq = d.kq;
+  m.verify_n = h->lay[layer].verify_n;     // a pending verify stays pending
+  m.verify_L0 = h->lay[layer].verify_L0;
   h->lay[layer] = m;   // resynchronise the host shadow
   fill_info(h, m, info);
   return QE_OK;

@@ -42,6 +42,8 @@ struct CombineParams {
   const float* lse;
   void* out;             // [B][Hq][D] float32 or bf16
   int out_fp32;
+  float* delta;          // null: window masses are added to the scores; else written to
+                         // delta[unit][window] (a speculative query, committed later or dropped)
 };
 
 constexpr int COMBINE_MAXP = 256;   // partials one unit may receive
@@ -110,6 +112,8 @@ cudaError_t prepare_attn_kernels(int D, int W);
 cudaError_t prepare_route_kernels(const State& st);
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream);
 int attn_warps_per_cta();
+cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, int n_accept, const float* delta,
+                                 long long qstride, cudaStream_t s);
 cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
                           cudaStream_t s);
 cudaError_t launch_route(const RouteParams& p, cudaStream_t s);

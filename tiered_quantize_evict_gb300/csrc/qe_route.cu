@@ -827,6 +827,48 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
 }
 
 // ------------------------------------------------------------------------------ launchers
+// Commit of a speculative verify of n_q draft tokens from length L0 (H2O page §5, speculative
+// decoding): drafts [n_accept, n_q) are dropped -- the windows they opened close in reverse
+// opening order (their bf16 slots go back to the free list's head, from which they were taken;
+// the slot no longer holds an evicted window's exact data) -- and the accepted queries' window
+// masses are added to the scores in query order.  One CTA per unit; block 0 sets the length.
+__global__ void qe_verify_commit_kernel(State st, int layer, int L0, int n_q, int n_accept, const float* delta,
+                                        long long qstride) {
+  const int u = blockIdx.x;
+  const long long gu = (long long)layer * st.units + u;
+  const int W = st.geo.W;
+  const int new_L = L0 + n_accept, old_L = L0 + n_q;
+  const int first_opened = (L0 + W - 1) / W;             // windows starting at or after L0
+  const int new_nwin = (new_L + W - 1) / W, old_nwin = (old_L + W - 1) / W;
+  if (threadIdx.x == 0) {
+    for (int j = old_nwin - 1; j >= new_nwin && j >= first_opened; --j) {
+      const int s = st.bslot[gu * st.maxw + j];
+      const int head = st.bfree_head[gu] - 1;
+      if (s < 0 || s >= st.capb || head < 0 || st.bfree[gu * st.capb + head] != s) {
+        atomicOr(st.err, ERR_FREELIST);
+        break;
+      }
+      st.bfree_head[gu] = head;
+      st.bvictim[gu * st.capb + s] = -1;
+      st.bslot[gu * st.maxw + j] = -1;
+      st.tier[gu * st.maxw + j] = TIER_NONE;
+      st.score[gu * st.maxw + j] = 0.f;
+    }
+  }
+  for (int j = threadIdx.x; j < new_nwin; j += blockDim.x) {
+    float sc = st.score[gu * st.maxw + j];
+    for (int q = 0; q < n_accept; ++q) sc += delta[q * qstride + (long long)u * st.maxw + j];
+    st.score[gu * st.maxw + j] = sc;
+  }
+  if (u == 0 && threadIdx.x == 0) st.ldev[layer].L = new_L;
+}
+
+cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, int n_accept, const float* delta,
+                                 long long qstride, cudaStream_t s) {
+  qe_verify_commit_kernel<<<st.units, 128, 0, s>>>(st, layer, L0, n_q, n_accept, delta, qstride);
+  return cudaGetLastError();
+}
+
 cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
                           cudaStream_t s) {
   if (n == 1) {
