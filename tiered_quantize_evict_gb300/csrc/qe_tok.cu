@@ -994,9 +994,29 @@ __device__ __forceinline__ float tk_value_t(const uint8_t* tile, int tok, int c,
   return fmaf((float)code, par.y, par.x);
 }
 
-// Rows of one destination tile of the B-bit tier (1-bit: the normal quantizer): codes of rows that
-// keep their tier are moved, rows arriving from another tier are re-quantized from the values it
-// held.  Lane r < 16 holds row r's source (my_sz, my_si, my_id); `valid` marks rows present.
+// Field masks of the code words (layout in qe_tok.cuh): key side, the fields of row rr (0: row
+// g, 1: row g + 8) of lane 4 g + t; value side, the fields of token 2 t + hf + 8 rb.
+template <int B>
+__host__ __device__ constexpr unsigned tk_kmask(int rr) {
+  unsigned m = 0u;
+  for (int hf = 0; hf < 2; ++hf)
+    for (int k = 0; k < 4 / B; ++k)
+      for (int q = 0; q < 2; ++q) m |= ((1u << B) - 1u) << (16 * hf + B * (4 * k + rr + 2 * q));
+  return m;
+}
+template <int B>
+__host__ __device__ constexpr unsigned tk_vmask(int hf, int rb) {
+  unsigned m = 0u;
+  for (int k = 0; k < 4 / B; ++k)
+    for (int q = 0; q < 2; ++q) m |= ((1u << B) - 1u) << (16 * hf + B * (4 * k + 2 * rb + q));
+  return m;
+}
+
+// Rows of one destination tile of the B-bit tier (1-bit: the normal quantizer).  Rows that keep
+// their tier move word-wise: a row's fields sit in fixed lanes and bit positions, so moving it
+// from source row s to destination row d is a mask, a shift and an or per code word.  Rows
+// arriving from another tier are re-quantized from the values it held.  Lane r < 16 holds row
+// r's source (my_sz, my_si, my_id); `valid` marks rows present.
 template <int D, int B>
 __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, TkWarpBuf& W, uint8_t* dst,
                                  unsigned valid, int my_sz, int my_si, int my_id, int lane) {
@@ -1004,15 +1024,24 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
   constexpr float LEVELS = (float)((1 << B) - 1);
   constexpr int WPL = D * B / 64, CW = WPL < 4 ? WPL : 4, PW = 4 / B;
   const Geo g16{D, 16};
+  const int g = lane >> 2, t = lane & 3;
 #pragma unroll 1
   for (int half = 0; half < 2; ++half) {   // keys, then values
     const bool value = half == 1;
-    if (lane < 16) W.need[lane] = my_id >= 0 && my_sz != Z;
-    for (unsigned m = ~valid & 0xFFFFu; m; m &= m - 1) {
-      const int row = __ffs(m) - 1;
-      for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = 0;
-      if (lane == 0) W.par[row] = make_float2(0.f, 0.f);
+    const int NT = value ? 4 : 2;           // tokens whose fields this lane's words hold
+    int tok[4], tid[4], tsi[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      tok[i] = value ? 2 * t + (i & 1) + 8 * (i >> 1) : g + 8 * (i & 1);
+      tid[i] = __shfl_sync(0xffffffffu, my_id, tok[i]);
+      tsi[i] = __shfl_sync(0xffffffffu, my_si, tok[i]);
     }
+    if (lane < 16) W.need[lane] = my_id >= 0 && my_sz != Z;
+    if (lane < 16 && my_id < 0) W.par[lane] = make_float2(0.f, 0.f);
+    unsigned word[WPL];
+#pragma unroll
+    for (int j = 0; j < WPL; ++j) word[j] = 0u;
+    const int boff = value ? 2 * D * B : 0;
     // 1. gather, one staged source tile at a time
     unsigned todo = valid;
     while (todo) {
@@ -1020,25 +1049,50 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
       const unsigned grp = __ballot_sync(0xffffffffu, my_id == id) & todo;
       const uint8_t* st = tk_stage(W, s, layer, buf, u, id, lane);
       const int sz = id >> 28;
-      for (unsigned m = grp; m; m &= m - 1) {
-        const int row = __ffs(m) - 1;
-        const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
-        if (sz == Z) {
+      if (sz == Z) {
+        // word-wise moves of this lane's rows that come from the staged tile
 #pragma unroll
-          for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)tk_code_t<D, B>(st, srow, c, value);
-          if (lane == 0) W.par[row] = reinterpret_cast<const float2*>(st + 4 * D * B + (value ? 128 : 0))[srow];
-        } else if (sz == TK_BF16 || sz == TK_TAIL) {
-#pragma unroll
-          for (int c = lane; c < D; c += 32) {
-            const int off = value ? bf16_v_off(g16, srow, c) : bf16_k_off(g16, srow, c);
-            W.vals[row * TK_VROW + c] = __uint_as_float((unsigned)*reinterpret_cast<const uint16_t*>(st + off) << 16);
+        for (int i = 0; i < 4; ++i) {
+          if (i >= NT || tid[i] != id) continue;
+          const int sr = tsi[i] & 15;
+          int src_lane, sh;
+          unsigned mask;
+          if (!value) {
+            src_lane = 4 * (sr & 7) + t;
+            mask = (sr >> 3) ? tk_kmask<B>(1) : tk_kmask<B>(0);
+            sh = B * (i - (sr >> 3));
+          } else {
+            src_lane = 4 * g + ((sr & 7) >> 1);
+            const int hf_s = sr & 1, rb_s = sr >> 3;
+            mask = hf_s ? (rb_s ? tk_vmask<B>(1, 1) : tk_vmask<B>(1, 0)) : (rb_s ? tk_vmask<B>(0, 1) : tk_vmask<B>(0, 0));
+            sh = 16 * ((i & 1) - hf_s) + 2 * B * ((i >> 1) - rb_s);
           }
-        } else if (sz == TK_INT4) {
 #pragma unroll
-          for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_t<D, 4>(st, srow, c, value);
-        } else {   // 2-bit (a token only moves down, so a 1-bit source never reaches another tier)
+          for (int j = 0; j < WPL; ++j) {
+            const unsigned sw = *reinterpret_cast<const unsigned*>(st + boff + ((j / CW) * 32 + src_lane) * (CW * 4) +
+                                                                   (j % CW) * 4) & mask;
+            word[j] |= sh >= 0 ? sw << sh : sw >> (-sh);
+          }
+        }
+        if (lane < 16 && my_id == id)
+          W.par[lane] = reinterpret_cast<const float2*>(st + 4 * D * B + (value ? 128 : 0))[my_si & 15];
+      } else {
+        for (unsigned m = grp; m; m &= m - 1) {
+          const int row = __ffs(m) - 1;
+          const int srow = __shfl_sync(0xffffffffu, my_si, row) & 15;
+          if (sz == TK_BF16 || sz == TK_TAIL) {
 #pragma unroll
-          for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_t<D, 2>(st, srow, c, value);
+            for (int c = lane; c < D; c += 32) {
+              const int off = value ? bf16_v_off(g16, srow, c) : bf16_k_off(g16, srow, c);
+              W.vals[row * TK_VROW + c] = __uint_as_float((unsigned)*reinterpret_cast<const uint16_t*>(st + off) << 16);
+            }
+          } else if (sz == TK_INT4) {
+#pragma unroll
+            for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_t<D, 4>(st, srow, c, value);
+          } else {   // 2-bit (a token only moves down, so a 1-bit source never reaches another tier)
+#pragma unroll
+            for (int c = lane; c < D; c += 32) W.vals[row * TK_VROW + c] = tk_value_t<D, 2>(st, srow, c, value);
+          }
         }
       }
       todo &= ~grp;
@@ -1096,27 +1150,37 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
       }
     }
     __syncwarp();
-    // 3. pack this lane's words and write the block and its parameters
-    uint8_t* blk = dst + (value ? 2 * D * B : 0);
+    // 3. the fields of this lane's re-quantized tokens, then the words and the parameters
 #pragma unroll
-    for (int j = 0; j < WPL; ++j) {
-      unsigned word = 0u;
+    for (int i = 0; i < 4; ++i) {
+      if (i >= NT || !W.need[tok[i]]) continue;
+      const int tk = tok[i];
 #pragma unroll
-      for (int kk = 0; kk < PW; ++kk) {
-        const int step = j * PW + kk;
+      for (int j = 0; j < WPL; ++j)
 #pragma unroll
-        for (int r = 0; r < 4; ++r)
+        for (int kk = 0; kk < PW; ++kk) {
+          const int step = j * PW + kk;
 #pragma unroll
-          for (int hf = 0; hf < 2; ++hf) {
-            const int row16 = (lane >> 2) + 8 * (r & 1);
-            const int col16 = ((lane & 3) << 1) + hf + 8 * (r >> 1);
-            const int tok = value ? col16 : row16;
-            const int ch = 16 * step + (value ? row16 : col16);
-            word |= (unsigned)W.codes[tok * 128 + ch] << (16 * hf + B * (4 * kk + r));
+          for (int q = 0; q < 2; ++q) {
+            if (!value) {   // row tk = g + 8 i: registers r = i + 2 q, both halves
+              const int r = i + 2 * q;
+#pragma unroll
+              for (int hf = 0; hf < 2; ++hf) {
+                const int ch = 16 * step + 2 * t + hf + 8 * q;
+                word[j] |= (unsigned)W.codes[tk * 128 + ch] << (16 * hf + B * (4 * kk + r));
+              }
+            } else {        // token tk = 2 t + hf + 8 rb: registers r = 2 rb + q (rows g + 8 q), half hf
+              const int hf = i & 1, r = 2 * (i >> 1) + q;
+              const int ch = 16 * step + g + 8 * q;
+              word[j] |= (unsigned)W.codes[tk * 128 + ch] << (16 * hf + B * (4 * kk + r));
+            }
           }
-      }
-      *reinterpret_cast<unsigned*>(blk + ((j / CW) * 32 + lane) * (CW * 4) + (j % CW) * 4) = word;
+        }
     }
+    uint8_t* blk = dst + boff;
+#pragma unroll
+    for (int j = 0; j < WPL; ++j)
+      *reinterpret_cast<unsigned*>(blk + ((j / CW) * 32 + lane) * (CW * 4) + (j % CW) * 4) = word[j];
     if (lane < 16) reinterpret_cast<float2*>(dst + 4 * D * B + (value ? 128 : 0))[lane] = W.par[lane];
     __syncwarp();
   }
