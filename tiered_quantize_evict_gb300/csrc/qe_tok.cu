@@ -1190,7 +1190,7 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
 // tiers: TK_REBUILD_SPLIT CTAs per unit share its destination tiles, one tile per warp at a time.
 // A destination tile's rows (position order) come from few source tiles: the warp stages each
 // distinct source tile once in shared memory and serves every row that reads from it.
-constexpr int TK_REBUILD_SPLIT = 4;
+constexpr int TK_REBUILD_SPLIT = 7;
 
 template <int D>
 __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const TokState s, int layer) {
