@@ -34,6 +34,7 @@ constexpr int TK_STAGE_TOTAL = 196608;
 constexpr unsigned long long TK_WAIT_NS = 200000000ull;   // 0.2 s
 constexpr float TK_NQ1_C = 0.67448975f;                   // Phi^-1(3/4) rounded to float32
 constexpr int TK_MERGE_THREADS = 512;
+constexpr int TK_MERGE_SPLIT = 4;       // CTAs per unit: each takes a quarter of the outputs and tokens
 constexpr int TK_RERANK_THREADS = 256;
 constexpr int TK_RERANK_WARPS = TK_RERANK_THREADS / 32;
 
@@ -644,7 +645,7 @@ struct TkMergeArgs {
   int out_fp32;
 };
 
-// One CTA per unit: merge the partials of the warps whose ranges met the unit, write o_h, and on
+// TK_MERGE_SPLIT CTAs per unit: merge the partials of the warps whose ranges met the unit, write o_h, and on
 // scoring steps add each token's mass (sum over the G heads of 2^(logit - lse_h)) to its score.
 // A programmatic dependent of the attention launch.  The last CTA commits the appended token.
 template <int D>
@@ -653,7 +654,8 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
   __shared__ float s_inv[4], s_lse[4];
   __shared__ bool s_last;
   const TokState& S = p.st;
-  const int u = blockIdx.x, tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int u = blockIdx.x / TK_MERGE_SPLIT, part = blockIdx.x - u * TK_MERGE_SPLIT;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int G = S.G;
   const TokLayer hd = S.hdr[p.layer];
   const int n_tail = hd.n_tail + p.pend;
@@ -687,7 +689,9 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
     }
   }
   __syncthreads();
-  for (int e = tid; e < G * D; e += TK_MERGE_THREADS) {
+  const int e_per = (G * D + TK_MERGE_SPLIT - 1) / TK_MERGE_SPLIT;
+  const int e_end = (part + 1) * e_per < G * D ? (part + 1) * e_per : G * D;
+  for (int e = part * e_per + tid; e < e_end; e += TK_MERGE_THREADS) {
     const int h = e / D, c = e - h * D;
     float acc = 0.f;
     for (int k0 = 0; k0 < np; k0 += 16) {   // 16 partial loads in flight
@@ -714,14 +718,17 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
       if (z < 4) sc = S.score[z] + tk_pool_tok_index(S, z, p.layer, hd.buf, u);
       else sc = S.tail_score + tk_tail_tok_index(S, p.layer, hd.buf, u);
       const int first = z < 4 ? 0 : S.n_sink;   // sink tokens are never scored
-      for (int i0 = first + tid; i0 < un.n[z]; i0 += 4 * TK_MERGE_THREADS) {   // 4 tokens in flight
+      const int per = (un.n[z] - first + TK_MERGE_SPLIT - 1) / TK_MERGE_SPLIT;
+      const int lo = first + part * per;
+      const int hi = lo + per < un.n[z] ? lo + per : un.n[z];
+      for (int i0 = lo + tid; i0 < hi; i0 += 4 * TK_MERGE_THREADS) {   // 4 tokens in flight
         float m[4], old[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int i = i0 + j * TK_MERGE_THREADS;
           m[j] = 0.f;
           old[j] = 0.f;
-          if (i < un.n[z]) {
+          if (i < hi) {
             const float* lg = lgu + (long long)(un.tok0[z] + i) * G;
             for (int h = 0; h < G; ++h) m[j] += ex2(__ldg(lg + h) - s_lse[h]);
             old[j] = sc[i];
@@ -730,7 +737,7 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int i = i0 + j * TK_MERGE_THREADS;
-          if (i < un.n[z]) sc[i] = old[j] + m[j];
+          if (i < hi) sc[i] = old[j] + m[j];
         }
       }
     }
@@ -740,7 +747,7 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
   if (tid == 0) {
     __threadfence();
     const unsigned prev = atomicAdd(S.done + p.layer, 1u);
-    s_last = prev == (unsigned)S.units - 1;
+    s_last = prev == (unsigned)(S.units * TK_MERGE_SPLIT) - 1;
   }
   __syncthreads();
   if (s_last && tid == 0) {
@@ -1440,7 +1447,7 @@ cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float*
   m.out = out;
   m.out_fp32 = out_fp32;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(s.units);
+  cfg.gridDim = dim3(s.units * TK_MERGE_SPLIT);
   cfg.blockDim = dim3(TK_MERGE_THREADS);
   cfg.dynamicSmemBytes = (size_t)s.G * (m.NW + 2) * sizeof(float);
   cfg.stream = st;
