@@ -271,6 +271,9 @@ typedef struct {
                               contents no other window had overwritten (no host read) */
   long long int2_reclaims; /* re-demotions that took back their previous 2-bit slot (no
                               host read of the ledger) */
+  long long ledger_writes; /* ledgers written to the host store: a window's codes are saved
+                              only when the 2-bit slot still holding them is handed to another
+                              window while the window is kept */
 } qe_route_stats;
 
 /* Cumulative routing counters of one layer (layer = -1: summed); synchronous. */

@@ -1,5 +1,7 @@
 """The router on chosen scores (GPU): exact tiers under heavy ties, ledger reuse across
-demote/promote cycles, exact bf16 restore on promotion, pool bookkeeping."""
+demote/promote cycles (codes taken back from a freed 2-bit slot, and codes saved to the host
+ledger when their slot is handed to another window, then read back), exact bf16 restore on
+promotion, pool bookkeeping."""
 import dataclasses
 
 import numpy as np
@@ -30,8 +32,9 @@ def test_router_cycles_with_ties():
     info = cache.layer_info(0)
     units, maxw = info.units, info.max_windows
     kept_before = {}
-    for event in range(6):
-        S = _scores(event, units, maxw, levels=3 + event)
+    n_events = 12
+    for event in range(n_events):
+        S = _scores(event, units, maxw, levels=3 + event % 6)
         # windows that are evicted keep their (irrelevant) scores; the oracle sees the same floats
         cache.set_scores(0, S)
         for tr in run.tracked:
@@ -49,5 +52,9 @@ def test_router_cycles_with_ties():
             run.check_bf16_windows(tr)
     cache.qe_synchronize()
     st = cache.route_stats(0)
-    assert st.routes == 6 and st.promotions > 0 and st.ledger_reuses > 0 and st.evictions > 0
+    assert st.routes == n_events and st.promotions > 0 and st.ledger_reuses > 0 and st.evictions > 0
+    # both ledger paths ran: codes taken back from their old slot, and codes saved to the host
+    # ledger before their slot was reused, later read back by a re-demotion (checked above)
+    assert st.int2_reclaims > 0 and st.ledger_writes > 0
+    assert st.ledger_reuses > st.int2_reclaims
     assert run.codes_checked > 0

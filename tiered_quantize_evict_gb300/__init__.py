@@ -62,7 +62,7 @@ class QERouteStats(ctypes.Structure):
     _fields_ = [("routes", ctypes.c_longlong), ("first_packs", ctypes.c_longlong),
                 ("ledger_reuses", ctypes.c_longlong), ("promotions", ctypes.c_longlong),
                 ("evictions", ctypes.c_longlong), ("bf16_reclaims", ctypes.c_longlong),
-                ("int2_reclaims", ctypes.c_longlong)]
+                ("int2_reclaims", ctypes.c_longlong), ("ledger_writes", ctypes.c_longlong)]
 
 
 class QERouteDiag(ctypes.Structure):

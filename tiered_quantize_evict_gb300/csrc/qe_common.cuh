@@ -33,7 +33,7 @@ enum : int { TIER_NONE = 0, TIER_PINNED = 1, TIER_FULL = 2, TIER_QUANT = 3, TIER
 
 // routing counters per layer: routes, first packs, ledger reuses, promotions, evictions, and
 // promotions / re-demotions that took their previous slot back (no host transfer)
-constexpr int N_STATS = 7;
+constexpr int N_STATS = 8;
 
 enum : unsigned { ERR_FREELIST = 1u, ERR_TABLE = 2u, ERR_TIMEOUT = 4u, ERR_COUNT = 8u, ERR_MOVES = 16u,
                   ERR_CAPACITY = 32u };

@@ -188,7 +188,10 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   st.n_layers = c.n_layers;
   st.maxw = maxw;
   st.capb = 1 + maxw;
-  st.capq = kq_max > 0 ? kq_max : 1;
+  // the 2-bit slab holds K_q windows plus slack: a freed slot keeps its window's codes until it
+  // is handed out again (oldest first), so a window that returns soon takes its codes back and
+  // a kept window's ledger reaches the host only when its codes are about to be overwritten
+  st.capq = kq_max > 0 ? kq_max + (kq_max / 2 > 16 ? kq_max / 2 : 16) : 1;
   st.caps = (kf_max + kq_max) > 0 ? kf_max + kq_max : 1;
   if (st.caps > maxw) st.caps = maxw;
   if (st.capq > maxw) st.capq = maxw;
@@ -250,7 +253,15 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(h->lse, (size_t)h->units * h->ntiles_cap * G, "tile log-sum-exp");
   QE_ALLOC(h->diag, (size_t)c.n_layers * h->units, "routing records");
   QE_ALLOC(h->tok_stage, (size_t)c.n_layers * 2 * h->units * c.head_dim, "token staging");
-  h->max_moves = h->units * st.caps + 16;
+  {
+    const long long mm = (long long)c.n_layers * h->units * st.caps + 16;   // one event of every layer
+    if (mm > 0x7FFFFFFFLL) {
+      free_all(h);
+      delete h;
+      return fail(nullptr, QE_ERR_OOM, "move list of %lld entries exceeds the int range", mm);
+    }
+    h->max_moves = (int)mm;
+  }
   {
     void* mp = nullptr;
     if (cudaMalloc(&mp, (size_t)h->max_moves * sizeof(qe::Move)) != cudaSuccess) {
@@ -592,11 +603,13 @@ qe_status qe_verify_commit(qe_handle h, int layer, int n_accept) {
   return QE_OK;
 }
 
-static qe_status route_layer(qe_handle h, int layer) {
+// Checks one layer before a routing event and returns its new mirror values; launches nothing
+// but the commit of a pending append.
+static qe_status route_check(qe_handle h, int layer, LayerMirror& next) {
   if (h->lay[layer].verify_n) return fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", layer);
   qe_status s0 = commit_pending(h, layer);
   if (s0 != QE_OK) return s0;
-  LayerMirror& m = h->lay[layer];
+  const LayerMirror& m = h->lay[layer];
   const qe_config& c = h->cfg;
   int aged = (m.L - c.n_recent) >= 0 ? (m.L - c.n_recent) / c.window : 0;
   if (aged < m.routed_upto) aged = m.routed_upto;
@@ -607,38 +620,45 @@ static qe_status route_layer(qe_handle h, int layer) {
   const int nf = kf < ncand ? kf : ncand;
   const int nq = kq < ncand - nf ? kq : ncand - nf;
   if (nf + nq > h->st.caps) return fail(h, QE_ERR_CAPACITY, "kept windows %d exceed the host store (%d)", nf + nq, h->st.caps);
+  next = m;
+  next.routed_upto = aged;
+  next.n_full = nf;
+  next.n_quant = nq;
+  next.kf = kf;
+  next.kq = kq;
+  return QE_OK;
+}
+
+// Routes layers [l0, l0 + n): every layer is checked first (nothing is routed if one fails),
+// then one route launch covers all of them and one move launch carries out their moves.
+static qe_status route_layers(qe_handle h, int l0, int n) {
+  std::vector<LayerMirror> next((size_t)n);
+  for (int i = 0; i < n; ++i) {
+    qe_status s = route_check(h, l0 + i, next[(size_t)i]);
+    if (s != QE_OK) return s;
+  }
   qe::RouteParams p{};
   p.st = h->st;
-  p.layer = layer;
+  p.layer = l0;
   p.moves = h->moves;
   p.n_moves = h->n_moves;
   p.max_moves = h->max_moves;
   p.diag = h->diag;
   QE_CK(h, cudaMemsetAsync(h->n_moves, 0, 4, h->stream));
-  QE_CK(h, qe::launch_route(p, h->stream));
+  QE_CK(h, qe::launch_route(p, n, h->stream));
   QE_CK(h, qe::launch_moves(h->st, h->moves, h->n_moves, h->n_sm, h->stream));
   h->launches += 2;
-  m.routed_upto = aged;
-  m.n_full = nf;
-  m.n_quant = nq;
-  m.kf = kf;
-  m.kq = kq;
+  for (int i = 0; i < n; ++i) h->lay[(size_t)(l0 + i)] = next[(size_t)i];
   return QE_OK;
 }
 
 qe_status qe_route(qe_handle h, int layer) {
   if (!h) return QE_ERR_INVALID_ARG;
   if (h->tok) return qe::tok_route(h, layer);
-  if (layer == -1) {
-    for (int l = 0; l < h->cfg.n_layers; ++l) {
-      qe_status s = route_layer(h, l);
-      if (s != QE_OK) return s;
-    }
-    return QE_OK;
-  }
+  if (layer == -1) return route_layers(h, 0, h->cfg.n_layers);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
-  return route_layer(h, layer);
+  return route_layers(h, layer, 1);
 }
 
 qe_status qe_synchronize(qe_handle h) {
@@ -838,6 +858,7 @@ qe_status qe_get_route_stats(qe_handle h, int layer, qe_route_stats* out) {
   out->evictions = a[4];
   out->bf16_reclaims = a[5];
   out->int2_reclaims = a[6];
+  out->ledger_writes = a[7];
   return QE_OK;
 }
 

@@ -65,10 +65,15 @@ struct Move {
   int win;
   int src;     // pack / copy: bf16 slot; reuse / promotion: store entry
   int dst;     // pack / reuse: 2-bit slot; promotion: bf16 slot; copy: store entry
-  int sent;    // pack: store entry (ledger, and the exact copy for MOVE_PACK_COPY)
+  int sent;    // pack: store entry (the exact copy for MOVE_PACK_COPY)
+  int wb;      // pack / reuse: store entry whose ledger receives the 2-bit slot's previous codes
+               // before the slot is overwritten, or -1
 };
-// bit of a window's store entry number that says its ledger (2-bit codes) exists
+// bits of a window's store entry number: its 2-bit codes exist (packed once, held by a 2-bit
+// slot or by the host ledger), and the host ledger entry holds them
+constexpr int SENT_PACKED = 1 << 29;
 constexpr int SENT_LEDGER = 1 << 30;
+constexpr int SENT_FLAGS = SENT_PACKED | SENT_LEDGER;
 
 #if defined(__CUDACC__)
 // Open window j of unit gu when its first token arrives: take the next free bf16 slot, Pinned,
@@ -116,7 +121,8 @@ cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, in
                                  long long qstride, cudaStream_t s);
 cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
                           cudaStream_t s);
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s);
+// routes layers [p.layer, p.layer + n_layers) in one launch
+cudaError_t launch_route(const RouteParams& p, int n_layers, cudaStream_t s);
 cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t s);
 cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves, int n_sm, cudaStream_t s);
 

@@ -135,77 +135,113 @@ __global__ void qe_append_kernel(State st, int layer, int n, const uint16_t* __r
 constexpr int ROUTE_THREADS = 256;
 constexpr int ROUTE_MAX_CAND = 4096;
 
+// Block-wide exclusive prefix sum of one value per thread (ROUTE_THREADS threads, every thread
+// calls it); returns this thread's prefix and sets *total.  s_w: ROUTE_THREADS / 32 + 1 ints of
+// shared scratch, free again when the call returns.
+__device__ int block_scan(int v, int* s_w, int* total) {
+  const int tid = threadIdx.x, lane = tid & 31, wid = tid >> 5;
+  int x = v;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31) s_w[wid] = x;
+  __syncthreads();
+  if (wid == 0) {
+    int w = lane < ROUTE_THREADS / 32 ? s_w[lane] : 0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const int y = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += y;
+    }
+    if (lane < ROUTE_THREADS / 32) s_w[lane] = w;   // inclusive warp totals
+  }
+  __syncthreads();
+  const int excl = (wid ? s_w[wid - 1] : 0) + x - v;
+  *total = s_w[ROUTE_THREADS / 32 - 1];
+  __syncthreads();
+  return excl;
+}
+
 // Block-wide: write front[0, nf) and then the entries of rest[0, nr) whose slot is flagged free,
 // in order, to dst (at most cap entries; more is a free-list error).  Returns the count on every
 // thread.
 __device__ int compact_free(const int* front, int nf, const int* rest, int nr, const uint8_t* flag, int* dst,
-                            int cap, int* s_cnt, unsigned* err) {
-  __shared__ int s_total;
+                            int cap, int* s_w, unsigned* err) {
   const int tid = threadIdx.x;
   const int per = (nr + ROUTE_THREADS - 1) / ROUTE_THREADS;
   const int i0 = tid * per, i1 = min(i0 + per, nr);
   auto keep = [&](int sl) { return sl >= 0 && sl < cap && flag[sl] != 0; };
   int cnt = 0;
   for (int i = i0; i < i1; ++i) cnt += keep(rest[i]);
-  s_cnt[tid] = cnt;
-  __syncthreads();
-  if (tid == 0) {
-    int acc = nf;
-    for (int t = 0; t < ROUTE_THREADS; ++t) {
-      const int c = s_cnt[t];
-      s_cnt[t] = acc;
-      acc += c;
-    }
-    if (acc > cap) atomicOr(err, ERR_FREELIST);
-    s_total = acc < cap ? acc : cap;
-  }
-  __syncthreads();
+  int kept;
+  int o = nf + block_scan(cnt, s_w, &kept);
+  const int acc = nf + kept;
+  if (tid == 0 && acc > cap) atomicOr(err, ERR_FREELIST);
   for (int i = tid; i < nf && i < cap; i += ROUTE_THREADS) dst[i] = front[i];
-  int o = s_cnt[tid];
   for (int i = i0; i < i1; ++i)
     if (keep(rest[i])) {
       if (o < cap) dst[o] = rest[i];
       ++o;
     }
-  const int total = s_total;
-  __syncthreads();   // s_cnt and s_total are reused by the next call
-  return total;
+  return acc < cap ? acc : cap;
 }
 
-// One CTA per unit.  Shared memory: sort keys, the changed windows' table entries, the free lists.
+// Candidate capacity of one unit's event: every candidate is a window below the current count,
+// so the table's window capacity bounds it (and ROUTE_MAX_CAND bounds the shared memory).
+__host__ __device__ inline int route_cand_cap(const State& st) {
+  return st.maxw < ROUTE_MAX_CAND ? st.maxw : ROUTE_MAX_CAND;
+}
+// sort-key array length: the candidate capacity rounded up to a power of two
+__host__ __device__ inline int route_key_cap(const State& st) {
+  int k = 1;
+  while (k < route_cand_cap(st)) k <<= 1;
+  return k;
+}
+
+// One CTA per (unit, layer): blockIdx.x = unit, layer = p.layer + blockIdx.y, so one launch
+// routes a run of layers.  Shared memory: sort keys, the changed windows' table entries, the
+// free lists.
 __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RouteParams p) {
   extern __shared__ __align__(16) uint8_t sm[];
   const State& st = p.st;
   const int u = blockIdx.x;
-  const long long gu = (long long)p.layer * st.units + u;
+  const int layer = p.layer + (int)blockIdx.y;
+  const long long gu = (long long)layer * st.units + u;
+  const int CC = route_cand_cap(st);
   // Changed windows carry a shared-memory copy of their table entries (old tier, bf16 slot,
   // 2-bit slot, store entry), so the serial bookkeeping below touches no global memory.
-  unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm);              // ROUTE_MAX_CAND
-  int* ch_win = reinterpret_cast<int*>(keys + ROUTE_MAX_CAND);                       // ROUTE_MAX_CAND
-  int* ch_b = ch_win + ROUTE_MAX_CAND;                                               // ROUTE_MAX_CAND
-  int* ch_q = ch_b + ROUTE_MAX_CAND;                                                 // ROUTE_MAX_CAND
-  int* ch_s = ch_q + ROUTE_MAX_CAND;                                                 // ROUTE_MAX_CAND
-  int* ch_bv = ch_s + ROUTE_MAX_CAND;      // previous bf16 slot still holding the window, or -1
-  int* ch_qv = ch_bv + ROUTE_MAX_CAND;     // previous 2-bit slot still holding the window, or -1
-  uint8_t* ch_new = reinterpret_cast<uint8_t*>(ch_qv + ROUTE_MAX_CAND);              // ROUTE_MAX_CAND
-  uint8_t* ch_old = ch_new + ROUTE_MAX_CAND;                                         // ROUTE_MAX_CAND
+  unsigned long long* keys = reinterpret_cast<unsigned long long*>(sm);              // route_key_cap
+  int* ch_win = reinterpret_cast<int*>(keys + route_key_cap(st));                    // CC
+  int* ch_b = ch_win + CC;                                                           // CC
+  int* ch_q = ch_b + CC;                                                             // CC
+  int* ch_s = ch_q + CC;                                                             // CC
+  int* ch_bv = ch_s + CC;                  // previous bf16 slot still holding the window, or -1
+  int* ch_qv = ch_bv + CC;                 // previous 2-bit slot still holding the window, or -1
+  const int CC16 = (CC + 15) & ~15;
+  uint8_t* ch_new = reinterpret_cast<uint8_t*>(ch_qv + CC);                          // CC16
+  uint8_t* ch_old = ch_new + CC16;                                                   // CC16
   // free lists: the current entries (next to hand out first), then slots freed at the back;
   // slots freed at the front apart; a flag per slot says whether it is free
-  int* bfa = reinterpret_cast<int*>(ch_old + ROUTE_MAX_CAND);                        // 2 capb
+  int* bfa = reinterpret_cast<int*>(ch_old + CC16);                                  // 2 capb
   int* bfront = bfa + 2 * st.capb;                                                   // capb
   int* qfa = bfront + st.capb;                                                       // 2 capq
   int* qfront = qfa + 2 * st.capq;                                                   // capq
   int* sstack = qfront + st.capq;                                                    // caps
-  uint8_t* bflag = reinterpret_cast<uint8_t*>(sstack + st.caps);                     // capb
+  // per 2-bit slot: the change-list index of the window promoted in this event whose codes the
+  // slot still holds, else -1 (its store entry's flags then live in ch_s, not in the table)
+  int* qch = sstack + st.caps;                                                       // capq
+  uint8_t* bflag = reinterpret_cast<uint8_t*>(qch + st.capq);                        // capb
   uint8_t* qflag = bflag + st.capb;                                                  // capq
   __shared__ int s_n, s_nch, s_pos[8];
   __shared__ int s_diag[9];   // full old/new/both, kept old/new/both, promotions, demotions, evictions
   __shared__ float s_cut[4];  // scores at the two cuts (read before the keys are reused)
-  __shared__ int s_cnt2[ROUTE_THREADS];
+  __shared__ int s_w[ROUTE_THREADS / 32 + 1];
 
   const int tid = threadIdx.x;
   // this event's geometry and capacities, from the device-resident header (identical in every CTA)
-  const LayerDev hd = st.ldev[p.layer];
+  const LayerDev hd = st.ldev[layer];
   const int W = st.geo.W;
   const int L = hd.L;
   const int n_windows = (L + W - 1) / W;
@@ -216,7 +252,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   const int ncand = hd.n_full + hd.n_quant + (aged_upto - hd.routed_upto);
   const int exp_nfull = kf < ncand ? kf : ncand;
   const int exp_nquant = kq < ncand - exp_nfull ? kq : ncand - exp_nfull;
-  const bool fits = exp_nquant <= st.capq && exp_nfull + exp_nquant <= st.caps && ncand <= ROUTE_MAX_CAND;
+  const bool fits = exp_nquant <= st.capq && exp_nfull + exp_nquant <= st.caps && ncand <= CC;
   if (tid == 0) { s_n = 0; s_nch = 0; }
   if (tid < 9) s_diag[tid] = 0;
   __syncthreads();
@@ -232,7 +268,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     const bool cand = (z == TIER_FULL) || (z == TIER_QUANT) || (z == TIER_PINNED && j >= hd.routed_upto);
     if (cand) {
       const int pos = atomicAdd(&s_n, 1);
-      if (pos < ROUTE_MAX_CAND) {
+      if (pos < CC) {
         // ascending key order = score descending, then window ascending (scores are >= 0)
         const unsigned sb = __float_as_uint(score[j]);
         keys[pos] = ((unsigned long long)(0xFFFFFFFFu - sb) << 32) | (unsigned)j;
@@ -240,8 +276,8 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     }
   }
   __syncthreads();
-  if (tid == 0 && s_n > ROUTE_MAX_CAND) atomicOr(st.err, ERR_COUNT);
-  const int n = s_n < ROUTE_MAX_CAND ? s_n : ROUTE_MAX_CAND;
+  if (tid == 0 && s_n > CC) atomicOr(st.err, ERR_COUNT);
+  const int n = s_n < CC ? s_n : CC;
   int npow = 1;
   while (npow < n) npow <<= 1;
   for (int i = n + tid; i < npow; i += ROUTE_THREADS) keys[i] = ~0ull;
@@ -269,9 +305,11 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   int* qsl = st.qslot + gu * st.maxw;
   int* sen = st.sent + gu * st.maxw;
   int dg[9] = {0, 0, 0, 0, 0, 0, 0, 0, 0};   // this thread's share of the event record
+  auto new_tier = [&](int r) { return r < kf ? TIER_FULL : (r < kf + kq ? TIER_QUANT : TIER_EVICTED); };
+  int myc = 0;
   for (int r = tid; r < n; r += ROUTE_THREADS) {
     const int j = (int)(keys[r] & 0xFFFFFFFFu);
-    const int nt = r < kf ? TIER_FULL : (r < kf + kq ? TIER_QUANT : TIER_EVICTED);
+    const int nt = new_tier(r);
     const int ot = tier[j];
     const bool fo = ot == TIER_FULL, fn = nt == TIER_FULL;
     const bool ko = fo || ot == TIER_QUANT, kn = fn || nt == TIER_QUANT;
@@ -280,29 +318,37 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     dg[6] += ot == TIER_QUANT && fn;
     dg[7] += fo && nt == TIER_QUANT;
     dg[8] += nt == TIER_EVICTED;
-    if (nt != ot) {
-      {
-        const int c = atomicAdd(&s_nch, 1);
-        ch_win[c] = j;
-        ch_new[c] = (uint8_t)nt;
-        ch_old[c] = (uint8_t)ot;
-        ch_b[c] = bsl[j];
-        ch_q[c] = qsl[j];
-        ch_s[c] = sen[j];
-        // the slot the window last held, if its contents are still the window's
-        int bv = -1, qv = -1;
-        if (nt == TIER_FULL && ot == TIER_QUANT) {
-          const int sb = st.bprev[gu * st.maxw + j];
-          if (sb > 0 && sb < st.capb && st.bvictim[gu * st.capb + sb] == j) bv = sb;
-        }
-        if (nt == TIER_QUANT) {
-          const int sq = st.qprev[gu * st.maxw + j];
-          if (sq >= 0 && sq < st.capq && st.qvictim[gu * st.capq + sq] == j) qv = sq;
-        }
-        ch_bv[c] = bv;
-        ch_qv[c] = qv;
-      }
+    myc += nt != ot;
+  }
+  // the change list in a fixed order (thread, then rank), so slot hand-out is reproducible
+  int nch_total;
+  int c = block_scan(myc, s_w, &nch_total);
+  if (tid == 0) s_nch = nch_total;
+  for (int r = tid; r < n; r += ROUTE_THREADS) {
+    const int j = (int)(keys[r] & 0xFFFFFFFFu);
+    const int nt = new_tier(r);
+    const int ot = tier[j];
+    if (nt == ot) continue;
+    ch_win[c] = j;
+    ch_new[c] = (uint8_t)nt;
+    ch_old[c] = (uint8_t)ot;
+    ch_b[c] = bsl[j];
+    ch_q[c] = qsl[j];
+    ch_s[c] = sen[j];
+    // the slot the window last held, if its contents are still the window's (a window leaving
+    // Full for eviction also needs its 2-bit slot, whose codes must then never be saved)
+    int bv = -1, qv = -1;
+    if (nt == TIER_FULL && ot == TIER_QUANT) {
+      const int sb = st.bprev[gu * st.maxw + j];
+      if (sb > 0 && sb < st.capb && st.bvictim[gu * st.capb + sb] == j) bv = sb;
     }
+    if (nt == TIER_QUANT || (nt == TIER_EVICTED && ot == TIER_FULL)) {
+      const int sq = st.qprev[gu * st.maxw + j];
+      if (sq >= 0 && sq < st.capq && st.qvictim[gu * st.capq + sq] == j) qv = sq;
+    }
+    ch_bv[c] = bv;
+    ch_qv[c] = qv;
+    ++c;
   }
   for (int i = 0; i < 9; ++i)
     if (dg[i]) atomicAdd(&s_diag[i], dg[i]);
@@ -310,7 +356,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   const int bhead = st.bfree_head[gu], btop = st.bfree_top[gu], qtop = st.qfree_top[gu], stop = st.sfree_top[gu];
   const int nbf = btop > bhead ? btop - bhead : 0;
   for (int i = tid; i < st.capb; i += ROUTE_THREADS) bflag[i] = 0;
-  for (int i = tid; i < st.capq; i += ROUTE_THREADS) qflag[i] = 0;
+  for (int i = tid; i < st.capq; i += ROUTE_THREADS) {
+    qflag[i] = 0;
+    qch[i] = -1;
+  }
   __syncthreads();
   for (int i = tid; i < nbf; i += ROUTE_THREADS) {
     const int sl = st.bfree[gu * st.capb + bhead + i];
@@ -352,7 +401,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       qflag[sl] = 0;
       return sl;
     };
-    unsigned long long nfirst = 0, nreuse = 0, nprom = 0, nev = 0, brec = 0, qrec = 0;
+    unsigned long long nfirst = 0, nreuse = 0, nprom = 0, nev = 0, brec = 0, qrec = 0, nwb = 0;
     // (a) leaving the 2-bit pool: a promoted window's slot keeps its codes (back), an evicted
     //     window's slot goes to the front
     for (int c = 0; c < nch; ++c) {
@@ -364,6 +413,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
         st.qvictim[gu * st.capq + sl] = -1;
       } else {
         qfa[qn++] = sl;
+        qch[sl] = c;
         st.qprev[gu * st.maxw + ch_win[c]] = sl;
       }
       qflag[sl] = 1;
@@ -374,9 +424,11 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       if (ch_new[c] != TIER_EVICTED) continue;
       ++nev;
       if (ch_s[c] >= 0) {
-        if (stt >= st.caps) err |= ERR_FREELIST; else sstack[stt++] = ch_s[c] & ~SENT_LEDGER;
+        if (stt >= st.caps) err |= ERR_FREELIST; else sstack[stt++] = ch_s[c] & ~SENT_FLAGS;
         ch_s[c] = -1;
       }
+      // a Full window's codes left in a free 2-bit slot die with it: never saved to its entry
+      if (ch_old[c] == TIER_FULL && ch_qv[c] >= 0) st.qvictim[gu * st.capq + ch_qv[c]] = -1;
       if (ch_old[c] == TIER_PINNED || ch_old[c] == TIER_FULL) {
         const int sl = ch_b[c];
         if (sl <= 0 || sl >= st.capb) err |= ERR_FREELIST;
@@ -424,7 +476,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     for (int c = 0; c < nch; ++c) {
       if (ch_new[c] != TIER_QUANT) continue;
       const int qv = ch_qv[c];
-      if (qv >= 0 && (ch_s[c] & SENT_LEDGER) && qflag[qv]) {
+      if (qv >= 0 && ch_s[c] >= 0 && (ch_s[c] & SENT_PACKED) && qflag[qv]) {
         qflag[qv] = 0;
         ch_q[c] = qv;
         ch_qv[c] = -2;
@@ -436,6 +488,23 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       if (ch_qv[c] == -2) { ++nreuse; continue; }
       const int sl = pop_q();
       if (sl < 0) { err |= ERR_FREELIST; continue; }
+      // The slot may still hold the codes of a kept window (Full since an earlier event) whose
+      // ledger was never written to the host: the move saves them to that window's entry
+      // before it overwrites the slot.
+      int wb = -1;
+      {
+        const int jo = st.qvictim[gu * st.capq + sl];
+        if (jo >= 0 && jo < st.maxw && jo != ch_win[c]) {
+          const int co = qch[sl];
+          const int so = co >= 0 ? ch_s[co] : sen[jo];
+          if (so >= 0 && (so & SENT_PACKED) && !(so & SENT_LEDGER)) {
+            wb = so & ~SENT_FLAGS;
+            if (co >= 0) ch_s[co] = so | SENT_LEDGER; else sen[jo] = so | SENT_LEDGER;
+            ++nwb;
+          }
+        }
+      }
+      ch_qv[c] = wb;
       ch_q[c] = sl;
       st.qvictim[gu * st.capq + sl] = ch_win[c];
       int kind;
@@ -443,11 +512,14 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
         if (stt <= 0) { err |= ERR_FREELIST; continue; }
         ch_s[c] = sstack[--stt];
         kind = MOVE_PACK_COPY;
+      } else if (ch_s[c] & SENT_PACKED) {
+        kind = MOVE_REUSE;   // the codes' only copy is the host ledger by now
+        if (!(ch_s[c] & SENT_LEDGER)) err |= ERR_FREELIST;
       } else {
-        kind = (ch_s[c] & SENT_LEDGER) ? MOVE_REUSE : MOVE_PACK;
+        kind = MOVE_PACK;
       }
       if (kind == MOVE_REUSE) ++nreuse; else ++nfirst;
-      ch_s[c] |= SENT_LEDGER;
+      ch_s[c] |= SENT_PACKED;
       keys[nm++] = ((unsigned long long)kind << 56) | ((unsigned long long)(unsigned)c << 24);
     }
     // move records (slot numbers captured before the bf16 frees below clear them)
@@ -456,12 +528,13 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     for (int k = 0; k < nm; ++k) {
       const int kind = (int)(keys[k] >> 56);
       const int c = (int)((keys[k] >> 24) & 0xFFFFFFFF);
-      const int ent = ch_s[c] & ~SENT_LEDGER;
+      const int ent = ch_s[c] & ~SENT_FLAGS;
       Move mv;
       mv.kind = kind;
       mv.gu = (int)gu;
       mv.win = ch_win[c];
       mv.sent = ent;
+      mv.wb = (kind == MOVE_PACK_COPY || kind == MOVE_PACK || kind == MOVE_REUSE) ? ch_qv[c] : -1;
       if (kind == MOVE_PACK_COPY || kind == MOVE_PACK) { mv.src = ch_b[c]; mv.dst = ch_q[c]; }
       else if (kind == MOVE_REUSE) { mv.src = ent; mv.dst = ch_q[c]; }
       else if (kind == MOVE_PROMOTE) { mv.src = ent; mv.dst = ch_b[c]; }
@@ -481,7 +554,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
       }
       ch_b[c] = -1;
     }
-    unsigned long long* sp = st.stats + (size_t)p.layer * N_STATS;
+    unsigned long long* sp = st.stats + (size_t)layer * N_STATS;
     if (u == 0) atomicAdd(sp + 0, 1ull);
     if (nfirst) atomicAdd(sp + 1, nfirst);
     if (nreuse) atomicAdd(sp + 2, nreuse);
@@ -489,6 +562,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     if (nev) atomicAdd(sp + 4, nev);
     if (brec) atomicAdd(sp + 5, brec);
     if (qrec) atomicAdd(sp + 6, qrec);
+    if (nwb) atomicAdd(sp + 7, nwb);
     st.sfree_top[gu] = stt;
     s_pos[0] = bh;
     s_pos[1] = bn;
@@ -516,10 +590,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   {
     const int bh = s_pos[0], bn = s_pos[1], bf_i = s_pos[2], bf_n = s_pos[3];
     const int nb = compact_free(bfront + bf_i, bf_n - bf_i, bfa + bh, bn - bh, bflag, st.bfree + gu * st.capb,
-                                st.capb, s_cnt2, st.err);
+                                st.capb, s_w, st.err);
     const int qh = s_pos[4], qn = s_pos[5], qf_i = s_pos[6], qf_n = s_pos[7];
     const int nq2 = compact_free(qfront + qf_i, qf_n - qf_i, qfa + qh, qn - qh, qflag, st.qfree + gu * st.capq,
-                                 st.capq, s_cnt2, st.err);
+                                 st.capq, s_w, st.err);
     if (tid == 0) {
       st.bfree_head[gu] = 0;
       st.bfree_top[gu] = nb;
@@ -539,11 +613,10 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     d.full_cut_next = s_cut[1];
     d.kept_cut_kept = s_cut[2];
     d.kept_cut_next = s_cut[3];
-    p.diag[(size_t)p.layer * st.units + u] = d;
+    p.diag[(size_t)layer * st.units + u] = d;
   }
   // 5. rebuild the tile lists: bf16 = sink + Pinned/Full windows, 2-bit = Quantized windows,
   //    both in ascending window order (block-wide stream compaction)
-  __shared__ int s_cnt[ROUTE_THREADS][2];
   const int per = (n_windows + ROUTE_THREADS - 1) / ROUTE_THREADS;
   const int j0 = tid * per, j1 = min(j0 + per, n_windows);
   int cb = 0, cq = 0;
@@ -552,24 +625,15 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     cb += (z == TIER_PINNED || z == TIER_FULL);
     cq += (z == TIER_QUANT);
   }
-  s_cnt[tid][0] = cb;
-  s_cnt[tid][1] = cq;
-  __syncthreads();
+  int tb, tq;
+  const int ob0 = 1 + block_scan(cb, s_w, &tb);   // bf16 entry 0 is the sink
+  const int oq0 = block_scan(cq, s_w, &tq);
   if (tid == 0) {
-    int ab = 1, aq = 0;   // bf16 entry 0 is the sink
-    for (int i = 0; i < ROUTE_THREADS; ++i) {
-      const int b = s_cnt[i][0], q = s_cnt[i][1];
-      s_cnt[i][0] = ab;
-      s_cnt[i][1] = aq;
-      ab += b;
-      aq += q;
-    }
     const int exp_b = 1 + exp_nfull + (n_windows - aged_upto);
-    if (ab != exp_b || aq != exp_nquant) atomicOr(st.err, ERR_COUNT);
+    if (1 + tb != exp_b || tq != exp_nquant) atomicOr(st.err, ERR_COUNT);
     st.blist[gu * st.capb] = make_int2(-1, 0);
   }
-  __syncthreads();
-  int ob = s_cnt[tid][0], oq = s_cnt[tid][1];
+  int ob = ob0, oq = oq0;
   for (int j = j0; j < j1; ++j) {
     const int z = st.tier[gu * st.maxw + j];
     if (z == TIER_PINNED || z == TIER_FULL) {
@@ -584,7 +648,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
   __syncthreads();
   if (tid == 0) {
     __threadfence();
-    LayerDev* h = st.ldev + p.layer;
+    LayerDev* h = st.ldev + layer;
     if (atomicAdd(&h->done, 1u) == gridDim.x - 1) {
       h->routed_upto = aged_upto;
       h->n_full = exp_nfull;
@@ -658,6 +722,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
   float* ks = kz + D;                                                  // [D]
   float* vz = ks + D;                                                  // [W]
   float* vs = vz + W;                                                  // [W]
+  uint8_t* qimg = reinterpret_cast<uint8_t*>(vs + W);                  // the packed 2-bit slot
   const int tid = threadIdx.x;
   for (int mi = blockIdx.x; mi < n; mi += gridDim.x) {
     const Move mv = moves[mi];
@@ -666,7 +731,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
       const bool ok_gu = gu >= 0 && gu < (long long)st.units * st.n_layers;
       const bool src_store = mv.src >= 0 && mv.src < st.caps, src_bf16 = mv.src > 0 && mv.src < st.capb;
       const bool dst_q = mv.dst >= 0 && mv.dst < st.capq, sent_ok = mv.sent >= 0 && mv.sent < st.caps;
-      bool ok = ok_gu && mv.win >= 0 && mv.win < st.maxw;
+      bool ok = ok_gu && mv.win >= 0 && mv.win < st.maxw && mv.wb >= -1 && mv.wb < st.caps;
       switch (mv.kind) {
         case MOVE_PROMOTE: ok = ok && src_store && mv.dst > 0 && mv.dst < st.capb; break;
         case MOVE_REUSE: ok = ok && src_store && dst_q; break;
@@ -692,6 +757,12 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
       copy16(dst, src, g.bslot_bytes(), tid);
       continue;
     }
+    if (mv.wb >= 0) {   // save the codes the 2-bit slot still holds for a kept window first
+      const uint8_t* src = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
+      uint8_t* dst = st.hledger + (gu * st.caps + mv.wb) * (long long)g.qslot_bytes();
+      copy16(dst, src, g.qslot_bytes(), tid);
+      __syncthreads();
+    }
     if (mv.kind == MOVE_REUSE) {
       const uint8_t* src = st.hledger + (gu * st.caps + mv.src) * (long long)g.qslot_bytes();
       uint8_t* dst = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
@@ -702,7 +773,6 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
     const uint8_t* bs = st.bslab + (gu * st.capb + mv.src) * (long long)g.bslot_bytes();
     uint8_t* qs = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
     uint8_t* hs = st.hstore + (gu * st.caps + mv.sent) * (long long)g.bslot_bytes();
-    uint8_t* hl = st.hledger + (gu * st.caps + mv.sent) * (long long)g.qslot_bytes();
     const bool copy_exact = mv.kind == MOVE_PACK_COPY;
     {
       constexpr int STEP = MOVE_THREADS * 16;
@@ -805,23 +875,23 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
         }
       }
       const int wo = (value ? g.off_vcode() / 4 : 0) + widx;
-      reinterpret_cast<unsigned*>(qs)[wo] = word;
-      reinterpret_cast<unsigned*>(hl)[wo] = word;
+      reinterpret_cast<unsigned*>(qimg)[wo] = word;
     }
     for (int c = tid; c < D; c += MOVE_THREADS) {
       const int pc = kparam_pos(c);
-      reinterpret_cast<float*>(qs + g.off_kmin())[pc] = kz[c];
-      reinterpret_cast<float*>(qs + g.off_kscale())[pc] = ks[c];
-      reinterpret_cast<float*>(hl + g.off_kmin())[pc] = kz[c];
-      reinterpret_cast<float*>(hl + g.off_kscale())[pc] = ks[c];
+      reinterpret_cast<float*>(qimg + g.off_kmin())[pc] = kz[c];
+      reinterpret_cast<float*>(qimg + g.off_kscale())[pc] = ks[c];
     }
     for (int r = tid; r < W; r += MOVE_THREADS) {
       const int pr = vparam_pos(g, r);
-      reinterpret_cast<float*>(qs + g.off_vmin())[pr] = vz[r];
-      reinterpret_cast<float*>(qs + g.off_vscale())[pr] = vs[r];
-      reinterpret_cast<float*>(hl + g.off_vmin())[pr] = vz[r];
-      reinterpret_cast<float*>(hl + g.off_vscale())[pr] = vs[r];
+      reinterpret_cast<float*>(qimg + g.off_vmin())[pr] = vz[r];
+      reinterpret_cast<float*>(qimg + g.off_vscale())[pr] = vs[r];
     }
+    __syncthreads();
+    // the slot in whole 16-byte vectors; its codes reach the host ledger only if the slot is
+    // later handed to another window while this one is still kept (the write-back above)
+    for (int o = tid * 16; o < g.qslot_bytes(); o += MOVE_THREADS * 16)
+      *reinterpret_cast<uint4*>(qs + o) = *reinterpret_cast<const uint4*>(qimg + o);
     __syncthreads();   // shared memory is reused by this CTA's next move
   }
 }
@@ -892,18 +962,19 @@ cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t
 }
 
 size_t route_smem_bytes(const State& st) {
-  return (size_t)ROUTE_MAX_CAND * (8 + 4 * 6 + 2) + (size_t)(3 * st.capb + 3 * st.capq + st.caps) * 4 +
-         (size_t)(st.capb + st.capq) + 16;
+  const int cc = route_cand_cap(st);
+  return (size_t)route_key_cap(st) * 8 + (size_t)cc * 4 * 6 + (size_t)((cc + 15) & ~15) * 2 +
+         (size_t)(3 * st.capb + 4 * st.capq + st.caps) * 4 + (size_t)(st.capb + st.capq) + 16;
 }
 
-cudaError_t launch_route(const RouteParams& p, cudaStream_t s) {
-  qe_route_kernel<<<p.st.units, ROUTE_THREADS, route_smem_bytes(p.st), s>>>(p);
+cudaError_t launch_route(const RouteParams& p, int n_layers, cudaStream_t s) {
+  qe_route_kernel<<<dim3(p.st.units, n_layers), ROUTE_THREADS, route_smem_bytes(p.st), s>>>(p);
   return cudaGetLastError();
 }
 
 size_t move_smem_bytes(const State& st) {
   const int W = st.geo.W, D = st.geo.D;
-  return (size_t)st.geo.bslot_bytes() + (size_t)(2 * D + 2 * W) * 4;
+  return (size_t)st.geo.bslot_bytes() + (size_t)(2 * D + 2 * W) * 4 + (size_t)st.geo.qslot_bytes();
 }
 
 cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves, int n_sm, cudaStream_t s) {
