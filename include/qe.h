@@ -121,6 +121,12 @@ typedef struct {
    * p * rope_theta^(-2i / head_dim).  q is passed already rotated at its own position.
    * 0: keys are used as stored. */
   double rope_theta;
+  /* 2-bit window slots beyond the most Kq at max_context (window tiering).  A freed slot keeps
+   * its window's codes until it is handed out again (oldest first): a window demoted again by
+   * then takes its codes back, and a kept window's codes are written to the host ledger only
+   * when their slot is about to be handed to another window.  0: max(16, Kq / 2); -1: none;
+   * n > 0: n slots. */
+  int int2_slack;
 } qe_config;
 
 enum { QE_TIERING_WINDOWS = 0, QE_TIERING_TOKENS = 1 };

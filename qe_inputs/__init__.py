@@ -142,6 +142,8 @@ class Workload:
     score_window: int = 0
     # rotary embedding base for keys stored pre-RoPE (0 = keys carry no rotation)
     rope_theta: float = 0.0
+    # 2-bit window slots beyond the most K_q (cache setting): 0 automatic, -1 none, n > 0
+    int2_slack: int = 0
 
     @property
     def group(self) -> int:

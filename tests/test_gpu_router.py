@@ -24,9 +24,11 @@ def _scores(event, units, maxw, levels):
     return (gen.splitmix64(k) % np.uint64(levels)).astype(np.float32) / np.float32(4)
 
 
-def test_router_cycles_with_ties():
-    track = [(b, 0, h) for b in range(WL.batch) for h in range(WL.n_kv_heads)]
-    run = ParityRun(WL, WL.batch, 1, track)
+@pytest.mark.parametrize("slack", [0, -1], ids=["slack_auto", "no_slack"])
+def test_router_cycles_with_ties(slack):
+    wl = dataclasses.replace(WL, int2_slack=slack)
+    track = [(b, 0, h) for b in range(wl.batch) for h in range(wl.n_kv_heads)]
+    run = ParityRun(wl, wl.batch, 1, track)
     run.prefill()
     cache = run.cache
     info = cache.layer_info(0)
@@ -53,8 +55,9 @@ def test_router_cycles_with_ties():
     cache.qe_synchronize()
     st = cache.route_stats(0)
     assert st.routes == n_events and st.promotions > 0 and st.ledger_reuses > 0 and st.evictions > 0
-    # both ledger paths ran: codes taken back from their old slot, and codes saved to the host
-    # ledger before their slot was reused, later read back by a re-demotion (checked above)
-    assert st.int2_reclaims > 0 and st.ledger_writes > 0
-    assert st.ledger_reuses > st.int2_reclaims
+    if slack == 0:   # freed slots outlive most returns: codes taken back from their old slot
+        assert st.int2_reclaims > 0
+    else:            # no spare slot: codes saved to the host ledger before their slot is reused,
+        # and read back from it by later re-demotions (their codes were checked above)
+        assert st.ledger_writes > 0 and st.ledger_reuses > st.int2_reclaims
     assert run.codes_checked > 0

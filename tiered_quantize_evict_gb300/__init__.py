@@ -45,7 +45,7 @@ class QEConfig(ctypes.Structure):
         ("kq", ctypes.c_int), ("frac_bf16", ctypes.c_double), ("frac_int2", ctypes.c_double),
         ("budget_frac", ctypes.c_double), ("out_fp32", ctypes.c_int),
         ("tiering", ctypes.c_int), ("frac_int4", ctypes.c_double), ("frac_nq1", ctypes.c_double),
-        ("score_window", ctypes.c_int), ("rope_theta", ctypes.c_double),
+        ("score_window", ctypes.c_int), ("rope_theta", ctypes.c_double), ("int2_slack", ctypes.c_int),
     ]
 
 
@@ -309,4 +309,5 @@ def config_from_workload(wl, out_fp32: bool = True, max_context: Optional[int] =
         out_fp32=1 if out_fp32 else 0,
         tiering=QE_TIERING_TOKENS if getattr(wl, "tiering", "windows") == "tokens" else QE_TIERING_WINDOWS,
         frac_int4=getattr(wl, "frac_int4", 0.0), frac_nq1=getattr(wl, "frac_nq1", 0.0),
-        score_window=getattr(wl, "score_window", 0), rope_theta=getattr(wl, "rope_theta", 0.0))
+        score_window=getattr(wl, "score_window", 0), rope_theta=getattr(wl, "rope_theta", 0.0),
+        int2_slack=getattr(wl, "int2_slack", 0))

@@ -162,6 +162,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   if (c.n_recent < 1) return fail(nullptr, QE_ERR_INVALID_ARG, "n_recent must be >= 1");
   if (c.max_context < 1 || c.cap_mode < 0 || c.cap_mode > 2) return fail(nullptr, QE_ERR_INVALID_ARG, "bad max_context or cap_mode");
   if (c.cap_mode == 0 && (c.kf < 0 || c.kq < 0)) return fail(nullptr, QE_ERR_INVALID_ARG, "kf, kq must be >= 0");
+  if (c.int2_slack < -1) return fail(nullptr, QE_ERR_INVALID_ARG, "int2_slack must be >= -1");
 
   qe_handle h = new qe_handle_s();
   h->cfg = c;
@@ -191,7 +192,10 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   // the 2-bit slab holds K_q windows plus slack: a freed slot keeps its window's codes until it
   // is handed out again (oldest first), so a window that returns soon takes its codes back and
   // a kept window's ledger reaches the host only when its codes are about to be overwritten
-  st.capq = kq_max > 0 ? kq_max + (kq_max / 2 > 16 ? kq_max / 2 : 16) : 1;
+  {
+    const int slack = c.int2_slack == 0 ? (kq_max / 2 > 16 ? kq_max / 2 : 16) : (c.int2_slack < 0 ? 0 : c.int2_slack);
+    st.capq = kq_max > 0 ? kq_max + slack : 1;
+  }
   st.caps = (kf_max + kq_max) > 0 ? kf_max + kq_max : 1;
   if (st.caps > maxw) st.caps = maxw;
   if (st.capq > maxw) st.capq = maxw;
