@@ -692,121 +692,201 @@ __device__ __forceinline__ void copy16(uint8_t* dst, const uint8_t* src, int byt
   }
 }
 
-// eq. (2): code = clamp(rint((x - z) / s), 0, 3) with z = min, s = (max - min) / 3 in float32.
-// The quotient is decided as the IEEE float32 division would decide it: a fast estimate (a few
-// ulp from the true quotient) settles every value that is not within 1e-5 of a half-integer;
-// those few, and scales outside [1e-30, 1e30], take the correctly rounded division.
-__device__ __forceinline__ unsigned quant_code(float x, float z, float s) {
+// eq. (2): code = clamp(rint((x - z) / s), 0, 3) with z = min, s = (max - min) / 3 in float32,
+// the quotient rounded as IEEE float32 division rounds it.  For q = fl(d / s) >= 0 that code is
+// [q > 1/2] + [q >= 3/2] + [q > 5/2] (rint ties to even: 1/2 -> 0, 3/2 -> 2, 5/2 -> 2), and as
+// fl(d / s) never decreases with d, each term is [d >= T] for the smallest float T that passes
+// it.  A group finds its three T once (a few correctly rounded divisions next to t s); each
+// element then needs one subtraction and three compares.
+
+// the code of one element by the division itself (groups whose thresholds are not searched)
+__device__ __forceinline__ unsigned quant_code_div(float x, float z, float s) {
   if (s == 0.f) return 0u;
-  const float d = __fsub_rn(x, z);
-  float qv = __fdividef(d, s);
-  const float fr = qv - floorf(qv);
-  if (fabsf(fr - 0.5f) < 1e-5f || !(s >= 1e-30f && s <= 1e30f)) qv = __fdiv_rn(d, s);
-  qv = rintf(qv);
+  float qv = rintf(__fdiv_rn(__fsub_rn(x, z), s));
   qv = fminf(fmaxf(qv, 0.f), 3.f);
   return (unsigned)qv;
+}
+
+// smallest non-negative float d with fl(d / s) > t (strict) or >= t; ok = false if it is not
+// within 8 steps of fl(t s)
+__device__ __forceinline__ float quant_threshold(float s, float t, bool strict, bool& ok) {
+  auto pass = [&](float d) {
+    const float q = __fdiv_rn(d, s);
+    return strict ? q > t : q >= t;
+  };
+  float T = __fmul_rn(t, s);
+  int i = 0;
+  while (!pass(T) && i < 8) {
+    T = __uint_as_float(__float_as_uint(T) + 1u);
+    ++i;
+  }
+  if (i == 8) ok = false;
+  i = 0;
+  while (T > 0.f && i < 8 && pass(__uint_as_float(__float_as_uint(T) - 1u))) {
+    T = __uint_as_float(__float_as_uint(T) - 1u);
+    ++i;
+  }
+  if (i == 8) ok = false;
+  return T;
+}
+
+// The thresholds of a group with scale s, found by its TPG threads (part k finds T_k, T_k+TPG,
+// ...): {T_1/2, T_3/2, T_5/2}, or T_1/2 = -1 where the group's elements take the division (a
+// scale outside [1e-30, 1e30], or a search that did not settle).  s = 0: every code is 0.
+template <int TPG>
+__device__ __forceinline__ void group_thresholds(float s, int part, float (&T)[3]) {
+  const bool ranged = s >= 1e-30f && s <= 1e30f;
+  bool ok = true;
+  float mine[2] = {INFINITY, INFINITY};
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const int k = part + j * TPG;
+    if (ranged && k < 3) mine[j] = quant_threshold(s, 0.5f + k, k != 1, ok);
+  }
+  unsigned okv = ok ? 1u : 0u;
+#pragma unroll
+  for (int o = 1; o < TPG; o <<= 1) okv &= __shfl_xor_sync(0xffffffffu, okv, o);
+  const int base = (threadIdx.x & 31) & ~(TPG - 1);
+#pragma unroll
+  for (int k = 0; k < 3; ++k) T[k] = __shfl_sync(0xffffffffu, mine[k / TPG], base + k % TPG);
+  if (s == 0.f) T[0] = T[1] = T[2] = INFINITY;
+  else if (!ranged || !okv) T[0] = -1.f;
+}
+
+__device__ __forceinline__ unsigned quant_code(float x, const float4& p, float s) {
+  if (p.y < 0.f) return quant_code_div(x, p.x, s);
+  const float d = __fsub_rn(x, p.x);
+  return (unsigned)(d >= p.y) + (unsigned)(d >= p.z) + (unsigned)(d >= p.w);
 }
 
 __device__ __forceinline__ float bf16_at(const uint8_t* raw, int off) {
   return __uint_as_float((unsigned)*reinterpret_cast<const uint16_t*>(raw + off) << 16);
 }
 
+// every index of a move record in range for its kind
+__device__ __forceinline__ bool move_ok(const State& st, const Move& mv) {
+  const bool ok_gu = mv.gu >= 0 && (long long)mv.gu < (long long)st.units * st.n_layers;
+  const bool src_store = mv.src >= 0 && mv.src < st.caps, src_bf16 = mv.src > 0 && mv.src < st.capb;
+  const bool dst_q = mv.dst >= 0 && mv.dst < st.capq, sent_ok = mv.sent >= 0 && mv.sent < st.caps;
+  const bool ok = ok_gu && mv.win >= 0 && mv.win < st.maxw && mv.wb >= -1 && mv.wb < st.caps;
+  switch (mv.kind) {
+    case MOVE_PROMOTE: return ok && src_store && mv.dst > 0 && mv.dst < st.capb;
+    case MOVE_REUSE: return ok && src_store && dst_q;
+    case MOVE_PACK_COPY:
+    case MOVE_PACK: return ok && src_bf16 && dst_q && sent_ok;
+    case MOVE_COPY: return ok && src_bf16 && mv.dst >= 0 && mv.dst < st.caps;
+    default: return false;
+  }
+}
+
+__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all_but_newest() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
+
+// Each CTA takes every gridDim.x-th move.  A pack's bf16 source slot is fetched into one of two
+// shared-memory buffers by asynchronous copies issued one move ahead, so it lands while the
+// CTA works on the move before.
+template <int D, int W>
 __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel(State st, const Move* __restrict__ moves,
                                                                                 const int* __restrict__ n_moves) {
   extern __shared__ __align__(16) uint8_t sm[];
   const int n = *n_moves;
-  const Geo g = st.geo;
-  const int D = g.D, W = g.W;
-  uint8_t* raw = sm;                                                   // the bf16 slot [4 W D]
-  float* kz = reinterpret_cast<float*>(sm + g.bslot_bytes());          // [D]
+  const Geo g{D, W};
+  constexpr int BSLOT = 4 * W * D, QSLOT = 2 * (W * D / 4) + 8 * D + 8 * W;
+  uint8_t* rawbuf[2] = {sm, sm + BSLOT};                               // bf16 slots [4 W D]
+  float4* kp = reinterpret_cast<float4*>(sm + 2 * BSLOT);              // [D] {min, T_1/2, T_3/2, T_5/2}
+  float4* vp = kp + D;                                                 // [W]
+  float* kz = reinterpret_cast<float*>(vp + W);                        // [D]
   float* ks = kz + D;                                                  // [D]
   float* vz = ks + D;                                                  // [W]
   float* vs = vz + W;                                                  // [W]
   uint8_t* qimg = reinterpret_cast<uint8_t*>(vs + W);                  // the packed 2-bit slot
   const int tid = threadIdx.x;
-  for (int mi = blockIdx.x; mi < n; mi += gridDim.x) {
-    const Move mv = moves[mi];
-    const long long gu = mv.gu;
-    {
-      const bool ok_gu = gu >= 0 && gu < (long long)st.units * st.n_layers;
-      const bool src_store = mv.src >= 0 && mv.src < st.caps, src_bf16 = mv.src > 0 && mv.src < st.capb;
-      const bool dst_q = mv.dst >= 0 && mv.dst < st.capq, sent_ok = mv.sent >= 0 && mv.sent < st.caps;
-      bool ok = ok_gu && mv.win >= 0 && mv.win < st.maxw && mv.wb >= -1 && mv.wb < st.caps;
-      switch (mv.kind) {
-        case MOVE_PROMOTE: ok = ok && src_store && mv.dst > 0 && mv.dst < st.capb; break;
-        case MOVE_REUSE: ok = ok && src_store && dst_q; break;
-        case MOVE_PACK_COPY:
-        case MOVE_PACK: ok = ok && src_bf16 && dst_q && sent_ok; break;
-        case MOVE_COPY: ok = ok && src_bf16 && mv.dst >= 0 && mv.dst < st.caps; break;
-        default: ok = false;
-      }
-      if (!ok) {
-        if (tid == 0) atomicOr(st.err, ERR_MOVES);
-        continue;
+  auto is_pack = [](int kind) { return kind == MOVE_PACK || kind == MOVE_PACK_COPY; };
+  // one commit group per move (empty unless the move is a valid pack)
+  auto prefetch = [&](int m, int b) {
+    if (m < n) {
+      const Move mv = moves[m];
+      if (is_pack(mv.kind) && move_ok(st, mv)) {
+        const uint8_t* src = st.bslab + ((long long)mv.gu * st.capb + mv.src) * (long long)BSLOT;
+        for (int o = tid * 16; o < BSLOT; o += MOVE_THREADS * 16) cp_async16(rawbuf[b] + o, src + o);
       }
     }
+    cp_async_commit();
+  };
+  int cur = 0;
+  prefetch(blockIdx.x, 0);
+  for (int mi = blockIdx.x; mi < n; mi += gridDim.x, cur ^= 1) {
+    const Move mv = moves[mi];
+    // The other buffer's last reader was the move two back, which ended with a barrier.
+    prefetch(mi + gridDim.x, cur ^ 1);
+    const long long gu = mv.gu;
+    if (!move_ok(st, mv)) {
+      if (tid == 0) atomicOr(st.err, ERR_MOVES);
+      continue;
+    }
     if (mv.kind == MOVE_PROMOTE) {
-      const uint8_t* src = st.hstore + (gu * st.caps + mv.src) * (long long)g.bslot_bytes();
-      uint8_t* dst = st.bslab + (gu * st.capb + mv.dst) * (long long)g.bslot_bytes();
-      copy16(dst, src, g.bslot_bytes(), tid);
+      const uint8_t* src = st.hstore + (gu * st.caps + mv.src) * (long long)BSLOT;
+      uint8_t* dst = st.bslab + (gu * st.capb + mv.dst) * (long long)BSLOT;
+      copy16(dst, src, BSLOT, tid);
       continue;
     }
     if (mv.kind == MOVE_COPY) {
-      const uint8_t* src = st.bslab + (gu * st.capb + mv.src) * (long long)g.bslot_bytes();
-      uint8_t* dst = st.hstore + (gu * st.caps + mv.dst) * (long long)g.bslot_bytes();
-      copy16(dst, src, g.bslot_bytes(), tid);
+      const uint8_t* src = st.bslab + (gu * st.capb + mv.src) * (long long)BSLOT;
+      uint8_t* dst = st.hstore + (gu * st.caps + mv.dst) * (long long)BSLOT;
+      copy16(dst, src, BSLOT, tid);
       continue;
     }
     if (mv.wb >= 0) {   // save the codes the 2-bit slot still holds for a kept window first
-      const uint8_t* src = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
-      uint8_t* dst = st.hledger + (gu * st.caps + mv.wb) * (long long)g.qslot_bytes();
-      copy16(dst, src, g.qslot_bytes(), tid);
+      const uint8_t* src = st.qslab + (gu * st.capq + mv.dst) * (long long)QSLOT;
+      uint8_t* dst = st.hledger + (gu * st.caps + mv.wb) * (long long)QSLOT;
+      copy16(dst, src, QSLOT, tid);
       __syncthreads();
     }
     if (mv.kind == MOVE_REUSE) {
-      const uint8_t* src = st.hledger + (gu * st.caps + mv.src) * (long long)g.qslot_bytes();
-      uint8_t* dst = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
-      copy16(dst, src, g.qslot_bytes(), tid);
+      const uint8_t* src = st.hledger + (gu * st.caps + mv.src) * (long long)QSLOT;
+      uint8_t* dst = st.qslab + (gu * st.capq + mv.dst) * (long long)QSLOT;
+      copy16(dst, src, QSLOT, tid);
       continue;
     }
-    // ---- pack: the bf16 slot into shared memory, and its exact copy into the host store
-    const uint8_t* bs = st.bslab + (gu * st.capb + mv.src) * (long long)g.bslot_bytes();
-    uint8_t* qs = st.qslab + (gu * st.capq + mv.dst) * (long long)g.qslot_bytes();
-    uint8_t* hs = st.hstore + (gu * st.caps + mv.sent) * (long long)g.bslot_bytes();
-    const bool copy_exact = mv.kind == MOVE_PACK_COPY;
-    {
-      constexpr int STEP = MOVE_THREADS * 16;
-      for (int o0 = 0; o0 < g.bslot_bytes(); o0 += 4 * STEP) {
-        uint4 x[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int o = o0 + i * STEP + tid * 16;
-          if (o < g.bslot_bytes()) x[i] = *reinterpret_cast<const uint4*>(bs + o);
-        }
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const int o = o0 + i * STEP + tid * 16;
-          if (o < g.bslot_bytes()) {
-            *reinterpret_cast<uint4*>(raw + o) = x[i];
-            if (copy_exact) *reinterpret_cast<uint4*>(hs + o) = x[i];
-          }
-        }
-      }
-    }
+    // ---- pack: the bf16 slot (fetched one move ahead), and its exact copy into the host store
+    const uint8_t* raw = rawbuf[cur];
+    uint8_t* qs = st.qslab + (gu * st.capq + mv.dst) * (long long)QSLOT;
+    uint8_t* hs = st.hstore + (gu * st.caps + mv.sent) * (long long)BSLOT;
+    cp_async_wait_all_but_newest();
     __syncthreads();
+    if (mv.kind == MOVE_PACK_COPY)
+      for (int o = tid * 16; o < BSLOT; o += MOVE_THREADS * 16)
+        *reinterpret_cast<uint4*>(hs + o) = *reinterpret_cast<const uint4*>(raw + o);
     const int lo = (mv.win == 0) ? st.n_sink : 0;
-    // key groups: one per channel over rows [lo, W)
-    for (int c = tid; c < D; c += MOVE_THREADS) {
-      float mn = bf16_at(raw, bf16_k_off(g, lo, c)), mx = mn;
-      for (int r = lo + 1; r < W; ++r) {
+    // key groups: one per channel over rows [lo, W), TPC threads per channel
+    {
+      constexpr int TPC = MOVE_THREADS / D;
+      const int c = tid / TPC, part = tid % TPC;
+      float mn = INFINITY, mx = -INFINITY;
+      for (int r = lo + part; r < W; r += TPC) {
         const float x = bf16_at(raw, bf16_k_off(g, r, c));
         mn = fminf(mn, x);
         mx = fmaxf(mx, x);
       }
-      kz[c] = mn;
-      ks[c] = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+#pragma unroll
+      for (int o = 1; o < TPC; o <<= 1) {
+        mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
+      }
+      const float sc = __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      float T[3];
+      group_thresholds<TPC>(sc, part, T);
+      if (part == 0) {
+        kz[c] = mn;
+        ks[c] = sc;
+        kp[c] = make_float4(mn, T[0], T[1], T[2]);
+      }
     }
     // value groups: one per token over D channels; 8 threads per token, shuffle-reduced
+#pragma unroll
     for (int t0 = 0; t0 < W; t0 += MOVE_THREADS / 8) {
       const int r = t0 + tid / 8, part = tid % 8;
       float mn = INFINITY, mx = -INFINITY;
@@ -822,9 +902,14 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
         mn = fminf(mn, __shfl_xor_sync(0xffffffffu, mn, o));
         mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, o));
       }
+      const bool sink = r < lo;
+      const float sc = sink ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+      float T[3];
+      group_thresholds<8>(r < W ? sc : 0.f, part, T);
       if (r < W && part == 0) {
-        vz[r] = (r < lo) ? 0.f : mn;
-        vs[r] = (r < lo) ? 0.f : __fdiv_rn(__fsub_rn(mx, mn), 3.0f);
+        vz[r] = sink ? 0.f : mn;
+        vs[r] = sc;
+        vp[r] = make_float4(sink ? 0.f : mn, T[0], T[1], T[2]);
       }
     }
     __syncthreads();
@@ -832,12 +917,14 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
     // fragments 2 wi and 2 wi + 1 of that lane; the bf16 slot stores the same fragment of the
     // same lane as one 16-byte vector (element (reg, e) at bits 32 reg + 16 e), so a word needs
     // two vector loads and its code (reg, f, e) goes to bit 8 f + 2 reg + 16 e.
-    const int wpl = g.wpl(), cw = g.cw(), KS = D / 16, KT = W / 16;
-    for (int t = tid; t < 64 * wpl; t += MOVE_THREADS) {
-      const bool value = t >= 32 * wpl;
-      const int tt = value ? t - 32 * wpl : t;
+    constexpr int WPL = (W / 16) * (D / 16) / 2, CW = WPL < 4 ? WPL : 4, KS = D / 16, KT = W / 16;
+    constexpr int SUB = 64 * D, OFF_VCODE = W * D / 4 + 8 * D;
+#pragma unroll
+    for (int t = tid; t < 64 * WPL; t += MOVE_THREADS) {
+      const bool value = t >= 32 * WPL;
+      const int tt = value ? t - 32 * WPL : t;
       const int lane = tt & 31, wi = tt >> 5;
-      const int widx = ((wi / cw) * 32 + lane) * cw + (wi - (wi / cw) * cw);
+      const int widx = ((wi / CW) * 32 + lane) * CW + (wi % CW);
       const int a = lane >> 2, b = 2 * (lane & 3);
       unsigned word = 0u;
 #pragma unroll
@@ -846,35 +933,54 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
         uint4 x;
         int r0, c0;   // row / column of element (reg 0, e 0) of this lane's fragment
         if (!value) {
-          const int mt = F / KS, kst = F - mt * KS;
-          x = *reinterpret_cast<const uint4*>(raw + mt * g.sub_bytes() + kst * 512 + lane * 16);
+          const int mt = F / KS, kst = F % KS;
+          x = *reinterpret_cast<const uint4*>(raw + mt * SUB + kst * 512 + lane * 16);
           r0 = 16 * mt + a;
           c0 = 16 * kst + b;
         } else {
-          const int mc = F / KT, kt = F - mc * KT;
-          x = *reinterpret_cast<const uint4*>(raw + kt * g.sub_bytes() + 32 * D + mc * 512 + lane * 16);
+          const int mc = F / KT, kt = F % KT;
+          x = *reinterpret_cast<const uint4*>(raw + kt * SUB + 32 * D + mc * 512 + lane * 16);
           r0 = 16 * kt + b;   // token
           c0 = 16 * mc + a;   // channel
         }
         const unsigned xr[4] = {x.x, x.y, x.z, x.w};
+        if (!value) {
+          // channels c0, c0 + 1, c0 + 8, c0 + 9; rows r0, r0 + 8
 #pragma unroll
-        for (int reg = 0; reg < 4; ++reg) {
+          for (int hc = 0; hc < 2; ++hc)
 #pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float xv = __uint_as_float(e ? (xr[reg] & 0xFFFF0000u) : (xr[reg] << 16));
-            unsigned code;
-            if (!value) {
-              const int r = r0 + 8 * (reg & 1), c = c0 + e + 8 * (reg >> 1);
-              code = r >= lo ? quant_code(xv, kz[c], ks[c]) : 0u;
-            } else {
-              const int r = r0 + e + 8 * (reg >> 1);
-              code = r >= lo ? quant_code(xv, vz[r], vs[r]) : 0u;
+            for (int e = 0; e < 2; ++e) {
+              const int c = c0 + e + 8 * hc;
+              const float4 pc = kp[c];
+              const float sc = ks[c];
+#pragma unroll
+              for (int hr = 0; hr < 2; ++hr) {
+                const int reg = hr + 2 * hc;
+                const float xv = __uint_as_float(e ? (xr[reg] & 0xFFFF0000u) : (xr[reg] << 16));
+                const unsigned code = r0 + 8 * hr >= lo ? quant_code(xv, pc, sc) : 0u;
+                word |= code << (8 * f + 2 * reg + 16 * e);
+              }
             }
-            word |= code << (8 * f + 2 * reg + 16 * e);
-          }
+        } else {
+          // tokens r0, r0 + 1, r0 + 8, r0 + 9; channels c0, c0 + 8
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+              const int r = r0 + e + 8 * hr;
+              const float4 pr = vp[r];
+              const float sr = vs[r];
+#pragma unroll
+              for (int hc = 0; hc < 2; ++hc) {
+                const int reg = hc + 2 * hr;
+                const float xv = __uint_as_float(e ? (xr[reg] & 0xFFFF0000u) : (xr[reg] << 16));
+                const unsigned code = r >= lo ? quant_code(xv, pr, sr) : 0u;
+                word |= code << (8 * f + 2 * reg + 16 * e);
+              }
+            }
         }
       }
-      const int wo = (value ? g.off_vcode() / 4 : 0) + widx;
+      const int wo = (value ? OFF_VCODE / 4 : 0) + widx;
       reinterpret_cast<unsigned*>(qimg)[wo] = word;
     }
     for (int c = tid; c < D; c += MOVE_THREADS) {
@@ -890,7 +996,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
     __syncthreads();
     // the slot in whole 16-byte vectors; its codes reach the host ledger only if the slot is
     // later handed to another window while this one is still kept (the write-back above)
-    for (int o = tid * 16; o < g.qslot_bytes(); o += MOVE_THREADS * 16)
+    for (int o = tid * 16; o < QSLOT; o += MOVE_THREADS * 16)
       *reinterpret_cast<uint4*>(qs + o) = *reinterpret_cast<const uint4*>(qimg + o);
     __syncthreads();   // shared memory is reused by this CTA's next move
   }
@@ -974,11 +1080,21 @@ cudaError_t launch_route(const RouteParams& p, int n_layers, cudaStream_t s) {
 
 size_t move_smem_bytes(const State& st) {
   const int W = st.geo.W, D = st.geo.D;
-  return (size_t)st.geo.bslot_bytes() + (size_t)(2 * D + 2 * W) * 4 + (size_t)st.geo.qslot_bytes();
+  return (size_t)2 * st.geo.bslot_bytes() + (size_t)(D + W) * (16 + 8) + (size_t)st.geo.qslot_bytes();
+}
+
+// the move kernel of a geometry (head_dim 64 or 128, window 16, 32 or 64), or null
+using MoveKernel = void (*)(State, const Move*, const int*);
+static MoveKernel move_kernel_for(int D, int W) {
+  if (D == 128) return W == 16 ? qe_move_kernel<128, 16> : W == 32 ? qe_move_kernel<128, 32> : W == 64 ? qe_move_kernel<128, 64> : nullptr;
+  if (D == 64) return W == 16 ? qe_move_kernel<64, 16> : W == 32 ? qe_move_kernel<64, 32> : W == 64 ? qe_move_kernel<64, 64> : nullptr;
+  return nullptr;
 }
 
 cudaError_t launch_moves(const State& st, const Move* moves, const int* n_moves, int n_sm, cudaStream_t s) {
-  qe_move_kernel<<<n_sm * MOVE_CTAS_PER_SM, MOVE_THREADS, move_smem_bytes(st), s>>>(st, moves, n_moves);
+  const MoveKernel k = move_kernel_for(st.geo.D, st.geo.W);
+  if (!k) return cudaErrorInvalidValue;
+  k<<<n_sm * MOVE_CTAS_PER_SM, MOVE_THREADS, move_smem_bytes(st), s>>>(st, moves, n_moves);
   return cudaGetLastError();
 }
 
@@ -991,14 +1107,16 @@ cudaError_t prepare_route_kernels(const State& st) {
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
   if (e != cudaSuccess) return e;
+  const MoveKernel mk = move_kernel_for(st.geo.D, st.geo.W);
+  if (!mk) return cudaErrorInvalidValue;
   cudaFuncAttributes ra{}, ma{};
   if ((e = cudaFuncGetAttributes(&ra, qe_route_kernel)) != cudaSuccess) return e;
-  if ((e = cudaFuncGetAttributes(&ma, qe_move_kernel)) != cudaSuccess) return e;
+  if ((e = cudaFuncGetAttributes(&ma, mk)) != cudaSuccess) return e;
   const int rmax = optin - (int)ra.sharedSizeBytes, mmax = optin - (int)ma.sharedSizeBytes;
   if (route_smem_bytes(st) > (size_t)rmax || move_smem_bytes(st) > (size_t)mmax) return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(qe_route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, rmax);
   if (e != cudaSuccess) return e;
-  return cudaFuncSetAttribute(qe_move_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, mmax);
+  return cudaFuncSetAttribute(mk, cudaFuncAttributeMaxDynamicSharedMemorySize, mmax);
 }
 
 }  // namespace qe
