@@ -47,6 +47,11 @@ def test_init_reports_errors_without_crashing(lib):
     h = ctypes.c_void_p()
     st = lib.qe_init(ctypes.byref(cfg), None, ctypes.byref(h))
     assert st == qe.QE_ERR_INVALID_ARG and b"head_dim" in lib.qe_last_error(None)
+    cfg.head_dim = 64
+    cfg.int2_slack = -2
+    st = lib.qe_init(ctypes.byref(cfg), None, ctypes.byref(h))
+    assert st == qe.QE_ERR_INVALID_ARG and b"int2_slack" in lib.qe_last_error(None)
+    cfg.int2_slack = 0
     if not torch.cuda.is_available():
         cfg.head_dim = 64
         st = lib.qe_init(ctypes.byref(cfg), None, ctypes.byref(h))
