@@ -145,6 +145,16 @@ def _traffic(workload: str, kernel: str = "qe_decode_attn"):
         return None
 
 
+def _route_counts(cache):
+    """Cumulative routing counters of all layers (window tiering), or None."""
+    try:
+        st = cache.route_stats(-1)
+    except Exception:
+        return None
+    return {f: int(getattr(st, f)) for f in ("first_packs", "ledger_reuses", "promotions", "evictions",
+                                            "bf16_reclaims", "int2_reclaims", "ledger_writes")}
+
+
 # ---------------------------------------------------------------------------- our implementation
 def run_ours(args):
     import torch
@@ -216,7 +226,7 @@ def run_ours(args):
     def routes_at(t):
         return (t * NQ) // omega > ((t - 1) * NQ) // omega
 
-    def step(t, k, v, q, o=out):
+    def step(t, k, v, q, o=out, route_events=None):
         for layer in range(Lyr):
             if verify:
                 cache.qe_verify(layer, q[layer], k[layer], v[layer], o, NQ)
@@ -225,7 +235,14 @@ def run_ours(args):
                 cache.qe_append(layer, k[layer], v[layer], 1)
                 cache.qe_decode_step(layer, q[layer], o)
         if routes_at(t):
-            cache.qe_route(-1)
+            if route_events is not None:      # CUDA events around the routing call of all layers
+                ev = (torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                ev[0].record(stream)
+                cache.qe_route(-1)
+                ev[1].record(stream)
+                route_events.append((t, ev))
+            else:
+                cache.qe_route(-1)
 
     t = 0
     for _ in range(pre + W):            # pre-roll through the first routing event, then warm-up
@@ -275,13 +292,18 @@ def run_ours(args):
     # every qe_decode_attn launch on the handle's stream
     rl = [make_inputs(t + 1 + i) for i in range(K)]
     torch.cuda.synchronize(dev)
+    route_events = []
+    rs0 = _route_counts(cache)
     cache.set_timing(True)
     for i in range(K):
         t += 1
-        step(t, *rl[i])
+        step(t, *rl[i], route_events=route_events)
     torch.cuda.synchronize(dev)
     cache.set_timing(False)
     attn_ms, attn_launches, attn_bytes = cache.timing()
+    rs1 = _route_counts(cache)
+    route_ms = [a.elapsed_time(b) for _, (a, b) in route_events]
+    route_steps = [ts * NQ for ts, _ in route_events]
     cache.qe_synchronize()
     del rl
 
@@ -349,6 +371,15 @@ def run_ours(args):
             "avg_launch_us": round(attn_ms * 1e3 / max(attn_launches, 1), 2),
             "attn_share_of_step": round(attn_ms / ms_total, 4) if ms_total > 0 else None,
             "measured_on": "the next K decode steps launched directly, CUDA events around each launch",
+        },
+        "routing": {
+            "events": len(route_ms),
+            "at_decode_steps": route_steps,
+            "ms_per_event": [round(x, 3) for x in route_ms],
+            "ms_per_step_amortized": round(sum(route_ms) / K, 4),
+            "counts": {kk: rs1[kk] - rs0[kk] for kk in rs1} if rs0 and rs1 else None,
+            "measured_on": ("the same K direct-launch steps, CUDA events around each qe_route(-1) call "
+                            "(every layer's %s and moves)" % ("re-rank" if tok else "routing")),
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h,

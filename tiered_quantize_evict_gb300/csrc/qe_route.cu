@@ -779,12 +779,6 @@ __device__ __forceinline__ bool move_ok(const State& st, const Move& mv) {
   }
 }
 
-__device__ __forceinline__ void cp_async16(void* sdst, const void* gsrc) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;\n" ::"r"(smem_u32(sdst)), "l"(gsrc) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;\n" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait_all_but_newest() { asm volatile("cp.async.wait_group 1;\n" ::: "memory"); }
-
 // Each CTA takes every gridDim.x-th move.  A pack's bf16 source slot is fetched into one of two
 // shared-memory buffers by asynchronous copies issued one move ahead, so it lands while the
 // CTA works on the move before.

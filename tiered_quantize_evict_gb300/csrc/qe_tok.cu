@@ -811,7 +811,7 @@ struct TkWarpBuf {
 };
 
 template <int D>
-__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const TokState s, int layer) {
+__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const TokState s, int layer0) {
   extern __shared__ __align__(1024) uint8_t smem[];
   __shared__ unsigned hist[4][256];
   __shared__ unsigned long long pref[4];
@@ -820,6 +820,8 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
   __shared__ int scan[4][TK_RERANK_THREADS];
   __shared__ int s_cnt[4];
   const int u = blockIdx.x, tid = threadIdx.x;
+  const int layer = layer0 + (int)blockIdx.y;
+  const long long su = (long long)blockIdx.y * s.units + u;   // scratch slot of (layer, unit)
   const TokLayer hd = s.hdr[layer];
   const int L = hd.L, nt = hd.n_tail, buf = hd.buf;
   const int4 c4 = *reinterpret_cast<const int4*>(s.cnt + ((long long)layer * s.units + u) * 4);
@@ -828,11 +830,11 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
   if (n_aged < 0) n_aged = 0;
   const int ncand = cnt[0] + cnt[1] + cnt[2] + cnt[3] + n_aged;
   const size_t mc = (size_t)s.max_context;
-  unsigned long long* key = s.ckey + u * mc;
-  int* src = s.csrc + u * mc;
-  uint8_t* newt = s.newt + u * mc;
-  int* src_of = s.src_of + u * mc;
-  int* order = s.order + u * 4 * mc;
+  unsigned long long* key = s.ckey + su * mc;
+  int* src = s.csrc + su * mc;
+  uint8_t* newt = s.newt + su * mc;
+  int* src_of = s.src_of + su * mc;
+  int* order = s.order + su * 4 * mc;
   // cut ranks (cumulative), double arithmetic without contraction as the host and oracle do
   long long cuts[4];
   {
@@ -952,7 +954,7 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rerank_kernel(const T
     }
   }
   __syncthreads();
-  if (tid < 4) s.ncnt[u * 4 + tid] = s_cnt[tid] < s.cap[tid] ? s_cnt[tid] : s.cap[tid];
+  if (tid < 4) s.ncnt[su * 4 + tid] = s_cnt[tid] < s.cap[tid] ? s_cnt[tid] : s.cap[tid];
 }
 
 // stage source tile `id` ((pool or tail) << 28 | tile) of unit u in the warp's shared buffer
@@ -963,8 +965,10 @@ __device__ __forceinline__ const uint8_t* tk_stage(TkWarpBuf& W, const TokState&
     const int sz = id >> 28, ti = id & 0x0FFFFFFF;
     const uint8_t* g = tk_src_tile(s, layer, buf, u, sz, ti * 16);
     const int bytes = tk_tile_bytes(s, sz);
-    for (int off = lane * 16; off < bytes; off += 512)
-      *reinterpret_cast<uint4*>(W.src + off) = *reinterpret_cast<const uint4*>(g + off);
+    // every lane's pieces in flight at once: one memory latency per staged tile
+    for (int off = lane * 16; off < bytes; off += 512) cp_async16(W.src + off, g + off);
+    cp_async_commit();
+    cp_async_wait_all();
     __syncwarp();
     if (lane == 0) W.src_id = id;
     __syncwarp();
@@ -1200,10 +1204,12 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
 constexpr int TK_REBUILD_SPLIT = 7;
 
 template <int D>
-__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const TokState s, int layer) {
+__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const TokState s, int layer0) {
   extern __shared__ __align__(1024) uint8_t smem[];
   TkWarpBuf* wb = reinterpret_cast<TkWarpBuf*>(smem);
   const int u = blockIdx.x / TK_REBUILD_SPLIT, part = blockIdx.x - u * TK_REBUILD_SPLIT;
+  const int layer = layer0 + (int)blockIdx.y;
+  const long long su = (long long)blockIdx.y * s.units + u;   // scratch slot of (layer, unit)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int wall = part * TK_RERANK_WARPS + warp, nwall = TK_REBUILD_SPLIT * TK_RERANK_WARPS;
   const TokGeo geo = s.g;
@@ -1213,11 +1219,11 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const 
   int n_aged = nt - s.n_sink - s.n_recent;
   if (n_aged < 0) n_aged = 0;
   const size_t mc = (size_t)s.max_context;
-  const int* order = s.order + u * 4 * mc;
-  const int* src_of = s.src_of + u * mc;
+  const int* order = s.order + su * 4 * mc;
+  const int* src_of = s.src_of + su * mc;
   const bool reset = s.score_window > 0;
   int ncnt[4];
-  for (int z = 0; z < 4; ++z) ncnt[z] = s.ncnt[u * 4 + z];
+  for (int z = 0; z < 4; ++z) ncnt[z] = s.ncnt[su * 4 + z];
   TkWarpBuf& W = wb[warp];
   if (lane == 0) W.src_id = -1;
   __syncwarp();
@@ -1322,11 +1328,13 @@ __global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const 
 }
 
 // After the re-rank of a layer: cost prefix of the new counts and the header switch.
-__global__ void tk_finish_kernel(TokState s, int layer) {
+__global__ void tk_finish_kernel(TokState s, int layer0) {
   __shared__ long long part[256];
   const int tid = threadIdx.x;
+  const int layer = layer0 + (int)blockIdx.y;
   int* cnt = s.cnt + (long long)layer * s.units * 4;
-  for (int i = tid; i < s.units * 4; i += 256) cnt[i] = s.ncnt[i];
+  const int* ncnt = s.ncnt + (long long)blockIdx.y * s.units * 4;
+  for (int i = tid; i < s.units * 4; i += 256) cnt[i] = ncnt[i];
   __syncthreads();
   long long* cum = s.cum + (long long)layer * (s.units + 1);
   // each thread sums a contiguous run of units, then a serial prefix over the threads
@@ -1460,17 +1468,18 @@ cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float*
   return cudaLaunchKernelEx(&cfg, tk_merge_kernel<64>, m);
 }
 
-cudaError_t tk_launch_rerank(const TokState& s, int layer, cudaStream_t st) {
+cudaError_t tk_launch_rerank(const TokState& s, int layer0, int n_layers, cudaStream_t st) {
   const size_t sm = tk_rerank_smem(s.g.D);
-  if (s.g.D == 128) tk_rerank_kernel<128><<<s.units, TK_RERANK_THREADS, 0, st>>>(s, layer);
-  else tk_rerank_kernel<64><<<s.units, TK_RERANK_THREADS, 0, st>>>(s, layer);
+  const dim3 sel(s.units, n_layers), reb(s.units * TK_REBUILD_SPLIT, n_layers), fin(1, n_layers);
+  if (s.g.D == 128) tk_rerank_kernel<128><<<sel, TK_RERANK_THREADS, 0, st>>>(s, layer0);
+  else tk_rerank_kernel<64><<<sel, TK_RERANK_THREADS, 0, st>>>(s, layer0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (s.g.D == 128) tk_rebuild_kernel<128><<<s.units * TK_REBUILD_SPLIT, TK_RERANK_THREADS, sm, st>>>(s, layer);
-  else tk_rebuild_kernel<64><<<s.units * TK_REBUILD_SPLIT, TK_RERANK_THREADS, sm, st>>>(s, layer);
+  if (s.g.D == 128) tk_rebuild_kernel<128><<<reb, TK_RERANK_THREADS, sm, st>>>(s, layer0);
+  else tk_rebuild_kernel<64><<<reb, TK_RERANK_THREADS, sm, st>>>(s, layer0);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  tk_finish_kernel<<<1, 256, 0, st>>>(s, layer);
+  tk_finish_kernel<<<fin, 256, 0, st>>>(s, layer0);
   return cudaGetLastError();
 }
 

@@ -94,13 +94,14 @@ struct TokState {
   int* cnt;                // [layers][units][4] ranked pool counts
   long long* cum;          // [layers][units + 1] ranked cost prefix
   unsigned* err;
-  // re-rank scratch, [units][max_context] each (shared by the layers: one layer re-ranks at a time)
+  // re-rank scratch, [layers][units][max_context] each: one slot per layer of a call, which
+  // re-ranks a run of layers in one launch (slot = layer - first layer of the run)
   unsigned long long* ckey;
   int* csrc;
   uint8_t* newt;
-  int* order;              // [units][4][max_context]
-  int* src_of;             // [units][max_context]
-  int* ncnt;               // [units][4] ranked pool counts after the re-rank being applied
+  int* order;              // [layers][units][4][max_context]
+  int* src_of;             // [layers][units][max_context]
+  int* ncnt;               // [layers][units][4] ranked pool counts after the re-rank being applied
   unsigned* done;          // [layers] combine completion counters
 };
 

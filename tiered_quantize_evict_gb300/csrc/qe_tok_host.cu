@@ -187,12 +187,14 @@ qe_status tok_init(const qe_config& c, cudaStream_t stream, qe_handle* out, std:
   A(talloc(h, &s.cnt, (size_t)c.n_layers * s.units * 4));
   A(talloc(h, &s.cum, (size_t)c.n_layers * (s.units + 1)));
   A(talloc(h, &s.err, 1));
-  A(talloc(h, &s.ckey, (size_t)s.units * mc));
-  A(talloc(h, &s.csrc, (size_t)s.units * mc));
-  A(talloc(h, &s.newt, (size_t)s.units * mc));
-  A(talloc(h, &s.order, (size_t)s.units * 4 * mc));
-  A(talloc(h, &s.src_of, (size_t)s.units * mc));
-  A(talloc(h, &s.ncnt, (size_t)s.units * 4));
+  // re-rank scratch, one slot per layer: qe_route(-1) re-ranks every layer in one launch
+  const size_t NLU = (size_t)c.n_layers * s.units;
+  A(talloc(h, &s.ckey, NLU * mc));
+  A(talloc(h, &s.csrc, NLU * mc));
+  A(talloc(h, &s.newt, NLU * mc));
+  A(talloc(h, &s.order, NLU * 4 * mc));
+  A(talloc(h, &s.src_of, NLU * mc));
+  A(talloc(h, &s.ncnt, NLU * 4));
   A(talloc(h, &s.done, (size_t)c.n_layers));
   A(talloc(h, &h->tk_part_o, (size_t)(NW + s.units) * G * c.head_dim));
   A(talloc(h, &h->tk_part_ml, (size_t)(NW + s.units) * G));
@@ -347,8 +349,10 @@ qe_status tok_route(qe_handle h, int layer) {
   for (int l = l0; l < l1; ++l) {
     qe_status st = commit(h, l);
     if (st != QE_OK) return st;
-    TK_CK(h, tk_launch_rerank(h->ts, l, h->stream));
-    h->launches += 2;
+  }
+  TK_CK(h, tk_launch_rerank(h->ts, l0, l1 - l0, h->stream));
+  h->launches += 3;
+  for (int l = l0; l < l1; ++l) {
     TokMirror& m = h->tlay[l];
     int aged = m.n_tail - h->ts.n_sink - h->ts.n_recent;
     if (aged < 0) aged = 0;

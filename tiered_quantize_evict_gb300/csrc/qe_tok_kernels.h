@@ -23,6 +23,7 @@ cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_
 cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float* part_o, const float2* part_ml,
                             const float* logits, int lg_cap, int grid, void* out, int out_fp32, cudaStream_t st);
 // re-rank of one layer and its header switch
-cudaError_t tk_launch_rerank(const TokState& s, int layer, cudaStream_t st);
+// re-ranks layers [layer0, layer0 + n_layers) in one launch per kernel (scratch slot = layer - layer0)
+cudaError_t tk_launch_rerank(const TokState& s, int layer0, int n_layers, cudaStream_t st);
 
 }  // namespace qe
