@@ -1201,17 +1201,20 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
 // tiers: TK_REBUILD_SPLIT CTAs per unit share its destination tiles, one tile per warp at a time.
 // A destination tile's rows (position order) come from few source tiles: the warp stages each
 // distinct source tile once in shared memory and serves every row that reads from it.
-constexpr int TK_REBUILD_SPLIT = 7;
+constexpr int TK_REBUILD_SPLIT = 9;
+// six warps per CTA: two CTAs fit on an SM (shared memory: six warp buffers each)
+constexpr int TK_REBUILD_WARPS = 6;
+constexpr int TK_REBUILD_THREADS = TK_REBUILD_WARPS * 32;
 
 template <int D>
-__global__ void __launch_bounds__(TK_RERANK_THREADS, 1) tk_rebuild_kernel(const TokState s, int layer0) {
+__global__ void __launch_bounds__(TK_REBUILD_THREADS, 2) tk_rebuild_kernel(const TokState s, int layer0) {
   extern __shared__ __align__(1024) uint8_t smem[];
   TkWarpBuf* wb = reinterpret_cast<TkWarpBuf*>(smem);
   const int u = blockIdx.x / TK_REBUILD_SPLIT, part = blockIdx.x - u * TK_REBUILD_SPLIT;
   const int layer = layer0 + (int)blockIdx.y;
   const long long su = (long long)blockIdx.y * s.units + u;   // scratch slot of (layer, unit)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  const int wall = part * TK_RERANK_WARPS + warp, nwall = TK_REBUILD_SPLIT * TK_RERANK_WARPS;
+  const int wall = part * TK_REBUILD_WARPS + warp, nwall = TK_REBUILD_SPLIT * TK_REBUILD_WARPS;
   const TokGeo geo = s.g;
   const Geo g16{D, 16};
   const TokLayer hd = s.hdr[layer];
@@ -1373,7 +1376,7 @@ __global__ void tk_finish_kernel(TokState s, int layer0) {
 }
 
 // ------------------------------------------------------------------------------ launchers
-size_t tk_rerank_smem(int D) { return (size_t)TK_RERANK_WARPS * sizeof(TkWarpBuf) + 0 * D; }
+size_t tk_rerank_smem(int /*D*/) { return (size_t)TK_REBUILD_WARPS * sizeof(TkWarpBuf); }
 
 template <int D>
 static cudaError_t tk_prepare_t() {
@@ -1475,8 +1478,8 @@ cudaError_t tk_launch_rerank(const TokState& s, int layer0, int n_layers, cudaSt
   else tk_rerank_kernel<64><<<sel, TK_RERANK_THREADS, 0, st>>>(s, layer0);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  if (s.g.D == 128) tk_rebuild_kernel<128><<<reb, TK_RERANK_THREADS, sm, st>>>(s, layer0);
-  else tk_rebuild_kernel<64><<<reb, TK_RERANK_THREADS, sm, st>>>(s, layer0);
+  if (s.g.D == 128) tk_rebuild_kernel<128><<<reb, TK_REBUILD_THREADS, sm, st>>>(s, layer0);
+  else tk_rebuild_kernel<64><<<reb, TK_REBUILD_THREADS, sm, st>>>(s, layer0);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   tk_finish_kernel<<<fin, 256, 0, st>>>(s, layer0);
