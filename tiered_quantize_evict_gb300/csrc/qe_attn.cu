@@ -455,6 +455,10 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   const int g = lane >> 2, t = lane & 3;
   const int G = p.st.G;
   const int wg = blockIdx.x * ATTN_WARPS + warp;
+  // The launch is a programmatic dependent of the kernel before it on the stream (the previous
+  // layer's combine, which reads the split-K scratch this launch rewrites): the CTAs may be
+  // resident early, but nothing is read or written before that kernel has completed.
+  griddep_wait();
   // the layer's step-dependent counts live in shared memory (read when a batch of tiles is
   // described), not in registers the tile loop needs
   __shared__ Lay s_lay;
@@ -930,6 +934,8 @@ __global__ void __launch_bounds__(COMBINE_THREADS) qe_attn_combine_kernel(const 
     sc[j] = (ent[j].x >= 0 && ent[j].x < p.st.maxw) ? p.st.score[gu * p.st.maxw + ent[j].x] : 0.f;
   }
   griddep_wait();
+  // the next layer's attention may now take the SMs this grid leaves (it waits for completion)
+  griddep_launch_dependents();
   // ---- loads of this thread's partial outputs (head h, channel c) and tile log-sum-exps
   const int h = tid / D, c = tid - h * D;
   const bool out_thread = h < G;
@@ -1050,9 +1056,18 @@ static size_t attn_smem_bytes() {
 
 template <int D, int W>
 static cudaError_t launch_attn_t(const AttnParams& p, int grid, cudaStream_t stream) {
-  if (p.rope_blk) qe_decode_attn_kernel<D, W, true><<<grid, ATTN_WARPS * 32, attn_smem_bytes<D, W>(), stream>>>(p);
-  else qe_decode_attn_kernel<D, W, false><<<grid, ATTN_WARPS * 32, attn_smem_bytes<D, W>(), stream>>>(p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(ATTN_WARPS * 32);
+  cfg.dynamicSmemBytes = attn_smem_bytes<D, W>();
+  cfg.stream = stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (p.rope_blk) return cudaLaunchKernelEx(&cfg, qe_decode_attn_kernel<D, W, true>, p);
+  return cudaLaunchKernelEx(&cfg, qe_decode_attn_kernel<D, W, false>, p);
 }
 
 template <int D, int W>
