@@ -31,6 +31,10 @@ struct TokMirror {
   int L = 0;
   int n_tail = 0;     // tail tokens, the pending one included
   int pending = 0;    // appended token whose length the next decode step's merge commits
+  // the pending token's K and V (device-accessible) while it is not written yet: the next
+  // decode step's attention writes it, any other call first writes it with its own launch
+  const uint16_t* pk = nullptr;
+  const uint16_t* pv = nullptr;
 };
 
 }  // namespace qe

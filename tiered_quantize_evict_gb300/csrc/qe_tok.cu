@@ -207,6 +207,8 @@ __device__ __forceinline__ int tk_per_stage(int z) {
 struct TkAttnArgs {
   TokState st;
   int layer, pend;
+  const uint16_t* knew;   // this step's appended token (K, V: [units][D]) to write first, or null
+  const uint16_t* vnew;
   const uint16_t* q;
   float scale_log2;
   float* part_o;
@@ -282,6 +284,42 @@ __device__ __forceinline__ void tk_tile_q(const uint8_t* sp, int nvalid, bool no
   }
 }
 
+// The decode step's own append, by the one warp that owns the tail tile holding the new token:
+// K and V into the tile in fragment order, its position and a zero score.  The stores are made
+// visible at device scope and ordered, by the async-proxy fence, before the bulk copy that later
+// reads the tile.
+__device__ __forceinline__ void tk_append_newest(const TokState& s, int layer, int buf, int u, int idx, int pos,
+                                                 const uint16_t* kn, const uint16_t* vn, int lane) {
+  const int D = s.g.D;
+  if (idx >= s.cap_tail) {
+    if (lane == 0) atomicOr(s.err, ERR_CAPACITY);
+    return;
+  }
+  const long long tb = tk_tail_tok_index(s, layer, buf, u);
+  uint8_t* tile = s.tail + (tb / 16 + idx / 16) * (long long)s.g.bf_tile();
+  const Geo g16{D, 16};
+  const int row = idx & 15;
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {   // channel pairs 2 lane + 64 i (D <= 128)
+    const int c = 2 * lane + 64 * i;
+    if (c < D) {
+      const size_t src = (size_t)u * D + c;
+      const unsigned kk = *reinterpret_cast<const unsigned*>(kn + src);
+      const uint16_t v0 = vn[src], v1 = vn[src + 1];
+      *reinterpret_cast<unsigned*>(tile + bf16_k_off(g16, row, c)) = kk;
+      *reinterpret_cast<uint16_t*>(tile + bf16_v_off(g16, row, c)) = v0;
+      *reinterpret_cast<uint16_t*>(tile + bf16_v_off(g16, row, c + 1)) = v1;
+    }
+  }
+  if (lane == 0) {
+    s.tail_pos[tb + idx] = pos;
+    s.tail_score[tb + idx] = 0.f;
+  }
+  __threadfence();
+  asm volatile("fence.proxy.async;" ::: "memory");
+  __syncwarp();
+}
+
 // whether this decode step adds to the importance (the last score_window steps of a period)
 __device__ __forceinline__ bool tk_scoring(const TokState& s, int step_before) {
   const int sidx = step_before + 1;
@@ -321,6 +359,17 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   }
   const int u_first = tk_unit_of(cum, S.units, tail_cost, x_lo);
   const int u_last = tk_unit_of(cum, S.units, tail_cost, x_hi - 1);
+
+  // this step's appended token (the last tail slot of every unit), written by the warp whose
+  // range holds its tail tile, before that warp issues any copy
+  if (p.knew) {
+    const int idx = n_tail - 1, pc = tk_per_stage<D>(4), ts = (idx >> 4) / pc;   // the stage holding it
+    for (int u = u_first; u <= u_last; ++u) {
+      const TkUnit uu = tk_unit(S, p.layer, u, n_tail);
+      const long long start = tk_X(cum, u, tail_cost) + uu.s0[4] + (long long)ts * pc * S.cost[4];
+      if (start >= x_lo && start < x_hi) tk_append_newest(S, p.layer, buf, u, idx, hd.L, p.knew, p.vnew, lane);
+    }
+  }
 
   uint8_t* stage_base = smem + (size_t)warp * NST * STAGE;
   if (lane == 0) {
@@ -1423,13 +1472,16 @@ cudaError_t tk_launch_commit_pending(const TokState& s, int layer, int pend, cud
   return cudaGetLastError();
 }
 
-cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* q, float scale_log2, float* part_o,
-                           float2* part_ml, float* logits, int lg_cap, int grid, cudaStream_t st) {
+cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* knew, const uint16_t* vnew,
+                           const uint16_t* q, float scale_log2, float* part_o, float2* part_ml, float* logits, int lg_cap,
+                           int grid, cudaStream_t st) {
   const int D = s.g.D;
   TkAttnArgs a;
   a.st = s;
   a.layer = layer;
   a.pend = pend;
+  a.knew = pend > 0 ? knew : nullptr;
+  a.vnew = pend > 0 ? vnew : nullptr;
   a.q = q;
   a.scale_log2 = scale_log2;
   a.part_o = part_o;

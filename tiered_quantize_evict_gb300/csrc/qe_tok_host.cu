@@ -79,9 +79,21 @@ qe_status check(qe_handle h, int layer) {
   return QE_OK;
 }
 
+// Writes the pending token into the tail if no decode step has written it yet.
+qe_status flush_token(qe_handle h, int layer) {
+  TokMirror& m = h->tlay[layer];
+  if (!m.pk) return QE_OK;
+  TK_CK(h, tk_launch_append1(h->ts, layer, m.pk, m.pv, h->stream));
+  ++h->launches;
+  m.pk = m.pv = nullptr;
+  return QE_OK;
+}
+
 qe_status commit(qe_handle h, int layer) {
   TokMirror& m = h->tlay[layer];
   if (!m.pending) return QE_OK;
+  qe_status st = flush_token(h, layer);
+  if (st != QE_OK) return st;
   TK_CK(h, tk_launch_commit_pending(h->ts, layer, m.pending, h->stream));
   ++h->launches;
   m.pending = 0;
@@ -247,28 +259,39 @@ qe_status tok_append(qe_handle h, int layer, const void* k, const void* v, int n
   const size_t bytes = (size_t)s.units * n * h->cfg.head_dim * 2;
   const uint16_t* kd = static_cast<const uint16_t*>(k);
   const uint16_t* vd = static_cast<const uint16_t*>(v);
-  if (flags & QE_HOST_PTRS) {
-    const void* mk = n == 1 ? mapped(k, 4) : nullptr;
-    const void* mv = n == 1 ? mapped(v, 2) : nullptr;
-    if (mk && mv) {   // a pinned token is read in place by the append kernel
-      kd = static_cast<const uint16_t*>(mk);
-      vd = static_cast<const uint16_t*>(mv);
-    } else {
-      void *sk, *sv;
-      if ((st = stage(h, 0, bytes, &sk)) != QE_OK || (st = stage(h, 1, bytes, &sv)) != QE_OK) return st;
-      TK_CK(h, cudaMemcpyAsync(sk, k, bytes, cudaMemcpyHostToDevice, h->stream));
-      TK_CK(h, cudaMemcpyAsync(sv, v, bytes, cudaMemcpyHostToDevice, h->stream));
-      kd = static_cast<const uint16_t*>(sk);
-      vd = static_cast<const uint16_t*>(sv);
-    }
-  }
   if (n == 1) {
-    TK_CK(h, tk_launch_append1(s, layer, kd, vd, h->stream));
-    ++h->launches;
+    // The token is written by the next decode step's attention launch (or by a launch of its
+    // own before any other call reads the layer).  Host memory: pinned is read in place,
+    // pageable is copied now into this layer's staging.
+    if (flags & QE_HOST_PTRS) {
+      const void* mk = mapped(k, 4);
+      const void* mv = mapped(v, 2);
+      if (mk && mv) {
+        kd = static_cast<const uint16_t*>(mk);
+        vd = static_cast<const uint16_t*>(mv);
+      } else {
+        uint16_t* ks = h->tok_stage + (size_t)layer * 2 * s.units * h->cfg.head_dim;
+        uint16_t* vs = ks + (size_t)s.units * h->cfg.head_dim;
+        TK_CK(h, cudaMemcpyAsync(ks, k, bytes, cudaMemcpyHostToDevice, h->stream));
+        TK_CK(h, cudaMemcpyAsync(vs, v, bytes, cudaMemcpyHostToDevice, h->stream));
+        kd = ks;
+        vd = vs;
+      }
+    }
+    m.pk = kd;
+    m.pv = vd;
     m.pending = 1;
     m.L += 1;
     m.n_tail += 1;
     return QE_OK;
+  }
+  if (flags & QE_HOST_PTRS) {
+    void *sk, *sv;
+    if ((st = stage(h, 0, bytes, &sk)) != QE_OK || (st = stage(h, 1, bytes, &sv)) != QE_OK) return st;
+    TK_CK(h, cudaMemcpyAsync(sk, k, bytes, cudaMemcpyHostToDevice, h->stream));
+    TK_CK(h, cudaMemcpyAsync(sv, v, bytes, cudaMemcpyHostToDevice, h->stream));
+    kd = static_cast<const uint16_t*>(sk);
+    vd = static_cast<const uint16_t*>(sv);
   }
   TK_CK(h, tk_launch_append(s, layer, n, prefill, kd, vd, h->n_sm, h->stream));
   h->launches += 2;
@@ -323,9 +346,10 @@ qe_status tok_decode(qe_handle h, int layer, const void* q, void* out, int flags
     ev_flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
     TK_CK(h, cudaEventRecordWithFlags(e0, h->stream, ev_flags));
   }
-  TK_CK(h, tk_launch_attn(h->ts, layer, m.pending, qd, scale_log2, h->tk_part_o, h->tk_part_ml, h->tk_logits,
-                          h->tk_lgcap, h->tk_grid, h->stream));
+  TK_CK(h, tk_launch_attn(h->ts, layer, m.pending, m.pk, m.pv, qd, scale_log2, h->tk_part_o, h->tk_part_ml,
+                          h->tk_logits, h->tk_lgcap, h->tk_grid, h->stream));
   ++h->launches;
+  m.pk = m.pv = nullptr;   // written by this launch
   if (h->timing) {
     TK_CK(h, cudaEventRecordWithFlags(e1, h->stream, ev_flags));
     h->timed_launches += 1;
@@ -406,6 +430,8 @@ struct TokSnapshot {
 
 static qe_status tok_snapshot(qe_handle h, int layer, TokSnapshot& sn, bool scores) {
   const qe::TokState& s = h->ts;
+  qe_status fs = qe::flush_token(h, layer);   // the pending token is read from the tail below
+  if (fs != QE_OK) return fs;
   sn.cnt.assign((size_t)s.units * 4, 0);
   cudaError_t e = cudaStreamSynchronize(h->stream);
   if (e == cudaSuccess)

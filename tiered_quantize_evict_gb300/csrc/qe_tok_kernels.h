@@ -18,8 +18,11 @@ cudaError_t tk_launch_append(const TokState& s, int layer, int n, bool prefill, 
                              int n_sm, cudaStream_t st);
 cudaError_t tk_launch_commit_pending(const TokState& s, int layer, int pend, cudaStream_t st);
 // attention of one decode step, then its merge (a programmatic dependent of the attention)
-cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* q, float scale_log2, float* part_o,
-                           float2* part_ml, float* logits, int lg_cap, int grid, cudaStream_t st);
+// knew / vnew: this step's appended token ([units][head_dim] each, device-accessible), written
+// into the tail by the launch itself; null when it is written already
+cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* knew, const uint16_t* vnew,
+                           const uint16_t* q, float scale_log2, float* part_o, float2* part_ml, float* logits, int lg_cap,
+                           int grid, cudaStream_t st);
 cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float* part_o, const float2* part_ml,
                             const float* logits, int lg_cap, int grid, void* out, int out_fp32, cudaStream_t st);
 // re-rank of one layer and its header switch
