@@ -340,6 +340,10 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   const int G = S.G;
   const int NW = gridDim.x * TK_WARPS;
   const int wg = blockIdx.x * TK_WARPS + warp;
+  // The launch is a programmatic dependent of the kernel before it on the stream (the previous
+  // layer's merge, which reads the split-K scratch this launch rewrites): nothing is read or
+  // written before that kernel has completed.
+  griddep_wait();
   const TokLayer hd = S.hdr[p.layer];
   const int n_tail = hd.n_tail + p.pend;
   const int buf = hd.buf;
@@ -718,6 +722,8 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
   const long long slot0 = w0 + u;
   const TkUnit un = tk_unit(S, p.layer, u, n_tail);
   griddep_wait();
+  // the next layer's attention may now take the SMs this grid leaves (it waits for completion)
+  griddep_launch_dependents();
   if (warp < G) {
     const int h = warp;
     float M = -INFINITY;
@@ -1490,9 +1496,18 @@ cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_
   a.lg_cap = lg_cap;
   const int stage = 64 * D;
   const int nst = TK_STAGE_TOTAL / (TK_WARPS * stage) < 4 ? TK_STAGE_TOTAL / (TK_WARPS * stage) : 4;
-  if (D == 128) tk_attn_kernel<128><<<grid, TK_WARPS * 32, TK_WARPS * nst * stage, st>>>(a);
-  else tk_attn_kernel<64><<<grid, TK_WARPS * 32, TK_WARPS * nst * stage, st>>>(a);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(TK_WARPS * 32);
+  cfg.dynamicSmemBytes = (size_t)TK_WARPS * nst * stage;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (D == 128) return cudaLaunchKernelEx(&cfg, tk_attn_kernel<128>, a);
+  return cudaLaunchKernelEx(&cfg, tk_attn_kernel<64>, a);
 }
 
 // programmatic dependent of the attention launch before it on the stream
