@@ -36,7 +36,6 @@ constexpr float TK_NQ1_C = 0.67448975f;                   // Phi^-1(3/4) rounded
 constexpr int TK_MERGE_THREADS = 512;
 constexpr int TK_MERGE_SPLIT = 4;       // CTAs per unit: each takes a quarter of the outputs and tokens
 constexpr int TK_RERANK_THREADS = 256;
-constexpr int TK_RERANK_WARPS = TK_RERANK_THREADS / 32;
 
 // ------------------------------------------------------------------------------ unit geometry
 struct TkUnit {
@@ -724,6 +723,24 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
   griddep_wait();
   // the next layer's attention may now take the SMs this grid leaves (it waits for completion)
   griddep_launch_dependents();
+  // Output element (h, c) of this CTA's share is summed by TPE adjacent threads, each over the
+  // partials k = q, q + TPE, ...; their first loads are issued here, before the head
+  // statistics that weight them.
+  constexpr int TPE = 4, PF = 8;   // threads per element, partials per thread per round
+  const int e_per = (G * D + TK_MERGE_SPLIT - 1) / TK_MERGE_SPLIT;   // <= TK_MERGE_THREADS / TPE
+  const int e_end = (part + 1) * e_per < G * D ? (part + 1) * e_per : G * D;
+  const int e = part * e_per + tid / TPE, q = tid % TPE;
+  const bool has_e = tid / TPE < e_per && e < e_end;
+  const int h_e = has_e ? e / D : 0, c_e = has_e ? e - h_e * D : 0;
+  float pv[PF];
+  auto load_round = [&](int k0) {
+#pragma unroll
+    for (int j = 0; j < PF; ++j) {
+      const int k = k0 + q + TPE * j;
+      pv[j] = (has_e && k < np) ? __ldg(p.part_o + ((slot0 + k) * G + h_e) * D + c_e) : 0.f;
+    }
+  };
+  load_round(0);
   if (warp < G) {
     const int h = warp;
     float M = -INFINITY;
@@ -744,27 +761,28 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
     }
   }
   __syncthreads();
-  const int e_per = (G * D + TK_MERGE_SPLIT - 1) / TK_MERGE_SPLIT;
-  const int e_end = (part + 1) * e_per < G * D ? (part + 1) * e_per : G * D;
-  for (int e = part * e_per + tid; e < e_end; e += TK_MERGE_THREADS) {
-    const int h = e / D, c = e - h * D;
+  {
     float acc = 0.f;
-    for (int k0 = 0; k0 < np; k0 += 16) {   // 16 partial loads in flight
-      float v[16];
+    for (int k0 = 0; k0 < np; k0 += TPE * PF) {
+      if (k0 > 0) load_round(k0);
 #pragma unroll
-      for (int j = 0; j < 16; ++j) {
-        const int k = k0 + j;
-        v[j] = (k < np && s_sc[h * np + k] != 0.f) ? __ldg(p.part_o + ((slot0 + k) * G + h) * D + c) : 0.f;
+      for (int j = 0; j < PF; ++j) {
+        const int k = k0 + q + TPE * j;
+        if (has_e && k < np) {
+          const float w = s_sc[h_e * np + k];
+          if (w != 0.f) acc = fmaf(pv[j], w, acc);   // an empty partial (never written) weighs 0
+        }
       }
-#pragma unroll
-      for (int j = 0; j < 16; ++j)
-        if (k0 + j < np) acc = fmaf(v[j], s_sc[h * np + k0 + j], acc);
     }
-    const float o = acc * s_inv[h];
-    const int bb = u / S.Hkv, kvh = u - bb * S.Hkv;
-    const size_t oi = ((size_t)bb * S.Hq + kvh * G + h) * D + c;
-    if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
-    else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+#pragma unroll
+    for (int o = 1; o < TPE; o <<= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+    if (has_e && q == 0) {
+      const float o = acc * s_inv[h_e];
+      const int bb = u / S.Hkv, kvh = u - bb * S.Hkv;
+      const size_t oi = ((size_t)bb * S.Hq + kvh * G + h_e) * D + c_e;
+      if (p.out_fp32) reinterpret_cast<float*>(p.out)[oi] = o;
+      else reinterpret_cast<__nv_bfloat16*>(p.out)[oi] = __float2bfloat16_rn(o);
+    }
   }
   if (scoring) {
     const float* lgu = p.logits + (long long)u * p.lg_cap * G;
