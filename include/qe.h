@@ -195,10 +195,15 @@ qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int f
  * position); top Kf -> Full, next Kq -> Quantized, rest -> Evicted (eq. (5)).
  * A window quantized for the first time is packed from its bf16 values (keys
  * per channel over the window's tokens, values per token over head_dim,
- * eq. (2) with b = 2, round half to even, float32 min and scale) and its bf16
- * values and codes are written to the host backing store; a later demotion
- * reuses the stored codes; a promotion copies the stored bf16 values back.
- * All moves complete on the handle's stream before it runs anything else. */
+ * eq. (2) with b = 2, round half to even, float32 min and scale).  A kept
+ * window's exact bf16 values are in the host backing store; its codes stay in
+ * its 2-bit slot after a promotion and are written to the store only when that
+ * slot is handed to another window (int2_slack).  A later demotion reuses the
+ * codes (from the old slot, else the store); a promotion takes back its old
+ * bf16 slot when no window has reused it, else copies the stored values back.
+ * layer = -1 checks every layer first (nothing is routed if one fails) and
+ * routes all of them with one launch of each kernel.  All moves complete on
+ * the handle's stream before it runs anything else. */
 qe_status qe_route(qe_handle h, int layer);
 
 /* ---------------------------------------------------------------- speculative verify
