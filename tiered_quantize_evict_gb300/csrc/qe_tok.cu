@@ -785,34 +785,43 @@ __global__ void __launch_bounds__(TK_MERGE_THREADS) tk_merge_kernel(const TkMerg
     }
   }
   if (scoring) {
+    // The scored tokens of the pools and the tail (sink tokens are never scored) as one range,
+    // split evenly over the unit's CTAs; NF tokens per thread in flight.
     const float* lgu = p.logits + (long long)u * p.lg_cap * G;
+    int base[6];
+    base[0] = 0;
+#pragma unroll
     for (int z = 0; z < 5; ++z) {
-      float* sc;
-      if (z < 4) sc = S.score[z] + tk_pool_tok_index(S, z, p.layer, hd.buf, u);
-      else sc = S.tail_score + tk_tail_tok_index(S, p.layer, hd.buf, u);
-      const int first = z < 4 ? 0 : S.n_sink;   // sink tokens are never scored
-      const int per = (un.n[z] - first + TK_MERGE_SPLIT - 1) / TK_MERGE_SPLIT;
-      const int lo = first + part * per;
-      const int hi = lo + per < un.n[z] ? lo + per : un.n[z];
-      for (int i0 = lo + tid; i0 < hi; i0 += 4 * TK_MERGE_THREADS) {   // 4 tokens in flight
-        float m[4], old[4];
+      const int first = z < 4 ? 0 : S.n_sink;
+      base[z + 1] = base[z] + (un.n[z] > first ? un.n[z] - first : 0);
+    }
+    const int per = (base[5] + TK_MERGE_SPLIT - 1) / TK_MERGE_SPLIT;
+    const int lo = part * per;
+    const int hi = lo + per < base[5] ? lo + per : base[5];
+    constexpr int NF = 8;
+    for (int i0 = lo + tid; i0 < hi; i0 += NF * TK_MERGE_THREADS) {
+      float m[NF], old[NF];
+      float* dst[NF];
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = i0 + j * TK_MERGE_THREADS;
-          m[j] = 0.f;
-          old[j] = 0.f;
-          if (i < hi) {
-            const float* lg = lgu + (long long)(un.tok0[z] + i) * G;
-            for (int h = 0; h < G; ++h) m[j] += ex2(__ldg(lg + h) - s_lse[h]);
-            old[j] = sc[i];
-          }
-        }
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const int i = i0 + j * TK_MERGE_THREADS;
-          if (i < hi) sc[i] = old[j] + m[j];
+      for (int j = 0; j < NF; ++j) {
+        const int gi = i0 + j * TK_MERGE_THREADS;
+        m[j] = 0.f;
+        old[j] = 0.f;
+        dst[j] = nullptr;
+        if (gi < hi) {
+          int z = 0;
+          while (z < 4 && gi >= base[z + 1]) ++z;
+          const int i = gi - base[z] + (z < 4 ? 0 : S.n_sink);
+          dst[j] = (z < 4 ? S.score[z] + tk_pool_tok_index(S, z, p.layer, hd.buf, u)
+                          : S.tail_score + tk_tail_tok_index(S, p.layer, hd.buf, u)) + i;
+          const float* lg = lgu + (long long)(un.tok0[z] + i) * G;
+          for (int h = 0; h < G; ++h) m[j] += ex2(__ldg(lg + h) - s_lse[h]);
+          old[j] = *dst[j];
         }
       }
+#pragma unroll
+      for (int j = 0; j < NF; ++j)
+        if (dst[j]) *dst[j] = old[j] + m[j];
     }
   }
   // commit: the last CTA advances the header
