@@ -472,7 +472,7 @@ __global__ void __launch_bounds__(ROUTE_THREADS) qe_route_kernel(const RoutePara
     }
     // (d) demotions: the previous 2-bit slot if it still holds the window's codes, else a free
     //     slot: the first demotion packs (and, from Pinned, takes a store entry for the exact
-    //     copy), later ones reuse the ledger
+    //     copy), later ones copy the codes back from the host ledger
     for (int c = 0; c < nch; ++c) {
       if (ch_new[c] != TIER_QUANT) continue;
       const int qv = ch_qv[c];
