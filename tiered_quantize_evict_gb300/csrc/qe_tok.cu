@@ -236,9 +236,15 @@ __device__ __forceinline__ void tk_tile_bf16(const uint8_t* sp, int nvalid, cons
   }
 }
 
+// 1-bit keys: the four registers of a channel step are built after one shift of the code word,
+// register r as 1 + code 2^(r - 4) (its code at mantissa bit 3 + r).  The channels of registers
+// 2 and 3 meet the query divided by 4 (qb1, exact), so a row's codes all weigh 2^-4 (row g) or
+// 2^-3 (row g + 8); the row's key scale takes the factor back, and q1sum (the query summed with
+// the same 1 / 4 on those channels) replaces qsum in the offset.
 template <int D, int B>
 __device__ __forceinline__ void tk_tile_q(const uint8_t* sp, int nvalid, bool normal, const unsigned (&qb)[D / 16][2],
-                                          float qsum, TkRun<D / 16>& rs, float* lg, float scale_log2, int G, int lane) {
+                                          const unsigned (&qb1)[D / 16], float qsum, float q1sum, TkRun<D / 16>& rs,
+                                          float* lg, float scale_log2, int G, int lane) {
   constexpr int KS = D / 16, MC = D / 16, WPL = D * B / 64, PW = 4 / B;
   constexpr float TWO_B = (float)(1 << B);
   const TokGeo geo{D};
@@ -251,8 +257,13 @@ __device__ __forceinline__ void tk_tile_q(const uint8_t* sp, int nvalid, bool no
   for (int j = 0; j < 2; ++j) {
     const float2 ka = tk_affine(kp[g + 8 * j], normal);
     const float2 va = tk_affine(vp[g + 8 * j], normal);
-    ksc[j] = TWO_B * ka.y;
-    kbi[j] = fmaf(-TWO_B, ka.y, ka.x) * qsum;
+    if constexpr (B == 1) {
+      ksc[j] = (j ? 8.f : 16.f) * ka.y;
+      kbi[j] = fmaf(-ksc[j], q1sum, ka.x * qsum);
+    } else {
+      ksc[j] = TWO_B * ka.y;
+      kbi[j] = fmaf(-TWO_B, ka.y, ka.x) * qsum;
+    }
     vs[j] = TWO_B * va.y;
     vz[j] = fmaf(-TWO_B, va.y, va.x);
   }
@@ -264,8 +275,15 @@ __device__ __forceinline__ void tk_tile_q(const uint8_t* sp, int nvalid, bool no
     for (int ks = 0; ks < KS; ++ks) {
       const unsigned w = wk[ks / PW];
       const int k = ks % PW;
-      mma_bf16(acc[ks & 1], tk_pair<B, 7, 0x3F80u>(w, k, 0), tk_pair<B, 7, 0x3F80u>(w, k, 1),
-               tk_pair<B, 7, 0x3F80u>(w, k, 2), tk_pair<B, 7, 0x3F80u>(w, k, 3), qb[ks][0], qb[ks][1]);
+      if constexpr (B == 1) {
+        const int sh = 4 * k - 3;   // bit 4 k (register 0 of step k) to bit 3
+        const unsigned x = sh >= 0 ? (w >> sh) : (w << (-sh));
+        mma_bf16(acc[ks & 1], (x & 0x00080008u) | 0x3F803F80u, (x & 0x00100010u) | 0x3F803F80u,
+                 (x & 0x00200020u) | 0x3F803F80u, (x & 0x00400040u) | 0x3F803F80u, qb[ks][0], qb1[ks]);
+      } else {
+        mma_bf16(acc[ks & 1], tk_pair<B, 7, 0x3F80u>(w, k, 0), tk_pair<B, 7, 0x3F80u>(w, k, 1),
+                 tk_pair<B, 7, 0x3F80u>(w, k, 2), tk_pair<B, 7, 0x3F80u>(w, k, 3), qb[ks][0], qb[ks][1]);
+      }
     }
   }
   unsigned Bp[2];
@@ -467,7 +485,8 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   // ---- consumer
   TkRun<MC> rs;
   unsigned qb[KS][2];
-  float qsum = 0.f;
+  unsigned qb1[KS];   // qb[.][1] / 4, for 1-bit keys
+  float qsum = 0.f, q1sum = 0.f;
   int cur_u = u_first, q_unit = -1;
   const int hh = g >> 1;
   const bool lo_col = (g & 1) != 0;
@@ -533,18 +552,26 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
       const int b = cur_u / S.Hkv, kvh = cur_u - b * S.Hkv;
       const uint16_t* qh = p.q + ((size_t)b * S.Hq + kvh * G + hh) * D;
       const bool act = hh < G;
-      float part = 0.f;
+      float part = 0.f, part1 = 0.f;
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
         const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
         part += (bf16lo_to_f32(a0) + bf16hi_to_f32(a0)) + (bf16lo_to_f32(a1) + bf16hi_to_f32(a1));
+        part1 += (bf16lo_to_f32(a0) + bf16hi_to_f32(a0)) + 0.25f * (bf16lo_to_f32(a1) + bf16hi_to_f32(a1));
         qb[ks][0] = lo_col ? 0u : a0;
         qb[ks][1] = lo_col ? 0u : a1;
+        // q / 4 on channels 8..15 of the step, for 1-bit keys (a power-of-two scale: exact)
+        const unsigned q4 = (__float_as_uint(0.25f * bf16lo_to_f32(a1)) >> 16) |
+                            (__float_as_uint(0.25f * bf16hi_to_f32(a1)) & 0xFFFF0000u);
+        qb1[ks] = lo_col ? 0u : q4;
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
       part += __shfl_xor_sync(0xffffffffu, part, 2);
-      qsum = __shfl_sync(0xffffffffu, part, 8 * t);   // sum of q over the channels, head t
+      part1 += __shfl_xor_sync(0xffffffffu, part1, 1);
+      part1 += __shfl_xor_sync(0xffffffffu, part1, 2);
+      qsum = __shfl_sync(0xffffffffu, part, 8 * t);     // sum of q over the channels, head t
+      q1sum = __shfl_sync(0xffffffffu, part1, 8 * t);   // the same with q / 4 on channels 8..15 of each step
     }
     float* lg = scoring ? p.logits + ((long long)d.u * p.lg_cap + d.tokslot) * G : nullptr;
     const int nv0 = d.rem < 16 ? d.rem : 16;
@@ -561,9 +588,9 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
           const int nv = r < 16 ? r : 16;
           const uint8_t* ti = sp + i * tb;
           float* lgi = lg ? lg + 16 * i * G : nullptr;
-          if (d.kind == 1) tk_tile_q<D, 4>(ti, nv, false, qb, qsum, rs, lgi, p.scale_log2, G, lane);
-          else if (d.kind == 2) tk_tile_q<D, 2>(ti, nv, false, qb, qsum, rs, lgi, p.scale_log2, G, lane);
-          else tk_tile_q<D, 1>(ti, nv, true, qb, qsum, rs, lgi, p.scale_log2, G, lane);
+          if (d.kind == 1) tk_tile_q<D, 4>(ti, nv, false, qb, qb1, qsum, q1sum, rs, lgi, p.scale_log2, G, lane);
+          else if (d.kind == 2) tk_tile_q<D, 2>(ti, nv, false, qb, qb1, qsum, q1sum, rs, lgi, p.scale_log2, G, lane);
+          else tk_tile_q<D, 1>(ti, nv, true, qb, qb1, qsum, q1sum, rs, lgi, p.scale_log2, G, lane);
         }
         break;
       }
