@@ -361,8 +361,13 @@ long long qe_kernel_launches(qe_handle h);
  *    the handle.
  * Limits (QE_ERR_CAPACITY beyond them): batch * n_kv_heads <= 16 units; at most 8192 tiles per
  * unit (a tile is 16 bf16 tokens or one 2-bit window); G <= 4; head_dim <= 128.
+ * The handle's device (the one current at qe_init) must be the current device at every call
+ * (QE_ERR_STATE otherwise): the array's address is looked up, and used, for that device only.
  * The first call on each device looks up the array's device address (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.  All calls share
+ * with that device current); make that first call before any stream capture.
+ * QE_ERR_STATE too while the layer awaits qe_verify_commit, as for qe_decode_step.
+ * qe_set_timing does not cover this entry point: its launches are not timed or counted by
+ * qe_get_timing.  All calls share
  * the one array: calls whose work may overlap on the GPU (other streams, other handles on the
  * same device) race on it and must be serialised by the caller.  Nothing in the array needs to
  * start at zero: each call writes every scratch value it reads.  Like qe_decode_step, it counts

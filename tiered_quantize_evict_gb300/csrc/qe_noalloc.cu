@@ -63,6 +63,9 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   if (layer < 0 || layer >= h->cfg.n_layers) return na_fail(h, QE_ERR_INVALID_ARG, "layer %d out of range", layer);
   if (!q || !out) return na_fail(h, QE_ERR_INVALID_ARG, "noalloc decode needs device q and out");
   qe::LayerMirror& m = h->lay[layer];
+  // a speculative verify leaves uncommitted drafts in the layer: attending over them here would
+  // add their masses to the scores, which the commit could not take back
+  if (m.verify_n) return na_fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", layer);
   if (m.L < 1) return na_fail(h, QE_ERR_STATE, "decode on an empty layer");
   const int W = h->cfg.window, D = h->cfg.head_dim, G = h->st.G;
   if (h->units > NA_MAX_UNITS)
@@ -76,10 +79,14 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
                    NA_MAX_TILES, ntiles);
   if (G > NA_MAX_G || D > NA_MAX_D) return na_fail(h, QE_ERR_CAPACITY, "noalloc decode: head shape too large");
 
-  // device address of the static scratch on the current device (looked up once per device)
+  // Device address of the static scratch on the handle's device (looked up once per device).
+  // The kernels run on the handle's stream, which belongs to the device the handle was created
+  // on; the array's address is only valid there, so that device must be the current one.
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return na_fail(h, QE_ERR_CUDA, "cudaGetDevice: %s", cudaGetErrorString(e));
+  if (dev != h->device)
+    return na_fail(h, QE_ERR_STATE, "the current device %d is not the handle's device %d", dev, h->device);
   if (dev < 0 || dev >= NA_MAX_DEVICES) return na_fail(h, QE_ERR_INVALID_ARG, "device %d out of range", dev);
   unsigned char* base = nullptr;
   {

@@ -558,12 +558,15 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
         const unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
         const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
         part += (bf16lo_to_f32(a0) + bf16hi_to_f32(a0)) + (bf16lo_to_f32(a1) + bf16hi_to_f32(a1));
-        part1 += (bf16lo_to_f32(a0) + bf16hi_to_f32(a0)) + 0.25f * (bf16lo_to_f32(a1) + bf16hi_to_f32(a1));
         qb[ks][0] = lo_col ? 0u : a0;
         qb[ks][1] = lo_col ? 0u : a1;
-        // q / 4 on channels 8..15 of the step, for 1-bit keys (a power-of-two scale: exact)
+        // q / 4 on channels 8..15 of the step, for 1-bit keys: exact while q / 4 stays a normal
+        // float32 (|q| >= 2^-124); below that the bf16 truncation drops bits.  The offset sum
+        // takes the truncated operands themselves, so it matches what the tensor core multiplies
+        // in every case.
         const unsigned q4 = (__float_as_uint(0.25f * bf16lo_to_f32(a1)) >> 16) |
                             (__float_as_uint(0.25f * bf16hi_to_f32(a1)) & 0xFFFF0000u);
+        part1 += (bf16lo_to_f32(a0) + bf16hi_to_f32(a0)) + (bf16lo_to_f32(q4) + bf16hi_to_f32(q4));
         qb1[ks] = lo_col ? 0u : q4;
       }
       part += __shfl_xor_sync(0xffffffffu, part, 1);
