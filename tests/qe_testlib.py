@@ -8,7 +8,10 @@ Comparison protocol
 * 2-bit codes: identical; float32 min/scale: bitwise identical;
 * tiers: identical at every routing event, unless the oracle's cutoff margin (lowest kept
   score minus highest dropped score, H2O page §5.1) at a changed cut is below 1e-4 relative:
-  then both branches are correct and the unit is no longer compared (the two runs diverge).
+  then both branches are correct, the two runs diverge and the unit is no longer compared.
+  Such a unit is recorded with its margin; every test then calls ``assert_all_live``, so a run
+  in which any compared unit stopped being compared fails (none of the seeded cases has a cut
+  that close).
 """
 from __future__ import annotations
 
@@ -234,6 +237,11 @@ class ParityRun:
                 self.ambiguous += 1
                 continue
             self.check_codes(tr)
+
+    def assert_all_live(self):
+        """Every tracked unit was compared to the end (no tie-ambiguous routing event)."""
+        dropped = [(tr.b, tr.layer, tr.kvh, tr.note) for tr in self.tracked if not tr.live]
+        assert not dropped and self.ambiguous == 0, f"units no longer compared: {dropped}"
 
     def check_codes(self, tr: Tracked, windows: Optional[List[int]] = None):
         wl = self.wl

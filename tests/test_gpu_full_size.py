@@ -99,6 +99,7 @@ def test_throughput_32k_sampled_units_graph_replay():
     print(f"full-size sampled parity: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
           f"2-bit windows compared {run.codes_checked}, Full windows compared {full_checked}, "
           f"tie-ambiguous units {run.ambiguous} {[tr.note for tr in run.tracked if tr.note]}")
+    run.assert_all_live()
     assert run.codes_checked > 0 and full_checked > 0
 
 
@@ -125,6 +126,7 @@ def test_llama8b_stack_byte_budget_sampled_units():
     print(f"llama8b_stack: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
           f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}, "
           f"tie-ambiguous {run.ambiguous} {[tr.note for tr in run.tracked if tr.note]}")
+    run.assert_all_live()
     assert run.codes_checked > 0
 
 
@@ -142,6 +144,7 @@ def test_long_131k_sampled_units():
     print(f"long_131k: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
           f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}, Kf {info.kf}, Kq {info.kq}, "
           f"tie-ambiguous {run.ambiguous}")
+    run.assert_all_live()
     assert run.codes_checked > 0
 
 
@@ -155,4 +158,5 @@ def test_throughput_32k_pre_rope_sampled_units():
     full_checked = sum(run.check_bf16_windows(tr) for tr in run.tracked if tr.live)
     print(f"throughput_32k_rope: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
           f"2-bit windows compared {run.codes_checked}, Full windows {full_checked}")
+    run.assert_all_live()
     assert run.codes_checked > 0

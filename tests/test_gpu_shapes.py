@@ -47,8 +47,7 @@ def test_trajectory_parity(name):
         run.step()
     run.check_scores()
     run.cache.qe_synchronize()
-    live = sum(tr.live for tr in run.tracked)
-    assert live >= len(run.tracked) - 1, [tr.note for tr in run.tracked if not tr.live]
+    run.assert_all_live()
     assert run.codes_checked > 0
     for tr in run.tracked:
         if tr.live:
@@ -70,7 +69,7 @@ def test_host_buffers_trajectory(host):
         run.step()
     run.check_scores()
     run.cache.qe_synchronize()
-    assert sum(tr.live for tr in run.tracked) >= len(run.tracked) - 1
+    run.assert_all_live()
     assert run.codes_checked > 0 and run.route_events == wl.decode_steps // wl.route_period
     print(f"host {host}: out err {run.max_out_err:.2e}, score rel err {run.max_score_err:.2e}, "
           f"codes {run.codes_checked}")
@@ -97,7 +96,7 @@ def test_pre_rope_keys_trajectory(name):
         run.step()
     run.check_scores()
     run.cache.qe_synchronize()
-    assert sum(tr.live for tr in run.tracked) >= len(run.tracked) - 1
+    run.assert_all_live()
     assert run.codes_checked > 0
     for tr in run.tracked:
         if tr.live:

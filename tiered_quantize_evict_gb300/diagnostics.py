@@ -12,8 +12,8 @@ Definitions (QEvict reading notes §3, H2O page §5.1):
 * dropped mass at a decode step: the attention mass, under an uncompressed cache, that falls on
   windows the compressed cache has evicted, as a fraction of the step's total (the G query
   heads of a KV head each carry mass 1);
-* future missed mass (FMM) of a routing event: the dropped mass of the windows evicted by that
-  event, averaged over the decode steps that follow it.
+* future missed mass (FMM) of a routing event: the dropped mass of the windows evicted at or
+  before that event (eviction is final), averaged over the decode steps that follow it.
 
 The uncompressed distribution comes from a companion cache fed the same inputs whose routing
 keeps every window Full (fixed capacities, K_f larger than any window count): its per-window
