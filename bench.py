@@ -179,9 +179,23 @@ def run_ours(args):
     K, W = args.steps, args.warmup
     NQ = max(1, args.verify)          # tokens per step: a speculative verify of NQ drafts, all kept
     verify = args.verify > 0
-    pre = (omega + NQ - 1) // NQ      # steps through the first routing event
-    # steps: pre-roll (all-bf16 cache, first routing event), W warm-up, K timed, K roofline, K e2e
-    total_steps = pre + W + 3 * K
+
+    def routes_at(t):
+        return (t * NQ) // omega > ((t - 1) * NQ) // omega
+
+    def next_route_step(t):           # first step >= t that ends with a routing event
+        while not routes_at(t):
+            t += 1
+        return t
+
+    pre = next_route_step(1)          # steps through the first routing event
+    # The warm-up ends with a routing event, so the timed region starts right after one and each
+    # whole Omega-token period inside it holds exactly one event.
+    W_eff = next_route_step(pre + W) - pre
+    P = next_route_step(pre + 1) - pre          # steps between routing events
+    KR = max(K, P)                              # per-launch timing leg: sees at least one event
+    # steps: pre-roll, warm-up, K timed, KR per-launch timing, up to P aligning, K end to end
+    total_steps = pre + W_eff + K + KR + P + K
     max_ctx = wl.prefill + max(wl.decode_steps, (total_steps + pre + 1) * NQ)
     stream = torch.cuda.Stream(dev)     # capturable: all work of this run is ordered on it
     torch.cuda.set_stream(stream)
@@ -223,9 +237,6 @@ def run_ours(args):
     out = torch.empty(NQ, B, Hq, D, device=dev, dtype=torch.float32) if verify else \
         torch.empty(B, Hq, D, device=dev, dtype=torch.float32)
 
-    def routes_at(t):
-        return (t * NQ) // omega > ((t - 1) * NQ) // omega
-
     def step(t, k, v, q, o=out, route_events=None):
         for layer in range(Lyr):
             if verify:
@@ -245,11 +256,12 @@ def run_ours(args):
                 cache.qe_route(-1)
 
     t = 0
-    for _ in range(pre + W):            # pre-roll through the first routing event, then warm-up
+    for _ in range(pre + W_eff):        # pre-roll through the first routing event, then warm-up
         t += 1
         k, v, q = make_inputs(t)
         step(t, k, v, q)
     cache.qe_synchronize()
+    t_timed0 = t + 1
 
     # The K timed decode steps of the whole stack captured as one CUDA graph and launched once:
     # every step's inputs sit in their own device buffers, as a model's projections would leave
@@ -289,13 +301,13 @@ def run_ours(args):
     del timed
 
     # per-launch attention times: the same step, launched directly with CUDA events around
-    # every qe_decode_attn launch on the handle's stream
-    rl = [make_inputs(t + 1 + i) for i in range(K)]
+    # every qe_decode_attn launch on the handle's stream, and around every routing call
+    rl = [make_inputs(t + 1 + i) for i in range(KR)]
     torch.cuda.synchronize(dev)
     route_events = []
     rs0 = _route_counts(cache)
     cache.set_timing(True)
-    for i in range(K):
+    for i in range(KR):
         t += 1
         step(t, *rl[i], route_events=route_events)
     torch.cuda.synchronize(dev)
@@ -306,6 +318,15 @@ def run_ours(args):
     route_steps = [ts * NQ for ts, _ in route_events]
     cache.qe_synchronize()
     del rl
+
+    # align: the end-to-end leg, like the timed one, starts right after a routing event
+    if not routes_at(t):
+        for _ in range(next_route_step(t) - t):
+            t += 1
+            step(t, *make_inputs(t))
+    cache.qe_synchronize()
+    t_e2e0 = t + 1
+    e2e_routes = sum(routes_at(t + 1 + i) for i in range(K))
 
     # end to end through the C ABI with host buffers: pinned inputs copied in and the
     # outputs read back every step, inside the timed region
@@ -331,6 +352,17 @@ def run_ours(args):
     e2e_ms = max(e2.elapsed_time(e3), (time.perf_counter() - t_e2e0) * 1e3)
     cache.qe_synchronize()
 
+    # Routing belongs to every step (one event per Omega tokens).  A timed region of K steps that
+    # starts right after an event holds floor(K NQ / Omega) of them; when K is not a whole
+    # number of periods, the missing fraction of an event is added at the measured mean cost
+    # of the events of the per-launch leg.
+    per_k = K * NQ / omega
+    route_mean = sum(route_ms) / len(route_ms) if route_ms else 0.0
+    graph_ms = ms_total
+    add_ms = max(0.0, per_k - n_routes) * route_mean
+    add_e2e_ms = max(0.0, per_k - e2e_routes) * route_mean
+    ms_total = graph_ms + add_ms
+    e2e_ms = e2e_ms + add_e2e_ms
     ms_total = max_over_ranks(ms_total, world, dev)
     e2e_ms = max_over_ranks(e2e_ms, world, dev)
     value = whole_job_rate(B * NQ * K, world, ms_total)
@@ -351,11 +383,19 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic (seeded qe_inputs generator, device-side)",
         "config": {
             **workload_config(wl, world),
-            "timed_decode_steps": [pre + W + 1, pre + W + K],
+            "timed_decode_steps": [t_timed0, t_timed0 + K - 1],
             "launch": ("the K timed steps as one CUDA graph (per step %d layers x token append, attention, merge; "
-                       "re-rank every Omega)" % Lyr) if tok else
+                       "re-rank every Omega), started right after a re-rank" % Lyr) if tok else
                       ("the K timed steps as one CUDA graph (per step %d layers x attention with the token "
-                       "append, combine; routing every Omega)" % Lyr),
+                       "append, combine; routing every Omega), started right after a routing event" % Lyr),
+            "routing_in_value": {
+                "events_per_K_steps_at_one_per_Omega": round(per_k, 4),
+                "events_in_timed_graph": n_routes,
+                "added_ms_for_missing_fraction": round(add_ms, 4),
+                "graph_ms": round(graph_ms, 4),
+                "rule": "value = tokens / (graph time + (K NQ / Omega - events in the graph) x mean measured "
+                        "event time); the timed graph starts right after an event, so it holds the whole "
+                        "periods' events itself and only a partial period is added"},
             ("kv_tokens_per_layer_unit" if tok else "kv_per_layer_unit"): kv_unit,
             "l2": "inputs larger than L2: %.0f MB read per layer launch, %.1f GB per step (a layer's data is "
                   "read again only after the other layers' data)" % (info.attn_bytes / 1e6, info.attn_bytes * Lyr / 1e9),
@@ -370,7 +410,7 @@ def run_ours(args):
             "algorithmic_bytes_per_launch": round(attn_bytes / max(attn_launches, 1)),
             "avg_launch_us": round(attn_ms * 1e3 / max(attn_launches, 1), 2),
             "attn_share_of_step": round(attn_ms / ms_total, 4) if ms_total > 0 else None,
-            "measured_on": "the next K decode steps launched directly, CUDA events around each launch",
+            "measured_on": "the next %d decode steps launched directly, CUDA events around each launch" % KR,
         },
         "routing": {
             "events": len(route_ms),
@@ -378,11 +418,12 @@ def run_ours(args):
             "ms_per_event": [round(x, 3) for x in route_ms],
             "ms_per_step_amortized": round(sum(route_ms) / K, 4),
             "counts": {kk: rs1[kk] - rs0[kk] for kk in rs1} if rs0 and rs1 else None,
-            "measured_on": ("the same K direct-launch steps, CUDA events around each qe_route(-1) call "
-                            "(every layer's %s and moves)" % ("re-rank" if tok else "routing")),
+            "measured_on": ("%d direct-launch steps after the timed ones, CUDA events around each qe_route(-1) "
+                            "call (every layer's %s and moves)" % (KR, "re-rank" if tok else "routing")),
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h,
+                "d2h_bytes_per_step": d2h, "decode_steps": [t_e2e0, t_e2e0 + K - 1],
+                "routing_events_timed": e2e_routes, "added_ms_for_missing_fraction": round(add_e2e_ms, 4),
                 "path": "direct C-ABI calls on pinned host buffers: queries copied in, new K/V read "
                         "and outputs written in place by the kernels over the host link"},
         "gpu_launches": launches,
@@ -453,10 +494,15 @@ def oracle_baseline(workload: str, n_units: int, n_steps: int, n_warm: int = 0):
         res = pool.map(_oracle_worker, jobs)
     per_unit_step = sum(sum(r[n_warm:]) for r in res) / (n_units * n_steps)   # seconds, one core
     step_s = per_unit_step * units_total / workers                       # all units, `workers` cores
+    # what one step of the sample itself took: the units run side by side, one per core
+    sample_step_s = max(sum(r[n_warm:]) for r in res) / n_steps * math.ceil(n_units / workers)
     return {"value": round(wl.batch / step_s, 4), "unit": "tokens/s", "cores": workers, "kind": "oracle",
+            "extrapolated": True, "sample_ms_per_step": round(sample_step_s * 1e3, 3),
+            "extrapolated_ms_per_step": round(step_s * 1e3, 3),
             "sample": f"{n_units} units x {n_steps} timed steady-state decode steps (after the first routing "
                       f"event and {n_warm} untimed warm-up steps) of {workload}, extrapolated to all "
-                      f"{units_total} units on {workers} cores; setup (prefill, pre-roll, first route) untimed"}, step_s
+                      f"{units_total} units on {workers} cores; setup (prefill, pre-roll, first route) untimed"}, \
+        step_s, sample_step_s
 
 
 def run_reference(args):
@@ -469,11 +515,14 @@ def run_reference(args):
     # each step: one decode step of `cores` sampled units (bounded sample of the workload)
     n_units = max(1, min(cores, 16))
     t0 = time.perf_counter()
-    base, step_s = oracle_baseline(args.workload, n_units, args.steps, n_warm=args.warmup)
+    base, step_s, sample_step_s = oracle_baseline(args.workload, n_units, args.steps, n_warm=args.warmup)
     wall = time.perf_counter() - t0
     v = base["value"]
+    # ms_per_step is what one step of the bounded sample took here (the run's own clock);
+    # value is the whole workload's rate extrapolated from it (cpu_baseline.extrapolated_ms_per_step)
     return {"impl": "reference", "metric": METRIC, "value": v, "unit": "tokens/s", "n_gpus": world,
-            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(step_s * 1e3, 3),
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sample_step_s * 1e3, 3),
+            "extrapolated": True, "extrapolated_ms_per_step": round(step_s * 1e3, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic (seeded qe_inputs generator)",
             "config": workload_config(wl, world),
@@ -506,7 +555,7 @@ def main():
     line = run_ours(args)
     if rank == 0:
         if world == 1 and not args.no_cpu_baseline:
-            base, _ = oracle_baseline(args.workload, n_units=min(16, len(os.sched_getaffinity(0))), n_steps=2)
+            base, _, _ = oracle_baseline(args.workload, n_units=min(16, len(os.sched_getaffinity(0))), n_steps=2)
             line["cpu_baseline"] = base
         print(json.dumps(line), flush=True)
 
