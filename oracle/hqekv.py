@@ -31,11 +31,11 @@ Readings where the pages leave a step open
   Phi^-1((j + 1) / 2^b), where the two probability masses are equal, and a
   value on a boundary takes the lower center.  For b = 1 the centers are
   +-0.6745 and the boundary is 0: the code is 1 exactly when x > m.
-* Mean and population standard deviation are computed in float32 (the precision the
-  pages leave open; the CUDA path decides codes in it): two passes, each sum in one
-  fixed order (per-lane partials over channels l, l + 32, ..., then a pairwise
-  butterfly over the 32 partials), every operation rounded once; s = 0 gives all-zero
-  codes.
+* Mean and population standard deviation (eq. (3)) are the exact values for the
+  token's float32 entries, each rounded once to the nearest float32 (ties to even): m =
+  round(sum x / D), s = round(sqrt(sum (x - mean)^2 / D)) with the exact mean inside the
+  square.  The pages fix neither a precision nor an order of summation; exact values
+  rounded once depend on neither.  s = 0 gives all-zero codes.
 * Uniform decisions are eq. (2) in float32 as in ``oracle.quant``.
 * Dequantization is one float32 fused multiply-add, code * s + z (uniform) or
   c_j * s + m (normal); re-quantization to a lower tier starts from those
@@ -146,31 +146,64 @@ def normal_boundaries(bits: int) -> np.ndarray:
     return _symmetric([(j + 1) / n for j in range(n - 1)])
 
 
-def _lane_sum(x):
-    """float32 sum of each row of x [n, D] (D a multiple of 32) in a fixed order: partial j of
-    32 is x[j] + x[j + 32] + ... left to right, then the partials are combined pairwise, each
-    partial j with partial j xor o for o = 16, 8, 4, 2, 1 (every step one float32 add)."""
-    x = np.asarray(x, np.float32)
-    n, D = x.shape
-    a = x[:, 0:32].copy()
-    for k in range(1, D // 32):
-        a = (a + x[:, 32 * k:32 * (k + 1)]).astype(np.float32)
-    lanes = np.arange(32)
-    for o in (16, 8, 4, 2, 1):
-        a = (a + a[:, lanes ^ o]).astype(np.float32)
-    return a[:, 0]
+def _f32_exp_floor(num: int, den: int) -> int:
+    """floor(log2(num / den)) for integers num, den > 0."""
+    e = num.bit_length() - den.bit_length()
+    if (num << max(0, -e)) < (den << max(0, e)):
+        e -= 1
+    return e
+
+
+def _f32_from_ratio(num: int, den: int) -> np.float32:
+    """num / den (integers, den > 0) rounded to the nearest float32, ties to even, with
+    subnormals (the spacing of float32 values below 2^-126 is 2^-149)."""
+    if num == 0:
+        return F32(0.0)
+    a = abs(num)
+    q = max(_f32_exp_floor(a, den) - 23, -149)          # exponent of the result's last place
+    n, r = divmod(a << -q, den) if q < 0 else divmod(a, den << q)
+    rd = den if q < 0 else den << q
+    if 2 * r > rd or (2 * r == rd and n & 1):
+        n += 1
+    v = F32(math.ldexp(n, q))                              # exact: n <= 2^24
+    return -v if num < 0 else v
+
+
+def _f32_sqrt_of_ratio(num: int, den: int) -> np.float32:
+    """sqrt(num / den) (integers, num >= 0, den > 0) rounded to the nearest float32, ties to
+    even: n = floor(sqrt(y)) for y = num / (den 4^q) from an integer square root, then one
+    exact comparison of y with (n + 1/2)^2."""
+    if num == 0:
+        return F32(0.0)
+    q = max(_f32_exp_floor(num, den) // 2 - 23, -149)
+    if q < 0:
+        ynum, yden = num << (-2 * q), den
+    else:
+        ynum, yden = num, den << (2 * q)
+    n = math.isqrt(ynum // yden)
+    lhs, rhs = 4 * ynum, (4 * n * n + 4 * n + 1) * yden    # y vs (n + 1/2)^2, times 4 yden
+    if lhs > rhs or (lhs == rhs and n & 1):
+        n += 1
+    return F32(math.ldexp(n, q))
 
 
 def mean_std_f32(x):
-    """Per-row mean and population std of x [n, D] (float32) in float32: m = sum / D,
-    s = sqrt(sum((x - m)^2) / D), the sums in the order of ``_lane_sum``, every operation
-    rounded once (no fused multiply-add)."""
+    """Per-row mean and population std of x [n, D] (float32), each the exact value rounded
+    once to float32 (ties to even).  Every float32 is an integer multiple of 2^-149, so with
+    X_i = x_i 2^149, S = sum X_i and Q = sum X_i^2 (exact integers):
+    mean = S / (D 2^149) and std = sqrt((D Q - S^2) / (D^2 2^298))."""
     x = np.asarray(x, np.float32)
     n, D = x.shape
-    m = (_lane_sum(x) / np.float32(D)).astype(np.float32)
-    d = (x - m[:, None]).astype(np.float32)
-    q = _lane_sum((d * d).astype(np.float32))
-    return m, np.sqrt((q / np.float32(D)).astype(np.float32)).astype(np.float32)
+    ints = np.ldexp(x.astype(np.float64), 149)             # exact: integers below 2^277
+    m = np.zeros(n, np.float32)
+    sd = np.zeros(n, np.float32)
+    for r in range(n):
+        X = [int(v) for v in ints[r]]
+        S = sum(X)
+        Q = sum(v * v for v in X)
+        m[r] = _f32_from_ratio(S, D << 149)
+        sd[r] = _f32_sqrt_of_ratio(D * Q - S * S, (D * D) << 298)
+    return m, sd
 
 
 def normal_quantize(x, bits: int = 1):

@@ -90,18 +90,107 @@ def test_mean_std_match_the_closed_form():
         assert np.allclose(s, xd.std(axis=1), rtol=1e-6)
 
 
-def test_mean_std_exact_when_every_step_is_exact():
-    # integer rows with a sum divisible by D: every add, the division by D, x - m and (x - m)^2
-    # are exact in float32, so m and the variance are exact and s is the rounded square root
-    rng = np.random.default_rng(11)
+def _f32_neighbours(c):
+    c = np.float32(c)
+    out = {float(c)}
+    lo = hi = c
+    for _ in range(3):
+        lo = np.nextafter(lo, np.float32(-np.inf))
+        hi = np.nextafter(hi, np.float32(np.inf))
+        out |= {float(lo), float(hi)}
+    return sorted(v for v in out if math.isfinite(v))
+
+
+def _even(v):
+    return int(np.array([v], np.float32).view(np.uint32)[0]) & 1 == 0
+
+
+def _nearest_f32(t: Fraction) -> float:
+    """The float32 nearest the rational t (ties to even), by exact comparison among the float32
+    values around float(t)."""
+    best = None
+    for c in _f32_neighbours(float(t)):
+        d = abs(Fraction(c) - t)
+        if best is None or d < best[0] or (d == best[0] and _even(c)):
+            best = (d, c)
+    return best[1]
+
+
+def _nearest_f32_sqrt(v: Fraction) -> float:
+    """The float32 nearest sqrt(v) (ties to even): candidate c_i wins when sqrt(v) lies between
+    the midpoints it shares with its neighbours, decided by comparing v with their squares."""
+    cands = [c for c in _f32_neighbours(math.sqrt(float(v))) if c >= 0]
+    for i, c in enumerate(cands):
+        lo = (Fraction(cands[i - 1]) + Fraction(c)) / 2 if i > 0 else None
+        hi = (Fraction(c) + Fraction(cands[i + 1])) / 2 if i + 1 < len(cands) else None
+        above_lo = lo is None or v > lo * lo or (v == lo * lo and _even(c))
+        below_hi = hi is None or v < hi * hi or (v == hi * hi and _even(c))
+        if above_lo and below_hi:
+            return c
+    raise AssertionError("sqrt outside the candidates")
+
+
+def _adversarial_rows(D, rng):
+    rows = []
+    big = np.float32(3e38)
+    rows.append(np.full(D, big, np.float32))                        # a float32 sum would overflow
+    r = np.ones(D, np.float32); r[-1] = np.float32(1 + 2.0 ** -17)  # mean exactly between 1 and
+    rows.append(r)                                                  # its successor: ties to even
+    r = np.zeros(D, np.float32); r[3] = np.float32(1.5)             # one nonzero value
+    rows.append(r)
+    r = (rng.standard_normal(D) * 1e3).astype(np.float32)           # cancellation: +-x pairs and a
+    r[D // 2:] = -r[:D // 2]; r[0] = np.float32(r[0] + np.float32(1e-3))   # small residual
+    rows.append(r)
+    r = rng.standard_normal(D).astype(np.float32)                   # magnitudes 2^-100 .. 2^100
+    r *= np.exp2(rng.integers(-100, 101, D)).astype(np.float32)
+    rows.append(r)
+    r = (rng.integers(1, 1000, D) * 2.0 ** -149).astype(np.float32)  # subnormals only
+    rows.append(r)
+    r = rng.standard_normal(D).astype(np.float32); r[::7] = np.float32(1e-30)   # tiny beside O(1)
+    rows.append(r)
+    rows.append(np.full(D, np.float32(-2.75), np.float32))           # constant row: s = 0
+    r = rng.standard_normal(D).astype(np.float32); r[5] = np.float32(1e30)      # one huge value
+    rows.append(r)
+    return np.stack(rows)
+
+
+def test_mean_std_are_the_exact_values_rounded_once():
+    """eq. (3)'s mean and population std: the exact values for the row, rounded once to the
+    nearest float32 (ties to even), against Fraction arithmetic, bit for bit, on random rows and
+    on rows chosen to break any fixed-order float32 or float64 summation."""
+    rng = np.random.default_rng(31)
     for D in (64, 128):
-        x = rng.integers(-100, 101, (40, D)).astype(np.int64)
-        x[:, -1] -= x.sum(axis=1) % D          # sum divisible by D (the last value moves a little)
-        m, s = H.mean_std_f32(x.astype(np.float32))
-        me = x.sum(axis=1) // D
-        var = ((x - me[:, None]) ** 2).sum(axis=1) / D
-        assert np.array_equal(m, me.astype(np.float32))
-        assert np.array_equal(s, np.sqrt(var).astype(np.float32))
+        x = np.concatenate([(rng.standard_normal((12, D)) * rng.uniform(0.1, 10, (12, 1))).astype(np.float32),
+                            _adversarial_rows(D, rng)])
+        m, s = H.mean_std_f32(x)
+        for r in range(x.shape[0]):
+            fx = [Fraction(float(v)) for v in x[r]]
+            mu = sum(fx) / D
+            var = sum((f - mu) ** 2 for f in fx) / D
+            assert float(m[r]) == _nearest_f32(mu), (D, r, m[r], float(mu))
+            assert float(s[r]) == _nearest_f32_sqrt(var), (D, r, s[r], math.sqrt(float(var)))
+    # the tie row: exact mean 1 + 2^-24 lies halfway between 1 and 1 + 2^-23, so it rounds to 1
+    m, _ = H.mean_std_f32(_adversarial_rows(128, rng)[1:2])
+    assert m[0] == np.float32(1.0)
+    # the row whose float32 sum would overflow still has mean 3e38 and std 0
+    m, s = H.mean_std_f32(_adversarial_rows(64, rng)[0:1])
+    assert m[0] == np.float32(3e38) and s[0] == 0
+
+
+def test_mean_std_closed_forms_of_structured_rows():
+    # one nonzero value a among D: mean a / D (exact, D a power of two), std |a| sqrt(D - 1) / D
+    for D in (64, 128):
+        for a in (1.5, -3.0, 1e-20, 7e30):
+            x = np.zeros((1, D), np.float32)
+            x[0, 0] = np.float32(a)
+            m, s = H.mean_std_f32(x)
+            assert m[0] == np.float32(np.float32(a) / D)
+            want = _nearest_f32_sqrt(Fraction(float(np.float32(a))) ** 2 * (D - 1) / D ** 2)
+            assert float(s[0]) == want
+    # two values +-c in equal numbers: mean 0, std |c| exactly
+    x = np.tile(np.array([2.5, -2.5], np.float32), 64)[None, :]
+    m, s = H.mean_std_f32(x)
+    assert m[0] == 0 and s[0] == np.float32(2.5)
 
 
 def test_fmaf32_rounds_once():
