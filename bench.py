@@ -325,7 +325,7 @@ def run_ours(args):
             t += 1
             step(t, *make_inputs(t))
     cache.qe_synchronize()
-    t_e2e0 = t + 1
+    step_e2e0 = t + 1
     e2e_routes = sum(routes_at(t + 1 + i) for i in range(K))
 
     # end to end through the C ABI with host buffers: pinned inputs copied in and the
@@ -409,7 +409,7 @@ def run_ours(args):
             "traffic": _traffic(wl.name, "tk_attn" if tok else "qe_decode_attn"),
             "algorithmic_bytes_per_launch": round(attn_bytes / max(attn_launches, 1)),
             "avg_launch_us": round(attn_ms * 1e3 / max(attn_launches, 1), 2),
-            "attn_share_of_step": round(attn_ms / ms_total, 4) if ms_total > 0 else None,
+            "attn_share_of_step": round((attn_ms / KR) / (ms_total / K), 4) if ms_total > 0 else None,
             "measured_on": "the next %d decode steps launched directly, CUDA events around each launch" % KR,
         },
         "routing": {
@@ -422,7 +422,7 @@ def run_ours(args):
                             "call (every layer's %s and moves)" % (KR, "re-rank" if tok else "routing")),
         },
         "e2e": {"value": round(e2e_val, 2), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "decode_steps": [t_e2e0, t_e2e0 + K - 1],
+                "d2h_bytes_per_step": d2h, "decode_steps": [step_e2e0, step_e2e0 + K - 1],
                 "routing_events_timed": e2e_routes, "added_ms_for_missing_fraction": round(add_e2e_ms, 4),
                 "path": "direct C-ABI calls on pinned host buffers: queries copied in, new K/V read "
                         "and outputs written in place by the kernels over the host link"},

@@ -333,3 +333,77 @@ def test_hqe_16k_sampled_units_graph_replay():
     print(f"hqe_16k: max out rel-L2 {stats['out']:.2e}, max score rel {stats['score']:.2e}, codes {stats['codes']}, "
           f"counts layer 0 unit 0 {cache.token_counts(0)[0].tolist()}")
     assert stats["codes"] > 0
+
+
+def _adversarial_bf16_rows(D, rng):
+    """bf16 rows whose exact mean and std stress the rebuild's 1-bit statistics: values 2^50
+    below their neighbours (the wide path), magnitudes from 2^-60 to 2^8, bf16 subnormals,
+    tiny normals, a constant row, cancelling pairs, one nonzero value, and a row whose exact
+    mean 1 + 2^-24 lies halfway between two float32 values."""
+    rows = []
+    r = rng.standard_normal(D).astype(np.float32)
+    r[::5] *= np.float32(2.0 ** -50)
+    rows.append(r)
+    rows.append(rng.standard_normal(D).astype(np.float32) * np.exp2(rng.integers(-60, 9, D)).astype(np.float32))
+    rows.append((rng.integers(-120, 121, D) * 2.0 ** -133).astype(np.float32))   # subnormal bf16
+    rows.append((rng.standard_normal(D) * 1e-35).astype(np.float32))
+    rows.append(np.full(D, 1.5, np.float32))
+    r = rng.standard_normal(D).astype(np.float32) * 4
+    r[D // 2:] = -r[:D // 2]
+    r[1] = np.float32(r[1] * np.float32(1.0078125))
+    rows.append(r)
+    r = np.zeros(D, np.float32)
+    r[7] = np.float32(-2.25)
+    rows.append(r)
+    r = np.ones(D, np.float32)
+    r[0], r[1] = np.float32(2.0), np.float32(2.0 ** -17)
+    r[2:] = 1.0
+    r[-1] = 0.0
+    rows.append(r)
+    return gen.bf16_bits_rne(np.stack(rows))   # rounded to bf16 (most rows already are bf16 values)
+
+
+class PlantedTokRun(TokRun):
+    """A five-tier run whose prefill carries adversarial key and value rows at chosen positions."""
+
+    def __init__(self, wl, plant):
+        super().__init__(wl)
+        self.plant = plant   # position -> (key bits [D], value bits [D])
+
+    def prefill(self):
+        wl = self.wl
+        for layer in range(wl.n_layers):
+            K, V = host_kv(wl, layer, 0, wl.prefill, wl.batch)
+            for p, (kr, vr) in self.plant.items():
+                K[:, :, p] = kr
+                V[:, :, p] = vr
+            self.cache.qe_append(layer, self.place(K), self.place(V), wl.prefill)
+            self.cache.qe_synchronize()
+            for b in range(wl.batch):
+                for h in range(wl.n_kv_heads):
+                    self.units[(b, layer, h)].append(gen.bf16_bits_to_f32(K[b, h]), gen.bf16_bits_to_f32(V[b, h]))
+
+
+@pytest.mark.parametrize("D", [128, 64])
+def test_five_tier_adversarial_rows_one_bit(D):
+    """Adversarial rows reach the 1-bit tier through the rebuild kernel (90 % of the ranked tokens
+    go 1-bit): their codes and float32 mean and std equal the oracle's exact values rounded once,
+    bit for bit, and attention over them follows the oracle."""
+    G = 4 if D == 128 else 2
+    wl = dataclasses.replace(BASE, name=f"adversarial_d{D}", head_dim=D, n_q_heads=2 * G, n_kv_heads=2, batch=1,
+                             n_layers=1, prefill=300, decode_steps=16, route_period=16, score_window=0, n_sink=4,
+                             n_recent=16, frac_bf16=0.1, frac_int4=0.0, frac_int2=0.0, frac_nq1=0.9, seed=77 + D)
+    rng = np.random.default_rng(D)
+    krows, vrows = _adversarial_bf16_rows(D, rng), _adversarial_bf16_rows(D, rng)[::-1]
+    plant = {}
+    for i in range(3 * len(krows)):                  # each row three times, at spread positions
+        plant[30 + 9 * i] = (krows[i % len(krows)], vrows[(i + 1) % len(vrows)])
+    run = PlantedTokRun(wl, plant)
+    run.prefill()
+    for _ in range(wl.decode_steps):
+        run.step()
+    run.cache.qe_synchronize()
+    one_bit = sum(int(run.units[(0, 0, h)].tier[p] == H.NQ1) for h in range(wl.n_kv_heads) for p in plant)
+    print(f"adversarial d{D}: planted tokens in the 1-bit tier {one_bit} of {2 * len(plant)}, "
+          f"codes compared {run.codes_checked}, max out rel-L2 {run.max_out:.2e}")
+    assert run.codes_checked > 0 and one_bit >= len(plant)

@@ -24,6 +24,7 @@
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
+#include "qe_exact_stats.cuh"
 #include "qe_tok.cuh"
 #include "qe_tok_kernels.h"
 
@@ -1135,6 +1136,57 @@ __host__ __device__ constexpr unsigned tk_vmask(int hf, int rb) {
   return m;
 }
 
+// Mean and population std of one row of D float32 values in shared memory (HqeKV reading notes,
+// §2.3 eq. (3)), each the exact value rounded once to float32 (qe_exact_stats.cuh).  Every lane
+// turns its D / 32 values into integers at the row's scale and the warp adds the integer sums;
+// a row whose nonzero values span more than the fast path's window goes to the wide path on
+// lane 0.  Every lane returns the same m and sd.
+template <int D>
+__device__ __forceinline__ void tk_row_mean_std(const float* x, int lane, float& m, float& sd) {
+  constexpr int NV = D / 32, LGD = D == 128 ? 7 : 6;
+  float v[NV];
+  unsigned E = 0u;
+#pragma unroll
+  for (int i = 0; i < NV; ++i) {
+    v[i] = x[lane + 32 * i];
+    const xs::Parts pt = xs::parts(v[i]);
+    if (pt.mant && (unsigned)pt.ee > E) E = (unsigned)pt.ee;
+  }
+  E = __reduce_max_sync(0xffffffffu, E);
+  if (E == 0u) {   // all zeros
+    m = 0.f;
+    sd = 0.f;
+    return;
+  }
+  xs::FastAcc a{0, 0, 0};
+#pragma unroll
+  for (int i = 0; i < NV; ++i) xs::fast_add(a, v[i], (int)E);
+  if (__any_sync(0xffffffffu, a.bad)) {
+    float mw = 0.f, sw = 0.f;
+    if (lane == 0) {
+      xs::WideAcc w;
+      xs::wide_zero(w);
+      for (int c = 0; c < D; ++c) xs::wide_acc(w, x[c]);
+      xs::wide_finish(w, LGD, mw, sw);
+    }
+    m = __shfl_sync(0xffffffffu, mw, 0);
+    sd = __shfl_sync(0xffffffffu, sw, 0);
+    return;
+  }
+  long long S = a.s;
+  unsigned long long qlo = (unsigned long long)a.q, qhi = (unsigned long long)(a.q >> 64);
+#pragma unroll
+  for (int o = 16; o; o >>= 1) {
+    S += __shfl_xor_sync(0xffffffffu, S, o);
+    const unsigned long long lo2 = __shfl_xor_sync(0xffffffffu, qlo, o);
+    const unsigned long long hi2 = __shfl_xor_sync(0xffffffffu, qhi, o);
+    const xs::u128 sum = (((xs::u128)qhi << 64) | qlo) + (((xs::u128)hi2 << 64) | lo2);
+    qlo = (unsigned long long)sum;
+    qhi = (unsigned long long)(sum >> 64);
+  }
+  xs::fast_finish(S, ((xs::u128)qhi << 64) | qlo, (int)E, LGD, m, sd);
+}
+
 // Rows of one destination tile of the B-bit tier (1-bit: the normal quantizer).  Rows that keep
 // their tier move word-wise: a row's fields sit in fixed lanes and bit positions, so moving it
 // from source row s to destination row d is a mask, a shift and an or per code word.  Rows
@@ -1223,28 +1275,13 @@ __device__ void tk_rebuild_qtile(const TokState& s, int layer, int buf, int u, T
     __syncwarp();
     // 2. quantize the rows arriving from another tier
     if (B == 1) {
-      // eqs. (3)-(4), b = 1: mean and population std in float32, each sum as per-lane partials
-      // over channels lane, lane + 32, ... then a xor butterfly, every operation rounded once
-      // (no contraction); code 1 where x > mean
+      // eqs. (3)-(4), b = 1: the row's exact mean and population std, each rounded once to
+      // float32; code 1 where x > mean (all zeros when the std is 0)
       for (int row = 0; row < 16; ++row) {
         if (!W.need[row]) continue;
         const float* x = W.vals + row * TK_VROW;
-        float a = x[lane];
-#pragma unroll
-        for (int c = lane + 32; c < D; c += 32) a = __fadd_rn(a, x[c]);
-#pragma unroll
-        for (int o = 16; o; o >>= 1) a = __fadd_rn(a, __shfl_xor_sync(0xffffffffu, a, o));
-        const float m = __fdiv_rn(a, (float)D);
-        float dl = __fsub_rn(x[lane], m);
-        float q = __fmul_rn(dl, dl);
-#pragma unroll
-        for (int c = lane + 32; c < D; c += 32) {
-          dl = __fsub_rn(x[c], m);
-          q = __fadd_rn(q, __fmul_rn(dl, dl));
-        }
-#pragma unroll
-        for (int o = 16; o; o >>= 1) q = __fadd_rn(q, __shfl_xor_sync(0xffffffffu, q, o));
-        const float sd = __fsqrt_rn(__fdiv_rn(q, (float)D));
+        float m, sd;
+        tk_row_mean_std<D>(x, lane, m, sd);
 #pragma unroll
         for (int c = lane; c < D; c += 32) W.codes[row * 128 + c] = (uint8_t)(sd > 0.f && x[c] > m);
         if (lane == 0) W.par[row] = make_float2(m, sd);
