@@ -178,6 +178,10 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
 
 /* One decode step of one layer (QEvict notes §4.1 eq. "attention"; H2O page
  * §2.1 order: the token appended last is attended too).
+ * Any finite bf16 keys, values and queries are served: 2-bit windows whose parameters, with
+ * the step's queries, would push the tensor-core operands out of the f16 range take bf16
+ * operands instead (decided per window from magnitudes recorded when it was packed), and keys
+ * stored pre-RoPE always meet the queries in tf32.
  * q:   [batch][n_q_heads][head_dim] bf16.
  * out: [batch][n_q_heads][head_dim] float32 (out_fp32) or bf16.
  * Computes softmax(q K_acc^T / sqrt(d)) V_acc over the sink, the Pinned and
@@ -342,6 +346,26 @@ qe_status qe_get_token(qe_handle h, int layer, int unit, int pos, int* tier, uin
 
 /* Number of kernel launches the handle has enqueued since qe_init. */
 long long qe_kernel_launches(qe_handle h);
+
+/* ---------------------------------------------------------------- fault injection (tests)
+ *
+ * Not part of the method on the pages (H2O page §5.1 asks for failure canaries and a fallback;
+ * this is how the library's failure paths are exercised).  Every injection acts on the host or
+ * on a wait whose data has already arrived: none faults, traps or hangs a GPU.
+ *  QE_DEBUG_FAIL_DEVICE_ALLOC (h unused, may be NULL; process-wide): value n >= 1 makes the n-th
+ *    device allocation of the next qe_init fail as out of memory: qe_init frees what it had
+ *    allocated and returns QE_ERR_OOM naming the buffer.  0 clears.  One-shot.
+ *  QE_DEBUG_FAIL_HOST_STORE (h unused; process-wide): value != 0 makes the pinned host backing
+ *    store allocation of the next window-tiered qe_init fail: QE_ERR_HOST_STORE.  One-shot.
+ *  QE_DEBUG_EXPIRE_WAIT (h required): value k >= 1: in the handle's next decode step
+ *    (qe_decode_step of either tiering), every warp of the attention launch that streams at
+ *    least k tiles reports its k-th tile wait as expired once that tile's copy has landed,
+ *    lets its other copies land and leaves.  The sticky device flag then makes qe_synchronize
+ *    return QE_ERR_TIMEOUT, as a real expiry (0.2 s without data) would; that step's outputs
+ *    and score updates are undefined.  0 clears.
+ * Errors: QE_ERR_INVALID_ARG (unknown kind, negative value, NULL handle for the wait). */
+enum { QE_DEBUG_FAIL_DEVICE_ALLOC = 1, QE_DEBUG_FAIL_HOST_STORE = 2, QE_DEBUG_EXPIRE_WAIT = 3 };
+qe_status qe_debug_inject(qe_handle h, int what, long long value);
 
 /* ---------------------------------------------------------------- no-allocation decode step
  *

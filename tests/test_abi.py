@@ -57,3 +57,13 @@ def test_init_reports_errors_without_crashing(lib):
         st = lib.qe_init(ctypes.byref(cfg), None, ctypes.byref(h))
         assert st == qe.QE_ERR_CUDA and lib.qe_last_error(None)
     assert lib.qe_append(None, 0, None, None, 1, 0) == qe.QE_ERR_INVALID_ARG
+
+
+def test_debug_inject_validates_its_arguments(lib):
+    """qe_debug_inject acts on host state only; its argument checks need no GPU."""
+    import tiered_quantize_evict_gb300 as qe
+    assert lib.qe_debug_inject(None, qe.QE_DEBUG_EXPIRE_WAIT, 1) == qe.QE_ERR_INVALID_ARG   # needs a handle
+    assert lib.qe_debug_inject(None, 99, 1) == qe.QE_ERR_INVALID_ARG
+    assert lib.qe_debug_inject(None, qe.QE_DEBUG_FAIL_DEVICE_ALLOC, -1) == qe.QE_ERR_INVALID_ARG
+    assert lib.qe_debug_inject(None, qe.QE_DEBUG_FAIL_DEVICE_ALLOC, 0) == qe.QE_OK
+    assert lib.qe_debug_inject(None, qe.QE_DEBUG_FAIL_HOST_STORE, 0) == qe.QE_OK

@@ -29,8 +29,9 @@ EXPORTED = [
     "qe_get_quant_window", "qe_get_bf16_window", "qe_get_route_stats", "qe_set_timing",
     "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc", "qe_get_route_diag",
     "qe_get_token_tiers", "qe_get_token_scores", "qe_get_token_counts", "qe_get_token",
-    "qe_verify", "qe_verify_commit",
+    "qe_verify", "qe_verify_commit", "qe_debug_inject",
 ]
+QE_DEBUG_FAIL_DEVICE_ALLOC, QE_DEBUG_FAIL_HOST_STORE, QE_DEBUG_EXPIRE_WAIT = 1, 2, 3
 QE_VERIFY_MAX = 16
 QE_TIERING_WINDOWS, QE_TIERING_TOKENS = 0, 1
 TOK_BF16, TOK_INT4, TOK_INT2, TOK_NQ1, TOK_EVICTED, TOK_ABSENT = 0, 1, 2, 3, 4, 255
@@ -116,6 +117,7 @@ def load_library() -> ctypes.CDLL:
         "qe_get_token": ([P, I, I, I, ctypes.POINTER(I), P, P, P, P, P], I),
         "qe_verify": ([P, I, P, P, P, P, I, I], I),
         "qe_verify_commit": ([P, I, I], I),
+        "qe_debug_inject": ([P, I, ctypes.c_longlong], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -139,6 +141,13 @@ def _is_host(x) -> bool:
     if isinstance(x, np.ndarray):
         return True
     return not x.is_cuda
+
+
+def debug_inject(what: int, value: int, cache: Optional["QECache"] = None) -> int:
+    """qe_debug_inject: host-side fault injection for tests (returns the status code)."""
+    lib = load_library()
+    h = cache.h if cache is not None else None
+    return int(lib.qe_debug_inject(h, what, value))
 
 
 class QECache:

@@ -26,6 +26,14 @@
 //    (1 + code / 4).  The factor 4 goes into the logit scale (keys) and the B operand
 //    (4 p s_V for values); the constant 1 into the key bias (q . (z_K / 4 - s_K)) and the value
 //    offset (p . (z_V - 4 s_V)).  Dequantized values never exist in memory.
+//  * Magnitudes: f16 holds those products while |q| s_K < 2^15 and 2^-13 <= s_V < 2^5.  Each
+//    2-bit slot carries a record of its largest key scale and its largest and smallest value
+//    scales (written when the slot receives codes); a tile whose record, with the unit's largest
+//    query, says otherwise takes bf16 operands: the key products as three exact bf16 parts in
+//    two mma passes, the value products as bf16 truncated + remainder.
+//  * Keys stored pre-RoPE are rotated in float32 and meet the query as tf32 truncated +
+//    remainder parts (m16n8k8; tf32 keeps float32's exponent range, the bf16 query is exact),
+//    so no key or query magnitude leaves the operand format.
 //  * Per-window mass leaves the kernel as a log-sum-exp per (tile, head); the combine kernel
 //    turns it into a probability mass once the unit's global softmax normaliser is known.
 #include <cstdint>
@@ -46,6 +54,7 @@ struct TileDesc {
   int lo, hi;      // valid rows inside the tile
   int kind;        // 0 bf16 sub-tile, 1 2-bit window
   int sub;         // bf16 sub-tile index inside its window slot
+  int range;       // 2-bit window: its slot's range record (qrange_word)
 };
 
 // What the consumer needs of a tile (written per stage by the producer lane).
@@ -182,6 +191,7 @@ __device__ __forceinline__ bool describe(const AttnParams& p, const Lay& y, int 
     atomicOr(st.err, ERR_TABLE);
     return false;
   }
+  d.range = st.qrange[((long long)p.layer * st.units + u) * st.capq + ent.y];
   d.lo = (ent.x == 0) ? st.n_sink : 0;
   d.hi = W;
   return true;
@@ -344,10 +354,11 @@ struct RunState {
 };
 
 // acc[mt][f][.] are split accumulators of the Q K^T products of token tile mt (summed here).
-template <int MT, int NF, int MC, bool INT2>
+template <int MT, int NF, int MC, bool INT2, bool WIDE = false>
 __device__ __forceinline__ void softmax_tile(float (&acc)[MT][NF][4], bool full, int lo, int hi, float bias,
                                              const float (&vz)[2 * MT], const float (&vs)[2 * MT], float scale_log2,
-                                             RunState<MC>& st, unsigned (&Bp)[MT][2], float* lse_out, int G, int lane) {
+                                             RunState<MC>& st, unsigned (&Bp)[MT][2], float* lse_out, int G, int lane,
+                                             bool pbf16 = false) {
   const int g = lane >> 2, t = lane & 3;
   float x[MT][2];   // rows g and g + 8 of each token tile
 #pragma unroll
@@ -405,7 +416,10 @@ __device__ __forceinline__ void softmax_tile(float (&acc)[MT][NF][4], bool full,
   st.l += mass;
   if (g == 0 && t < G) lse_out[t] = mass > 0.f ? muse + lg2(mass) : -INFINITY;
   // P^T fragments in D layout: (row g: hi, lo of head t), (row g+8: ...), then transposed
-  constexpr unsigned KEEP = INT2 ? 0xFFFFE000u : 0xFFFF0000u;
+  // 2-bit values meet f16 codes (f16 truncated + remainder), or bf16 codes on a wide tile (WIDE,
+  // or at run time pbf16)
+  constexpr bool F16 = INT2 && !WIDE;
+  const unsigned KEEP = (F16 && !pbf16) ? 0xFFFFE000u : 0xFFFF0000u;
 #pragma unroll
   for (int mt = 0; mt < MT; ++mt) {
     unsigned rr[2];
@@ -414,7 +428,7 @@ __device__ __forceinline__ void softmax_tile(float (&acc)[MT][NF][4], bool full,
       float y = pr[mt][j];
       if constexpr (INT2) y *= vs[mt * 2 + j];
       const float yh = __uint_as_float(__float_as_uint(y) & KEEP);
-      if constexpr (INT2) rr[j] = pack_f16x2_rz(yh, y - yh);
+      if constexpr (F16) rr[j] = pbf16 ? pack_bf16x2_rz(yh, y - yh) : pack_f16x2_rz(yh, y - yh);
       else rr[j] = pack_bf16x2_rz(yh, y - yh);
     }
     Bp[mt][0] = movmatrix_t(rr[0]);
@@ -428,16 +442,19 @@ __device__ __forceinline__ void softmax_tile(float (&acc)[MT][NF][4], bool full,
 __device__ __forceinline__ float2 rope_cs(float2 b, float2 o) {
   return make_float2(fmaf(b.x, o.x, -b.y * o.y), fmaf(b.y, o.x, b.x * o.y));
 }
-// the channel pair (x0, x1) rotated by (cos, sin), as an f16x2 truncated part and an f16x2
-// remainder: 22 bits of the rotated key reach the f16 mma against the query (the bf16 query is
-// exact in f16 inside the f16 range)
-__device__ __forceinline__ void rope_rot_split(float x0, float x1, float2 cs, unsigned& hi, unsigned& lo) {
+// The channel pair (x0, x1) rotated by (cos, sin), each rotated value as a tf32 truncated part
+// and a tf32-truncated remainder (22 bits together; tf32 keeps float32's exponent range, so no
+// key magnitude leaves it, and the bf16 query is exact in tf32).  In the m16n8k8 tf32 mma a lane
+// holds k = t and k = t + 4 of its rows: k = t carries channel 2i and k = t + 4 channel 2i + 1 of
+// the lane's pair i, the same mapping for the query's B fragment (b0 = q_2i, b1 = q_2i+1).
+__device__ __forceinline__ void rope_rot_tf32(float x0, float x1, float2 cs, unsigned& h0, unsigned& h1, unsigned& l0,
+                                              unsigned& l1) {
   const float y0 = fmaf(x0, cs.x, -x1 * cs.y);
   const float y1 = fmaf(x0, cs.y, x1 * cs.x);
-  const float h0 = __uint_as_float(__float_as_uint(y0) & 0xFFFFE000u);
-  const float h1 = __uint_as_float(__float_as_uint(y1) & 0xFFFFE000u);
-  hi = pack_f16x2_rz(h0, h1);
-  lo = pack_f16x2_rz(y0 - h0, y1 - h1);
+  h0 = __float_as_uint(y0) & 0xFFFFE000u;
+  h1 = __float_as_uint(y1) & 0xFFFFE000u;
+  l0 = __float_as_uint(y0 - __uint_as_float(h0)) & 0xFFFFE000u;
+  l1 = __float_as_uint(y1 - __uint_as_float(h1)) & 0xFFFFE000u;
 }
 constexpr int ROPE_OFF_STRIDE_PAD = 4;   // float2 padding of a row of the offset table in shared memory
 
@@ -526,7 +543,12 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         bd.sd.lse_off = (u * y.ntiles + d.i) * G;
         bd.sd.meta = d.lo | (d.hi << 8) | (d.kind << 16);
         // 16-token block of the tile's first row (its position / 16; the sink tile is block 0)
-        bd.sd.pad = ROPE ? (d.win < 0 ? 0 : d.win * (W / 16) + (d.kind == 0 ? d.sub : 0)) : 0;
+        // (the default kernel: a 2-bit window's range record instead)
+        // (keys stored pre-RoPE: the block, and bit 30 set when a 2-bit window's value products
+        // need bf16 operands; the default kernel: a 2-bit window's range record)
+        bd.sd.pad = ROPE ? (d.win < 0 ? 0 : d.win * (W / 16) + (d.kind == 0 ? d.sub : 0)) |
+                               (d.kind && qrange_values_wide(d.range) ? (1 << 30) : 0)
+                         : (d.kind ? d.range : 0);
         bd.pad = 0;
         batch[__popc(vb & ((1u << lane) - 1))] = bd;
       }
@@ -566,6 +588,10 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   RunState<MC> rs;
   unsigned long long qf[KS][2];   // q of head g/2 at channels (16ks + 2t, +1), (+8, +9), as fp32 pairs
   unsigned qb[KS][2];      // bf16 B fragments: q of head g/2 in even columns, 0 in odd ones
+  // keys stored pre-RoPE: tf32 B fragments of the two m16n8k8 per channel step (q_2i, q_2i+1 of
+  // pair t, then of pair t + 4), q of head g/2 in even columns, 0 in odd ones
+  unsigned qt[ROPE ? KS : 1][4];
+  int qexp = 0;            // largest biased exponent of the unit's queries (qrange_wide)
   int cur_u = u_first;
   int q_unit = -1;
   auto reset = [&]() {
@@ -617,7 +643,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   int k = 0;
   for (; k < issued; ++k) {
     const int s = k % NST;
-    if (!wait_tile(k)) { timed_out = true; break; }
+    // (a test can make the k-th wait report expiry; the tile's copy has landed by then)
+    if (!wait_tile(k) || k + 1 == p.debug_expire) { timed_out = true; break; }
     const StageDesc sd = descs[warp][s];
     const int d_lo = sd.meta & 0xFF, d_hi = (sd.meta >> 8) & 0xFF, d_kind = sd.meta >> 16;
     const uint8_t* sp = stage_base + (size_t)s * S::STAGE;
@@ -631,41 +658,51 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       const int b = cur_u / p.st.Hkv, kvh = cur_u - b * p.st.Hkv;
       const uint16_t* qh = p.q + ((size_t)b * p.st.Hq + kvh * G + hh) * D;
       const bool act = hh < G;
+      unsigned qmaxbits = 0u;   // largest |q| bits (bf16 pairs: both halves' magnitudes)
 #pragma unroll
       for (int ks = 0; ks < KS; ++ks) {
         const unsigned a0 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 2 * t) : 0u;
         const unsigned a1 = act ? *reinterpret_cast<const unsigned*>(qh + ks * 16 + 8 + 2 * t) : 0u;
+        qmaxbits = max(qmaxbits, max(max(a0 & 0x7FFFu, (a0 >> 16) & 0x7FFFu), max(a1 & 0x7FFFu, (a1 >> 16) & 0x7FFFu)));
         qf[ks][0] = f2_pack(bf16lo_to_f32(a0), bf16hi_to_f32(a0));
         qf[ks][1] = f2_pack(bf16lo_to_f32(a1), bf16hi_to_f32(a1));
-        if constexpr (ROPE) {   // f16 B fragments (exact for queries inside the f16 range)
-          qb[ks][0] = lo_col ? 0u : pack_f16x2_rz(bf16lo_to_f32(a0), bf16hi_to_f32(a0));
-          qb[ks][1] = lo_col ? 0u : pack_f16x2_rz(bf16lo_to_f32(a1), bf16hi_to_f32(a1));
-        } else {
-          qb[ks][0] = lo_col ? 0u : a0;
-          qb[ks][1] = lo_col ? 0u : a1;
+        qb[ks][0] = lo_col ? 0u : a0;
+        qb[ks][1] = lo_col ? 0u : a1;
+        if constexpr (ROPE) {
+          qt[ks][0] = lo_col ? 0u : (a0 << 16);
+          qt[ks][1] = lo_col ? 0u : (a0 & 0xFFFF0000u);
+          qt[ks][2] = lo_col ? 0u : (a1 << 16);
+          qt[ks][3] = lo_col ? 0u : (a1 & 0xFFFF0000u);
         }
       }
+      qexp = (int)(__reduce_max_sync(0xffffffffu, qmaxbits) >> 7);
     }
     float* lse_out = p.lse + sd.lse_off;
     if (d_kind == 0) {
-      // ---- bf16 sub-tile: 16 tokens; two accumulators halve the mma dependency chain
+      // ---- bf16 sub-tile: 16 tokens; independent accumulators shorten the mma dependency
+      //      chains (two for stored keys, one per part for rotated keys)
       float acc[1][2][4] = {};
       if constexpr (ROPE) {
         // registers: (row g, pair 8 ks + t), (row g + 8, same), (row g, pair 8 ks + 4 + t), (row g + 8, same);
-        // rotated keys meet the query as f16 truncated + remainder parts
-        const float2* bt = p.rope_blk + (size_t)sd.pad * (D / 2);
+        // rotated keys meet the query as tf32 truncated + remainder parts, one m16n8k8 per pair
+        // block of four pairs and part
+        const float2* bt = p.rope_blk + (size_t)(sd.pad & 0x3FFFFFFF) * (D / 2);
 #pragma unroll
         for (int ks = 0; ks < KS; ++ks) {
           const uint4 a = lds128(sp + ks * 512 + lane * 16);
           const int i0 = 8 * ks + t, i1 = i0 + 4;
           const float2 b0 = bt[i0], b1 = bt[i1];
-          unsigned h[4], l[4];
-          rope_rot_split(bf16lo_to_f32(a.x), bf16hi_to_f32(a.x), rope_cs(b0, s_roff[g * ROS + i0]), h[0], l[0]);
-          rope_rot_split(bf16lo_to_f32(a.y), bf16hi_to_f32(a.y), rope_cs(b0, s_roff[(g + 8) * ROS + i0]), h[1], l[1]);
-          rope_rot_split(bf16lo_to_f32(a.z), bf16hi_to_f32(a.z), rope_cs(b1, s_roff[g * ROS + i1]), h[2], l[2]);
-          rope_rot_split(bf16lo_to_f32(a.w), bf16hi_to_f32(a.w), rope_cs(b1, s_roff[(g + 8) * ROS + i1]), h[3], l[3]);
-          mma_f16(acc[0][ks & 1], h[0], h[1], h[2], h[3], qb[ks][0], qb[ks][1]);
-          mma_f16(acc[0][ks & 1], l[0], l[1], l[2], l[3], qb[ks][0], qb[ks][1]);
+          unsigned h[8], l[8];   // [pair block][row][channel of the pair]
+          rope_rot_tf32(bf16lo_to_f32(a.x), bf16hi_to_f32(a.x), rope_cs(b0, s_roff[g * ROS + i0]), h[0], h[2], l[0], l[2]);
+          rope_rot_tf32(bf16lo_to_f32(a.y), bf16hi_to_f32(a.y), rope_cs(b0, s_roff[(g + 8) * ROS + i0]), h[1], h[3], l[1],
+                        l[3]);
+          rope_rot_tf32(bf16lo_to_f32(a.z), bf16hi_to_f32(a.z), rope_cs(b1, s_roff[g * ROS + i1]), h[4], h[6], l[4], l[6]);
+          rope_rot_tf32(bf16lo_to_f32(a.w), bf16hi_to_f32(a.w), rope_cs(b1, s_roff[(g + 8) * ROS + i1]), h[5], h[7], l[5],
+                        l[7]);
+          mma_tf32(acc[0][0], h[0], h[1], h[2], h[3], qt[ks][0], qt[ks][1]);
+          mma_tf32(acc[0][1], l[0], l[1], l[2], l[3], qt[ks][0], qt[ks][1]);
+          mma_tf32(acc[0][0], h[4], h[5], h[6], h[7], qt[ks][2], qt[ks][3]);
+          mma_tf32(acc[0][1], l[4], l[5], l[6], l[7], qt[ks][2], qt[ks][3]);
         }
       } else {
 #pragma unroll
@@ -699,7 +736,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
         }
         float acc[MT][2][4] = {};
           // keys dequantized per element (one float32 fma), rotated at their positions, then split
-          // into f16 truncated and remainder parts against the f16 query; register r of fragment
+          // into tf32 truncated + remainder parts against the tf32 query; register r of fragment
           // F holds the codes of channels 2i, 2i + 1 at bits 8 (F & 1) + 2 r and 16 above
           unsigned wk[WPL];
           load_words<WPL, CW>(sp, lane, wk);
@@ -716,114 +753,211 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
             for (int mt = 0; mt < MT; ++mt) {
               const int F = mt * KS + ks;
               const unsigned w = wk[F >> 1];
-              const float2* bt = p.rope_blk + (size_t)(sd.pad + mt) * (D / 2);
+              const float2* bt = p.rope_blk + (size_t)((sd.pad & 0x3FFFFFFF) + mt) * (D / 2);
               const float2 b0 = bt[i0], b1 = bt[i1];
-              unsigned h[4], l[4];
+              unsigned h[8], l[8];   // [pair block][row][channel of the pair]
 #pragma unroll
               for (int r = 0; r < 4; ++r) {
                 const int sh = 8 * (F & 1) + 2 * r;
                 const int pc = (r >> 1) * 2;   // channel pair (2t, 2t+1) or (2t+8, 2t+9)
                 const float x0 = fmaf((float)((w >> sh) & 3u), ksv[pc], kzv[pc]);
                 const float x1 = fmaf((float)((w >> (sh + 16)) & 3u), ksv[pc + 1], kzv[pc + 1]);
-                rope_rot_split(x0, x1, rope_cs(r < 2 ? b0 : b1, o[r]), h[r], l[r]);
+                const int e = 4 * (r >> 1) + (r & 1);   // register r: row g + 8 (r & 1), pair block r >> 1
+                rope_rot_tf32(x0, x1, rope_cs(r < 2 ? b0 : b1, o[r]), h[e], h[e + 2], l[e], l[e + 2]);
               }
-              mma_f16(acc[mt][ks & 1], h[0], h[1], h[2], h[3], qb[ks][0], qb[ks][1]);
-              mma_f16(acc[mt][ks & 1], l[0], l[1], l[2], l[3], qb[ks][0], qb[ks][1]);
+              mma_tf32(acc[mt][0], h[0], h[1], h[2], h[3], qt[ks][0], qt[ks][1]);
+              mma_tf32(acc[mt][1], l[0], l[1], l[2], l[3], qt[ks][0], qt[ks][1]);
+              mma_tf32(acc[mt][0], h[4], h[5], h[6], h[7], qt[ks][2], qt[ks][3]);
+              mma_tf32(acc[mt][1], l[4], l[5], l[6], l[7], qt[ks][2], qt[ks][3]);
             }
           }
+        // values meet f16 codes (4 p s_V as f16 truncated + remainder, 22 bits), or bf16 codes
+        // when the window's value scales could leave the f16 range (bit 30 of the descriptor)
         unsigned Bp[MT][2];
-        softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, 0.f, vz, vs, p.scale_log2, rs, Bp, lse_out, G,
-                                      lane);
+        const bool vwide = (sd.pad >> 30) & 1;
+        softmax_tile<MT, 2, MC, true, false>(acc, d_lo == 0, d_lo, d_hi, 0.f, vz, vs, p.scale_log2, rs, Bp, lse_out,
+                                             G, lane, vwide);
         // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
         // the outer loop, so consecutive mma go to the MC independent accumulators
         {
           unsigned wv[WPL];
           load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
+          if (!vwide) {
 #pragma unroll
-          for (int kt = 0; kt < KT; ++kt)
+            for (int kt = 0; kt < KT; ++kt)
 #pragma unroll
-            for (int mc = 0; mc < MC; ++mc) {
-              const int F = mc * KT + kt;
-              unsigned a[4];
-              if (F & 1) unpack_half<1>(wv[F >> 1], a);
-              else unpack_half<0>(wv[F >> 1], a);
-              mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
-            }
+              for (int mc = 0; mc < MC; ++mc) {
+                const int F = mc * KT + kt;
+                unsigned a[4];
+                if (F & 1) unpack_half<1>(wv[F >> 1], a);
+                else unpack_half<0>(wv[F >> 1], a);
+                mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
+              }
+          } else {
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt)
+#pragma unroll
+              for (int mc = 0; mc < MC; ++mc) {
+                const int F = mc * KT + kt;
+                unsigned a[4];
+                if (F & 1) unpack_half_bf16<1>(wv[F >> 1], a);
+                else unpack_half_bf16<0>(wv[F >> 1], a);
+                mma_bf16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
+              }
+          }
         }
       } else {
-        // ---- 2-bit window: W tokens
-        const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
-        const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
-        // B fragments q s_K in f16: trunc part in even columns, remainder in odd ones.  The codes
-        // arrive as 1 + code / 4, so logit / 4 = q s_K . A + q . (z_K - 4 s_K) / 4: the bias
-        // accumulates q . (z_K - 4 s_K), the logit scale below carries the factor 4.
-        unsigned qp[KS][2];
-        unsigned long long bp2 = 0ull;
-        const unsigned long long neg4 = f2_pack(-4.f, -4.f);
-        const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
+        if (!qrange_wide(sd.pad, qexp)) {
+          // ---- 2-bit window: W tokens
+          const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
+          const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
+          // B fragments q s_K in f16: trunc part in even columns, remainder in odd ones.  The codes
+          // arrive as 1 + code / 4, so logit / 4 = q s_K . A + q . (z_K - 4 s_K) / 4: the bias
+          // accumulates q . (z_K - 4 s_K), the logit scale below carries the factor 4.
+          unsigned qp[KS][2];
+          unsigned long long bp2 = 0ull;
+          const unsigned long long neg4 = f2_pack(-4.f, -4.f);
+          const unsigned keep = lo_col ? 0xFFFFE000u : 0u;
+  #pragma unroll
+          for (int ks = 0; ks < KS; ++ks) {
+            const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
+            const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
+            bp2 = f2_fma(qf[ks][0], zc.x, bp2);
+            bp2 = f2_fma(qf[ks][1], zc.y, bp2);
+            const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
+            bp2 = f2_fma(y01, neg4, bp2);   // q . (z_K - 4 s_K)
+            bp2 = f2_fma(y23, neg4, bp2);
+            const unsigned long long k2 = ((unsigned long long)keep << 32) | keep;
+            const unsigned long long r01 = f2_sub(y01, y01 & k2), r23 = f2_sub(y23, y23 & k2);
+            qp[ks][0] = pack_f16x2_rz(f2_lo(r01), f2_hi(r01));
+            qp[ks][1] = pack_f16x2_rz(f2_lo(r23), f2_hi(r23));
+          }
+          float bpart = 0.25f * (f2_lo(bp2) + f2_hi(bp2));
+          bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
+          bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
+          const float bias = __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . (z_K / 4 - s_K) of head t
+          float vz[2 * MT], vs[2 * MT];
+          load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
+          load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
+          // codes arrive as 1 + code / 4: B = 4 p s_V, and the offset p . (z_V - 4 s_V) per token
+  #pragma unroll
+          for (int i = 0; i < 2 * MT; ++i) {
+            vs[i] *= 4.f;
+            vz[i] -= vs[i];
+          }
+          // Q K^T over the unpacked key codes (fragment F = mt KS + ks is half F % 2 of word F / 2);
+          // channel-step parity splits the accumulators, and consecutive mma go to different
+          // accumulators (2 MT independent chains)
+          float acc[MT][2][4] = {};
+          {
+            unsigned wk[WPL];
+            load_words<WPL, CW>(sp, lane, wk);
+  #pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+  #pragma unroll
+              for (int mt = 0; mt < MT; ++mt) {
+                const int F = mt * KS + ks;
+                unsigned a[4];
+                if (F & 1) unpack_half<1>(wk[F >> 1], a);
+                else unpack_half<0>(wk[F >> 1], a);
+                mma_f16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qp[ks][0], qp[ks][1]);
+              }
+          }
+          unsigned Bp[MT][2];
+          softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 4.f * p.scale_log2, rs, Bp, lse_out,
+                                        G, lane);
+          // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
+          // the outer loop, so consecutive mma go to the MC independent accumulators
+          {
+            unsigned wv[WPL];
+            load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
+  #pragma unroll
+            for (int kt = 0; kt < KT; ++kt)
+  #pragma unroll
+              for (int mc = 0; mc < MC; ++mc) {
+                const int F = mc * KT + kt;
+                unsigned a[4];
+                if (F & 1) unpack_half<1>(wv[F >> 1], a);
+                else unpack_half<0>(wv[F >> 1], a);
+                mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
+              }
+          }
+        } else {
+          // ---- 2-bit window whose products could leave the f16 range (qrange_wide): the same
+          //      algebra on bf16 operands.  Keys: B = q s_K as three bf16 parts (truncated, the
+          //      truncated remainder, the rest), exact together, in two mma passes into the same
+          //      accumulators (pass one: parts one and two in the even and odd columns, pass two:
+          //      part three in the even ones).  Values: B = 4 p s_V as bf16 truncated + remainder.
+          const float* kmin = reinterpret_cast<const float*>(sp + S::OFF_KMIN);
+          const float* kscale = reinterpret_cast<const float*>(sp + S::OFF_KSCALE);
+          // the B operands of one channel step at a time, next to their mma (few live registers)
+          float acc[MT][2][4] = {};
+          unsigned long long bp2 = 0ull;
+          const unsigned long long neg4 = f2_pack(-4.f, -4.f);
+          {
+            unsigned wk[WPL];
+            load_words<WPL, CW>(sp, lane, wk);
 #pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
-          const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
-          bp2 = f2_fma(qf[ks][0], zc.x, bp2);
-          bp2 = f2_fma(qf[ks][1], zc.y, bp2);
-          const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
-          bp2 = f2_fma(y01, neg4, bp2);   // q . (z_K - 4 s_K)
-          bp2 = f2_fma(y23, neg4, bp2);
-          const unsigned long long k2 = ((unsigned long long)keep << 32) | keep;
-          const unsigned long long r01 = f2_sub(y01, y01 & k2), r23 = f2_sub(y23, y23 & k2);
-          qp[ks][0] = pack_f16x2_rz(f2_lo(r01), f2_hi(r01));
-          qp[ks][1] = pack_f16x2_rz(f2_lo(r23), f2_hi(r23));
-        }
-        float bpart = 0.25f * (f2_lo(bp2) + f2_hi(bp2));
-        bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
-        bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
-        const float bias = __shfl_sync(0xffffffffu, bpart, 8 * t);   // q . (z_K / 4 - s_K) of head t
-        float vz[2 * MT], vs[2 * MT];
-        load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
-        load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
-        // codes arrive as 1 + code / 4: B = 4 p s_V, and the offset p . (z_V - 4 s_V) per token
+            for (int ks = 0; ks < KS; ++ks) {
+              const ulonglong2 sc = *reinterpret_cast<const ulonglong2*>(kscale + ks * 16 + t * 4);
+              const ulonglong2 zc = *reinterpret_cast<const ulonglong2*>(kmin + ks * 16 + t * 4);
+              bp2 = f2_fma(qf[ks][0], zc.x, bp2);
+              bp2 = f2_fma(qf[ks][1], zc.y, bp2);
+              const unsigned long long y01 = f2_mul(qf[ks][0], sc.x), y23 = f2_mul(qf[ks][1], sc.y);
+              bp2 = f2_fma(y01, neg4, bp2);
+              bp2 = f2_fma(y23, neg4, bp2);
+              const float y[4] = {f2_lo(y01), f2_hi(y01), f2_lo(y23), f2_hi(y23)};
+              float pa[4], pb[4];
 #pragma unroll
-        for (int i = 0; i < 2 * MT; ++i) {
-          vs[i] *= 4.f;
-          vz[i] -= vs[i];
-        }
-        // Q K^T over the unpacked key codes (fragment F = mt KS + ks is half F % 2 of word F / 2);
-        // channel-step parity splits the accumulators, and consecutive mma go to different
-        // accumulators (2 MT independent chains)
-        float acc[MT][2][4] = {};
-        {
-          unsigned wk[WPL];
-          load_words<WPL, CW>(sp, lane, wk);
+              for (int i = 0; i < 4; ++i) {
+                const float h = __uint_as_float(__float_as_uint(y[i]) & 0xFFFF0000u);
+                const float r = y[i] - h;
+                const float m = __uint_as_float(__float_as_uint(r) & 0xFFFF0000u);
+                pa[i] = lo_col ? m : h;
+                pb[i] = lo_col ? 0.f : r - m;
+              }
+              const unsigned qa0 = pack_bf16x2_rz(pa[0], pa[1]), qa1 = pack_bf16x2_rz(pa[2], pa[3]);
+              const unsigned qz0 = pack_bf16x2_rz(pb[0], pb[1]), qz1 = pack_bf16x2_rz(pb[2], pb[3]);
 #pragma unroll
-          for (int ks = 0; ks < KS; ++ks)
-#pragma unroll
-            for (int mt = 0; mt < MT; ++mt) {
-              const int F = mt * KS + ks;
-              unsigned a[4];
-              if (F & 1) unpack_half<1>(wk[F >> 1], a);
-              else unpack_half<0>(wk[F >> 1], a);
-              mma_f16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qp[ks][0], qp[ks][1]);
+              for (int mt = 0; mt < MT; ++mt) {
+                const int F = mt * KS + ks;
+                unsigned a[4];
+                if (F & 1) unpack_half_bf16<1>(wk[F >> 1], a);
+                else unpack_half_bf16<0>(wk[F >> 1], a);
+                mma_bf16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qa0, qa1);
+                mma_bf16(acc[mt][ks & 1], a[0], a[1], a[2], a[3], qz0, qz1);
+              }
             }
-        }
-        unsigned Bp[MT][2];
-        softmax_tile<MT, 2, MC, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 4.f * p.scale_log2, rs, Bp, lse_out,
-                                      G, lane);
-        // P V over the unpacked value codes (A = V^T: fragment F = mc KT + kt); token steps in
-        // the outer loop, so consecutive mma go to the MC independent accumulators
-        {
-          unsigned wv[WPL];
-          load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
+          }
+          float bpart = 0.25f * (f2_lo(bp2) + f2_hi(bp2));
+          bpart += __shfl_xor_sync(0xffffffffu, bpart, 1);
+          bpart += __shfl_xor_sync(0xffffffffu, bpart, 2);
+          const float bias = __shfl_sync(0xffffffffu, bpart, 8 * t);
+          float vz[2 * MT], vs[2 * MT];
+          load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VMIN) + g * 2 * MT, vz);
+          load_floats<2 * MT>(reinterpret_cast<const float*>(sp + S::OFF_VSCALE) + g * 2 * MT, vs);
 #pragma unroll
-          for (int kt = 0; kt < KT; ++kt)
-#pragma unroll
-            for (int mc = 0; mc < MC; ++mc) {
-              const int F = mc * KT + kt;
-              unsigned a[4];
-              if (F & 1) unpack_half<1>(wv[F >> 1], a);
-              else unpack_half<0>(wv[F >> 1], a);
-              mma_f16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
-            }
+          for (int i = 0; i < 2 * MT; ++i) {
+            vs[i] *= 4.f;
+            vz[i] -= vs[i];
+          }
+          unsigned Bp[MT][2];
+          softmax_tile<MT, 2, MC, true, true>(acc, d_lo == 0, d_lo, d_hi, bias, vz, vs, 4.f * p.scale_log2, rs, Bp,
+                                              lse_out, G, lane);
+          {
+            unsigned wv[WPL];
+            load_words<WPL, CW>(sp + S::OFF_VCODE, lane, wv);
+  #pragma unroll
+            for (int kt = 0; kt < KT; ++kt)
+  #pragma unroll
+              for (int mc = 0; mc < MC; ++mc) {
+                const int F = mc * KT + kt;
+                unsigned a[4];
+                if (F & 1) unpack_half_bf16<1>(wv[F >> 1], a);
+                else unpack_half_bf16<0>(wv[F >> 1], a);
+                mma_bf16(rs.O[mc], a[0], a[1], a[2], a[3], Bp[kt][0], Bp[kt][1]);
+              }
+          }
         }
       }
     }
@@ -832,9 +966,10 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
     __syncwarp();
   }
   if (timed_out) {
-    // report, then give the copies still in flight a bounded chance to land before exiting
+    // report, then give the copies still in flight (the expired tile's included) a bounded
+    // chance to land before exiting
     if (lane == 0) atomicOr(p.st.err, ERR_TIMEOUT);
-    for (int kk = k + 1; kk < issued; ++kk) wait_tile(kk);
+    for (int kk = k; kk < issued; ++kk) wait_tile(kk);
     return;
   }
   while (cur_u <= u_last) {

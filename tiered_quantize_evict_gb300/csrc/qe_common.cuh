@@ -184,6 +184,7 @@ struct State {
   int* qprev;         // [GU][maxw] last 2-bit slot of the window, -1 if none
   uint8_t* bslab;     // [GU][capb][bslot_bytes]
   uint8_t* qslab;     // [GU][capq][qslot_bytes]
+  int* qrange;        // [GU][capq] magnitudes of the parameters a 2-bit slot holds (qrange_word)
   uint8_t* hstore;    // device pointer to pinned host [GU][caps][bslot_bytes]
   uint8_t* hledger;   // device pointer to pinned host [GU][caps][qslot_bytes]
   unsigned* err;      // sticky flag
@@ -311,10 +312,62 @@ __device__ __forceinline__ void unpack_half(unsigned w, unsigned (&a)[4]) {
   a[2] = code_pair_f16<4 * F + 2>(w);
   a[3] = code_pair_f16<4 * F + 3>(w);
 }
+// The same pair as bf16 (1 + code / 4 is exact in bf16 too): the codes go to bits 5 and 21, the
+// top two bits of the bf16 mantissa under the exponent of 1.0.
+template <int R>
+__device__ __forceinline__ unsigned code_pair_bf16(unsigned w) {
+  constexpr int SH = 5 - 2 * R;
+  const unsigned x = SH >= 0 ? (w << (SH >= 0 ? SH : 0)) : (w >> (SH < 0 ? -SH : 0));
+  unsigned d;
+  asm("lop3.b32 %0, %1, 0x00600060, 0x3F803F80, 0xEA;" : "=r"(d) : "r"(x));   // (a & b) | c
+  return d;
+}
+template <int F>
+__device__ __forceinline__ void unpack_half_bf16(unsigned w, unsigned (&a)[4]) {
+  a[0] = code_pair_bf16<4 * F + 0>(w);
+  a[1] = code_pair_bf16<4 * F + 1>(w);
+  a[2] = code_pair_bf16<4 * F + 2>(w);
+  a[3] = code_pair_bf16<4 * F + 3>(w);
+}
+#endif
+
+// Range record of a 2-bit slot's parameters (written whenever a slot receives codes): the
+// biased float32 exponents of the largest key scale (bits 0-7), of the largest value scale
+// (bits 8-15) and of the smallest nonzero value scale (bits 16-23; 255 when every value scale
+// is 0).  Scales are >= 0, so their bit patterns order like their values.
+QE_HD int qrange_word(unsigned kscale_max_bits, unsigned vscale_max_bits, unsigned vscale_min_nonzero_bits) {
+  const unsigned vmin = vscale_min_nonzero_bits == 0xFFFFFFFFu ? 255u : (vscale_min_nonzero_bits >> 23) & 0xFFu;
+  return (int)(((kscale_max_bits >> 23) & 0xFFu) | (((vscale_max_bits >> 23) & 0xFFu) << 8) | (vmin << 16));
+}
+// Whether a 2-bit tile needs bf16 operands instead of f16 ones.  Its products meet the tensor
+// cores as f16 truncated + remainder pairs: q_c s_c for the keys and 4 p s_V for the values,
+// with p <= 2^8 (the softmax reference maximum is raised once a tile's scores pass it by 2^8).
+// f16 holds them while |q| s_K < 2^15 and s_V < 2^5 (then 4 p s_V < 2^15); below s_V = 2^-13
+// the remainder part falls into f16 subnormals and the value products lose relative precision.
+// q_exp: the largest biased exponent of the unit's queries (bf16 and float32 share the bias).
+QE_HD bool qrange_values_wide(int word) {
+  const int evmax = (word >> 8) & 0xFF, evmin = (word >> 16) & 0xFF;
+  return evmax >= 127 + 5 || evmin <= 127 - 14;
+}
+QE_HD bool qrange_wide(int word, int q_exp) {
+  const int ek = word & 0xFF;
+  return (ek > 0 && ek + q_exp >= 2 * 127 + 14) || qrange_values_wide(word);
+}
+#if defined(__CUDACC__)
 __device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
                                         unsigned b0, unsigned b1) {
   asm(
       "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+// m16n8k8 with tf32 operands (float32 bit patterns whose 13 low mantissa bits are zero):
+// A rows g, g + 8 at k = t (a0, a1) and k = t + 4 (a2, a3); B rows k = t (b0), t + 4 (b1) of
+// column g; the accumulator layout is the m16n8k16 one
+__device__ __forceinline__ void mma_tf32(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                         unsigned b0, unsigned b1) {
+  asm(
+      "mma.sync.aligned.m16n8k8.row.col.f32.tf32.tf32.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
 }

@@ -82,6 +82,7 @@ struct qe_handle_s {
   double timed_bytes = 0;
   long long timed_launches = 0;
   long long launches = 0;
+  int debug_expire = 0;   // qe_debug_inject(QE_DEBUG_EXPIRE_WAIT): applies to the next decode step
   std::string err;
   // five-tier per-token mode (cfg.tiering == QE_TIERING_TOKENS)
   bool tok = false;
@@ -96,6 +97,11 @@ struct qe_handle_s {
 };
 
 namespace qe {
+// qe_debug_inject(QE_DEBUG_FAIL_DEVICE_ALLOC): true when this device allocation of qe_init is
+// the one chosen to fail (qe_host.cu); qe_init restarts the count
+bool inject_alloc_failure();
+void inject_begin_init();
+const char* injected_note();   // " (injected by qe_debug_inject)" once after an injected failure, else ""
 // five-tier mode (qe_tok_host.cu)
 qe_status tok_init(const qe_config& c, cudaStream_t stream, qe_handle* out, std::string& err);
 void tok_free(qe_handle h);

@@ -4,6 +4,7 @@
 // layer have the same length, so after each routing event every unit has the same number of
 // Full, Quantized and Pinned windows); launch shapes are computed from it without reading the
 // device.  Window identities, slots, scores and codes live only on the device.
+#include <atomic>
 #include <cmath>
 #include <cstdarg>
 #include <cstdint>
@@ -26,7 +27,28 @@ using qe::LayerMirror;
 
 thread_local std::string g_init_error;
 
+// qe_debug_inject: the device allocation of the next qe_init that fails (1-based, 0 none), the
+// count of device allocations the current qe_init has made, and whether the next pinned host
+// store allocation fails.  Process-wide and one-shot.
+std::atomic<int> g_fail_alloc_nth{0};
+std::atomic<int> g_alloc_count{0};
+std::atomic<int> g_fail_host_store{0};
+std::atomic<int> g_fired{0};   // an injected allocation failure has fired and is not yet reported
+
 }  // namespace
+
+namespace qe {
+void inject_begin_init() { g_alloc_count.store(0); }
+bool inject_alloc_failure() {
+  const int n = g_fail_alloc_nth.load();
+  if (n <= 0) return false;
+  if (g_alloc_count.fetch_add(1) + 1 != n) return false;
+  g_fail_alloc_nth.store(0);
+  g_fired.store(1);
+  return true;
+}
+const char* injected_note() { return g_fired.exchange(0) ? " (injected by qe_debug_inject)" : ""; }
+}  // namespace qe
 
 namespace {
 
@@ -60,6 +82,8 @@ void capacities(const qe_config& c, int L, int& kf, int& kq) {
 
 template <class T>
 qe_status dalloc(qe_handle h, T** p, size_t count, const char* what) {
+  if (qe::inject_alloc_failure())
+    return fail(h, QE_ERR_OOM, "cudaMalloc of %s (%zu bytes) failed%s", what, count * sizeof(T), qe::injected_note());
   cudaError_t e = cudaMalloc((void**)p, count * sizeof(T) > 0 ? count * sizeof(T) : 16);
   if (e != cudaSuccess)
     return fail(h, QE_ERR_OOM, "cudaMalloc of %s (%zu bytes) failed: %s", what, count * sizeof(T), cudaGetErrorString(e));
@@ -119,7 +143,7 @@ int nbw_of(const qe_handle h, const LayerMirror& m) {
 void free_all(qe_handle h) {
   qe::State& s = h->st;
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_head, s.bfree_top,
-                  s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
+                  s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.qrange, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
                   h->tok_stage, h->diag, h->rope_blk, h->rope_off, h->vdelta};
   for (void* p : ptrs)
@@ -139,6 +163,7 @@ long long qe_kernel_launches(qe_handle h) { return h ? h->launches : 0; }
 
 qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   if (!cfg || !out) return fail(nullptr, QE_ERR_INVALID_ARG, "null argument");
+  qe::inject_begin_init();
   const qe_config& c = *cfg;
   if (c.batch < 1 || c.n_layers < 1 || c.n_kv_heads < 1 || c.n_q_heads < 1 || c.n_q_heads % c.n_kv_heads)
     return fail(nullptr, QE_ERR_INVALID_ARG, "bad head/batch/layer counts");
@@ -241,6 +266,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   QE_ALLOC(st.sfree_top, GU, "sfree_top");
   QE_ALLOC(st.bslab, GU * st.capb * bslot_b, "bf16 window pool");
   QE_ALLOC(st.qslab, GU * st.capq * qslot_b, "2-bit window pool");
+  QE_ALLOC(st.qrange, GU * st.capq, "2-bit slot ranges");
   QE_ALLOC(st.err, 1, "error flag");
   QE_ALLOC(st.stats, (size_t)c.n_layers * qe::N_STATS, "stats");
   QE_ALLOC(st.ldev, (size_t)c.n_layers, "layer headers");
@@ -268,10 +294,10 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   }
   {
     void* mp = nullptr;
-    if (cudaMalloc(&mp, (size_t)h->max_moves * sizeof(qe::Move)) != cudaSuccess) {
+    if (qe::inject_alloc_failure() || cudaMalloc(&mp, (size_t)h->max_moves * sizeof(qe::Move)) != cudaSuccess) {
       free_all(h);
       delete h;
-      return fail(nullptr, QE_ERR_OOM, "cudaMalloc of the move list failed");
+      return fail(nullptr, QE_ERR_OOM, "cudaMalloc of the move list failed%s", qe::injected_note());
     }
     h->moves = static_cast<qe::Move*>(mp);
   }
@@ -279,14 +305,16 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
 #undef QE_ALLOC
 
   // pinned host backing store, mapped into the device address space
-  e = cudaHostAlloc(&h->hstore_host, (size_t)GU * st.caps * bslot_b, cudaHostAllocMapped);
+  const bool inj_store = g_fail_host_store.exchange(0) != 0;
+  e = inj_store ? cudaErrorMemoryAllocation
+                : cudaHostAlloc(&h->hstore_host, (size_t)GU * st.caps * bslot_b, cudaHostAllocMapped);
   if (e == cudaSuccess) e = cudaHostAlloc(&h->hledger_host, (size_t)GU * st.caps * qslot_b, cudaHostAllocMapped);
   void* dstore = nullptr;
   void* dledger = nullptr;
   if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dstore, h->hstore_host, 0);
   if (e == cudaSuccess) e = cudaHostGetDevicePointer(&dledger, h->hledger_host, 0);
   if (e != cudaSuccess) {
-    std::string m = std::string("pinned host store: ") + cudaGetErrorString(e);
+    std::string m = std::string("pinned host store: ") + cudaGetErrorString(e) + (inj_store ? " (injected by qe_debug_inject)" : "");
     free_all(h);
     delete h;
     g_init_error = m;
@@ -305,6 +333,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   set(cudaMemsetAsync(st.score, 0, GU * maxw * 4, h->stream));
   set(cudaMemsetAsync(st.bslab, 0, GU * st.capb * bslot_b, h->stream));
   set(cudaMemsetAsync(st.qslab, 0, GU * st.capq * qslot_b, h->stream));
+  set(cudaMemsetAsync(st.qrange, 0, GU * st.capq * 4, h->stream));
   set(cudaMemsetAsync(st.err, 0, 4, h->stream));
   set(cudaMemsetAsync(h->diag, 0, (size_t)c.n_layers * h->units * sizeof(qe::RouteDiag), h->stream));
   set(cudaMemsetAsync(st.stats, 0, (size_t)c.n_layers * qe::N_STATS * 8, h->stream));
@@ -354,8 +383,8 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
     }
     void* pb = nullptr;
     void* po = nullptr;
-    set(cudaMalloc(&pb, blk.size() * sizeof(float2)));
-    set(cudaMalloc(&po, off.size() * sizeof(float2)));
+    set(qe::inject_alloc_failure() ? cudaErrorMemoryAllocation : cudaMalloc(&pb, blk.size() * sizeof(float2)));
+    set(qe::inject_alloc_failure() ? cudaErrorMemoryAllocation : cudaMalloc(&po, off.size() * sizeof(float2)));
     h->rope_blk = static_cast<float2*>(pb);
     h->rope_off = static_cast<float2*>(po);
     if (ie == cudaSuccess) set(cudaMemcpy(pb, blk.data(), blk.size() * sizeof(float2), cudaMemcpyHostToDevice));
@@ -365,11 +394,11 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
   set(qe::prepare_route_kernels(st));
   set(cudaStreamSynchronize(h->stream));
   if (ie != cudaSuccess) {
-    std::string m = std::string("initialising the cache: ") + cudaGetErrorString(ie);
+    std::string m = std::string("initialising the cache: ") + cudaGetErrorString(ie) + qe::injected_note();
     free_all(h);
     delete h;
     g_init_error = m;
-    return QE_ERR_CUDA;
+    return ie == cudaErrorMemoryAllocation ? QE_ERR_OOM : QE_ERR_CUDA;
   }
   *out = h;
   return QE_OK;
@@ -497,6 +526,8 @@ static qe_status decode_impl(qe_handle h, int layer, const void* q, void* out, i
   p.lse = h->lse;
   p.rope_blk = h->rope_blk;
   p.rope_off = h->rope_off;
+  p.debug_expire = h->debug_expire;
+  h->debug_expire = 0;   // one step only
   {
     const int sub = c.window / 16;
     const int ntiles = nbw_of(h, m) * sub + m.n_quant;
@@ -877,6 +908,25 @@ qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n
   QE_CK(h, cudaMemcpy(out, h->diag + (size_t)layer * h->units, n_units * sizeof(qe_route_diag),
                       cudaMemcpyDeviceToHost));
   return QE_OK;
+}
+
+qe_status qe_debug_inject(qe_handle h, int what, long long value) {
+  switch (what) {
+    case QE_DEBUG_FAIL_DEVICE_ALLOC:
+      if (value < 0) return QE_ERR_INVALID_ARG;
+      g_fail_alloc_nth.store((int)value);
+      return QE_OK;
+    case QE_DEBUG_FAIL_HOST_STORE:
+      g_fail_host_store.store(value != 0 ? 1 : 0);
+      return QE_OK;
+    case QE_DEBUG_EXPIRE_WAIT:
+      if (!h) return QE_ERR_INVALID_ARG;
+      if (value < 0 || value > (1 << 30)) return fail(h, QE_ERR_INVALID_ARG, "wait index %lld out of range", value);
+      h->debug_expire = (int)value;
+      return QE_OK;
+    default:
+      return h ? fail(h, QE_ERR_INVALID_ARG, "unknown injection %d", what) : QE_ERR_INVALID_ARG;
+  }
 }
 
 qe_status qe_set_timing(qe_handle h, int enable) {

@@ -28,6 +28,9 @@ struct AttnParams {
   // [blocks][D/2], and of r theta_i per row offset r < 16 [16][D/2]
   const float2* rope_blk;
   const float2* rope_off;
+  // fault injection for tests (qe_debug_inject): k >= 1 makes every warp report its k-th tile
+  // wait as expired once that tile's copy has landed; 0: off
+  int debug_expire;
 };
 
 // qe_attn_combine

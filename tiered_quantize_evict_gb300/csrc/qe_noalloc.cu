@@ -122,6 +122,7 @@ extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* 
   p.lse = lse;
   p.rope_blk = h->rope_blk;
   p.rope_off = h->rope_off;
+  p.debug_expire = 0;
   const int grid = qe::attn_grid(h->n_sm, h->units, NA_PSLOTS);
   e = qe::launch_decode_attn(p, grid, h->stream);
   if (e != cudaSuccess) return na_fail(h, QE_ERR_CUDA, "attention launch: %s", cudaGetErrorString(e));

@@ -782,6 +782,23 @@ __device__ __forceinline__ bool move_ok(const State& st, const Move& mv) {
 // Each CTA takes every gridDim.x-th move.  A pack's bf16 source slot is fetched into one of two
 // shared-memory buffers by asynchronous copies issued one move ahead, so it lands while the
 // CTA works on the move before.
+// Range record (qrange_word) of the codes 2-bit slot `slot` of unit gu now holds, from its key
+// scales ks[D] and value scales vs[W] (any order); executed by one warp.
+__device__ __forceinline__ void write_qrange(const State& st, long long gu, int slot, const float* ks, const float* vs,
+                                             int D, int W, int lane) {
+  unsigned kmax = 0u, vmax = 0u, vmin = 0xFFFFFFFFu;
+  for (int c = lane; c < D; c += 32) kmax = max(kmax, __float_as_uint(ks[c]));
+  for (int r = lane; r < W; r += 32) {
+    const unsigned b = __float_as_uint(vs[r]);
+    vmax = max(vmax, b);
+    if (b) vmin = min(vmin, b);
+  }
+  kmax = __reduce_max_sync(0xffffffffu, kmax);
+  vmax = __reduce_max_sync(0xffffffffu, vmax);
+  vmin = __reduce_min_sync(0xffffffffu, vmin);
+  if (lane == 0) st.qrange[gu * st.capq + slot] = qrange_word(kmax, vmax, vmin);
+}
+
 template <int D, int W>
 __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel(State st, const Move* __restrict__ moves,
                                                                                 const int* __restrict__ n_moves) {
@@ -843,6 +860,12 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
       const uint8_t* src = st.hledger + (gu * st.caps + mv.src) * (long long)QSLOT;
       uint8_t* dst = st.qslab + (gu * st.capq + mv.dst) * (long long)QSLOT;
       copy16(dst, src, QSLOT, tid);
+      __syncthreads();
+      // the slot's range record, from the parameters it now holds
+      if (tid < 32)
+        write_qrange(st, gu, mv.dst, reinterpret_cast<const float*>(dst + g.off_kscale()),
+                     reinterpret_cast<const float*>(dst + g.off_vscale()), D, W, tid);
+      __syncthreads();
       continue;
     }
     // ---- pack: the bf16 slot (fetched one move ahead), and its exact copy into the host store
@@ -987,6 +1010,7 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
       reinterpret_cast<float*>(qimg + g.off_vmin())[pr] = vz[r];
       reinterpret_cast<float*>(qimg + g.off_vscale())[pr] = vs[r];
     }
+    if (tid < 32) write_qrange(st, gu, mv.dst, ks, vs, D, W, tid);
     __syncthreads();
     // the slot in whole 16-byte vectors; its codes reach the host ledger only if the slot is
     // later handed to another window while this one is still kept (the write-back above)

@@ -215,6 +215,7 @@ struct TkAttnArgs {
   float2* part_ml;
   float* logits;
   int lg_cap;
+  int debug_expire;   // qe_debug_inject: k >= 1 reports the k-th tile wait as expired after it landed
 };
 
 template <int D>
@@ -540,7 +541,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   int k = 0;
   for (; k < issued; ++k) {
     const int s = k % NST;
-    if (!wait_tile(k)) { timed_out = true; break; }
+    if (!wait_tile(k) || k + 1 == p.debug_expire) { timed_out = true; break; }
     const TkDesc d = descs[warp][s];
     const uint8_t* sp = stage_base + (size_t)s * STAGE;
     while (d.u > cur_u) {
@@ -606,7 +607,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   }
   if (timed_out) {
     if (lane == 0) atomicOr(S.err, ERR_TIMEOUT);
-    for (int kk = k + 1; kk < issued; ++kk) wait_tile(kk);
+    for (int kk = k; kk < issued; ++kk) wait_tile(kk);   // copies in flight, the expired one's too
     return;
   }
   while (cur_u <= u_last) {
@@ -1574,7 +1575,7 @@ cudaError_t tk_launch_commit_pending(const TokState& s, int layer, int pend, cud
 
 cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* knew, const uint16_t* vnew,
                            const uint16_t* q, float scale_log2, float* part_o, float2* part_ml, float* logits, int lg_cap,
-                           int grid, cudaStream_t st) {
+                           int grid, cudaStream_t st, int debug_expire) {
   const int D = s.g.D;
   TkAttnArgs a;
   a.st = s;
@@ -1588,6 +1589,7 @@ cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_
   a.part_ml = part_ml;
   a.logits = logits;
   a.lg_cap = lg_cap;
+  a.debug_expire = debug_expire;
   const int stage = 64 * D;
   const int nst = TK_STAGE_TOTAL / (TK_WARPS * stage) < 4 ? TK_STAGE_TOTAL / (TK_WARPS * stage) : 4;
   cudaLaunchConfig_t cfg{};

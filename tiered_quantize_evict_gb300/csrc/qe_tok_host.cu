@@ -43,6 +43,7 @@ int round16(long long x) { return (int)((x + 15) / 16 * 16); }
 template <class T>
 cudaError_t talloc(qe_handle h, T** p, size_t count) {
   void* q = nullptr;
+  if (inject_alloc_failure()) return cudaErrorMemoryAllocation;
   cudaError_t e = cudaMalloc(&q, count > 0 ? count * sizeof(T) : 16);
   if (e != cudaSuccess) return e;
   h->tk_allocs.push_back(q);
@@ -215,7 +216,7 @@ qe_status tok_init(const qe_config& c, cudaStream_t stream, qe_handle* out, std:
   A(tk_prepare(c.head_dim));
   A(cudaStreamSynchronize(stream));
   if (ae != cudaSuccess) {
-    err = std::string("setting up the five-tier cache: ") + cudaGetErrorString(ae);
+    err = std::string("setting up the five-tier cache: ") + cudaGetErrorString(ae) + injected_note();
     tok_free(h);
     delete h;
     return ae == cudaErrorMemoryAllocation ? QE_ERR_OOM : QE_ERR_CUDA;
@@ -347,7 +348,8 @@ qe_status tok_decode(qe_handle h, int layer, const void* q, void* out, int flags
     TK_CK(h, cudaEventRecordWithFlags(e0, h->stream, ev_flags));
   }
   TK_CK(h, tk_launch_attn(h->ts, layer, m.pending, m.pk, m.pv, qd, scale_log2, h->tk_part_o, h->tk_part_ml,
-                          h->tk_logits, h->tk_lgcap, h->tk_grid, h->stream));
+                          h->tk_logits, h->tk_lgcap, h->tk_grid, h->stream, h->debug_expire));
+  h->debug_expire = 0;   // one step only
   ++h->launches;
   m.pk = m.pv = nullptr;   // written by this launch
   if (h->timing) {

@@ -22,7 +22,7 @@ cudaError_t tk_launch_commit_pending(const TokState& s, int layer, int pend, cud
 // into the tail by the launch itself; null when it is written already
 cudaError_t tk_launch_attn(const TokState& s, int layer, int pend, const uint16_t* knew, const uint16_t* vnew,
                            const uint16_t* q, float scale_log2, float* part_o, float2* part_ml, float* logits, int lg_cap,
-                           int grid, cudaStream_t st);
+                           int grid, cudaStream_t st, int debug_expire = 0);
 cudaError_t tk_launch_merge(const TokState& s, int layer, int pend, const float* part_o, const float2* part_ml,
                             const float* logits, int lg_cap, int grid, void* out, int out_fp32, cudaStream_t st);
 // re-rank of one layer and its header switch
