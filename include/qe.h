@@ -363,8 +363,15 @@ long long qe_kernel_launches(qe_handle h);
  *    lets its other copies land and leaves.  The sticky device flag then makes qe_synchronize
  *    return QE_ERR_TIMEOUT, as a real expiry (0.2 s without data) would; that step's outputs
  *    and score updates are undefined.  0 clears.
- * Errors: QE_ERR_INVALID_ARG (unknown kind, negative value, NULL handle for the wait). */
-enum { QE_DEBUG_FAIL_DEVICE_ALLOC = 1, QE_DEBUG_FAIL_HOST_STORE = 2, QE_DEBUG_EXPIRE_WAIT = 3 };
+ *  QE_DEBUG_VERIFY_PATH (h required): which path qe_verify takes on the handle from now on:
+ *    0 automatic (the default: the fused tensor-core launch when it is allowed and expected to
+ *    be faster), 1 the fused launch whenever it is allowed (keys used as stored, n_q *
+ *    group <= 64), 2 draft by draft.  Both paths compute the same results up to float32
+ *    summation order; this lets tests cover each.  Not a fault: it persists until changed.
+ * Errors: QE_ERR_INVALID_ARG (unknown kind, negative value, NULL handle for the wait or the
+ * verify path, a path outside 0..2). */
+enum { QE_DEBUG_FAIL_DEVICE_ALLOC = 1, QE_DEBUG_FAIL_HOST_STORE = 2, QE_DEBUG_EXPIRE_WAIT = 3,
+       QE_DEBUG_VERIFY_PATH = 4 };
 qe_status qe_debug_inject(qe_handle h, int what, long long value);
 
 /* ---------------------------------------------------------------- no-allocation decode step

@@ -63,6 +63,7 @@ def test_debug_inject_validates_its_arguments(lib):
     """qe_debug_inject acts on host state only; its argument checks need no GPU."""
     import tiered_quantize_evict_gb300 as qe
     assert lib.qe_debug_inject(None, qe.QE_DEBUG_EXPIRE_WAIT, 1) == qe.QE_ERR_INVALID_ARG   # needs a handle
+    assert lib.qe_debug_inject(None, qe.QE_DEBUG_VERIFY_PATH, 1) == qe.QE_ERR_INVALID_ARG   # needs a handle
     assert lib.qe_debug_inject(None, 99, 1) == qe.QE_ERR_INVALID_ARG
     assert lib.qe_debug_inject(None, qe.QE_DEBUG_FAIL_DEVICE_ALLOC, -1) == qe.QE_ERR_INVALID_ARG
     assert lib.qe_debug_inject(None, qe.QE_DEBUG_FAIL_DEVICE_ALLOC, 0) == qe.QE_OK

@@ -1,13 +1,19 @@
 """Speculative verify with rollback on the GPU against the oracle (H2O page §5, speculative
 decoding): decode steps, verifies of several drafts with seeded acceptance counts (all, some,
 none), and routing events interleave; every draft query's output, the scores after each commit,
-the tiers after each routing event, and the 2-bit codes and bf16 windows are compared."""
+the tiers after each routing event, and the 2-bit codes and bf16 windows are compared.
+
+Keys used as stored may take the fused path (all drafts against one read of the cache on the
+tensor cores, up to 64 draft x head rows); keys stored pre-RoPE verify draft by draft.  Every case
+runs with the automatic choice and, where keys are used as stored, with each path forced, with up
+to 16 drafts (64 rows at G = 4), head dims 64 and 128, windows 16, 32 and 64."""
 import dataclasses
 
 import numpy as np
 import pytest
 
 import qe_inputs as gen
+import tiered_quantize_evict_gb300 as qe
 from qe_testlib import OUT_TOL, TIER_CODE, ParityRun, host_kv, host_q, to_dev
 
 pytestmark = pytest.mark.gpu
@@ -21,15 +27,36 @@ CASES = {
                                            n_kv_heads=2, head_dim=64, prefill=150, decode_steps=60, window=16,
                                            route_period=8, n_sink=3, n_recent=16, kf=3, kq=4, plant_tokens=(),
                                            rope_theta=10000.0, seed=52),
+    # fused path at its limits: 16 drafts x 4 heads = 64 rows
+    "d128_w32_g4_16drafts": dataclasses.replace(gen.WORKLOADS["tiny_qevict"], name="verify_d128_16",
+                                                batch=2, n_q_heads=8, n_kv_heads=2, head_dim=128, prefill=420,
+                                                decode_steps=320, window=32, route_period=12, n_sink=5, n_recent=32,
+                                                kf=4, kq=6, plant_tokens=(), seed=53),
+    "d64_w16_g2_16drafts": dataclasses.replace(gen.WORKLOADS["tiny_qevict"], name="verify_d64_16", batch=1,
+                                               n_q_heads=4, n_kv_heads=2, head_dim=64, prefill=150, decode_steps=320,
+                                               window=16, route_period=8, n_sink=3, n_recent=16, kf=3, kq=4,
+                                               plant_tokens=(), seed=54),
+    "d128_w64_g1_16drafts": dataclasses.replace(gen.WORKLOADS["tiny_qevict"], name="verify_d128_w64", batch=3,
+                                                n_q_heads=1, n_kv_heads=1, head_dim=128, prefill=700,
+                                                decode_steps=320, window=64, route_period=16, n_sink=0, n_recent=20,
+                                                kf=2, kq=4, plant_tokens=(), seed=55),
 }
+MAX_DRAFTS = {"d128_w32_g4_16drafts": 16, "d64_w16_g2_16drafts": 16, "d128_w64_g1_16drafts": 16}
 
 
+PATHS = {"auto": 0, "fused": 1, "per_draft": 2}
+
+
+@pytest.mark.parametrize("path", sorted(PATHS))
 @pytest.mark.parametrize("name", sorted(CASES))
-def test_verify_commit_trajectory(name):
+def test_verify_commit_trajectory(name, path):
     import torch
     wl = CASES[name]
+    if wl.rope_theta and path != "auto":
+        pytest.skip("keys stored pre-RoPE always verify draft by draft")
     track = [(b, 0, h) for b in range(wl.batch) for h in range(wl.n_kv_heads)]
     run = ParityRun(wl, wl.batch, 1, track)
+    assert qe.debug_inject(qe.QE_DEBUG_VERIFY_PATH, PATHS[path], run.cache) == 0
     run.prefill()
     rng = np.random.default_rng(7)
     cache, G, D = run.cache, wl.group, wl.head_dim
@@ -39,7 +66,7 @@ def test_verify_commit_trajectory(name):
         if event % 3 == 2:
             run.step(check=True)                          # an ordinary decode step between verifies
         else:
-            n_q = int(rng.integers(1, 5))
+            n_q = int(rng.integers(1, MAX_DRAFTS.get(name, 4) + 1))
             acc = int(rng.integers(0, n_q + 1))
             t0, L0 = run.t, wl.prefill + run.t
             K = np.stack([host_kv(wl, 0, L0 + j, 1, wl.batch)[0][:, :, 0] for j in range(n_q)])

@@ -31,7 +31,7 @@ EXPORTED = [
     "qe_get_token_tiers", "qe_get_token_scores", "qe_get_token_counts", "qe_get_token",
     "qe_verify", "qe_verify_commit", "qe_debug_inject",
 ]
-QE_DEBUG_FAIL_DEVICE_ALLOC, QE_DEBUG_FAIL_HOST_STORE, QE_DEBUG_EXPIRE_WAIT = 1, 2, 3
+QE_DEBUG_FAIL_DEVICE_ALLOC, QE_DEBUG_FAIL_HOST_STORE, QE_DEBUG_EXPIRE_WAIT, QE_DEBUG_VERIFY_PATH = 1, 2, 3, 4
 QE_VERIFY_MAX = 16
 QE_TIERING_WINDOWS, QE_TIERING_TOKENS = 0, 1
 TOK_BF16, TOK_INT4, TOK_INT2, TOK_NQ1, TOK_EVICTED, TOK_ABSENT = 0, 1, 2, 3, 4, 255

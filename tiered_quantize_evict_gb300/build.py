@@ -17,7 +17,7 @@ ROOT = os.path.dirname(HERE)
 CSRC = os.path.join(HERE, "csrc")
 LIBDIR = os.path.join(HERE, "_lib")
 BUILD = os.path.join(HERE, "_build")
-SOURCES = ["qe_attn.cu", "qe_route.cu", "qe_host.cu", "qe_noalloc.cu", "qe_tok.cu", "qe_tok_host.cu"]
+SOURCES = ["qe_attn.cu", "qe_route.cu", "qe_host.cu", "qe_noalloc.cu", "qe_tok.cu", "qe_tok_host.cu", "qe_verify.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-ffp-contract=off",
          "--expt-relaxed-constexpr"]

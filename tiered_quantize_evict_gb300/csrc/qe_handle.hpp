@@ -70,6 +70,12 @@ struct qe_handle_s {
   // speculative verify: window masses of each draft query, [n_layers][verify_cap][units][maxw]
   float* vdelta = nullptr;
   int verify_cap = 0;
+  // fused verify scratch (grown on first use, outside any capture): per-split partials and
+  // per-window log2-sum-exps of the up to 64 draft x head rows
+  float* vf_part_o = nullptr;
+  float2* vf_part_ml = nullptr;
+  float* vf_lse = nullptr;
+  int vf_splits = 0;
   // keys stored pre-RoPE: angle tables (null when rope_theta == 0)
   float2* rope_blk = nullptr;   // [ceil(max_context / 16)][D/2] cos, sin of 16 b theta_i
   float2* rope_off = nullptr;   // [16][D/2] cos, sin of r theta_i
@@ -83,6 +89,7 @@ struct qe_handle_s {
   long long timed_launches = 0;
   long long launches = 0;
   int debug_expire = 0;   // qe_debug_inject(QE_DEBUG_EXPIRE_WAIT): applies to the next decode step
+  int verify_path = 0;    // qe_debug_inject(QE_DEBUG_VERIFY_PATH): 0 automatic, 1 fused, 2 per draft
   std::string err;
   // five-tier per-token mode (cfg.tiering == QE_TIERING_TOKENS)
   bool tok = false;

@@ -145,7 +145,8 @@ void free_all(qe_handle h) {
   void* ptrs[] = {s.tier, s.bslot, s.qslot, s.sent, s.score, s.blist, s.qlist, s.bfree, s.bfree_head, s.bfree_top,
                   s.qfree, s.qfree_top, s.sfree, s.sfree_top, s.bvictim, s.qvictim, s.bprev, s.qprev, s.bslab, s.qslab, s.qrange, s.err, s.stats, s.ldev, h->part_o, h->part_ml,
                   h->lse, h->moves, h->n_moves, h->stage[0], h->stage[1], h->stage[2], h->stage[3],
-                  h->tok_stage, h->diag, h->rope_blk, h->rope_off, h->vdelta};
+                  h->tok_stage, h->diag, h->rope_blk, h->rope_off, h->vdelta, h->vf_part_o, h->vf_part_ml,
+                  h->vf_lse};
   for (void* p : ptrs)
     if (p) cudaFree(p);
   if (h->hstore_host) cudaFreeHost(h->hstore_host);
@@ -391,6 +392,7 @@ qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
     if (ie == cudaSuccess) set(cudaMemcpy(po, off.data(), off.size() * sizeof(float2), cudaMemcpyHostToDevice));
   }
   set(qe::prepare_attn_kernels(c.head_dim, c.window));
+  set(qe::prepare_verify_kernels(c.head_dim, c.window));
   set(qe::prepare_route_kernels(st));
   set(cudaStreamSynchronize(h->stream));
   if (ie != cudaSuccess) {
@@ -580,6 +582,78 @@ static qe_status decode_impl(qe_handle h, int layer, const void* q, void* out, i
   return QE_OK;
 }
 
+// qe_verify's fused path: append the drafts in one launch (the length becomes L0 + n_q), then
+// one attention launch over (unit, split) and one combine launch writing every draft's output
+// and its window masses into dl.
+static qe_status verify_fused(qe_handle h, int layer, const void* q, const void* k, const void* v, void* out, int n_q,
+                              int flags, float* dl) {
+  qe_status s;
+  LayerMirror& m = h->lay[layer];
+  const qe_config& c = h->cfg;
+  const int D = c.head_dim;
+  const size_t kv_bytes = (size_t)n_q * h->units * D * 2;
+  const size_t q_bytes = (size_t)n_q * c.batch * c.n_q_heads * D * 2;
+  const size_t o_bytes = (size_t)n_q * c.batch * c.n_q_heads * D * (c.out_fp32 ? 4 : 2);
+  const uint16_t* kd = static_cast<const uint16_t*>(k);
+  const uint16_t* vd = static_cast<const uint16_t*>(v);
+  const uint16_t* qd = static_cast<const uint16_t*>(q);
+  void* od = out;
+  if (flags & QE_HOST_PTRS) {   // every buffer through the handle's staging
+    if ((s = ensure_stage(h, 0, kv_bytes)) != QE_OK || (s = ensure_stage(h, 1, kv_bytes)) != QE_OK ||
+        (s = ensure_stage(h, 2, q_bytes)) != QE_OK || (s = ensure_stage(h, 3, o_bytes)) != QE_OK)
+      return s;
+    QE_CK(h, cudaMemcpyAsync(h->stage[0], k, kv_bytes, cudaMemcpyHostToDevice, h->stream));
+    QE_CK(h, cudaMemcpyAsync(h->stage[1], v, kv_bytes, cudaMemcpyHostToDevice, h->stream));
+    QE_CK(h, cudaMemcpyAsync(h->stage[2], q, q_bytes, cudaMemcpyHostToDevice, h->stream));
+    kd = static_cast<const uint16_t*>(h->stage[0]);
+    vd = static_cast<const uint16_t*>(h->stage[1]);
+    qd = static_cast<const uint16_t*>(h->stage[2]);
+    od = h->stage[3];
+  }
+  // splits: about two CTAs per SM over the layer's units
+  int splits = (2 * h->n_sm + h->units - 1) / h->units;
+  if (splits > qe::verify_max_splits()) splits = qe::verify_max_splits();
+  if (splits < 1) splits = 1;
+  const int rows = qe::verify_max_rows();
+  const int ent_cap = h->st.capb + h->st.capq;
+  if (!h->vf_part_o || h->vf_splits < splits) {
+    if (h->vf_part_o) cudaFree(h->vf_part_o);
+    if (h->vf_part_ml) cudaFree(h->vf_part_ml);
+    if (h->vf_lse) cudaFree(h->vf_lse);
+    h->vf_part_o = nullptr;
+    h->vf_part_ml = nullptr;
+    h->vf_lse = nullptr;
+    h->vf_splits = 0;
+    if ((s = dalloc(h, &h->vf_part_o, (size_t)h->units * splits * rows * D, "verify partials")) != QE_OK ||
+        (s = dalloc(h, &h->vf_part_ml, (size_t)h->units * splits * rows, "verify partial stats")) != QE_OK ||
+        (s = dalloc(h, &h->vf_lse, (size_t)h->units * ent_cap * rows, "verify window sums")) != QE_OK)
+      return s;
+    h->vf_splits = splits;
+  }
+  QE_CK(h, qe::launch_append(h->st, layer, n_q, kd, vd, h->n_sm, h->stream, true));
+  h->launches += 2;
+  qe::VerifyParams vp{};
+  vp.st = h->st;
+  vp.layer = layer;
+  vp.L0 = m.L;
+  vp.n_q = n_q;
+  vp.R = n_q * h->st.G;
+  vp.splits = splits;
+  vp.q = qd;
+  vp.scale_log2 = (float)(1.4426950408889634 / std::sqrt((double)D));
+  vp.part_o = h->vf_part_o;
+  vp.part_ml = h->vf_part_ml;
+  vp.lse = h->vf_lse;
+  vp.ent_cap = ent_cap;
+  QE_CK(h, qe::launch_verify_fused(vp, od, c.out_fp32, dl, (long long)h->units * h->st.maxw, h->stream));
+  h->launches += 2;
+  if (od != out) QE_CK(h, cudaMemcpyAsync(out, od, o_bytes, cudaMemcpyDeviceToHost, h->stream));
+  m.verify_L0 = m.L;
+  m.L += n_q;
+  m.verify_n = n_q;
+  return QE_OK;
+}
+
 qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const void* v, void* out, int n_q,
                     int flags) {
   if (h && h->tok) return fail(h, QE_ERR_STATE, "speculative verify serves window-tiered handles");
@@ -605,6 +679,14 @@ qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const 
   const long long qstride = (long long)h->units * h->st.maxw;
   float* dl = h->vdelta + (size_t)layer * h->verify_cap * qstride;
   QE_CK(h, cudaMemsetAsync(dl, 0, (size_t)n_q * qstride * sizeof(float), h->stream));
+  // All drafts against one read of the cache on the tensor cores, when the rows fit one mma tile
+  // and the keys are used as stored (keys stored pre-RoPE verify draft by draft).  The fused
+  // launch's cost hardly depends on the row count, so by default it serves enough rows to beat
+  // one decode step per draft.
+  const int rows = n_q * h->st.G;
+  const bool fused_ok = !h->rope_blk && rows <= qe::verify_max_rows();
+  const bool fused = fused_ok && (h->verify_path == 1 || (h->verify_path == 0 && rows >= qe::verify_min_rows()));
+  if (fused) return verify_fused(h, layer, q, k, v, out, n_q, flags, dl);
   const int D = c.head_dim;
   const size_t kv_tok = (size_t)h->units * D * 2;                       // one draft's K (or V)
   const size_t q_tok = (size_t)c.batch * c.n_q_heads * D * 2;           // one draft's queries
@@ -923,6 +1005,11 @@ qe_status qe_debug_inject(qe_handle h, int what, long long value) {
       if (!h) return QE_ERR_INVALID_ARG;
       if (value < 0 || value > (1 << 30)) return fail(h, QE_ERR_INVALID_ARG, "wait index %lld out of range", value);
       h->debug_expire = (int)value;
+      return QE_OK;
+    case QE_DEBUG_VERIFY_PATH:
+      if (!h) return QE_ERR_INVALID_ARG;
+      if (value < 0 || value > 2) return fail(h, QE_ERR_INVALID_ARG, "verify path %lld outside 0..2", value);
+      h->verify_path = (int)value;
       return QE_OK;
     default:
       return h ? fail(h, QE_ERR_INVALID_ARG, "unknown injection %d", what) : QE_ERR_INVALID_ARG;

@@ -114,6 +114,29 @@ struct RouteParams {
   RouteDiag* diag;   // [layers][units]
 };
 
+// Fused speculative verify (qe_verify.cu): every draft query of a unit against one read of its
+// windows, on the tensor cores.  Rows r = j G + h < 64; the drafts are already appended.
+struct VerifyParams {
+  State st;
+  int layer;
+  int L0;                 // length before the drafts (draft j sees positions < L0 + j + 1)
+  int n_q;                // drafts
+  int R;                  // rows, n_q G <= 64
+  int splits;             // CTAs per unit, each over a share of its windows
+  const uint16_t* q;      // [n_q][B][Hq][D] bf16
+  float scale_log2;       // log2(e) / sqrt(d)
+  float* part_o;          // [units][splits][64][D] unnormalised output of each split
+  float2* part_ml;        // [units][splits][64] (reference max, sum) in the log2 domain
+  float* lse;             // [units][ent_cap][64] per-window log2-sum-exp of each row
+  int ent_cap;            // windows (bf16 entries + 2-bit entries) a unit can list
+};
+cudaError_t launch_verify_fused(const VerifyParams& p, void* out, int out_fp32, float* delta, long long qstride,
+                                cudaStream_t s);
+cudaError_t prepare_verify_kernels(int D, int W);
+int verify_max_rows();
+int verify_min_rows();   // automatic path choice: fused from this many draft x head rows
+int verify_max_splits();
+
 cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t stream);
 int attn_grid(int n_sm, int units, int pslots);
 cudaError_t prepare_attn_kernels(int D, int W);
@@ -122,8 +145,9 @@ cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream);
 int attn_warps_per_cta();
 cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, int n_accept, const float* delta,
                                  long long qstride, cudaStream_t s);
+// tok_major: k and v are [n][units][D] (token-major, as a verify's drafts) instead of [units][n][D]
 cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
-                          cudaStream_t s);
+                          cudaStream_t s, bool tok_major = false);
 // routes layers [p.layer, p.layer + n_layers) in one launch
 cudaError_t launch_route(const RouteParams& p, int n_layers, cudaStream_t s);
 cudaError_t launch_commit_length(const State& st, int layer, int n, cudaStream_t s);

@@ -97,7 +97,7 @@ __global__ void qe_open_windows_kernel(State st, int layer, int n) {
 // Prefill part 2: copy n tokens (positions [L, L+n)) of K and V into their window slots in
 // fragment order.  Thread per (unit, token, channel pair); sink positions go to the sink slot.
 __global__ void qe_append_kernel(State st, int layer, int n, const uint16_t* __restrict__ k,
-                                 const uint16_t* __restrict__ v) {
+                                 const uint16_t* __restrict__ v, int tok_major) {
   const int D = st.geo.D, W = st.geo.W;
   const int pos0 = st.ldev[layer].L;
   if (pos0 + n > st.max_context) {
@@ -115,7 +115,7 @@ __global__ void qe_append_kernel(State st, int layer, int n, const uint16_t* __r
     const int pos = pos0 + tk;
     const int c = 2 * cp;
     const long long gu = (long long)layer * st.units + u;
-    const size_t src = ((size_t)u * n + tk) * D + c;
+    const size_t src = (tok_major ? (size_t)tk * st.units + u : (size_t)u * n + tk) * D + c;
     int slot, row;
     if (pos < st.n_sink) {
       slot = 0;
@@ -1064,8 +1064,8 @@ cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, in
 }
 
 cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, const uint16_t* v, int n_sm,
-                          cudaStream_t s) {
-  if (n == 1) {
+                          cudaStream_t s, bool tok_major) {
+  if (n == 1 && !tok_major) {
     qe_append1_kernel<<<(st.units + APPEND1_UNITS - 1) / APPEND1_UNITS, APPEND1_UNITS * (st.geo.D / 2), 0, s>>>(
         st, layer, k, v);
     return cudaGetLastError();
@@ -1076,7 +1076,7 @@ cudaError_t launch_append(const State& st, int layer, int n, const uint16_t* k, 
   const long long cap = (long long)n_sm * 16;
   if (blocks > cap) blocks = cap;
   if (blocks < 1) blocks = 1;
-  qe_append_kernel<<<(int)blocks, 256, 0, s>>>(st, layer, n, k, v);
+  qe_append_kernel<<<(int)blocks, 256, 0, s>>>(st, layer, n, k, v, tok_major ? 1 : 0);
   return cudaGetLastError();
 }
 
