@@ -200,6 +200,9 @@ def run_ours(args):
     stream = torch.cuda.Stream(dev)     # capturable: all work of this run is ordered on it
     torch.cuda.set_stream(stream)
     cache = qe.QECache(qe.config_from_workload(wl, max_context=max_ctx), stream.cuda_stream)
+    if verify:
+        vpath = {"auto": 0, "fused": 1, "per_draft": 2}[args.verify_path]
+        assert qe.debug_inject(qe.QE_DEBUG_VERIFY_PATH, vpath, cache) == qe.QE_OK
     g = gcuda.DeviceGenerator(wl, device=dev)
 
     # prefill, one layer at a time (2 x B x Hkv x L0 x d bf16 = 2 GB per layer)
@@ -431,7 +434,7 @@ def run_ours(args):
     }
     if verify:
         line["config"]["verify"] = {
-            "drafts_per_step": NQ, "accepted": "all",
+            "drafts_per_step": NQ, "accepted": "all", "path": args.verify_path,
             "step": "per layer qe_verify of the drafts (each draft query attends over the cache and the "
                     "drafts before it; masses held per query) then qe_verify_commit; value counts every draft"}
     cache.close()
@@ -543,6 +546,9 @@ def main():
     ap.add_argument("--batch", type=int, default=0, help="profiling only: other batch than the workload")
     ap.add_argument("--verify", type=int, default=0,
                     help="steps are speculative verifies of this many drafts per layer, all accepted")
+    ap.add_argument("--verify-path", choices=["auto", "fused", "per_draft"], default="auto",
+                    help="qe_verify's path (QE_DEBUG_VERIFY_PATH): automatic, the fused tensor-core "
+                         "launch, or one decode step per draft")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3

@@ -610,10 +610,21 @@ static qe_status verify_fused(qe_handle h, int layer, const void* q, const void*
     qd = static_cast<const uint16_t*>(h->stage[2]);
     od = h->stage[3];
   }
-  // splits: about two CTAs per SM over the layer's units
-  int splits = (2 * h->n_sm + h->units - 1) / h->units;
-  if (splits > qe::verify_max_splits()) splits = qe::verify_max_splits();
-  if (splits < 1) splits = 1;
+  // splits: the fewest that fill the resident CTA slots in nearly whole waves (a partial last
+  // wave leaves SMs idle for a whole CTA's time)
+  const int slots = h->n_sm * qe::verify_ctas_per_sm(D, c.window);
+  int splits = 1;
+  double best = -1.0;
+  for (int sp = 1; sp <= qe::verify_max_splits(); ++sp) {
+    const long long ctas = (long long)h->units * sp;
+    const long long waves = (ctas + slots - 1) / slots;
+    const double eff = (double)ctas / (double)(waves * slots);
+    if (eff > best + 1e-9) {
+      best = eff;
+      splits = sp;
+    }
+    if (ctas >= slots && eff >= 0.9) break;
+  }
   const int rows = qe::verify_max_rows();
   const int ent_cap = h->st.capb + h->st.capq;
   if (!h->vf_part_o || h->vf_splits < splits) {

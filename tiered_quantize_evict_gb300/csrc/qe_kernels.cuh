@@ -136,6 +136,7 @@ cudaError_t prepare_verify_kernels(int D, int W);
 int verify_max_rows();
 int verify_min_rows();   // automatic path choice: fused from this many draft x head rows
 int verify_max_splits();
+int verify_ctas_per_sm(int D, int W);   // resident verify CTAs per SM (tensor memory, shared memory)
 
 cudaError_t launch_decode_attn(const AttnParams& p, int grid, cudaStream_t stream);
 int attn_grid(int n_sm, int units, int pslots);

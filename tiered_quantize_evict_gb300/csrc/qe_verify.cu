@@ -2,35 +2,43 @@
 //
 // H2O page, §5 (speculative decoding): each draft query attends over the cache and the drafts
 // before it, and its window masses are held back until the drafts are accepted or rejected.
-// The n_q draft queries of a unit share every cached key and value, so their attention is one
-// dense contraction of (n_q x G) query rows against each window: this file runs it on the 5th-
-// generation tensor cores (tcgen05.mma, accumulators in tensor memory), reading every window
+// The n_q draft queries of a unit share every cached key and value, so their attention is a
+// dense contraction of the (n_q x G) query rows against each window: this file runs it on the
+// 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory), reading every window
 // once for all rows, instead of one decode step per draft.
 //
-// Layout of the work: one CTA of 128 threads per (unit, split of the unit's windows).
-//  * Rows: row r = j G + h is draft j's query head h (r < 64 = 16 drafts x 4 heads).  The mma
-//    is M = 64; its accumulator row r sits in tensor-memory lane 32 (r / 16) + r % 16, so warp
-//    w's lanes 0..15 own rows 16 w .. 16 w + 15 and each such thread runs its row's softmax.
-//  * Per window (W tokens), all in shared memory in the no-swizzle K-major core-matrix layout
-//    (8 rows x 16 bytes per core matrix, the two halves of a 16-wide K step 128 bytes apart):
-//      - keys as the B operand of S = Q K^T: bf16 windows as stored; a 2-bit window's keys
-//        dequantized (code * s + z, one float32 fma, as the oracle does) and split into three
-//        bf16 parts (truncated, truncated remainder, rest: exact together), placed as three
-//        blocks of W rows so that one mma chain over N = 3W gives all three partial products;
-//      - values as the B operand of O += P V, channels as rows: bf16 values, or a 2-bit window's
-//        codes as 1 + code / 4 (exact in bf16), the value scale folded into P and the offset
-//        sum_t p_t (z_t - 4 s_t) kept per row in a register;
-//      - P (times 4 s_V for 2-bit windows) as the A operand of O += P V, three exact bf16 parts
-//        along K.
-//    Q (bf16, exact) is loaded once.  Every operand is bf16, so all products are exact and
-//    accumulate in float32: no magnitude leaves the operand format.
-//  * S (up to 3W columns) and O (D columns) live in tensor memory; a row's online softmax rescales
-//    its O row there (tcgen05.ld / st) when its reference maximum grows by more than 2^8.
+// One CTA of 256 threads per (unit, split of the unit's windows); a window is a "chunk".
+//  * Rows: row r = j G + h (draft j, query head h), r < 64.
+//  * S = Q K^T per chunk: M = 64 rows, N = W tokens (bf16 window) or 3W (a 2-bit window's
+//    keys dequantized as code * s + z, one float32 fma as the oracle does, and split into three
+//    bf16 parts -- truncated, truncated remainder, rest -- that are exact together; the three
+//    parts' products land in three column blocks and are summed in float32).  Q is bf16, so
+//    every product is exact.  Accumulator row r sits in tensor-memory lane 32 (r / 16) + r % 16.
+//  * O^T += V^T P^T per chunk: M = D channels (A: values with channels as rows), N = 64 rows
+//    (B: P), K = the chunk's tokens, once for P's truncated bf16 part and once for its rounded
+//    remainder (P to about 17 significant bits).  A 2-bit window's values enter as 1 + code / 4
+//    (exact in bf16) with 4 s_V folded into P and sum_t p_t (z_t - 4 s_t) kept per row.
+//    O^T lives in tensor memory for the whole CTA, channel d in lane d (lane 32 (d / 16) +
+//    d % 16 when D = 64).
+//  * Warps 0-3 run the softmax: warp w reads rows 16 w .. 16 w + 15 of S with the 16x256b
+//    tensor-memory load, which gives lane T the rows 16 w + T / 4 and 16 w + 8 + T / 4 and two
+//    adjacent columns of every 8-column block (the mma accumulator fragment), so a row's four
+//    lanes reduce with two shuffles.  A row's reference maximum grows lazily (by more than 2^8
+//    in the log2 domain); O^T's columns are then rescaled in tensor memory.
+//  * Warps 4-7 build the operands of chunk c + 1 (keys, values, the 2-bit value parameters)
+//    while the softmax works on chunk c; keys, values and P enter shared memory through
+//    stmatrix, in the no-swizzle K-major core-matrix layout (8 rows x 16 bytes per core matrix,
+//    the two halves of a 16-wide K step 128 bytes apart).  Operands and S are double-buffered;
+//    2-bit slots arrive by bulk copies three chunks ahead, bf16 slots by direct loads.
 //  * Causality among the drafts: draft j sees positions < L0 + j + 1.
 //  * Per window and row the kernel writes the log2-sum-exp of the window's logits; the combine
 //    kernel turns them into each draft's window masses once the row's normaliser is known.
-// Waits are bounded (0.2 s); an expired wait sets the sticky timeout bit and the CTA leaves
-// after the tensor-core work it issued has finished.
+// Handshakes (mbarriers): stage[s] (a 2-bit slot landed), s[b] (S of the chunk in buffer b is
+// complete), built[b] (the builders wrote buffer b; 128 arrivals), o[b] (the P V of the chunk in
+// buffer b is complete: its operands, its S buffer and P buffer are free).  Every wait is
+// bounded (0.2 s); an expired wait sets the sticky timeout bit and an abort flag that ends both
+// warp groups' loops, and the CTA leaves after the tensor-core work and copies it issued have
+// finished.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
@@ -39,28 +47,37 @@
 
 namespace qe {
 
-constexpr int VF_THREADS = 256;   // warps 0-3 own the rows; all eight build the operands
+constexpr int VF_THREADS = 256;   // warps 0-3: softmax and P V; warps 4-7: operands and S
 constexpr int VF_ROWS = 64;
+constexpr int VF_STAGES = 3;
 constexpr unsigned long long VF_WAIT_NS = 200000000ull;
 
 template <int D, int W>
 struct VfShape {
   static constexpr int NKQ = 3 * W;                       // key rows of S's B operand (3 parts)
-  static constexpr int KP = 3 * W;                        // K extent of P (3 parts)
+  static constexpr int KP = 2 * W;                        // K extent of P (2 parts)
   static constexpr int SQ = VF_ROWS * D * 2;
   static constexpr int SBK = NKQ * D * 2;
   static constexpr int SBV = D * W * 2;
   static constexpr int SAP = VF_ROWS * KP * 2;
   static constexpr int BSLOT = 4 * W * D;
   static constexpr int QSLOT = 2 * (W * D / 4) + 8 * D + 8 * W;
-  static constexpr int STAGE = ((BSLOT > QSLOT ? BSLOT : QSLOT) + 127) / 128 * 128;
-  static constexpr int SMEM = SQ + SBK + SBV + SAP + 2 * STAGE;
-  static constexpr int TO_OFF = NKQ <= 128 ? 128 : 256;  // tensor-memory column of O
-  static constexpr int TMEM_COLS = TO_OFF + D <= 256 ? 256 : 512;
+  static constexpr int STAGE = (QSLOT + 127) / 128 * 128;
+  static constexpr int OFF_BK = SQ;
+  static constexpr int OFF_BV = OFF_BK + 2 * SBK;
+  static constexpr int OFF_AP = OFF_BV + 2 * SBV;
+  static constexpr int OFF_STG = OFF_AP + 2 * SAP;
+  static constexpr int SMEM = OFF_STG + VF_STAGES * STAGE;
+  static constexpr int SCOLS = (NKQ + 31) / 32 * 32;      // tensor-memory columns of one S buffer
+  static constexpr int TO_OFF = 2 * SCOLS;                // column of O^T (64 columns)
+  static constexpr int TMEM_COLS = TO_OFF + VF_ROWS <= 256 ? 256 : 512;
+  static constexpr int CTAS_PER_SM = TMEM_COLS == 256 ? 2 : 1;
   // Dynamic shared memory requested per CTA: at least enough that no more CTAs share an SM than
-  // its 512 tensor-memory columns hold (two of 256 columns, or one of 512).
+  // its 512 tensor-memory columns hold.
   static constexpr int SMEM_FLOOR = TMEM_COLS == 256 ? 80 * 1024 : 120 * 1024;
   static constexpr int SMEM_REQ = SMEM > SMEM_FLOOR ? SMEM : SMEM_FLOOR;
+  static_assert(SMEM_REQ + 4096 <= 227 * 1024, "verify tile exceeds shared memory");
+  static_assert(CTAS_PER_SM == 1 || 2 * (SMEM_REQ + 4096) <= 228 * 1024, "two CTAs must fit an SM");
 };
 
 // byte offset of element (row, k) of an operand with kdim elements per row, K-major, no swizzle
@@ -70,9 +87,9 @@ __device__ __forceinline__ int vf_canon(int row, int k, int kdim) {
 
 // shared-memory matrix descriptor: start, leading byte offset (between the K halves of a core
 // matrix pair, 128), stride byte offset (between 8-row groups), descriptor version 1, no swizzle
-__device__ __forceinline__ unsigned long long vf_desc(const void* smem, unsigned sbo) {
+__device__ __forceinline__ unsigned long long vf_desc(unsigned saddr, unsigned sbo) {
   unsigned long long d = 0;
-  d |= (unsigned long long)((smem_u32(smem) >> 4) & 0x3FFF);
+  d |= (unsigned long long)((saddr >> 4) & 0x3FFF);
   d |= (unsigned long long)((128u >> 4) & 0x3FFF) << 16;
   d |= (unsigned long long)((sbo >> 4) & 0x3FFF) << 32;
   d |= 1ull << 46;
@@ -80,7 +97,7 @@ __device__ __forceinline__ unsigned long long vf_desc(const void* smem, unsigned
 }
 
 // instruction descriptor of kind::f16: bf16 A and B (K-major), float32 accumulator, M x N
-__device__ __forceinline__ unsigned vf_idesc(int m, int n) {
+__host__ __device__ constexpr unsigned vf_idesc(int m, int n) {
   return (1u << 4) | (1u << 7) | (1u << 10) | ((unsigned)(n >> 3) << 17) | ((unsigned)(m >> 4) << 24);
 }
 
@@ -98,6 +115,45 @@ __device__ __forceinline__ void vf_commit(unsigned bar) {
 __device__ __forceinline__ void vf_fence_before() { asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void vf_fence_after() { asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory"); }
 __device__ __forceinline__ void vf_proxy_fence() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+__device__ __forceinline__ void vf_arrive(unsigned bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+// named barrier of one warp group (128 threads); the reductions return the group's AND / OR
+__device__ __forceinline__ void vf_group_sync(int id) { asm volatile("bar.sync %0, 128;" ::"r"(id) : "memory"); }
+__device__ __forceinline__ bool vf_group_and(int id, bool v) {
+  unsigned r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.and.pred p, %2, 128, q;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((unsigned)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ bool vf_group_or(int id, bool v) {
+  unsigned r;
+  asm volatile(
+      "{\n.reg .pred p, q;\nsetp.ne.u32 q, %1, 0;\nbar.red.or.pred p, %2, 128, q;\nselp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(r)
+      : "r"((unsigned)v), "r"(id)
+      : "memory");
+  return r != 0;
+}
+// four 8 x 8 b16 matrices: register k of lane T is row T / 4, columns 2 (T % 4), +1 of matrix k;
+// lane i gives the address of row i % 8 of matrix i / 8
+__device__ __forceinline__ void vf_stmatrix4(unsigned saddr, unsigned r0, unsigned r1, unsigned r2, unsigned r3) {
+  asm volatile("stmatrix.sync.aligned.m8n8.x4.shared.b16 [%0], {%1, %2, %3, %4};" ::"r"(saddr), "r"(r0), "r"(r1),
+               "r"(r2), "r"(r3)
+               : "memory");
+}
+
+// Waits for this thread's tensor-memory loads; the registers pass through empty volatile asm
+// statements after the wait, so that no use of them is scheduled before it.
+template <int N>
+__device__ __forceinline__ void vf_wait_ld(unsigned (&v)[N]) {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < N; ++i) asm volatile("" : "+r"(v[i]));
+}
 
 // 16 consecutive float32 columns of this thread's tensor-memory lane
 __device__ __forceinline__ void vf_ld16(unsigned taddr, float (&v)[16]) {
@@ -108,7 +164,7 @@ __device__ __forceinline__ void vf_ld16(unsigned taddr, float (&v)[16]) {
         "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
       : "r"(taddr)
       : "memory");
-  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+  vf_wait_ld(r);
 #pragma unroll
   for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
 }
@@ -123,35 +179,69 @@ __device__ __forceinline__ void vf_st16(unsigned taddr, const float (&v)[16]) {
       : "memory");
 }
 
-// bounded wait on an mbarrier phase; false (and the timeout bit) when it expires
-__device__ __forceinline__ bool vf_wait(unsigned bar, unsigned parity, unsigned* err) {
-  unsigned long long t0 = 0;
+// NB 8-column blocks of 16 lanes (16x256b shape): v[4 j + e] = (lane T / 4, column 8 j + 2 (T % 4)
+// + e), v[4 j + 2 + e] = (lane 8 + T / 4, same column); the caller waits (tcgen05.wait::ld)
+template <int NB>
+__device__ __forceinline__ void vf_ld_rows(unsigned taddr, unsigned (&v)[4 * NB]);
+template <>
+__device__ __forceinline__ void vf_ld_rows<2>(unsigned taddr, unsigned (&v)[8]) {
+  asm volatile("tcgen05.ld.sync.aligned.16x256b.x2.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7])
+               : "r"(taddr)
+               : "memory");
+}
+template <>
+__device__ __forceinline__ void vf_ld_rows<4>(unsigned taddr, unsigned (&v)[16]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x4.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15])
+      : "r"(taddr)
+      : "memory");
+}
+template <>
+__device__ __forceinline__ void vf_ld_rows<8>(unsigned taddr, unsigned (&v)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.16x256b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,"
+      "%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]), "=r"(v[4]), "=r"(v[5]), "=r"(v[6]), "=r"(v[7]), "=r"(v[8]),
+        "=r"(v[9]), "=r"(v[10]), "=r"(v[11]), "=r"(v[12]), "=r"(v[13]), "=r"(v[14]), "=r"(v[15]), "=r"(v[16]),
+        "=r"(v[17]), "=r"(v[18]), "=r"(v[19]), "=r"(v[20]), "=r"(v[21]), "=r"(v[22]), "=r"(v[23]), "=r"(v[24]),
+        "=r"(v[25]), "=r"(v[26]), "=r"(v[27]), "=r"(v[28]), "=r"(v[29]), "=r"(v[30]), "=r"(v[31])
+      : "r"(taddr)
+      : "memory");
+}
+// Bounded wait on an mbarrier phase.  False when it expires (the timeout bit and the abort flag
+// are set) or when another thread has raised the abort flag meanwhile.
+__device__ __forceinline__ bool vf_wait(unsigned bar, unsigned parity, unsigned* err, volatile int* abort_flag) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const unsigned long long t0 = globaltimer_ns();
   int spins = 0;
   while (!mbar_try_wait(bar, parity)) {
-    if (++spins == 64) {
+    if (*abort_flag) return false;
+    if (++spins == 16) {
       spins = 0;
-      const unsigned long long now = globaltimer_ns();
-      if (t0 == 0) t0 = now;
-      else if (now - t0 > VF_WAIT_NS) {
+      if (globaltimer_ns() - t0 > VF_WAIT_NS) {
         atomicOr(err, ERR_TIMEOUT);
+        *abort_flag = 1;
         return false;
       }
     }
   }
   return true;
 }
-
-// the three bf16 parts of x (truncated, truncated remainder, rest), exact together
-__device__ __forceinline__ void vf_split3(float x, unsigned& h, unsigned& m, unsigned& l) {
-  const unsigned hb = __float_as_uint(x) & 0xFFFF0000u;
-  const float r = x - __uint_as_float(hb);
-  const unsigned mb = __float_as_uint(r) & 0xFFFF0000u;
-  h = hb >> 16;
-  m = mb >> 16;
-  l = pack_bf16x2_rz(r - __uint_as_float(mb), 0.f) & 0xFFFFu;
+// the same without the abort flag: the exit path's wait for work already issued
+__device__ __forceinline__ void vf_drain(unsigned bar, unsigned parity, unsigned* err) {
+  const unsigned long long t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, parity))
+    if (globaltimer_ns() - t0 > VF_WAIT_NS) {
+      atomicOr(err, ERR_TIMEOUT);
+      return;
+    }
 }
 
-// the same for a pair (x0, x1): three bf16x2 words, x0 in the low halves
+// the three bf16 parts of a pair (x0, x1) -- truncated, truncated remainder, rest (truncated),
+// exact together -- as three bf16x2 words, x0 in the low halves
 __device__ __forceinline__ void vf_split3_pair(float x0, float x1, unsigned& h, unsigned& m, unsigned& l) {
   const unsigned h0 = __float_as_uint(x0) & 0xFFFF0000u, h1 = __float_as_uint(x1) & 0xFFFF0000u;
   const float r0 = x0 - __uint_as_float(h0), r1 = x1 - __uint_as_float(h1);
@@ -160,20 +250,27 @@ __device__ __forceinline__ void vf_split3_pair(float x0, float x1, unsigned& h, 
   m = __byte_perm(m0, m1, 0x7632);
   l = pack_bf16x2_rz(r0 - __uint_as_float(m0), r1 - __uint_as_float(m1));
 }
+// two bf16 parts of a pair: truncated, and the remainder rounded to nearest
+__device__ __forceinline__ void vf_split2_pair(float x0, float x1, unsigned& h, unsigned& l) {
+  const unsigned h0 = __float_as_uint(x0) & 0xFFFF0000u, h1 = __float_as_uint(x1) & 0xFFFF0000u;
+  h = __byte_perm(h0, h1, 0x7632);
+  l = pack_bf16x2(x0 - __uint_as_float(h0), x1 - __uint_as_float(h1));
+}
+// a small integer code (0..3) as float32
+__device__ __forceinline__ float vf_code_f(unsigned x) { return __uint_as_float(0x4B000000u | x) - 8388608.f; }
 
 template <int D, int W>
-__global__ void __launch_bounds__(VF_THREADS) qe_verify_attn_kernel(const VerifyParams p) {
+__global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_verify_attn_kernel(const VerifyParams p) {
   using S = VfShape<D, W>;
+  constexpr int KS = D / 16, KT = W / 16, NB = W / 8;
   extern __shared__ __align__(1024) uint8_t smem[];
-  uint8_t* sQ = smem;
-  uint8_t* sBK = sQ + S::SQ;
-  uint8_t* sBV = sBK + S::SBK;
-  uint8_t* sAP = sBV + S::SBV;
-  uint8_t* stg_base = sAP + S::SAP;
-  __shared__ __align__(8) unsigned long long bar_stage[2], bar_s, bar_o;
+  __shared__ __align__(8) unsigned long long bar_stage[VF_STAGES], bar_s[2], bar_sfree[2], bar_built[2], bar_o[2];
   __shared__ unsigned s_tmem;
-  __shared__ float s_vs[W], s_vz[W];   // 2-bit window: 4 s_V and z_V - 4 s_V per token
-  __shared__ int s_stop;
+  __shared__ __align__(16) float s_vs[2][W];   // 2-bit window: 4 s_V per token
+  __shared__ __align__(16) float s_vz[2][W];   // and z_V - 4 s_V
+  __shared__ float s_alpha[VF_ROWS], s_zs[VF_ROWS];
+  __shared__ int s_abort;
+  __shared__ int s_pend[VF_STAGES];   // thread 128: 2-bit chunk whose copy a stage has in flight, or -1
 
   const State& st = p.st;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -181,16 +278,13 @@ __global__ void __launch_bounds__(VF_THREADS) qe_verify_attn_kernel(const Verify
   const long long gu = (long long)p.layer * st.units + u;
   const int G = st.G;
   const Geo g{D, W};
-  const LayerDev hd = st.ldev[p.layer];
-  const LayerView lv = layer_view(g, hd);
+  const LayerView lv = layer_view(g, st.ldev[p.layer]);
   const int L = lv.L, nbw = lv.nbw, nq = lv.nq;
   const int b0 = (int)((long long)split * nbw / p.splits), b1 = (int)((long long)(split + 1) * nbw / p.splits);
   const int q0 = (int)((long long)split * nq / p.splits), q1 = (int)((long long)(split + 1) * nq / p.splits);
-  const int nchunk = (b1 - b0) + (q1 - q0);
-  const bool row_warp = warp < 4;                      // warps whose lanes 0..15 own the rows
-  const int r = (warp & 3) * 16 + (lane & 15);         // the row this thread serves
-  const bool row_valid = row_warp && lane < 16 && r < p.R;
-  const int jdraft = r / G;
+  const int nbc = b1 - b0, nqc = q1 - q0, nchunk = nbc + nqc;
+  const unsigned sbase = smem_u32(smem);
+  volatile int* abort_flag = &s_abort;
 
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&s_tmem)),
@@ -199,14 +293,17 @@ __global__ void __launch_bounds__(VF_THREADS) qe_verify_attn_kernel(const Verify
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    mbar_init(smem_u32(&bar_stage[0]), 1);
-    mbar_init(smem_u32(&bar_stage[1]), 1);
-    mbar_init(smem_u32(&bar_s), 1);
-    mbar_init(smem_u32(&bar_o), 1);
+    for (int i = 0; i < VF_STAGES; ++i) mbar_init(smem_u32(&bar_stage[i]), 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&bar_s[i]), 1);
+      mbar_init(smem_u32(&bar_sfree[i]), 128);
+      mbar_init(smem_u32(&bar_built[i]), 128);
+      mbar_init(smem_u32(&bar_o[i]), 1);
+    }
     mbar_fence_init();
-    s_stop = 0;
+    s_abort = 0;
   }
-  // Q rows (zero beyond R) and zero P rows beyond R, once
+  // Q rows (zero beyond R), once
   {
     const int b = u / st.Hkv, kvh = u - b * st.Hkv, B = st.units / st.Hkv;
     for (int i = tid; i < VF_ROWS * (D / 2); i += VF_THREADS) {
@@ -216,181 +313,258 @@ __global__ void __launch_bounds__(VF_THREADS) qe_verify_attn_kernel(const Verify
         const int jj = rr / G, hh = rr - jj * G;
         val = *reinterpret_cast<const unsigned*>(p.q + (((size_t)jj * B + b) * st.Hq + kvh * G + hh) * D + c);
       }
-      *reinterpret_cast<unsigned*>(sQ + vf_canon(rr, c, D)) = val;
-    }
-    for (int i = tid; i < VF_ROWS * (S::KP / 2); i += VF_THREADS) {
-      const int rr = i / (S::KP / 2), k = 2 * (i - rr * (S::KP / 2));
-      if (rr >= p.R) *reinterpret_cast<unsigned*>(sAP + vf_canon(rr, k, S::KP)) = 0u;
+      *reinterpret_cast<unsigned*>(smem + vf_canon(rr, c, D)) = val;
     }
   }
   vf_proxy_fence();
   vf_fence_before();
   __syncthreads();
   vf_fence_after();
-  const unsigned tS = s_tmem, tO = s_tmem + S::TO_OFF;
-  const unsigned lane_off = (unsigned)((warp & 3) * 32) << 16;
+  const unsigned tbase = s_tmem;
+  const unsigned tO = tbase + S::TO_OFF;
 
-  // chunk c: bf16 entry b0 + c, then 2-bit entry q0 + (c - (b1 - b0))
-  auto chunk_entry = [&](int c, bool& is_q, int& eidx) -> int2 {
-    if (c < b1 - b0) {
-      is_q = false;
+  // chunk c: bf16 entry b0 + c, then 2-bit entry q0 + (c - nbc)
+  auto chunk_entry = [&](int c, int& eidx) -> int2 {
+    if (c < nbc) {
       eidx = b0 + c;
       return st.blist[gu * st.capb + eidx];
     }
-    is_q = true;
-    const int qi = q0 + (c - (b1 - b0));
+    const int qi = q0 + (c - nbc);
     eidx = nbw + qi;
     return st.qlist[gu * st.capq + qi];
   };
-  int pending[2] = {-1, -1};   // thread 0: chunk whose copy a stage has in flight, or -1
-  auto issue = [&](int c, int s) {
-    if (tid != 0 || c >= nchunk) return;
-    bool is_q;
-    int eidx;
-    const int2 e = chunk_entry(c, is_q, eidx);
-    const unsigned bar = smem_u32(&bar_stage[s]);
-    const uint8_t* src;
-    unsigned bytes;
-    if (!is_q) {
-      if (e.y < 0 || e.y >= st.capb) { atomicOr(st.err, ERR_TABLE); s_stop = 1; return; }
-      src = st.bslab + (gu * st.capb + e.y) * (long long)S::BSLOT;
-      bytes = S::BSLOT;
-    } else {
-      if (e.y < 0 || e.y >= st.capq) { atomicOr(st.err, ERR_TABLE); s_stop = 1; return; }
-      src = st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT;
-      bytes = S::QSLOT;
-    }
-    mbar_expect_tx(bar, bytes);
-    bulk_g2s(smem_u32(stg_base + (size_t)s * S::STAGE), src, bytes, bar);
-    pending[s] = c;
-  };
-  issue(0, 0);
-  issue(1, 1);
 
-  float mref = -INFINITY, lsum = 0.f, zs = 0.f;
-  bool o_init = false;
-  bool s_left = false;   // an S mma whose completion was not seen
-  int c = 0;
-  bool ok = true;
-  for (; c < nchunk; ++c) {
-    const int sidx = c & 1;
-    bool is_q;
-    int eidx;
-    const int2 ent = chunk_entry(c, is_q, eidx);
-    const int win = ent.x;
-    // previous P V done (its operands and O may be rewritten) and this chunk's copy landed; every
-    // thread agrees on the outcome before anyone leaves the loop
-    bool w_ok = c == 0 || vf_wait(smem_u32(&bar_o), (c - 1) & 1, st.err);
-    w_ok = vf_wait(smem_u32(&bar_stage[sidx]), (c >> 1) & 1, st.err) && w_ok;
-    if (tid == 0 && w_ok) pending[sidx] = -1;
-    if (!__syncthreads_and(w_ok) || s_stop) { ok = false; break; }
-    const uint8_t* sp = stg_base + (size_t)sidx * S::STAGE;
-    // ---- operands.  Layout arithmetic at compile time (every divisor is a power of two); in the
-    // K-major core-matrix layout, row + 8 is the next 8-row group (+ kdim * 16 bytes) and column
-    // + 8 the next core matrix (+ 128 bytes), so each piece's four registers land at one base plus
-    // constants.
-    if (!is_q) {
-      // a bf16 slot in mma fragment order: each 16-byte piece is one lane's four registers of a
-      // 16 x 16 fragment (rows g, g + 8 at columns 2t, 2t + 8); keys have tokens as rows, values
-      // channels as rows
-      constexpr int KS = D / 16, SUBB = 64 * D, NKC = (W / 16) * KS * 32;
-      for (int i = tid; i < 2 * NKC; i += VF_THREADS) {
-        const bool value = i >= NKC;
-        const int ii = value ? i - NKC : i;
-        const int ln = ii & 31, blk = (ii >> 5) % KS, sub = (ii >> 5) / KS;
-        const int gg = ln >> 2, tt = ln & 3;
-        const uint4 x = *reinterpret_cast<const uint4*>(sp + sub * SUBB + (value ? 32 * D : 0) + blk * 512 + ln * 16);
-        // keys: token 16 sub + gg, channel 16 blk + 2 tt; values: channel 16 blk + gg, token 16 sub + 2 tt
-        uint8_t* dst = value ? sBV + vf_canon(16 * blk + gg, 16 * sub + 2 * tt, W)
-                             : sBK + vf_canon(16 * sub + gg, 16 * blk + 2 * tt, D);
-        const int row8 = value ? W * 16 : D * 16;   // + 8 rows
-        *reinterpret_cast<unsigned*>(dst) = x.x;
-        *reinterpret_cast<unsigned*>(dst + row8) = x.y;
-        *reinterpret_cast<unsigned*>(dst + 128) = x.z;
-        *reinterpret_cast<unsigned*>(dst + row8 + 128) = x.w;
+  if (warp >= 4) {
+    // ============================== operand builders (warps 4-7) and the S issuer (thread 128)
+    const int bt = tid - 128, bw = warp - 4;
+    const int tt = lane & 3;
+    int s_issued = 0;
+    if (bt == 0)
+      for (int i = 0; i < VF_STAGES; ++i) s_pend[i] = -1;
+    auto issue_copy = [&](int i) {   // thread 128: 2-bit chunk i of this split into stage i % VF_STAGES
+      int eidx;
+      const int2 e = chunk_entry(nbc + i, eidx);
+      if (e.y < 0 || e.y >= st.capq) return;   // reported by the builders when they reach it
+      const unsigned bar = smem_u32(&bar_stage[i % VF_STAGES]);
+      mbar_expect_tx(bar, S::QSLOT);
+      bulk_g2s(sbase + S::OFF_STG + (i % VF_STAGES) * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT,
+               S::QSLOT, bar);
+      s_pend[i % VF_STAGES] = i;
+    };
+    if (bt == 0)
+      for (int i = 0; i < VF_STAGES && i < nqc; ++i) issue_copy(i);
+    for (int c = 0; c < nchunk; ++c) {
+      const int b = c & 1;
+      int eidx;
+      const int2 ent = chunk_entry(c, eidx);
+      const bool is_q = c >= nbc;
+      const int qi = c - nbc;
+      bool ok = ent.y >= 0 && ent.y < (is_q ? st.capq : st.capb);
+      if (!ok && bt == 0) {
+        atomicOr(st.err, ERR_TABLE);
+        *abort_flag = 1;
       }
-    } else {
-      // 2-bit codes: word wi of a code block holds fragments 2 wj, 2 wj + 1 of one lane (wj and
-      // the lane from wi), register reg of fragment f at bits 8 f + 2 reg (+ 16 for the second
-      // element); fragment 2 wj + 1 is the next 16-wide K step (keys) or token step (values)
-      constexpr int KS = D / 16, KT = W / 16, WPL = KT * KS / 2, CW = WPL < 4 ? WPL : 4, NWORD = 32 * WPL;
-      const float* kmin = reinterpret_cast<const float*>(sp + g.off_kmin());
-      const float* kscale = reinterpret_cast<const float*>(sp + g.off_kscale());
-      static_assert(KS % 2 == 0, "a key word's two fragments are consecutive channel steps");
-      for (int i = tid; i < 2 * NWORD; i += VF_THREADS) {
-        const bool value = i >= NWORD;
-        const int wi = value ? i - NWORD : i;
-        const unsigned w = *reinterpret_cast<const unsigned*>(sp + (value ? g.off_vcode() : 0) + 4 * wi);
-        const int chunk = wi / (32 * CW), rem = wi % (32 * CW);
-        const int ln = rem / CW, wj = chunk * CW + rem % CW;
-        const int gg = ln >> 2, tt = ln & 3;
-        const int F0 = 2 * wj;
-        if (!value) {
-          const int mt = F0 / KS, ks = F0 % KS;   // fragment 2 wj + 1: channel step ks + 1
-          const int t = 16 * mt + gg, ch = 16 * ks + 2 * tt;
-          uint8_t* dst = sBK + vf_canon(t, ch, D);
+      // keys of buffer b: their last reader, S of chunk c - 2, must be complete
+      if (ok && c >= 2) ok = vf_wait(smem_u32(&bar_s[b]), ((c - 2) >> 1) & 1, st.err, abort_flag);
+      if (ok && is_q) ok = vf_wait(smem_u32(&bar_stage[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag);
+      if (!vf_group_and(1, ok && !*abort_flag)) break;
+      if (bt == 0 && is_q) s_pend[qi % VF_STAGES] = -1;
+      const unsigned sBK = sbase + S::OFF_BK + b * S::SBK, sBV = sbase + S::OFF_BV + b * S::SBV;
+      const uint8_t* sp = smem + S::OFF_STG + (qi % VF_STAGES) * S::STAGE;   // 2-bit chunk's stage
+      constexpr int WPL = (W / 16) * (D / 16) / 2, CW = WPL < 4 ? WPL : 4;
+      auto word_at = [&](int byte0, int wj) -> unsigned {   // this lane's word wj of a code block
+        return *reinterpret_cast<const unsigned*>(sp + byte0 + ((wj / CW) * 32 + lane) * (CW * 4) + (wj % CW) * 4);
+      };
+      // bf16 slot, straight from global memory: each 512-byte fragment is one lane's 16 bytes
+      // (rows g, g + 8 at columns 2t, 2t + 8); keys have tokens as rows, values channels
+      constexpr int NF = 2 * KT * KS, FPW = (NF + 3) / 4;
+      uint4 x[FPW];
+      if (!is_q) {
+        const uint8_t* slot = st.bslab + (gu * st.capb + ent.y) * (long long)S::BSLOT;
 #pragma unroll
-          for (int f = 0; f < 2; ++f)
-#pragma unroll
-            for (int reg = 0; reg < 4; ++reg) {
-              const int c2 = ch + 16 * f + 8 * (reg >> 1);
-              const float2 sc = *reinterpret_cast<const float2*>(kscale + kparam_pos(c2));
-              const float2 mn = *reinterpret_cast<const float2*>(kmin + kparam_pos(c2));
-              const unsigned x = w >> (8 * f + 2 * reg);
-              unsigned hp, mp, lp;
-              vf_split3_pair(fmaf((float)(x & 3u), sc.x, mn.x), fmaf((float)((x >> 16) & 3u), sc.y, mn.y), hp, mp,
-                             lp);
-              uint8_t* d0 = dst + f * 256 + (reg & 1) * (D * 16) + (reg >> 1) * 128;
-              *reinterpret_cast<unsigned*>(d0) = hp;
-              *reinterpret_cast<unsigned*>(d0 + W * D * 2) = mp;        // part 2: rows W ..
-              *reinterpret_cast<unsigned*>(d0 + 2 * W * D * 2) = lp;    // part 3: rows 2W ..
-            }
-        } else {
-          // fragment 2 wj + 1: token step kt + 1, or with one token step (W = 16) the next channel
-          // block (16 rows further)
-          const int mc = F0 / KT, kt = F0 % KT;
-          constexpr int F1 = KT >= 2 ? 256 : 2 * W * 16;
-          uint8_t* dst = sBV + vf_canon(16 * mc + gg, 16 * kt + 2 * tt, W);
-#pragma unroll
-          for (int f = 0; f < 2; ++f)
-#pragma unroll
-            for (int reg = 0; reg < 4; ++reg) {
-              const unsigned x = w >> (8 * f + 2 * reg);
-              *reinterpret_cast<unsigned*>(dst + f * F1 + (reg & 1) * (W * 16) + (reg >> 1) * 128) =
-                  0x3F803F80u | ((x & 3u) << 5) | (((x >> 16) & 3u) << 21);
-            }
+        for (int k = 0; k < FPW; ++k) {
+          const int fi = bw + 4 * k;
+          if (fi < NF) {
+            const bool value = fi >= KT * KS;
+            const int ff = value ? fi - KT * KS : fi, sub = ff / KS, blk = ff % KS;
+            x[k] = __ldg(reinterpret_cast<const uint4*>(slot + sub * (64 * D) + (value ? 32 * D : 0) + blk * 512) + lane);
+          }
         }
       }
-      if (tid < W) {
-        const float vsc = reinterpret_cast<const float*>(sp + g.off_vscale())[vparam_pos(g, tid)];
-        const float vmn = reinterpret_cast<const float*>(sp + g.off_vmin())[vparam_pos(g, tid)];
-        s_vs[tid] = 4.f * vsc;
-        s_vz[tid] = vmn - 4.f * vsc;
-      }
-    }
-    vf_proxy_fence();
-    vf_fence_before();
-    __syncthreads();
-    vf_fence_after();
-    issue(c + 2, sidx);   // every thread has read the stage
-    // ---- S = Q K^T (N = W, or 3W for a 2-bit window's three key parts)
-    const int nk = is_q ? 3 * W : W;
-    if (tid == 0) {
-      const unsigned idesc = vf_idesc(VF_ROWS, nk);
+      auto store_bf16 = [&](bool values) {   // matrix k: rows + 8 (k & 1) + row, columns + 8 (k >> 1)
+        const int m = lane >> 3;
 #pragma unroll
-      for (int ks = 0; ks < D / 16; ++ks)
-        vf_mma(tS, vf_desc(sQ + ks * 256, (D / 8) * 128), vf_desc(sBK + ks * 256, (D / 8) * 128), idesc, ks > 0);
-      vf_commit(smem_u32(&bar_s));
+        for (int k = 0; k < FPW; ++k) {
+          const int fi = bw + 4 * k;
+          if (fi < NF && (fi >= KT * KS) == values) {
+            const int ff = values ? fi - KT * KS : fi, sub = ff / KS, blk = ff % KS;
+            const unsigned dst = values
+                                     ? sBV + vf_canon(16 * blk + 8 * (m & 1) + (lane & 7), 16 * sub + 8 * (m >> 1), W)
+                                     : sBK + vf_canon(16 * sub + 8 * (m & 1) + (lane & 7), 16 * blk + 8 * (m >> 1), D);
+            vf_stmatrix4(dst, x[k].x, x[k].y, x[k].z, x[k].w);
+          }
+        }
+      };
+      // ---- keys
+      if (!is_q) {
+        store_bf16(false);
+      } else if (bw < WPL) {
+        // word wj holds fragments 2 wj, 2 wj + 1 (token tile mt, channel steps ks, ks + 1); a
+        // warp's words share ks, so its lanes' channel parameters load once
+        const int ks = (2 * bw) % KS;
+        const float* kmin = reinterpret_cast<const float*>(sp + g.off_kmin());
+        const float* kscale = reinterpret_cast<const float*>(sp + g.off_kscale());
+        // lane's channels of channel step ks + f: 16 (ks + f) + 2 tt + {0, 1, 8, 9}, one vector
+        const float4 sc0 = *reinterpret_cast<const float4*>(kscale + 16 * ks + 4 * tt);
+        const float4 sc1 = *reinterpret_cast<const float4*>(kscale + 16 * (ks + 1) + 4 * tt);
+        const float4 mn0 = *reinterpret_cast<const float4*>(kmin + 16 * ks + 4 * tt);
+        const float4 mn1 = *reinterpret_cast<const float4*>(kmin + 16 * (ks + 1) + 4 * tt);
+        for (int wj = bw; wj < WPL; wj += 4) {
+          const unsigned w = word_at(0, wj);
+          const int mt = (2 * wj) / KS;
+#pragma unroll
+          for (int f = 0; f < 2; ++f) {
+            const float4 sc = f ? sc1 : sc0, mn = f ? mn1 : mn0;
+            unsigned hp[4], mp[4], lp[4];
+#pragma unroll
+            for (int reg = 0; reg < 4; ++reg) {
+              // reg: token 16 mt + gg + 8 (reg & 1), channels 16 (ks + f) + 2 tt + 8 (reg >> 1) + {0, 1}
+              const unsigned xw = w >> (8 * f + 2 * reg);
+              const float s0 = (reg >> 1) ? sc.z : sc.x, s1 = (reg >> 1) ? sc.w : sc.y;
+              const float z0 = (reg >> 1) ? mn.z : mn.x, z1 = (reg >> 1) ? mn.w : mn.y;
+              vf_split3_pair(fmaf(vf_code_f(xw & 3u), s0, z0), fmaf(vf_code_f((xw >> 16) & 3u), s1, z1), hp[reg],
+                             mp[reg], lp[reg]);
+            }
+            const int m = lane >> 3;
+            const unsigned dst = sBK + vf_canon(16 * mt + 8 * (m & 1) + (lane & 7), 16 * (ks + f) + 8 * (m >> 1), D);
+            vf_stmatrix4(dst, hp[0], hp[1], hp[2], hp[3]);
+            vf_stmatrix4(dst + W * D * 2, mp[0], mp[1], mp[2], mp[3]);       // part 2: rows W ..
+            vf_stmatrix4(dst + 2 * W * D * 2, lp[0], lp[1], lp[2], lp[3]);   // part 3: rows 2W ..
+          }
+        }
+      }
+      vf_proxy_fence();
+      vf_group_sync(1);   // every builder's keys are in place
+      if (bt == 0) {
+        // ---- S = Q K^T once the softmax of chunk c - 2 has read S out of tensor-memory buffer b
+        // (an expired wait raises the abort flag: this chunk's S is not issued and both warp
+        // groups leave at their next wait)
+        if (c < 2 || vf_wait(smem_u32(&bar_sfree[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)) {
+          vf_fence_after();
+          const unsigned tS = tbase + b * S::SCOLS;
+          const unsigned sQ = sbase;
+          if (is_q) {
+            constexpr unsigned idesc = vf_idesc(VF_ROWS, 3 * W);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+              vf_mma(tS, vf_desc(sQ + ks * 256, D * 16), vf_desc(sBK + ks * 256, D * 16), idesc, ks > 0);
+          } else {
+            constexpr unsigned idesc = vf_idesc(VF_ROWS, W);
+#pragma unroll
+            for (int ks = 0; ks < KS; ++ks)
+              vf_mma(tS, vf_desc(sQ + ks * 256, D * 16), vf_desc(sBK + ks * 256, D * 16), idesc, ks > 0);
+          }
+          vf_commit(smem_u32(&bar_s[b]));
+          ++s_issued;
+        }
+      }
+      // values of buffer b: their last reader, P V of chunk c - 2, must be complete (so are its
+      // softmax, the last reader of the value parameters).  An expired wait raises the abort
+      // flag; the group still meets at the barrier below and leaves at the next chunk.
+      if (c >= 2) vf_wait(smem_u32(&bar_o[b]), ((c - 2) >> 1) & 1, st.err, abort_flag);
+      // ---- values
+      if (!is_q) {
+        store_bf16(true);
+      } else {
+        // word wj holds fragments 2 wj, 2 wj + 1 (channel tile mc, token steps kt, kt + 1; with
+        // one token step the second fragment is the next channel tile), as 1 + code / 4
+        for (int wj = bw; wj < WPL; wj += 4) {
+          const unsigned w = word_at(g.off_vcode(), wj);
+          const int F0 = 2 * wj, mc = F0 / KT, kt = F0 % KT;
+#pragma unroll
+          for (int f = 0; f < 2; ++f) {
+            const int mcf = KT >= 2 ? mc : mc + f, ktf = KT >= 2 ? kt + f : kt;
+            unsigned r[4];
+#pragma unroll
+            for (int reg = 0; reg < 4; ++reg) {
+              const unsigned xw = w >> (8 * f + 2 * reg);
+              r[reg] = 0x3F803F80u | ((xw & 3u) << 5) | (((xw >> 16) & 3u) << 21);
+            }
+            // matrix k = reg: channels 16 mcf + 8 (k & 1) + row, tokens 16 ktf + 8 (k >> 1)
+            const int m = lane >> 3;
+            vf_stmatrix4(sBV + vf_canon(16 * mcf + 8 * (m & 1) + (lane & 7), 16 * ktf + 8 * (m >> 1), W), r[0], r[1],
+                         r[2], r[3]);
+          }
+        }
+        if (bt < W) {
+          const float vsc = reinterpret_cast<const float*>(sp + g.off_vscale())[vparam_pos(g, bt)];
+          const float vmn = reinterpret_cast<const float*>(sp + g.off_vmin())[vparam_pos(g, bt)];
+          s_vs[b][bt] = 4.f * vsc;
+          s_vz[b][bt] = vmn - 4.f * vsc;
+        }
+      }
+      vf_proxy_fence();
+      vf_arrive(smem_u32(&bar_built[b]));
+      vf_group_sync(1);   // every builder has read the stage
+      if (bt == 0 && is_q && qi + VF_STAGES < nqc) issue_copy(qi + VF_STAGES);
     }
-    if (!__syncthreads_and(vf_wait(smem_u32(&bar_s), c & 1, st.err))) {
-      ok = false;
-      ++c;   // this chunk's S mma was issued: its completion is awaited below with the P V ones
-      s_left = true;
-      break;
+    // exit: S work issued must finish before tensor memory is freed, copies before the CTA leaves
+    if (bt == 0) {
+      if (s_issued > 0) vf_drain(smem_u32(&bar_s[(s_issued - 1) & 1]), ((s_issued - 1) >> 1) & 1, st.err);
+      for (int i = 0; i < VF_STAGES; ++i)
+        if (s_pend[i] >= 0) vf_drain(smem_u32(&bar_stage[i]), (s_pend[i] / VF_STAGES) & 1, st.err);
     }
-    vf_fence_after();
-    // ---- softmax of this window, per row
-    if (row_warp) {   // warps 0-3: the sub-partitions holding the rows
+  } else {
+    // ============================== softmax (warps 0-3) and the P V issuer (thread 0)
+    const int q4 = lane & 3;
+    const int ra = 16 * warp + (lane >> 2), rb = ra + 8;   // this lane's rows
+    const bool va = ra < p.R, vb = rb < p.R;
+    const int jda = ra / G, jdb = rb / G;
+    const unsigned lane_off = (unsigned)(32 * warp) << 16;
+    float mref_a = -INFINITY, mref_b = -INFINITY, lsum_a = 0.f, lsum_b = 0.f, zs_a = 0.f, zs_b = 0.f;
+    int c = 0;
+    bool ok = true;
+    for (; c < nchunk; ++c) {
+      const int b = c & 1;
+      int eidx;
+      const int2 ent = chunk_entry(c, eidx);
+      const bool is_q = c >= nbc;
+      const int win = ent.x;
+      // S of this chunk (the wait's outcome is made uniform per warp: the loads are collective;
+      // the group agrees at the barrier below)
+      ok = __all_sync(0xffffffffu, vf_wait(smem_u32(&bar_s[b]), (c >> 1) & 1, st.err, abort_flag));
+      // ---- logits of this lane's two rows: x[4 j + e] row a, x[4 j + 2 + e] row b, token 8 j + 2 q4 + e
+      float x[4 * NB];
+      if (ok) {
+        vf_fence_after();
+        const unsigned tS = tbase + b * S::SCOLS + lane_off;
+        unsigned v0[4 * NB];
+        vf_ld_rows<NB>(tS, v0);
+        if (is_q) {
+          unsigned v1[4 * NB];
+          vf_ld_rows<NB>(tS + W, v1);
+          vf_wait_ld(v0);
+          vf_wait_ld(v1);
+#pragma unroll
+          for (int i = 0; i < 4 * NB; ++i) x[i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
+          vf_ld_rows<NB>(tS + 2 * W, v1);
+          vf_wait_ld(v1);
+#pragma unroll
+          for (int i = 0; i < 4 * NB; ++i) x[i] = (x[i] + __uint_as_float(v1[i])) * p.scale_log2;
+        } else {
+          vf_wait_ld(v0);
+#pragma unroll
+          for (int i = 0; i < 4 * NB; ++i) x[i] = __uint_as_float(v0[i]) * p.scale_log2;
+        }
+        vf_fence_before();
+        vf_arrive(smem_u32(&bar_sfree[b]));   // tensor-memory buffer b may take S of chunk c + 2
+      } else {
+#pragma unroll
+        for (int i = 0; i < 4 * NB; ++i) x[i] = -INFINITY;
+      }
+      // operands and value parameters of this chunk
+      ok = ok && vf_wait(smem_u32(&bar_built[b]), (c >> 1) & 1, st.err, abort_flag);
+      // valid tokens of the window for a row: [tmin, tmax); draft j sees positions < L0 + j + 1
       int lo, hi, pos0;
       if (!is_q && win < 0) {
         lo = 0;
@@ -401,128 +575,176 @@ __global__ void __launch_bounds__(VF_THREADS) qe_verify_attn_kernel(const Verify
         hi = is_q ? W : (L - win * W < W ? L - win * W : W);
         pos0 = win * W;
       }
-      // valid tokens of the window for this row: [tmin, tmax); draft j sees positions < L0 + j + 1
-      const int tmin = lo, tmax = min(hi, p.L0 + jdraft + 1 - pos0);
-      float x[W];
+      const int tmax_a = va ? min(hi, p.L0 + jda + 1 - pos0) : 0;
+      const int tmax_b = vb ? min(hi, p.L0 + jdb + 1 - pos0) : 0;
+      if (lo > 0 || tmax_a < W || tmax_b < W) {
 #pragma unroll
-      for (int t0 = 0; t0 < W; t0 += 16) {
-        float a[16];
-        vf_ld16(tS + lane_off + t0, a);
-        if (is_q) {
-          float b[16], d[16];
-          vf_ld16(tS + lane_off + W + t0, b);
-          vf_ld16(tS + lane_off + 2 * W + t0, d);
+        for (int j = 0; j < NB; ++j)
 #pragma unroll
-          for (int i = 0; i < 16; ++i) a[i] = (a[i] + b[i]) + d[i];
+          for (int e = 0; e < 2; ++e) {
+            const int t = 8 * j + 2 * q4 + e;
+            if (t < lo || t >= tmax_a) x[4 * j + e] = -INFINITY;
+            if (t < lo || t >= tmax_b) x[4 * j + 2 + e] = -INFINITY;
+          }
+      }
+      float ma = -INFINITY, mb = -INFINITY;
+#pragma unroll
+      for (int j = 0; j < NB; ++j) {
+        ma = fmaxf(ma, fmaxf(x[4 * j], x[4 * j + 1]));
+        mb = fmaxf(mb, fmaxf(x[4 * j + 2], x[4 * j + 3]));
+      }
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 1));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 1));
+      ma = fmaxf(ma, __shfl_xor_sync(0xffffffffu, ma, 2));
+      mb = fmaxf(mb, __shfl_xor_sync(0xffffffffu, mb, 2));
+      const bool raise_a = ma > mref_a + 8.f, raise_b = mb > mref_b + 8.f;   // false for -inf
+      const float alpha_a = (raise_a && mref_a != -INFINITY) ? ex2(mref_a - ma) : 1.f;
+      const float alpha_b = (raise_b && mref_b != -INFINITY) ? ex2(mref_b - mb) : 1.f;
+      if (q4 == 0) {
+        s_alpha[ra] = alpha_a;
+        s_alpha[rb] = alpha_b;
+      }
+      // one group barrier in the common case: nothing to rescale and no wait expired
+      if (vf_group_or(2, !ok || alpha_a != 1.f || alpha_b != 1.f)) {
+        if (vf_group_or(2, !ok)) {
+          ok = false;
+          break;
         }
+        // rescale O^T's columns: the previous chunk's P V must be complete; each lane scales its
+        // own tensor-memory lane (one channel) across the 64 row columns
+        ok = vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag);
+        if (!vf_group_and(2, ok)) {
+          ok = false;
+          break;
+        }
+        vf_fence_after();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) x[t0 + i] = a[i] * p.scale_log2;
-      }
-      if (tmin > 0 || tmax < W) {
-#pragma unroll
-        for (int t = 0; t < W; ++t)
-          if (t < tmin || t >= tmax) x[t] = -INFINITY;
-      }
-      float mx = -INFINITY;
-#pragma unroll
-      for (int t = 0; t < W; ++t) mx = fmaxf(mx, x[t]);
-      const bool raise = row_valid && mx > mref + 8.f;
-      const float mnew = raise ? mx : mref;
-      const float alpha = (raise && mref != -INFINITY) ? ex2(mref - mnew) : 1.f;
-      if (__any_sync(0xffffffffu, raise && o_init && mref != -INFINITY)) {
-        // rescale this warp's O rows (the warp's loads and stores are collective)
-#pragma unroll
-        for (int c0 = 0; c0 < D; c0 += 16) {
+        for (int c0 = 0; c0 < VF_ROWS; c0 += 16) {
           float o[16];
           vf_ld16(tO + lane_off + c0, o);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= alpha;
+          for (int i = 0; i < 16; ++i) o[i] *= s_alpha[c0 + i];
           vf_st16(tO + lane_off + c0, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
-      if (raise) {
-        lsum *= alpha;
-        zs *= alpha;
-        mref = mnew;
+      if (raise_a) {
+        lsum_a *= alpha_a;
+        zs_a *= alpha_a;
+        mref_a = ma;
       }
-      const float muse = mref == -INFINITY ? 0.f : mref;
-      float mass = 0.f, zadd = 0.f;
-      if (row_valid) {
-        uint8_t* prow = sAP + vf_canon(r, 0, S::KP);   // K index t: + (t / 8) 128 + (t % 8) 2 bytes
+      if (raise_b) {
+        lsum_b *= alpha_b;
+        zs_b *= alpha_b;
+        mref_b = mb;
+      }
+      const float mua = mref_a == -INFINITY ? 0.f : mref_a, mub = mref_b == -INFINITY ? 0.f : mref_b;
+      // ---- P (times 4 s_V for a 2-bit window) in two bf16 parts, into buffer b: rows ra, rb,
+      // K index token t (part 1) and W + t (part 2).  Buffer b's previous reader, the P V of
+      // chunk c - 2, finished before the builders marked this chunk's operands built.
+      float mass_a = 0.f, mass_b = 0.f;
+      unsigned ph[4 * NB / 2], pl[4 * NB / 2];   // [2 j + h]: block j, row half h (a, b)
 #pragma unroll
-        for (int t = 0; t < W; t += 2) {
-          float y[2];
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const float pv = ex2(x[t + e] - muse);
-            mass += pv;
-            y[e] = pv;
-            if (is_q) {
-              zadd = fmaf(pv, s_vz[t + e], zadd);
-              y[e] = pv * s_vs[t + e];
-            }
-          }
-          unsigned hp, mp, lp;
-          vf_split3_pair(y[0], y[1], hp, mp, lp);
-          uint8_t* d0 = prow + (t >> 3) * 128 + (t & 7) * 2;
-          *reinterpret_cast<unsigned*>(d0) = hp;
-          *reinterpret_cast<unsigned*>(d0 + W * 16) = mp;       // K index W + t
-          *reinterpret_cast<unsigned*>(d0 + 2 * W * 16) = lp;   // K index 2W + t
+      for (int j = 0; j < NB; ++j) {
+        const int t = 8 * j + 2 * q4;
+        float pa0 = ex2(x[4 * j] - mua), pa1 = ex2(x[4 * j + 1] - mua);
+        float pb0 = ex2(x[4 * j + 2] - mub), pb1 = ex2(x[4 * j + 3] - mub);
+        mass_a += pa0 + pa1;
+        mass_b += pb0 + pb1;
+        if (is_q) {
+          const float2 vs = *reinterpret_cast<const float2*>(&s_vs[b][t]);
+          const float2 vz = *reinterpret_cast<const float2*>(&s_vz[b][t]);
+          zs_a = fmaf(pa0, vz.x, fmaf(pa1, vz.y, zs_a));
+          zs_b = fmaf(pb0, vz.x, fmaf(pb1, vz.y, zs_b));
+          pa0 *= vs.x;
+          pa1 *= vs.y;
+          pb0 *= vs.x;
+          pb1 *= vs.y;
         }
-        lsum += mass;
-        zs += zadd;
-        p.lse[((long long)u * p.ent_cap + eidx) * VF_ROWS + r] = mass > 0.f ? muse + lg2(mass) : -INFINITY;
+        vf_split2_pair(pa0, pa1, ph[2 * j], pl[2 * j]);
+        vf_split2_pair(pb0, pb1, ph[2 * j + 1], pl[2 * j + 1]);
+      }
+      {
+        const unsigned sAP = sbase + S::OFF_AP + b * S::SAP;
+        const int m = lane >> 3;
+#pragma unroll
+        for (int j = 0; j < NB; j += 2) {
+          // matrix k: rows 16 warp + 8 (k & 1) + row, K columns 8 (j + (k >> 1)) (+ W for part 2)
+          const unsigned dst = sAP + vf_canon(16 * warp + 8 * (m & 1) + (lane & 7), 8 * (j + (m >> 1)), S::KP);
+          vf_stmatrix4(dst, ph[2 * j], ph[2 * j + 1], ph[2 * j + 2], ph[2 * j + 3]);
+          vf_stmatrix4(dst + (W / 8) * 128, pl[2 * j], pl[2 * j + 1], pl[2 * j + 2], pl[2 * j + 3]);
+        }
+      }
+      mass_a += __shfl_xor_sync(0xffffffffu, mass_a, 1);
+      mass_b += __shfl_xor_sync(0xffffffffu, mass_b, 1);
+      mass_a += __shfl_xor_sync(0xffffffffu, mass_a, 2);
+      mass_b += __shfl_xor_sync(0xffffffffu, mass_b, 2);
+      lsum_a += mass_a;   // the row's four lanes hold the same sums
+      lsum_b += mass_b;
+      if (q4 == 0) {
+        float* lrow = p.lse + ((long long)u * p.ent_cap + eidx) * VF_ROWS;
+        if (va) lrow[ra] = mass_a > 0.f ? mua + lg2(mass_a) : -INFINITY;
+        if (vb) lrow[rb] = mass_b > 0.f ? mub + lg2(mass_b) : -INFINITY;
+      }
+      vf_proxy_fence();
+      vf_fence_before();
+      vf_group_sync(2);
+      if (tid == 0) {
+        // ---- O^T += V^T P^T: both parts of P along K against the same value block
+        vf_fence_after();
+        constexpr unsigned idesc = vf_idesc(D, VF_ROWS);
+        const unsigned sBV = sbase + S::OFF_BV + b * S::SBV, sAP = sbase + S::OFF_AP + b * S::SAP;
+#pragma unroll
+        for (int part = 0; part < 2; ++part)
+#pragma unroll
+          for (int kt = 0; kt < KT; ++kt)
+            vf_mma(tO, vf_desc(sBV + kt * 256, W * 16), vf_desc(sAP + (part * KT + kt) * 256, S::KP * 16), idesc,
+                   c > 0 || part > 0 || kt > 0);
+        vf_commit(smem_u32(&bar_o[b]));
       }
     }
-    vf_proxy_fence();
-    vf_fence_before();
-    __syncthreads();
+    // c = P V launches issued (all of them on a normal exit)
+    if (ok && c > 0) ok = vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag);
+    ok = vf_group_and(2, ok);
+    if (!ok && tid == 0 && c > 0) vf_drain(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err);
     vf_fence_after();
-    // ---- O += P V: three parts of P along K, each against the same value block
-    if (tid == 0) {
-      const unsigned idesc = vf_idesc(VF_ROWS, D);
-#pragma unroll
-      for (int part = 0; part < 3; ++part)
-#pragma unroll
-        for (int kt = 0; kt < W / 16; ++kt)
-          vf_mma(tO, vf_desc(sAP + (part * (W / 16) + kt) * 256, (S::KP / 8) * 128),
-                 vf_desc(sBV + kt * 256, (W / 8) * 128), idesc, o_init || part > 0 || kt > 0);
-      vf_commit(smem_u32(&bar_o));
-    }
-    o_init = true;
-  }
-  // Before tensor memory is read or freed, the tensor-core work issued must have finished (the
-  // last P V: chunk c - 1 on a normal exit; after an expired wait also a pending S mma), and
-  // before the CTA leaves, the copies still in flight must have landed (bounded waits).
-  if (s_left) vf_wait(smem_u32(&bar_s), (c - 1) & 1, st.err);
-  if (o_init) vf_wait(smem_u32(&bar_o), ((s_left ? c - 1 : c) - 1) & 1, st.err);
-  if (tid == 0)
-    for (int s = 0; s < 2; ++s)
-      if (pending[s] >= 0) vf_wait(smem_u32(&bar_stage[s]), (pending[s] >> 1) & 1, st.err);
-  vf_fence_after();
-  const size_t pbase = ((size_t)u * p.splits + split) * VF_ROWS;
-  if (ok && row_warp) {
-#pragma unroll
-    for (int c0 = 0; c0 < D; c0 += 16) {
-      float o[16];
-      if (o_init) vf_ld16(tO + lane_off + c0, o);
-      else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) o[i] = 0.f;
+    if (ok) {
+      zs_a += __shfl_xor_sync(0xffffffffu, zs_a, 1);   // per-lane shares of the row's offset sum
+      zs_b += __shfl_xor_sync(0xffffffffu, zs_b, 1);
+      zs_a += __shfl_xor_sync(0xffffffffu, zs_a, 2);
+      zs_b += __shfl_xor_sync(0xffffffffu, zs_b, 2);
+      const size_t pbase = ((size_t)u * p.splits + split) * VF_ROWS;
+      if (q4 == 0) {
+        s_zs[ra] = zs_a;
+        s_zs[rb] = zs_b;
+        if (va) p.part_ml[pbase + ra] = make_float2(mref_a, lsum_a);
+        if (vb) p.part_ml[pbase + rb] = make_float2(mref_b, lsum_b);
       }
-      if (row_valid) {
-        float* po = p.part_o + (pbase + r) * D + c0;
+      vf_group_sync(2);
+      // O^T: this lane's tensor-memory lane is channel d, its columns the rows
+      const int d = D == 128 ? 32 * warp + lane : 16 * warp + lane;
+      const bool dv = D == 128 || lane < 16;
 #pragma unroll
-        for (int i = 0; i < 16; ++i) po[i] = o[i] + zs;
+      for (int c0 = 0; c0 < VF_ROWS; c0 += 16) {
+        float o[16];
+        if (c > 0) vf_ld16(tO + lane_off + c0, o);
+        else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+        }
+        if (dv)
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (c0 + i < p.R) p.part_o[(pbase + c0 + i) * D + d] = o[i] + s_zs[c0 + i];
       }
     }
-    if (row_valid) p.part_ml[pbase + r] = make_float2(mref, lsum);
   }
   vf_fence_before();
   __syncthreads();
-  if (warp == 0)
+  if (warp == 0) {
+    vf_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s_tmem), "r"(S::TMEM_COLS) : "memory");
+  }
 }
 
 // ------------------------------------------------------------------------------ combine
@@ -626,6 +848,16 @@ cudaError_t launch_verify_fused(const VerifyParams& p, void* out, int out_fp32, 
   if (D == 64 && W == 32) return vf_launch_t<64, 32>(p, out, out_fp32, delta, qstride, s);
   if (D == 64 && W == 64) return vf_launch_t<64, 64>(p, out, out_fp32, delta, qstride, s);
   return cudaErrorInvalidValue;
+}
+
+int verify_ctas_per_sm(int D, int W) {
+  if (D == 128 && W == 16) return VfShape<128, 16>::CTAS_PER_SM;
+  if (D == 128 && W == 32) return VfShape<128, 32>::CTAS_PER_SM;
+  if (D == 128 && W == 64) return VfShape<128, 64>::CTAS_PER_SM;
+  if (D == 64 && W == 16) return VfShape<64, 16>::CTAS_PER_SM;
+  if (D == 64 && W == 32) return VfShape<64, 32>::CTAS_PER_SM;
+  if (D == 64 && W == 64) return VfShape<64, 64>::CTAS_PER_SM;
+  return 1;
 }
 
 int verify_max_rows() { return VF_ROWS; }
