@@ -1025,16 +1025,19 @@ __global__ void __launch_bounds__(MOVE_THREADS, MOVE_CTAS_PER_SM) qe_move_kernel
 // decoding): drafts [n_accept, n_q) are dropped -- the windows they opened close in reverse
 // opening order (their bf16 slots go back to the free list's head, from which they were taken;
 // the slot no longer holds an evicted window's exact data) -- and the accepted queries' window
-// masses are added to the scores in query order.  One CTA per unit; block 0 sets the length.
-__global__ void qe_verify_commit_kernel(State st, int layer, int L0, int n_q, int n_accept, const float* delta,
-                                        long long qstride) {
-  const int u = blockIdx.x;
+// masses are added to the scores in query order.  CTAs (unit, y): y = 0 closes the dropped
+// drafts' windows (all of them at or past the new window count), every y adds the masses of a
+// quarter of the kept windows; block (0, 0) sets the length.
+constexpr int VCOMMIT_SPLIT = 4;
+__global__ void __launch_bounds__(256) qe_verify_commit_kernel(State st, int layer, int L0, int n_q, int n_accept,
+                                                               const float* delta, long long qstride) {
+  const int u = blockIdx.x, y = blockIdx.y;
   const long long gu = (long long)layer * st.units + u;
   const int W = st.geo.W;
   const int new_L = L0 + n_accept, old_L = L0 + n_q;
   const int first_opened = (L0 + W - 1) / W;             // windows starting at or after L0
   const int new_nwin = (new_L + W - 1) / W, old_nwin = (old_L + W - 1) / W;
-  if (threadIdx.x == 0) {
+  if (y == 0 && threadIdx.x == 0) {
     for (int j = old_nwin - 1; j >= new_nwin && j >= first_opened; --j) {
       const int s = st.bslot[gu * st.maxw + j];
       const int head = st.bfree_head[gu] - 1;
@@ -1049,17 +1052,19 @@ __global__ void qe_verify_commit_kernel(State st, int layer, int L0, int n_q, in
       st.score[gu * st.maxw + j] = 0.f;
     }
   }
-  for (int j = threadIdx.x; j < new_nwin; j += blockDim.x) {
+  const int j0 = (int)((long long)y * new_nwin / VCOMMIT_SPLIT), j1 = (int)((long long)(y + 1) * new_nwin / VCOMMIT_SPLIT);
+  for (int j = j0 + threadIdx.x; j < j1; j += blockDim.x) {
+    const float* dj = delta + (long long)u * st.maxw + j;
     float sc = st.score[gu * st.maxw + j];
-    for (int q = 0; q < n_accept; ++q) sc += delta[q * qstride + (long long)u * st.maxw + j];
+    for (int q = 0; q < n_accept; ++q) sc += dj[q * qstride];
     st.score[gu * st.maxw + j] = sc;
   }
-  if (u == 0 && threadIdx.x == 0) st.ldev[layer].L = new_L;
+  if (u == 0 && y == 0 && threadIdx.x == 0) st.ldev[layer].L = new_L;
 }
 
 cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, int n_accept, const float* delta,
                                  long long qstride, cudaStream_t s) {
-  qe_verify_commit_kernel<<<st.units, 128, 0, s>>>(st, layer, L0, n_q, n_accept, delta, qstride);
+  qe_verify_commit_kernel<<<dim3(st.units, VCOMMIT_SPLIT), 256, 0, s>>>(st, layer, L0, n_q, n_accept, delta, qstride);
   return cudaGetLastError();
 }
 

@@ -47,7 +47,7 @@
 
 namespace qe {
 
-constexpr int VF_THREADS = 256;   // warps 0-3: softmax and P V; warps 4-7: operands and S
+constexpr int VF_THREADS = 288;   // warps 0-3: softmax; warps 4-7: operands; warp 8: tensor-core issue
 constexpr int VF_ROWS = 64;
 constexpr int VF_STAGES = 3;
 constexpr unsigned long long VF_WAIT_NS = 200000000ull;
@@ -67,7 +67,8 @@ struct VfShape {
   static constexpr int OFF_BV = OFF_BK + 2 * SBK;
   static constexpr int OFF_AP = OFF_BV + 2 * SBV;
   static constexpr int OFF_STG = OFF_AP + 2 * SAP;
-  static constexpr int SMEM = OFF_STG + VF_STAGES * STAGE;
+  static constexpr int OFF_TAB = OFF_STG + VF_STAGES * STAGE;   // key tables: 4 x [32 channels][4 codes] x 8 B
+  static constexpr int SMEM = OFF_TAB + 4 * 1024;
   static constexpr int SCOLS = (NKQ + 31) / 32 * 32;      // tensor-memory columns of one S buffer
   static constexpr int TO_OFF = 2 * SCOLS;                // column of O^T (64 columns)
   static constexpr int TMEM_COLS = TO_OFF + VF_ROWS <= 256 ? 256 : 512;
@@ -263,14 +264,18 @@ template <int D, int W>
 __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_verify_attn_kernel(const VerifyParams p) {
   using S = VfShape<D, W>;
   constexpr int KS = D / 16, KT = W / 16, NB = W / 8;
+  constexpr int WPL = (W / 16) * (D / 16) / 2, CW = WPL < 4 ? WPL : 4;   // code words per lane
+  constexpr int NFK = KT * KS, FK = (NFK + 3) / 4;                       // bf16 key (value) fragments, per warp
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) unsigned long long bar_stage[VF_STAGES], bar_s[2], bar_sfree[2], bar_built[2], bar_o[2];
+  __shared__ __align__(8) unsigned long long bar_stage[VF_STAGES], bar_s[2], bar_sfree[2], bar_keys[2], bar_built[2],
+      bar_p[2], bar_o[2];
   __shared__ unsigned s_tmem;
   __shared__ __align__(16) float s_vs[2][W];   // 2-bit window: 4 s_V per token
   __shared__ __align__(16) float s_vz[2][W];   // and z_V - 4 s_V
   __shared__ float s_alpha[VF_ROWS], s_zs[VF_ROWS];
   __shared__ int s_abort;
-  __shared__ int s_pend[VF_STAGES];   // thread 128: 2-bit chunk whose copy a stage has in flight, or -1
+  __shared__ int s_stage_rel[VF_STAGES];   // builder warps done with a stage's current slot
+  __shared__ int s_stage_cnt[VF_STAGES];   // copies issued into a stage
 
   const State& st = p.st;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -293,11 +298,17 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
-    for (int i = 0; i < VF_STAGES; ++i) mbar_init(smem_u32(&bar_stage[i]), 1);
+    for (int i = 0; i < VF_STAGES; ++i) {
+      mbar_init(smem_u32(&bar_stage[i]), 1);
+      s_stage_rel[i] = 0;
+      s_stage_cnt[i] = 0;
+    }
     for (int i = 0; i < 2; ++i) {
       mbar_init(smem_u32(&bar_s[i]), 1);
       mbar_init(smem_u32(&bar_sfree[i]), 128);
+      mbar_init(smem_u32(&bar_keys[i]), 128);
       mbar_init(smem_u32(&bar_built[i]), 128);
+      mbar_init(smem_u32(&bar_p[i]), 128);
       mbar_init(smem_u32(&bar_o[i]), 1);
     }
     mbar_fence_init();
@@ -325,6 +336,10 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
 
   // chunk c: bf16 entry b0 + c, then 2-bit entry q0 + (c - nbc)
   auto chunk_entry = [&](int c, int& eidx) -> int2 {
+    if (c >= nchunk) {
+      eidx = 0;
+      return make_int2(0, -1);
+    }
     if (c < nbc) {
       eidx = b0 + c;
       return st.blist[gu * st.capb + eidx];
@@ -333,71 +348,120 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
     eidx = nbw + qi;
     return st.qlist[gu * st.capq + qi];
   };
+  // thread that issues a copy: 2-bit chunk i of this split into stage i % VF_STAGES
+  auto issue_copy = [&](int i) {
+    int eidx;
+    const int2 e = chunk_entry(nbc + i, eidx);
+    if (e.y < 0 || e.y >= st.capq) return;   // reported by the builders when they reach it
+    const int sidx = i % VF_STAGES;
+    const unsigned bar = smem_u32(&bar_stage[sidx]);
+    atomicAdd(&s_stage_cnt[sidx], 1);
+    mbar_expect_tx(bar, S::QSLOT);
+    bulk_g2s(sbase + S::OFF_STG + sidx * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT, S::QSLOT,
+             bar);
+  };
 
-  if (warp >= 4) {
-    // ============================== operand builders (warps 4-7) and the S issuer (thread 128)
-    const int bt = tid - 128, bw = warp - 4;
-    const int tt = lane & 3;
-    int s_issued = 0;
-    if (bt == 0)
-      for (int i = 0; i < VF_STAGES; ++i) s_pend[i] = -1;
-    auto issue_copy = [&](int i) {   // thread 128: 2-bit chunk i of this split into stage i % VF_STAGES
-      int eidx;
-      const int2 e = chunk_entry(nbc + i, eidx);
-      if (e.y < 0 || e.y >= st.capq) return;   // reported by the builders when they reach it
-      const unsigned bar = smem_u32(&bar_stage[i % VF_STAGES]);
-      mbar_expect_tx(bar, S::QSLOT);
-      bulk_g2s(sbase + S::OFF_STG + (i % VF_STAGES) * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT,
-               S::QSLOT, bar);
-      s_pend[i % VF_STAGES] = i;
-    };
-    if (bt == 0)
+  if (warp == 8) {
+    // ============================== tensor-core issuer (lane 0): S of chunk c, then P V of c - 1
+    if (lane == 0) {
       for (int i = 0; i < VF_STAGES && i < nqc; ++i) issue_copy(i);
+      int s_done = 0, pv_done = 0;   // launches issued
+      // descriptors of the operands' first K step; the next K step starts 256 bytes further,
+      // + 16 in the start-address field (16-byte units; shared addresses stay below 2^18 bytes)
+      const unsigned long long dQ = vf_desc(sbase, D * 16);
+      // buffer 1 lies a fixed distance after buffer 0: + SBK, SBV, SAP bytes
+      const unsigned long long dK0 = vf_desc(sbase + S::OFF_BK, D * 16), dV0 = vf_desc(sbase + S::OFF_BV, W * 16),
+                               dP0 = vf_desc(sbase + S::OFF_AP, S::KP * 16);
+      for (int c = 0; c <= nchunk; ++c) {
+        if (c < nchunk) {
+          const int b = c & 1;
+          bool ok = vf_wait(smem_u32(&bar_keys[b]), (c >> 1) & 1, st.err, abort_flag);
+          if (ok && c >= 2) ok = vf_wait(smem_u32(&bar_sfree[b]), ((c - 2) >> 1) & 1, st.err, abort_flag);
+          if (!ok) break;
+          vf_fence_after();
+          const unsigned tS = tbase + b * S::SCOLS;
+          const unsigned idesc = c >= nbc ? vf_idesc(VF_ROWS, 3 * W) : vf_idesc(VF_ROWS, W);
+          const unsigned long long dK = dK0 + (unsigned)(b * (S::SBK >> 4));
+#pragma unroll
+          for (int ks = 0; ks < KS; ++ks) vf_mma(tS, dQ + 16 * ks, dK + 16 * ks, idesc, ks > 0);
+          vf_commit(smem_u32(&bar_s[b]));
+          ++s_done;
+        }
+        if (c >= 1) {
+          const int cc = c - 1, b = cc & 1;
+          if (!vf_wait(smem_u32(&bar_p[b]), (cc >> 1) & 1, st.err, abort_flag)) break;
+          vf_fence_after();
+          constexpr unsigned idesc = vf_idesc(D, VF_ROWS);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)
+#pragma unroll
+            for (int kt = 0; kt < KT; ++kt)
+              vf_mma(tO, dV0 + (unsigned)(b * (S::SBV >> 4)) + 16 * kt, dP0 + (unsigned)(b * (S::SAP >> 4)) + 16 * (part * KT + kt),
+                     idesc, cc > 0 || part > 0 || kt > 0);
+          vf_commit(smem_u32(&bar_o[b]));
+          ++pv_done;
+        }
+      }
+      // the tensor-core work issued must finish before tensor memory is read or freed
+      if (s_done > 0) vf_drain(smem_u32(&bar_s[(s_done - 1) & 1]), ((s_done - 1) >> 1) & 1, st.err);
+      if (pv_done > 0) vf_drain(smem_u32(&bar_o[(pv_done - 1) & 1]), ((pv_done - 1) >> 1) & 1, st.err);
+    }
+    __syncwarp();
+  } else if (warp >= 4) {
+    // ============================== operand builders (warps 4-7), each on its own share of a chunk
+    const int bw = warp - 4, tt = lane & 3;
+    int eidx_n;
+    int2 ent_n = chunk_entry(0, eidx_n);   // the next chunk's entry, loaded a chunk ahead
+    // a bf16 slot's fragments (512 bytes each: one lane's 16 bytes, rows g, g + 8 at columns 2t,
+    // 2t + 8; keys have tokens as rows, values channels), this warp's share, loaded ahead: the
+    // keys of chunk c + 1 while chunk c's values are built, its values after those
+    uint4 xk[FK], xv[FK];
+    auto load_bf16 = [&](int2 e, bool values, uint4 (&x)[FK]) {
+      if (e.y < 0 || e.y >= st.capb) return;
+      const uint8_t* slot = st.bslab + (gu * st.capb + e.y) * (long long)S::BSLOT + (values ? 32 * D : 0);
+#pragma unroll
+      for (int k = 0; k < FK; ++k) {
+        const int ff = bw + 4 * k;
+        if (ff < NFK) x[k] = __ldg(reinterpret_cast<const uint4*>(slot + (ff / KS) * (64 * D) + (ff % KS) * 512) + lane);
+      }
+    };
+    if (nbc > 0) {
+      load_bf16(ent_n, false, xk);
+      load_bf16(ent_n, true, xv);
+    }
     for (int c = 0; c < nchunk; ++c) {
       const int b = c & 1;
-      int eidx;
-      const int2 ent = chunk_entry(c, eidx);
+      const int2 ent = ent_n;
       const bool is_q = c >= nbc;
       const int qi = c - nbc;
-      bool ok = ent.y >= 0 && ent.y < (is_q ? st.capq : st.capb);
-      if (!ok && bt == 0) {
-        atomicOr(st.err, ERR_TABLE);
-        *abort_flag = 1;
+      ent_n = chunk_entry(c + 1, eidx_n);
+      const bool slot_ok = ent.y >= 0 && ent.y < (is_q ? st.capq : st.capb);
+      if (!slot_ok) {
+        if (lane == 0) {
+          atomicOr(st.err, ERR_TABLE);
+          *abort_flag = 1;
+        }
+        break;
       }
-      // keys of buffer b: their last reader, S of chunk c - 2, must be complete
-      if (ok && c >= 2) ok = vf_wait(smem_u32(&bar_s[b]), ((c - 2) >> 1) & 1, st.err, abort_flag);
-      if (ok && is_q) ok = vf_wait(smem_u32(&bar_stage[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag);
-      if (!vf_group_and(1, ok && !*abort_flag)) break;
-      if (bt == 0 && is_q) s_pend[qi % VF_STAGES] = -1;
+      // keys of buffer b: their last reader, S of chunk c - 2, must be complete (every wait's
+      // outcome is made uniform across the warp: its stores are collective)
+      if (c >= 2 && !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_s[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)))
+        break;
+      if (is_q &&
+          !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_stage[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag)))
+        break;
       const unsigned sBK = sbase + S::OFF_BK + b * S::SBK, sBV = sbase + S::OFF_BV + b * S::SBV;
       const uint8_t* sp = smem + S::OFF_STG + (qi % VF_STAGES) * S::STAGE;   // 2-bit chunk's stage
-      constexpr int WPL = (W / 16) * (D / 16) / 2, CW = WPL < 4 ? WPL : 4;
       auto word_at = [&](int byte0, int wj) -> unsigned {   // this lane's word wj of a code block
         return *reinterpret_cast<const unsigned*>(sp + byte0 + ((wj / CW) * 32 + lane) * (CW * 4) + (wj % CW) * 4);
       };
-      // bf16 slot, straight from global memory: each 512-byte fragment is one lane's 16 bytes
-      // (rows g, g + 8 at columns 2t, 2t + 8); keys have tokens as rows, values channels
-      constexpr int NF = 2 * KT * KS, FPW = (NF + 3) / 4;
-      uint4 x[FPW];
-      if (!is_q) {
-        const uint8_t* slot = st.bslab + (gu * st.capb + ent.y) * (long long)S::BSLOT;
-#pragma unroll
-        for (int k = 0; k < FPW; ++k) {
-          const int fi = bw + 4 * k;
-          if (fi < NF) {
-            const bool value = fi >= KT * KS;
-            const int ff = value ? fi - KT * KS : fi, sub = ff / KS, blk = ff % KS;
-            x[k] = __ldg(reinterpret_cast<const uint4*>(slot + sub * (64 * D) + (value ? 32 * D : 0) + blk * 512) + lane);
-          }
-        }
-      }
-      auto store_bf16 = [&](bool values) {   // matrix k: rows + 8 (k & 1) + row, columns + 8 (k >> 1)
+      auto store_bf16 = [&](bool values, const uint4 (&x)[FK]) {   // matrix k: rows + 8 (k & 1) + row, columns + 8 (k >> 1)
         const int m = lane >> 3;
 #pragma unroll
-        for (int k = 0; k < FPW; ++k) {
-          const int fi = bw + 4 * k;
-          if (fi < NF && (fi >= KT * KS) == values) {
-            const int ff = values ? fi - KT * KS : fi, sub = ff / KS, blk = ff % KS;
+        for (int k = 0; k < FK; ++k) {
+          const int ff = bw + 4 * k;
+          if (ff < NFK) {
+            const int sub = ff / KS, blk = ff % KS;
             const unsigned dst = values
                                      ? sBV + vf_canon(16 * blk + 8 * (m & 1) + (lane & 7), 16 * sub + 8 * (m >> 1), W)
                                      : sBK + vf_canon(16 * sub + 8 * (m & 1) + (lane & 7), 16 * blk + 8 * (m >> 1), D);
@@ -407,33 +471,51 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
       };
       // ---- keys
       if (!is_q) {
-        store_bf16(false);
+        store_bf16(false, xk);
+        if (c + 1 < nbc) load_bf16(ent_n, false, xk);
       } else if (bw < WPL) {
         // word wj holds fragments 2 wj, 2 wj + 1 (token tile mt, channel steps ks, ks + 1); a
-        // warp's words share ks, so its lanes' channel parameters load once
+        // warp's words share ks, so the warp needs the 32 channels 16 ks .. 16 ks + 31 only:
+        // its own table of them, per channel and code the three bf16 parts of code * s + z (one
+        // float32 fma, as the oracle dequantizes; truncated, truncated remainder, rest)
         const int ks = (2 * bw) % KS;
-        const float* kmin = reinterpret_cast<const float*>(sp + g.off_kmin());
-        const float* kscale = reinterpret_cast<const float*>(sp + g.off_kscale());
-        // lane's channels of channel step ks + f: 16 (ks + f) + 2 tt + {0, 1, 8, 9}, one vector
-        const float4 sc0 = *reinterpret_cast<const float4*>(kscale + 16 * ks + 4 * tt);
-        const float4 sc1 = *reinterpret_cast<const float4*>(kscale + 16 * (ks + 1) + 4 * tt);
-        const float4 mn0 = *reinterpret_cast<const float4*>(kmin + 16 * ks + 4 * tt);
-        const float4 mn1 = *reinterpret_cast<const float4*>(kmin + 16 * (ks + 1) + 4 * tt);
+        uint8_t* tab = smem + S::OFF_TAB + bw * 1024;   // [32 channels][4 codes] x 8 bytes
+        {
+          const float* kmin = reinterpret_cast<const float*>(sp + g.off_kmin());
+          const float* kscale = reinterpret_cast<const float*>(sp + g.off_kscale());
+          const int ch = 16 * ks + lane;
+          const float sc = kscale[kparam_pos(ch)], mn = kmin[kparam_pos(ch)];
+          uint2 e4[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k) {
+            const float val = fmaf((float)k, sc, mn);
+            const unsigned hb = __float_as_uint(val) & 0xFFFF0000u;
+            const float r = val - __uint_as_float(hb);
+            const unsigned mb = __float_as_uint(r) & 0xFFFF0000u;
+            e4[k] = make_uint2(__byte_perm(hb, mb, 0x7632), pack_bf16x2_rz(r - __uint_as_float(mb), 0.f));
+          }
+          uint4* tdst = reinterpret_cast<uint4*>(tab + lane * 32);
+          tdst[0] = make_uint4(e4[0].x, e4[0].y, e4[1].x, e4[1].y);
+          tdst[1] = make_uint4(e4[2].x, e4[2].y, e4[3].x, e4[3].y);
+        }
+        __syncwarp();
+        const uint8_t* tlane = tab + 2 * tt * 32;   // channel 16 ks + 2 tt, code 0; + 32 per channel, + 8 per code
         for (int wj = bw; wj < WPL; wj += 4) {
           const unsigned w = word_at(0, wj);
           const int mt = (2 * wj) / KS;
 #pragma unroll
           for (int f = 0; f < 2; ++f) {
-            const float4 sc = f ? sc1 : sc0, mn = f ? mn1 : mn0;
             unsigned hp[4], mp[4], lp[4];
 #pragma unroll
             for (int reg = 0; reg < 4; ++reg) {
               // reg: token 16 mt + gg + 8 (reg & 1), channels 16 (ks + f) + 2 tt + 8 (reg >> 1) + {0, 1}
-              const unsigned xw = w >> (8 * f + 2 * reg);
-              const float s0 = (reg >> 1) ? sc.z : sc.x, s1 = (reg >> 1) ? sc.w : sc.y;
-              const float z0 = (reg >> 1) ? mn.z : mn.x, z1 = (reg >> 1) ? mn.w : mn.y;
-              vf_split3_pair(fmaf(vf_code_f(xw & 3u), s0, z0), fmaf(vf_code_f((xw >> 16) & 3u), s1, z1), hp[reg],
-                             mp[reg], lp[reg]);
+              const int sh = 8 * f + 2 * reg;
+              const uint8_t* te = tlane + (16 * f + 8 * (reg >> 1)) * 32;
+              const uint2 e0 = *reinterpret_cast<const uint2*>(te + (((w >> sh) & 3u) << 3));
+              const uint2 e1 = *reinterpret_cast<const uint2*>(te + 32 + (((w >> (sh + 16)) & 3u) << 3));
+              hp[reg] = __byte_perm(e0.x, e1.x, 0x5410);
+              mp[reg] = __byte_perm(e0.x, e1.x, 0x7632);
+              lp[reg] = __byte_perm(e0.y, e1.y, 0x5410);
             }
             const int m = lane >> 3;
             const unsigned dst = sBK + vf_canon(16 * mt + 8 * (m & 1) + (lane & 7), 16 * (ks + f) + 8 * (m >> 1), D);
@@ -444,37 +526,15 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
         }
       }
       vf_proxy_fence();
-      vf_group_sync(1);   // every builder's keys are in place
-      if (bt == 0) {
-        // ---- S = Q K^T once the softmax of chunk c - 2 has read S out of tensor-memory buffer b
-        // (an expired wait raises the abort flag: this chunk's S is not issued and both warp
-        // groups leave at their next wait)
-        if (c < 2 || vf_wait(smem_u32(&bar_sfree[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)) {
-          vf_fence_after();
-          const unsigned tS = tbase + b * S::SCOLS;
-          const unsigned sQ = sbase;
-          if (is_q) {
-            constexpr unsigned idesc = vf_idesc(VF_ROWS, 3 * W);
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-              vf_mma(tS, vf_desc(sQ + ks * 256, D * 16), vf_desc(sBK + ks * 256, D * 16), idesc, ks > 0);
-          } else {
-            constexpr unsigned idesc = vf_idesc(VF_ROWS, W);
-#pragma unroll
-            for (int ks = 0; ks < KS; ++ks)
-              vf_mma(tS, vf_desc(sQ + ks * 256, D * 16), vf_desc(sBK + ks * 256, D * 16), idesc, ks > 0);
-          }
-          vf_commit(smem_u32(&bar_s[b]));
-          ++s_issued;
-        }
-      }
+      vf_arrive(smem_u32(&bar_keys[b]));
       // values of buffer b: their last reader, P V of chunk c - 2, must be complete (so are its
-      // softmax, the last reader of the value parameters).  An expired wait raises the abort
-      // flag; the group still meets at the barrier below and leaves at the next chunk.
-      if (c >= 2) vf_wait(smem_u32(&bar_o[b]), ((c - 2) >> 1) & 1, st.err, abort_flag);
+      // softmax, the last reader of the value parameters)
+      if (c >= 2 && !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_o[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)))
+        break;
       // ---- values
       if (!is_q) {
-        store_bf16(true);
+        store_bf16(true, xv);
+        if (c + 1 < nbc) load_bf16(ent_n, true, xv);
       } else {
         // word wj holds fragments 2 wj, 2 wj + 1 (channel tile mc, token steps kt, kt + 1; with
         // one token step the second fragment is the next channel tile), as 1 + code / 4
@@ -496,26 +556,31 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
                          r[2], r[3]);
           }
         }
-        if (bt < W) {
-          const float vsc = reinterpret_cast<const float*>(sp + g.off_vscale())[vparam_pos(g, bt)];
-          const float vmn = reinterpret_cast<const float*>(sp + g.off_vmin())[vparam_pos(g, bt)];
-          s_vs[b][bt] = 4.f * vsc;
-          s_vz[b][bt] = vmn - 4.f * vsc;
-        }
+        if (bw == 0)
+          for (int t = lane; t < W; t += 32) {
+            const float vsc = reinterpret_cast<const float*>(sp + g.off_vscale())[vparam_pos(g, t)];
+            const float vmn = reinterpret_cast<const float*>(sp + g.off_vmin())[vparam_pos(g, t)];
+            s_vs[b][t] = 4.f * vsc;
+            s_vz[b][t] = vmn - 4.f * vsc;
+          }
       }
       vf_proxy_fence();
       vf_arrive(smem_u32(&bar_built[b]));
-      vf_group_sync(1);   // every builder has read the stage
-      if (bt == 0 && is_q && qi + VF_STAGES < nqc) issue_copy(qi + VF_STAGES);
-    }
-    // exit: S work issued must finish before tensor memory is freed, copies before the CTA leaves
-    if (bt == 0) {
-      if (s_issued > 0) vf_drain(smem_u32(&bar_s[(s_issued - 1) & 1]), ((s_issued - 1) >> 1) & 1, st.err);
-      for (int i = 0; i < VF_STAGES; ++i)
-        if (s_pend[i] >= 0) vf_drain(smem_u32(&bar_stage[i]), (s_pend[i] / VF_STAGES) & 1, st.err);
+      if (is_q) {
+        // the last builder warp done with the stage refills it
+        __syncwarp();
+        if (lane == 0) {
+          const int sidx = qi % VF_STAGES;
+          __threadfence_block();
+          if (atomicAdd(&s_stage_rel[sidx], 1) == 3) {
+            s_stage_rel[sidx] = 0;
+            if (qi + VF_STAGES < nqc) issue_copy(qi + VF_STAGES);
+          }
+        }
+      }
     }
   } else {
-    // ============================== softmax (warps 0-3) and the P V issuer (thread 0)
+    // ============================== softmax (warps 0-3)
     const int q4 = lane & 3;
     const int ra = 16 * warp + (lane >> 2), rb = ra + 8;   // this lane's rows
     const bool va = ra < p.R, vb = rb < p.R;
@@ -524,10 +589,13 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
     float mref_a = -INFINITY, mref_b = -INFINITY, lsum_a = 0.f, lsum_b = 0.f, zs_a = 0.f, zs_b = 0.f;
     int c = 0;
     bool ok = true;
+    int eidx_n;
+    int2 ent_n = chunk_entry(0, eidx_n);   // the next chunk's entry, loaded a chunk ahead
     for (; c < nchunk; ++c) {
       const int b = c & 1;
-      int eidx;
-      const int2 ent = chunk_entry(c, eidx);
+      const int2 ent = ent_n;
+      const int eidx = eidx_n;
+      ent_n = chunk_entry(c + 1, eidx_n);
       const bool is_q = c >= nbc;
       const int win = ent.x;
       // S of this chunk (the wait's outcome is made uniform per warp: the loads are collective;
@@ -675,6 +743,10 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
           vf_stmatrix4(dst + (W / 8) * 128, pl[2 * j], pl[2 * j + 1], pl[2 * j + 2], pl[2 * j + 3]);
         }
       }
+      // P (and any rescale of O^T) ready for the tensor-core issuer
+      vf_proxy_fence();
+      vf_fence_before();
+      vf_arrive(smem_u32(&bar_p[b]));
       mass_a += __shfl_xor_sync(0xffffffffu, mass_a, 1);
       mass_b += __shfl_xor_sync(0xffffffffu, mass_b, 1);
       mass_a += __shfl_xor_sync(0xffffffffu, mass_a, 2);
@@ -686,27 +758,10 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
         if (va) lrow[ra] = mass_a > 0.f ? mua + lg2(mass_a) : -INFINITY;
         if (vb) lrow[rb] = mass_b > 0.f ? mub + lg2(mass_b) : -INFINITY;
       }
-      vf_proxy_fence();
-      vf_fence_before();
-      vf_group_sync(2);
-      if (tid == 0) {
-        // ---- O^T += V^T P^T: both parts of P along K against the same value block
-        vf_fence_after();
-        constexpr unsigned idesc = vf_idesc(D, VF_ROWS);
-        const unsigned sBV = sbase + S::OFF_BV + b * S::SBV, sAP = sbase + S::OFF_AP + b * S::SAP;
-#pragma unroll
-        for (int part = 0; part < 2; ++part)
-#pragma unroll
-          for (int kt = 0; kt < KT; ++kt)
-            vf_mma(tO, vf_desc(sBV + kt * 256, W * 16), vf_desc(sAP + (part * KT + kt) * 256, S::KP * 16), idesc,
-                   c > 0 || part > 0 || kt > 0);
-        vf_commit(smem_u32(&bar_o[b]));
-      }
     }
-    // c = P V launches issued (all of them on a normal exit)
+    // c = chunks whose P went to the issuer (all of them on a normal exit)
     if (ok && c > 0) ok = vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag);
     ok = vf_group_and(2, ok);
-    if (!ok && tid == 0 && c > 0) vf_drain(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err);
     vf_fence_after();
     if (ok) {
       zs_a += __shfl_xor_sync(0xffffffffu, zs_a, 1);   // per-lane shares of the row's offset sum
@@ -741,6 +796,10 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
   }
   vf_fence_before();
   __syncthreads();
+  // copies still in flight (after an expired wait) land before the CTA leaves
+  if (tid == 0)
+    for (int i = 0; i < VF_STAGES; ++i)
+      if (s_stage_cnt[i] > 0) vf_drain(smem_u32(&bar_stage[i]), (s_stage_cnt[i] - 1) & 1, st.err);
   if (warp == 0) {
     vf_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(s_tmem), "r"(S::TMEM_COLS) : "memory");
@@ -748,10 +807,10 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
 }
 
 // ------------------------------------------------------------------------------ combine
-// One CTA per unit: merge each row's splits into draft j's output for head h, and turn every
-// window's per-row log2-sum-exp into draft j's window mass (summed over its G heads), written
-// to delta[j][unit][window] for qe_verify_commit.
-constexpr int VF_COMBINE_THREADS = 256;
+// One CTA per (unit, draft j): merge the splits of draft j's G rows into its outputs, and turn
+// every window's per-row log2-sum-exp into draft j's window mass (summed over its G heads),
+// written to delta[j][unit][window] for qe_verify_commit.
+constexpr int VF_COMBINE_THREADS = 128;
 constexpr int VF_MAX_SPLITS = 16;
 
 template <int D>
@@ -759,16 +818,16 @@ __global__ void __launch_bounds__(VF_COMBINE_THREADS) qe_verify_combine_kernel(c
                                                                               int out_fp32, float* delta,
                                                                               long long qstride) {
   const State& st = p.st;
-  const int u = blockIdx.x, tid = threadIdx.x;
-  const int G = st.G;
+  const int u = blockIdx.x, j = blockIdx.y, tid = threadIdx.x;
+  const int G = st.G, r0 = j * G;
   const long long gu = (long long)p.layer * st.units + u;
   __shared__ float s_sc[VF_ROWS][VF_MAX_SPLITS];
   __shared__ float s_inv[VF_ROWS], s_lse[VF_ROWS];
   const Geo g{D, st.geo.W};
   const LayerView lv = layer_view(g, st.ldev[p.layer]);
-  // row statistics
-  if (tid < p.R) {
-    const float2* ml = p.part_ml + (size_t)u * p.splits * VF_ROWS + tid;
+  // row statistics of the draft's G rows
+  if (tid < G) {
+    const float2* ml = p.part_ml + (size_t)u * p.splits * VF_ROWS + r0 + tid;
     float M = -INFINITY;
     for (int s = 0; s < p.splits; ++s) M = fmaxf(M, ml[(size_t)s * VF_ROWS].x);
     const float Mu = M == -INFINITY ? 0.f : M;
@@ -783,29 +842,38 @@ __global__ void __launch_bounds__(VF_COMBINE_THREADS) qe_verify_combine_kernel(c
     s_lse[tid] = Mu + lg2(Ls);
   }
   __syncthreads();
-  // outputs: draft j, head h, channel c
+  // outputs: head h, channels c .. c + 3
   const int b = u / st.Hkv, kvh = u - b * st.Hkv;
-  for (int i = tid; i < p.R * D; i += VF_COMBINE_THREADS) {
-    const int rr = i / D, c = i - rr * D;
-    float acc = 0.f;
-    for (int s = 0; s < p.splits; ++s)
-      if (s_sc[rr][s] != 0.f) acc = fmaf(p.part_o[(((size_t)u * p.splits + s) * VF_ROWS + rr) * D + c], s_sc[rr][s], acc);
-    const float o = acc * s_inv[rr];
-    const int jj = rr / G, hh = rr - jj * G;
-    const size_t oi = (((size_t)jj * st.units / st.Hkv + b) * st.Hq + kvh * G + hh) * D + c;
-    if (out_fp32) reinterpret_cast<float*>(out)[oi] = o;
-    else reinterpret_cast<__nv_bfloat16*>(out)[oi] = __float2bfloat16_rn(o);
+  for (int i = tid; i < G * (D / 4); i += VF_COMBINE_THREADS) {
+    const int hh = i / (D / 4), c = 4 * (i - hh * (D / 4));
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    for (int s = 0; s < p.splits; ++s) {   // a split without mass for the row wrote zeros
+      const float sc = s_sc[hh][s];
+      const float4 v = *reinterpret_cast<const float4*>(p.part_o + (((size_t)u * p.splits + s) * VF_ROWS + r0 + hh) * D + c);
+      acc.x = fmaf(v.x, sc, acc.x);
+      acc.y = fmaf(v.y, sc, acc.y);
+      acc.z = fmaf(v.z, sc, acc.z);
+      acc.w = fmaf(v.w, sc, acc.w);
+    }
+    const float inv = s_inv[hh];
+    const size_t oi = (((size_t)j * st.units / st.Hkv + b) * st.Hq + kvh * G + hh) * D + c;
+    if (out_fp32) {
+      *reinterpret_cast<float4*>(reinterpret_cast<float*>(out) + oi) =
+          make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv);
+    } else {
+      *reinterpret_cast<uint2*>(reinterpret_cast<__nv_bfloat16*>(out) + oi) =
+          make_uint2(pack_bf16x2(acc.x * inv, acc.y * inv), pack_bf16x2(acc.z * inv, acc.w * inv));
+    }
   }
-  // window masses per draft
+  // window masses of draft j
   const int nent = lv.nbw + lv.nq;
-  for (int i = tid; i < nent * p.n_q; i += VF_COMBINE_THREADS) {
-    const int e = i / p.n_q, jj = i - e * p.n_q;
+  for (int e = tid; e < nent; e += VF_COMBINE_THREADS) {
     const int2 ent = e < lv.nbw ? st.blist[gu * st.capb + e] : st.qlist[gu * st.capq + (e - lv.nbw)];
     if (ent.x < 0 || ent.x >= st.maxw) continue;   // the sink is not scored
-    const float* ls = p.lse + ((long long)u * p.ent_cap + e) * VF_ROWS + jj * G;
+    const float* ls = p.lse + ((long long)u * p.ent_cap + e) * VF_ROWS + r0;
     float dS = 0.f;
-    for (int hh = 0; hh < G; ++hh) dS += ex2(ls[hh] - s_lse[jj * G + hh]);
-    delta[jj * qstride + (long long)u * st.maxw + ent.x] = dS;
+    for (int hh = 0; hh < G; ++hh) dS += ex2(ls[hh] - s_lse[hh]);
+    delta[j * qstride + (long long)u * st.maxw + ent.x] = dS;
   }
 }
 
@@ -817,7 +885,7 @@ static cudaError_t vf_launch_t(const VerifyParams& p, void* out, int out_fp32, f
   qe_verify_attn_kernel<D, W><<<dim3(p.st.units, p.splits), VF_THREADS, S::SMEM_REQ, s>>>(p);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
-  qe_verify_combine_kernel<D><<<p.st.units, VF_COMBINE_THREADS, 0, s>>>(p, out, out_fp32, delta, qstride);
+  qe_verify_combine_kernel<D><<<dim3(p.st.units, p.n_q), VF_COMBINE_THREADS, 0, s>>>(p, out, out_fp32, delta, qstride);
   return cudaGetLastError();
 }
 
