@@ -69,13 +69,13 @@ struct VfShape {
   static constexpr int OFF_STG = OFF_AP + 2 * SAP;
   static constexpr int OFF_TAB = OFF_STG + VF_STAGES * STAGE;   // key tables: 4 x [32 channels][4 codes] x 8 B
   static constexpr int SMEM = OFF_TAB + 4 * 1024;
-  static constexpr int SCOLS = (NKQ + 31) / 32 * 32;      // tensor-memory columns of one S buffer
-  static constexpr int TO_OFF = 2 * SCOLS;                // column of O^T (64 columns)
-  static constexpr int TMEM_COLS = TO_OFF + VF_ROWS <= 256 ? 256 : 512;
-  static constexpr int CTAS_PER_SM = TMEM_COLS == 256 ? 2 : 1;
+  static constexpr int TO_OFF = (NKQ + 63) / 64 * 64;     // tensor memory: S at column 0, O (D columns) here
+  static constexpr int TMEM_COLS = TO_OFF + D <= 256 ? 256 : 512;
+  static constexpr bool FITS2 = 2 * (SMEM + 4096) <= 228 * 1024;   // two CTAs' shared memory per SM
+  static constexpr int CTAS_PER_SM = TMEM_COLS == 256 && FITS2 ? 2 : 1;
   // Dynamic shared memory requested per CTA: at least enough that no more CTAs share an SM than
-  // its 512 tensor-memory columns hold.
-  static constexpr int SMEM_FLOOR = TMEM_COLS == 256 ? 80 * 1024 : 120 * 1024;
+  // its 512 tensor-memory columns hold (two of 256 columns, or one of 512).
+  static constexpr int SMEM_FLOOR = CTAS_PER_SM == 2 ? 80 * 1024 : 120 * 1024;
   static constexpr int SMEM_REQ = SMEM > SMEM_FLOOR ? SMEM : SMEM_FLOOR;
   static_assert(SMEM_REQ + 4096 <= 227 * 1024, "verify tile exceeds shared memory");
   static_assert(CTAS_PER_SM == 1 || 2 * (SMEM_REQ + 4096) <= 228 * 1024, "two CTAs must fit an SM");
@@ -212,21 +212,40 @@ __device__ __forceinline__ void vf_ld_rows<8>(unsigned taddr, unsigned (&v)[32])
       : "r"(taddr)
       : "memory");
 }
+// 4 8-column blocks (32 columns) of 16 lanes, the 16x256b layout of vf_ld_rows<4>
+__device__ __forceinline__ void vf_st_rows4(unsigned taddr, const unsigned (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.16x256b.x4.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(
+          taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]), "r"(v[9]),
+      "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15])
+      : "memory");
+}
+
+// One test of an mbarrier phase that may suspend the thread until the phase completes, for at
+// most about 20 us: a waiting warp takes no issue slots from the working ones.
+__device__ __forceinline__ bool vf_try_wait(unsigned bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return done != 0;
+}
 // Bounded wait on an mbarrier phase.  False when it expires (the timeout bit and the abort flag
 // are set) or when another thread has raised the abort flag meanwhile.
 __device__ __forceinline__ bool vf_wait(unsigned bar, unsigned parity, unsigned* err, volatile int* abort_flag) {
-  if (mbar_try_wait(bar, parity)) return true;
+  if (vf_try_wait(bar, parity)) return true;
   const unsigned long long t0 = globaltimer_ns();
-  int spins = 0;
-  while (!mbar_try_wait(bar, parity)) {
+  while (!vf_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (++spins == 16) {
-      spins = 0;
-      if (globaltimer_ns() - t0 > VF_WAIT_NS) {
-        atomicOr(err, ERR_TIMEOUT);
-        *abort_flag = 1;
-        return false;
-      }
+    if (globaltimer_ns() - t0 > VF_WAIT_NS) {
+      atomicOr(err, ERR_TIMEOUT);
+      *abort_flag = 1;
+      return false;
     }
   }
   return true;
@@ -267,14 +286,12 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
   constexpr int WPL = (W / 16) * (D / 16) / 2, CW = WPL < 4 ? WPL : 4;   // code words per lane
   constexpr int NFK = KT * KS, FK = (NFK + 3) / 4;                       // bf16 key (value) fragments, per warp
   extern __shared__ __align__(1024) uint8_t smem[];
-  __shared__ __align__(8) unsigned long long bar_stage[VF_STAGES], bar_s[2], bar_sfree[2], bar_keys[2], bar_built[2],
-      bar_p[2], bar_o[2];
+  __shared__ __align__(8) unsigned long long bar_stage[VF_STAGES], bar_stfree[VF_STAGES], bar_s, bar_sfree, bar_sk[2],
+      bar_keys[2], bar_built[2], bar_p[2], bar_o[2];
   __shared__ unsigned s_tmem;
   __shared__ __align__(16) float s_vs[2][W];   // 2-bit window: 4 s_V per token
   __shared__ __align__(16) float s_vz[2][W];   // and z_V - 4 s_V
-  __shared__ float s_alpha[VF_ROWS], s_zs[VF_ROWS];
   __shared__ int s_abort;
-  __shared__ int s_stage_rel[VF_STAGES];   // builder warps done with a stage's current slot
   __shared__ int s_stage_cnt[VF_STAGES];   // copies issued into a stage
 
   const State& st = p.st;
@@ -298,17 +315,20 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
   if (tid == 0) {
+    // commit barriers take one arrival; the others one per warp of the producing group, after
+    // the warp's own __syncwarp
     for (int i = 0; i < VF_STAGES; ++i) {
       mbar_init(smem_u32(&bar_stage[i]), 1);
-      s_stage_rel[i] = 0;
+      mbar_init(smem_u32(&bar_stfree[i]), 4);
       s_stage_cnt[i] = 0;
     }
+    mbar_init(smem_u32(&bar_s), 1);
+    mbar_init(smem_u32(&bar_sfree), 4);
     for (int i = 0; i < 2; ++i) {
-      mbar_init(smem_u32(&bar_s[i]), 1);
-      mbar_init(smem_u32(&bar_sfree[i]), 128);
-      mbar_init(smem_u32(&bar_keys[i]), 128);
-      mbar_init(smem_u32(&bar_built[i]), 128);
-      mbar_init(smem_u32(&bar_p[i]), 128);
+      mbar_init(smem_u32(&bar_sk[i]), 1);
+      mbar_init(smem_u32(&bar_keys[i]), 4);
+      mbar_init(smem_u32(&bar_built[i]), 4);
+      mbar_init(smem_u32(&bar_p[i]), 4);
       mbar_init(smem_u32(&bar_o[i]), 1);
     }
     mbar_fence_init();
@@ -331,8 +351,8 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
   vf_fence_before();
   __syncthreads();
   vf_fence_after();
-  const unsigned tbase = s_tmem;
-  const unsigned tO = tbase + S::TO_OFF;
+  const unsigned tS = s_tmem;                 // S: M = 64 rows, up to 3W columns
+  const unsigned tO = s_tmem + S::TO_OFF;     // O: M = 64 rows, D columns
 
   // chunk c: bf16 entry b0 + c, then 2-bit entry q0 + (c - nbc)
   auto chunk_entry = [&](int c, int& eidx) -> int2 {
@@ -348,62 +368,69 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
     eidx = nbw + qi;
     return st.qlist[gu * st.capq + qi];
   };
-  // thread that issues a copy: 2-bit chunk i of this split into stage i % VF_STAGES
-  auto issue_copy = [&](int i) {
-    int eidx;
-    const int2 e = chunk_entry(nbc + i, eidx);
-    if (e.y < 0 || e.y >= st.capq) return;   // reported by the builders when they reach it
-    const int sidx = i % VF_STAGES;
-    const unsigned bar = smem_u32(&bar_stage[sidx]);
-    atomicAdd(&s_stage_cnt[sidx], 1);
-    mbar_expect_tx(bar, S::QSLOT);
-    bulk_g2s(sbase + S::OFF_STG + sidx * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT, S::QSLOT,
-             bar);
-  };
 
   if (warp == 8) {
-    // ============================== tensor-core issuer (lane 0): S of chunk c, then P V of c - 1
+    // ============================== tensor cores and copies (lane 0): S of chunk c, P V of chunk
+    // c - 1, then the refill of the stage chunk c - 1 read
     if (lane == 0) {
-      for (int i = 0; i < VF_STAGES && i < nqc; ++i) issue_copy(i);
-      int s_done = 0, pv_done = 0;   // launches issued
-      // descriptors of the operands' first K step; the next K step starts 256 bytes further,
-      // + 16 in the start-address field (16-byte units; shared addresses stay below 2^18 bytes)
+      auto issue_copy = [&](int i, int2 e) {   // 2-bit chunk i of this split into stage i % VF_STAGES
+        if (e.y < 0 || e.y >= st.capq) return;   // reported by the builders when they reach it
+        const int sidx = i % VF_STAGES;
+        const unsigned bar = smem_u32(&bar_stage[sidx]);
+        s_stage_cnt[sidx] += 1;
+        mbar_expect_tx(bar, S::QSLOT);
+        bulk_g2s(sbase + S::OFF_STG + sidx * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT,
+                 S::QSLOT, bar);
+      };
+      int ei;
+      for (int i = 0; i < VF_STAGES && i < nqc; ++i) issue_copy(i, chunk_entry(nbc + i, ei));
+      int2 refill = chunk_entry(nbc + VF_STAGES, ei);   // entry of the next refill, loaded ahead
+      // descriptors of the operands' first K step; the next K step starts 256 bytes further, + 16
+      // in the start-address field (16-byte units; shared addresses stay below 2^18 bytes); buffer
+      // 1 lies a fixed distance after buffer 0
       const unsigned long long dQ = vf_desc(sbase, D * 16);
-      // buffer 1 lies a fixed distance after buffer 0: + SBK, SBV, SAP bytes
       const unsigned long long dK0 = vf_desc(sbase + S::OFF_BK, D * 16), dV0 = vf_desc(sbase + S::OFF_BV, W * 16),
                                dP0 = vf_desc(sbase + S::OFF_AP, S::KP * 16);
+      int s_done = 0, pv_done = 0;   // launches issued
       for (int c = 0; c <= nchunk; ++c) {
         if (c < nchunk) {
           const int b = c & 1;
           bool ok = vf_wait(smem_u32(&bar_keys[b]), (c >> 1) & 1, st.err, abort_flag);
-          if (ok && c >= 2) ok = vf_wait(smem_u32(&bar_sfree[b]), ((c - 2) >> 1) & 1, st.err, abort_flag);
+          if (ok && c >= 1) ok = vf_wait(smem_u32(&bar_sfree), (c - 1) & 1, st.err, abort_flag);
           if (!ok) break;
           vf_fence_after();
-          const unsigned tS = tbase + b * S::SCOLS;
           const unsigned idesc = c >= nbc ? vf_idesc(VF_ROWS, 3 * W) : vf_idesc(VF_ROWS, W);
           const unsigned long long dK = dK0 + (unsigned)(b * (S::SBK >> 4));
 #pragma unroll
           for (int ks = 0; ks < KS; ++ks) vf_mma(tS, dQ + 16 * ks, dK + 16 * ks, idesc, ks > 0);
-          vf_commit(smem_u32(&bar_s[b]));
+          vf_commit(smem_u32(&bar_s));       // for the softmax
+          vf_commit(smem_u32(&bar_sk[b]));   // for the builders: key buffer b free again
           ++s_done;
         }
         if (c >= 1) {
           const int cc = c - 1, b = cc & 1;
           if (!vf_wait(smem_u32(&bar_p[b]), (cc >> 1) & 1, st.err, abort_flag)) break;
           vf_fence_after();
-          constexpr unsigned idesc = vf_idesc(D, VF_ROWS);
+          // O += P V: M = 64 rows (A = P, both parts along K), N = D channels (B = values)
+          constexpr unsigned idesc = vf_idesc(VF_ROWS, D);
+          const unsigned long long dV = dV0 + (unsigned)(b * (S::SBV >> 4)), dP = dP0 + (unsigned)(b * (S::SAP >> 4));
 #pragma unroll
           for (int part = 0; part < 2; ++part)
 #pragma unroll
             for (int kt = 0; kt < KT; ++kt)
-              vf_mma(tO, dV0 + (unsigned)(b * (S::SBV >> 4)) + 16 * kt, dP0 + (unsigned)(b * (S::SAP >> 4)) + 16 * (part * KT + kt),
-                     idesc, cc > 0 || part > 0 || kt > 0);
+              vf_mma(tO, dP + 16 * (part * KT + kt), dV + 16 * kt, idesc, cc > 0 || part > 0 || kt > 0);
           vf_commit(smem_u32(&bar_o[b]));
           ++pv_done;
+          const int qi = cc - nbc;
+          if (qi >= 0 && qi + VF_STAGES < nqc) {
+            if (!vf_wait(smem_u32(&bar_stfree[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag)) break;
+            issue_copy(qi + VF_STAGES, refill);
+            refill = chunk_entry(nbc + qi + VF_STAGES + 1, ei);
+          }
         }
       }
       // the tensor-core work issued must finish before tensor memory is read or freed
-      if (s_done > 0) vf_drain(smem_u32(&bar_s[(s_done - 1) & 1]), ((s_done - 1) >> 1) & 1, st.err);
+      if (s_done > 0) vf_drain(smem_u32(&bar_s), (s_done - 1) & 1, st.err);
       if (pv_done > 0) vf_drain(smem_u32(&bar_o[(pv_done - 1) & 1]), ((pv_done - 1) >> 1) & 1, st.err);
     }
     __syncwarp();
@@ -445,7 +472,7 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
       }
       // keys of buffer b: their last reader, S of chunk c - 2, must be complete (every wait's
       // outcome is made uniform across the warp: its stores are collective)
-      if (c >= 2 && !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_s[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)))
+      if (c >= 2 && !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_sk[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)))
         break;
       if (is_q &&
           !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_stage[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag)))
@@ -477,9 +504,11 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
         // word wj holds fragments 2 wj, 2 wj + 1 (token tile mt, channel steps ks, ks + 1); a
         // warp's words share ks, so the warp needs the 32 channels 16 ks .. 16 ks + 31 only:
         // its own table of them, per channel and code the three bf16 parts of code * s + z (one
-        // float32 fma, as the oracle dequantizes; truncated, truncated remainder, rest)
+        // float32 fma, as the oracle dequantizes; truncated, truncated remainder, rest), laid out
+        // [channel parity][16 channel pairs][4 codes] x 8 bytes so that a lookup instruction's
+        // four lane groups (tt) read four disjoint sets of eight banks
         const int ks = (2 * bw) % KS;
-        uint8_t* tab = smem + S::OFF_TAB + bw * 1024;   // [32 channels][4 codes] x 8 bytes
+        uint8_t* tab = smem + S::OFF_TAB + bw * 1024;
         {
           const float* kmin = reinterpret_cast<const float*>(sp + g.off_kmin());
           const float* kscale = reinterpret_cast<const float*>(sp + g.off_kscale());
@@ -494,12 +523,12 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
             const unsigned mb = __float_as_uint(r) & 0xFFFF0000u;
             e4[k] = make_uint2(__byte_perm(hb, mb, 0x7632), pack_bf16x2_rz(r - __uint_as_float(mb), 0.f));
           }
-          uint4* tdst = reinterpret_cast<uint4*>(tab + lane * 32);
+          uint4* tdst = reinterpret_cast<uint4*>(tab + (lane & 1) * 512 + (lane >> 1) * 32);
           tdst[0] = make_uint4(e4[0].x, e4[0].y, e4[1].x, e4[1].y);
           tdst[1] = make_uint4(e4[2].x, e4[2].y, e4[3].x, e4[3].y);
         }
         __syncwarp();
-        const uint8_t* tlane = tab + 2 * tt * 32;   // channel 16 ks + 2 tt, code 0; + 32 per channel, + 8 per code
+        const uint8_t* tlane = tab + tt * 32;   // channel 16 ks + 2 tt, code 0; odd channel + 512, + 8 per code
         for (int wj = bw; wj < WPL; wj += 4) {
           const unsigned w = word_at(0, wj);
           const int mt = (2 * wj) / KS;
@@ -510,9 +539,9 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
             for (int reg = 0; reg < 4; ++reg) {
               // reg: token 16 mt + gg + 8 (reg & 1), channels 16 (ks + f) + 2 tt + 8 (reg >> 1) + {0, 1}
               const int sh = 8 * f + 2 * reg;
-              const uint8_t* te = tlane + (16 * f + 8 * (reg >> 1)) * 32;
+              const uint8_t* te = tlane + (8 * f + 4 * (reg >> 1)) * 32;   // channel pair (16 f + 8 (reg >> 1)) / 2 further
               const uint2 e0 = *reinterpret_cast<const uint2*>(te + (((w >> sh) & 3u) << 3));
-              const uint2 e1 = *reinterpret_cast<const uint2*>(te + 32 + (((w >> (sh + 16)) & 3u) << 3));
+              const uint2 e1 = *reinterpret_cast<const uint2*>(te + 512 + (((w >> (sh + 16)) & 3u) << 3));
               hp[reg] = __byte_perm(e0.x, e1.x, 0x5410);
               mp[reg] = __byte_perm(e0.x, e1.x, 0x7632);
               lp[reg] = __byte_perm(e0.y, e1.y, 0x5410);
@@ -526,9 +555,10 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
         }
       }
       vf_proxy_fence();
-      vf_arrive(smem_u32(&bar_keys[b]));
+      __syncwarp();
+      if (lane == 0) vf_arrive(smem_u32(&bar_keys[b]));
       // values of buffer b: their last reader, P V of chunk c - 2, must be complete (so are its
-      // softmax, the last reader of the value parameters)
+      // softmax, the last reader of the value parameters and of P buffer b)
       if (c >= 2 && !__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_o[b]), ((c - 2) >> 1) & 1, st.err, abort_flag)))
         break;
       // ---- values
@@ -565,22 +595,14 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
           }
       }
       vf_proxy_fence();
-      vf_arrive(smem_u32(&bar_built[b]));
-      if (is_q) {
-        // the last builder warp done with the stage refills it
-        __syncwarp();
-        if (lane == 0) {
-          const int sidx = qi % VF_STAGES;
-          __threadfence_block();
-          if (atomicAdd(&s_stage_rel[sidx], 1) == 3) {
-            s_stage_rel[sidx] = 0;
-            if (qi + VF_STAGES < nqc) issue_copy(qi + VF_STAGES);
-          }
-        }
+      __syncwarp();
+      if (lane == 0) {
+        vf_arrive(smem_u32(&bar_built[b]));
+        if (is_q) vf_arrive(smem_u32(&bar_stfree[qi % VF_STAGES]));   // done with the stage
       }
     }
   } else {
-    // ============================== softmax (warps 0-3)
+    // ============================== softmax (warps 0-3), each warp on its own 16 rows
     const int q4 = lane & 3;
     const int ra = 16 * warp + (lane >> 2), rb = ra + 8;   // this lane's rows
     const bool va = ra < p.R, vb = rb < p.R;
@@ -598,24 +620,25 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
       ent_n = chunk_entry(c + 1, eidx_n);
       const bool is_q = c >= nbc;
       const int win = ent.x;
-      // S of this chunk (the wait's outcome is made uniform per warp: the loads are collective;
-      // the group agrees at the barrier below)
-      ok = __all_sync(0xffffffffu, vf_wait(smem_u32(&bar_s[b]), (c >> 1) & 1, st.err, abort_flag));
+      // S of this chunk (every wait's outcome is made uniform across the warp: the loads are
+      // collective)
+      ok = __all_sync(0xffffffffu, vf_wait(smem_u32(&bar_s), c & 1, st.err, abort_flag));
+      if (!ok) break;
       // ---- logits of this lane's two rows: x[4 j + e] row a, x[4 j + 2 + e] row b, token 8 j + 2 q4 + e
       float x[4 * NB];
-      if (ok) {
+      {
         vf_fence_after();
-        const unsigned tS = tbase + b * S::SCOLS + lane_off;
+        const unsigned tSl = tS + lane_off;
         unsigned v0[4 * NB];
-        vf_ld_rows<NB>(tS, v0);
+        vf_ld_rows<NB>(tSl, v0);
         if (is_q) {
           unsigned v1[4 * NB];
-          vf_ld_rows<NB>(tS + W, v1);
+          vf_ld_rows<NB>(tSl + W, v1);
           vf_wait_ld(v0);
           vf_wait_ld(v1);
 #pragma unroll
           for (int i = 0; i < 4 * NB; ++i) x[i] = __uint_as_float(v0[i]) + __uint_as_float(v1[i]);
-          vf_ld_rows<NB>(tS + 2 * W, v1);
+          vf_ld_rows<NB>(tSl + 2 * W, v1);
           vf_wait_ld(v1);
 #pragma unroll
           for (int i = 0; i < 4 * NB; ++i) x[i] = (x[i] + __uint_as_float(v1[i])) * p.scale_log2;
@@ -625,13 +648,9 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
           for (int i = 0; i < 4 * NB; ++i) x[i] = __uint_as_float(v0[i]) * p.scale_log2;
         }
         vf_fence_before();
-        vf_arrive(smem_u32(&bar_sfree[b]));   // tensor-memory buffer b may take S of chunk c + 2
-      } else {
-#pragma unroll
-        for (int i = 0; i < 4 * NB; ++i) x[i] = -INFINITY;
+        __syncwarp();
+        if (lane == 0) vf_arrive(smem_u32(&bar_sfree));   // tensor memory may take S of chunk c + 1
       }
-      // operands and value parameters of this chunk
-      ok = ok && vf_wait(smem_u32(&bar_built[b]), (c >> 1) & 1, st.err, abort_flag);
       // valid tokens of the window for a row: [tmin, tmax); draft j sees positions < L0 + j + 1
       int lo, hi, pos0;
       if (!is_q && win < 0) {
@@ -668,31 +687,27 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
       const bool raise_a = ma > mref_a + 8.f, raise_b = mb > mref_b + 8.f;   // false for -inf
       const float alpha_a = (raise_a && mref_a != -INFINITY) ? ex2(mref_a - ma) : 1.f;
       const float alpha_b = (raise_b && mref_b != -INFINITY) ? ex2(mref_b - mb) : 1.f;
-      if (q4 == 0) {
-        s_alpha[ra] = alpha_a;
-        s_alpha[rb] = alpha_b;
-      }
-      // one group barrier in the common case: nothing to rescale and no wait expired
-      if (vf_group_or(2, !ok || alpha_a != 1.f || alpha_b != 1.f)) {
-        if (vf_group_or(2, !ok)) {
-          ok = false;
-          break;
-        }
-        // rescale O^T's columns: the previous chunk's P V must be complete; each lane scales its
-        // own tensor-memory lane (one channel) across the 64 row columns
-        ok = vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag);
-        if (!vf_group_and(2, ok)) {
+      if (__any_sync(0xffffffffu, alpha_a != 1.f || alpha_b != 1.f)) {
+        // rescale this warp's rows of O: the previous chunk's P V must be complete
+        if (!__all_sync(0xffffffffu,
+                        vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag))) {
           ok = false;
           break;
         }
         vf_fence_after();
 #pragma unroll
-        for (int c0 = 0; c0 < VF_ROWS; c0 += 16) {
-          float o[16];
-          vf_ld16(tO + lane_off + c0, o);
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          unsigned o[16];
+          vf_ld_rows<4>(tO + lane_off + c0, o);
+          vf_wait_ld(o);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] *= s_alpha[c0 + i];
-          vf_st16(tO + lane_off + c0, o);
+          for (int j = 0; j < 4; ++j) {
+            o[4 * j] = __float_as_uint(__uint_as_float(o[4 * j]) * alpha_a);
+            o[4 * j + 1] = __float_as_uint(__uint_as_float(o[4 * j + 1]) * alpha_a);
+            o[4 * j + 2] = __float_as_uint(__uint_as_float(o[4 * j + 2]) * alpha_b);
+            o[4 * j + 3] = __float_as_uint(__uint_as_float(o[4 * j + 3]) * alpha_b);
+          }
+          vf_st_rows4(tO + lane_off + c0, o);
         }
         asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
       }
@@ -707,9 +722,14 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
         mref_b = mb;
       }
       const float mua = mref_a == -INFINITY ? 0.f : mref_a, mub = mref_b == -INFINITY ? 0.f : mref_b;
+      // operands and value parameters of this chunk; P buffer b is free (its previous reader,
+      // the P V of chunk c - 2, finished before the builders marked this chunk's operands built)
+      if (!__all_sync(0xffffffffu, vf_wait(smem_u32(&bar_built[b]), (c >> 1) & 1, st.err, abort_flag))) {
+        ok = false;
+        break;
+      }
       // ---- P (times 4 s_V for a 2-bit window) in two bf16 parts, into buffer b: rows ra, rb,
-      // K index token t (part 1) and W + t (part 2).  Buffer b's previous reader, the P V of
-      // chunk c - 2, finished before the builders marked this chunk's operands built.
+      // K index token t (part 1) and W + t (part 2)
       float mass_a = 0.f, mass_b = 0.f;
       unsigned ph[4 * NB / 2], pl[4 * NB / 2];   // [2 j + h]: block j, row half h (a, b)
 #pragma unroll
@@ -743,10 +763,11 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
           vf_stmatrix4(dst + (W / 8) * 128, pl[2 * j], pl[2 * j + 1], pl[2 * j + 2], pl[2 * j + 3]);
         }
       }
-      // P (and any rescale of O^T) ready for the tensor-core issuer
+      // P (and the rescale of O) ready for the tensor-core issuer
       vf_proxy_fence();
       vf_fence_before();
-      vf_arrive(smem_u32(&bar_p[b]));
+      __syncwarp();
+      if (lane == 0) vf_arrive(smem_u32(&bar_p[b]));
       mass_a += __shfl_xor_sync(0xffffffffu, mass_a, 1);
       mass_b += __shfl_xor_sync(0xffffffffu, mass_b, 1);
       mass_a += __shfl_xor_sync(0xffffffffu, mass_a, 2);
@@ -760,37 +781,40 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
       }
     }
     // c = chunks whose P went to the issuer (all of them on a normal exit)
-    if (ok && c > 0) ok = vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag);
-    ok = vf_group_and(2, ok);
-    vf_fence_after();
+    if (ok && c > 0)
+      ok = __all_sync(0xffffffffu, vf_wait(smem_u32(&bar_o[(c - 1) & 1]), ((c - 1) >> 1) & 1, st.err, abort_flag));
     if (ok) {
+      vf_fence_after();
       zs_a += __shfl_xor_sync(0xffffffffu, zs_a, 1);   // per-lane shares of the row's offset sum
       zs_b += __shfl_xor_sync(0xffffffffu, zs_b, 1);
       zs_a += __shfl_xor_sync(0xffffffffu, zs_a, 2);
       zs_b += __shfl_xor_sync(0xffffffffu, zs_b, 2);
       const size_t pbase = ((size_t)u * p.splits + split) * VF_ROWS;
       if (q4 == 0) {
-        s_zs[ra] = zs_a;
-        s_zs[rb] = zs_b;
         if (va) p.part_ml[pbase + ra] = make_float2(mref_a, lsum_a);
         if (vb) p.part_ml[pbase + rb] = make_float2(mref_b, lsum_b);
       }
-      vf_group_sync(2);
-      // O^T: this lane's tensor-memory lane is channel d, its columns the rows
-      const int d = D == 128 ? 32 * warp + lane : 16 * warp + lane;
-      const bool dv = D == 128 || lane < 16;
+      // O: this lane's rows ra, rb, columns 8 j + 2 q4, +1 of each 8-column block
 #pragma unroll
-      for (int c0 = 0; c0 < VF_ROWS; c0 += 16) {
-        float o[16];
-        if (c > 0) vf_ld16(tO + lane_off + c0, o);
-        else {
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        unsigned o[16];
+        if (c > 0) {
+          vf_ld_rows<4>(tO + lane_off + c0, o);
+          vf_wait_ld(o);
+        } else {
 #pragma unroll
-          for (int i = 0; i < 16; ++i) o[i] = 0.f;
+          for (int i = 0; i < 16; ++i) o[i] = 0u;
         }
-        if (dv)
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (c0 + i < p.R) p.part_o[(pbase + c0 + i) * D + d] = o[i] + s_zs[c0 + i];
+        for (int j = 0; j < 4; ++j) {
+          const int col = c0 + 8 * j + 2 * q4;
+          if (va)
+            *reinterpret_cast<float2*>(p.part_o + (pbase + ra) * D + col) =
+                make_float2(__uint_as_float(o[4 * j]) + zs_a, __uint_as_float(o[4 * j + 1]) + zs_a);
+          if (vb)
+            *reinterpret_cast<float2*>(p.part_o + (pbase + rb) * D + col) =
+                make_float2(__uint_as_float(o[4 * j + 2]) + zs_b, __uint_as_float(o[4 * j + 3]) + zs_b);
+        }
       }
     }
   }
