@@ -215,9 +215,19 @@ qe_status qe_route(qe_handle h, int layer);
  * older positions, so a rejected draft's score increments must be rolled back; here they are
  * held aside and only the accepted ones are added).
  *
- * qe_verify appends n_q draft tokens one by one and runs draft query j over the cache and
- * drafts 0..j, exactly as n_q decode steps would, except that each query's window masses are
- * kept per query instead of being added to the scores.
+ * qe_verify appends n_q draft tokens and runs draft query j over the cache and drafts 0..j, as
+ * n_q decode steps would, except that each query's window masses are kept per query instead of
+ * being added to the scores.  Two paths compute it (the same results up to float32 summation
+ * order):
+ *  - fused (keys used as stored, n_q * group <= 64, n_q >= 5 by default): the drafts are
+ *    appended in one launch and one attention launch reads every window of the cache once for
+ *    all n_q * group query rows, on the tensor cores (tcgen05.mma, float32 accumulators in
+ *    tensor memory; bf16 operands, a 2-bit window's dequantized keys as three exact bf16 parts,
+ *    the probabilities as two bf16 parts, about 17 significant bits); a combine launch writes
+ *    the outputs and each draft's window masses;
+ *  - draft by draft (keys stored pre-RoPE, more rows, or fewer drafts): one append and one
+ *    decode-step attention per draft.
+ * qe_debug_inject(QE_DEBUG_VERIFY_PATH) overrides the choice.
  *   q:   [n_q][batch][n_q_heads][head_dim] bf16 (draft-major: draft j's queries are contiguous)
  *   k,v: [n_q][batch][n_kv_heads][head_dim] bf16
  *   out: [n_q][batch][n_q_heads][head_dim] float32 (out_fp32) or bf16

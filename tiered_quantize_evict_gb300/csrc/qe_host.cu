@@ -692,11 +692,11 @@ qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const 
   QE_CK(h, cudaMemsetAsync(dl, 0, (size_t)n_q * qstride * sizeof(float), h->stream));
   // All drafts against one read of the cache on the tensor cores, when the rows fit one mma tile
   // and the keys are used as stored (keys stored pre-RoPE verify draft by draft).  The fused
-  // launch's cost hardly depends on the row count, so by default it serves enough rows to beat
-  // one decode step per draft.
+  // launch costs about as much as five decode steps whatever the number of rows (32K context,
+  // head_dim 128), so by default it serves five drafts or more.
   const int rows = n_q * h->st.G;
   const bool fused_ok = !h->rope_blk && rows <= qe::verify_max_rows();
-  const bool fused = fused_ok && (h->verify_path == 1 || (h->verify_path == 0 && rows >= qe::verify_min_rows()));
+  const bool fused = fused_ok && (h->verify_path == 1 || (h->verify_path == 0 && n_q >= qe::verify_min_drafts()));
   if (fused) return verify_fused(h, layer, q, k, v, out, n_q, flags, dl);
   const int D = c.head_dim;
   const size_t kv_tok = (size_t)h->units * D * 2;                       // one draft's K (or V)

@@ -134,7 +134,7 @@ cudaError_t launch_verify_fused(const VerifyParams& p, void* out, int out_fp32, 
                                 cudaStream_t s);
 cudaError_t prepare_verify_kernels(int D, int W);
 int verify_max_rows();
-int verify_min_rows();   // automatic path choice: fused from this many draft x head rows
+int verify_min_drafts();   // automatic path choice: fused from this many drafts
 int verify_max_splits();
 int verify_ctas_per_sm(int D, int W);   // resident verify CTAs per SM (tensor memory, shared memory)
 

@@ -953,7 +953,7 @@ int verify_ctas_per_sm(int D, int W) {
 }
 
 int verify_max_rows() { return VF_ROWS; }
-int verify_min_rows() { return 48; }
+int verify_min_drafts() { return 5; }
 int verify_max_splits() { return VF_MAX_SPLITS; }
 
 }  // namespace qe
