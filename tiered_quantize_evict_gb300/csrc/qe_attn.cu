@@ -623,19 +623,18 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
 
   const int hh = g >> 1;               // head of the B columns this lane supplies
   const bool lo_col = (g & 1) != 0;    // ... and whether it is the remainder column
+  // a waiting warp is suspended on the barrier (up to ~20 us per test) instead of spinning
   auto wait_tile = [&](int k) -> bool {
     const unsigned bar = smem_u32(&bars[warp][k % NST]);
     const unsigned parity = (k / NST) & 1;
-    unsigned long long t0 = 0;
-    int spins = 0;
     bool ok = true;
-    while (!mbar_try_wait(bar, parity)) {
-      if (++spins == 64) {
-        spins = 0;
-        const unsigned long long now = globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        else if (now - t0 > WAIT_LIMIT_NS) { ok = false; break; }
-      }
+    if (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (!mbar_try_wait_sleep(bar, parity, 20000u))
+        if (globaltimer_ns() - t0 > WAIT_LIMIT_NS) {
+          ok = false;
+          break;
+        }
     }
     return __all_sync(0xffffffffu, ok);
   };

@@ -80,6 +80,16 @@ __device__ __forceinline__ int tk_unit_of(const long long* cum, int units, long 
   return lo;
 }
 
+// a[i] for a runtime i, by unrolled selects: the small per-unit arrays stay in registers
+template <typename T, int N>
+__device__ __forceinline__ T tk_pick(const T (&a)[N], int i) {
+  T r = a[0];
+#pragma unroll
+  for (int k = 1; k < N; ++k)
+    if (i == k) r = a[k];
+  return r;
+}
+
 __device__ __forceinline__ const uint8_t* tk_tile_src(const TokState& s, int layer, int buf, int u, int z, int k) {
   if (z == 4) return s.tail + (tk_tail_tok_index(s, layer, buf, u) / 16 + k) * (long long)s.g.bf_tile();
   return s.pool[z] + (tk_pool_tile_index(s, z, layer, buf, u) + k) * (long long)tk_tile_bytes(s, z);
@@ -87,6 +97,20 @@ __device__ __forceinline__ const uint8_t* tk_tile_src(const TokState& s, int lay
 
 // ------------------------------------------------------------------------------ helpers
 __device__ __forceinline__ uint4 tk_lds128(const uint8_t* p) { return *reinterpret_cast<const uint4*>(p); }
+
+// one test of an mbarrier phase that may suspend the thread until the phase completes (at most
+// about 20 us)
+__device__ __forceinline__ bool tk_try_wait(unsigned bar, unsigned parity) {
+  unsigned done;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(done)
+      : "r"(bar), "r"(parity), "r"(20000u)
+      : "memory");
+  return done != 0;
+}
 
 template <int WPL>
 __device__ __forceinline__ void tk_load_words(const uint8_t* blk, int lane, unsigned (&w)[WPL]) {
@@ -409,14 +433,17 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   bool cvalid = true;
   // the cursor walks stages: stage k of segment z holds tiles [k pc, (k + 1) pc) (pc tiles per
   // stage) and starts at cost s0[z] + k pc cost[z]
-  auto nstages = [&](int z) -> int { const int pc = tk_per_stage<D>(z); return (un.t[z] + pc - 1) / pc; };
+  int cost[5];   // per-tile cost of each segment kind, in registers
+#pragma unroll
+  for (int z = 0; z < 5; ++z) cost[z] = S.cost[z];
+  auto nstages = [&](int z) -> int { const int pc = tk_per_stage<D>(z); return (tk_pick(un.t, z) + pc - 1) / pc; };
   {
     // first stage whose start >= x_lo
     const long long r = x_lo - ux;
     cz = 5;
     for (int z = 0; z < 5; ++z) {
       if (un.t[z] == 0) continue;
-      const long long step = (long long)tk_per_stage<D>(z) * S.cost[z];
+      const long long step = (long long)tk_per_stage<D>(z) * cost[z];
       const long long last = un.s0[z] + (long long)(nstages(z) - 1) * step;
       if (r <= last) {
         cz = z;
@@ -432,7 +459,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
         ux = tk_X(cum, cu, tail_cost);
         cz = 0;
         ck = 0;
-        while (cz < 5 && un.t[cz] == 0) ++cz;
+        while (cz < 5 && tk_pick(un.t, cz) == 0) ++cz;
       }
     }
   }
@@ -441,7 +468,7 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
     if (ck < nstages(cz)) return;
     ck = 0;
     ++cz;
-    while (cz < 5 && un.t[cz] == 0) ++cz;
+    while (cz < 5 && tk_pick(un.t, cz) == 0) ++cz;
     if (cz < 5) return;
     ++cu;
     if (cu >= S.units) {
@@ -451,24 +478,25 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
     un = tk_unit(S, p.layer, cu, n_tail);
     ux = tk_X(cum, cu, tail_cost);
     cz = 0;
-    while (cz < 5 && un.t[cz] == 0) ++cz;
+    while (cz < 5 && tk_pick(un.t, cz) == 0) ++cz;
   };
   auto issue_next = [&](int stage) -> bool {
     if (!cvalid || cz >= 5) return false;
     const int pc = tk_per_stage<D>(cz);
-    const long long start = ux + un.s0[cz] + (long long)ck * pc * S.cost[cz];
+    const long long start = ux + tk_pick(un.s0, cz) + (long long)ck * pc * tk_pick(cost, cz);
     if (start >= x_hi) return false;
     if (lane == 0) {
       const int kind = cz;
       const int t0 = ck * pc;
-      const int nt = un.t[cz] - t0 < pc ? un.t[cz] - t0 : pc;
+      const int tz = tk_pick(un.t, cz);
+      const int nt = tz - t0 < pc ? tz - t0 : pc;
       const unsigned bytes = (unsigned)(nt * tk_tile_bytes(S, kind == 4 ? TK_TAIL : kind));
       TkDesc d;
       d.u = cu;
       d.kind = kind;
       d.ntile = nt;
-      d.rem = un.n[cz] - 16 * t0;
-      d.tokslot = un.tok0[cz] + 16 * t0;
+      d.rem = tk_pick(un.n, cz) - 16 * t0;
+      d.tokslot = tk_pick(un.tok0, cz) + 16 * t0;
       descs[warp][stage] = d;
       const unsigned bar = smem_u32(&bars[warp][stage]);
       mbar_expect_tx(bar, bytes);
@@ -521,19 +549,18 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
     }
   };
   reset();
+  // a waiting warp is suspended on the barrier (up to ~20 us per test) instead of spinning
   auto wait_tile = [&](int k) -> bool {
     const unsigned bar = smem_u32(&bars[warp][k % NST]);
     const unsigned parity = (k / NST) & 1;
-    unsigned long long t0 = 0;
-    int spins = 0;
     bool ok = true;
-    while (!mbar_try_wait(bar, parity)) {
-      if (++spins == 64) {
-        spins = 0;
-        const unsigned long long now = globaltimer_ns();
-        if (t0 == 0) t0 = now;
-        else if (now - t0 > TK_WAIT_NS) { ok = false; break; }
-      }
+    if (!tk_try_wait(bar, parity)) {
+      const unsigned long long t0 = globaltimer_ns();
+      while (!tk_try_wait(bar, parity))
+        if (globaltimer_ns() - t0 > TK_WAIT_NS) {
+          ok = false;
+          break;
+        }
     }
     return __all_sync(0xffffffffu, ok);
   };
