@@ -31,13 +31,13 @@ if ROOT not in sys.path:
 METRIC = "decode tokens/s and attn HBM GB/s vs peak; GQA 32q/8kv d128, 32K ctx"
 
 
-def _peaks():
+def _peaks(key="hbm_gbs", fallback=6800.0):
     try:
         with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
             p = json.load(f)
-        return float(p["hbm_gbs"]), "measured"
+        return float(p[key]), "measured"
     except Exception:
-        return 6800.0, "fallback"
+        return fallback, "fallback"
 
 
 def _dist():
@@ -432,6 +432,29 @@ def run_ours(args):
         "gpu_launches": launches,
         "clocks": clk,
     }
+    # a verify on the fused path: its attention launch is the tensor-core contraction
+    G = Hq // Hkv
+    fused = verify and (args.verify_path == "fused" or (args.verify_path == "auto" and NQ >= 5)) \
+        and not wl.rope_theta and NQ * G <= 64
+    if fused:
+        tokens = B * Hkv * ((info.n_full + info.n_quant + info.n_pinned) * wl.window + wl.n_sink)
+        flops = 4.0 * NQ * G * D * tokens   # Q K^T and P V per attended token and query row
+        avg_s = attn_ms / 1e3 / max(attn_launches, 1)
+        tpeak, tpeak_kind = _peaks("bf16_tflops", 1900.0)
+        t_ach = flops / avg_s / 1e12 if attn_ms > 0 else None
+        line["roofline"] = {
+            "bound": "tensor", "kernel": "qe_verify_attn", "achieved": round(t_ach, 2) if t_ach else None,
+            "peak": tpeak, "peak_kind": tpeak_kind + " (dense bf16, burst)", "unit": "TFLOP/s",
+            "frac": round(t_ach / tpeak, 4) if t_ach else None, "traffic": None,
+            "algorithmic_flops_per_launch": flops,
+            "flops_rule": "4 R d per attended token (Q K^T and P V), R = drafts x G rows; tokens = the kept "
+                          "windows of every unit (the 2-bit keys' three exact bf16 parts and P's two are not "
+                          "counted)",
+            "avg_launch_us": round(avg_s * 1e6, 2),
+            "attn_gbs": round(achieved, 1) if achieved else None,
+            "measured_on": "the next %d verify steps launched directly, CUDA events around each fused attention "
+                           "launch" % KR,
+        }
     if verify:
         line["config"]["verify"] = {
             "drafts_per_step": NQ, "accepted": "all", "path": args.verify_path,

@@ -327,10 +327,12 @@ typedef struct {
  * been routed are zero. */
 qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n_units);
 
-/* Time every qe_decode_step attention launch with CUDA events on the handle's
- * stream (enable = 1) or stop (0).  qe_get_timing returns the summed device
- * time in ms, the number of launches and the summed algorithmic bytes of
- * the timed launches since the last enable, and resets nothing. */
+/* Time every attention launch with CUDA events on the handle's stream (enable = 1) or stop
+ * (0): the decode step's (qe_decode_step, and qe_verify draft by draft) and the fused verify's
+ * (qe_verify with the tensor-core path; its combine launch is not timed).  qe_get_timing
+ * returns the summed device time in ms, the number of launches and the summed algorithmic
+ * bytes (the kept windows each launch reads) of the timed launches since the last enable, and
+ * resets nothing. */
 qe_status qe_set_timing(qe_handle h, int enable);
 qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, double* attn_bytes);
 

@@ -656,7 +656,34 @@ static qe_status verify_fused(qe_handle h, int layer, const void* q, const void*
   vp.part_ml = h->vf_part_ml;
   vp.lse = h->vf_lse;
   vp.ent_cap = ent_cap;
-  QE_CK(h, qe::launch_verify_fused(vp, od, c.out_fp32, dl, (long long)h->units * h->st.maxw, h->stream));
+  // the attention launch is timed like a decode step's (qe_set_timing)
+  cudaEvent_t e0 = nullptr, e1 = nullptr;
+  unsigned ev_flags = cudaEventRecordDefault;
+  if (h->timing) {
+    while (h->ev_pool.size() < h->ev_used + 2) {
+      cudaEvent_t ev;
+      QE_CK(h, cudaEventCreate(&ev));
+      h->ev_pool.push_back(ev);
+    }
+    e0 = h->ev_pool[h->ev_used];
+    e1 = h->ev_pool[h->ev_used + 1];
+    h->ev_used += 2;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    QE_CK(h, cudaStreamIsCapturing(h->stream, &cs));
+    ev_flags = cs == cudaStreamCaptureStatusActive ? cudaEventRecordExternal : cudaEventRecordDefault;
+    QE_CK(h, cudaEventRecordWithFlags(e0, h->stream, ev_flags));
+  }
+  QE_CK(h, qe::launch_verify_attn(vp, h->stream));
+  if (h->timing) {
+    QE_CK(h, cudaEventRecordWithFlags(e1, h->stream, ev_flags));
+    h->timed_launches += 1;
+    LayerMirror mm = m;
+    mm.L += n_q;   // the drafts are appended
+    qe_layer_info info;
+    fill_info(h, mm, &info);
+    h->timed_bytes += info.attn_bytes;
+  }
+  QE_CK(h, qe::launch_verify_combine(vp, od, c.out_fp32, dl, (long long)h->units * h->st.maxw, h->stream));
   h->launches += 2;
   if (od != out) QE_CK(h, cudaMemcpyAsync(out, od, o_bytes, cudaMemcpyDeviceToHost, h->stream));
   m.verify_L0 = m.L;

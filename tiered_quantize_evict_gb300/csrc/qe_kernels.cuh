@@ -130,8 +130,9 @@ struct VerifyParams {
   float* lse;             // [units][ent_cap][64] per-window log2-sum-exp of each row
   int ent_cap;            // windows (bf16 entries + 2-bit entries) a unit can list
 };
-cudaError_t launch_verify_fused(const VerifyParams& p, void* out, int out_fp32, float* delta, long long qstride,
-                                cudaStream_t s);
+cudaError_t launch_verify_attn(const VerifyParams& p, cudaStream_t s);
+cudaError_t launch_verify_combine(const VerifyParams& p, void* out, int out_fp32, float* delta, long long qstride,
+                                  cudaStream_t s);
 cudaError_t prepare_verify_kernels(int D, int W);
 int verify_max_rows();
 int verify_min_drafts();   // automatic path choice: fused from this many drafts

@@ -370,8 +370,8 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
   };
 
   if (warp == 8) {
-    // ============================== tensor cores and copies (lane 0): S of chunk c, P V of chunk
-    // c - 1, then the refill of the stage chunk c - 1 read
+    // ============================== tensor cores and copies (lane 0): S of chunk c, the refill of
+    // the stage chunk c - 1 read, then P V of chunk c - 1
     if (lane == 0) {
       auto issue_copy = [&](int i, int2 e) {   // 2-bit chunk i of this split into stage i % VF_STAGES
         if (e.y < 0 || e.y >= st.capq) return;   // reported by the builders when they reach it
@@ -407,6 +407,16 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
           vf_commit(smem_u32(&bar_sk[b]));   // for the builders: key buffer b free again
           ++s_done;
         }
+        // the builders finished the stage of chunk c - 1 before they wrote chunk c's keys: refill
+        // it now, three 2-bit chunks ahead
+        if (c >= 1) {
+          const int qi = c - 1 - nbc;
+          if (qi >= 0 && qi + VF_STAGES < nqc) {
+            if (!vf_wait(smem_u32(&bar_stfree[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag)) break;
+            issue_copy(qi + VF_STAGES, refill);
+            refill = chunk_entry(nbc + qi + VF_STAGES + 1, ei);
+          }
+        }
         if (c >= 1) {
           const int cc = c - 1, b = cc & 1;
           if (!vf_wait(smem_u32(&bar_p[b]), (cc >> 1) & 1, st.err, abort_flag)) break;
@@ -421,12 +431,6 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
               vf_mma(tO, dP + 16 * (part * KT + kt), dV + 16 * kt, idesc, cc > 0 || part > 0 || kt > 0);
           vf_commit(smem_u32(&bar_o[b]));
           ++pv_done;
-          const int qi = cc - nbc;
-          if (qi >= 0 && qi + VF_STAGES < nqc) {
-            if (!vf_wait(smem_u32(&bar_stfree[qi % VF_STAGES]), (qi / VF_STAGES) & 1, st.err, abort_flag)) break;
-            issue_copy(qi + VF_STAGES, refill);
-            refill = chunk_entry(nbc + qi + VF_STAGES + 1, ei);
-          }
         }
       }
       // the tensor-core work issued must finish before tensor memory is read or freed
@@ -903,13 +907,9 @@ __global__ void __launch_bounds__(VF_COMBINE_THREADS) qe_verify_combine_kernel(c
 
 // ------------------------------------------------------------------------------ launchers
 template <int D, int W>
-static cudaError_t vf_launch_t(const VerifyParams& p, void* out, int out_fp32, float* delta, long long qstride,
-                               cudaStream_t s) {
+static cudaError_t vf_launch_t(const VerifyParams& p, cudaStream_t s) {
   using S = VfShape<D, W>;
   qe_verify_attn_kernel<D, W><<<dim3(p.st.units, p.splits), VF_THREADS, S::SMEM_REQ, s>>>(p);
-  cudaError_t e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  qe_verify_combine_kernel<D><<<dim3(p.st.units, p.n_q), VF_COMBINE_THREADS, 0, s>>>(p, out, out_fp32, delta, qstride);
   return cudaGetLastError();
 }
 
@@ -929,17 +929,28 @@ cudaError_t prepare_verify_kernels(int D, int W) {
   return cudaErrorInvalidValue;
 }
 
-cudaError_t launch_verify_fused(const VerifyParams& p, void* out, int out_fp32, float* delta, long long qstride,
-                                cudaStream_t s) {
+cudaError_t launch_verify_attn(const VerifyParams& p, cudaStream_t s) {
   const int D = p.st.geo.D, W = p.st.geo.W;
   if (p.splits < 1 || p.splits > VF_MAX_SPLITS || p.R < 1 || p.R > VF_ROWS) return cudaErrorInvalidValue;
-  if (D == 128 && W == 16) return vf_launch_t<128, 16>(p, out, out_fp32, delta, qstride, s);
-  if (D == 128 && W == 32) return vf_launch_t<128, 32>(p, out, out_fp32, delta, qstride, s);
-  if (D == 128 && W == 64) return vf_launch_t<128, 64>(p, out, out_fp32, delta, qstride, s);
-  if (D == 64 && W == 16) return vf_launch_t<64, 16>(p, out, out_fp32, delta, qstride, s);
-  if (D == 64 && W == 32) return vf_launch_t<64, 32>(p, out, out_fp32, delta, qstride, s);
-  if (D == 64 && W == 64) return vf_launch_t<64, 64>(p, out, out_fp32, delta, qstride, s);
+  if (D == 128 && W == 16) return vf_launch_t<128, 16>(p, s);
+  if (D == 128 && W == 32) return vf_launch_t<128, 32>(p, s);
+  if (D == 128 && W == 64) return vf_launch_t<128, 64>(p, s);
+  if (D == 64 && W == 16) return vf_launch_t<64, 16>(p, s);
+  if (D == 64 && W == 32) return vf_launch_t<64, 32>(p, s);
+  if (D == 64 && W == 64) return vf_launch_t<64, 64>(p, s);
   return cudaErrorInvalidValue;
+}
+
+cudaError_t launch_verify_combine(const VerifyParams& p, void* out, int out_fp32, float* delta, long long qstride,
+                                  cudaStream_t s) {
+  if (p.splits < 1 || p.splits > VF_MAX_SPLITS || p.R < 1 || p.R > VF_ROWS) return cudaErrorInvalidValue;
+  if (p.st.geo.D == 128)
+    qe_verify_combine_kernel<128><<<dim3(p.st.units, p.n_q), VF_COMBINE_THREADS, 0, s>>>(p, out, out_fp32, delta, qstride);
+  else if (p.st.geo.D == 64)
+    qe_verify_combine_kernel<64><<<dim3(p.st.units, p.n_q), VF_COMBINE_THREADS, 0, s>>>(p, out, out_fp32, delta, qstride);
+  else
+    return cudaErrorInvalidValue;
+  return cudaGetLastError();
 }
 
 int verify_ctas_per_sm(int D, int W) {
