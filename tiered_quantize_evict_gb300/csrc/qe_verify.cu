@@ -7,38 +7,43 @@
 // 5th-generation tensor cores (tcgen05.mma, accumulators in tensor memory), reading every window
 // once for all rows, instead of one decode step per draft.
 //
-// One CTA of 256 threads per (unit, split of the unit's windows); a window is a "chunk".
+// One CTA of 288 threads (9 warps) per (unit, split of the unit's windows); a window is a
+// "chunk".
 //  * Rows: row r = j G + h (draft j, query head h), r < 64.
 //  * S = Q K^T per chunk: M = 64 rows, N = W tokens (bf16 window) or 3W (a 2-bit window's
 //    keys dequantized as code * s + z, one float32 fma as the oracle does, and split into three
 //    bf16 parts -- truncated, truncated remainder, rest -- that are exact together; the three
 //    parts' products land in three column blocks and are summed in float32).  Q is bf16, so
 //    every product is exact.  Accumulator row r sits in tensor-memory lane 32 (r / 16) + r % 16.
-//  * O^T += V^T P^T per chunk: M = D channels (A: values with channels as rows), N = 64 rows
-//    (B: P), K = the chunk's tokens, once for P's truncated bf16 part and once for its rounded
+//  * O += P V per chunk: M = 64 rows (A: P), N = D channels (B: values with channels as rows),
+//    K = the chunk's tokens, once for P's truncated bf16 part and once for its rounded
 //    remainder (P to about 17 significant bits).  A 2-bit window's values enter as 1 + code / 4
-//    (exact in bf16) with 4 s_V folded into P and sum_t p_t (z_t - 4 s_t) kept per row.
-//    O^T lives in tensor memory for the whole CTA, channel d in lane d (lane 32 (d / 16) +
-//    d % 16 when D = 64).
-//  * Warps 0-3 run the softmax: warp w reads rows 16 w .. 16 w + 15 of S with the 16x256b
-//    tensor-memory load, which gives lane T the rows 16 w + T / 4 and 16 w + 8 + T / 4 and two
-//    adjacent columns of every 8-column block (the mma accumulator fragment), so a row's four
-//    lanes reduce with two shuffles.  A row's reference maximum grows lazily (by more than 2^8
-//    in the log2 domain); O^T's columns are then rescaled in tensor memory.
-//  * Warps 4-7 build the operands of chunk c + 1 (keys, values, the 2-bit value parameters)
-//    while the softmax works on chunk c; keys, values and P enter shared memory through
-//    stmatrix, in the no-swizzle K-major core-matrix layout (8 rows x 16 bytes per core matrix,
-//    the two halves of a 16-wide K step 128 bytes apart).  Operands and S are double-buffered;
-//    2-bit slots arrive by bulk copies three chunks ahead, bf16 slots by direct loads.
+//    (exact in bf16) with 4 s_V folded into P and sum_t p_t (z_t - 4 s_t) kept per row.  O
+//    lives in tensor memory for the whole CTA, in the same lanes as S.
+//  * Warps 0-3 run the softmax, warp w on rows 16 w .. 16 w + 15: the 16x256b tensor-memory
+//    load gives lane T the rows 16 w + T / 4 and 16 w + 8 + T / 4 and two adjacent columns of
+//    every 8-column block (the mma accumulator fragment), so a row's four lanes reduce with two
+//    shuffles.  A row's reference maximum grows lazily (by more than 2^8 in the log2 domain)
+//    and the warp rescales its own rows of O in tensor memory.
+//  * Warps 4-7 build the operands of the next chunks (keys through per-warp tables of the three
+//    bf16 parts of each channel's four codes; values; P is written by the softmax warps), in
+//    the no-swizzle K-major core-matrix layout (8 rows x 16 bytes per core matrix, the two
+//    halves of a 16-wide K step 128 bytes apart), through stmatrix.  Keys, values and P are
+//    double-buffered; S is single-buffered (the softmax copies it to registers first).  2-bit
+//    slots arrive by bulk copies three chunks ahead; bf16 slots by direct loads a chunk ahead.
+//  * Warp 8 (one lane) issues the tensor-core work -- S of chunk c, then P V of chunk c - 1 --
+//    and the stage refills.
 //  * Causality among the drafts: draft j sees positions < L0 + j + 1.
 //  * Per window and row the kernel writes the log2-sum-exp of the window's logits; the combine
 //    kernel turns them into each draft's window masses once the row's normaliser is known.
-// Handshakes (mbarriers): stage[s] (a 2-bit slot landed), s[b] (S of the chunk in buffer b is
-// complete), built[b] (the builders wrote buffer b; 128 arrivals), o[b] (the P V of the chunk in
-// buffer b is complete: its operands, its S buffer and P buffer are free).  Every wait is
-// bounded (0.2 s); an expired wait sets the sticky timeout bit and an abort flag that ends both
-// warp groups' loops, and the CTA leaves after the tensor-core work and copies it issued have
-// finished.
+// Handshakes (mbarriers): stage[s] (a 2-bit slot landed), stfree[s] (the builders are done
+// with a stage), s (S complete), sfree (the softmax warps have read S), sk[b] (the S that read
+// key buffer b is complete), keys[b] (keys of buffer b written), built[b] (values of buffer b
+// written), p[b] (P of buffer b written, and any rescale of O done), o[b] (the P V of buffer b
+// is complete).  Producers arrive once per warp after __syncwarp, or by tcgen05.commit.  Every
+// wait is bounded (0.2 s); an expired wait sets the sticky timeout bit and an abort flag that
+// ends every warp's loop, and the CTA leaves after the tensor-core work and copies it issued
+// have finished.
 #include <cstdint>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
