@@ -74,15 +74,17 @@ class ParityRun:
     """A cache on the GPU plus oracle units for a chosen set of (b, layer, kvh)."""
 
     def __init__(self, wl, batch: int, n_layers: int, track: Sequence[Tuple[int, int, int]],
-                 device_inputs: bool = False, host: Optional[str] = None):
+                 device_inputs: bool = False, host: Optional[str] = None, out_fp32: bool = True):
         """host: None (device buffers), "pinned" (page-locked torch tensors) or "pageable"
-        (numpy arrays): where the inputs and the outputs of every call live."""
+        (numpy arrays): where the inputs and the outputs of every call live.  out_fp32: the
+        cache's output type (float32, else bf16; outputs are read back as float32)."""
         import tiered_quantize_evict_gb300 as qe
         torch, dev = torch_dev()
         self.torch, self.dev = torch, dev
         self.wl, self.batch, self.n_layers = wl, batch, n_layers
-        self.cache = qe.QECache(qe.config_from_workload(wl, batch=batch, n_layers=n_layers),
+        self.cache = qe.QECache(qe.config_from_workload(wl, batch=batch, n_layers=n_layers, out_fp32=out_fp32),
                                 torch.cuda.current_stream().cuda_stream)
+        self.out_fp32 = out_fp32
         self.units_per_layer = batch * wl.n_kv_heads
         self.tracked = [Tracked(b, l, h, make_unit(wl)) for (b, l, h) in track]
         self.device_inputs = device_inputs
@@ -99,12 +101,24 @@ class ParityRun:
         self.route_events = 0
         assert host in (None, "pinned", "pageable") and not (host and device_inputs)
         self.host = host
-        if host == "pinned":
-            self.out = torch.empty(batch, wl.n_q_heads, wl.head_dim, dtype=torch.float32).pin_memory()
-        elif host == "pageable":
-            self.out = np.zeros((batch, wl.n_q_heads, wl.head_dim), np.float32)
-        else:
-            self.out = torch.empty(batch, wl.n_q_heads, wl.head_dim, device=dev, dtype=torch.float32)
+        self.out = self.out_buffer((batch, wl.n_q_heads, wl.head_dim))
+
+    def out_buffer(self, shape):
+        """An output buffer of the cache's output type, where this run keeps its buffers."""
+        torch = self.torch
+        tdt = torch.float32 if self.out_fp32 else torch.bfloat16
+        if self.host == "pinned":
+            return torch.empty(*shape, dtype=tdt).pin_memory()
+        if self.host == "pageable":
+            return np.zeros(shape, np.float32 if self.out_fp32 else np.uint16)
+        return torch.empty(*shape, device=self.dev, dtype=tdt)
+
+    def read_buffer(self, out) -> np.ndarray:
+        """An output buffer's values as float32 (the stream has passed the call)."""
+        if isinstance(out, np.ndarray):
+            a = np.array(out, copy=True)
+            return a if self.out_fp32 else gen.bf16_bits_to_f32(a)
+        return out.float().cpu().numpy().copy()
 
     def _place(self, a: np.ndarray):
         a = np.ascontiguousarray(a).view(np.int16)
@@ -117,8 +131,7 @@ class ParityRun:
     def _read_out(self):
         if self.host:   # host buffers are complete once the stream has passed the call
             self.cache.qe_synchronize()
-            return np.array(self.out, copy=True) if self.host == "pageable" else self.out.numpy().copy()
-        return self.out.cpu().numpy().copy()
+        return self.read_buffer(self.out)
 
     # ------------------------------------------------------------------ inputs
     def _kv(self, layer, pos0, n):

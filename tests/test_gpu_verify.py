@@ -144,3 +144,56 @@ def test_rejected_draft_returns_its_window_slot():
     for tr in run.tracked:
         run.check_bf16_windows(tr)
     cache.qe_synchronize()
+
+
+@pytest.mark.parametrize("host", ["pinned", "pageable"])
+def test_fused_verify_host_buffers_bf16_outputs(host):
+    """The fused path with every buffer in host memory (staged through the handle's buffers)
+    and bf16 outputs: each draft's output against the oracle within 4e-3 relative L2 (bf16
+    rounding of the outputs included), then the scores after each commit and the tiers after
+    each routing event, as with device buffers."""
+    wl = CASES["d128_w32_g4"]
+    track = [(b, 0, h) for b in range(wl.batch) for h in range(wl.n_kv_heads)]
+    run = ParityRun(wl, wl.batch, 1, track, host=host, out_fp32=False)
+    assert qe.debug_inject(qe.QE_DEBUG_VERIFY_PATH, 1, run.cache) == 0
+    run.prefill()
+    cache, G, D = run.cache, wl.group, wl.head_dim
+    rng = np.random.default_rng(11)
+    last_route = 0
+    for event in range(6):
+        n_q = int(rng.integers(5, 17))
+        acc = int(rng.integers(0, n_q + 1))
+        t0, L0 = run.t, wl.prefill + run.t
+        K = np.stack([host_kv(wl, 0, L0 + j, 1, wl.batch)[0][:, :, 0] for j in range(n_q)])
+        V = np.stack([host_kv(wl, 0, L0 + j, 1, wl.batch)[1][:, :, 0] for j in range(n_q)])
+        Q = np.stack([host_q(wl, 0, t0 + 1 + j, wl.batch) for j in range(n_q)])
+        out = run.out_buffer((n_q, wl.batch, wl.n_q_heads, D))
+        k_, v_, q_ = run._place(K), run._place(V), run._place(Q)
+        cache.qe_verify(0, q_, k_, v_, out, n_q)
+        cache.qe_synchronize()
+        del k_, v_, q_
+        got = run.read_buffer(out).astype(np.float64)
+        for tr in run.tracked:
+            qs = [gen.bf16_bits_to_f32(Q[j, tr.b, tr.kvh * G:(tr.kvh + 1) * G]) for j in range(n_q)]
+            ks = [gen.bf16_bits_to_f32(K[j, tr.b, tr.kvh]) for j in range(n_q)]
+            vs = [gen.bf16_bits_to_f32(V[j, tr.b, tr.kvh]) for j in range(n_q)]
+            outs, _ = tr.unit.verify(qs, ks, vs)
+            for j in range(n_q):
+                for i in range(G):
+                    ref = outs[j][i]
+                    err = np.linalg.norm(got[j, tr.b, tr.kvh * G + i] - ref) / np.linalg.norm(ref)
+                    run.max_out_err = max(run.max_out_err, err)
+                    assert err <= 4e-3, f"verify {event} draft {j} unit {(tr.b, tr.kvh)}: rel-L2 {err:.2e}"
+        cache.qe_verify_commit(0, acc)
+        for tr in run.tracked:
+            tr.unit.commit(acc)
+        run.t += acc
+        run.check_scores()
+        assert cache.layer_info(0).length == wl.prefill + run.t
+        if run.t // wl.route_period > last_route:
+            last_route = run.t // wl.route_period
+            run.route_and_check()
+    cache.qe_synchronize()
+    run.assert_all_live()
+    print(f"{host}: max out rel-L2 {run.max_out_err:.2e}, max score rel {run.max_score_err:.2e}, "
+          f"routes {run.route_events}")
