@@ -327,6 +327,11 @@ typedef struct {
  * been routed are zero. */
 qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n_units);
 
+/* Profiling: qe_init, qe_append, qe_decode_step, qe_decode_step_noalloc, qe_verify,
+ * qe_verify_commit, qe_route and qe_synchronize each open an NVTX range named after the call
+ * (NVTX v3, header-only; without a profiler attached a range costs one test of a null
+ * function pointer).  The ranges mark host-side enqueueing, not device time. */
+
 /* Time every attention launch with CUDA events on the handle's stream (enable = 1) or stop
  * (0): the decode step's (qe_decode_step, and qe_verify draft by draft) and the fused verify's
  * (qe_verify with the tensor-core path; its combine launch is not timed).  qe_get_timing

@@ -4,12 +4,22 @@
 #include <vector>
 
 #include <cuda_runtime.h>
+#include <nvtx3/nvToolsExt.h>
 
 #include "qe.h"
 #include "qe_kernels.cuh"
 #include "qe_tok.cuh"
 
 namespace qe {
+
+// An NVTX range over one call of the ABI (header-only NVTX v3: without a profiler attached,
+// a push or pop is one test of a null function pointer).
+struct NvtxRange {
+  explicit NvtxRange(const char* name) { nvtxRangePushA(name); }
+  ~NvtxRange() { nvtxRangePop(); }
+  NvtxRange(const NvtxRange&) = delete;
+  NvtxRange& operator=(const NvtxRange&) = delete;
+};
 
 // Host shadow of a layer's device header (launch shapes never depend on it; checks and
 // introspection do).

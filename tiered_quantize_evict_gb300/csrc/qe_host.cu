@@ -163,6 +163,7 @@ const char* qe_last_error(qe_handle h) { return h ? h->err.c_str() : g_init_erro
 long long qe_kernel_launches(qe_handle h) { return h ? h->launches : 0; }
 
 qe_status qe_init(const qe_config* cfg, void* cuda_stream, qe_handle* out) {
+  qe::NvtxRange nvtx_("qe_init");
   if (!cfg || !out) return fail(nullptr, QE_ERR_INVALID_ARG, "null argument");
   qe::inject_begin_init();
   const qe_config& c = *cfg;
@@ -420,6 +421,7 @@ qe_status qe_destroy(qe_handle h) {
 }
 
 qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_tokens, int flags) {
+  qe::NvtxRange nvtx_("qe_append");
   if (h && h->tok) return qe::tok_append(h, layer, k, v, n_tokens, flags);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
@@ -474,6 +476,7 @@ qe_status qe_append(qe_handle h, int layer, const void* k, const void* v, int n_
 static qe_status decode_impl(qe_handle h, int layer, const void* q, void* out, int flags, float* delta);
 
 qe_status qe_decode_step(qe_handle h, int layer, const void* q, void* out, int flags) {
+  qe::NvtxRange nvtx_("qe_decode_step");
   if (h && h->tok) return qe::tok_decode(h, layer, q, out, flags);
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
@@ -694,6 +697,7 @@ static qe_status verify_fused(qe_handle h, int layer, const void* q, const void*
 
 qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const void* v, void* out, int n_q,
                     int flags) {
+  qe::NvtxRange nvtx_("qe_verify");
   if (h && h->tok) return fail(h, QE_ERR_STATE, "speculative verify serves window-tiered handles");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
@@ -743,6 +747,7 @@ qe_status qe_verify(qe_handle h, int layer, const void* q, const void* k, const 
 }
 
 qe_status qe_verify_commit(qe_handle h, int layer, int n_accept) {
+  qe::NvtxRange nvtx_("qe_verify_commit");
   qe_status s = check_layer(h, layer);
   if (s != QE_OK) return s;
   LayerMirror& m = h->lay[layer];
@@ -808,6 +813,7 @@ static qe_status route_layers(qe_handle h, int l0, int n) {
 }
 
 qe_status qe_route(qe_handle h, int layer) {
+  qe::NvtxRange nvtx_("qe_route");
   if (!h) return QE_ERR_INVALID_ARG;
   if (h->tok) return qe::tok_route(h, layer);
   if (layer == -1) return route_layers(h, 0, h->cfg.n_layers);
@@ -817,6 +823,7 @@ qe_status qe_route(qe_handle h, int layer) {
 }
 
 qe_status qe_synchronize(qe_handle h) {
+  qe::NvtxRange nvtx_("qe_synchronize");
   if (!h) return QE_ERR_INVALID_ARG;
   QE_CK(h, cudaStreamSynchronize(h->stream));
   unsigned flag = 0;

@@ -58,6 +58,7 @@ qe_status na_fail(qe_handle h, qe_status s, const char* fmt, ...) {
 }  // namespace
 
 extern "C" qe_status qe_decode_step_noalloc(qe_handle h, int layer, const void* q, void* out) {
+  qe::NvtxRange nvtx_("qe_decode_step_noalloc");
   if (!h) return QE_ERR_INVALID_ARG;
   if (h->tok) return na_fail(h, QE_ERR_STATE, "the no-allocation decode step serves window-tiered handles");
   if (layer < 0 || layer >= h->cfg.n_layers) return na_fail(h, QE_ERR_INVALID_ARG, "layer %d out of range", layer);
