@@ -391,6 +391,32 @@ enum { QE_DEBUG_FAIL_DEVICE_ALLOC = 1, QE_DEBUG_FAIL_HOST_STORE = 2, QE_DEBUG_EX
        QE_DEBUG_VERIFY_PATH = 4 };
 qe_status qe_debug_inject(qe_handle h, int what, long long value);
 
+/* ---------------------------------------------------------------- snapshots (session restore)
+ *
+ * H2O page §6 (session restore): what a cache needs to resume is more than its K and V -- the
+ * tiers, the cumulative scores (which the K and V cannot rebuild), the window boundaries,
+ * positions and lengths.  A snapshot holds all of a window-tiered handle's state: the table
+ * (tiers, slots, scores, lists, free stacks, victim and previous-slot marks), the bf16 and
+ * 2-bit window slabs and their magnitude records, the pinned host store and ledger, the layer
+ * headers, the routing counters and records, and each layer's host-side length and counts.
+ * Split-K scratch, staging and verify deltas are rebuilt by every call and not saved.  The
+ * format is this build's own (magic "QESNAP01"); it is not meant to cross builds or machines.
+ *
+ * qe_snapshot_size: bytes a snapshot of h takes (synchronous, no device work).
+ * qe_snapshot: writes the snapshot into host (at least qe_snapshot_size bytes; any host
+ *   memory).  Synchronous: a pending single-token append is written first, then the handle's
+ *   stream is synchronised and the state copied out.
+ * qe_restore: replaces h's whole state with a snapshot of a handle with the same
+ *   configuration (every field that fixes the layout must match; QE_ERR_INVALID_ARG
+ *   otherwise, h unchanged).  Synchronous; afterwards h continues exactly as the snapshotted
+ *   handle would have: the same outputs, scores and tiers, bit for bit.
+ * Errors: QE_ERR_STATE (a five-tier handle; a layer awaiting qe_verify_commit),
+ * QE_ERR_INVALID_ARG (null pointers, a buffer too small, not a snapshot, another
+ * configuration), QE_ERR_CUDA. */
+qe_status qe_snapshot_size(qe_handle h, size_t* bytes);
+qe_status qe_snapshot(qe_handle h, void* host, size_t bytes);
+qe_status qe_restore(qe_handle h, const void* host, size_t bytes);
+
 /* ---------------------------------------------------------------- no-allocation decode step
  *
  * Not part of the method on the pages (the paper has no counterpart): a library service.

@@ -29,7 +29,7 @@ EXPORTED = [
     "qe_get_quant_window", "qe_get_bf16_window", "qe_get_route_stats", "qe_set_timing",
     "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc", "qe_get_route_diag",
     "qe_get_token_tiers", "qe_get_token_scores", "qe_get_token_counts", "qe_get_token",
-    "qe_verify", "qe_verify_commit", "qe_debug_inject",
+    "qe_verify", "qe_verify_commit", "qe_debug_inject", "qe_snapshot_size", "qe_snapshot", "qe_restore",
 ]
 QE_DEBUG_FAIL_DEVICE_ALLOC, QE_DEBUG_FAIL_HOST_STORE, QE_DEBUG_EXPIRE_WAIT, QE_DEBUG_VERIFY_PATH = 1, 2, 3, 4
 QE_VERIFY_MAX = 16
@@ -118,6 +118,9 @@ def load_library() -> ctypes.CDLL:
         "qe_verify": ([P, I, P, P, P, P, I, I], I),
         "qe_verify_commit": ([P, I, I], I),
         "qe_debug_inject": ([P, I, ctypes.c_longlong], I),
+    "qe_snapshot_size": ([P, ctypes.POINTER(ctypes.c_size_t)], I),
+    "qe_snapshot": ([P, P, ctypes.c_size_t], I),
+    "qe_restore": ([P, P, ctypes.c_size_t], I),
     }
     for name, (args, res) in sig.items():
         fn = getattr(lib, name)
@@ -293,6 +296,19 @@ class QECache:
         self._check(self._lib.qe_get_token(self.h, layer, unit, pos, ctypes.byref(tier), kb.ctypes.data, vb.ctypes.data,
                                            kc.ctypes.data, vc.ctypes.data, par.ctypes.data))
         return tier.value, kb, vb, kc, vc, par
+
+    def snapshot(self) -> np.ndarray:
+        """qe_snapshot: the handle's whole state as a host byte array (synchronous)."""
+        n = ctypes.c_size_t()
+        self._check(self._lib.qe_snapshot_size(self.h, ctypes.byref(n)))
+        buf = np.empty(n.value, np.uint8)
+        self._check(self._lib.qe_snapshot(self.h, buf.ctypes.data, n.value))
+        return buf
+
+    def restore(self, snap: np.ndarray):
+        """qe_restore: replace the handle's state with a snapshot of a same-config handle."""
+        snap = np.ascontiguousarray(snap, dtype=np.uint8)
+        self._check(self._lib.qe_restore(self.h, snap.ctypes.data, snap.nbytes))
 
     def set_timing(self, enable: bool):
         self._check(self._lib.qe_set_timing(self.h, 1 if enable else 0))

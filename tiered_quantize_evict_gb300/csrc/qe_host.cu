@@ -1088,3 +1088,187 @@ qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, doubl
 }
 
 }  // extern "C"
+
+// ------------------------------------------------------------------------------ snapshots
+// The state a window-tiered handle carries from one call to the next: every device array of
+// the table, the two slabs, the host store and ledger, the layer headers, the routing counters
+// and records, and the host mirror of each layer.  Scratch (split-K partials, staging, move
+// lists, verify deltas) is rebuilt by every call and not saved.
+namespace {
+
+struct Region {
+  void* p;
+  size_t bytes;
+  bool host;   // pinned host memory (memcpy) rather than device memory (cudaMemcpy)
+};
+
+std::vector<Region> state_regions(qe_handle h) {
+  const qe::State& st = h->st;
+  const size_t GU = (size_t)h->gu_total, maxw = (size_t)st.maxw, capb = (size_t)st.capb, capq = (size_t)st.capq,
+               caps = (size_t)st.caps, L = (size_t)h->cfg.n_layers;
+  const size_t bslot_b = (size_t)st.geo.bslot_bytes(), qslot_b = (size_t)st.geo.qslot_bytes();
+  return {
+      {st.tier, GU * maxw, false},
+      {st.bslot, GU * maxw * 4, false},
+      {st.qslot, GU * maxw * 4, false},
+      {st.sent, GU * maxw * 4, false},
+      {st.score, GU * maxw * 4, false},
+      {st.blist, GU * capb * sizeof(int2), false},
+      {st.qlist, GU * capq * sizeof(int2), false},
+      {st.bfree, GU * capb * 4, false},
+      {st.bfree_head, GU * 4, false},
+      {st.bfree_top, GU * 4, false},
+      {st.bvictim, GU * capb * 4, false},
+      {st.qvictim, GU * capq * 4, false},
+      {st.bprev, GU * maxw * 4, false},
+      {st.qprev, GU * maxw * 4, false},
+      {st.qfree, GU * capq * 4, false},
+      {st.qfree_top, GU * 4, false},
+      {st.sfree, GU * caps * 4, false},
+      {st.sfree_top, GU * 4, false},
+      {st.bslab, GU * capb * bslot_b, false},
+      {st.qslab, GU * capq * qslot_b, false},
+      {st.qrange, GU * capq * 4, false},
+      {st.err, 4, false},
+      {st.stats, L * qe::N_STATS * sizeof(unsigned long long), false},
+      {st.ldev, L * sizeof(qe::LayerDev), false},
+      {h->diag, L * (size_t)h->units * sizeof(qe::RouteDiag), false},
+      {h->hstore_host, GU * caps * bslot_b, true},
+      {h->hledger_host, GU * caps * qslot_b, true},
+  };
+}
+
+// The configuration fields that fix the layout, as doubles (no struct padding involved)
+constexpr int SNAP_CFG = 22;
+void snap_cfg(const qe_config& c, double (&v)[SNAP_CFG]) {
+  const double x[SNAP_CFG] = {(double)c.batch, (double)c.n_layers, (double)c.n_q_heads, (double)c.n_kv_heads,
+                              (double)c.head_dim, (double)c.window, (double)c.route_period, (double)c.n_sink,
+                              (double)c.n_recent, (double)c.max_context, (double)c.cap_mode, (double)c.kf,
+                              (double)c.kq, c.frac_bf16, c.frac_int2, c.budget_frac, (double)c.out_fp32,
+                              (double)c.tiering, c.rope_theta, (double)c.int2_slack, c.frac_int4, c.frac_nq1};
+  for (int i = 0; i < SNAP_CFG; ++i) v[i] = x[i];
+}
+
+constexpr char SNAP_MAGIC[8] = {'Q', 'E', 'S', 'N', 'A', 'P', '0', '1'};
+struct SnapHeader {
+  char magic[8];
+  uint64_t total_bytes;
+  uint64_t n_regions;
+  double cfg[SNAP_CFG];
+};
+struct SnapLayer {
+  int32_t L, routed_upto, n_full, n_quant, kf, kq;
+};
+
+size_t snap_bytes(qe_handle h, const std::vector<Region>& regs) {
+  size_t n = sizeof(SnapHeader) + (size_t)h->cfg.n_layers * sizeof(SnapLayer) + regs.size() * sizeof(uint64_t);
+  for (const Region& r : regs) n += r.bytes;
+  return n;
+}
+
+qe_status snap_usable(qe_handle h) {
+  if (!h) return QE_ERR_INVALID_ARG;
+  if (h->tok) return fail(h, QE_ERR_STATE, "snapshots serve window-tiered handles");
+  for (int l = 0; l < h->cfg.n_layers; ++l)
+    if (h->lay[l].verify_n) return fail(h, QE_ERR_STATE, "layer %d awaits qe_verify_commit", l);
+  return QE_OK;
+}
+
+}  // namespace
+
+qe_status qe_snapshot_size(qe_handle h, size_t* bytes) {
+  qe_status s = snap_usable(h);
+  if (s != QE_OK) return s;
+  if (!bytes) return fail(h, QE_ERR_INVALID_ARG, "bytes is null");
+  *bytes = snap_bytes(h, state_regions(h));
+  return QE_OK;
+}
+
+qe_status qe_snapshot(qe_handle h, void* host, size_t bytes) {
+  qe::NvtxRange nvtx_("qe_snapshot");
+  qe_status s = snap_usable(h);
+  if (s != QE_OK) return s;
+  const std::vector<Region> regs = state_regions(h);
+  const size_t need = snap_bytes(h, regs);
+  if (!host || bytes < need) return fail(h, QE_ERR_INVALID_ARG, "snapshot needs %zu bytes", need);
+  for (int l = 0; l < h->cfg.n_layers; ++l)   // a pending single-token append is written first
+    if ((s = commit_pending(h, l)) != QE_OK) return s;
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  uint8_t* o = static_cast<uint8_t*>(host);
+  SnapHeader hd{};
+  std::memcpy(hd.magic, SNAP_MAGIC, 8);
+  hd.total_bytes = need;
+  hd.n_regions = regs.size();
+  snap_cfg(h->cfg, hd.cfg);
+  std::memcpy(o, &hd, sizeof hd);
+  o += sizeof hd;
+  for (int l = 0; l < h->cfg.n_layers; ++l) {
+    const LayerMirror& m = h->lay[l];
+    const SnapLayer sl{m.L, m.routed_upto, m.n_full, m.n_quant, m.kf, m.kq};
+    std::memcpy(o, &sl, sizeof sl);
+    o += sizeof sl;
+  }
+  for (const Region& r : regs) {
+    const uint64_t b = r.bytes;
+    std::memcpy(o, &b, sizeof b);
+    o += sizeof b;
+  }
+  for (const Region& r : regs) {
+    if (r.host) std::memcpy(o, r.p, r.bytes);
+    else QE_CK(h, cudaMemcpy(o, r.p, r.bytes, cudaMemcpyDeviceToHost));
+    o += r.bytes;
+  }
+  return QE_OK;
+}
+
+qe_status qe_restore(qe_handle h, const void* host, size_t bytes) {
+  qe::NvtxRange nvtx_("qe_restore");
+  qe_status s = snap_usable(h);
+  if (s != QE_OK) return s;
+  const std::vector<Region> regs = state_regions(h);
+  const size_t need = snap_bytes(h, regs);
+  if (!host || bytes < sizeof(SnapHeader)) return fail(h, QE_ERR_INVALID_ARG, "not a snapshot");
+  const uint8_t* in = static_cast<const uint8_t*>(host);
+  SnapHeader hd;
+  std::memcpy(&hd, in, sizeof hd);
+  if (std::memcmp(hd.magic, SNAP_MAGIC, 8) != 0) return fail(h, QE_ERR_INVALID_ARG, "not a snapshot");
+  double cfg[SNAP_CFG];
+  snap_cfg(h->cfg, cfg);
+  for (int i = 0; i < SNAP_CFG; ++i)
+    if (cfg[i] != hd.cfg[i]) return fail(h, QE_ERR_INVALID_ARG, "snapshot of another configuration (field %d)", i);
+  if (hd.total_bytes != need || bytes < need || hd.n_regions != regs.size())
+    return fail(h, QE_ERR_INVALID_ARG, "snapshot of %llu bytes, this handle's are %zu",
+                (unsigned long long)hd.total_bytes, need);
+  const uint8_t* p = in + sizeof hd;
+  std::vector<SnapLayer> lays((size_t)h->cfg.n_layers);
+  for (int l = 0; l < h->cfg.n_layers; ++l) {
+    std::memcpy(&lays[(size_t)l], p, sizeof(SnapLayer));
+    p += sizeof(SnapLayer);
+  }
+  for (const Region& r : regs) {
+    uint64_t b;
+    std::memcpy(&b, p, sizeof b);
+    p += sizeof b;
+    if (b != r.bytes) return fail(h, QE_ERR_INVALID_ARG, "snapshot region of %llu bytes, expected %zu",
+                                  (unsigned long long)b, r.bytes);
+  }
+  // the handle's own work is finished before its state is replaced
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  for (const Region& r : regs) {
+    if (r.host) std::memcpy(r.p, p, r.bytes);
+    else QE_CK(h, cudaMemcpy(r.p, p, r.bytes, cudaMemcpyHostToDevice));
+    p += r.bytes;
+  }
+  for (int l = 0; l < h->cfg.n_layers; ++l) {
+    LayerMirror m{};
+    const SnapLayer& sl = lays[(size_t)l];
+    m.L = sl.L;
+    m.routed_upto = sl.routed_upto;
+    m.n_full = sl.n_full;
+    m.n_quant = sl.n_quant;
+    m.kf = sl.kf;
+    m.kq = sl.kq;
+    h->lay[(size_t)l] = m;
+  }
+  return QE_OK;
+}
