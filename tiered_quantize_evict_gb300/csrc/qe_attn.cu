@@ -100,7 +100,10 @@ __device__ __forceinline__ Lay make_lay(const State& st, int layer, int pend, in
 // warp's range mixes memory-bound bf16 tiles with compute-bound 2-bit tiles and the SM's warps
 // overlap the two instead of splitting into bf16 warps and 2-bit warps.
 __device__ __forceinline__ int q_before(const Lay& y, int i) {   // 2-bit tiles among [0, i)
-  return (int)(((long long)i * y.nq) / y.ntiles);
+  const unsigned long long n = (unsigned long long)i * (unsigned)y.nq;
+  // 32-bit division where the product fits (a 64-bit one is a long software sequence)
+  if (n <= 0xFFFFFFFFull) return (int)((unsigned)n / (unsigned)y.ntiles);
+  return (int)(n / (unsigned long long)y.ntiles);
 }
 __device__ __forceinline__ long long tile_start_in(const AttnParams& p, const Lay& y, int i) {
   const int qb = q_before(y, i);
@@ -111,17 +114,55 @@ __device__ __forceinline__ long long tile_start(const AttnParams& p, const Lay& 
 }
 
 // first tile whose start position is >= x
-__device__ __forceinline__ void first_tile(const AttnParams& p, const Lay& y, long long x, int& u, int& i) {
-  u = (int)(x / y.Cu);
-  const long long r = x - (long long)u * y.Cu;
-  int lo = 0, hi = y.ntiles;   // smallest i in [0, ntiles] with start(i) >= r (start is increasing)
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (tile_start_in(p, y, mid) >= r) hi = mid;
-    else lo = mid + 1;
+// (the launch-start arithmetic below avoids 64-bit integer division, a long software sequence:
+// every quotient is exact, from 32-bit divisions where the operands fit)
+__device__ __forceinline__ unsigned long long udiv_fit(unsigned long long a, unsigned b) {
+  return a <= 0xFFFFFFFFull ? (unsigned long long)((unsigned)a / b) : a / b;
+}
+// End of the cost ranges before warp w (0 <= w <= NW): ceil(w C / NW) with C = units Cu, written
+// as k Cu + c with k = floor(w units / NW) and 0 <= c = ceil(Cu (w units mod NW) / NW) <= Cu.
+struct RangeEnd {
+  long long x, c;
+  int k;
+};
+__device__ __forceinline__ RangeEnd range_end(const Lay& y, int units, int w) {
+  const unsigned NW = (unsigned)y.NW;
+  const unsigned long long a = (unsigned long long)w * (unsigned)units;
+  const unsigned long long k = udiv_fit(a, NW);
+  const unsigned long long rem = a - k * NW;
+  RangeEnd e;
+  e.c = (long long)udiv_fit((unsigned long long)y.Cu * rem + (NW - 1), NW);
+  e.k = (int)k;
+  e.x = (long long)k * y.Cu + e.c;
+  return e;
+}
+
+// First tile whose start position is >= u Cu + r (0 <= r <= Cu); warp-collective.  Tile i starts
+// less than |cb - cq| from i Cu / n (n = ntiles), so the answer lies next to floor(r n / Cu): the
+// lanes test the 32 tiles around that estimate at once (a binary search takes the rare case in
+// which they do not bracket it).
+__device__ __forceinline__ void first_tile(const AttnParams& p, const Lay& y, int u0, long long r, int lane, int& u,
+                                           int& i) {
+  u = u0;
+  const int n = y.ntiles;
+  // P(c): c >= n, or tile c starts at or after r (false below 0); the answer is the smallest c with P
+  auto P = [&](int c) -> bool { return c >= n || (c >= 0 && tile_start_in(p, y, c) >= r); };
+  const unsigned long long rn = (unsigned long long)r * (unsigned)n;
+  const long long est = y.Cu <= 0xFFFFFFFFll ? (long long)udiv_fit(rn, (unsigned)y.Cu) : (long long)(rn / y.Cu);
+  const int c0 = (int)est - 15;
+  const unsigned b = __ballot_sync(0xffffffffu, P(c0 + lane));
+  if (b != 0u && (!(b & 1u) || c0 == 0)) {
+    i = c0 + __ffs(b) - 1;
+  } else {
+    int lo = 0, hi = n;   // smallest c in [0, n] with P(c) (P is monotone)
+    while (lo < hi) {
+      const int mid = (lo + hi) >> 1;
+      if (P(mid)) hi = mid;
+      else lo = mid + 1;
+    }
+    i = lo;
   }
-  i = lo;
-  if (i >= y.ntiles) {
+  if (i >= n) {
     u += 1;
     i = 0;
   }
@@ -191,10 +232,15 @@ __device__ __forceinline__ bool describe(const AttnParams& p, const Lay& y, int 
     atomicOr(st.err, ERR_TABLE);
     return false;
   }
-  d.range = st.qrange[((long long)p.layer * st.units + u) * st.capq + ent.y];
+  d.range = 0;   // the slot's range record: loaded by the caller (slot_range)
   d.lo = (ent.x == 0) ? st.n_sink : 0;
   d.hi = W;
   return true;
+}
+
+// a 2-bit tile's slot range record (qrange_word)
+__device__ __forceinline__ int slot_range(const AttnParams& p, const TileDesc& d) {
+  return p.st.qrange[((long long)p.layer * p.st.units + d.u) * p.st.capq + d.slot];
 }
 
 __device__ __forceinline__ const uint8_t* tile_src(const AttnParams& p, const TileDesc& d, unsigned& bytes) {
@@ -215,14 +261,11 @@ __device__ __forceinline__ int newest_token_tile(const State& st, const Lay& y) 
   const int P = y.L - 1, W = st.geo.W;
   int loc = 0;   // bf16 tile number (bf16 list order)
   if (P >= st.n_sink) loc = (y.nbw - 1) * (W / 16) + (P - (P / W) * W) / 16;
-  // tile i is bf16 tile number i - q_before(i); find the smallest i with (i + 1) - q_before(i + 1) > loc
-  int lo = 0, hi = y.ntiles - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi) >> 1;
-    if (mid + 1 - q_before(y, mid + 1) > loc) hi = mid;
-    else lo = mid + 1;
-  }
-  return lo;
+  // Tiles [0, j) hold j - floor(j nq / n) = ceil(j nbt / n) bf16 tiles (n = ntiles), so the
+  // smallest j holding more than loc of them is floor(loc n / nbt) + 1, and the tile is j - 1.
+  const unsigned long long m = (unsigned long long)loc * (unsigned)y.ntiles;
+  if (m <= 0xFFFFFFFFull) return (int)((unsigned)m / (unsigned)y.nbt);
+  return (int)(m / (unsigned long long)y.nbt);
 }
 
 // The decode step's own append, done at the start of the launch by the one warp that owns the
@@ -489,17 +532,30 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   griddep_launch_dependents();
   __syncthreads();
   const Lay& y = s_lay;
-  const long long x_lo = (wg * y.C + y.NW - 1) / y.NW;
-  const long long x_hi = ((wg + 1) * y.C + y.NW - 1) / y.NW;
+  // this warp's cost range [x_lo, x_hi); units u_first .. u_last; the range starts r_lo into
+  // unit u_first
+  // (lanes 0 and 1 compute the two ends at once)
+  const RangeEnd e = range_end(y, p.st.units, wg + (lane & 1));
+  RangeEnd e_lo, e_hi;
+  e_lo.x = __shfl_sync(0xffffffffu, e.x, 0);
+  e_lo.c = __shfl_sync(0xffffffffu, e.c, 0);
+  e_lo.k = __shfl_sync(0xffffffffu, e.k, 0);
+  e_hi.x = __shfl_sync(0xffffffffu, e.x, 1);
+  e_hi.c = __shfl_sync(0xffffffffu, e.c, 1);
+  e_hi.k = __shfl_sync(0xffffffffu, e.k, 1);
+  const long long x_lo = e_lo.x, x_hi = e_hi.x;
+  const int u_first = e_lo.k + (e_lo.c >= y.Cu ? 1 : 0);
+  const long long r_lo = e_lo.c >= y.Cu ? e_lo.c - y.Cu : e_lo.c;
   // the warps whose ranges meet unit u are u NW / units .. ; partial slot = warp - first warp
-  auto slot_of = [&](int u) -> long long { return (long long)u * p.pslots + (wg - (int)((long long)u * y.NW / p.st.units)); };
+  auto slot_of = [&](int u) -> long long {
+    return (long long)u * p.pslots + (wg - (int)udiv_fit((unsigned long long)u * (unsigned)y.NW, (unsigned)p.st.units));
+  };
   if (x_lo >= x_hi) {   // empty range: leave an empty partial in the unit it falls into
-    const int u = (int)(x_lo / y.Cu);
+    const int u = u_first;
     if (u < p.st.units && lane < G) p.part_ml[slot_of(u) * G + lane] = make_float2(-INFINITY, 0.f);
     return;
   }
-  const int u_first = (int)(x_lo / y.Cu);
-  const int u_last = (int)((x_hi - 1) / y.Cu);
+  const int u_last = e_hi.k - (e_hi.c == 0 ? 1 : 0);
   // This decode step's appended token sits in tile inew of every unit; the warp that owns that
   // tile writes it first.  When the token opens its window, only that warp may use the window's
   // list entry (it writes it): the window's other sub-tiles are empty (rows past the token) and
@@ -524,10 +580,11 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   //      compacted out), then issues them one by one from shared memory
   BatchDesc* batch = batches[warp];
   int cu, ci;                        // cursor: first tile not yet described
-  first_tile(p, y, x_lo, cu, ci);
+  first_tile(p, y, u_first, r_lo, lane, cu, ci);
   bool range_done = !(cu < p.st.units && tile_start(p, y, cu, ci) < x_hi);
   int bcount = 0, bnext = 0;
-  auto describe_batch = [&]() {
+  // pro: copies the batch issues itself (the prologue's first batch: NST, later batches: 0)
+  auto describe_batch = [&](int pro) {
     while (!range_done) {
       int u = cu, i = ci + lane;
       while (i >= y.ntiles) { i -= y.ntiles; ++u; }
@@ -536,9 +593,21 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       bool ok = false;
       if (inr) ok = describe(p, y, u, i, list_entry(p, y, u, i, SUBT), d, inew, opens);
       const unsigned vb = __ballot_sync(0xffffffffu, ok);
+      const int pos = __popc(vb & ((1u << lane) - 1));
+      unsigned bytes = 0;
+      const uint8_t* src = ok ? tile_src(p, d, bytes) : nullptr;
+      // prologue: the lanes holding the first tiles issue their copies before the 2-bit tiles'
+      // range records (a second dependent load) arrive
+      if (ok && pos < pro) {
+        const unsigned bar = smem_u32(&bars[warp][pos]);
+        mbar_expect_tx(bar, bytes);
+        bulk_g2s_hint(smem_u32(stage_base + (size_t)pos * S::STAGE), src, bytes, bar, l2_evict_first_policy());
+      }
+      if (ok && d.kind) d.range = slot_range(p, d);
       if (ok) {
         BatchDesc bd;
-        bd.src = tile_src(p, d, bd.bytes);
+        bd.src = src;
+        bd.bytes = bytes;
         bd.sd.u = u;
         bd.sd.lse_off = (u * y.ntiles + d.i) * G;
         bd.sd.meta = d.lo | (d.hi << 8) | (d.kind << 16);
@@ -550,7 +619,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
                                (d.kind && qrange_values_wide(d.range) ? (1 << 30) : 0)
                          : (d.kind ? d.range : 0);
         bd.pad = 0;
-        batch[__popc(vb & ((1u << lane) - 1))] = bd;
+        batch[pos] = bd;
       }
       range_done = __any_sync(0xffffffffu, !inr);
       ci += BATCH;
@@ -558,13 +627,20 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       bcount = __popc(vb);
       bnext = 0;
       __syncwarp();
-      if (bcount > 0) return;
+      if (bcount > 0) {
+        if (pro > 0) {   // stage descriptors of the copies issued above
+          bnext = bcount < pro ? bcount : pro;
+          if (lane < bnext) descs[warp][lane] = batch[lane].sd;
+          __syncwarp();
+        }
+        return;
+      }
     }
   };
   auto issue_next = [&](int stage) -> bool {
     if (bnext == bcount) {
       if (range_done) return false;
-      describe_batch();
+      describe_batch(0);
       if (bcount == 0) return false;
     }
     if (lane == 0) {
@@ -572,13 +648,15 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
       descs[warp][stage] = bd.sd;
       const unsigned bar = smem_u32(&bars[warp][stage]);
       mbar_expect_tx(bar, bd.bytes);
-      bulk_g2s(smem_u32(stage_base + (size_t)stage * S::STAGE), bd.src, bd.bytes, bar);
+      // the tiles are read once per step: evict-first in L2
+      bulk_g2s_hint(smem_u32(stage_base + (size_t)stage * S::STAGE), bd.src, bd.bytes, bar, l2_evict_first_policy());
     }
     ++bnext;
     return true;
   };
-  int issued = 0;
-  for (int s = 0; s < NST; ++s) {
+  describe_batch(NST);   // issues the copies of the range's first tiles
+  int issued = bnext;
+  for (int s = issued; s < NST; ++s) {
     if (!issue_next(s)) break;
     ++issued;
   }

@@ -500,7 +500,9 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
       descs[warp][stage] = d;
       const unsigned bar = smem_u32(&bars[warp][stage]);
       mbar_expect_tx(bar, bytes);
-      bulk_g2s(smem_u32(stage_base + (size_t)stage * STAGE), tk_tile_src(S, p.layer, buf, cu, kind, t0), bytes, bar);
+      // the tiles are read once per step: evict-first in L2
+      bulk_g2s_hint(smem_u32(stage_base + (size_t)stage * STAGE), tk_tile_src(S, p.layer, buf, cu, kind, t0), bytes, bar,
+                    l2_evict_first_policy());
     }
     advance();
     return true;

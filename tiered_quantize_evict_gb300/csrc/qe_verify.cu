@@ -384,8 +384,8 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
         const unsigned bar = smem_u32(&bar_stage[sidx]);
         s_stage_cnt[sidx] += 1;
         mbar_expect_tx(bar, S::QSLOT);
-        bulk_g2s(sbase + S::OFF_STG + sidx * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT,
-                 S::QSLOT, bar);
+        bulk_g2s_hint(sbase + S::OFF_STG + sidx * S::STAGE, st.qslab + (gu * st.capq + e.y) * (long long)S::QSLOT,
+                      S::QSLOT, bar, l2_evict_first_policy());
       };
       int ei;
       for (int i = 0; i < VF_STAGES && i < nqc; ++i) issue_copy(i, chunk_entry(nbc + i, ei));
@@ -452,13 +452,14 @@ __global__ void __launch_bounds__(VF_THREADS, VfShape<D, W>::CTAS_PER_SM) qe_ver
     // 2t + 8; keys have tokens as rows, values channels), this warp's share, loaded ahead: the
     // keys of chunk c + 1 while chunk c's values are built, its values after those
     uint4 xk[FK], xv[FK];
+    const unsigned long long ef = l2_evict_first_policy();   // the slots are read once per call
     auto load_bf16 = [&](int2 e, bool values, uint4 (&x)[FK]) {
       if (e.y < 0 || e.y >= st.capb) return;
       const uint8_t* slot = st.bslab + (gu * st.capb + e.y) * (long long)S::BSLOT + (values ? 32 * D : 0);
 #pragma unroll
       for (int k = 0; k < FK; ++k) {
         const int ff = bw + 4 * k;
-        if (ff < NFK) x[k] = __ldg(reinterpret_cast<const uint4*>(slot + (ff / KS) * (64 * D) + (ff % KS) * 512) + lane);
+        if (ff < NFK) x[k] = ldg_hint(reinterpret_cast<const uint4*>(slot + (ff / KS) * (64 * D) + (ff % KS) * 512) + lane, ef);
       }
     };
     if (nbc > 0) {
