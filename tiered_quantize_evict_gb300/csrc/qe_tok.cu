@@ -69,15 +69,25 @@ __device__ __forceinline__ long long tk_X(const long long* cum, int u, long long
   return cum[u] + (long long)u * tail_cost;
 }
 
-// unit holding cost position x (largest u with X(u) <= x)
-__device__ __forceinline__ int tk_unit_of(const long long* cum, int units, long long tail_cost, long long x) {
-  int lo = 0, hi = units - 1;
-  while (lo < hi) {
-    const int mid = (lo + hi + 1) >> 1;
-    if (tk_X(cum, mid, tail_cost) <= x) lo = mid;
-    else hi = mid - 1;
+// The units holding cost positions xa and xb, found together by the warp: each round the lanes
+// test 32 units spread over each remaining interval (one load each, all in flight at once)
+// instead of a binary search's chain of dependent loads.  X(lo) <= x holds throughout (X(0) = 0).
+__device__ __forceinline__ int2 tk_units_of(const long long* cum, int units, long long tail_cost, long long xa,
+                                            long long xb, int lane) {
+  int lo0 = 0, hi0 = units - 1, lo1 = 0, hi1 = units - 1;
+  while (hi0 > lo0 || hi1 > lo1) {
+    const int s0 = hi0 - lo0 + 1, s1 = hi1 - lo1 + 1;
+    const int c0 = lo0 + (int)(((long long)lane * s0) >> 5), c1 = lo1 + (int)(((long long)lane * s1) >> 5);
+    const bool p0 = tk_X(cum, c0, tail_cost) <= xa, p1 = tk_X(cum, c1, tail_cost) <= xb;
+    const unsigned b0 = __ballot_sync(0xffffffffu, p0) | 1u, b1 = __ballot_sync(0xffffffffu, p1) | 1u;
+    const int m0 = 31 - __clz(b0), m1 = 31 - __clz(b1);   // last lane whose unit starts at or before x
+    const int n_lo0 = lo0 + (int)(((long long)m0 * s0) >> 5), n_lo1 = lo1 + (int)(((long long)m1 * s1) >> 5);
+    hi0 = m0 == 31 ? hi0 : lo0 + (int)(((long long)(m0 + 1) * s0) >> 5) - 1;
+    hi1 = m1 == 31 ? hi1 : lo1 + (int)(((long long)(m1 + 1) * s1) >> 5) - 1;
+    lo0 = n_lo0;
+    lo1 = n_lo1;
   }
-  return lo;
+  return make_int2(lo0, lo1);
 }
 
 // a[i] for a runtime i, by unrolled selects: the small per-unit arrays stay in registers
@@ -395,17 +405,18 @@ __global__ void __launch_bounds__(TK_WARPS * 32, 1) tk_attn_kernel(const TkAttnA
   const long long* cum = S.cum + (long long)p.layer * (S.units + 1);
   const long long tail_cost = (long long)S.cost[4] * ((n_tail + 15) >> 4);
   const long long C = tk_X(cum, S.units, tail_cost);
-  const long long x_lo = ((long long)wg * C + NW - 1) / NW;
-  const long long x_hi = (((long long)wg + 1) * C + NW - 1) / NW;
+  // this warp's cost range [x_lo, x_hi) (lanes 0 and 1 compute the two ends at once)
+  const long long xe = ((long long)(wg + (lane & 1)) * C + NW - 1) / NW;
+  const long long x_lo = __shfl_sync(0xffffffffu, xe, 0), x_hi = __shfl_sync(0xffffffffu, xe, 1);
   if (x_lo >= x_hi) {   // empty range: an empty partial in the unit it falls into
     if (x_lo < C) {
-      const int u = tk_unit_of(cum, S.units, tail_cost, x_lo);
+      const int u = tk_units_of(cum, S.units, tail_cost, x_lo, x_lo, lane).x;
       if (lane < G) p.part_ml[((long long)wg + u) * G + lane] = make_float2(-INFINITY, 0.f);
     }
     return;
   }
-  const int u_first = tk_unit_of(cum, S.units, tail_cost, x_lo);
-  const int u_last = tk_unit_of(cum, S.units, tail_cost, x_hi - 1);
+  const int2 uf = tk_units_of(cum, S.units, tail_cost, x_lo, x_hi - 1, lane);
+  const int u_first = uf.x, u_last = uf.y;
 
   // this step's appended token (the last tail slot of every unit), written by the warp whose
   // range holds its tail tile, before that warp issues any copy
