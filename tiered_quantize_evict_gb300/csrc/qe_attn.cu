@@ -41,6 +41,7 @@
 #include <cuda_runtime.h>
 
 #include "qe_kernels.cuh"
+#include "qe_partition.cuh"
 
 namespace qe {
 
@@ -95,46 +96,18 @@ __device__ __forceinline__ Lay make_lay(const State& st, int layer, int pend, in
   return y;
 }
 
-// Tile order inside a unit: the nbt bf16 sub-tiles and the nq 2-bit windows are interleaved
-// evenly (tile i is a 2-bit window iff floor((i+1) nq / ntiles) > floor(i nq / ntiles)), so every
-// warp's range mixes memory-bound bf16 tiles with compute-bound 2-bit tiles and the SM's warps
-// overlap the two instead of splitting into bf16 warps and 2-bit warps.
+// Tile order inside a unit: the bf16 sub-tiles and the 2-bit windows are interleaved evenly
+// (qe_partition.cuh), so every warp's range mixes memory-bound bf16 tiles with compute-bound
+// 2-bit tiles and the SM's warps overlap the two instead of splitting into bf16 warps and
+// 2-bit warps.
 __device__ __forceinline__ int q_before(const Lay& y, int i) {   // 2-bit tiles among [0, i)
-  const unsigned long long n = (unsigned long long)i * (unsigned)y.nq;
-  // 32-bit division where the product fits (a 64-bit one is a long software sequence)
-  if (n <= 0xFFFFFFFFull) return (int)((unsigned)n / (unsigned)y.ntiles);
-  return (int)(n / (unsigned long long)y.ntiles);
+  return tiles_q_before(i, y.nq, y.ntiles);
 }
 __device__ __forceinline__ long long tile_start_in(const AttnParams& p, const Lay& y, int i) {
-  const int qb = q_before(y, i);
-  return (long long)(i - qb) * p.cb + (long long)qb * p.cq;
+  return tile_cost_start(i, y.nq, y.ntiles, p.cb, p.cq);
 }
 __device__ __forceinline__ long long tile_start(const AttnParams& p, const Lay& y, int u, int i) {
   return (long long)u * y.Cu + tile_start_in(p, y, i);
-}
-
-// first tile whose start position is >= x
-// (the launch-start arithmetic below avoids 64-bit integer division, a long software sequence:
-// every quotient is exact, from 32-bit divisions where the operands fit)
-__device__ __forceinline__ unsigned long long udiv_fit(unsigned long long a, unsigned b) {
-  return a <= 0xFFFFFFFFull ? (unsigned long long)((unsigned)a / b) : a / b;
-}
-// End of the cost ranges before warp w (0 <= w <= NW): ceil(w C / NW) with C = units Cu, written
-// as k Cu + c with k = floor(w units / NW) and 0 <= c = ceil(Cu (w units mod NW) / NW) <= Cu.
-struct RangeEnd {
-  long long x, c;
-  int k;
-};
-__device__ __forceinline__ RangeEnd range_end(const Lay& y, int units, int w) {
-  const unsigned NW = (unsigned)y.NW;
-  const unsigned long long a = (unsigned long long)w * (unsigned)units;
-  const unsigned long long k = udiv_fit(a, NW);
-  const unsigned long long rem = a - k * NW;
-  RangeEnd e;
-  e.c = (long long)udiv_fit((unsigned long long)y.Cu * rem + (NW - 1), NW);
-  e.k = (int)k;
-  e.x = (long long)k * y.Cu + e.c;
-  return e;
 }
 
 // First tile whose start position is >= u Cu + r (0 <= r <= Cu); warp-collective.  Tile i starts
@@ -147,9 +120,7 @@ __device__ __forceinline__ void first_tile(const AttnParams& p, const Lay& y, in
   const int n = y.ntiles;
   // P(c): c >= n, or tile c starts at or after r (false below 0); the answer is the smallest c with P
   auto P = [&](int c) -> bool { return c >= n || (c >= 0 && tile_start_in(p, y, c) >= r); };
-  const unsigned long long rn = (unsigned long long)r * (unsigned)n;
-  const long long est = y.Cu <= 0xFFFFFFFFll ? (long long)udiv_fit(rn, (unsigned)y.Cu) : (long long)(rn / y.Cu);
-  const int c0 = (int)est - 15;
+  const int c0 = (int)first_tile_estimate(r, n, y.Cu) - 15;
   const unsigned b = __ballot_sync(0xffffffffu, P(c0 + lane));
   if (b != 0u && (!(b & 1u) || c0 == 0)) {
     i = c0 + __ffs(b) - 1;
@@ -261,11 +232,7 @@ __device__ __forceinline__ int newest_token_tile(const State& st, const Lay& y) 
   const int P = y.L - 1, W = st.geo.W;
   int loc = 0;   // bf16 tile number (bf16 list order)
   if (P >= st.n_sink) loc = (y.nbw - 1) * (W / 16) + (P - (P / W) * W) / 16;
-  // Tiles [0, j) hold j - floor(j nq / n) = ceil(j nbt / n) bf16 tiles (n = ntiles), so the
-  // smallest j holding more than loc of them is floor(loc n / nbt) + 1, and the tile is j - 1.
-  const unsigned long long m = (unsigned long long)loc * (unsigned)y.ntiles;
-  if (m <= 0xFFFFFFFFull) return (int)((unsigned)m / (unsigned)y.nbt);
-  return (int)(m / (unsigned long long)y.nbt);
+  return bf16_tile_index(loc, y.ntiles, y.nbt);
 }
 
 // The decode step's own append, done at the start of the launch by the one warp that owns the
@@ -535,7 +502,7 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   // this warp's cost range [x_lo, x_hi); units u_first .. u_last; the range starts r_lo into
   // unit u_first
   // (lanes 0 and 1 compute the two ends at once)
-  const RangeEnd e = range_end(y, p.st.units, wg + (lane & 1));
+  const RangeEnd e = range_end(y.Cu, y.NW, p.st.units, wg + (lane & 1));
   RangeEnd e_lo, e_hi;
   e_lo.x = __shfl_sync(0xffffffffu, e.x, 0);
   e_lo.c = __shfl_sync(0xffffffffu, e.c, 0);
