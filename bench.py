@@ -128,17 +128,31 @@ class ClockSampler:
 
 
 # ---------------------------------------------------------------------------- ncu traffic record
+# the sources each attention kernel is built from: its translation unit and the local headers it
+# includes (the ncu record names the same list and their joint sha256)
+KERNEL_SOURCES = {
+    "qe_decode_attn": ["qe_attn.cu", "qe_kernels.cuh", "qe_partition.cuh", "qe_common.cuh"],
+    "tk_attn": ["qe_tok.cu", "qe_exact_stats.cuh", "qe_tok.cuh", "qe_tok_kernels.h", "qe_common.cuh"],
+}
+
+
+def kernel_sources_sha256(kernel: str) -> str:
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        h.update(open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", name), "rb").read())
+    return h.hexdigest()
+
+
 def _traffic(workload: str, kernel: str = "qe_decode_attn"):
     """DRAM bytes per launch of the attention kernel from the committed ncu summary, if the
-    kernel source is unchanged since it was captured (else None)."""
-    src_file = {"qe_decode_attn": "qe_attn.cu", "tk_attn": "qe_tok.cu"}[kernel]
+    kernel's sources are unchanged since it was captured (else None)."""
     path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.json")
     try:
         with open(path) as f:
             rec = json.load(f)
-        src = open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", src_file), "rb").read()
-        sha = rec.get("source_sha256", rec.get("qe_attn_sha256"))
-        if sha != hashlib.sha256(src).hexdigest():
+        if rec.get("source_files") != KERNEL_SOURCES[kernel]:
+            return None
+        if rec.get("source_sha256") != kernel_sources_sha256(kernel):
             return None
         return rec.get("dram_bytes_per_launch_full")
     except Exception:
