@@ -330,6 +330,11 @@ def run_ours(args):
     torch.cuda.synchronize(dev)
     cache.set_timing(False)
     attn_ms, attn_launches, attn_bytes = cache.timing()
+    # the launch and event overhead inside each of those event times: an empty launch of the
+    # same shape between the same events (window path; the five-tier launch has its own shape)
+    overhead_us = None
+    if getattr(wl, "tiering", "windows") != "tokens" and not verify:
+        overhead_us = cache.launch_overhead(200)
     rs1 = _route_counts(cache)
     route_ms = [a.elapsed_time(b) for _, (a, b) in route_events]
     route_steps = [ts * NQ for ts, _ in route_events]
@@ -428,6 +433,16 @@ def run_ours(args):
             "avg_launch_us": round(attn_ms * 1e3 / max(attn_launches, 1), 2),
             "attn_share_of_step": round((attn_ms / KR) / (ms_total / K), 4) if ms_total > 0 else None,
             "measured_on": "the next %d decode steps launched directly, CUDA events around each launch" % KR,
+            # the event times hold launch and event overhead; measured, not subtracted above
+            "event_overhead_us": round(overhead_us, 2) if overhead_us is not None else None,
+            "frac_without_event_overhead": (
+                round(attn_bytes / max(attn_launches, 1) / ((attn_ms * 1e3 / max(attn_launches, 1) - overhead_us) * 1e-6)
+                      / 1e9 / peak, 4)
+                if overhead_us is not None and attn_ms > 0 and attn_ms * 1e3 / max(attn_launches, 1) > overhead_us
+                else None),
+            "event_overhead_measured_on": "200 empty launches of the attention launch's shape (grid, block, dynamic "
+                                          "shared memory, programmatic serialization) between two events each, "
+                                          "same stream, same run (qe_launch_overhead)",
         },
         "routing": {
             "events": len(route_ms),

@@ -341,6 +341,15 @@ qe_status qe_get_route_diag(qe_handle h, int layer, qe_route_diag* out, size_t n
 qe_status qe_set_timing(qe_handle h, int enable);
 qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, double* attn_bytes);
 
+/* Measurement aid: the mean CUDA-event time, in microseconds, of n launches (1 <= n <= 10000)
+ * that have the window path's attention launch shape (its grid, block and dynamic shared memory,
+ * programmatic serialization) and do nothing, enqueued back to back, each between two events
+ * on the handle's stream.  That is the part of a timed attention launch that is launch and
+ * event overhead rather than kernel work.  Synchronous; enqueues nothing that changes the
+ * handle's state.  QE_ERR_STATE on a five-tier handle; QE_ERR_INVALID_ARG for n out of range
+ * or a null us. */
+qe_status qe_launch_overhead(qe_handle h, int n, double* us);
+
 /* ---------------------------------------------------------------- five-tier introspection
  * (QE_TIERING_TOKENS handles; all synchronous; QE_ERR_STATE on a window-tiered handle) */
 

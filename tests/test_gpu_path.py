@@ -70,3 +70,24 @@ def test_error_codes():
     assert e.value.status == qe.QE_ERR_STATE
     c.qe_synchronize()
     c.close()
+
+
+def test_launch_overhead_measure():
+    """qe_launch_overhead times empty launches of the attention launch's shape: a positive
+    number of microseconds well below a real attention launch, with the handle's state
+    untouched; it refuses a bad count."""
+    import tiered_quantize_evict_gb300 as qe
+    torch, dev = torch_dev()
+    wl = gen.WORKLOADS["tiny_qevict"]
+    c = qe.QECache(qe.config_from_workload(wl, max_context=64))
+    k = torch.zeros(1, 1, 20, 64, device=dev, dtype=torch.int16)
+    c.qe_append(0, k, k, 20)
+    before = c.layer_info(0).length
+    us = c.launch_overhead(20)
+    assert 0.0 < us < 50.0
+    assert c.layer_info(0).length == before
+    with pytest.raises(qe.QEError) as e:
+        c.launch_overhead(0)
+    assert e.value.status == qe.QE_ERR_INVALID_ARG
+    c.qe_synchronize()
+    c.close()

@@ -30,6 +30,7 @@ EXPORTED = [
     "qe_get_timing", "qe_kernel_launches", "qe_decode_step_noalloc", "qe_get_route_diag",
     "qe_get_token_tiers", "qe_get_token_scores", "qe_get_token_counts", "qe_get_token",
     "qe_verify", "qe_verify_commit", "qe_debug_inject", "qe_snapshot_size", "qe_snapshot", "qe_restore",
+    "qe_launch_overhead",
 ]
 QE_DEBUG_FAIL_DEVICE_ALLOC, QE_DEBUG_FAIL_HOST_STORE, QE_DEBUG_EXPIRE_WAIT, QE_DEBUG_VERIFY_PATH = 1, 2, 3, 4
 QE_VERIFY_MAX = 16
@@ -108,6 +109,7 @@ def load_library() -> ctypes.CDLL:
         "qe_get_route_stats": ([P, I, ctypes.POINTER(QERouteStats)], I),
         "qe_set_timing": ([P, I], I),
         "qe_get_timing": ([P, ctypes.POINTER(D), ctypes.POINTER(ctypes.c_longlong), ctypes.POINTER(D)], I),
+        "qe_launch_overhead": ([P, I, ctypes.POINTER(D)], I),
         "qe_kernel_launches": ([P], ctypes.c_longlong),
         "qe_decode_step_noalloc": ([P, I, P, P], I),
         "qe_get_route_diag": ([P, I, ctypes.POINTER(QERouteDiag), S], I),
@@ -320,6 +322,12 @@ class QECache:
 
     def kernel_launches(self) -> int:
         return int(self._lib.qe_kernel_launches(self.h))
+
+    def launch_overhead(self, n: int = 100) -> float:
+        """qe_launch_overhead: mean event time (us) of an empty launch shaped like the attention's."""
+        us = ctypes.c_double()
+        self._check(self._lib.qe_launch_overhead(self.h, int(n), ctypes.byref(us)))
+        return us.value
 
 
 def config_from_workload(wl, out_fp32: bool = True, max_context: Optional[int] = None,

@@ -37,6 +37,7 @@
 //  * Per-window mass leaves the kernel as a log-sum-exp per (tile, head); the combine kernel
 //    turns it into a probability mass once the unit's global softmax normaliser is known.
 #include <cstdint>
+#include <vector>
 #include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
@@ -1297,6 +1298,58 @@ cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream) {
 }
 
 int attn_warps_per_cta() { return ATTN_WARPS; }
+
+// A launch with the attention launch's shape (grid, block, dynamic shared memory, programmatic
+// serialization) that does nothing: timing it between two events gives the part of an event
+// time that is launch and event overhead rather than the kernel's work.
+__global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_empty_attn_shaped_kernel(int* never) {
+  extern __shared__ unsigned char smem_unused[];
+  if (never != nullptr && threadIdx.x == 0 && blockIdx.x == 0x7fffffff) never[0] = smem_unused[0];
+}
+
+cudaError_t time_empty_attn_launch(int D, int W, int grid, int n, cudaStream_t stream, double* us) {
+  size_t smem = 0;
+  if (D == 128 && W == 32) smem = attn_smem_bytes<128, 32>();
+  else if (D == 128 && W == 16) smem = attn_smem_bytes<128, 16>();
+  else if (D == 128 && W == 64) smem = attn_smem_bytes<128, 64>();
+  else if (D == 64 && W == 16) smem = attn_smem_bytes<64, 16>();
+  else if (D == 64 && W == 32) smem = attn_smem_bytes<64, 32>();
+  else if (D == 64 && W == 64) smem = attn_smem_bytes<64, 64>();
+  else return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(qe_empty_attn_shaped_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  // all launches enqueued back to back, each between its own two events, as the timed attention
+  // launches are; one synchronization at the end
+  std::vector<cudaEvent_t> ev(2 * (size_t)n, nullptr);
+  for (size_t i = 0; i < ev.size() && e == cudaSuccess; ++i) e = cudaEventCreate(&ev[i]);
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(ATTN_WARPS * 32);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    e = cudaEventRecord(ev[2 * i], stream);
+    if (e == cudaSuccess) e = cudaLaunchKernelEx(&cfg, qe_empty_attn_shaped_kernel, (int*)nullptr);
+    if (e == cudaSuccess) e = cudaEventRecord(ev[2 * i + 1], stream);
+  }
+  if (e == cudaSuccess) e = cudaStreamSynchronize(stream);
+  double total = 0;
+  for (int i = 0; i < n && e == cudaSuccess; ++i) {
+    float t = 0;
+    e = cudaEventElapsedTime(&t, ev[2 * i], ev[2 * i + 1]);
+    total += t;
+  }
+  for (cudaEvent_t x : ev)
+    if (x) cudaEventDestroy(x);
+  if (e == cudaSuccess && us) *us = n > 0 ? 1000.0 * total / n : 0.0;
+  return e;
+}
 
 // Persistent grid: one CTA per SM, but few enough warps that a unit meets at most pslots - 2
 // warp ranges.

@@ -1072,6 +1072,14 @@ qe_status qe_set_timing(qe_handle h, int enable) {
   return QE_OK;
 }
 
+qe_status qe_launch_overhead(qe_handle h, int n, double* us) {
+  if (!h || n < 1 || n > 10000 || !us) return h ? fail(h, QE_ERR_INVALID_ARG, "n %d or null output", n) : QE_ERR_INVALID_ARG;
+  if (h->cfg.tiering != QE_TIERING_WINDOWS) return fail(h, QE_ERR_STATE, "window-tiered handles only");
+  QE_CK(h, cudaStreamSynchronize(h->stream));
+  QE_CK(h, qe::time_empty_attn_launch(h->cfg.head_dim, h->cfg.window, h->attn_grid, n, h->stream, us));
+  return QE_OK;
+}
+
 qe_status qe_get_timing(qe_handle h, double* attn_ms, long long* launches, double* attn_bytes) {
   if (!h) return QE_ERR_INVALID_ARG;
   QE_CK(h, cudaStreamSynchronize(h->stream));

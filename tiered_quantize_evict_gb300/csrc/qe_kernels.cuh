@@ -145,6 +145,8 @@ cudaError_t prepare_attn_kernels(int D, int W);
 cudaError_t prepare_route_kernels(const State& st);
 cudaError_t launch_attn_combine(const CombineParams& p, cudaStream_t stream);
 int attn_warps_per_cta();
+// mean CUDA-event time (us) of n empty launches shaped like the attention launch (synchronous)
+cudaError_t time_empty_attn_launch(int D, int W, int grid, int n, cudaStream_t stream, double* us);
 cudaError_t launch_verify_commit(const State& st, int layer, int L0, int n_q, int n_accept, const float* delta,
                                  long long qstride, cudaStream_t s);
 // tok_major: k and v are [n][units][D] (token-major, as a verify's drafts) instead of [units][n][D]
