@@ -18,6 +18,7 @@ import hashlib
 import json
 import math
 import os
+import re
 import statistics
 import subprocess
 import sys
@@ -137,9 +138,14 @@ KERNEL_SOURCES = {
 
 
 def kernel_sources_sha256(kernel: str) -> str:
+    """sha256 of the kernel's sources with comments removed and whitespace runs collapsed: an
+    edit of a comment does not void the counters, an edit of the code does."""
     h = hashlib.sha256()
     for name in KERNEL_SOURCES[kernel]:
-        h.update(open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", name), "rb").read())
+        src = open(os.path.join(ROOT, "tiered_quantize_evict_gb300", "csrc", name)).read()
+        src = re.sub(r"/\*.*?\*/", " ", src, flags=re.S)
+        src = re.sub(r"//[^\n]*", " ", src)
+        h.update(" ".join(src.split()).encode())
     return h.hexdigest()
 
 

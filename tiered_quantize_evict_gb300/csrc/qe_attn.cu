@@ -13,7 +13,12 @@
 //    the layer is cut into one contiguous, cost-weighted range per warp (stream-K), so every
 //    warp streams its own range through a private ring of shared-memory stages filled by
 //    cp.async.bulk (one 1-D bulk copy per tile, completion on an mbarrier), and the whole GPU
-//    is busy until the last tile regardless of how units and tiles divide.
+//    is busy until the last tile regardless of how units and tiles divide.  The copies carry an
+//    evict-first L2 policy: the tiles are read once per step and the cache is many times the
+//    L2, so they must not push out what every step reuses (lists, partials, queries, code).
+//  * Launch start: the range arithmetic is exact 32-bit integer work (qe_partition.cuh), a
+//    warp's first tile is found by one 32-lane test around its estimate, and the range's first
+//    copies leave before the 2-bit slots' range records are loaded.
 //  * The G query heads of a KV head share every K/V element: the Q K^T and P V products are
 //    small dense contractions ([16 tokens x d] x [d x 8]) run on the tensor cores with
 //    mma.m16n8k16 (fp32 accumulate).  Column 2h carries head h's operand truncated to the
