@@ -3,7 +3,8 @@ cost-weighted ranges (``qe_partition.cuh``), built for the host and checked agai
 definitions: the range ends ceil(w C / NW), the interleaved tile order floor(i nq / n), the
 tile's cost position, the interleaved index of a bf16 tile, and the first-tile estimate, which
 the kernel refines by testing the 32 tiles around it.  The cases include operands past 2^32,
-where the helpers take their 64-bit branches."""
+where the helpers take their 64-bit branches.  Also the five-tier attention's 32-way search for
+the unit that holds a cost position (``qe_tok.cuh``), with the lanes' tests run in a loop."""
 import os
 import random
 import shutil
@@ -143,3 +144,49 @@ def test_first_tile_lies_in_the_window_the_kernel_tests(run):
                 lo = mid + 1
         if max(cb, cq) <= 8 * min(cb, cq):
             assert est - 15 <= lo <= est + 16, (r, n, cu, cb, cq, est, lo)
+
+
+@pytest.fixture(scope="module")
+def search32():
+    nvcc = _nvcc()
+    if nvcc is None:
+        pytest.skip("nvcc not found")
+    d = tempfile.mkdtemp(prefix="qe_s32_")
+    exe = os.path.join(d, "search32_check")
+    subprocess.run([nvcc, "-x", "cu", "-O2", "-std=c++17", "-I", CSRC,
+                    os.path.join(ROOT, "tests", "search32_check.cu"), "-o", exe], check=True)
+
+    def go(cases):
+        fin, fout = os.path.join(d, "in.txt"), os.path.join(d, "out.txt")
+        with open(fin, "w") as f:
+            for X, x in cases:
+                f.write(f"{len(X)} {x} " + " ".join(map(str, X)) + "\n")
+        subprocess.run([exe, fin, fout], check=True)
+        return [tuple(map(int, ln.split())) for ln in open(fout).read().splitlines()]
+
+    yield go
+    shutil.rmtree(d, ignore_errors=True)
+
+
+def test_five_tier_unit_search_finds_the_unit(search32):
+    """The five-tier attention finds the unit holding a cost position (the largest u with
+    X(u) <= x over the per-unit cost prefix) by rounds of 32 tests; it must equal the
+    definition for any nondecreasing prefix, empty units (repeated X) included, in at most
+    ceil(log32 n) + 1 rounds."""
+    rng = random.Random(11)
+    cases = []
+    for _ in range(600):
+        n = rng.choice([1, 2, 5, 31, 32, 33, 64, 100, 1000, 5000])
+        X = [0]
+        for _ in range(n - 1):
+            X.append(X[-1] + rng.choice([0, rng.randint(1, 100), rng.randint(1, 10 ** 9)]))
+        x = rng.choice([0, X[-1], rng.randint(0, X[-1] + 5)])
+        cases.append((X, x))
+    got = search32(cases)
+    for (X, x), (u, rounds) in zip(cases, got):
+        want = max(i for i in range(len(X)) if X[i] <= x)
+        assert u == want, (len(X), x, u, want)
+        bound = 1
+        while 32 ** bound < len(X):
+            bound += 1
+        assert rounds <= bound + 1

@@ -76,16 +76,11 @@ __device__ __forceinline__ int2 tk_units_of(const long long* cum, int units, lon
                                             long long xb, int lane) {
   int lo0 = 0, hi0 = units - 1, lo1 = 0, hi1 = units - 1;
   while (hi0 > lo0 || hi1 > lo1) {
-    const int s0 = hi0 - lo0 + 1, s1 = hi1 - lo1 + 1;
-    const int c0 = lo0 + (int)(((long long)lane * s0) >> 5), c1 = lo1 + (int)(((long long)lane * s1) >> 5);
-    const bool p0 = tk_X(cum, c0, tail_cost) <= xa, p1 = tk_X(cum, c1, tail_cost) <= xb;
+    const bool p0 = tk_X(cum, search32_unit(lo0, hi0, lane), tail_cost) <= xa;
+    const bool p1 = tk_X(cum, search32_unit(lo1, hi1, lane), tail_cost) <= xb;
     const unsigned b0 = __ballot_sync(0xffffffffu, p0) | 1u, b1 = __ballot_sync(0xffffffffu, p1) | 1u;
-    const int m0 = 31 - __clz(b0), m1 = 31 - __clz(b1);   // last lane whose unit starts at or before x
-    const int n_lo0 = lo0 + (int)(((long long)m0 * s0) >> 5), n_lo1 = lo1 + (int)(((long long)m1 * s1) >> 5);
-    hi0 = m0 == 31 ? hi0 : lo0 + (int)(((long long)(m0 + 1) * s0) >> 5) - 1;
-    hi1 = m1 == 31 ? hi1 : lo1 + (int)(((long long)(m1 + 1) * s1) >> 5) - 1;
-    lo0 = n_lo0;
-    lo1 = n_lo1;
+    search32_narrow(lo0, hi0, 31 - __clz(b0));   // the last lane whose unit starts at or before x
+    search32_narrow(lo1, hi1, 31 - __clz(b1));
   }
   return make_int2(lo0, lo1);
 }

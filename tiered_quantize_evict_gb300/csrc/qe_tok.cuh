@@ -118,4 +118,16 @@ QE_HD int tk_tile_bytes(const TokState& s, int z) {
   return z == TK_BF16 || z == TK_TAIL ? s.g.bf_tile() : s.g.q_tile(tk_bits(z));
 }
 
+// One round of the warp's 32-way search for the largest u in [lo, hi] with X(u) <= x (X
+// nondecreasing, X(lo) <= x): lane l tests unit search32_unit(lo, hi, l); with m the last lane
+// whose unit passed, the answer lies in [unit(m), unit(m + 1) - 1], or [unit(31), hi] for
+// m = 31 (search32_narrow).  Each round shrinks the interval about 32-fold.
+QE_HD int search32_unit(int lo, int hi, int lane) { return lo + (int)(((long long)lane * (hi - lo + 1)) >> 5); }
+QE_HD void search32_narrow(int& lo, int& hi, int m) {
+  const int s = hi - lo + 1;
+  const int n_lo = lo + (int)(((long long)m * s) >> 5);
+  hi = m == 31 ? hi : lo + (int)(((long long)(m + 1) * s) >> 5) - 1;
+  lo = n_lo;
+}
+
 }  // namespace qe
