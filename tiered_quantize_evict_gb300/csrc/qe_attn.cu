@@ -505,9 +505,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   griddep_launch_dependents();
   __syncthreads();
   const Lay& y = s_lay;
-  // this warp's cost range [x_lo, x_hi); units u_first .. u_last; the range starts r_lo into
-  // unit u_first
-  // (lanes 0 and 1 compute the two ends at once)
+  // this warp's cost range [x_lo, x_hi) (lanes 0 and 1 compute the two ends at once), its units
+  // u_first .. u_last, and r_lo, where the range starts inside unit u_first
   const RangeEnd e = range_end(y.Cu, y.NW, p.st.units, wg + (lane & 1));
   RangeEnd e_lo, e_hi;
   e_lo.x = __shfl_sync(0xffffffffu, e.x, 0);
@@ -550,7 +549,8 @@ __global__ void __launch_bounds__(ATTN_WARPS * 32, 1) qe_decode_attn_kernel(cons
   __syncwarp();
 
   // ---- producer: the warp describes BATCH tiles at a time (one per lane, empty tiles
-  //      compacted out), then issues them one by one from shared memory
+  //      compacted out), then issues them one by one from shared memory; the first batch's
+  //      lanes issue the range's first NST copies themselves
   BatchDesc* batch = batches[warp];
   int cu, ci;                        // cursor: first tile not yet described
   first_tile(p, y, u_first, r_lo, lane, cu, ci);
